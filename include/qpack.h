@@ -1,0 +1,163 @@
+/*
+ * qpack.h — C ABI of libqpack: group-quantized low-bit weights with dequantization fused into the
+ * decode-phase matrix-vector product (and the small-batch and prefill matrix products), for one NVIDIA
+ * GB300 (sm_103a).
+ *
+ * Sources. P1 = the 2/3/5/6-bit quantization article (lpnh.cn/news/2857666); P2 = the DBHOO-CIM INT4 CPU
+ * inference article (pwwt.cn/news/4452170). FORMATS.md in the source tree fixes every bit order the pages
+ * leave open.
+ *
+ * Conventions shared by every entry point:
+ *  - W is row-major [N, K]: N output features (rows), K input features. Groups and super-blocks run along K.
+ *  - All data pointers are DEVICE pointers owned by the caller; the library never allocates device memory
+ *    and never frees caller memory. Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *  - fp16 and bf16 data are passed as their 16-bit patterns (uint16_t).
+ *  - Argument errors are detected on the host before anything is launched and returned as a negative
+ *    qpack_status; a failed launch returns QPACK_ERR_CUDA. Data-dependent conditions are reported through a
+ *    device status word (qpack_quantize*) and never trap.
+ *  - N == 0 (or M == 0) is accepted and launches nothing.
+ */
+#ifndef QPACK_H_
+#define QPACK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qpack_stream_t; /* identical to cudaStream_t */
+
+/* Weight formats. Q4G32: INT4 symmetric, group 32, fp32 group scales (P2 §3.1–§3.2, §4.1).
+ * Q2S/Q3S/Q5S/Q6S: 256-weight super-blocks of 84/110/176/210 bytes (P1 §2.3 byte table). */
+typedef enum {
+    QPACK_Q4G32 = 0,
+    QPACK_Q2S = 1,
+    QPACK_Q3S = 2,
+    QPACK_Q5S = 3,
+    QPACK_Q6S = 4
+} qpack_format;
+
+typedef enum { QPACK_F32 = 0, QPACK_F16 = 1, QPACK_BF16 = 2 } qpack_dtype;
+
+typedef enum {
+    QPACK_OK = 0,
+    QPACK_ERR_ARG = -1,        /* null pointer where one is required, bad enum, negative size */
+    QPACK_ERR_SHAPE = -2,      /* K not a multiple of the format's group (32) or super-block (256), M out of range */
+    QPACK_ERR_ALIGN = -3,      /* a pointer or leading dimension breaks the stated alignment */
+    QPACK_ERR_RANGE = -4,      /* reserved: data-dependent range failure reported synchronously */
+    QPACK_ERR_CUDA = -5,       /* a CUDA runtime call or kernel launch failed */
+    QPACK_ERR_UNSUPPORTED = -6 /* format / path combination not provided */
+} qpack_status;
+
+/* Bit OR-ed into the device status word when a super-block's fp16 d or dmin overflows to infinity
+ * (P1 §2.3 warns about fp16 super-scale overflow). */
+#define QPACK_FLAG_RANGE 1
+
+/* Sizes of the packed representation (host-only, no GPU work).
+ *  row_stride    bytes between consecutive packed rows (super-block formats: rows padded to 16 B, P1 §3.3)
+ *  packed_bytes  N * row_stride
+ *  scale_stride  Q4G32 only: floats between consecutive rows of the separate fp32 scale array
+ *                (K/32 rounded up to a multiple of 4, P2 §4.1); 0 otherwise
+ *  scale_bytes   Q4G32 only: N * scale_stride * 4; 0 otherwise
+ *  block_bytes   bytes per 256-weight super-block (84/110/176/210, P1 §2.3); 0 for Q4G32
+ *  nsub          sub-blocks per super-block (16, or 8 for Q5S); for Q4G32 the groups per row (K/32)
+ *  weight_bytes  packed_bytes + scale_bytes: the bytes one product call streams from memory
+ * Returns QPACK_OK, QPACK_ERR_ARG (bad format, negative size, null out) or QPACK_ERR_SHAPE. */
+typedef struct {
+    int64_t row_stride;
+    int64_t packed_bytes;
+    int64_t scale_stride;
+    int64_t scale_bytes;
+    int64_t block_bytes;
+    int64_t nsub;
+    int64_t weight_bytes;
+} qpack_layout_t;
+int qpack_layout(int fmt, int64_t N, int64_t K, qpack_layout_t *out);
+
+/* Quantize W into unpacked parts (P2 §3.1 for Q4G32; two-level round-to-nearest of FORMATS.md §2a/§2b for
+ * the super-block formats, following P1 §2.1's fp16 super-scale -> sub-block scale -> weight structure).
+ *  W          [N, K] of dtype wdt (F32, F16 or BF16), 16-byte aligned
+ *  codes      [N, K] int8: the signed integer q (Q4G32 -8..7, Q3S -4..3, Q6S -32..31, Q2S 0..3, Q5S 0..31)
+ *  gscale     Q4G32: [N, K/32] fp32 group scales; NULL for other formats
+ *  sub_scale  super-block formats: [N, K/256 * nsub] uint8 sub-block scale integers L_j; NULL for Q4G32
+ *  sub_min    Q2S/Q5S: [N, K/256 * nsub] uint8 sub-block minimum integers M_j; NULL otherwise
+ *  d, dmin    super-block formats: [N, K/256] fp16 bits of d; dmin for Q2S/Q5S only (NULL otherwise)
+ *  status     device int32 (may be NULL): QPACK_FLAG_RANGE is OR-ed in; the caller clears it.
+ * The results are bit-identical to FORMATS.md's IEEE fp32 definition. */
+int qpack_quantize(int fmt, const void *W, int wdt, int64_t N, int64_t K, int8_t *codes, float *gscale,
+                   uint8_t *sub_scale, uint8_t *sub_min, uint16_t *d, uint16_t *dmin, int32_t *status,
+                   qpack_stream_t stream);
+
+/* Pack unpacked parts (layouts as produced by qpack_quantize) into the format's bytes: P2 §3.2 nibble
+ * packing (low nibble = even index) for Q4G32; P1 §2.2 cross-byte packing and §2.3 bit planes for the
+ * super-block formats, bit orders of FORMATS.md §2c.
+ *  packed        [N, row_stride] bytes, 16-byte aligned; padding bytes are written as zero
+ *  group_scales  Q4G32: [N, scale_stride] fp32, 16-byte aligned, padding written as 0.0f; NULL otherwise */
+int qpack_pack(int fmt, int64_t N, int64_t K, const int8_t *codes, const float *gscale, const uint8_t *sub_scale,
+               const uint8_t *sub_min, const uint16_t *d, const uint16_t *dmin, uint8_t *packed,
+               float *group_scales, qpack_stream_t stream);
+
+/* Fused quantize + pack: W straight to packed bytes (and Q4G32 group scales) in one pass over W.
+ * Arguments as qpack_quantize (W, wdt, status) and qpack_pack (packed, group_scales). */
+int qpack_quantize_pack(int fmt, const void *W, int wdt, int64_t N, int64_t K, uint8_t *packed,
+                        float *group_scales, int32_t *status, qpack_stream_t stream);
+
+/* Inverse of qpack_pack: packed bytes back to unpacked parts (same pointer conventions). */
+int qpack_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float *group_scales, int8_t *codes,
+                 float *gscale, uint8_t *sub_scale, uint8_t *sub_min, uint16_t *d, uint16_t *dmin,
+                 qpack_stream_t stream);
+
+/* Dequantize a packed matrix to fp32 out [N, K] (the page's self-check path, P1 §3.4): Q4G32 w' = s*q;
+ * symmetric super-blocks w' = (d*L_j)*q; asymmetric w' = (d*L_j)*q - (dmin*M_j), each step an fp32 rounding,
+ * no FMA. Bit-identical to FORMATS.md. out must be 16-byte aligned. */
+int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float *group_scales, float *out,
+                  qpack_stream_t stream);
+
+/* Fused dequant-GEMV (decode, batch 1; P1 §1.2 and §3.3, P2 §3.3 "fused dequantization"):
+ *   y[r] = sum_k w'[r,k] * x[k],  r < N
+ * packed weights are read exactly once and unpacked in registers; fp32 accumulation.
+ *  packed, group_scales  as produced by qpack_pack (group_scales NULL except Q4G32), 16-byte aligned
+ *  x                     [K] fp16, 16-byte aligned
+ *  y                     [N] fp32, 4-byte aligned
+ * Parity bound against an fp64 sum: |y[r] - y_ref[r]| <= 1e-4 * ||w'_r||_2 * ||x||_2. */
+int qgemv(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, const uint16_t *x,
+          float *y, qpack_stream_t stream);
+
+/* Small-batch decode GEMM (P2 §5.2 decode vs prefill; batch up to 16):
+ *   Y[m, r] = sum_k w'[r,k] * X[m,k],  m < M, r < N,  1 <= M <= 16
+ * each packed weight is read once and reused across the M activation rows; fp32 accumulation.
+ *  X  [M, ldx] fp16, 16-byte aligned, ldx >= K and ldx a multiple of 8
+ *  Y  [M, ldy] fp32, ldy >= N
+ * Same parity bound as qgemv, per element. */
+int qgemm_small(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, int M,
+                const uint16_t *X, int64_t ldx, float *Y, int64_t ldy, qpack_stream_t stream);
+
+/* Prefill dequant GEMM on the tensor cores (P1 §1.2: prefill is a dense [tokens, hidden] x [hidden, hidden]
+ * contraction):
+ *   Y[m, n] = sum_k bf16(X[m,k]) * bf16(w'[n,k]),  fp32 accumulation, Y rounded to bf16
+ * Weight tiles are dequantized to bf16 in shared memory and fed to tcgen05 MMA with TMEM accumulators.
+ *  formats  Q4G32 (K a multiple of 64) and the super-block formats (K a multiple of 256)
+ *  X        [M, ldx] bf16, 16-byte aligned, ldx >= K, ldx a multiple of 8
+ *  Y        [M, ldy] bf16, 16-byte aligned, ldy >= N, ldy a multiple of 8
+ * Parity bound: ||Y - Y_ref||_2 / ||Y_ref||_2 <= 2e-2 with Y_ref in fp64. */
+int qgemm_prefill(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, int64_t M,
+                  const uint16_t *X, int64_t ldx, uint16_t *Y, int64_t ldy, qpack_stream_t stream);
+
+/* Human-readable name of a qpack_status value. Never NULL. */
+const char *qpack_status_string(int status);
+
+/* Device-side fault record: bounded waits inside the kernels that give up OR a bit into a per-device word
+ * instead of hanging. Copies the current device's word to *flags (synchronous) and clears it.
+ * Returns QPACK_OK or QPACK_ERR_CUDA. A non-zero *flags means some kernel result is invalid. */
+int qpack_fetch_fault_flags(int32_t *flags);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int qpack_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QPACK_H_ */
