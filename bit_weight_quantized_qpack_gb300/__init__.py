@@ -1,0 +1,207 @@
+"""qpack for GB300: fused dequantization + matrix-vector / small-batch / prefill products over group-quantized
+low-bit weights (INT4 group-32 and the 2/3/5/6-bit 256-weight super-block formats).
+
+This module is a thin ctypes binding over the C ABI of ``libqpack.so`` (declared in ``include/qpack.h``). It
+only marshals arguments: every computation runs in the library's CUDA kernels. PyTorch supplies device memory
+and streams. There is no CPU fallback: importing works anywhere, but every compute call raises ``QpackError``
+when the CUDA library is not built or no GPU is present.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+Q4G32, Q2S, Q3S, Q5S, Q6S = 0, 1, 2, 3, 4
+FORMATS = {"Q4G32": Q4G32, "Q2S": Q2S, "Q3S": Q3S, "Q5S": Q5S, "Q6S": Q6S}
+F32, F16, BF16 = 0, 1, 2
+FLAG_RANGE = 1
+# (sub-blocks per super-block, asymmetric) for the super-block formats
+_SB = {Q2S: (16, True), Q3S: (16, False), Q5S: (8, True), Q6S: (16, False)}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqpack.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class QpackError(RuntimeError):
+    pass
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [("row_stride", ctypes.c_int64), ("packed_bytes", ctypes.c_int64),
+                ("scale_stride", ctypes.c_int64), ("scale_bytes", ctypes.c_int64),
+                ("block_bytes", ctypes.c_int64), ("nsub", ctypes.c_int64),
+                ("weight_bytes", ctypes.c_int64)]
+
+
+def lib():
+    """Load libqpack.so (raises QpackError if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise QpackError(f"libqpack.so not built ({LIB_PATH}); run __graft_entry__.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            sigs = {
+                "qpack_layout": ([I, I64, I64, ctypes.POINTER(Layout)], I),
+                "qpack_quantize": ([I, P, I, I64, I64, P, P, P, P, P, P, P, P], I),
+                "qpack_pack": ([I, I64, I64, P, P, P, P, P, P, P, P, P], I),
+                "qpack_quantize_pack": ([I, P, I, I64, I64, P, P, P, P], I),
+                "qpack_unpack": ([I, I64, I64, P, P, P, P, P, P, P, P, P], I),
+                "qpack_dequant": ([I, I64, I64, P, P, P, P], I),
+                "qgemv": ([I, P, P, I64, I64, P, P, P], I),
+                "qgemm_small": ([I, P, P, I64, I64, I, P, I64, P, I64, P], I),
+                "qgemm_prefill": ([I, P, P, I64, I64, I64, P, I64, P, I64, P], I),
+                "qpack_status_string": ([I], ctypes.c_char_p),
+                "qpack_fetch_fault_flags": ([ctypes.POINTER(ctypes.c_int32)], I),
+                "qpack_version": ([], I),
+            }
+            for name, (args, res) in sigs.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = lib().qpack_status_string(rc).decode()
+        raise QpackError(f"{what}: {msg} (status {rc})")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise QpackError("qpack kernels take CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(t):
+    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[t.dtype]
+
+
+def layout(fmt: int, N: int, K: int) -> dict:
+    out = Layout()
+    _check(lib().qpack_layout(int(fmt), int(N), int(K), ctypes.byref(out)), "qpack_layout")
+    return {f: getattr(out, f) for f, _ in Layout._fields_}
+
+
+def alloc_packed(fmt, N, K, device="cuda"):
+    """Caller-owned packed buffers of the right sizes: (packed uint8 [N, row_stride], scales or None)."""
+    L = layout(fmt, N, K)
+    packed = torch.empty((N, L["row_stride"]), dtype=torch.uint8, device=device)
+    gs = torch.empty((N, L["scale_stride"]), dtype=torch.float32, device=device) if fmt == Q4G32 else None
+    return packed, gs
+
+
+def alloc_parts(fmt, N, K, device="cuda"):
+    parts = dict(q=torch.empty((N, K), dtype=torch.int8, device=device), gscale=None, sub_scale=None,
+                 sub_min=None, d=None, dmin=None)
+    if fmt == Q4G32:
+        parts["gscale"] = torch.empty((N, K // 32), dtype=torch.float32, device=device)
+    else:
+        nsub, asym = _SB[fmt]
+        nb = K // 256
+        parts["sub_scale"] = torch.empty((N, nb * nsub), dtype=torch.uint8, device=device)
+        parts["d"] = torch.empty((N, nb), dtype=torch.int16, device=device)
+        if asym:
+            parts["sub_min"] = torch.empty((N, nb * nsub), dtype=torch.uint8, device=device)
+            parts["dmin"] = torch.empty((N, nb), dtype=torch.int16, device=device)
+    return parts
+
+
+def qpack_quantize(fmt, W, parts=None, status=None, stream=None):
+    N, K = W.shape
+    parts = alloc_parts(fmt, N, K, W.device) if parts is None else parts
+    rc = lib().qpack_quantize(int(fmt), _ptr(W), _dt(W), N, K, _ptr(parts["q"]), _ptr(parts["gscale"]),
+                              _ptr(parts["sub_scale"]), _ptr(parts["sub_min"]), _ptr(parts["d"]),
+                              _ptr(parts["dmin"]), _ptr(status), _stream(stream))
+    _check(rc, "qpack_quantize")
+    return parts
+
+
+def qpack_pack(fmt, N, K, parts, packed=None, group_scales=None, stream=None):
+    if packed is None:
+        packed, group_scales = alloc_packed(fmt, N, K, parts["q"].device)
+    rc = lib().qpack_pack(int(fmt), N, K, _ptr(parts["q"]), _ptr(parts["gscale"]), _ptr(parts["sub_scale"]),
+                          _ptr(parts["sub_min"]), _ptr(parts["d"]), _ptr(parts["dmin"]), _ptr(packed),
+                          _ptr(group_scales), _stream(stream))
+    _check(rc, "qpack_pack")
+    return packed, group_scales
+
+
+def qpack_quantize_pack(fmt, W, packed=None, group_scales=None, status=None, stream=None):
+    N, K = W.shape
+    if packed is None:
+        packed, group_scales = alloc_packed(fmt, N, K, W.device)
+    rc = lib().qpack_quantize_pack(int(fmt), _ptr(W), _dt(W), N, K, _ptr(packed), _ptr(group_scales),
+                                   _ptr(status), _stream(stream))
+    _check(rc, "qpack_quantize_pack")
+    return packed, group_scales
+
+
+def qpack_unpack(fmt, N, K, packed, group_scales=None, parts=None, stream=None):
+    parts = alloc_parts(fmt, N, K, packed.device) if parts is None else parts
+    rc = lib().qpack_unpack(int(fmt), N, K, _ptr(packed), _ptr(group_scales), _ptr(parts["q"]),
+                            _ptr(parts["gscale"]), _ptr(parts["sub_scale"]), _ptr(parts["sub_min"]),
+                            _ptr(parts["d"]), _ptr(parts["dmin"]), _stream(stream))
+    _check(rc, "qpack_unpack")
+    return parts
+
+
+def qpack_dequant(fmt, N, K, packed, group_scales=None, out=None, stream=None):
+    out = torch.empty((N, K), dtype=torch.float32, device=packed.device) if out is None else out
+    rc = lib().qpack_dequant(int(fmt), N, K, _ptr(packed), _ptr(group_scales), _ptr(out), _stream(stream))
+    _check(rc, "qpack_dequant")
+    return out
+
+
+def qgemv(fmt, packed, group_scales, N, K, x, y=None, stream=None):
+    y = torch.empty(N, dtype=torch.float32, device=x.device) if y is None else y
+    rc = lib().qgemv(int(fmt), _ptr(packed), _ptr(group_scales), N, K, _ptr(x), _ptr(y), _stream(stream))
+    _check(rc, "qgemv")
+    return y
+
+
+def qgemm_small(fmt, packed, group_scales, N, K, X, Y=None, stream=None):
+    M = X.shape[0]
+    Y = torch.empty((M, N), dtype=torch.float32, device=X.device) if Y is None else Y
+    rc = lib().qgemm_small(int(fmt), _ptr(packed), _ptr(group_scales), N, K, M, _ptr(X), X.stride(0), _ptr(Y),
+                           Y.stride(0), _stream(stream))
+    _check(rc, "qgemm_small")
+    return Y
+
+
+def qgemm_prefill(fmt, packed, group_scales, N, K, X, Y=None, stream=None):
+    M = X.shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    rc = lib().qgemm_prefill(int(fmt), _ptr(packed), _ptr(group_scales), N, K, M, _ptr(X), X.stride(0),
+                             _ptr(Y), Y.stride(0), _stream(stream))
+    _check(rc, "qgemm_prefill")
+    return Y
+
+
+def qpack_fetch_fault_flags() -> int:
+    v = ctypes.c_int32(0)
+    _check(lib().qpack_fetch_fault_flags(ctypes.byref(v)), "qpack_fetch_fault_flags")
+    return int(v.value)
+
+
+def qpack_status_string(status: int) -> str:
+    return lib().qpack_status_string(int(status)).decode()
+
+
+def qpack_version() -> int:
+    return int(lib().qpack_version())

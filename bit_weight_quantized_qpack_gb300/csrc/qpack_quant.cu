@@ -1,0 +1,423 @@
+// qpack_quant.cu — quantize, pack, fused quantize+pack, unpack and dequantize kernels (sm_103a).
+//
+// One warp owns one 256-weight block of a row (a super-block, or eight INT4 groups); lane l owns weights
+// 8l .. 8l+7 of the block. Loads are 16-byte vectors, the per-group / per-sub-block reductions are warp
+// shuffles, and every floating-point step uses an explicitly rounded intrinsic (no FMA contraction) so that
+// codes, scales and dequantized values are bit-identical to the IEEE definition in FORMATS.md.
+//
+// Quantizers: INT4 group-32 per the DBHOO-CIM article (pwwt.cn/news/4452170) §3.1; two-level round-to-nearest
+// super-blocks per the 2/3/5/6-bit article (lpnh.cn/news/2857666) §2.1 and §2.3 with the reading of
+// FORMATS.md §2a/§2b. Packing: §3.2 of the INT4 article (low nibble first), §2.2 (8 three-bit codes in 3
+// bytes, four 6-bit fields in 3 bytes) and §2.3 (4-bit plane + high-bit plane) of the 2/3/5/6-bit article.
+#include <cuda_runtime.h>
+
+#include "qpack_dev.cuh"
+#include "qpack_launch.h"
+
+namespace qpack {
+
+enum : int { MODE_QUANT_PARTS = 0, MODE_QUANT_PACKED = 1, MODE_PACK = 2, MODE_UNPACK = 3, MODE_DEQUANT = 4 };
+
+// Per-lane state of one 256-weight block.
+struct LaneBlock {
+    uint8_t u[8];     // stored codes (q + offset)
+    int L, M;         // this lane's sub-block scale / minimum integers
+    uint16_t d16, dm16;
+    float gscale;     // Q4G32: this lane's group scale
+};
+
+template <int F>
+__device__ __forceinline__ float sub_reduce_max(float v) {
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    if (Fmt<F>::sublen == 32) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+    return v;
+}
+template <int F>
+__device__ __forceinline__ float sub_reduce_min(float v) {
+    v = fminf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    if (Fmt<F>::sublen == 32) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ------------------------------------------------------------------------------------------------------------
+// Quantization of one block held by the warp. Returns the RANGE flag (fp16 d / dmin overflow).
+// ------------------------------------------------------------------------------------------------------------
+template <int F>
+__device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
+    using T = Fmt<F>;
+    if constexpr (F == FMT_Q4G32) {
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
+        a = sub_reduce_max<F>(a);                         // group of 32 = 4 lanes
+        float s = __fdiv_rn(a, 8.0f);
+        if (s < 1e-12f) s = 1e-12f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float t = clampf_ord(rintf(__fdiv_rn(w[i], s)), -8.0f, 7.0f);
+            B.u[i] = uint8_t(int(t) + 8);
+        }
+        B.gscale = s;
+        B.L = B.M = 0;
+        B.d16 = B.dm16 = 0;
+        return 0;
+    } else if constexpr (!T::asym) {
+        const float half_range = float(1 << (T::bits - 1));
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
+        a = sub_reduce_max<F>(a);
+        const float s = __fdiv_rn(a, half_range);
+        const float smax = warp_max(s);
+        const float d = __fdiv_rn(smax, float(T::lmax));
+        const uint16_t d16 = f2h_bits(d);
+        const float D = h2f_bits(d16);
+        float L = 0.0f;
+        if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
+        const float e = __fmul_rn(D, L);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float t = 0.0f;
+            if (e > 0.0f) t = clampf_ord(rintf(__fdiv_rn(w[i], e)), -half_range, half_range - 1.0f);
+            B.u[i] = uint8_t(int(t) + T::offset);
+        }
+        B.L = int(L);
+        B.M = 0;
+        B.d16 = d16;
+        B.dm16 = 0;
+        B.gscale = 0.0f;
+        return ((d16 & 0x7FFFu) == 0x7C00u) ? 1 : 0;
+    } else {
+        const float levels = float((1 << T::bits) - 1);
+        float lo = 0.0f, hi = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { lo = fminf(lo, w[i]); hi = fmaxf(hi, w[i]); }
+        lo = sub_reduce_min<F>(lo);
+        hi = sub_reduce_max<F>(hi);
+        const float s = __fdiv_rn(__fsub_rn(hi, lo), levels);
+        const float m = __fsub_rn(0.0f, lo);
+        const float smax = fmaxf(0.0f, warp_max(s));
+        const float mmax = fmaxf(0.0f, warp_max(m));
+        const uint16_t d16 = f2h_bits(__fdiv_rn(smax, float(T::lmax)));
+        const uint16_t dm16 = f2h_bits(__fdiv_rn(mmax, float(T::lmax)));
+        const float D = h2f_bits(d16), Dm = h2f_bits(dm16);
+        float L = 0.0f, M = 0.0f;
+        if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
+        if (Dm > 0.0f) M = clampf_ord(rintf(__fdiv_rn(m, Dm)), 0.0f, float(T::lmax));
+        const float es = __fmul_rn(D, L), em = __fmul_rn(Dm, M);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float t = 0.0f;
+            if (es > 0.0f) t = clampf_ord(rintf(__fdiv_rn(__fadd_rn(w[i], em), es)), 0.0f, levels);
+            B.u[i] = uint8_t(int(t));
+        }
+        B.L = int(L);
+        B.M = int(M);
+        B.d16 = d16;
+        B.dm16 = dm16;
+        B.gscale = 0.0f;
+        return (((d16 & 0x7FFFu) == 0x7C00u) || ((dm16 & 0x7FFFu) == 0x7C00u)) ? 1 : 0;
+    }
+}
+
+// ------------------------------------------------------------------------------------------------------------
+// Packing of one block (layouts of FORMATS.md §1 and §2c). `blk` points at the block's first packed byte;
+// `valid` is false for lanes beyond a partial INT4 row tail.
+// ------------------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void st_u16(uint8_t *p, uint32_t v) { *reinterpret_cast<uint16_t *>(p) = uint16_t(v); }
+__device__ __forceinline__ void st_u32(uint8_t *p, uint32_t v) { *reinterpret_cast<uint32_t *>(p) = v; }
+
+template <int F>
+__device__ __forceinline__ void pack_lane(const LaneBlock &B, int lane, bool valid, uint8_t *blk) {
+    if constexpr (F == FMT_Q4G32) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v |= uint32_t(B.u[i] & 15u) << (4 * i);
+        if (valid) st_u32(blk + 4 * lane, v);
+    } else if constexpr (F == FMT_Q2S) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v |= uint32_t(B.u[i] & 3u) << (2 * i);
+        st_u16(blk + 2 * lane, v);
+        if ((lane & 1) == 0) blk[64 + (lane >> 1)] = uint8_t((B.L & 15) | ((B.M & 15) << 4));
+        if (lane == 0) { st_u16(blk + 80, B.d16); st_u16(blk + 82, B.dm16); }
+    } else if constexpr (F == FMT_Q3S) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v |= uint32_t(B.u[i] & 7u) << (3 * i);
+        uint8_t *p = blk + 3 * lane;
+        p[0] = uint8_t(v); p[1] = uint8_t(v >> 8); p[2] = uint8_t(v >> 16);
+        // 16 six-bit sub-scales, 4 per 3 bytes: lane r < 4 packs L_{4r..4r+3}; L_j lives in lane 2j.
+        uint32_t f = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            int Lk = __shfl_sync(0xffffffffu, B.L, 8 * (lane & 3) + 2 * k);
+            f |= uint32_t(Lk & 63) << (6 * k);
+        }
+        if (lane < 4) {
+            uint8_t *q = blk + 96 + 3 * lane;
+            q[0] = uint8_t(f); q[1] = uint8_t(f >> 8); q[2] = uint8_t(f >> 16);
+        }
+        if (lane == 0) st_u16(blk + 108, B.d16);
+    } else if constexpr (F == FMT_Q5S) {
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            lo |= uint32_t(B.u[i] & 15u) << (4 * i);
+            hi |= uint32_t((B.u[i] >> 4) & 1u) << i;
+        }
+        st_u32(blk + 4 * lane, lo);
+        blk[128 + lane] = uint8_t(hi);
+        // fields 0..7 = L_0..L_7 (sub-block j in lanes 4j..4j+3), fields 8..15 = M_0..M_7; lane r < 4 packs
+        // fields 4r..4r+3.
+        const int r = lane & 3;
+        uint32_t f = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int src = 16 * (r & 1) + 4 * k;
+            int Lk = __shfl_sync(0xffffffffu, B.L, src);
+            int Mk = __shfl_sync(0xffffffffu, B.M, src);
+            f |= uint32_t((r >= 2 ? Mk : Lk) & 63) << (6 * k);
+        }
+        if (lane < 4) {
+            uint8_t *q = blk + 160 + 3 * lane;
+            q[0] = uint8_t(f); q[1] = uint8_t(f >> 8); q[2] = uint8_t(f >> 16);
+        }
+        if (lane == 0) st_u32(blk + 172, uint32_t(B.d16) | (uint32_t(B.dm16) << 16));
+    } else {  // Q6S
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            lo |= uint32_t(B.u[i] & 15u) << (4 * i);
+            hi |= uint32_t((B.u[i] >> 4) & 3u) << (2 * i);
+        }
+        st_u16(blk + 4 * lane, lo & 0xFFFFu);          // block start is only 2-byte aligned
+        st_u16(blk + 4 * lane + 2, lo >> 16);
+        st_u16(blk + 128 + 2 * lane, hi);
+        if ((lane & 1) == 0) blk[192 + (lane >> 1)] = uint8_t(B.L);
+        if (lane == 0) st_u16(blk + 208, B.d16);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------------------
+// Unpacking of one block from global memory into per-lane state.
+// ------------------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_u16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+__device__ __forceinline__ uint32_t ld_u24(const uint8_t *p) {
+    return uint32_t(p[0]) | (uint32_t(p[1]) << 8) | (uint32_t(p[2]) << 16);
+}
+
+template <int F>
+__device__ __forceinline__ void unpack_lane(const uint8_t *blk, int lane, bool valid, LaneBlock &B) {
+    if constexpr (F == FMT_Q4G32) {
+        uint32_t v = valid ? ld_u32(blk + 4 * lane) : 0x88888888u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) B.u[i] = uint8_t((v >> (4 * i)) & 15u);
+        B.L = B.M = 0; B.d16 = B.dm16 = 0;
+    } else if constexpr (F == FMT_Q2S) {
+        uint32_t v = ld_u16(blk + 2 * lane);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) B.u[i] = uint8_t((v >> (2 * i)) & 3u);
+        uint32_t lm = blk[64 + (lane >> 1)];
+        B.L = int(lm & 15u); B.M = int(lm >> 4);
+        B.d16 = uint16_t(ld_u16(blk + 80)); B.dm16 = uint16_t(ld_u16(blk + 82));
+    } else if constexpr (F == FMT_Q3S) {
+        uint32_t v = ld_u24(blk + 3 * lane);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) B.u[i] = uint8_t((v >> (3 * i)) & 7u);
+        const int j = lane >> 1;
+        uint32_t f = ld_u24(blk + 96 + 3 * (j >> 2));
+        B.L = int((f >> (6 * (j & 3))) & 63u); B.M = 0;
+        B.d16 = uint16_t(ld_u16(blk + 108)); B.dm16 = 0;
+    } else if constexpr (F == FMT_Q5S) {
+        uint32_t lo = ld_u32(blk + 4 * lane), hi = blk[128 + lane];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) B.u[i] = uint8_t(((lo >> (4 * i)) & 15u) | (((hi >> i) & 1u) << 4));
+        const int j = lane >> 2;
+        uint32_t fl = ld_u24(blk + 160 + 3 * (j >> 2)), fm = ld_u24(blk + 166 + 3 * (j >> 2));
+        B.L = int((fl >> (6 * (j & 3))) & 63u);
+        B.M = int((fm >> (6 * (j & 3))) & 63u);
+        B.d16 = uint16_t(ld_u16(blk + 172)); B.dm16 = uint16_t(ld_u16(blk + 174));
+    } else {  // Q6S
+        uint32_t lo = ld_u16(blk + 4 * lane) | (ld_u16(blk + 4 * lane + 2) << 16), hi = ld_u16(blk + 128 + 2 * lane);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) B.u[i] = uint8_t(((lo >> (4 * i)) & 15u) | (((hi >> (2 * i)) & 3u) << 4));
+        B.L = int(int8_t(blk[192 + (lane >> 1)])); B.M = 0;
+        B.d16 = uint16_t(ld_u16(blk + 208)); B.dm16 = 0;
+    }
+}
+
+// Dequantize a lane's 8 weights (FORMATS.md step 5 of each quantizer; Q4G32 w' = s * q).
+template <int F>
+__device__ __forceinline__ void dequant_lane(const LaneBlock &B, float out[8]) {
+    using T = Fmt<F>;
+    if constexpr (F == FMT_Q4G32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) out[i] = __fmul_rn(B.gscale, float(int(B.u[i]) - 8));
+    } else {
+        const float D = h2f_bits(B.d16);
+        const float es = __fmul_rn(D, float(B.L));
+        const float em = T::asym ? __fmul_rn(h2f_bits(B.dm16), float(B.M)) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float v = __fmul_rn(es, float(int(B.u[i]) - T::offset));
+            if (T::asym) v = __fsub_rn(v, em);
+            out[i] = v;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------------------------
+// The block kernel: one template per (format, mode, input dtype).
+// ------------------------------------------------------------------------------------------------------------
+template <int F, int MODE, int WDT>
+__global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
+    using T = Fmt<F>;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int64_t total = a.N * a.nbk;
+    int flags = 0;
+    for (int64_t wb = warp0; wb < total; wb += nwarps) {
+        const int64_t r = wb / a.nbk, b = wb - r * a.nbk;
+        const int64_t k0 = 256 * b + 8 * lane;           // first weight of this lane within the row
+        const bool valid = k0 < a.K;                      // only INT4 rows can end inside a block
+        LaneBlock B;
+        B.gscale = 0.0f;
+        const int j = lane / (T::sublen / 8);             // this lane's group / sub-block within the block
+        if constexpr (MODE == MODE_QUANT_PARTS || MODE == MODE_QUANT_PACKED) {
+            float w[8];
+            if (valid) {
+                load8<WDT>(a.W, r * a.K + k0, w);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = 0.0f;
+            }
+            flags |= quantize_lane<F>(w, B);
+        } else if constexpr (MODE == MODE_PACK) {
+            if (valid) {
+                uint2 c = *reinterpret_cast<const uint2 *>(a.codes + r * a.K + k0);
+                uint32_t cw[2] = {c.x, c.y};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) B.u[i] = uint8_t(int(int8_t(cw[i >> 2] >> (8 * (i & 3)))) + T::offset);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) B.u[i] = uint8_t(T::offset);
+            }
+            if constexpr (F == FMT_Q4G32) {
+                B.gscale = valid ? a.gscale[r * (a.K / 32) + 8 * b + j] : 0.0f;
+                B.L = B.M = 0; B.d16 = B.dm16 = 0;
+            } else {
+                const int64_t sb = r * a.nbk + b;
+                B.L = a.sub_scale[sb * T::nsub + j];
+                B.M = T::asym ? a.sub_min[sb * T::nsub + j] : 0;
+                B.d16 = a.d[sb];
+                B.dm16 = T::asym ? a.dmin[sb] : uint16_t(0);
+            }
+        } else {  // UNPACK / DEQUANT read packed bytes
+            const uint8_t *blk = a.packed_in + r * a.row_stride + b * T::bytes;
+            unpack_lane<F>(blk, lane, valid, B);
+            if constexpr (F == FMT_Q4G32) B.gscale = valid ? a.gs_in[r * a.scale_stride + 8 * b + j] : 0.0f;
+        }
+
+        if constexpr (MODE == MODE_QUANT_PARTS || MODE == MODE_UNPACK) {
+            if (valid) {
+                uint32_t cw[2] = {0u, 0u};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) cw[i >> 2] |= uint32_t(uint8_t(int(B.u[i]) - T::offset)) << (8 * (i & 3));
+                *reinterpret_cast<uint2 *>(a.codes + r * a.K + k0) = make_uint2(cw[0], cw[1]);
+            }
+            const bool first_of_sub = (lane % (T::sublen / 8)) == 0;
+            if constexpr (F == FMT_Q4G32) {
+                if (valid && first_of_sub) a.gscale[r * (a.K / 32) + 8 * b + j] = B.gscale;
+            } else {
+                const int64_t sb = r * a.nbk + b;
+                if (first_of_sub) {
+                    a.sub_scale[sb * T::nsub + j] = uint8_t(B.L);
+                    if (T::asym) a.sub_min[sb * T::nsub + j] = uint8_t(B.M);
+                }
+                if (lane == 0) {
+                    a.d[sb] = B.d16;
+                    if (T::asym) a.dmin[sb] = B.dm16;
+                }
+            }
+        } else if constexpr (MODE == MODE_QUANT_PACKED || MODE == MODE_PACK) {
+            uint8_t *row = a.packed + r * a.row_stride;
+            pack_lane<F>(B, lane, valid, row + b * T::bytes);
+            if constexpr (F == FMT_Q4G32) {
+                const bool first_of_group = (lane & 3) == 0;
+                if (valid && first_of_group) a.gs_out[r * a.scale_stride + 8 * b + j] = B.gscale;
+                if (b == a.nbk - 1) {                      // zero the scale-row padding
+                    const int64_t g0 = a.K / 32;
+                    if (g0 + lane < a.scale_stride) a.gs_out[r * a.scale_stride + g0 + lane] = 0.0f;
+                }
+            } else {
+                if (b == a.nbk - 1) {                      // zero the row padding (< 16 bytes)
+                    const int64_t used = a.nbk * T::bytes;
+                    if (used + lane < a.row_stride) row[used + lane] = 0;
+                }
+            }
+        } else {  // DEQUANT
+            if (valid) {
+                float o[8];
+                dequant_lane<F>(B, o);
+                float4 *dst = reinterpret_cast<float4 *>(a.out + r * a.K + k0);
+                dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+            }
+        }
+    }
+    if constexpr (MODE == MODE_QUANT_PARTS || MODE == MODE_QUANT_PACKED) {
+        flags = __any_sync(0xffffffffu, flags != 0) ? 1 : 0;
+        if (flags && lane == 0 && a.status) atomicOr(a.status, 1);
+    }
+}
+
+template <int F, int MODE, int WDT>
+static cudaError_t launch_block(const BlockArgs &a, cudaStream_t s) {
+    const int64_t warps = a.N * a.nbk;
+    int64_t blocks = (warps + 7) / 8;
+    const int64_t cap = 152 * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) return cudaSuccess;
+    block_kernel<F, MODE, WDT><<<unsigned(blocks), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int F, int MODE>
+static cudaError_t launch_wdt(const BlockArgs &a, int wdt, cudaStream_t s) {
+    switch (wdt) {
+        case DT_F32: return launch_block<F, MODE, DT_F32>(a, s);
+        case DT_F16: return launch_block<F, MODE, DT_F16>(a, s);
+        default: return launch_block<F, MODE, DT_BF16>(a, s);
+    }
+}
+
+template <int F>
+static cudaError_t launch_mode(const BlockArgs &a, int mode, int wdt, cudaStream_t s) {
+    switch (mode) {
+        case MODE_QUANT_PARTS: return launch_wdt<F, MODE_QUANT_PARTS>(a, wdt, s);
+        case MODE_QUANT_PACKED: return launch_wdt<F, MODE_QUANT_PACKED>(a, wdt, s);
+        case MODE_PACK: return launch_block<F, MODE_PACK, DT_F32>(a, s);
+        case MODE_UNPACK: return launch_block<F, MODE_UNPACK, DT_F32>(a, s);
+        default: return launch_block<F, MODE_DEQUANT, DT_F32>(a, s);
+    }
+}
+
+cudaError_t launch_block_op(int fmt, int mode, int wdt, const BlockArgs &a, cudaStream_t s) {
+    switch (fmt) {
+        case FMT_Q4G32: return launch_mode<FMT_Q4G32>(a, mode, wdt, s);
+        case FMT_Q2S: return launch_mode<FMT_Q2S>(a, mode, wdt, s);
+        case FMT_Q3S: return launch_mode<FMT_Q3S>(a, mode, wdt, s);
+        case FMT_Q5S: return launch_mode<FMT_Q5S>(a, mode, wdt, s);
+        default: return launch_mode<FMT_Q6S>(a, mode, wdt, s);
+    }
+}
+
+}  // namespace qpack

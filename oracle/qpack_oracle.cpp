@@ -231,7 +231,7 @@ int quantize_sb_row(const SbFormat &F, const float *w, int64_t K, int8_t *q, uin
                     hi = std::fmax(hi, v);
                 }
                 s[j] = (hi - lo) / levels;
-                m[j] = -lo;
+                m[j] = 0.0f - lo;          // -lo, written as a subtraction so that it is never -0
             }
             float smax = 0.0f, mmax = 0.0f;
             for (int j = 0; j < F.nsub; ++j) { smax = std::fmax(smax, s[j]); mmax = std::fmax(mmax, m[j]); }

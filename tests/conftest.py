@@ -42,3 +42,34 @@ def orc():
     import oracle
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def qpg():
+    """The built CUDA library on cuda:0 (GPU tests only)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_weight_quantized_qpack_gb300 import _build
+    _build.build()
+    import bit_weight_quantized_qpack_gb300 as qp
+    qp.lib()
+    return qp
+
+
+def to_np_fp32(t):
+    """Exact fp32 numpy copy of a CPU/GPU tensor of dtype fp32/fp16/bf16."""
+    import torch
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+def gemv_bound_check(y_gpu, y_ref, deq_rows, X, tol=1e-4):
+    """max |y - y_ref| / (||w'_r|| * ||x_m||) <= tol over every (m, r); returns the worst ratio."""
+    import numpy as np
+    deq = np.asarray(deq_rows, np.float64)
+    Xd = np.atleast_2d(np.asarray(X, np.float64))
+    bound = tol * np.outer(np.linalg.norm(Xd, axis=1), np.linalg.norm(deq, axis=1))
+    err = np.abs(np.atleast_2d(np.asarray(y_gpu, np.float64)) - np.atleast_2d(y_ref))
+    ratio = err / np.maximum(bound, 1e-300) * tol
+    assert np.all(err <= bound), f"worst |err|/(||w||*||x||) = {ratio.max():.3e} > {tol}"
+    return float(ratio.max())

@@ -1,0 +1,88 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function include/qpack.h declares, and its
+host-only entry points (layout, status strings, argument validation that rejects before any launch) behave."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def qp():
+    from bit_weight_quantized_qpack_gb300 import _build
+    _build.build()
+    import bit_weight_quantized_qpack_gb300 as qp
+    qp.lib()
+    return qp
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?(?:int|void|char\s*\*|const char\s*\*)\s*\*?\s*(\w+)\s*\(",
+                                text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(qp):
+    names = declared_functions()
+    assert {"qpack_quantize", "qpack_pack", "qgemv", "qgemm_small", "qgemm_prefill"} <= set(names)
+    L = ctypes.CDLL(qp.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_layout_matches_oracle(qp, orc):
+    for name, fmt in qp.FORMATS.items():
+        for N, K in ((1, 256), (7, 4096), (11008, 4096), (4096, 11008), (3, 28672)):
+            a = qp.layout(fmt, N, K)
+            b = orc.layout(fmt, N, K)
+            assert a["row_stride"] == b["row_stride"] and a["packed_bytes"] == b["packed_bytes"]
+            assert a["scale_stride"] == b["scale_stride"] and a["scale_bytes"] == b["scale_bytes"]
+            assert a["weight_bytes"] == a["packed_bytes"] + a["scale_bytes"]
+
+
+def test_config_byte_counts(qp):
+    # 4096x4096 INT4: 8,388,608 code bytes + 2,097,152 scale bytes; 11008x4096 3-bit: 19,374,080 bytes
+    assert qp.layout(qp.Q4G32, 4096, 4096)["weight_bytes"] == 10_485_760
+    assert qp.layout(qp.Q3S, 11008, 4096)["weight_bytes"] == 19_374_080
+    # padded rows for K = 11008
+    assert qp.layout(qp.Q2S, 1, 11008)["row_stride"] == 3616
+    assert qp.layout(qp.Q3S, 1, 11008)["row_stride"] == 4736
+    assert qp.layout(qp.Q6S, 1, 11008)["row_stride"] == 9040
+
+
+def test_argument_validation_rejects_before_launch(qp):
+    L = qp.lib()
+    P = ctypes.c_void_p
+    good = P(1 << 20)          # never dereferenced: every call below fails validation first
+    odd = P((1 << 20) + 4)
+    SHAPE, ALIGN, ARG, UNSUP = -2, -3, -1, -6
+    assert L.qgemv(qp.Q4G32, good, good, 8, 48, good, good, None) == SHAPE
+    assert L.qgemv(qp.Q3S, good, None, 8, 4096 + 32, good, good, None) == SHAPE
+    assert L.qgemv(qp.Q3S, odd, None, 8, 4096, good, good, None) == ALIGN
+    assert L.qgemv(qp.Q4G32, good, None, 8, 4096, good, good, None) == ARG
+    assert L.qgemv(9, good, good, 8, 4096, good, good, None) == ARG
+    assert L.qgemv(qp.Q3S, good, None, 8, 4096, odd, good, None) == ALIGN
+    assert L.qgemm_small(qp.Q5S, good, None, 8, 4096, 17, good, 4096, good, 8, None) == SHAPE
+    assert L.qgemm_small(qp.Q5S, good, None, 8, 4096, 2, good, 4095, good, 8, None) == SHAPE
+    assert L.qgemm_small(qp.Q5S, good, None, 8, 4096, 2, good, 4100, good, 8, None) == ALIGN
+    assert L.qgemv(qp.Q5S, good, None, 8, 65536 + 256, good, good, None) == UNSUP
+    assert L.qgemm_prefill(qp.Q4G32, good, good, 8, 96, 4, good, 96, good, 8, None) == SHAPE
+    assert L.qpack_quantize_pack(qp.Q2S, good, 7, 8, 256, good, None, None, None) == ARG
+    assert L.qpack_quantize_pack(qp.Q2S, odd, 0, 8, 256, good, None, None, None) == ALIGN
+    assert L.qpack_dequant(qp.Q6S, -1, 256, good, None, good, None) == ARG
+    # empty problems are accepted and launch nothing
+    assert L.qgemv(qp.Q3S, good, None, 0, 4096, good, good, None) == 0
+    assert L.qgemm_small(qp.Q3S, good, None, 8, 4096, 0, good, 4096, good, 8, None) == 0
+
+
+def test_status_strings(qp):
+    for s in (0, -1, -2, -3, -4, -5, -6, 12345):
+        assert qp.qpack_status_string(s)
+    assert qp.qpack_version() >= 10000

@@ -1,0 +1,137 @@
+"""GPU parity of the fused dequant-GEMV and the small-batch GEMM against the oracle's fp64 products:
+max |y - y_ref| / (||w'_r|| * ||x||) <= 1e-4 (2/3/5/6-bit article §1.2 / §3.3; DBHOO-CIM article §3.3)."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import gemv_bound_check, to_np_fp32
+
+pytestmark = pytest.mark.gpu
+
+ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S"]
+
+
+def case(orc, fmt, N, K, seed, b=0.02):
+    from bit_weight_quantized_qpack_gb300 import synth
+    W = synth.laplace((N, K), b, seed)
+    rp, rgs, _ = orc.quantize_pack(fmt, W.numpy())
+    return rp, rgs
+
+
+def run_gemv(qpg, fmt, rp, rgs, N, K, x):
+    pd = torch.from_numpy(rp).cuda()
+    gd = None if rgs is None else torch.from_numpy(rgs).cuda()
+    y = qpg.qgemv(fmt, pd, gd, N, K, x.cuda())
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def shapes(name):
+    s = [(1, 256), (3, 512), (4, 4096), (37, 4096 + 768), (130, 8192 + 256), (9, 12288)]
+    if name == "Q4G32":
+        s += [(5, 96), (7, 4096 + 32)]
+    return s
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_gemv_tiles_and_ragged_tails(qpg, orc, name):
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    for i, (N, K) in enumerate(shapes(name)):
+        rp, rgs = case(orc, fmt, N, K, 300 + i)
+        x = synth.normal((K,), 1.0, 400 + i, dtype=torch.float16)
+        y = run_gemv(qpg, fmt, rp, rgs, N, K, x)
+        xb = x.numpy().view(np.uint16)
+        y_ref = orc.gemv(fmt, N, K, rp, rgs, xb)
+        deq = orc.dequant(fmt, N, K, rp, rgs)
+        gemv_bound_check(y, y_ref, deq, x.numpy().astype(np.float64)[None, :])
+    assert qpg.qpack_fetch_fault_flags() == 0
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_gemv_one_hot_columns(qpg, orc, name):
+    fmt = qpg.FORMATS[name]
+    N, K = 21, 4096 + 256
+    rp, rgs = case(orc, fmt, N, K, 500)
+    deq = orc.dequant(fmt, N, K, rp, rgs)
+    for k in (0, 1, 31, 255, 4096, K - 1):
+        x = torch.zeros(K, dtype=torch.float16)
+        x[k] = 1.0
+        y = run_gemv(qpg, fmt, rp, rgs, N, K, x)
+        assert np.allclose(y, deq[:, k], rtol=1e-6, atol=1e-9 * np.abs(deq).max())
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_gemv_large_activations_and_zero_rows(qpg, orc, name):
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    N, K = 16, 2048
+    W = synth.laplace((N, K), 0.02, 600)
+    W[3] = 0
+    rp, rgs, _ = orc.quantize_pack(fmt, W.numpy())
+    x = (synth.normal((K,), 1.0, 601) * 30).to(torch.float16)   # |x| up to ~150
+    y = run_gemv(qpg, fmt, rp, rgs, N, K, x)
+    y_ref = orc.gemv(fmt, N, K, rp, rgs, x.numpy().view(np.uint16))
+    deq = orc.dequant(fmt, N, K, rp, rgs)
+    gemv_bound_check(y, y_ref, deq, x.numpy().astype(np.float64)[None, :])
+    assert y[3] == 0.0 or abs(y[3]) < 1e-6
+
+
+@pytest.mark.parametrize("name", ALL)
+@pytest.mark.parametrize("M", [2, 3, 4, 8, 16])
+def test_small_batch(qpg, orc, name, M):
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    N, K = 45, 4096 + 512
+    rp, rgs = case(orc, fmt, N, K, 700 + M)
+    X = synth.normal((M, K), 1.0, 800 + M, dtype=torch.float16)
+    pd = torch.from_numpy(rp).cuda()
+    gd = None if rgs is None else torch.from_numpy(rgs).cuda()
+    Y = qpg.qgemm_small(fmt, pd, gd, N, K, X.cuda())
+    torch.cuda.synchronize()
+    Y_ref = orc.gemm(fmt, N, K, rp, rgs, X.numpy().view(np.uint16))
+    deq = orc.dequant(fmt, N, K, rp, rgs)
+    gemv_bound_check(Y.cpu().numpy(), Y_ref, deq, X.numpy().astype(np.float64))
+
+
+def test_small_batch_strided(qpg, orc):
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.Q5S
+    N, K, M = 19, 1024, 5
+    rp, rgs = case(orc, fmt, N, K, 900)
+    Xfull = synth.normal((M, K + 64), 1.0, 901, dtype=torch.float16)
+    X = Xfull[:, :K]
+    Yfull = torch.full((M, N + 13), 7.0, device="cuda")
+    qpg.qgemm_small(fmt, torch.from_numpy(rp).cuda(), None, N, K, Xfull.cuda()[:, :K], Y=Yfull[:, :N])
+    torch.cuda.synchronize()
+    Yn = Yfull.cpu().numpy()
+    assert np.all(Yn[:, N:] == 7.0)                         # nothing written past ldy's valid columns
+    Y_ref = orc.gemm(fmt, N, K, rp, rgs, X.contiguous().numpy().view(np.uint16))
+    gemv_bound_check(Yn[:, :N], Y_ref, orc.dequant(fmt, N, K, rp, rgs), X.numpy().astype(np.float64))
+
+
+def test_config_int4_4096(qpg, orc):
+    from bit_weight_quantized_qpack_gb300 import synth
+    W = synth.normal_with_outliers((4096, 4096), 0.02, 0.001, 0.1, 0.5, seed=0)
+    x = synth.normal((4096,), 1.0, seed=1, dtype=torch.float16)
+    packed, gs = qpg.qpack_quantize_pack(qpg.Q4G32, W.cuda())
+    y = qpg.qgemv(qpg.Q4G32, packed, gs, 4096, 4096, x.cuda())
+    torch.cuda.synchronize()
+    rp, rgs, _ = orc.quantize_pack(orc.Q4G32, W.numpy())
+    y_ref = orc.gemv(orc.Q4G32, 4096, 4096, rp, rgs, x.numpy().view(np.uint16), nthreads=8)
+    gemv_bound_check(y.cpu().numpy(), y_ref, orc.dequant(orc.Q4G32, 4096, 4096, rp, rgs),
+                     x.numpy().astype(np.float64)[None, :])
+
+
+def test_config_q3s_11008(qpg, orc):
+    from bit_weight_quantized_qpack_gb300 import synth
+    W = synth.laplace((11008, 4096), 0.015, seed=0)
+    x = synth.normal((4096,), 1.0, seed=1, dtype=torch.float16)
+    packed, _ = qpg.qpack_quantize_pack(qpg.Q3S, W.cuda())
+    y = qpg.qgemv(qpg.Q3S, packed, None, 11008, 4096, x.cuda())
+    torch.cuda.synchronize()
+    rp, _, _ = orc.quantize_pack(orc.Q3S, W.numpy())
+    y_ref = orc.gemv(orc.Q3S, 11008, 4096, rp, None, x.numpy().view(np.uint16), nthreads=8)
+    gemv_bound_check(y.cpu().numpy(), y_ref, orc.dequant(orc.Q3S, 11008, 4096, rp, None),
+                     x.numpy().astype(np.float64)[None, :])
+    assert qpg.qpack_fetch_fault_flags() == 0

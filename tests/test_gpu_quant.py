@@ -1,0 +1,130 @@
+"""GPU parity of quantize / pack / fused quantize+pack / unpack / dequantize: every code, packed byte, scale and
+dequantized value must equal the oracle's bit for bit (FORMATS.md; DBHOO-CIM article §3.1-§3.2 for INT4,
+2/3/5/6-bit article §2.1-§2.3 for the super-block formats)."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import to_np_fp32
+
+pytestmark = pytest.mark.gpu
+
+ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S"]
+DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def weights(N, K, seed, dtype=torch.float32):
+    from bit_weight_quantized_qpack_gb300 import synth
+    W = synth.laplace((N, K), 0.02, seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    mask = torch.rand(N, K, generator=g) < 0.002
+    W[mask] *= 25.0                                      # outliers
+    if N > 2:
+        W[1] = 0.0                                       # an all-zero row
+        W[2, : min(K, 256)] = -W[2, : min(K, 256)].abs()  # a negative-only block
+    return W.to(dtype)
+
+
+def shapes(name):
+    out = [(1, 256), (37, 1024), (5, 4096 + 256)]
+    if name == "Q4G32":
+        out += [(9, 96), (3, 32), (6, 4096 + 160)]       # rows ending inside a 256-weight block
+    return out
+
+
+def cmp_parts(got, ref):
+    for k in ("q", "gscale", "sub_scale", "sub_min", "d", "dmin"):
+        if ref.get(k) is None:
+            continue
+        g = got[k].cpu().numpy()
+        r = ref[k]
+        if g.dtype == np.int16:
+            g = g.view(np.uint16)
+        if g.dtype == np.float32:
+            assert np.array_equal(g.view(np.uint32), r.view(np.uint32)), k
+        else:
+            assert np.array_equal(g, r), k
+
+
+@pytest.mark.parametrize("name", ALL)
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_quantize_parts_and_packed_bit_exact(qpg, orc, name, dt):
+    fmt = qpg.FORMATS[name]
+    for i, (N, K) in enumerate(shapes(name)):
+        W = weights(N, K, 100 + i, DT[dt])
+        Wd = W.cuda()
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        parts = qpg.qpack_quantize(fmt, Wd, status=st)
+        packed, gs = qpg.qpack_quantize_pack(fmt, Wd, status=st)
+        torch.cuda.synchronize()
+        Wn = to_np_fp32(W)
+        ref = orc.quantize(fmt, Wn)
+        cmp_parts(parts, ref)
+        rp, rgs = orc.pack(fmt, N, K, ref)
+        assert np.array_equal(packed.cpu().numpy(), rp)
+        if rgs is not None:
+            assert np.array_equal(gs.cpu().numpy().view(np.uint32), rgs.view(np.uint32))
+        assert int(st.item()) == ref["flags"] == 0
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_pack_unpack_dequant_bit_exact(qpg, orc, name):
+    fmt = qpg.FORMATS[name]
+    for i, (N, K) in enumerate(shapes(name)):
+        Wn = to_np_fp32(weights(N, K, 200 + i))
+        ref = orc.quantize(fmt, Wn)
+        rp, rgs = orc.pack(fmt, N, K, ref)
+        # pack the oracle's parts on the GPU
+        parts = {k: (None if v is None or k == "flags" else torch.from_numpy(
+            v.view(np.int16) if v.dtype == np.uint16 else v).cuda()) for k, v in ref.items()}
+        packed, gs = qpg.qpack_pack(fmt, N, K, parts)
+        torch.cuda.synchronize()
+        assert np.array_equal(packed.cpu().numpy(), rp)
+        # unpack and dequantize the oracle's bytes on the GPU
+        pd = torch.from_numpy(rp).cuda()
+        gd = None if rgs is None else torch.from_numpy(rgs).cuda()
+        back = qpg.qpack_unpack(fmt, N, K, pd, gd)
+        deq = qpg.qpack_dequant(fmt, N, K, pd, gd)
+        torch.cuda.synchronize()
+        cmp_parts(back, ref)
+        rdeq = orc.dequant(fmt, N, K, rp, rgs)
+        assert np.array_equal(deq.cpu().numpy().view(np.uint32), rdeq.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", ["Q2S", "Q3S", "Q5S", "Q6S"])
+def test_range_flag(qpg, orc, name):
+    fmt = qpg.FORMATS[name]
+    W = torch.zeros(3, 512)
+    W[1, 256:] = 1e9
+    W[1, 300] = -1e9
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    packed, _ = qpg.qpack_quantize_pack(fmt, W.cuda(), status=st)
+    torch.cuda.synchronize()
+    ref_packed, _, flags = orc.quantize_pack(fmt, W.numpy())
+    assert flags == 1 and int(st.item()) == 1
+    assert np.array_equal(packed.cpu().numpy(), ref_packed)
+    st.zero_()
+    qpg.qpack_quantize_pack(fmt, torch.ones(2, 256, device="cuda") * 0.5, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+
+def test_int4_config_matrix_bit_exact(qpg, orc):
+    """4096x4096 fp32 W ~ N(0, 0.02^2) with 0.1% ±U(0.1, 0.5) outliers (seed 0), INT4 group 32."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    W = synth.normal_with_outliers((4096, 4096), 0.02, 0.001, 0.1, 0.5, seed=0)
+    packed, gs = qpg.qpack_quantize_pack(qpg.Q4G32, W.cuda())
+    torch.cuda.synchronize()
+    rp, rgs, _ = orc.quantize_pack(orc.Q4G32, W.numpy())
+    assert np.array_equal(packed.cpu().numpy(), rp)
+    assert np.array_equal(gs.cpu().numpy().view(np.uint32), rgs.view(np.uint32))
+
+
+def test_q3s_config_matrix_bit_exact(qpg, orc):
+    """11008x4096 Laplace(0, 0.015) weights (seed 0), 3-bit 110-byte super-blocks."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    W = synth.laplace((11008, 4096), 0.015, seed=0)
+    packed, _ = qpg.qpack_quantize_pack(qpg.Q3S, W.cuda())
+    torch.cuda.synchronize()
+    rp, _, _ = orc.quantize_pack(orc.Q3S, W.numpy())
+    assert np.array_equal(packed.cpu().numpy(), rp)
