@@ -1,0 +1,423 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused dequant-GEMV (decode, batch 1) on one GB300 per rank.
+
+Workload (headline): the 3-bit super-block GEMV of an 11008x4096 weight matrix (110-byte / 256-weight
+super-blocks, Laplace(0, 0.015) weights, seed 0), fp16 activations ~ N(0, 1), fp32 output. One step = one GEMV
+over each of R distinct packed copies of that matrix with R distinct activation vectors (R chosen so the copies
+total well over the 129 MB L2, so every step streams its weights from HBM). Metric: effective weight GB/s =
+packed bytes (codes + scales + row padding) / time, the definition of the DBHOO-CIM article (pwwt.cn/news/
+4452170) §4.4 and of the 2/3/5/6-bit article (lpnh.cn/news/2857666) §1.2; also reported as a fraction of the
+measured HBM copy bandwidth.
+
+Extra (rank 0): a 7B-Llama-shaped decode step (32 layers x {q,k,v,o 4096x4096, gate/up 11008x4096,
+down 4096x11008}) per super-block format, as tokens/s-equivalent and GB/s.
+
+`--impl reference` times the CPU oracle (the plain C++ implementation the tests check against) on the same
+workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused dequant-GEMV effective weight GB/s & % of GB300 HBM peak; decode tok/s equiv"
+N_ROWS, K_COLS = 11008, 4096
+FALLBACK_HBM, FALLBACK_BF16 = 6800.0, 1900.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one headline launch from an ncu capture, valid only for the
+# CUDA sources whose digest is recorded here (profiles/gemv_q3s_11008x4096.md gives the command).
+TRAFFIC = {"csrc_digest": "043b3a139b68ef87", "bytes_per_launch": 19405824}
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "bit_weight_quantized_qpack_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM, FALLBACK_BF16, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_gemv_sample(packed_np, x_np, seconds_target=10.0, max_seconds=30.0):
+    """Time the oracle's fp64 GEMV over the whole matrix with every host core, repeated ~10-30 s."""
+    import oracle
+    n = os.cpu_count() or 1
+    wbytes = packed_np.nbytes
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.gemv(oracle.Q3S, N_ROWS, K_COLS, packed_np, None, x_np, nthreads=n)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target or el * (reps + 1) / reps > max_seconds:
+            break
+    return {"value": wbytes * reps / el / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{reps} full 11008x4096 3-bit GEMV(s) ({wbytes} packed bytes each), fp64 oracle, "
+                      f"{n} threads, {el:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """The oracle (CPU) on the same workload: one full 11008x4096 GEMV per step, all host cores."""
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from bit_weight_quantized_qpack_gb300 import synth
+    W = synth.laplace((N_ROWS, K_COLS), 0.015, seed=0)
+    packed, _, _ = oracle.quantize_pack(oracle.Q3S, W.numpy())
+    x = synth.normal((K_COLS,), 1.0, seed=1).half().numpy().view(np.uint16)
+    n = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.gemv(oracle.Q3S, N_ROWS, K_COLS, packed, None, x, nthreads=n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemv(oracle.Q3S, N_ROWS, K_COLS, packed, None, x, nthreads=n)
+    el = time.perf_counter() - t0
+    v = packed.nbytes * args.steps / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "3-bit super-block GEMV 11008x4096, batch 1 (one full GEMV per step)",
+                       "format": "Q3S", "N": N_ROWS, "K": K_COLS, "bytes_per_gemv": int(packed.nbytes)},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": n, "kind": "oracle",
+                             "sample": f"{args.steps} full GEMVs, fp64 oracle, {n} threads"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def decode_7b_extra(qp, torch, synth, dev, steps=10):
+    """7B-Llama-shaped decode step per super-block format: tokens/s-equivalent = 1 / (sum of GEMV times)."""
+    shapes = [(4096, 4096)] * 4 + [(11008, 4096)] * 2 + [(4096, 11008)]
+    out = {}
+    for name in ("Q2S", "Q3S", "Q5S", "Q6S"):
+        fmt = qp.FORMATS[name]
+        mats, total = [], 0
+        for layer in range(32):
+            for mi, (N, K) in enumerate(shapes):
+                W = synth.laplace((N, K), 0.02, seed=synth.seed_for(3, layer, mi), device=dev)
+                p, g = qp.qpack_quantize_pack(fmt, W)
+                del W
+                mats.append((p, N, K))
+                total += qp.layout(fmt, N, K)["weight_bytes"]
+        x4 = synth.normal((4096,), 1.0, seed=11, device=dev, dtype=torch.float16)
+        x11 = synth.normal((11008,), 1.0, seed=12, device=dev, dtype=torch.float16)
+        ys = {4096: torch.empty(4096, device=dev), 11008: torch.empty(11008, device=dev)}
+        s = torch.cuda.Stream(device=dev)
+
+        def step():
+            for p, N, K in mats:
+                qp.qgemv(fmt, p, None, N, K, x4 if K == 4096 else x11, ys[N], stream=s)
+
+        with torch.cuda.stream(s):
+            step()
+            torch.cuda.synchronize(dev)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=s):
+                step()
+            for _ in range(3):
+                gr.replay()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(steps):
+                gr.replay()
+            e1.record(s)
+        torch.cuda.synchronize(dev)
+        t = e0.elapsed_time(e1) / 1e3 / steps
+        out[name] = {"tok_per_s_equiv": 1.0 / t, "GBps": total / t / 1e9, "bytes_per_step": total,
+                     "ms_per_step": t * 1e3, "launches": len(mats)}
+        del mats, gr
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    from bit_weight_quantized_qpack_gb300 import _build
+    _build.build()
+    import bit_weight_quantized_qpack_gb300 as qp
+    from bit_weight_quantized_qpack_gb300 import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+
+    fmt = qp.Q3S
+    lay = qp.layout(fmt, N_ROWS, K_COLS)
+    wbytes = lay["weight_bytes"]
+    W = synth.laplace((N_ROWS, K_COLS), 0.015, seed=0, device=dev)
+    packed0, _ = qp.qpack_quantize_pack(fmt, W)
+    del W
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size or (126 << 20)
+    R = args.copies or max(8, int(-(-8 * l2 // wbytes)))              # copies total >= 8x L2
+    P = torch.empty((R, N_ROWS, lay["row_stride"]), dtype=torch.uint8, device=dev)
+    P.copy_(packed0.unsqueeze(0).expand(R, -1, -1))
+    del packed0
+    X = synth.normal((R, K_COLS), 1.0, seed=1, device=dev, dtype=torch.float16)
+    Y = torch.empty((R, N_ROWS), dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def step():
+        for i in range(R):
+            qp.qgemv(fmt, P[i], None, N_ROWS, K_COLS, X[i], Y[i], stream=s)
+
+    with torch.cuda.stream(s):
+        step()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    torch.cuda.synchronize(dev)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(s)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    clk = clocks.stop()
+    t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+    if pg:
+        tt = torch.tensor([t_step], device=dev, dtype=torch.float64)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        t_step = float(tt.item())
+    value = world * R * wbytes / t_step / 1e9
+    per_launch = t_step / R
+    achieved = wbytes / per_launch / 1e9
+    faults = qp.qpack_fetch_fault_flags()
+
+    # ---- end to end through the C ABI with host buffers: H2D of the step's activations, D2H of its outputs ----
+    Xh = torch.empty((R, K_COLS), dtype=torch.float16, pin_memory=True)
+    Xh.copy_(X.cpu())
+    Yh = torch.empty((R, N_ROWS), dtype=torch.float32, pin_memory=True)
+
+    def e2e_step():
+        X.copy_(Xh, non_blocking=True)
+        step()
+        Yh.copy_(Y, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(s)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(s)
+    torch.cuda.synchronize(dev)
+    t_e2e = f0.elapsed_time(f1) / 1e3 / args.steps
+    if pg:
+        tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    e2e = {"value": world * R * wbytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(Xh.nbytes),
+           "d2h_bytes_per_step": int(Yh.nbytes)}
+
+    cpu = None
+    extra = None
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            pk = P[0].cpu().numpy()
+            cpu = cpu_oracle_gemv_sample(pk, X[0].cpu().numpy().view(np.uint16))
+        if not args.no_extra:
+            del P, X, Y
+            torch.cuda.empty_cache()
+            extra = {"decode_7b": decode_7b_extra(qp, torch, synth, dev)}
+
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["csrc_digest"] == csrc_digest() else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "3-bit super-block fused dequant-GEMV, W 11008x4096 (Laplace(0,0.015), seed 0), "
+                               "batch-1 fp16 x, fp32 y",
+                   "format": "Q3S (110 B / 256 weights)", "N": N_ROWS, "K": K_COLS, "batch": 1,
+                   "copies_per_step": R, "bytes_per_gemv": wbytes,
+                   "l2": f"inputs larger than L2: {R} distinct packed copies ({R * wbytes / 1e9:.2f} GB) per step",
+                   "parallelism": "one GPU per rank; row shards need no exchange (weak-scaling replicas)"},
+        "pct_hbm_peak": value / world / hbm_peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic, "peak_source": peak_src,
+                     "kernel": "gemv1_kernel<Q3S>", "algorithmic_bytes_per_launch": wbytes},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * R,
+        "clocks": clk,
+        "faults": faults,
+    }
+    if extra:
+        line["extra"] = extra
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def run_ncu_case(args):
+    """A short run sized for an ncu capture (a few launches, a few hundred MB on the device): quantize one
+    matrix, replicate it `copies` times (> L2 in total) and run the product on each copy."""
+    import torch
+    from bit_weight_quantized_qpack_gb300 import _build
+    _build.build()
+    import bit_weight_quantized_qpack_gb300 as qp
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qp.FORMATS[args.fmt]
+    N, K = args.N, args.K
+    dev = torch.device("cuda", 0)
+    W = synth.laplace((N, K), 0.02, seed=1, device=dev)
+    p0, g0 = qp.qpack_quantize_pack(fmt, W)
+    del W
+    copies = args.copies or 8
+    ps = [p0.clone() for _ in range(copies)]
+    gs = [None if g0 is None else g0.clone() for _ in range(copies)]
+    if args.ncu_case == "gemv":
+        x = synth.normal((K,), 1.0, seed=2, device=dev, dtype=torch.float16)
+        y = torch.empty(N, device=dev)
+        for i in range(copies):
+            qp.qgemv(fmt, ps[i], gs[i], N, K, x, y)
+    elif args.ncu_case == "small":
+        X = synth.normal((args.M, K), 1.0, seed=2, device=dev, dtype=torch.float16)
+        Y = torch.empty((args.M, N), device=dev)
+        for i in range(copies):
+            qp.qgemm_small(fmt, ps[i], gs[i], N, K, X, Y)
+    else:
+        X = synth.normal((args.M, K), 1.0, seed=2, device=dev, dtype=torch.bfloat16)
+        Y = torch.empty((args.M, N), device=dev, dtype=torch.bfloat16)
+        for i in range(copies):
+            qp.qgemm_prefill(fmt, ps[i], gs[i], N, K, X, Y)
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_case": args.ncu_case, "fmt": args.fmt, "N": N, "K": K, "copies": copies,
+                      "faults": qp.qpack_fetch_fault_flags()}))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--copies", type=int, default=0, help="distinct weight copies per step (default: >= 8x L2)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the 7B decode-step extra")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", choices=["gemv", "small", "prefill"], default=None,
+                    help="short run of one product for an ncu capture (see profiles/)")
+    ap.add_argument("--fmt", default="Q3S")
+    ap.add_argument("--N", type=int, default=N_ROWS)
+    ap.add_argument("--K", type=int, default=K_COLS)
+    ap.add_argument("--M", type=int, default=8)
+    args = ap.parse_args()
+    if args.ncu_case:
+        return run_ncu_case(args)
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

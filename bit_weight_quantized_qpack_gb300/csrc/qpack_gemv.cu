@@ -4,16 +4,25 @@
 // (2/3/5/6-bit article, lpnh.cn/news/2857666, §1.2: time per token = weight bytes / bandwidth; DBHOO-CIM
 // article, pwwt.cn/news/4452170, §3.3: dequantization must stay fused, never materialised).
 //
-// Structure (one CTA per SM, persistent):
-//   warp 8      producer: streams (4-row tile x 4096-weight chunk) segments of the packed rows into a ring of
-//               shared-memory stages with 1-D bulk copies (cp.async.bulk, completion on an mbarrier), evict-first
-//               in L2 because each byte is used once.
-//   warps 0..7  consumers: warp pair p owns row p of the tile; each lane unpacks two 32-weight units per stage.
+// Batch-1 kernel (gemv1_kernel), one persistent CTA per SM:
+//   warp 16      producer: streams (4-row tile x 4096-weight chunk) segments of the packed rows into a ring of
+//                shared-memory stages with 1-D bulk copies (cp.async.bulk, completion on an mbarrier), L2
+//                evict-first because each byte is used once.
+//   warps 0..15  two consumer groups of 8 warps; group g consumes the stages whose item index has parity g. In
+//                a group, lane l of warp w owns the 32-weight unit uc = (32w + l) mod 128 of the rows
+//                (32w + l) div 128 and that + 2, so its activations are loaded once for two rows.
 // Unpacking (2/3/5/6-bit article §3.3: separate unpack from multiply-add, factor s*(q.x) + m*sum(x)): codes are
 // OR-ed into the mantissa of an fp16 1024.0 with one LOP3 per pair of weights, so a half holds 1024 + u*2^p
-// exactly; an fp32 FMA with fp16 inputs (exact product) accumulates (1024 + u*2^p)*x per bit-position class p,
-// and the constant 1024*sum(x) terms, the symmetric code offsets and the asymmetric minima are removed per
-// sub-block with activation sums that each CTA precomputes once from x into shared memory.
+// exactly, p being the code's bit position inside its 16-bit half. The activations are staged in shared memory
+// pre-scaled by 2^-p of the code they meet (x' = fp16(x * 2^-p), exact unless subnormal), so one fp32 FMA with
+// fp16 inputs (exact product) per weight accumulates 1024*x' + u*x for every class into one accumulator. The
+// 1024*sum(x') terms, the symmetric code offsets and the asymmetric minima are removed per sub-block with
+// activation sums that each CTA precomputes once. Per-row results are combined without a block barrier: each
+// warp reduces its two rows, publishes the partials and bumps a per-tile counter; the warp completing the count
+// sums the partials in a fixed order (deterministic) and writes y.
+//
+// Small-batch kernel (stream_kernel, M = 2..16): same producer; each unit is dequantized exactly to fp32
+// registers and multiplied against the M activation rows.
 #include <cuda_runtime.h>
 
 #include "qpack_dev.cuh"
@@ -25,49 +34,24 @@ __device__ int g_fault_gemv = 0;
 
 namespace {
 
-constexpr int NCW = 8;                   // consumer warps
-constexpr int NTHREADS = (NCW + 1) * 32; // + producer warp
-constexpr int TILE_R = 4;                // rows per tile (one warp pair per row)
-constexpr int CHW = 4096;                // weights per chunk
+constexpr int TILE_R = 4;                // rows per tile
+constexpr int CHW = 4096;                // weights per chunk (stage width)
 constexpr int UPC = CHW / 32;            // 32-weight units per chunk
 constexpr uint32_t MAGIC2 = 0x64006400u; // fp16 1024.0 in both halves
-constexpr int SMEM_BUDGET = 220 * 1024;
+constexpr uint32_t MAGICF = 0x4B000000u; // fp32 2^23
 
 template <int F> struct Geo {
     // bytes of one row's chunk in shared memory (codes; Q4G32 scales are a separate region)
     static constexpr int chunk_bytes = Fmt<F>::sb ? (CHW / 256) * Fmt<F>::bytes : CHW / 2;
     static constexpr int scale_bytes = Fmt<F>::sb ? 0 : (CHW / 32) * 4;
     static constexpr int stage_bytes = TILE_R * (chunk_bytes + scale_bytes);
-    // activation-derived constants per 32-weight unit
-    static constexpr int consts_per_unit = (F == FMT_Q4G32) ? 1 : (F == FMT_Q2S) ? 4 : (F == FMT_Q3S) ? 2 : (F == FMT_Q5S) ? 2 : 2;
 };
-
-__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 __device__ __forceinline__ uint16_t lo16(uint32_t v) { return uint16_t(v & 0xFFFFu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t v) { return uint16_t(v >> 16); }
-
-// Accumulate a half2 of magic-coded weights against two activation halves.
-__device__ __forceinline__ float fma2h(uint32_t codes, uint16_t xa, uint16_t xb, float acc) {
-    acc = fma_h(lo16(codes), xa, acc);
-    return fma_h(hi16(codes), xb, acc);
-}
-
-// x halves of a unit: xv[t] holds x[2t], x[2t+1].
-__device__ __forceinline__ uint16_t xh(const uint32_t *xv, int i) {
-    return (i & 1) ? hi16(xv[i >> 1]) : lo16(xv[i >> 1]);
-}
-
-__device__ __forceinline__ void load_x_unit(const uint16_t *xs, int64_t k0, uint32_t xv[16]) {
-    const uint4 *p = reinterpret_cast<const uint4 *>(xs + k0);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        uint4 v = p[t];
-        xv[4 * t] = v.x; xv[4 * t + 1] = v.y; xv[4 * t + 2] = v.z; xv[4 * t + 3] = v.w;
-    }
-}
-
 __device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+__device__ __forceinline__ float hbits(const uint8_t *p) { return h2f_bits(*reinterpret_cast<const uint16_t *>(p)); }
+__device__ __forceinline__ float small_int_f(uint32_t bits_or_magic) { return __uint_as_float(bits_or_magic) - 8388608.0f; }
 
 // Read `n` consecutive 32-bit words starting at a 2-byte aligned shared-memory address.
 template <int n>
@@ -82,226 +66,509 @@ __device__ __forceinline__ void lds_words_a2(const uint8_t *p, uint32_t *w) {
     for (int i = 0; i < n; ++i) w[i] = __funnelshift_r(r[i], r[i + 1], sh);
 }
 
-// INT4-style nibble word: 8 weights, nibble k at bits 4k. Accumulates class p=0 (even k) and p=4 (odd k).
-// `hb` (optional) holds high bits already positioned for the four pairs (see callers).
-__device__ __forceinline__ void nib_word(uint32_t c, const uint32_t *xv, int i0, float &a0, float &a4) {
-    const uint32_t c2 = c >> 8;
-    a0 = fma2h(lop3_and_or(c, 0x000F000Fu, MAGIC2), xh(xv, i0 + 0), xh(xv, i0 + 4), a0);
-    a4 = fma2h(lop3_and_or(c, 0x00F000F0u, MAGIC2), xh(xv, i0 + 1), xh(xv, i0 + 5), a4);
-    a0 = fma2h(lop3_and_or(c2, 0x000F000Fu, MAGIC2), xh(xv, i0 + 2), xh(xv, i0 + 6), a0);
-    a4 = fma2h(lop3_and_or(c2, 0x00F000F0u, MAGIC2), xh(xv, i0 + 3), xh(xv, i0 + 7), a4);
+// acc += lo(codes) * xa + hi(codes) * xb with exact products (fp16 x fp16 -> fp32 FMA).
+__device__ __forceinline__ float fma2h(uint32_t codes, uint16_t xa, uint16_t xb, float acc) {
+    acc = fma_h(lo16(codes), xa, acc);
+    return fma_h(hi16(codes), xb, acc);
 }
+// x halves of a unit: xv[t] holds x'[2t], x'[2t+1].
+__device__ __forceinline__ uint16_t xh(const uint32_t *xv, int i) { return (i & 1) ? hi16(xv[i >> 1]) : lo16(xv[i >> 1]); }
 
-// Nibble word with extra high bits merged above each nibble. X holds, for the pairs (0,4),(1,5),(2,6),(3,7),
-// the high bits already shifted so that (X << s_k) & mask_k lands them just above the pair's nibbles.
-template <int HB>   // 1 (5-bit) or 2 (6-bit) high bits
-__device__ __forceinline__ void nib_word_hi(uint32_t c, uint32_t X, const uint32_t *xv, int i0, float &a0, float &a4) {
-    constexpr uint32_t mlo = (HB == 1) ? 0x00100010u : 0x00300030u;   // bits 4(+5) of each half
-    constexpr uint32_t mhi = (HB == 1) ? 0x01000100u : 0x03000300u;   // bits 8(+9) of each half
-    // shifts that bring pair k's high bits of X to the target positions
-    constexpr int s0 = (HB == 1) ? 4 : 4, s1 = (HB == 1) ? 7 : 6, s2 = (HB == 1) ? 2 : 0, s3 = (HB == 1) ? 5 : 2;
+// ------------------------------------------------------------------------------------------------------------
+// Unpack + multiply helpers. Two accumulators (a, b) only for instruction-level parallelism.
+// ------------------------------------------------------------------------------------------------------------
+// 8 nibbles, nibble k at bits 4k (weights i0 + k). Bit classes: even k at p = 0, odd k at p = 4.
+__device__ __forceinline__ void nib_word(uint32_t c, const uint32_t *xv, int i0, float &a, float &b) {
     const uint32_t c2 = c >> 8;
-    uint32_t h;
-    h = lop3_and_or(c, 0x000F000Fu, MAGIC2);
-    h = lop3_and_or(X << s0, mlo, h);
-    a0 = fma2h(h, xh(xv, i0 + 0), xh(xv, i0 + 4), a0);
-    h = lop3_and_or(c, 0x00F000F0u, MAGIC2);
-    h = lop3_and_or(X << s1, mhi, h);
-    a4 = fma2h(h, xh(xv, i0 + 1), xh(xv, i0 + 5), a4);
-    h = lop3_and_or(c2, 0x000F000Fu, MAGIC2);
-    h = lop3_and_or(X << s2, mlo, h);
-    a0 = fma2h(h, xh(xv, i0 + 2), xh(xv, i0 + 6), a0);
-    h = lop3_and_or(c2, 0x00F000F0u, MAGIC2);
-    h = lop3_and_or(X << s3, mhi, h);
-    a4 = fma2h(h, xh(xv, i0 + 3), xh(xv, i0 + 7), a4);
+    a = fma2h(lop3_and_or(c, 0x000F000Fu, MAGIC2), xh(xv, i0 + 0), xh(xv, i0 + 4), a);
+    b = fma2h(lop3_and_or(c, 0x00F000F0u, MAGIC2), xh(xv, i0 + 1), xh(xv, i0 + 5), b);
+    a = fma2h(lop3_and_or(c2, 0x000F000Fu, MAGIC2), xh(xv, i0 + 2), xh(xv, i0 + 6), a);
+    b = fma2h(lop3_and_or(c2, 0x00F000F0u, MAGIC2), xh(xv, i0 + 3), xh(xv, i0 + 7), b);
 }
-
-// 2-bit word: 16 weights, weight 4b+k at bits 8b+2k. Classes p = 2k (k = 0..3).
-__device__ __forceinline__ void crumb_word(uint32_t c, const uint32_t *xv, int i0, float a[4]) {
+// Nibble word with HB extra high bits merged just above each nibble. X holds the high bits of weights
+// i0..i0+3 at bits HB*k (k = 0..3) and of weights i0+4..i0+7 at bits 16 + HB*k; (X << s_k) & mask lands pair
+// k's high bits right above its nibbles.
+template <int HB>
+__device__ __forceinline__ void nib_word_hi(uint32_t c, uint32_t X, const uint32_t *xv, int i0, float &a, float &b) {
+    constexpr uint32_t mlo = (HB == 1) ? 0x00100010u : 0x00300030u;
+    constexpr uint32_t mhi = (HB == 1) ? 0x01000100u : 0x03000300u;
+    constexpr int s0 = 4, s1 = (HB == 1) ? 7 : 6, s2 = (HB == 1) ? 2 : 0, s3 = (HB == 1) ? 5 : 2;
+    const uint32_t c2 = c >> 8;
+    a = fma2h(lop3_and_or(X << s0, mlo, lop3_and_or(c, 0x000F000Fu, MAGIC2)), xh(xv, i0 + 0), xh(xv, i0 + 4), a);
+    b = fma2h(lop3_and_or(X << s1, mhi, lop3_and_or(c, 0x00F000F0u, MAGIC2)), xh(xv, i0 + 1), xh(xv, i0 + 5), b);
+    a = fma2h(lop3_and_or(X << s2, mlo, lop3_and_or(c2, 0x000F000Fu, MAGIC2)), xh(xv, i0 + 2), xh(xv, i0 + 6), a);
+    b = fma2h(lop3_and_or(X << s3, mhi, lop3_and_or(c2, 0x00F000F0u, MAGIC2)), xh(xv, i0 + 3), xh(xv, i0 + 7), b);
+}
+// 16 two-bit codes, weight 4b + k at bits 8b + 2k (weights i0 + ...). Bit class p = 2k.
+__device__ __forceinline__ void crumb_word(uint32_t c, const uint32_t *xv, int i0, float &a, float &b) {
     const uint32_t c2 = c >> 8;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const uint32_t m = (3u << (2 * k)) * 0x00010001u;
-        a[k] = fma2h(lop3_and_or(c, m, MAGIC2), xh(xv, i0 + k), xh(xv, i0 + 8 + k), a[k]);
-        a[k] = fma2h(lop3_and_or(c2, m, MAGIC2), xh(xv, i0 + 4 + k), xh(xv, i0 + 12 + k), a[k]);
+        a = fma2h(lop3_and_or(c, m, MAGIC2), xh(xv, i0 + k), xh(xv, i0 + 8 + k), a);
+        b = fma2h(lop3_and_or(c2, m, MAGIC2), xh(xv, i0 + 4 + k), xh(xv, i0 + 12 + k), b);
     }
 }
-
-// 3-bit group: 24-bit value v (bits above 23 ignored), code t at bits 3t, weights i0..i0+7.
-// Classes: p=0 {0,3,4,7}, p=3 {1,5}, p=6 {2,6}.
-__device__ __forceinline__ void tri_group(uint32_t v, const uint32_t *xv, int i0, float &a0, float &a3, float &a6) {
+// One 24-bit group v (bits above 23 ignored), code t at bits 3t, weights i0..i0+7.
+// Bit classes: t in {0,3,4,7} at p = 0, {1,5} at p = 3, {2,6} at p = 6.
+__device__ __forceinline__ void tri_group(uint32_t v, const uint32_t *xv, int i0, float &a, float &b) {
     const uint32_t Y = lop3_sel(v, v << 4, 0x00000FFFu);   // codes 0..3 in the low half, 4..7 in the high half
     const uint32_t Y9 = Y >> 9;
-    a0 = fma2h(lop3_and_or(Y, 0x00070007u, MAGIC2), xh(xv, i0 + 0), xh(xv, i0 + 4), a0);
-    a3 = fma2h(lop3_and_or(Y, 0x00380038u, MAGIC2), xh(xv, i0 + 1), xh(xv, i0 + 5), a3);
-    a6 = fma2h(lop3_and_or(Y, 0x01C001C0u, MAGIC2), xh(xv, i0 + 2), xh(xv, i0 + 6), a6);
-    a0 = fma2h(lop3_and_or(Y9, 0x00070007u, MAGIC2), xh(xv, i0 + 3), xh(xv, i0 + 7), a0);
+    a = fma2h(lop3_and_or(Y, 0x00070007u, MAGIC2), xh(xv, i0 + 0), xh(xv, i0 + 4), a);
+    b = fma2h(lop3_and_or(Y, 0x00380038u, MAGIC2), xh(xv, i0 + 1), xh(xv, i0 + 5), b);
+    a = fma2h(lop3_and_or(Y, 0x01C001C0u, MAGIC2), xh(xv, i0 + 2), xh(xv, i0 + 6), a);
+    b = fma2h(lop3_and_or(Y9, 0x00070007u, MAGIC2), xh(xv, i0 + 3), xh(xv, i0 + 7), b);
 }
 
-__device__ __forceinline__ float hbits(const uint8_t *p) { return h2f_bits(*reinterpret_cast<const uint16_t *>(p)); }
+// 2^e for a small integer e, exactly (e is a compile-time constant where it is used).
+__host__ __device__ constexpr float pow2f(int e) { return e >= 0 ? float(1u << e) : 1.0f / float(1u << (-e)); }
 
-// ------------------------------------------------------------------------------------------------------------
-// Batch-1 unit dot products. `row` = the row's chunk in shared memory (codes), `uc` = unit within the chunk,
-// `cst` = activation constants of this unit, `xv` = the unit's 32 activations. Returns sum_i w'_i * x_i.
-// ------------------------------------------------------------------------------------------------------------
-template <int F> struct Unit1;
+// Bit-class shift p of element i (0..31) of a unit: the activation it meets is staged as x * 2^-p.
+template <int F>
+__host__ __device__ constexpr int xshift(int i) {
+    if constexpr (F == FMT_Q2S) return 2 * (i & 3);
+    else if constexpr (F == FMT_Q3S) {
+        const int t = i & 7;
+        return (t == 1 || t == 5) ? 3 : ((t == 2 || t == 6) ? 6 : 0);
+    } else return (i & 1) ? 4 : 0;
+}
 
-template <> struct Unit1<FMT_Q4G32> {
-    // constants: C = 1032*S_even + 72*S_odd
-    static __device__ __forceinline__ float dot(const uint8_t *row, const float *scl, int uc, const float *cst,
-                                                const uint32_t *xv) {
-        const uint4 c = *reinterpret_cast<const uint4 *>(row + 16 * uc);
-        float a0 = 0.f, a4 = 0.f;
-        nib_word(c.x, xv, 0, a0, a4);
-        nib_word(c.y, xv, 8, a0, a4);
-        nib_word(c.z, xv, 16, a0, a4);
-        nib_word(c.w, xv, 24, a0, a4);
-        return scl[uc] * (fmaf(a4, 0.0625f, a0) - cst[0]);
+// Activation constants per unit (XC<F>::n floats), from the staged x' (see the file comment).
+template <int F> struct XC;
+template <> struct XC<FMT_Q4G32> { static constexpr int n = 1; };   // C
+template <> struct XC<FMT_Q2S> { static constexpr int n = 4; };     // C0, S0, C1, S1 (two sub-blocks)
+template <> struct XC<FMT_Q3S> { static constexpr int n = 2; };     // C0, C1
+template <> struct XC<FMT_Q5S> { static constexpr int n = 2; };     // C, S
+template <> struct XC<FMT_Q6S> { static constexpr int n = 2; };     // C0, C1
+
+template <int F>
+__device__ __forceinline__ void unit_consts(const float xp[32], const float xt[32], float *out) {
+    // xp = staged x' (as fp32), xt = 2^p * x' (the activation the integer code effectively multiplies)
+    float sp[2] = {0.f, 0.f}, st[2] = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) { sp[i >> 4] += xp[i]; st[i >> 4] += xt[i]; }
+    if constexpr (F == FMT_Q4G32) {
+        out[0] = 1024.0f * (sp[0] + sp[1]) + 8.0f * (st[0] + st[1]);
+    } else if constexpr (F == FMT_Q2S) {
+        out[0] = 1024.0f * sp[0]; out[1] = st[0];
+        out[2] = 1024.0f * sp[1]; out[3] = st[1];
+    } else if constexpr (F == FMT_Q3S) {
+        out[0] = 1024.0f * sp[0] + 4.0f * st[0];
+        out[1] = 1024.0f * sp[1] + 4.0f * st[1];
+    } else if constexpr (F == FMT_Q5S) {
+        out[0] = 1024.0f * (sp[0] + sp[1]);
+        out[1] = st[0] + st[1];
+    } else {
+        out[0] = 1024.0f * sp[0] + 32.0f * st[0];
+        out[1] = 1024.0f * sp[1] + 32.0f * st[1];
     }
-    static __device__ __forceinline__ void consts(const uint16_t *xs, int64_t u, float *out) {
-        float se = 0.f, so = 0.f;
-        for (int i = 0; i < 32; i += 2) { se += h2f_bits(xs[32 * u + i]); so += h2f_bits(xs[32 * u + i + 1]); }
-        out[0] = 1032.0f * se + 72.0f * so;
+}
+
+// ------------------------------------------------------------------------------------------------------------
+// Per-lane geometry of one unit position (uc) within a 4096-weight chunk: byte offsets relative to the unit's
+// aligned code base, so that both rows of a lane use immediate offsets.
+// ------------------------------------------------------------------------------------------------------------
+struct LaneGeo {
+    uint32_t ubase;      // aligned byte offset of the unit's codes within a row chunk
+    int32_t o1, o2, o3;  // format-specific byte offsets relative to ubase
+    uint32_t sh0, sh1;   // format-specific shifts
+};
+
+template <int F>
+__device__ __forceinline__ LaneGeo lane_geo(int uc) {
+    LaneGeo g = {0u, 0, 0, 0, 0u, 0u};
+    const uint32_t sbk = uint32_t(uc) >> 3, su = uint32_t(uc) & 7u;
+    if constexpr (F == FMT_Q4G32) {
+        g.ubase = 16u * uc;
+    } else if constexpr (F == FMT_Q2S) {
+        g.ubase = 84u * sbk + 8u * su;
+        g.o1 = int32_t(64u + 2u * su) - int32_t(8u * su);     // L|M bytes of the two sub-blocks
+        g.o2 = int32_t(80u) - int32_t(8u * su);               // d, dmin
+    } else if constexpr (F == FMT_Q3S) {
+        const uint32_t a = 110u * sbk + 12u * su;             // 2-byte aligned code start
+        g.ubase = a & ~3u;
+        g.sh0 = (a & 3u) * 8u;                                // 0 or 16
+        const uint32_t fa = 110u * sbk + 96u + 3u * (su >> 1);
+        uint32_t fw = fa & ~3u, fs = 8u * (fa & 3u) + 6u * ((2u * su) & 3u);
+        if (fs >= 32u) { fw += 4u; fs -= 32u; }
+        g.o1 = int32_t(fw) - int32_t(g.ubase);                // word pair holding L_j0, L_j0+1 at bits fs..
+        g.sh1 = fs;
+        g.o2 = int32_t(110u * sbk + 108u) - int32_t(g.ubase); // d
+    } else if constexpr (F == FMT_Q5S) {
+        g.ubase = 176u * sbk + 16u * su;
+        g.o1 = int32_t(128u + 4u * su) - int32_t(16u * su);   // high-bit plane word
+        g.o2 = int32_t(160u) - int32_t(16u * su);             // 16 six-bit fields + d + dmin (16-byte aligned)
+        g.sh0 = 6u * su;                                      // bit of L_su in the field run
+        g.sh1 = 48u + 6u * su;                                // bit of M_su
+    } else {
+        const uint32_t a = 210u * sbk + 16u * su;
+        g.ubase = a & ~3u;
+        g.sh0 = (a & 3u) * 8u;
+        g.o1 = int32_t(((210u * sbk + 128u + 8u * su) & ~3u)) - int32_t(g.ubase);   // high-2 plane (same alignment)
+        g.o2 = int32_t(210u * sbk + 192u + 2u * su) - int32_t(g.ubase);            // two int8 sub-scales
+        g.o3 = int32_t(210u * sbk + 208u) - int32_t(g.ubase);                      // d
+    }
+    return g;
+}
+
+// sum_i w'_i x_i over one 32-weight unit of one row; `u` = aligned unit base in shared memory, `sp` = this
+// row's group-scale pointer (Q4G32), `c` = the unit's activation constants, `xv` = its staged activations.
+template <int F>
+__device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, const LaneGeo &g, const float *c,
+                                         const uint32_t *xv) {
+    if constexpr (F == FMT_Q4G32) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(u);
+        float a = 0.f, b = 0.f;
+        nib_word(w.x, xv, 0, a, b);
+        nib_word(w.y, xv, 8, a, b);
+        nib_word(w.z, xv, 16, a, b);
+        nib_word(w.w, xv, 24, a, b);
+        return sp[0] * ((a + b) - c[0]);
+    } else if constexpr (F == FMT_Q2S) {
+        const uint32_t w0 = lds32(u), w1 = lds32(u + 4);
+        const uint32_t dd = lds32(u + g.o2);
+        const float2 Dd = __half22float2(*reinterpret_cast<const __half2 *>(&dd));
+        const uint32_t lm = *reinterpret_cast<const uint16_t *>(u + g.o1);
+        const float L0 = small_int_f(lop3_and_or(lm, 0xFu, MAGICF));
+        const float M0 = small_int_f(lop3_and_or(lm >> 4, 0xFu, MAGICF));
+        const float L1 = small_int_f(lop3_and_or(lm >> 8, 0xFu, MAGICF));
+        const float M1 = small_int_f(lop3_and_or(lm >> 12, 0xFu, MAGICF));
+        float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+        crumb_word(w0, xv, 0, a0, b0);
+        crumb_word(w1, xv, 16, a1, b1);
+        float r = (Dd.x * L0) * ((a0 + b0) - c[0]);
+        r = fmaf(Dd.x * L1, (a1 + b1) - c[2], r);
+        r = fmaf(-(Dd.y * M0), c[1], r);
+        return fmaf(-(Dd.y * M1), c[3], r);
+    } else if constexpr (F == FMT_Q3S) {
+        const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
+        const uint32_t r0 = wp[0], r1 = wp[1], r2 = wp[2], r3 = wp[3];
+        const uint32_t s0 = __funnelshift_r(r0, r1, g.sh0), s1 = __funnelshift_r(r1, r2, g.sh0),
+                       s2 = __funnelshift_r(r2, r3, g.sh0);
+        const uint32_t *fp = reinterpret_cast<const uint32_t *>(u + g.o1);
+        const uint32_t f = __funnelshift_r(fp[0], fp[1], g.sh1);
+        const float L0 = small_int_f(lop3_and_or(f, 63u, MAGICF));
+        const float L1 = small_int_f(lop3_and_or(f >> 6, 63u, MAGICF));
+        const float D = hbits(u + g.o2);
+        float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+        tri_group(s0, xv, 0, a0, b0);
+        tri_group(__funnelshift_r(s0, s1, 24), xv, 8, a0, b0);
+        tri_group(__funnelshift_r(s1, s2, 16), xv, 16, a1, b1);
+        tri_group(s2 >> 8, xv, 24, a1, b1);
+        return fmaf(D * L1, (a1 + b1) - c[1], (D * L0) * ((a0 + b0) - c[0]));
+    } else if constexpr (F == FMT_Q5S) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(u);
+        const uint32_t H = lds32(u + g.o1);
+        const uint4 fld = *reinterpret_cast<const uint4 *>(u + g.o2);
+        const float2 Dd = __half22float2(*reinterpret_cast<const __half2 *>(&fld.w));
+        const uint64_t lo64 = (uint64_t(fld.y) << 32) | fld.x, hi64 = (uint64_t(fld.z) << 32) | fld.y;
+        const float L = small_int_f(lop3_and_or(uint32_t(lo64 >> g.sh0), 63u, MAGICF));
+        const float M = small_int_f(lop3_and_or(uint32_t(hi64 >> (g.sh1 - 32u)), 63u, MAGICF));
+        float a = 0.f, b = 0.f;
+        nib_word_hi<1>(w.x, lop3_sel(H, H << 12, 0x0000FFFFu), xv, 0, a, b);
+        nib_word_hi<1>(w.y, lop3_sel(H >> 8, H << 4, 0x0000FFFFu), xv, 8, a, b);
+        nib_word_hi<1>(w.z, lop3_sel(H >> 16, H >> 4, 0x0000FFFFu), xv, 16, a, b);
+        nib_word_hi<1>(w.w, lop3_sel(H >> 24, H >> 12, 0x0000FFFFu), xv, 24, a, b);
+        return fmaf(Dd.x * L, (a + b) - c[0], -(Dd.y * M) * c[1]);
+    } else {
+        const uint32_t sh = g.sh0;
+        const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
+        const uint32_t r0 = wp[0], r1 = wp[1], r2 = wp[2], r3 = wp[3], r4 = wp[4];
+        const uint32_t *hp = reinterpret_cast<const uint32_t *>(u + g.o1);
+        const uint32_t q0 = hp[0], q1 = hp[1], q2 = hp[2];
+        const uint32_t h0 = __funnelshift_r(q0, q1, sh), h1 = __funnelshift_r(q1, q2, sh);
+        const uint32_t lv = *reinterpret_cast<const uint16_t *>(u + g.o2);
+        // int8 -> float exactly: (b ^ 0x80) | 2^23 as fp32, minus 2^23 + 128
+        const float L0 = __uint_as_float((lv & 0xFFu) ^ (MAGICF | 0x80u)) - 8388736.0f;
+        const float L1 = __uint_as_float(((lv >> 8) & 0xFFu) ^ (MAGICF | 0x80u)) - 8388736.0f;
+        const float D = hbits(u + g.o3);
+        float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+        nib_word_hi<2>(__funnelshift_r(r0, r1, sh), __byte_perm(h0, 0u, 0x4140u), xv, 0, a0, b0);
+        nib_word_hi<2>(__funnelshift_r(r1, r2, sh), __byte_perm(h0, 0u, 0x4342u), xv, 8, a0, b0);
+        nib_word_hi<2>(__funnelshift_r(r2, r3, sh), __byte_perm(h1, 0u, 0x4140u), xv, 16, a1, b1);
+        nib_word_hi<2>(__funnelshift_r(r3, r4, sh), __byte_perm(h1, 0u, 0x4342u), xv, 24, a1, b1);
+        return fmaf(D * L1, (a1 + b1) - c[1], (D * L0) * ((a0 + b0) - c[0]));
+    }
+}
+
+// Staged activations: unit u's 32 halves are four 16-byte vectors stored at vector index t * U + u (t = 0..3,
+// U = units per row), so that consecutive lanes (consecutive units) read consecutive 16-byte vectors.
+__device__ __forceinline__ void load_xp(const uint16_t *xs, uint32_t U, uint32_t u, uint32_t xv[16]) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(xs);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint4 v = p[t * U + u];
+        xv[4 * t] = v.x; xv[4 * t + 1] = v.y; xv[4 * t + 2] = v.z; xv[4 * t + 3] = v.w;
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------------------------------
+// Batch-1 fused dequant-GEMV kernel.
+// ------------------------------------------------------------------------------------------------------------
+constexpr int G1_CW = 16;
+constexpr int G1_THREADS = (G1_CW + 1) * 32;
+
+template <int F, int NS>
+struct G1Layout {
+    static constexpr int NSLOT = NS + 2;
+    static __host__ __device__ uint32_t bar_bytes() { return uint32_t(round_up(16 * NS, 128)); }
+    static __host__ __device__ uint32_t red_bytes() { return uint32_t(round_up(NSLOT * 4 + NSLOT * G1_CW * 2 * 4, 128)); }
+    static __host__ __device__ uint32_t x_bytes(uint32_t K) { return uint32_t(round_up(2 * int64_t(K), 128)); }
+    static __host__ __device__ uint32_t c_bytes(uint32_t K) { return uint32_t(round_up(4 * int64_t(K / 32) * XC<F>::n, 128)); }
+    static __host__ __device__ uint32_t total(uint32_t K) {
+        return bar_bytes() + red_bytes() + x_bytes(K) + c_bytes(K) + uint32_t(NS) * Geo<F>::stage_bytes + 32;
     }
 };
 
-template <> struct Unit1<FMT_Q2S> {
-    // constants per sub-block j (16 weights): C_j = 1024 * sum_k 4^-k S_{j,k}, S_j
-    static __device__ __forceinline__ float dot(const uint8_t *row, const float *, int uc, const float *cst,
-                                                const uint32_t *xv) {
-        const int sbk = uc >> 3, su = uc & 7;
-        const uint8_t *blk = row + sbk * 84;
-        const uint32_t w0 = lds32(blk + 8 * su), w1 = lds32(blk + 8 * su + 4);
-        const float D = hbits(blk + 80), Dm = hbits(blk + 82);
-        const uint32_t lm = *reinterpret_cast<const uint16_t *>(blk + 64 + 2 * su);
-        float r = 0.f;
-        {
-            float a[4] = {0.f, 0.f, 0.f, 0.f};
-            crumb_word(w0, xv, 0, a);
-            const float t = fmaf(a[3], 0.015625f, fmaf(a[2], 0.0625f, fmaf(a[1], 0.25f, a[0]))) - cst[0];
-            r = fmaf(D * float(lm & 15u), t, r);
-            r = fmaf(-Dm * float((lm >> 4) & 15u), cst[1], r);
-        }
-        {
-            float a[4] = {0.f, 0.f, 0.f, 0.f};
-            crumb_word(w1, xv, 16, a);
-            const float t = fmaf(a[3], 0.015625f, fmaf(a[2], 0.0625f, fmaf(a[1], 0.25f, a[0]))) - cst[2];
-            r = fmaf(D * float((lm >> 8) & 15u), t, r);
-            r = fmaf(-Dm * float((lm >> 12) & 15u), cst[3], r);
-        }
-        return r;
-    }
-    static __device__ __forceinline__ void consts(const uint16_t *xs, int64_t u, float *out) {
-        for (int h = 0; h < 2; ++h) {
-            float S[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int i = 0; i < 16; ++i) S[i & 3] += h2f_bits(xs[32 * u + 16 * h + i]);
-            out[2 * h] = 1024.0f * (S[0] + 0.25f * S[1] + 0.0625f * S[2] + 0.015625f * S[3]);
-            out[2 * h + 1] = S[0] + S[1] + S[2] + S[3];
-        }
-    }
-};
+template <int F, int NS, bool FULLK>
+__global__ void __launch_bounds__(G1_THREADS, 1) gemv1_kernel(GemvArgs a) {
+    using G = Geo<F>;
+    using LY = G1Layout<F, NS>;
+    constexpr int NSLOT = LY::NSLOT;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t N = uint32_t(a.N), K = uint32_t(a.K);
+    const uint32_t ntiles = (N + TILE_R - 1) / TILE_R;
+    const uint32_t nch = (K + CHW - 1) / CHW;
+    const uint32_t U = K / 32;                        // units per row
 
-template <> struct Unit1<FMT_Q3S> {
-    // constants per sub-block j: C_j = 1024*(S0 + S3/8 + S6/64) + 4*(S0 + S3 + S6)
-    static __device__ __forceinline__ float dot(const uint8_t *row, const float *, int uc, const float *cst,
-                                                const uint32_t *xv) {
-        const int sbk = uc >> 3, su = uc & 7;
-        const uint8_t *blk = row + sbk * 110;
-        uint32_t s[3];
-        lds_words_a2<3>(blk + 12 * su, s);
-        const uint32_t v1 = __funnelshift_r(s[0], s[1], 24);
-        const uint32_t v2 = __funnelshift_r(s[1], s[2], 16);
-        const uint32_t v3 = s[2] >> 8;
-        const float D = hbits(blk + 108);
-        const uint8_t *fb = blk + 96 + 3 * (su >> 1);
-        const uint32_t f = uint32_t(fb[0]) | (uint32_t(fb[1]) << 8) | (uint32_t(fb[2]) << 16);
-        const int j0 = (2 * su) & 3;
-        const float L0 = float((f >> (6 * j0)) & 63u), L1 = float((f >> (6 * (j0 + 1))) & 63u);
-        float a0 = 0.f, a3 = 0.f, a6 = 0.f;
-        tri_group(s[0], xv, 0, a0, a3, a6);
-        tri_group(v1, xv, 8, a0, a3, a6);
-        float r = D * L0 * (fmaf(a6, 0.015625f, fmaf(a3, 0.125f, a0)) - cst[0]);
-        a0 = a3 = a6 = 0.f;
-        tri_group(v2, xv, 16, a0, a3, a6);
-        tri_group(v3, xv, 24, a0, a3, a6);
-        r = fmaf(D * L1, fmaf(a6, 0.015625f, fmaf(a3, 0.125f, a0)) - cst[1], r);
-        return r;
+    uint8_t *p = smem_raw;
+    uint64_t *full = reinterpret_cast<uint64_t *>(p);
+    uint64_t *empty = full + NS;
+    p += LY::bar_bytes();
+    int *cnt = reinterpret_cast<int *>(p);
+    float *red = reinterpret_cast<float *>(p + NSLOT * 4);
+    p += LY::red_bytes();
+    uint16_t *xs = reinterpret_cast<uint16_t *>(p);
+    p += LY::x_bytes(K);
+    float *cst = reinterpret_cast<float *>(p);
+    p += LY::c_bytes(K);
+    uint8_t *stages = p;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 8); }
+        for (int s = 0; s < NSLOT; ++s) cnt[s] = 0;
+        fence_mbar_init();
     }
-    static __device__ __forceinline__ void consts(const uint16_t *xs, int64_t u, float *out) {
-        for (int h = 0; h < 2; ++h) {
-            float S0 = 0.f, S3 = 0.f, S6 = 0.f;
-            for (int i = 0; i < 16; ++i) {
-                const float v = h2f_bits(xs[32 * u + 16 * h + i]);
-                const int t = i & 7;
-                if (t == 1 || t == 5) S3 += v; else if (t == 2 || t == 6) S6 += v; else S0 += v;
+    __syncthreads();
+
+    if (warp == G1_CW) {
+        // ------------------------------------ producer ------------------------------------
+        const uint64_t pol = l2_evict_first_policy();
+        uint32_t i = 0, s = 0, ph = 0;
+        for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            const uint32_t r0 = tile * TILE_R;
+            const uint32_t rows = min(uint32_t(TILE_R), N - r0);
+            for (uint32_t c = 0; c < nch; ++c) {
+                if (i >= uint32_t(NS)) {
+                    bool ok = true;
+                    if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1u);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    // A consumer stopped releasing stages: record it and stop producing; consumers then give up
+                    // on their next bounded wait, so nothing is left waiting.
+                    if (!ok) { if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_EMPTY); return; }
+                }
+                const uint32_t koff = c * CHW;
+                uint32_t cbytes, sbytes = 0;
+                if constexpr (Fmt<F>::sb) {
+                    const uint32_t off = (koff / 256) * Fmt<F>::bytes;
+                    cbytes = min(uint32_t(G::chunk_bytes), uint32_t(a.row_stride) - off);
+                } else {
+                    cbytes = min(uint32_t(G::chunk_bytes), (K - koff) / 2);
+                    sbytes = min(uint32_t(G::scale_bytes), (uint32_t(a.scale_stride) - koff / 32) * 4);
+                }
+                uint8_t *st = stages + s * uint32_t(G::stage_bytes);
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], rows * (cbytes + sbytes));
+                __syncwarp();
+                if (uint32_t(lane) < rows) {
+                    const uint8_t *src = a.packed + int64_t(r0 + lane) * a.row_stride +
+                                         (Fmt<F>::sb ? (koff / 256) * Fmt<F>::bytes : koff / 2);
+                    bulk_g2s(st + lane * G::chunk_bytes, src, cbytes, &full[s], pol);
+                } else if (!Fmt<F>::sb && lane >= 8 && uint32_t(lane - 8) < rows) {
+                    const uint8_t *src =
+                        reinterpret_cast<const uint8_t *>(a.gscale + int64_t(r0 + lane - 8) * a.scale_stride + koff / 32);
+                    bulk_g2s(st + TILE_R * G::chunk_bytes + (lane - 8) * G::scale_bytes, src, sbytes, &full[s], pol);
+                }
+                ++i;
+                if (++s == uint32_t(NS)) { s = 0; ph ^= 1u; }
             }
-            out[h] = 1024.0f * (S0 + 0.125f * S3 + 0.015625f * S6) + 4.0f * (S0 + S3 + S6);
+        }
+        return;
+    }
+
+    // -------------------------------------- consumers --------------------------------------
+    {
+        // stage x' = fp16(x * 2^-p) in the transposed vector layout, then the per-unit constants
+        const uint4 *xg = reinterpret_cast<const uint4 *>(a.X);
+        uint4 *xd = reinterpret_cast<uint4 *>(xs);
+        for (uint32_t v = tid; v < K / 8; v += G1_CW * 32) {
+            const uint4 raw = xg[v];
+            const uint32_t u = v >> 2, t = v & 3u;
+            uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                // element 8t + 2e (+1): the class depends only on the index mod 8
+                const float f0 = h2f_bits(lo16(w[e])) * pow2f(-xshift<F>(2 * e));
+                const float f1 = h2f_bits(hi16(w[e])) * pow2f(-xshift<F>(2 * e + 1));
+                w[e] = uint32_t(f2h_bits(f0)) | (uint32_t(f2h_bits(f1)) << 16);
+            }
+            xd[t * U + u] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        named_bar_sync(1, G1_CW * 32);
+        for (uint32_t u = tid; u < U; u += G1_CW * 32) {
+            uint32_t xv[16];
+            load_xp(xs, U, u, xv);
+            float xp[32], xt[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                xp[i] = h2f_bits(xh(xv, i));
+                xt[i] = xp[i] * pow2f(xshift<F>(i));
+            }
+            unit_consts<F>(xp, xt, cst + u * XC<F>::n);
+        }
+        named_bar_sync(1, G1_CW * 32);
+    }
+    const uint32_t group = uint32_t(warp) >> 3, wg = uint32_t(warp) & 7u;
+    const uint32_t gl = wg * 32u + uint32_t(lane);
+    const int uc = int(gl & 127u);
+    const uint32_t rlo = gl >> 7;                      // rows rlo and rlo + 2 of the tile
+    const LaneGeo geo = lane_geo<F>(uc);
+    const uint32_t uoff0 = rlo * uint32_t(G::chunk_bytes) + geo.ubase;            // row rlo; row rlo+2 is +2 chunks
+    const uint32_t soff0 = TILE_R * uint32_t(G::chunk_bytes) + rlo * uint32_t(G::scale_bytes) + 4u * uint32_t(uc);
+
+    // own items: i = group, group + 2, ... ; stage s = i mod NS (NS even -> stages of this group's parity)
+    uint32_t s = group, ph = 0;
+    uint32_t tile = blockIdx.x, c = group, ib = 0, slot = 0;   // ib = item index of the tile's first chunk
+    while (c >= nch && tile < ntiles) { c -= nch; tile += gridDim.x; ib += nch; if (++slot == uint32_t(NSLOT)) slot = 0; }
+    bool dead = false;
+    float acc0 = 0.f, acc1 = 0.f;
+    while (tile < ntiles) {
+        const uint32_t r0 = tile * TILE_R;
+        if (!dead && !mbar_wait_bounded(&full[s], ph)) {
+            if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
+            dead = true;
+        }
+        {
+            const uint8_t *st = stages + s * uint32_t(G::stage_bytes);
+            uint32_t ucv = uint32_t(uc);
+            bool use = !dead;
+            if constexpr (!FULLK) {
+                const uint32_t units = min(uint32_t(UPC), (K - c * CHW) / 32);
+                use = use && (uint32_t(uc) < units);
+                ucv = min(ucv, units - 1);                 // stay on this item's data
+            }
+            const uint32_t ug = c * UPC + ucv;             // unit index within the row
+            uint32_t xv[16];
+            load_xp(xs, U, ug, xv);
+            float cv[XC<F>::n];
+#pragma unroll
+            for (int q = 0; q < XC<F>::n; ++q) cv[q] = cst[ug * XC<F>::n + q];
+            const uint8_t *u0 = st + uoff0;
+            const float *sp0 = reinterpret_cast<const float *>(st + soff0);
+            const float d0 = row_dot<F>(u0, sp0, geo, cv, xv);
+            const float d1 = row_dot<F>(u0 + 2 * G::chunk_bytes, sp0 + 2 * (G::scale_bytes / 4), geo, cv, xv);
+            acc0 += use ? d0 : 0.f;
+            acc1 += use ? d1 : 0.f;
+        }
+        if (c + 2 >= nch) {
+            // this group's last item of the tile; transposing butterfly: lanes 0..15 reduce row rlo,
+            // lanes 16..31 row rlo + 2
+            const bool up = (lane & 16) != 0;
+            float v = up ? acc1 : acc0;
+            v += __shfl_xor_sync(0xffffffffu, up ? acc0 : acc1, 16);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            float *rs = red + slot * (G1_CW * 2);
+            if ((lane & 15) == 0) rs[warp * 2 + (lane >> 4)] = v;
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                const int expected = (nch >= 2) ? G1_CW : 8;
+                last = (atomicAdd(&cnt[slot], 1) == expected - 1);
+                if (last) __threadfence_block();
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                if (lane < TILE_R && r0 + lane < N) {
+                    const int jj = lane >> 1, hf = lane & 1;
+                    float yv = 0.f;
+#pragma unroll
+                    for (int gr = 0; gr < 2; ++gr) {
+                        if (nch >= 2 || uint32_t(gr) == (ib & 1u)) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) yv += rs[(gr * 8 + hf * 4 + q) * 2 + jj];
+                        }
+                    }
+                    a.Y[r0 + lane] = yv;
+                }
+                __syncwarp();
+                if (lane == 0) cnt[slot] = 0;
+            }
+            acc0 = acc1 = 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        s += 2;
+        if (s >= uint32_t(NS)) { s -= NS; ph ^= 1u; }
+        c += 2;
+        while (c >= nch) {
+            c -= nch;
+            tile += gridDim.x;
+            ib += nch;
+            if (++slot == uint32_t(NSLOT)) slot = 0;
         }
     }
-};
+}
 
-template <> struct Unit1<FMT_Q5S> {
-    // constants per unit (one sub-block of 32): C = 1024*S_even + 64*S_odd, S
-    static __device__ __forceinline__ float dot(const uint8_t *row, const float *, int uc, const float *cst,
-                                                const uint32_t *xv) {
-        const int sbk = uc >> 3, su = uc & 7;
-        const uint8_t *blk = row + sbk * 176;
-        const uint4 c = *reinterpret_cast<const uint4 *>(blk + 16 * su);
-        const uint32_t H = lds32(blk + 128 + 4 * su);
-        const float D = hbits(blk + 172), Dm = hbits(blk + 174);
-        // 6-bit fields: L_su = field su, M_su = field 8 + su
-        const uint8_t *fl = blk + 160 + 3 * (su >> 2);
-        const uint8_t *fm = blk + 166 + 3 * (su >> 2);
-        const uint32_t vl = uint32_t(fl[0]) | (uint32_t(fl[1]) << 8) | (uint32_t(fl[2]) << 16);
-        const uint32_t vm = uint32_t(fm[0]) | (uint32_t(fm[1]) << 8) | (uint32_t(fm[2]) << 16);
-        const float L = float((vl >> (6 * (su & 3))) & 63u), M = float((vm >> (6 * (su & 3))) & 63u);
-        float a0 = 0.f, a4 = 0.f;
-        // X_t: high bits of weights 8t..8t+3 at bits 0..3, of 8t+4..8t+7 at bits 16..19 (garbage elsewhere).
-        nib_word_hi<1>(c.x, lop3_sel(H, H << 12, 0x0000FFFFu), xv, 0, a0, a4);
-        nib_word_hi<1>(c.y, lop3_sel(H >> 8, H << 4, 0x0000FFFFu), xv, 8, a0, a4);
-        nib_word_hi<1>(c.z, lop3_sel(H >> 16, H >> 4, 0x0000FFFFu), xv, 16, a0, a4);
-        nib_word_hi<1>(c.w, lop3_sel(H >> 24, H >> 12, 0x0000FFFFu), xv, 24, a0, a4);
-        const float t = fmaf(a4, 0.0625f, a0) - cst[0];
-        return fmaf(D * L, t, -(Dm * M) * cst[1]);
+template <int F, int NS, bool FULLK>
+static cudaError_t try_launch_gemv1(const GemvArgs &a, cudaStream_t st, bool *launched) {
+    using LY = G1Layout<F, NS>;
+    *launched = false;
+    const uint32_t smem = LY::total(uint32_t(a.K));
+    if (smem > 227u * 1024u) return cudaSuccess;
+    static int opted[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!opted[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemv1_kernel<F, NS, FULLK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             227 * 1024);
+        if (e != cudaSuccess) return e;
+        opted[dev] = 1;
     }
-    static __device__ __forceinline__ void consts(const uint16_t *xs, int64_t u, float *out) {
-        float se = 0.f, so = 0.f;
-        for (int i = 0; i < 32; i += 2) { se += h2f_bits(xs[32 * u + i]); so += h2f_bits(xs[32 * u + i + 1]); }
-        out[0] = 1024.0f * se + 64.0f * so;
-        out[1] = se + so;
-    }
-};
+    const int64_t ntiles = (a.N + TILE_R - 1) / TILE_R;
+    int grid = num_sms();
+    if (ntiles < grid) grid = int(ntiles);
+    gemv1_kernel<F, NS, FULLK><<<grid, G1_THREADS, smem, st>>>(a);
+    *launched = true;
+    return cudaGetLastError();
+}
 
-template <> struct Unit1<FMT_Q6S> {
-    // constants per sub-block j (16): C_j = 1056*S_even + 96*S_odd
-    static __device__ __forceinline__ float dot(const uint8_t *row, const float *, int uc, const float *cst,
-                                                const uint32_t *xv) {
-        const int sbk = uc >> 3, su = uc & 7;
-        const uint8_t *blk = row + sbk * 210;
-        uint32_t c[4], h[2];
-        lds_words_a2<4>(blk + 16 * su, c);
-        lds_words_a2<2>(blk + 128 + 8 * su, h);
-        const float D = hbits(blk + 208);
-        const float L0 = float(int8_t(blk[192 + 2 * su])), L1 = float(int8_t(blk[193 + 2 * su]));
-        // X_t: high-2 byte pair (2t, 2t+1) of the sub-block's high word spread to bytes 0 and 2.
-        float a0 = 0.f, a4 = 0.f;
-        nib_word_hi<2>(c[0], __byte_perm(h[0], 0u, 0x4140u), xv, 0, a0, a4);
-        nib_word_hi<2>(c[1], __byte_perm(h[0], 0u, 0x4342u), xv, 8, a0, a4);
-        float r = D * L0 * (fmaf(a4, 0.0625f, a0) - cst[0]);
-        a0 = a4 = 0.f;
-        nib_word_hi<2>(c[2], __byte_perm(h[1], 0u, 0x4140u), xv, 16, a0, a4);
-        nib_word_hi<2>(c[3], __byte_perm(h[1], 0u, 0x4342u), xv, 24, a0, a4);
-        return fmaf(D * L1, fmaf(a4, 0.0625f, a0) - cst[1], r);
+template <int F, bool FULLK>
+static cudaError_t launch_gemv1_k(const GemvArgs &a, cudaStream_t st) {
+    bool done = false;
+    cudaError_t e;
+    if (Geo<F>::stage_bytes * 16 <= 140 * 1024) {
+        e = try_launch_gemv1<F, 16, FULLK>(a, st, &done);
+        if (e != cudaSuccess || done) return e;
     }
-    static __device__ __forceinline__ void consts(const uint16_t *xs, int64_t u, float *out) {
-        for (int h = 0; h < 2; ++h) {
-            float se = 0.f, so = 0.f;
-            for (int i = 0; i < 16; i += 2) { se += h2f_bits(xs[32 * u + 16 * h + i]); so += h2f_bits(xs[32 * u + 16 * h + i + 1]); }
-            out[h] = 1056.0f * se + 96.0f * so;
-        }
-    }
-};
+    e = try_launch_gemv1<F, 8, FULLK>(a, st, &done);
+    if (e != cudaSuccess || done) return e;
+    e = try_launch_gemv1<F, 4, FULLK>(a, st, &done);
+    if (e != cudaSuccess || done) return e;
+    return cudaErrorInvalidValue;
+}
 
+template <int F>
+static cudaError_t launch_gemv1(const GemvArgs &a, cudaStream_t st) {
+    if (a.K % CHW == 0) return launch_gemv1_k<F, true>(a, st);
+    return launch_gemv1_k<F, false>(a, st);
+}
+
+namespace {
 // ------------------------------------------------------------------------------------------------------------
 // Exact unit decode for the small-batch path: 32 dequantized fp32 weights (same roundings as FORMATS.md).
 // ------------------------------------------------------------------------------------------------------------
@@ -382,20 +649,17 @@ __device__ __forceinline__ void decode_unit(const uint8_t *row, const float *scl
     }
 }
 
-struct Smem {
-    uint64_t *full, *empty;
-    float *red;        // [2][NCW][MT]
-    uint16_t *xs;      // batch-1: x [K] (fp16)
-    float *cst;        // batch-1: per-unit activation constants
-    uint8_t *stages;   // NS x stage_bytes
-};
 
 }  // namespace
 
 // ------------------------------------------------------------------------------------------------------------
-// The streaming kernel. MT = 1: batch-1 GEMV with the magic-offset unpack; MT > 1: small-batch GEMM with exact
-// per-unit dequantization and M FMAs per weight (activations read through L1).
+// Small-batch kernel (M = 2..16): 8 consumer warps, warp pair p owns row p of the 4-row tile; each lane
+// dequantizes two 32-weight units exactly and multiplies them against the M activation rows (read through L1).
 // ------------------------------------------------------------------------------------------------------------
+constexpr int NCW = 8;
+constexpr int NTHREADS = (NCW + 1) * 32;
+constexpr int SMEM_BUDGET = 220 * 1024;
+
 template <int F, int MT>
 __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS) {
     using G = Geo<F>;
@@ -404,23 +668,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
     const int64_t N = a.N, K = a.K;
     const int64_t ntiles = (N + TILE_R - 1) / TILE_R;
     const int nchunks = int((K + CHW - 1) / CHW);
-    const int64_t units_row = K / 32;
 
-    // ---- carve shared memory ----
     uint8_t *p = smem_raw;
     uint64_t *full = reinterpret_cast<uint64_t *>(p);
     uint64_t *empty = full + NS;
     p += round_up(16 * NS, 128);
     float *red = reinterpret_cast<float *>(p);
     p += round_up(2 * NCW * MT * 4, 128);
-    uint16_t *xs = nullptr;
-    float *cst = nullptr;
-    if constexpr (MT == 1) {
-        xs = reinterpret_cast<uint16_t *>(p);
-        p += round_up(2 * K, 128);
-        cst = reinterpret_cast<float *>(p);
-        p += round_up(4 * units_row * G::consts_per_unit, 128);
-    }
     uint8_t *stages = p;
 
     if (tid == 0) {
@@ -430,12 +684,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
     __syncthreads();
 
     if (warp == NCW) {
-        // ================================= producer =================================
         const uint64_t pol = l2_evict_first_policy();
         int it = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
             const int64_t r0 = tile * TILE_R;
-            const int rows = int(imin64(TILE_R, N - r0));
+            const int rows = int(N - r0 < TILE_R ? N - r0 : TILE_R);
             for (int c = 0; c < nchunks; ++c) {
                 const int s = it % NS;
                 const uint32_t ph = uint32_t(it / NS) & 1u;
@@ -443,18 +696,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
                     bool ok = true;
                     if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1u);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
-                    // A consumer stopped releasing stages: record it and stop producing. Consumers then give up
-                    // on their next bounded wait, so nothing is left waiting.
                     if (!ok) { if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_EMPTY); return; }
                 }
                 int64_t cbytes, sbytes = 0;
                 const int64_t koff = int64_t(c) * CHW;
                 if constexpr (Fmt<F>::sb) {
                     const int64_t off = (koff / 256) * Fmt<F>::bytes;
-                    cbytes = imin64(G::chunk_bytes, a.row_stride - off);
+                    cbytes = a.row_stride - off < G::chunk_bytes ? a.row_stride - off : G::chunk_bytes;
                 } else {
-                    cbytes = imin64(G::chunk_bytes, (K - koff) / 2);
-                    sbytes = imin64(G::scale_bytes, (a.scale_stride - koff / 32) * 4);
+                    cbytes = (K - koff) / 2 < G::chunk_bytes ? (K - koff) / 2 : G::chunk_bytes;
+                    const int64_t sb = (a.scale_stride - koff / 32) * 4;
+                    sbytes = sb < G::scale_bytes ? sb : G::scale_bytes;
                 }
                 uint8_t *st = stages + int64_t(s) * G::stage_bytes;
                 if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(rows * (cbytes + sbytes)));
@@ -477,20 +729,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
         return;
     }
 
-    // =================================== consumers ===================================
-    if constexpr (MT == 1) {
-        // x -> shared memory, then per-unit activation constants (once per CTA)
-        const uint4 *xg = reinterpret_cast<const uint4 *>(a.X);
-        uint4 *xd = reinterpret_cast<uint4 *>(xs);
-        for (int64_t i = tid; i < K / 8; i += NCW * 32) xd[i] = xg[i];
-        named_bar_sync(1, NCW * 32);
-        for (int64_t u = tid; u < units_row; u += NCW * 32) Unit1<F>::consts(xs, u, cst + u * G::consts_per_unit);
-        named_bar_sync(1, NCW * 32);
-    }
-
     const int pair = warp >> 1, half = warp & 1;    // warp pair `pair` owns row `pair` of the tile
     int it = 0, tcount = 0;
-    bool dead = false;   // set after a bounded wait gave up: skip all further waits and work, keep the barriers
+    bool dead = false;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tcount) {
         const int64_t r0 = tile * TILE_R;
         const bool row_ok = (r0 + pair) < N;
@@ -507,7 +748,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
                 if (!ok) { if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL); dead = true; }
             }
             const int64_t koff = int64_t(c) * CHW;
-            const int units = int(imin64(UPC, (K - koff) / 32));
+            const int units = int((K - koff) / 32 < UPC ? (K - koff) / 32 : UPC);
             const uint8_t *st = stages + int64_t(s) * G::stage_bytes;
             const uint8_t *row = st + pair * G::chunk_bytes;
             const float *scl = reinterpret_cast<const float *>(st + TILE_R * G::chunk_bytes + pair * G::scale_bytes);
@@ -516,30 +757,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
                 for (int v = 0; v < 2; ++v) {
                     const int uc = 64 * half + 32 * v + lane;
                     if (uc < units) {
-                        if constexpr (MT == 1) {
-                            uint32_t xv[16];
-                            load_x_unit(xs, koff + 32 * uc, xv);
-                            acc[0] += Unit1<F>::dot(row, scl, uc, cst + (koff / 32 + uc) * G::consts_per_unit, xv);
-                        } else {
-                            float w[32];
-                            decode_unit<F>(row, scl, uc, w);
+                        float w[32];
+                        decode_unit<F>(row, scl, uc, w);
 #pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                if (m < a.M) {
-                                    const uint4 *xp = reinterpret_cast<const uint4 *>(a.X + m * a.ldx + koff + 32 * uc);
-                                    float t = 0.f;
+                        for (int m = 0; m < MT; ++m) {
+                            if (m < a.M) {
+                                const uint4 *xp = reinterpret_cast<const uint4 *>(a.X + m * a.ldx + koff + 32 * uc);
+                                float t = 0.f;
 #pragma unroll
-                                    for (int q = 0; q < 4; ++q) {
-                                        const uint4 xq = __ldg(xp + q);
-                                        const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w};
+                                for (int q = 0; q < 4; ++q) {
+                                    const uint4 xq = __ldg(xp + q);
+                                    const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w};
 #pragma unroll
-                                        for (int e = 0; e < 4; ++e) {
-                                            t = fmaf(w[8 * q + 2 * e], h2f_bits(lo16(xw[e])), t);
-                                            t = fmaf(w[8 * q + 2 * e + 1], h2f_bits(hi16(xw[e])), t);
-                                        }
+                                    for (int e = 0; e < 4; ++e) {
+                                        t = fmaf(w[8 * q + 2 * e], h2f_bits(lo16(xw[e])), t);
+                                        t = fmaf(w[8 * q + 2 * e + 1], h2f_bits(hi16(xw[e])), t);
                                     }
-                                    acc[m] += t;
                                 }
+                                acc[m] += t;
                             }
                         }
                     }
@@ -549,7 +784,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
             if (lane == 0) mbar_arrive(&empty[s]);
             ++it;
         }
-        // ---- reduce the row over the warp pair ----
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             float v = acc[m];
@@ -573,26 +807,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
 template <int F, int MT>
 static cudaError_t launch_stream(const GemvArgs &a, cudaStream_t s) {
     using G = Geo<F>;
-    const int64_t units_row = a.K / 32;
-    int64_t fixed = 128 /*barrier area upper bound for NS <= 8 is recomputed below*/;
-    int64_t extra = round_up(2 * NCW * MT * 4, 128);
-    if (MT == 1) extra += round_up(2 * a.K, 128) + round_up(4 * units_row * G::consts_per_unit, 128);
-    // choose the stage count so that barriers + extras + stages fit
+    const int64_t extra = round_up(2 * NCW * MT * 4, 128);
     int NS = 0;
+    int64_t tot = 0;
     for (int ns = 16; ns >= 2; --ns) {
-        const int64_t tot = round_up(16 * ns, 128) + extra + int64_t(ns) * G::stage_bytes + 16;
-        if (tot <= SMEM_BUDGET) { NS = ns; fixed = tot; break; }
+        tot = round_up(16 * ns, 128) + extra + int64_t(ns) * G::stage_bytes + 32;
+        if (tot <= SMEM_BUDGET) { NS = ns; break; }
     }
     if (NS == 0) return cudaErrorInvalidValue;
-    const size_t smem = size_t(fixed);
-    auto kern = stream_kernel<F, MT>;
-    // Raise the dynamic shared-memory limit once per device (not per launch, so launches can be graph-captured).
     static int opted[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (opted[dev] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BUDGET);
+    if (!opted[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(stream_kernel<F, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BUDGET);
         if (e != cudaSuccess) return e;
         opted[dev] = 1;
     }
@@ -600,13 +828,13 @@ static cudaError_t launch_stream(const GemvArgs &a, cudaStream_t s) {
     int grid = num_sms();
     if (ntiles < grid) grid = int(ntiles);
     if (grid < 1) return cudaSuccess;
-    kern<<<grid, NTHREADS, smem, s>>>(a, NS);
+    stream_kernel<F, MT><<<grid, NTHREADS, size_t(tot), s>>>(a, NS);
     return cudaGetLastError();
 }
 
 template <int F>
 static cudaError_t launch_fmt(const GemvArgs &a, cudaStream_t s) {
-    if (a.M <= 1) return launch_stream<F, 1>(a, s);
+    if (a.M <= 1) return launch_gemv1<F>(a, s);
     if (a.M <= 2) return launch_stream<F, 2>(a, s);
     if (a.M <= 4) return launch_stream<F, 4>(a, s);
     if (a.M <= 8) return launch_stream<F, 8>(a, s);
