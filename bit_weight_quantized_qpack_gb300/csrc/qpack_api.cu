@@ -254,7 +254,7 @@ int qgemm_prefill(int fmt, const uint8_t *packed, const float *group_scales, int
     if (fmt == QPACK_Q4G32 && K % 64) return QPACK_ERR_SHAPE;
     if (!X || !Y) return QPACK_ERR_ARG;
     if (ldx < K || ldy < N) return QPACK_ERR_SHAPE;
-    if (!aligned(X, 16) || (ldx % 8) || !aligned(Y, 16) || (ldy % 8)) return QPACK_ERR_ALIGN;
+    if (!aligned(X, 16) || (ldx % 8) || !aligned(Y, 2)) return QPACK_ERR_ALIGN;
     if (N == 0 || M == 0) return QPACK_OK;
     PrefillArgs a = {};
     a.packed = packed;
@@ -268,6 +268,7 @@ int qgemm_prefill(int fmt, const uint8_t *packed, const float *group_scales, int
     a.ldx = ldx;
     a.Y = Y;
     a.ldy = ldy;
+    a.vec_y = (aligned(Y, 16) && ldy % 8 == 0) ? 1 : 0;
     const cudaError_t e = launch_prefill(fmt, a, reinterpret_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return QPACK_ERR_UNSUPPORTED;
     return cuda_status(e);

@@ -57,6 +57,7 @@ struct PrefillArgs {
     int64_t ldx;
     uint16_t *Y;              // bf16 [M, ldy]
     int64_t ldy;
+    int vec_y;                // 1 when Y rows allow 16-byte stores (Y 16-byte aligned, ldy % 8 == 0)
 };
 cudaError_t launch_prefill(int fmt, const PrefillArgs &a, cudaStream_t s);
 
