@@ -230,6 +230,8 @@ def run_ours(args, world, rank, local):
         pg = dist
     hbm_peak, bf16_peak, peak_src = measured_peaks()
 
+    # decode over resident weights: products may start streaming their weights while the previous kernel ends
+    qp.qpack_set_option(qp.OPT_WEIGHT_PREFETCH, 0 if args.no_prefetch else 1)
     fmt = qp.Q3S
     lay = qp.layout(fmt, N_ROWS, K_COLS)
     wbytes = lay["weight_bytes"]
@@ -334,7 +336,8 @@ def run_ours(args, world, rank, local):
                    "format": "Q3S (110 B / 256 weights)", "N": N_ROWS, "K": K_COLS, "batch": 1,
                    "copies_per_step": R, "bytes_per_gemv": wbytes,
                    "l2": f"inputs larger than L2: {R} distinct packed copies ({R * wbytes / 1e9:.2f} GB) per step",
-                   "parallelism": "one GPU per rank; row shards need no exchange (weak-scaling replicas)"},
+                   "parallelism": "one GPU per rank; row shards need no exchange (weak-scaling replicas)",
+                   "weight_prefetch": not args.no_prefetch},
         "pct_hbm_peak": value / world / hbm_peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic, "peak_source": peak_src,
@@ -402,6 +405,7 @@ def main():
     ap.add_argument("--copies", type=int, default=0, help="distinct weight copies per step (default: >= 8x L2)")
     ap.add_argument("--no-extra", action="store_true", help="skip the 7B decode-step extra")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefetch", action="store_true", help="disable QPACK_OPT_WEIGHT_PREFETCH")
     ap.add_argument("--ncu-case", choices=["gemv", "small", "prefill"], default=None,
                     help="short run of one product for an ncu capture (see profiles/)")
     ap.add_argument("--fmt", default="Q3S")

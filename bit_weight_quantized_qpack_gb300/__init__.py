@@ -60,6 +60,7 @@ def lib():
                 "qpack_status_string": ([I], ctypes.c_char_p),
                 "qpack_fetch_fault_flags": ([ctypes.POINTER(ctypes.c_int32)], I),
                 "qpack_version": ([], I),
+                "qpack_set_option": ([I, I], I),
             }
             for name, (args, res) in sigs.items():
                 fn = getattr(L, name)
@@ -201,6 +202,13 @@ def qpack_fetch_fault_flags() -> int:
 
 def qpack_status_string(status: int) -> str:
     return lib().qpack_status_string(int(status)).decode()
+
+
+OPT_WEIGHT_PREFETCH = 1
+
+
+def qpack_set_option(option: int, value: int) -> None:
+    _check(lib().qpack_set_option(int(option), int(value)), "qpack_set_option")
 
 
 def qpack_version() -> int:

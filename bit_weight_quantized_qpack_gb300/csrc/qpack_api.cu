@@ -8,11 +8,13 @@
 
 #include <mutex>
 
-#include "../../include/qpack.h"
+#include "qpack.h"
 #include "qpack_dev.cuh"
 #include "qpack_launch.h"
 
 namespace qpack {
+
+int set_weight_prefetch(int v);
 
 int num_sms() {
     static int cached[64] = {0};
@@ -24,6 +26,21 @@ int num_sms() {
         cached[dev] = n;
     }
     return cached[dev];
+}
+
+static int g_weight_prefetch[64] = {0};
+
+int weight_prefetch_enabled() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    return g_weight_prefetch[dev];
+}
+
+int set_weight_prefetch(int v) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    g_weight_prefetch[dev] = v ? 1 : 0;
+    return 0;
 }
 
 }  // namespace qpack
@@ -236,6 +253,7 @@ int qgemm_small(int fmt, const uint8_t *packed, const float *group_scales, int64
     a.Y = Y;
     a.ldy = ldy;
     a.M = M;
+    a.weight_prefetch = weight_prefetch_enabled();
     return cuda_status(launch_gemv(fmt, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -293,6 +311,11 @@ int qpack_fetch_fault_flags(int32_t *flags) {
     cudaError_t e = fetch_fault_gemv(flags);
     if (e == cudaSuccess) e = fetch_fault_prefill(flags);
     return cuda_status(e);
+}
+
+int qpack_set_option(int option, int value) {
+    if (option != QPACK_OPT_WEIGHT_PREFETCH) return QPACK_ERR_ARG;
+    return set_weight_prefetch(value) == 0 ? QPACK_OK : QPACK_ERR_CUDA;
 }
 
 int qpack_version(void) { return 1 * 10000 + 0 * 100 + 0; }

@@ -213,17 +213,18 @@ __device__ __forceinline__ LaneGeo lane_geo(int uc) {
 
 // sum_i w'_i x_i over one 32-weight unit of one row; `u` = aligned unit base in shared memory, `sp` = this
 // row's group-scale pointer (Q4G32), `c` = the unit's activation constants, `xv` = its staged activations.
+// Each sub-block accumulator starts at -C (the activation constant), so no separate subtraction is needed.
 template <int F>
 __device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, const LaneGeo &g, const float *c,
                                          const uint32_t *xv) {
     if constexpr (F == FMT_Q4G32) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
-        float a = 0.f, b = 0.f;
+        float a = -c[0], b = 0.f;
         nib_word(w.x, xv, 0, a, b);
         nib_word(w.y, xv, 8, a, b);
         nib_word(w.z, xv, 16, a, b);
         nib_word(w.w, xv, 24, a, b);
-        return sp[0] * ((a + b) - c[0]);
+        return sp[0] * (a + b);
     } else if constexpr (F == FMT_Q2S) {
         const uint32_t w0 = lds32(u), w1 = lds32(u + 4);
         const uint32_t dd = lds32(u + g.o2);
@@ -233,11 +234,11 @@ __device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, cons
         const float M0 = small_int_f(lop3_and_or(lm >> 4, 0xFu, MAGICF));
         const float L1 = small_int_f(lop3_and_or(lm >> 8, 0xFu, MAGICF));
         const float M1 = small_int_f(lop3_and_or(lm >> 12, 0xFu, MAGICF));
-        float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+        float a0 = -c[0], b0 = 0.f, a1 = -c[2], b1 = 0.f;
         crumb_word(w0, xv, 0, a0, b0);
         crumb_word(w1, xv, 16, a1, b1);
-        float r = (Dd.x * L0) * ((a0 + b0) - c[0]);
-        r = fmaf(Dd.x * L1, (a1 + b1) - c[2], r);
+        float r = (Dd.x * L0) * (a0 + b0);
+        r = fmaf(Dd.x * L1, a1 + b1, r);
         r = fmaf(-(Dd.y * M0), c[1], r);
         return fmaf(-(Dd.y * M1), c[3], r);
     } else if constexpr (F == FMT_Q3S) {
@@ -250,12 +251,12 @@ __device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, cons
         const float L0 = small_int_f(lop3_and_or(f, 63u, MAGICF));
         const float L1 = small_int_f(lop3_and_or(f >> 6, 63u, MAGICF));
         const float D = hbits(u + g.o2);
-        float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+        float a0 = -c[0], b0 = 0.f, a1 = -c[1], b1 = 0.f;
         tri_group(s0, xv, 0, a0, b0);
         tri_group(__funnelshift_r(s0, s1, 24), xv, 8, a0, b0);
         tri_group(__funnelshift_r(s1, s2, 16), xv, 16, a1, b1);
         tri_group(s2 >> 8, xv, 24, a1, b1);
-        return fmaf(D * L1, (a1 + b1) - c[1], (D * L0) * ((a0 + b0) - c[0]));
+        return fmaf(D * L1, a1 + b1, (D * L0) * (a0 + b0));
     } else if constexpr (F == FMT_Q5S) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
         const uint32_t H = lds32(u + g.o1);
@@ -264,12 +265,12 @@ __device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, cons
         const uint64_t lo64 = (uint64_t(fld.y) << 32) | fld.x, hi64 = (uint64_t(fld.z) << 32) | fld.y;
         const float L = small_int_f(lop3_and_or(uint32_t(lo64 >> g.sh0), 63u, MAGICF));
         const float M = small_int_f(lop3_and_or(uint32_t(hi64 >> (g.sh1 - 32u)), 63u, MAGICF));
-        float a = 0.f, b = 0.f;
+        float a = -c[0], b = 0.f;
         nib_word_hi<1>(w.x, lop3_sel(H, H << 12, 0x0000FFFFu), xv, 0, a, b);
         nib_word_hi<1>(w.y, lop3_sel(H >> 8, H << 4, 0x0000FFFFu), xv, 8, a, b);
         nib_word_hi<1>(w.z, lop3_sel(H >> 16, H >> 4, 0x0000FFFFu), xv, 16, a, b);
         nib_word_hi<1>(w.w, lop3_sel(H >> 24, H >> 12, 0x0000FFFFu), xv, 24, a, b);
-        return fmaf(Dd.x * L, (a + b) - c[0], -(Dd.y * M) * c[1]);
+        return fmaf(Dd.x * L, a + b, -(Dd.y * M) * c[1]);
     } else {
         const uint32_t sh = g.sh0;
         const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
@@ -282,22 +283,27 @@ __device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, cons
         const float L0 = __uint_as_float((lv & 0xFFu) ^ (MAGICF | 0x80u)) - 8388736.0f;
         const float L1 = __uint_as_float(((lv >> 8) & 0xFFu) ^ (MAGICF | 0x80u)) - 8388736.0f;
         const float D = hbits(u + g.o3);
-        float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+        float a0 = -c[0], b0 = 0.f, a1 = -c[1], b1 = 0.f;
         nib_word_hi<2>(__funnelshift_r(r0, r1, sh), __byte_perm(h0, 0u, 0x4140u), xv, 0, a0, b0);
         nib_word_hi<2>(__funnelshift_r(r1, r2, sh), __byte_perm(h0, 0u, 0x4342u), xv, 8, a0, b0);
         nib_word_hi<2>(__funnelshift_r(r2, r3, sh), __byte_perm(h1, 0u, 0x4140u), xv, 16, a1, b1);
         nib_word_hi<2>(__funnelshift_r(r3, r4, sh), __byte_perm(h1, 0u, 0x4342u), xv, 24, a1, b1);
-        return fmaf(D * L1, (a1 + b1) - c[1], (D * L0) * ((a0 + b0) - c[0]));
+        return fmaf(D * L1, a1 + b1, (D * L0) * (a0 + b0));
     }
 }
 
-// Staged activations: unit u's 32 halves are four 16-byte vectors stored at vector index t * U + u (t = 0..3,
-// U = units per row), so that consecutive lanes (consecutive units) read consecutive 16-byte vectors.
-__device__ __forceinline__ void load_xp(const uint16_t *xs, uint32_t U, uint32_t u, uint32_t xv[16]) {
-    const uint4 *p = reinterpret_cast<const uint4 *>(xs);
+// Staged activations: within each 4096-weight chunk c, the 32 halves of unit uc are four 16-byte vectors at
+// vector index (c * 4 + t) * 128 + uc (t = 0..3), so consecutive lanes (consecutive units) read consecutive
+// 16-byte vectors and the four loads of a unit sit at constant 2 KB offsets.
+__device__ __forceinline__ uint32_t xvec_index(uint32_t k8) {   // k8 = element index / 8
+    const uint32_t u = k8 >> 2, t = k8 & 3u;
+    return ((u >> 7) * 4u + t) * 128u + (u & 127u);
+}
+__device__ __forceinline__ void load_xp(const uint16_t *xs, uint32_t c, uint32_t uc, uint32_t xv[16]) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(xs) + c * 512u + uc;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-        const uint4 v = p[t * U + u];
+        const uint4 v = p[t * 128];
         xv[4 * t] = v.x; xv[4 * t + 1] = v.y; xv[4 * t + 2] = v.z; xv[4 * t + 3] = v.w;
     }
 }
@@ -305,32 +311,42 @@ __device__ __forceinline__ void load_xp(const uint16_t *xs, uint32_t U, uint32_t
 }  // namespace
 
 // ------------------------------------------------------------------------------------------------------------
-// Batch-1 fused dequant-GEMV kernel.
+// Batch-1 fused dequant-GEMV kernel: NG consumer groups of 8 warps + 1 producer warp (TR lanes per group).
 // ------------------------------------------------------------------------------------------------------------
-constexpr int G1_CW = 16;
-constexpr int G1_THREADS = (G1_CW + 1) * 32;
-
-template <int F, int NS>
+constexpr int G1_NG = 3;     // consumer groups
+template <int F, int NS, int NG, int TR>
 struct G1Layout {
+    static constexpr int CW = 8 * NG;                  // consumer warps
+    static constexpr int THREADS = (CW + 1) * 32;
     static constexpr int NSLOT = NS + 2;
+    static constexpr int RPL = TR / 2;                 // rows per lane (rows rlo, rlo + 2, ...)
+    static constexpr int RED_PER_WARP = 4 * RPL;       // 4 partials per row per warp
+    static constexpr int RED_PER_SLOT = CW * RED_PER_WARP;
+    static constexpr int STAGE = TR * (Geo<F>::chunk_bytes + Geo<F>::scale_bytes);
     static __host__ __device__ uint32_t bar_bytes() { return uint32_t(round_up(16 * NS, 128)); }
-    static __host__ __device__ uint32_t red_bytes() { return uint32_t(round_up(NSLOT * 4 + NSLOT * G1_CW * 2 * 4, 128)); }
-    static __host__ __device__ uint32_t x_bytes(uint32_t K) { return uint32_t(round_up(2 * int64_t(K), 128)); }
+    static __host__ __device__ uint32_t red_bytes() { return uint32_t(round_up(NSLOT * 4 + NSLOT * RED_PER_SLOT * 4, 128)); }
+    static __host__ __device__ uint32_t x_bytes(uint32_t K) { return uint32_t(round_up(int64_t((K + CHW - 1) / CHW) * CHW * 2, 128)); }
     static __host__ __device__ uint32_t c_bytes(uint32_t K) { return uint32_t(round_up(4 * int64_t(K / 32) * XC<F>::n, 128)); }
     static __host__ __device__ uint32_t total(uint32_t K) {
-        return bar_bytes() + red_bytes() + x_bytes(K) + c_bytes(K) + uint32_t(NS) * Geo<F>::stage_bytes + 32;
+        return bar_bytes() + red_bytes() + x_bytes(K) + c_bytes(K) + uint32_t(NS) * STAGE + 32;
     }
 };
 
-template <int F, int NS, bool FULLK>
-__global__ void __launch_bounds__(G1_THREADS, 1) gemv1_kernel(GemvArgs a) {
+template <int F, int NS, int NG, int TR, bool FULLK>
+__global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_kernel(GemvArgs a) {
     using G = Geo<F>;
-    using LY = G1Layout<F, NS>;
+    using LY = G1Layout<F, NS, NG, TR>;
     constexpr int NSLOT = LY::NSLOT;
+    constexpr int CW = LY::CW;
+    constexpr int RPL = LY::RPL;
+    constexpr uint32_t STAGE = uint32_t(LY::STAGE);
+    constexpr uint32_t NSG = uint32_t(NS / NG);       // stages per consumer group
+    static_assert(NS % NG == 0, "each consumer group owns NS / NG stages");
+    static_assert(NG * TR <= 32, "producer lanes: TR per group");
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t N = uint32_t(a.N), K = uint32_t(a.K);
-    const uint32_t ntiles = (N + TILE_R - 1) / TILE_R;
+    const uint32_t ntiles = (N + TR - 1) / TR;
     const uint32_t nch = (K + CHW - 1) / CHW;
     const uint32_t U = K / 32;                        // units per row
 
@@ -352,24 +368,43 @@ __global__ void __launch_bounds__(G1_THREADS, 1) gemv1_kernel(GemvArgs a) {
         for (int s = 0; s < NSLOT; ++s) cnt[s] = 0;
         fence_mbar_init();
     }
+    pdl_launch_dependents();     // the next product may begin launching; it still waits for us before reading
     __syncthreads();
 
-    if (warp == G1_CW) {
+    if (warp == CW) {
         // ------------------------------------ producer ------------------------------------
-        const uint64_t pol = l2_evict_first_policy();
-        uint32_t i = 0, s = 0, ph = 0;
-        for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-            const uint32_t r0 = tile * TILE_R;
-            const uint32_t rows = min(uint32_t(TILE_R), N - r0);
-            for (uint32_t c = 0; c < nch; ++c) {
-                if (i >= uint32_t(NS)) {
-                    bool ok = true;
-                    if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1u);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
+        // Group g owns the private sub-ring of stages [g*NSG, (g+1)*NSG) and consumes its k-th item from stage
+        // g*NSG + k mod NSG, so every mbarrier is waited on only by the one group that consumed its previous phase
+        // (a parity wait is only meaningful one phase ahead). Producer lanes g*TR .. g*TR+TR-1 serve group g: lane
+        // r copies row r of the tile (bulk copies issued by one thread are processed one after another, so rows go
+        // out from different lanes), or lane 0 copies the whole tile when its rows are contiguous.
+        // The lanes advance in rounds (round k = every group's k-th item), and a round starts only once every
+        // group has released the stage it reuses, so no group runs more than NSG rounds ahead of another: the
+        // per-tile reduction slots, reused every NSLOT = NS + 2 tiles, depend on that bound.
+        constexpr uint32_t PMASK = (NG * TR >= 32) ? 0xffffffffu : ((1u << (NG * TR)) - 1u);
+        const int pg = lane / TR, pr = lane % TR;
+        if (pg < NG) {
+            // Packed weights are read before the previous grid has finished only when the caller opted in
+            // (QPACK_OPT_WEIGHT_PREFETCH: weights are not written by the kernel just before this one).
+            if (!a.weight_prefetch) pdl_wait();
+            const uint64_t pol = l2_evict_first_policy();
+            const bool whole_rows = (K == uint32_t(CHW));        // a tile of whole rows is one contiguous range
+            uint32_t k = 0, issued = 0, c = uint32_t(pg), tile = blockIdx.x;
+            while (c >= nch) { c -= nch; tile += gridDim.x; }
+            while (true) {
+                const bool have = tile < ntiles;
+                if (!__any_sync(PMASK, have)) break;
+                const uint32_t s = uint32_t(pg) * NSG + k % NSG, ph = (k / NSG) & 1u;
+                bool bad = false;
+                if (have && pr == 0 && k >= NSG && !mbar_wait_bounded(&empty[s], ph ^ 1u)) {
                     // A consumer stopped releasing stages: record it and stop producing; consumers then give up
                     // on their next bounded wait, so nothing is left waiting.
-                    if (!ok) { if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_EMPTY); return; }
+                    atomicOr(&g_fault_gemv, FAULT_WAIT_EMPTY);
+                    bad = true;
                 }
+                if (__any_sync(PMASK, bad)) break;
+                const uint32_t r0 = tile * TR;
+                const uint32_t rows = have ? min(uint32_t(TR), N - r0) : 0u;
                 const uint32_t koff = c * CHW;
                 uint32_t cbytes, sbytes = 0;
                 if constexpr (Fmt<F>::sb) {
@@ -379,33 +414,53 @@ __global__ void __launch_bounds__(G1_THREADS, 1) gemv1_kernel(GemvArgs a) {
                     cbytes = min(uint32_t(G::chunk_bytes), (K - koff) / 2);
                     sbytes = min(uint32_t(G::scale_bytes), (uint32_t(a.scale_stride) - koff / 32) * 4);
                 }
-                uint8_t *st = stages + s * uint32_t(G::stage_bytes);
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], rows * (cbytes + sbytes));
-                __syncwarp();
-                if (uint32_t(lane) < rows) {
-                    const uint8_t *src = a.packed + int64_t(r0 + lane) * a.row_stride +
-                                         (Fmt<F>::sb ? (koff / 256) * Fmt<F>::bytes : koff / 2);
-                    bulk_g2s(st + lane * G::chunk_bytes, src, cbytes, &full[s], pol);
-                } else if (!Fmt<F>::sb && lane >= 8 && uint32_t(lane - 8) < rows) {
-                    const uint8_t *src =
-                        reinterpret_cast<const uint8_t *>(a.gscale + int64_t(r0 + lane - 8) * a.scale_stride + koff / 32);
-                    bulk_g2s(st + TILE_R * G::chunk_bytes + (lane - 8) * G::scale_bytes, src, sbytes, &full[s], pol);
+                uint8_t *st = stages + s * STAGE;
+                if (have && pr == 0) mbar_arrive_expect_tx(&full[s], rows * (cbytes + sbytes));
+                __syncwarp(PMASK);                               // expect_tx before any of this item's copies
+                if (have) {
+                    const uint8_t *src0 =
+                        a.packed + int64_t(r0) * a.row_stride + (Fmt<F>::sb ? (koff / 256) * Fmt<F>::bytes : koff / 2);
+                    const uint8_t *ssrc0 =
+                        Fmt<F>::sb ? nullptr : reinterpret_cast<const uint8_t *>(a.gscale + int64_t(r0) * a.scale_stride + koff / 32);
+                    if (whole_rows) {
+                        if (pr == 0) bulk_g2s(st, src0, rows * cbytes, &full[s], pol);
+                        if constexpr (!Fmt<F>::sb) {
+                            if (pr == 1 % TR) bulk_g2s(st + TR * G::chunk_bytes, ssrc0, rows * sbytes, &full[s], pol);
+                        }
+                    } else if (uint32_t(pr) < rows) {
+                        bulk_g2s(st + pr * G::chunk_bytes, src0 + int64_t(pr) * a.row_stride, cbytes, &full[s], pol);
+                        if constexpr (!Fmt<F>::sb)
+                            bulk_g2s(st + TR * G::chunk_bytes + pr * G::scale_bytes,
+                                     ssrc0 + int64_t(pr) * a.scale_stride * 4, sbytes, &full[s], pol);
+                    }
+                    ++issued;
                 }
-                ++i;
-                if (++s == uint32_t(NS)) { s = 0; ph ^= 1u; }
+                ++k;
+                c += NG;
+                while (c >= nch) { c -= nch; tile += gridDim.x; }
+            }
+            // Drain: wait (bounded) until the last fill of each of the group's stages has landed, so the CTA never
+            // exits with bulk copies still writing its shared memory (consumers that gave up may exit early).
+            if (pr == 0) {
+                for (uint32_t j = (issued > NSG ? issued - NSG : 0u); j < issued; ++j) {
+                    if (!mbar_wait_bounded(&full[uint32_t(pg) * NSG + j % NSG], (j / NSG) & 1u)) {
+                        atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
+                        break;
+                    }
+                }
             }
         }
         return;
     }
 
     // -------------------------------------- consumers --------------------------------------
+    pdl_wait();                  // x (and y) may belong to the previous grid
     {
-        // stage x' = fp16(x * 2^-p) in the transposed vector layout, then the per-unit constants
+        // stage x' = fp16(x * 2^-p) in the chunk-major vector layout, then the per-unit constants
         const uint4 *xg = reinterpret_cast<const uint4 *>(a.X);
         uint4 *xd = reinterpret_cast<uint4 *>(xs);
-        for (uint32_t v = tid; v < K / 8; v += G1_CW * 32) {
+        for (uint32_t v = tid; v < K / 8; v += CW * 32) {
             const uint4 raw = xg[v];
-            const uint32_t u = v >> 2, t = v & 3u;
             uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -414,12 +469,12 @@ __global__ void __launch_bounds__(G1_THREADS, 1) gemv1_kernel(GemvArgs a) {
                 const float f1 = h2f_bits(hi16(w[e])) * pow2f(-xshift<F>(2 * e + 1));
                 w[e] = uint32_t(f2h_bits(f0)) | (uint32_t(f2h_bits(f1)) << 16);
             }
-            xd[t * U + u] = make_uint4(w[0], w[1], w[2], w[3]);
+            xd[xvec_index(v)] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        named_bar_sync(1, G1_CW * 32);
-        for (uint32_t u = tid; u < U; u += G1_CW * 32) {
+        named_bar_sync(1, CW * 32);
+        for (uint32_t u = tid; u < U; u += CW * 32) {
             uint32_t xv[16];
-            load_xp(xs, U, u, xv);
+            load_xp(xs, u >> 7, u & 127u, xv);
             float xp[32], xt[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -428,30 +483,33 @@ __global__ void __launch_bounds__(G1_THREADS, 1) gemv1_kernel(GemvArgs a) {
             }
             unit_consts<F>(xp, xt, cst + u * XC<F>::n);
         }
-        named_bar_sync(1, G1_CW * 32);
+        named_bar_sync(1, CW * 32);
     }
     const uint32_t group = uint32_t(warp) >> 3, wg = uint32_t(warp) & 7u;
     const uint32_t gl = wg * 32u + uint32_t(lane);
     const int uc = int(gl & 127u);
-    const uint32_t rlo = gl >> 7;                      // rows rlo and rlo + 2 of the tile
+    const uint32_t rlo = gl >> 7;                      // rows rlo, rlo + 2, ..., rlo + TR - 2 of the tile
     const LaneGeo geo = lane_geo<F>(uc);
-    const uint32_t uoff0 = rlo * uint32_t(G::chunk_bytes) + geo.ubase;            // row rlo; row rlo+2 is +2 chunks
-    const uint32_t soff0 = TILE_R * uint32_t(G::chunk_bytes) + rlo * uint32_t(G::scale_bytes) + 4u * uint32_t(uc);
+    const uint32_t uoff0 = rlo * uint32_t(G::chunk_bytes) + geo.ubase;
+    const uint32_t soff0 = TR * uint32_t(G::chunk_bytes) + rlo * uint32_t(G::scale_bytes) + 4u * uint32_t(uc);
 
-    // own items: i = group, group + 2, ... ; stage s = i mod NS (NS even -> stages of this group's parity)
-    uint32_t s = group, ph = 0;
+    // own items: the group's k-th item is global item group + NG*k, in stage group*NSG + k mod NSG
+    uint32_t sl = 0, ph = 0;
     uint32_t tile = blockIdx.x, c = group, ib = 0, slot = 0;   // ib = item index of the tile's first chunk
     while (c >= nch && tile < ntiles) { c -= nch; tile += gridDim.x; ib += nch; if (++slot == uint32_t(NSLOT)) slot = 0; }
     bool dead = false;
-    float acc0 = 0.f, acc1 = 0.f;
+    float acc[RPL];
+#pragma unroll
+    for (int j = 0; j < RPL; ++j) acc[j] = 0.f;
     while (tile < ntiles) {
-        const uint32_t r0 = tile * TILE_R;
+        const uint32_t r0 = tile * TR;
+        const uint32_t s = group * NSG + sl;
         if (!dead && !mbar_wait_bounded(&full[s], ph)) {
             if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
             dead = true;
         }
         {
-            const uint8_t *st = stages + s * uint32_t(G::stage_bytes);
+            const uint8_t *st = stages + s * STAGE;
             uint32_t ucv = uint32_t(uc);
             bool use = !dead;
             if constexpr (!FULLK) {
@@ -459,61 +517,78 @@ __global__ void __launch_bounds__(G1_THREADS, 1) gemv1_kernel(GemvArgs a) {
                 use = use && (uint32_t(uc) < units);
                 ucv = min(ucv, units - 1);                 // stay on this item's data
             }
-            const uint32_t ug = c * UPC + ucv;             // unit index within the row
             uint32_t xv[16];
-            load_xp(xs, U, ug, xv);
+            load_xp(xs, c, ucv, xv);
             float cv[XC<F>::n];
+            const float *cp = cst + (c * UPC + ucv) * XC<F>::n;
 #pragma unroll
-            for (int q = 0; q < XC<F>::n; ++q) cv[q] = cst[ug * XC<F>::n + q];
+            for (int q = 0; q < XC<F>::n; ++q) cv[q] = cp[q];
             const uint8_t *u0 = st + uoff0;
             const float *sp0 = reinterpret_cast<const float *>(st + soff0);
-            const float d0 = row_dot<F>(u0, sp0, geo, cv, xv);
-            const float d1 = row_dot<F>(u0 + 2 * G::chunk_bytes, sp0 + 2 * (G::scale_bytes / 4), geo, cv, xv);
-            acc0 += use ? d0 : 0.f;
-            acc1 += use ? d1 : 0.f;
-        }
-        if (c + 2 >= nch) {
-            // this group's last item of the tile; transposing butterfly: lanes 0..15 reduce row rlo,
-            // lanes 16..31 row rlo + 2
-            const bool up = (lane & 16) != 0;
-            float v = up ? acc1 : acc0;
-            v += __shfl_xor_sync(0xffffffffu, up ? acc0 : acc1, 16);
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            float *rs = red + slot * (G1_CW * 2);
-            if ((lane & 15) == 0) rs[warp * 2 + (lane >> 4)] = v;
+            for (int j = 0; j < RPL; ++j) {
+                const float d = row_dot<F>(u0 + 2 * j * G::chunk_bytes, sp0 + 2 * j * (G::scale_bytes / 4), geo, cv, xv);
+                acc[j] += use ? d : 0.f;
+            }
+        }
+        if (c + NG >= nch) {
+            // this group's last item of the tile. Per pair of the lane's rows, a partial butterfly: lanes 0..15
+            // carry the first row, 16..31 the second; after three steps lanes {0..3} / {16..19} hold 4 partials.
+            float *rs = red + slot * LY::RED_PER_SLOT + warp * LY::RED_PER_WARP;
+            const bool up = (lane & 16) != 0;
+#pragma unroll
+            for (int pr = 0; pr < RPL / 2; ++pr) {
+                float v = up ? acc[2 * pr + 1] : acc[2 * pr];
+                v += __shfl_xor_sync(0xffffffffu, up ? acc[2 * pr] : acc[2 * pr + 1], 16);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                if ((lane & 12) == 0) rs[pr * 8 + (lane >> 4) * 4 + (lane & 3)] = v;
+            }
             __syncwarp();
             int last = 0;
             if (lane == 0) {
                 __threadfence_block();
-                const int expected = (nch >= 2) ? G1_CW : 8;
+                const int expected = 8 * int(min(uint32_t(NG), nch));
                 last = (atomicAdd(&cnt[slot], 1) == expected - 1);
                 if (last) __threadfence_block();
             }
             last = __shfl_sync(0xffffffffu, last, 0);
             if (last) {
-                if (lane < TILE_R && r0 + lane < N) {
-                    const int jj = lane >> 1, hf = lane & 1;
-                    float yv = 0.f;
+                // output row rho = lane / LPR; lane j = lane % LPR sums every LPR-th partial of that row
+                constexpr int LPR = 32 / TR;
+                const int rho = lane / LPR, j = lane % LPR;
+                const int hf = rho & 1, jr = rho >> 1, pr = jr >> 1, jj = jr & 1;
+                const float *slot_base = red + slot * LY::RED_PER_SLOT;
+                float yv = 0.f;
 #pragma unroll
-                    for (int gr = 0; gr < 2; ++gr) {
-                        if (nch >= 2 || uint32_t(gr) == (ib & 1u)) {
+                for (int gr = 0; gr < NG; ++gr) {
+                    bool contributed = nch >= uint32_t(NG);
+                    if (!contributed) {
+                        for (uint32_t cc = 0; cc < nch; ++cc) contributed |= ((ib + cc) % NG) == uint32_t(gr);
+                    }
+                    if (contributed) {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) yv += rs[(gr * 8 + hf * 4 + q) * 2 + jj];
+                        for (int idx = 0; idx < 16; ++idx) {
+                            if (idx % LPR == j) {
+                                const int q = idx >> 2, e = idx & 3;
+                                yv += slot_base[(gr * 8 + hf * 4 + q) * LY::RED_PER_WARP + pr * 8 + jj * 4 + e];
+                            }
                         }
                     }
-                    a.Y[r0 + lane] = yv;
                 }
+#pragma unroll
+                for (int o = LPR / 2; o > 0; o >>= 1) yv += __shfl_xor_sync(0xffffffffu, yv, o);
+                if (j == 0 && r0 + rho < N) a.Y[r0 + rho] = yv;
                 __syncwarp();
                 if (lane == 0) cnt[slot] = 0;
             }
-            acc0 = acc1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < RPL; ++j) acc[j] = 0.f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        s += 2;
-        if (s >= uint32_t(NS)) { s -= NS; ph ^= 1u; }
-        c += 2;
+        if (++sl == uint32_t(NSG)) { sl = 0; ph ^= 1u; }
+        c += NG;
         while (c >= nch) {
             c -= nch;
             tile += gridDim.x;
@@ -523,9 +598,9 @@ __global__ void __launch_bounds__(G1_THREADS, 1) gemv1_kernel(GemvArgs a) {
     }
 }
 
-template <int F, int NS, bool FULLK>
+template <int F, int NS, int NG, int TR, bool FULLK>
 static cudaError_t try_launch_gemv1(const GemvArgs &a, cudaStream_t st, bool *launched) {
-    using LY = G1Layout<F, NS>;
+    using LY = G1Layout<F, NS, NG, TR>;
     *launched = false;
     const uint32_t smem = LY::total(uint32_t(a.K));
     if (smem > 227u * 1024u) return cudaSuccess;
@@ -534,38 +609,61 @@ static cudaError_t try_launch_gemv1(const GemvArgs &a, cudaStream_t st, bool *la
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!opted[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemv1_kernel<F, NS, FULLK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(gemv1_kernel<F, NS, NG, TR, FULLK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              227 * 1024);
         if (e != cudaSuccess) return e;
         opted[dev] = 1;
     }
-    const int64_t ntiles = (a.N + TILE_R - 1) / TILE_R;
+    const int64_t ntiles = (a.N + TR - 1) / TR;
     int grid = num_sms();
     if (ntiles < grid) grid = int(ntiles);
-    gemv1_kernel<F, NS, FULLK><<<grid, G1_THREADS, smem, st>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(unsigned(LY::THREADS));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = a.weight_prefetch ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     *launched = true;
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, gemv1_kernel<F, NS, NG, TR, FULLK>, a);
 }
 
-template <int F, bool FULLK>
+
+template <int F, int TR, bool FULLK>
 static cudaError_t launch_gemv1_k(const GemvArgs &a, cudaStream_t st) {
     bool done = false;
     cudaError_t e;
-    if (Geo<F>::stage_bytes * 16 <= 140 * 1024) {
-        e = try_launch_gemv1<F, 16, FULLK>(a, st, &done);
+    constexpr int SB = G1Layout<F, 4, G1_NG, TR>::STAGE;
+    // stage counts are multiples of G1_NG (private sub-rings); the largest ring that fits (with x and constants)
+    if (SB * 24 <= 176 * 1024) {
+        e = try_launch_gemv1<F, 24, G1_NG, TR, FULLK>(a, st, &done);
         if (e != cudaSuccess || done) return e;
     }
-    e = try_launch_gemv1<F, 8, FULLK>(a, st, &done);
+    if (SB * 18 <= 176 * 1024) {
+        e = try_launch_gemv1<F, 18, G1_NG, TR, FULLK>(a, st, &done);
+        if (e != cudaSuccess || done) return e;
+    }
+    if (SB * 12 <= 192 * 1024) {
+        e = try_launch_gemv1<F, 12, G1_NG, TR, FULLK>(a, st, &done);
+        if (e != cudaSuccess || done) return e;
+    }
+    e = try_launch_gemv1<F, 9, G1_NG, TR, FULLK>(a, st, &done);
     if (e != cudaSuccess || done) return e;
-    e = try_launch_gemv1<F, 4, FULLK>(a, st, &done);
+    e = try_launch_gemv1<F, 6, G1_NG, TR, FULLK>(a, st, &done);
     if (e != cudaSuccess || done) return e;
     return cudaErrorInvalidValue;
 }
 
+#ifndef QPACK_G1_TR
+#define QPACK_G1_TR 4
+#endif
 template <int F>
 static cudaError_t launch_gemv1(const GemvArgs &a, cudaStream_t st) {
-    if (a.K % CHW == 0) return launch_gemv1_k<F, true>(a, st);
-    return launch_gemv1_k<F, false>(a, st);
+    if (a.K % CHW == 0) return launch_gemv1_k<F, QPACK_G1_TR, true>(a, st);
+    return launch_gemv1_k<F, QPACK_G1_TR, false>(a, st);
 }
 
 namespace {
@@ -686,7 +784,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
     if (warp == NCW) {
         const uint64_t pol = l2_evict_first_policy();
         int it = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        bool bad = false;
+        for (int64_t tile = blockIdx.x; tile < ntiles && !bad; tile += gridDim.x) {
             const int64_t r0 = tile * TILE_R;
             const int rows = int(N - r0 < TILE_R ? N - r0 : TILE_R);
             for (int c = 0; c < nchunks; ++c) {
@@ -696,7 +795,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
                     bool ok = true;
                     if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1u);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) { if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_EMPTY); return; }
+                    if (!ok) { if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_EMPTY); bad = true; break; }
                 }
                 int64_t cbytes, sbytes = 0;
                 const int64_t koff = int64_t(c) * CHW;
@@ -724,6 +823,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS)
                              &full[s], pol);
                 }
                 ++it;
+            }
+        }
+        // Drain: wait (bounded) for the last fill of each stage, so the CTA never exits with bulk copies in flight.
+        if (lane == 0) {
+            for (int j = (it > NS ? it - NS : 0); j < it; ++j) {
+                if (!mbar_wait_bounded(&full[j % NS], uint32_t(j / NS) & 1u)) {
+                    atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
+                    break;
+                }
             }
         }
         return;

@@ -43,6 +43,8 @@ struct GemvArgs {
     float *Y;                 // [M, ldy] fp32
     int64_t ldy;
     int M;
+    int weight_prefetch;      // 1: launched as a programmatic dependent of the previous kernel and allowed to
+                              //    stream packed weights before that kernel has finished (caller's opt-in)
 };
 cudaError_t launch_gemv(int fmt, const GemvArgs &a, cudaStream_t s);
 
@@ -66,5 +68,6 @@ cudaError_t fetch_fault_gemv(int32_t *flags);
 cudaError_t fetch_fault_prefill(int32_t *flags);
 
 int num_sms();
+int weight_prefetch_enabled();   // per-device option QPACK_OPT_WEIGHT_PREFETCH
 
 }  // namespace qpack

@@ -153,6 +153,16 @@ const char *qpack_status_string(int status);
  * Returns QPACK_OK or QPACK_ERR_CUDA. A non-zero *flags means some kernel result is invalid. */
 int qpack_fetch_fault_flags(int32_t *flags);
 
+/* Per-device options (the device current at the call).
+ *  QPACK_OPT_WEIGHT_PREFETCH (default 0): when 1, qgemv / qgemm_small launch as programmatic dependents of the
+ *  previous kernel in the stream and start streaming their packed weights before that kernel has finished
+ *  (activations are still read only after it has finished, and outputs written after). The caller guarantees
+ *  that the packed weights and scales of a product are not written by the kernel launched just before it on
+ *  that stream (true for a decode loop over resident weights). Returns QPACK_OK, QPACK_ERR_ARG (unknown
+ *  option) or QPACK_ERR_CUDA (no current device). Host-only. */
+#define QPACK_OPT_WEIGHT_PREFETCH 1
+int qpack_set_option(int option, int value);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int qpack_version(void);
 

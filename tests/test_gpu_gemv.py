@@ -135,3 +135,32 @@ def test_config_q3s_11008(qpg, orc):
     gemv_bound_check(y.cpu().numpy(), y_ref, orc.dequant(orc.Q3S, 11008, 4096, rp, None),
                      x.numpy().astype(np.float64)[None, :])
     assert qpg.qpack_fetch_fault_flags() == 0
+
+
+def test_weight_prefetch_dependent_chain(qpg, orc):
+    """With QPACK_OPT_WEIGHT_PREFETCH each product may stream its weights before the previous kernel ends, but its
+    activations must still come from the finished previous kernel: a chain where every x is produced by the
+    kernel launched just before the product."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt, N, K = qpg.Q3S, 4096, 4096
+    mats = []
+    for i in range(3):
+        W = synth.laplace((N, K), 0.02, 950 + i)
+        rp, rgs, _ = orc.quantize_pack(fmt, W.numpy())
+        mats.append((rp, torch.from_numpy(rp).cuda()))
+    qpg.qpack_set_option(qpg.OPT_WEIGHT_PREFETCH, 1)
+    try:
+        x = synth.normal((K,), 1.0, 960, dtype=torch.float16).cuda()
+        xs, ys = [], []
+        for rp, pd in mats:
+            xs.append(x.clone())
+            y = qpg.qgemv(fmt, pd, None, N, K, x)
+            ys.append(y)
+            x = (y * 0.05).to(torch.float16)          # next activation depends on this product's output
+        torch.cuda.synchronize()
+    finally:
+        qpg.qpack_set_option(qpg.OPT_WEIGHT_PREFETCH, 0)
+    for (rp, _), xin, y in zip(mats, xs, ys):
+        xb = xin.cpu().numpy().view(np.uint16)
+        y_ref = orc.gemv(fmt, N, K, rp, None, xb, nthreads=8)
+        gemv_bound_check(y.cpu().numpy(), y_ref, orc.dequant(fmt, N, K, rp, None), xin.cpu().numpy().astype(np.float64)[None, :])
