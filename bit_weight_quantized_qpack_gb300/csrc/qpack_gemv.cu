@@ -109,28 +109,39 @@ __device__ __forceinline__ void crumb_word(uint32_t c, const uint32_t *xv, int i
         b = fma2h(lop3_and_or(c2, m, MAGIC2), xh(xv, i0 + 4 + k), xh(xv, i0 + 12 + k), b);
     }
 }
-// One 24-bit group v (bits above 23 ignored), code t at bits 3t, weights i0..i0+7.
-// Bit classes: t in {0,3,4,7} at p = 0, {1,5} at p = 3, {2,6} at p = 6.
-__device__ __forceinline__ void tri_group(uint32_t v, const uint32_t *xv, int i0, float &a, float &b) {
-    const uint32_t Y = lop3_sel(v, v << 4, 0x00000FFFu);   // codes 0..3 in the low half, 4..7 in the high half
-    const uint32_t Y9 = Y >> 9;
-    a = fma2h(lop3_and_or(Y, 0x00070007u, MAGIC2), xh(xv, i0 + 0), xh(xv, i0 + 4), a);
-    b = fma2h(lop3_and_or(Y, 0x00380038u, MAGIC2), xh(xv, i0 + 1), xh(xv, i0 + 5), b);
-    a = fma2h(lop3_and_or(Y, 0x01C001C0u, MAGIC2), xh(xv, i0 + 2), xh(xv, i0 + 6), a);
-    b = fma2h(lop3_and_or(Y9, 0x00070007u, MAGIC2), xh(xv, i0 + 3), xh(xv, i0 + 7), b);
+// Two 3-byte code groups (weights 8g..8g+7 and 8g+8..8g+15 of a unit, bytes b0 b1 b2 | b3 b4 b5) spread by three
+// byte permutes: W0 = (b0 b1 | b3 b4), W1 = (b1 b2 | b4 b5), W2 = (b2 b2 | b5 b5). Code t of the first group then
+// sits in the low half and code t of the second group in the high half, both at bit p = 3t mod 8 (t = 0..7 ->
+// p = 0, 3, 6, 1, 4, 7, 2, 5), so one LOP3 per pair yields 1024 + u*2^p in both halves. xv word w0 + t holds the
+// two matching staged activations.
+__device__ __forceinline__ void tri_pair(uint32_t W0, uint32_t W1, uint32_t W2, const uint32_t *xv, int w0, float &acc) {
+    acc = fma2h(lop3_and_or(W0, 0x00070007u, MAGIC2), lo16(xv[w0 + 0]), hi16(xv[w0 + 0]), acc);
+    acc = fma2h(lop3_and_or(W0, 0x00380038u, MAGIC2), lo16(xv[w0 + 1]), hi16(xv[w0 + 1]), acc);
+    acc = fma2h(lop3_and_or(W0, 0x01C001C0u, MAGIC2), lo16(xv[w0 + 2]), hi16(xv[w0 + 2]), acc);
+    acc = fma2h(lop3_and_or(W1, 0x000E000Eu, MAGIC2), lo16(xv[w0 + 3]), hi16(xv[w0 + 3]), acc);
+    acc = fma2h(lop3_and_or(W1, 0x00700070u, MAGIC2), lo16(xv[w0 + 4]), hi16(xv[w0 + 4]), acc);
+    acc = fma2h(lop3_and_or(W1, 0x03800380u, MAGIC2), lo16(xv[w0 + 5]), hi16(xv[w0 + 5]), acc);
+    acc = fma2h(lop3_and_or(W2, 0x001C001Cu, MAGIC2), lo16(xv[w0 + 6]), hi16(xv[w0 + 6]), acc);
+    acc = fma2h(lop3_and_or(W2, 0x00E000E0u, MAGIC2), lo16(xv[w0 + 7]), hi16(xv[w0 + 7]), acc);
 }
 
 // 2^e for a small integer e, exactly (e is a compile-time constant where it is used).
 __host__ __device__ constexpr float pow2f(int e) { return e >= 0 ? float(1u << e) : 1.0f / float(1u << (-e)); }
 
-// Bit-class shift p of element i (0..31) of a unit: the activation it meets is staged as x * 2^-p.
+// Bit-class shift p of staging slot i (0..31) of a unit: the activation in that slot is staged as x * 2^(E - p),
+// E being the vector's scale exponent. Slot i is half (i & 1) of staged word i >> 1. For every format but Q3S slot i
+// holds element i; for Q3S word 8*pi + t holds elements 16*pi + t and 16*pi + 8 + t (see tri_pair).
 template <int F>
 __host__ __device__ constexpr int xshift(int i) {
     if constexpr (F == FMT_Q2S) return 2 * (i & 3);
-    else if constexpr (F == FMT_Q3S) {
-        const int t = i & 7;
-        return (t == 1 || t == 5) ? 3 : ((t == 2 || t == 6) ? 6 : 0);
-    } else return (i & 1) ? 4 : 0;
+    else if constexpr (F == FMT_Q3S) return (3 * ((i >> 1) & 7)) & 7;
+    else return (i & 1) ? 4 : 0;
+}
+// Element (0..15, within a half-unit) staged in half h of word k (0..7) of that half-unit.
+template <int F>
+__host__ __device__ constexpr int slot_elem(int k, int h) {
+    if constexpr (F == FMT_Q3S) return 8 * h + k;
+    else return 2 * k + h;
 }
 
 // Activation constants per unit (XC<F>::n floats), from the staged x' (see the file comment).
@@ -172,11 +183,12 @@ struct LaneGeo {
     uint32_t ubase;      // aligned byte offset of the unit's codes within a row chunk
     int32_t o1, o2, o3;  // format-specific byte offsets relative to ubase
     uint32_t sh0, sh1;   // format-specific shifts
+    uint32_t p0, p1, p2, q0, q1, q2;   // Q3S byte-permute selectors of the two group pairs
 };
 
 template <int F>
 __device__ __forceinline__ LaneGeo lane_geo(int uc) {
-    LaneGeo g = {0u, 0, 0, 0, 0u, 0u};
+    LaneGeo g = {0u, 0, 0, 0, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     const uint32_t sbk = uint32_t(uc) >> 3, su = uint32_t(uc) & 7u;
     if constexpr (F == FMT_Q4G32) {
         g.ubase = 16u * uc;
@@ -185,15 +197,20 @@ __device__ __forceinline__ LaneGeo lane_geo(int uc) {
         g.o1 = int32_t(64u + 2u * su) - int32_t(8u * su);     // L|M bytes of the two sub-blocks
         g.o2 = int32_t(80u) - int32_t(8u * su);               // d, dmin
     } else if constexpr (F == FMT_Q3S) {
-        const uint32_t a = 110u * sbk + 12u * su;             // 2-byte aligned code start
-        g.ubase = a & ~3u;
-        g.sh0 = (a & 3u) * 8u;                                // 0 or 16
+        const uint32_t a = 110u * sbk + 12u * su;             // code start, 2-byte aligned
+        const uint32_t o = a & 3u;                            // 0 or 2
+        g.ubase = a - o;
+        g.o1 = int32_t(4u + 2u * o);                          // word pair holding the second group pair's 6 bytes
         const uint32_t fa = 110u * sbk + 96u + 3u * (su >> 1);
         uint32_t fw = fa & ~3u, fs = 8u * (fa & 3u) + 6u * ((2u * su) & 3u);
         if (fs >= 32u) { fw += 4u; fs -= 32u; }
-        g.o1 = int32_t(fw) - int32_t(g.ubase);                // word pair holding L_j0, L_j0+1 at bits fs..
+        g.o2 = int32_t(fw) - int32_t(g.ubase);                // word pair holding L_j0, L_j0+1 at bits fs..
         g.sh1 = fs;
-        g.o2 = int32_t(110u * sbk + 108u) - int32_t(g.ubase); // d
+        g.o3 = int32_t(110u * sbk + 108u) - int32_t(g.ubase); // d
+        // the first group pair starts at byte o of (w0, w1), the second at byte 2 - o of its word pair
+        const uint32_t s0 = o * 0x1111u, s1 = (2u - o) * 0x1111u;
+        g.p0 = 0x4310u + s0; g.p1 = 0x5421u + s0; g.p2 = 0x5522u + s0;
+        g.q0 = 0x4310u + s1; g.q1 = 0x5421u + s1; g.q2 = 0x5522u + s1;
     } else if constexpr (F == FMT_Q5S) {
         g.ubase = 176u * sbk + 16u * su;
         g.o1 = int32_t(128u + 4u * su) - int32_t(16u * su);   // high-bit plane word
@@ -243,20 +260,18 @@ __device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, cons
         return fmaf(-(Dd.y * M1), c[3], r);
     } else if constexpr (F == FMT_Q3S) {
         const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
-        const uint32_t r0 = wp[0], r1 = wp[1], r2 = wp[2], r3 = wp[3];
-        const uint32_t s0 = __funnelshift_r(r0, r1, g.sh0), s1 = __funnelshift_r(r1, r2, g.sh0),
-                       s2 = __funnelshift_r(r2, r3, g.sh0);
-        const uint32_t *fp = reinterpret_cast<const uint32_t *>(u + g.o1);
+        const uint32_t w0 = wp[0], w1 = wp[1];
+        const uint32_t *qp = reinterpret_cast<const uint32_t *>(u + g.o1);
+        const uint32_t w2 = qp[0], w3 = qp[1];
+        const uint32_t *fp = reinterpret_cast<const uint32_t *>(u + g.o2);
         const uint32_t f = __funnelshift_r(fp[0], fp[1], g.sh1);
         const float L0 = small_int_f(lop3_and_or(f, 63u, MAGICF));
         const float L1 = small_int_f(lop3_and_or(f >> 6, 63u, MAGICF));
-        const float D = hbits(u + g.o2);
-        float a0 = -c[0], b0 = 0.f, a1 = -c[1], b1 = 0.f;
-        tri_group(s0, xv, 0, a0, b0);
-        tri_group(__funnelshift_r(s0, s1, 24), xv, 8, a0, b0);
-        tri_group(__funnelshift_r(s1, s2, 16), xv, 16, a1, b1);
-        tri_group(s2 >> 8, xv, 24, a1, b1);
-        return fmaf(D * L1, a1 + b1, (D * L0) * (a0 + b0));
+        const float D = hbits(u + g.o3);
+        float a0 = -c[0], a1 = -c[1];
+        tri_pair(__byte_perm(w0, w1, g.p0), __byte_perm(w0, w1, g.p1), __byte_perm(w0, w1, g.p2), xv, 0, a0);
+        tri_pair(__byte_perm(w2, w3, g.q0), __byte_perm(w2, w3, g.q1), __byte_perm(w2, w3, g.q2), xv, 8, a1);
+        return fmaf(D * L1, a1, (D * L0) * a0);
     } else if constexpr (F == FMT_Q5S) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
         const uint32_t H = lds32(u + g.o1);
@@ -292,12 +307,21 @@ __device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, cons
     }
 }
 
-// Staged activations: within each 4096-weight chunk c, the 32 halves of unit uc are four 16-byte vectors at
-// vector index (c * 4 + t) * 128 + uc (t = 0..3), so consecutive lanes (consecutive units) read consecutive
-// 16-byte vectors and the four loads of a unit sit at constant 2 KB offsets.
-__device__ __forceinline__ uint32_t xvec_index(uint32_t k8) {   // k8 = element index / 8
-    const uint32_t u = k8 >> 2, t = k8 & 3u;
-    return ((u >> 7) * 4u + t) * 128u + (u & 127u);
+// Staged activations: within each 4096-weight chunk c, the 16 words of unit uc are four 16-byte vectors at vector
+// index (c * 4 + t) * 128 + uc (t = 0..3), so consecutive lanes (consecutive units) read consecutive 16-byte vectors
+// and the four loads of a unit sit at constant 2 KB offsets. Half-unit hh (elements 16 hh .. 16 hh + 15) is words
+// 8 hh .. 8 hh + 7, i.e. vectors t = 2 hh and 2 hh + 1.
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }   // -126 <= e <= 127
+
+// Stage one half-unit: xr = its 16 raw fp16 activations in element order, E = the vector's scale exponent.
+template <int F>
+__device__ __forceinline__ void stage_half_unit(const uint16_t *xr, int E, uint32_t w[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float f0 = h2f_bits(xr[slot_elem<F>(k, 0)]) * exp2i(E - xshift<F>(2 * k));
+        const float f1 = h2f_bits(xr[slot_elem<F>(k, 1)]) * exp2i(E - xshift<F>(2 * k + 1));
+        w[k] = uint32_t(f2h_bits(f0)) | (uint32_t(f2h_bits(f1)) << 16);
+    }
 }
 __device__ __forceinline__ void load_xp(const uint16_t *xs, uint32_t c, uint32_t uc, uint32_t xv[16]) {
     const uint4 *p = reinterpret_cast<const uint4 *>(xs) + c * 512u + uc;
@@ -318,19 +342,42 @@ template <int F, int NS, int NG, int TR>
 struct G1Layout {
     static constexpr int CW = 8 * NG;                  // consumer warps
     static constexpr int THREADS = (CW + 1) * 32;
-    static constexpr int NSLOT = NS + 2;
+    static constexpr int NSLOT = NS + 2;               // per-tile reduction slots (tiles in flight <= NS + 1)
     static constexpr int RPL = TR / 2;                 // rows per lane (rows rlo, rlo + 2, ...)
-    static constexpr int RED_PER_WARP = 4 * RPL;       // 4 partials per row per warp
-    static constexpr int RED_PER_SLOT = CW * RED_PER_WARP;
+    static constexpr int RED_PER_SLOT = NG * 8 * RPL;  // one partial per (group, warp, lane row)
     static constexpr int STAGE = TR * (Geo<F>::chunk_bytes + Geo<F>::scale_bytes);
     static __host__ __device__ uint32_t bar_bytes() { return uint32_t(round_up(16 * NS, 128)); }
-    static __host__ __device__ uint32_t red_bytes() { return uint32_t(round_up(NSLOT * 4 + NSLOT * RED_PER_SLOT * 4, 128)); }
+    static __host__ __device__ uint32_t red_bytes() {
+        return uint32_t(round_up(16 + NSLOT * 4 + NSLOT * RED_PER_SLOT * 4, 128));
+    }
     static __host__ __device__ uint32_t x_bytes(uint32_t K) { return uint32_t(round_up(int64_t((K + CHW - 1) / CHW) * CHW * 2, 128)); }
     static __host__ __device__ uint32_t c_bytes(uint32_t K) { return uint32_t(round_up(4 * int64_t(K / 32) * XC<F>::n, 128)); }
+    // + 32: the Q3S unpack reads the word pair holding a unit's scale fields, up to 4 bytes past its row chunk
     static __host__ __device__ uint32_t total(uint32_t K) {
         return bar_bytes() + red_bytes() + x_bytes(K) + c_bytes(K) + uint32_t(NS) * STAGE + 32;
     }
 };
+
+// Sum R per-lane values over the warp, one value per row: after the call, lanes j * (32 / R) (j < R) hold the warp
+// sum of v[j]. log2(R) transposing exchanges, then a butterfly inside each group of 32 / R lanes.
+template <int R>
+__device__ __forceinline__ float warp_rows_sum(float (&v)[R], int lane) {
+    int off = 16;
+#pragma unroll
+    for (int n = R; n > 1; n >>= 1, off >>= 1) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int k = 0; k < n / 2; ++k) {
+            const float keep = up ? v[k + n / 2] : v[k];
+            const float send = up ? v[k] : v[k + n / 2];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = off; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
 
 template <int F, int NS, int NG, int TR, bool FULLK>
 __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_kernel(GemvArgs a) {
@@ -343,10 +390,14 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
     constexpr uint32_t NSG = uint32_t(NS / NG);       // stages per consumer group
     static_assert(NS % NG == 0, "each consumer group owns NS / NG stages");
     static_assert(NG * TR <= 32, "producer lanes: TR per group");
+    static_assert(RPL >= 1 && (RPL & (RPL - 1)) == 0 && RPL <= 8, "rows per lane: a power of two");
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t N = uint32_t(a.N), K = uint32_t(a.K);
-    const uint32_t ntiles = (N + TR - 1) / TR;
+    // this CTA's rows: a contiguous range, the row counts of any two CTAs differ by at most one
+    const uint32_t rq = N / gridDim.x, rm = N % gridDim.x, b = blockIdx.x;
+    const uint32_t rbeg = b * rq + min(b, rm), rend = rbeg + rq + (b < rm ? 1u : 0u);
+    const uint32_t ntl = (rend - rbeg + TR - 1) / TR;  // row tiles of this CTA (the last one may be ragged)
     const uint32_t nch = (K + CHW - 1) / CHW;
     const uint32_t U = K / 32;                        // units per row
 
@@ -354,8 +405,9 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
     uint64_t *full = reinterpret_cast<uint64_t *>(p);
     uint64_t *empty = full + NS;
     p += LY::bar_bytes();
-    int *cnt = reinterpret_cast<int *>(p);
-    float *red = reinterpret_cast<float *>(p + NSLOT * 4);
+    int *misc = reinterpret_cast<int *>(p);           // [0]: max |x| as float bits
+    int *cnt = misc + 4;
+    float *red = reinterpret_cast<float *>(p + 16 + NSLOT * 4);
     p += LY::red_bytes();
     uint16_t *xs = reinterpret_cast<uint16_t *>(p);
     p += LY::x_bytes(K);
@@ -366,6 +418,7 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 8); }
         for (int s = 0; s < NSLOT; ++s) cnt[s] = 0;
+        misc[0] = 0;
         fence_mbar_init();
     }
     pdl_launch_dependents();     // the next product may begin launching; it still waits for us before reading
@@ -373,14 +426,14 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
 
     if (warp == CW) {
         // ------------------------------------ producer ------------------------------------
-        // Group g owns the private sub-ring of stages [g*NSG, (g+1)*NSG) and consumes its k-th item from stage
-        // g*NSG + k mod NSG, so every mbarrier is waited on only by the one group that consumed its previous phase
-        // (a parity wait is only meaningful one phase ahead). Producer lanes g*TR .. g*TR+TR-1 serve group g: lane
-        // r copies row r of the tile (bulk copies issued by one thread are processed one after another, so rows go
-        // out from different lanes), or lane 0 copies the whole tile when its rows are contiguous.
-        // The lanes advance in rounds (round k = every group's k-th item), and a round starts only once every
-        // group has released the stage it reuses, so no group runs more than NSG rounds ahead of another: the
-        // per-tile reduction slots, reused every NSLOT = NS + 2 tiles, depend on that bound.
+        // Item i of this CTA is (local tile i / nch, chunk i mod nch); group g consumes items g, g + NG, ... from
+        // its private sub-ring of stages [g*NSG, (g+1)*NSG), so every mbarrier is waited on only by the one group
+        // that consumed its previous phase (a parity wait is only meaningful one phase ahead). Producer lanes
+        // g*TR .. g*TR+TR-1 serve group g: lane r copies row r of the tile (bulk copies issued by one thread are
+        // processed one after another, so rows go out from different lanes), or lane 0 copies the whole tile when
+        // its rows are contiguous. The lanes advance in rounds (round k = every group's k-th item), and a round
+        // starts only once every group has released the stage it reuses, so no group runs more than NSG rounds
+        // ahead of another: the per-tile reduction slots, reused every NSLOT = NS + 2 tiles, depend on that bound.
         constexpr uint32_t PMASK = (NG * TR >= 32) ? 0xffffffffu : ((1u << (NG * TR)) - 1u);
         const int pg = lane / TR, pr = lane % TR;
         if (pg < NG) {
@@ -389,10 +442,10 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
             if (!a.weight_prefetch) pdl_wait();
             const uint64_t pol = l2_evict_first_policy();
             const bool whole_rows = (K == uint32_t(CHW));        // a tile of whole rows is one contiguous range
-            uint32_t k = 0, issued = 0, c = uint32_t(pg), tile = blockIdx.x;
-            while (c >= nch) { c -= nch; tile += gridDim.x; }
+            uint32_t k = 0, issued = 0, c = uint32_t(pg), lt = 0;
+            while (c >= nch) { c -= nch; ++lt; }
             while (true) {
-                const bool have = tile < ntiles;
+                const bool have = lt < ntl;
                 if (!__any_sync(PMASK, have)) break;
                 const uint32_t s = uint32_t(pg) * NSG + k % NSG, ph = (k / NSG) & 1u;
                 bool bad = false;
@@ -403,8 +456,8 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
                     bad = true;
                 }
                 if (__any_sync(PMASK, bad)) break;
-                const uint32_t r0 = tile * TR;
-                const uint32_t rows = have ? min(uint32_t(TR), N - r0) : 0u;
+                const uint32_t r0 = rbeg + lt * TR;
+                const uint32_t rows = have ? min(uint32_t(TR), rend - r0) : 0u;
                 const uint32_t koff = c * CHW;
                 uint32_t cbytes, sbytes = 0;
                 if constexpr (Fmt<F>::sb) {
@@ -437,7 +490,7 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
                 }
                 ++k;
                 c += NG;
-                while (c >= nch) { c -= nch; tile += gridDim.x; }
+                while (c >= nch) { c -= nch; ++lt; }
             }
             // Drain: wait (bounded) until the last fill of each of the group's stages has landed, so the CTA never
             // exits with bulk copies still writing its shared memory (consumers that gave up may exit early).
@@ -455,21 +508,36 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
 
     // -------------------------------------- consumers --------------------------------------
     pdl_wait();                  // x (and y) may belong to the previous grid
+    int E;                       // scale exponent: activations are staged as x * 2^E, with max |x| * 2^E in [2^14, 2^15)
     {
-        // stage x' = fp16(x * 2^-p) in the chunk-major vector layout, then the per-unit constants
         const uint4 *xg = reinterpret_cast<const uint4 *>(a.X);
-        uint4 *xd = reinterpret_cast<uint4 *>(xs);
+        // pass 1: max |x| over the whole vector (fp16 magnitudes order like their bit patterns)
+        uint32_t m = 0;
         for (uint32_t v = tid; v < K / 8; v += CW * 32) {
-            const uint4 raw = xg[v];
-            uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            const uint4 raw = __ldg(xg + v);
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                // element 8t + 2e (+1): the class depends only on the index mod 8
-                const float f0 = h2f_bits(lo16(w[e])) * pow2f(-xshift<F>(2 * e));
-                const float f1 = h2f_bits(hi16(w[e])) * pow2f(-xshift<F>(2 * e + 1));
-                w[e] = uint32_t(f2h_bits(f0)) | (uint32_t(f2h_bits(f1)) << 16);
-            }
-            xd[xvec_index(v)] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int e = 0; e < 4; ++e) m = max(m, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) atomicMax(misc, int(m));
+        named_bar_sync(1, CW * 32);
+        const float xm = h2f_bits(uint16_t(min(uint32_t(misc[0]), 0x7BFFu)));   // inf / nan inputs: clamp the exponent
+        E = (xm > 0.f) ? 14 - (int((__float_as_uint(xm) >> 23) & 255u) - 127) : 0;
+        // pass 2: stage x' = fp16(x * 2^(E - p)) half-unit by half-unit (16 activations, 8 words, 2 vectors)
+        uint4 *xd = reinterpret_cast<uint4 *>(xs);
+        for (uint32_t h = tid; h < K / 16; h += CW * 32) {
+            const uint4 r0 = __ldg(xg + 2 * h), r1 = __ldg(xg + 2 * h + 1);
+            const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+            uint16_t xr[16];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { xr[2 * e] = lo16(rw[e]); xr[2 * e + 1] = hi16(rw[e]); }
+            uint32_t w[8];
+            stage_half_unit<F>(xr, E, w);
+            const uint32_t u = h >> 1, hh = h & 1u, cc = u >> 7, uu = u & 127u;
+            xd[(cc * 4 + 2 * hh) * 128 + uu] = make_uint4(w[0], w[1], w[2], w[3]);
+            xd[(cc * 4 + 2 * hh + 1) * 128 + uu] = make_uint4(w[4], w[5], w[6], w[7]);
         }
         named_bar_sync(1, CW * 32);
         for (uint32_t u = tid; u < U; u += CW * 32) {
@@ -485,6 +553,7 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
         }
         named_bar_sync(1, CW * 32);
     }
+    const float unscale = exp2i(-E);
     const uint32_t group = uint32_t(warp) >> 3, wg = uint32_t(warp) & 7u;
     const uint32_t gl = wg * 32u + uint32_t(lane);
     const int uc = int(gl & 127u);
@@ -493,16 +562,16 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
     const uint32_t uoff0 = rlo * uint32_t(G::chunk_bytes) + geo.ubase;
     const uint32_t soff0 = TR * uint32_t(G::chunk_bytes) + rlo * uint32_t(G::scale_bytes) + 4u * uint32_t(uc);
 
-    // own items: the group's k-th item is global item group + NG*k, in stage group*NSG + k mod NSG
+    // own items: the group's k-th item is item group + NG*k, in stage group*NSG + k mod NSG
     uint32_t sl = 0, ph = 0;
-    uint32_t tile = blockIdx.x, c = group, ib = 0, slot = 0;   // ib = item index of the tile's first chunk
-    while (c >= nch && tile < ntiles) { c -= nch; tile += gridDim.x; ib += nch; if (++slot == uint32_t(NSLOT)) slot = 0; }
+    uint32_t lt = 0, c = group, ib = 0, slot = 0;      // ib = item index of the tile's first chunk
+    while (c >= nch && lt < ntl) { c -= nch; ++lt; ib += nch; if (++slot == uint32_t(NSLOT)) slot = 0; }
     bool dead = false;
     float acc[RPL];
 #pragma unroll
     for (int j = 0; j < RPL; ++j) acc[j] = 0.f;
-    while (tile < ntiles) {
-        const uint32_t r0 = tile * TR;
+    while (lt < ntl) {
+        const uint32_t r0 = rbeg + lt * TR;
         const uint32_t s = group * NSG + sl;
         if (!dead && !mbar_wait_bounded(&full[s], ph)) {
             if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
@@ -532,18 +601,11 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
             }
         }
         if (c + NG >= nch) {
-            // this group's last item of the tile. Per pair of the lane's rows, a partial butterfly: lanes 0..15
-            // carry the first row, 16..31 the second; after three steps lanes {0..3} / {16..19} hold 4 partials.
-            float *rs = red + slot * LY::RED_PER_SLOT + warp * LY::RED_PER_WARP;
-            const bool up = (lane & 16) != 0;
-#pragma unroll
-            for (int pr = 0; pr < RPL / 2; ++pr) {
-                float v = up ? acc[2 * pr + 1] : acc[2 * pr];
-                v += __shfl_xor_sync(0xffffffffu, up ? acc[2 * pr] : acc[2 * pr + 1], 16);
-                v += __shfl_xor_sync(0xffffffffu, v, 8);
-                v += __shfl_xor_sync(0xffffffffu, v, 4);
-                if ((lane & 12) == 0) rs[pr * 8 + (lane >> 4) * 4 + (lane & 3)] = v;
-            }
+            // this group's last item of the tile: one value per (warp, row) into the tile's slot, then a counter;
+            // the warp completing the count sums the tile's partials in a fixed order and writes y.
+            const float v = warp_rows_sum<RPL>(acc, lane);
+            float *rs = red + slot * LY::RED_PER_SLOT + (group * 8 + wg) * RPL;
+            if ((lane & (32 / RPL - 1)) == 0) rs[lane / (32 / RPL)] = v;
             __syncwarp();
             int last = 0;
             if (lane == 0) {
@@ -554,31 +616,25 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
             }
             last = __shfl_sync(0xffffffffu, last, 0);
             if (last) {
-                // output row rho = lane / LPR; lane j = lane % LPR sums every LPR-th partial of that row
-                constexpr int LPR = 32 / TR;
-                const int rho = lane / LPR, j = lane % LPR;
-                const int hf = rho & 1, jr = rho >> 1, pr = jr >> 1, jj = jr & 1;
-                const float *slot_base = red + slot * LY::RED_PER_SLOT;
-                float yv = 0.f;
+                // lane r < TR: tile row r = 2 j + rl, summed over the four warps holding rows of parity rl in every
+                // contributing group
+                if (lane < TR) {
+                    const int rl = lane & 1, j = lane >> 1;
+                    const float *sb = red + slot * LY::RED_PER_SLOT;
+                    float yv = 0.f;
 #pragma unroll
-                for (int gr = 0; gr < NG; ++gr) {
-                    bool contributed = nch >= uint32_t(NG);
-                    if (!contributed) {
-                        for (uint32_t cc = 0; cc < nch; ++cc) contributed |= ((ib + cc) % NG) == uint32_t(gr);
-                    }
-                    if (contributed) {
+                    for (int gr = 0; gr < NG; ++gr) {
+                        bool contributed = nch >= uint32_t(NG);
+                        if (!contributed) {
+                            for (uint32_t cc = 0; cc < nch; ++cc) contributed |= ((ib + cc) % NG) == uint32_t(gr);
+                        }
+                        if (contributed) {
 #pragma unroll
-                        for (int idx = 0; idx < 16; ++idx) {
-                            if (idx % LPR == j) {
-                                const int q = idx >> 2, e = idx & 3;
-                                yv += slot_base[(gr * 8 + hf * 4 + q) * LY::RED_PER_WARP + pr * 8 + jj * 4 + e];
-                            }
+                            for (int q = 0; q < 4; ++q) yv += sb[(gr * 8 + 4 * rl + q) * RPL + j];
                         }
                     }
+                    if (r0 + uint32_t(lane) < rend) a.Y[r0 + lane] = yv * unscale;
                 }
-#pragma unroll
-                for (int o = LPR / 2; o > 0; o >>= 1) yv += __shfl_xor_sync(0xffffffffu, yv, o);
-                if (j == 0 && r0 + rho < N) a.Y[r0 + rho] = yv;
                 __syncwarp();
                 if (lane == 0) cnt[slot] = 0;
             }
@@ -587,11 +643,11 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (++sl == uint32_t(NSG)) { sl = 0; ph ^= 1u; }
+        if (++sl == NSG) { sl = 0; ph ^= 1u; }
         c += NG;
         while (c >= nch) {
             c -= nch;
-            tile += gridDim.x;
+            ++lt;
             ib += nch;
             if (++slot == uint32_t(NSLOT)) slot = 0;
         }
@@ -614,9 +670,8 @@ static cudaError_t try_launch_gemv1(const GemvArgs &a, cudaStream_t st, bool *la
         if (e != cudaSuccess) return e;
         opted[dev] = 1;
     }
-    const int64_t ntiles = (a.N + TR - 1) / TR;
     int grid = num_sms();
-    if (ntiles < grid) grid = int(ntiles);
+    if (a.N < grid) grid = int(a.N);                   // every CTA gets at least one row
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
     cfg.blockDim = dim3(unsigned(LY::THREADS));
@@ -631,22 +686,18 @@ static cudaError_t try_launch_gemv1(const GemvArgs &a, cudaStream_t st, bool *la
     return cudaLaunchKernelEx(&cfg, gemv1_kernel<F, NS, NG, TR, FULLK>, a);
 }
 
-
+// Largest ring (a multiple of G1_NG stages, so every group owns the same number) that fits beside the staged
+// activations; about 200 KB of stages keeps far more bytes in flight per SM than the memory latency needs.
 template <int F, int TR, bool FULLK>
 static cudaError_t launch_gemv1_k(const GemvArgs &a, cudaStream_t st) {
     bool done = false;
     cudaError_t e;
-    constexpr int SB = G1Layout<F, 4, G1_NG, TR>::STAGE;
-    // stage counts are multiples of G1_NG (private sub-rings); the largest ring that fits (with x and constants)
-    if (SB * 24 <= 176 * 1024) {
-        e = try_launch_gemv1<F, 24, G1_NG, TR, FULLK>(a, st, &done);
+    constexpr int SB = G1Layout<F, 3, G1_NG, TR>::STAGE;
+    if constexpr (SB * 15 <= 200 * 1024) {
+        e = try_launch_gemv1<F, 15, G1_NG, TR, FULLK>(a, st, &done);
         if (e != cudaSuccess || done) return e;
     }
-    if (SB * 18 <= 176 * 1024) {
-        e = try_launch_gemv1<F, 18, G1_NG, TR, FULLK>(a, st, &done);
-        if (e != cudaSuccess || done) return e;
-    }
-    if (SB * 12 <= 192 * 1024) {
+    if constexpr (SB * 12 <= 200 * 1024) {
         e = try_launch_gemv1<F, 12, G1_NG, TR, FULLK>(a, st, &done);
         if (e != cudaSuccess || done) return e;
     }
@@ -654,11 +705,13 @@ static cudaError_t launch_gemv1_k(const GemvArgs &a, cudaStream_t st) {
     if (e != cudaSuccess || done) return e;
     e = try_launch_gemv1<F, 6, G1_NG, TR, FULLK>(a, st, &done);
     if (e != cudaSuccess || done) return e;
+    e = try_launch_gemv1<F, 3, G1_NG, TR, FULLK>(a, st, &done);
+    if (e != cudaSuccess || done) return e;
     return cudaErrorInvalidValue;
 }
 
 #ifndef QPACK_G1_TR
-#define QPACK_G1_TR 4
+#define QPACK_G1_TR 8
 #endif
 template <int F>
 static cudaError_t launch_gemv1(const GemvArgs &a, cudaStream_t st) {

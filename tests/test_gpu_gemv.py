@@ -62,6 +62,43 @@ def test_gemv_one_hot_columns(qpg, orc, name):
 
 
 @pytest.mark.parametrize("name", ALL)
+def test_gemv_tiny_and_mixed_magnitude_activations(qpg, orc, name):
+    """The bound scales with ||x||, so it must hold for activations near the fp16 subnormal range and for vectors
+    whose entries span many binades (the staged activations are rescaled by a power of two per vector)."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    N, K = 19, 4096 + 512
+    rp, rgs = case(orc, fmt, N, K, 620)
+    deq = orc.dequant(fmt, N, K, rp, rgs)
+    base = synth.normal((K,), 1.0, 621)
+    mixed = base.clone()
+    mixed[::7] *= 1e-4
+    mixed[::11] *= 300.0
+    for x32 in (base * 1e-5, base * 3e-7, mixed):
+        x = x32.to(torch.float16)
+        y = run_gemv(qpg, fmt, rp, rgs, N, K, x)
+        y_ref = orc.gemv(fmt, N, K, rp, rgs, x.numpy().view(np.uint16))
+        gemv_bound_check(y, y_ref, deq, x.numpy().astype(np.float64)[None, :])
+    y = run_gemv(qpg, fmt, rp, rgs, N, K, torch.zeros(K, dtype=torch.float16))
+    assert np.all(y == 0.0)
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_gemv_rows_spread_over_all_sms(qpg, orc, name):
+    """More rows than SMs but not a multiple of the tile: every CTA ends its row range with a ragged tile."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    N, K = 1000, 4096
+    rp, rgs = case(orc, fmt, N, K, 640)
+    x = synth.normal((K,), 1.0, 641, dtype=torch.float16)
+    y = run_gemv(qpg, fmt, rp, rgs, N, K, x)
+    y_ref = orc.gemv(fmt, N, K, rp, rgs, x.numpy().view(np.uint16))
+    deq = orc.dequant(fmt, N, K, rp, rgs)
+    gemv_bound_check(y, y_ref, deq, x.numpy().astype(np.float64)[None, :])
+    assert qpg.qpack_fetch_fault_flags() == 0
+
+
+@pytest.mark.parametrize("name", ALL)
 def test_gemv_large_activations_and_zero_rows(qpg, orc, name):
     from bit_weight_quantized_qpack_gb300 import synth
     fmt = qpg.FORMATS[name]
