@@ -228,55 +228,71 @@ __device__ __forceinline__ LaneGeo lane_geo(int uc) {
     return g;
 }
 
-// sum_i w'_i x_i over one 32-weight unit of one row; `u` = aligned unit base in shared memory, `sp` = this
-// row's group-scale pointer (Q4G32), `c` = the unit's activation constants, `xv` = its staged activations.
-// Each sub-block accumulator starts at -C (the activation constant), so no separate subtraction is needed.
+// fp16 pair arithmetic on raw bits: the two halves of a + b (each rounded; exact for the small integers used here).
+__device__ __forceinline__ uint32_t hadd2_bits(uint32_t a, uint32_t b) {
+    const __half2 r = __hadd2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t lop3_xor_or(uint32_t a, uint32_t b, uint32_t c) {
+    // (a ^ b) | c in one LOP3 (truth table 0xBE)
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xBE;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+constexpr uint32_t HNEG1024 = 0xE400E400u;   // fp16 -1024 in both halves
+constexpr uint32_t HNEG1152 = 0xE480E480u;   // fp16 -1152 = -(1024 + 128) in both halves
+
+// acc += sum_i w'_i x_i over one 32-weight unit of one row when `on`, else acc is left unchanged; `u` = aligned unit
+// base in shared memory, `sp` = this row's group-scale pointer (Q4G32), `c` = the unit's activation constants,
+// `xv` = its staged activations. Each sub-block accumulator starts at -C (the activation constant), so no separate
+// subtraction is needed. Sub-block scale integers are turned into exact fp16 values with the 1024 mantissa trick and
+// multiplied by the raw fp16 super-block scale with exact fp16 x fp16 -> fp32 products; masking zeroes that scale.
 template <int F>
-__device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, const LaneGeo &g, const float *c,
-                                         const uint32_t *xv) {
+__device__ __forceinline__ void row_acc(const uint8_t *u, const float *sp, const LaneGeo &g, const float *c,
+                                        const uint32_t *xv, bool on, float &acc) {
     if constexpr (F == FMT_Q4G32) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
+        const float s = on ? sp[0] : 0.f;
         float a = -c[0], b = 0.f;
         nib_word(w.x, xv, 0, a, b);
         nib_word(w.y, xv, 8, a, b);
         nib_word(w.z, xv, 16, a, b);
         nib_word(w.w, xv, 24, a, b);
-        return sp[0] * (a + b);
+        acc = fmaf(s, a + b, acc);
     } else if constexpr (F == FMT_Q2S) {
         const uint32_t w0 = lds32(u), w1 = lds32(u + 4);
-        const uint32_t dd = lds32(u + g.o2);
-        const float2 Dd = __half22float2(*reinterpret_cast<const __half2 *>(&dd));
+        const uint32_t dd = on ? lds32(u + g.o2) : 0u;                   // d (low half), dmin (high half)
         const uint32_t lm = *reinterpret_cast<const uint16_t *>(u + g.o1);
-        const float L0 = small_int_f(lop3_and_or(lm, 0xFu, MAGICF));
-        const float M0 = small_int_f(lop3_and_or(lm >> 4, 0xFu, MAGICF));
-        const float L1 = small_int_f(lop3_and_or(lm >> 8, 0xFu, MAGICF));
-        const float M1 = small_int_f(lop3_and_or(lm >> 12, 0xFu, MAGICF));
+        const uint32_t t = __byte_perm(lm, 0u, 0x4140u);                 // L0 | M0 << 4 at byte 0, L1 | M1 << 4 at byte 2
+        const uint32_t hl = hadd2_bits(lop3_and_or(t, 0x000F000Fu, MAGIC2), HNEG1024);        // (L0, L1)
+        const uint32_t hm = hadd2_bits(lop3_and_or(t >> 4, 0x000F000Fu, MAGIC2), HNEG1024);   // (M0, M1)
         float a0 = -c[0], b0 = 0.f, a1 = -c[2], b1 = 0.f;
         crumb_word(w0, xv, 0, a0, b0);
         crumb_word(w1, xv, 16, a1, b1);
-        float r = (Dd.x * L0) * (a0 + b0);
-        r = fmaf(Dd.x * L1, a1 + b1, r);
-        r = fmaf(-(Dd.y * M0), c[1], r);
-        return fmaf(-(Dd.y * M1), c[3], r);
+        acc = fmaf(fma_h(lo16(hl), lo16(dd), 0.f), a0 + b0, acc);
+        acc = fmaf(fma_h(hi16(hl), lo16(dd), 0.f), a1 + b1, acc);
+        acc = fmaf(-fma_h(lo16(hm), hi16(dd), 0.f), c[1], acc);
+        acc = fmaf(-fma_h(hi16(hm), hi16(dd), 0.f), c[3], acc);
     } else if constexpr (F == FMT_Q3S) {
         const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
         const uint32_t w0 = wp[0], w1 = wp[1];
         const uint32_t *qp = reinterpret_cast<const uint32_t *>(u + g.o1);
         const uint32_t w2 = qp[0], w3 = qp[1];
         const uint32_t *fp = reinterpret_cast<const uint32_t *>(u + g.o2);
-        const uint32_t f = __funnelshift_r(fp[0], fp[1], g.sh1);
-        const float L0 = small_int_f(lop3_and_or(f, 63u, MAGICF));
-        const float L1 = small_int_f(lop3_and_or(f >> 6, 63u, MAGICF));
-        const float D = hbits(u + g.o3);
+        const uint32_t f = __funnelshift_r(fp[0], fp[1], g.sh1);          // L_j0 at bits 0..5, L_j0+1 at bits 6..11
+        const uint32_t lh = hadd2_bits(lop3_and_or(lop3_sel(f << 10, f, 0xFFFF0000u), 0x003F003Fu, MAGIC2), HNEG1024);
+        const uint16_t D = on ? *reinterpret_cast<const uint16_t *>(u + g.o3) : uint16_t(0);
         float a0 = -c[0], a1 = -c[1];
         tri_pair(__byte_perm(w0, w1, g.p0), __byte_perm(w0, w1, g.p1), __byte_perm(w0, w1, g.p2), xv, 0, a0);
         tri_pair(__byte_perm(w2, w3, g.q0), __byte_perm(w2, w3, g.q1), __byte_perm(w2, w3, g.q2), xv, 8, a1);
-        return fmaf(D * L1, a1, (D * L0) * a0);
+        acc = fmaf(fma_h(lo16(lh), D, 0.f), a0, acc);
+        acc = fmaf(fma_h(hi16(lh), D, 0.f), a1, acc);
     } else if constexpr (F == FMT_Q5S) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
         const uint32_t H = lds32(u + g.o1);
         const uint4 fld = *reinterpret_cast<const uint4 *>(u + g.o2);
-        const float2 Dd = __half22float2(*reinterpret_cast<const __half2 *>(&fld.w));
+        const uint32_t ddw = on ? fld.w : 0u;
+        const float2 Dd = __half22float2(*reinterpret_cast<const __half2 *>(&ddw));
         const uint64_t lo64 = (uint64_t(fld.y) << 32) | fld.x, hi64 = (uint64_t(fld.z) << 32) | fld.y;
         const float L = small_int_f(lop3_and_or(uint32_t(lo64 >> g.sh0), 63u, MAGICF));
         const float M = small_int_f(lop3_and_or(uint32_t(hi64 >> (g.sh1 - 32u)), 63u, MAGICF));
@@ -285,7 +301,8 @@ __device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, cons
         nib_word_hi<1>(w.y, lop3_sel(H >> 8, H << 4, 0x0000FFFFu), xv, 8, a, b);
         nib_word_hi<1>(w.z, lop3_sel(H >> 16, H >> 4, 0x0000FFFFu), xv, 16, a, b);
         nib_word_hi<1>(w.w, lop3_sel(H >> 24, H >> 12, 0x0000FFFFu), xv, 24, a, b);
-        return fmaf(Dd.x * L, a + b, -(Dd.y * M) * c[1]);
+        acc = fmaf(Dd.x * L, a + b, acc);
+        acc = fmaf(-(Dd.y * M), c[1], acc);
     } else {
         const uint32_t sh = g.sh0;
         const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
@@ -294,23 +311,22 @@ __device__ __forceinline__ float row_dot(const uint8_t *u, const float *sp, cons
         const uint32_t q0 = hp[0], q1 = hp[1], q2 = hp[2];
         const uint32_t h0 = __funnelshift_r(q0, q1, sh), h1 = __funnelshift_r(q1, q2, sh);
         const uint32_t lv = *reinterpret_cast<const uint16_t *>(u + g.o2);
-        // int8 -> float exactly: (b ^ 0x80) | 2^23 as fp32, minus 2^23 + 128
-        const float L0 = __uint_as_float((lv & 0xFFu) ^ (MAGICF | 0x80u)) - 8388736.0f;
-        const float L1 = __uint_as_float(((lv >> 8) & 0xFFu) ^ (MAGICF | 0x80u)) - 8388736.0f;
-        const float D = hbits(u + g.o3);
+        // int8 pair -> exact fp16 pair: (b ^ 0x80) in the mantissa of 1024, minus 1024 + 128
+        const uint32_t lh = hadd2_bits(lop3_xor_or(__byte_perm(lv, 0u, 0x4140u), 0x00800080u, MAGIC2), HNEG1152);
+        const uint16_t D = on ? *reinterpret_cast<const uint16_t *>(u + g.o3) : uint16_t(0);
         float a0 = -c[0], b0 = 0.f, a1 = -c[1], b1 = 0.f;
         nib_word_hi<2>(__funnelshift_r(r0, r1, sh), __byte_perm(h0, 0u, 0x4140u), xv, 0, a0, b0);
         nib_word_hi<2>(__funnelshift_r(r1, r2, sh), __byte_perm(h0, 0u, 0x4342u), xv, 8, a0, b0);
         nib_word_hi<2>(__funnelshift_r(r2, r3, sh), __byte_perm(h1, 0u, 0x4140u), xv, 16, a1, b1);
         nib_word_hi<2>(__funnelshift_r(r3, r4, sh), __byte_perm(h1, 0u, 0x4342u), xv, 24, a1, b1);
-        return fmaf(D * L1, a1 + b1, (D * L0) * (a0 + b0));
+        acc = fmaf(fma_h(lo16(lh), D, 0.f), a0 + b0, acc);
+        acc = fmaf(fma_h(hi16(lh), D, 0.f), a1 + b1, acc);
     }
 }
 
-// Staged activations: within each 4096-weight chunk c, the 16 words of unit uc are four 16-byte vectors at vector
-// index (c * 4 + t) * 128 + uc (t = 0..3), so consecutive lanes (consecutive units) read consecutive 16-byte vectors
-// and the four loads of a unit sit at constant 2 KB offsets. Half-unit hh (elements 16 hh .. 16 hh + 15) is words
-// 8 hh .. 8 hh + 7, i.e. vectors t = 2 hh and 2 hh + 1.
+// Staged activations: the 16 words of unit u are four 16-byte vectors at vector index t * U + u (t = 0..3, U = K / 32
+// units per row), so consecutive lanes (consecutive units) read consecutive vectors. Half-unit hh (elements
+// 16 hh .. 16 hh + 15) is words 8 hh .. 8 hh + 7, i.e. vectors t = 2 hh and 2 hh + 1.
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }   // -126 <= e <= 127
 
 // Stage one half-unit: xr = its 16 raw fp16 activations in element order, E = the vector's scale exponent.
@@ -323,40 +339,38 @@ __device__ __forceinline__ void stage_half_unit(const uint16_t *xr, int E, uint3
         w[k] = uint32_t(f2h_bits(f0)) | (uint32_t(f2h_bits(f1)) << 16);
     }
 }
-__device__ __forceinline__ void load_xp(const uint16_t *xs, uint32_t c, uint32_t uc, uint32_t xv[16]) {
-    const uint4 *p = reinterpret_cast<const uint4 *>(xs) + c * 512u + uc;
+__device__ __forceinline__ void load_xp(const uint4 *xs, uint32_t U, uint32_t u, uint32_t xv[16]) {
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-        const uint4 v = p[t * 128];
+        const uint4 v = xs[t * U + u];
         xv[4 * t] = v.x; xv[4 * t + 1] = v.y; xv[4 * t + 2] = v.z; xv[4 * t + 3] = v.w;
     }
 }
+// Bytes of one unit position step (32 units) of a row: unit u + 32 lies 4 super-blocks (1024 weights) further on,
+// at the same offsets within its super-block, so a lane's unit geometry is computed once.
+template <int F>
+__host__ __device__ constexpr uint32_t step_bytes() { return Fmt<F>::sb ? 4u * Fmt<F>::bytes : 512u; }
 
 }  // namespace
 
 // ------------------------------------------------------------------------------------------------------------
-// Batch-1 fused dequant-GEMV kernel: NG consumer groups of 8 warps + 1 producer warp (TR lanes per group).
+// Batch-1 fused dequant-GEMV kernel.
+//
+// One CTA per SM, sized so that two fit on an SM (the next product in the stream, launched as a programmatic
+// dependent, starts streaming its weights while this one finishes). Warp 8 is the producer: its lane 0 copies
+// stages of SR = RC * RW consecutive whole rows (codes as one contiguous bulk copy, Q4G32 scales as a second one)
+// into a ring of shared-memory stages. Warps 0..7 consume every stage together: warp w handles row class
+// rc = w / P (rows rc, rc + RC, ... of the stage: RW rows) over K part q = w % P (units [q U / P, (q+1) U / P)),
+// P = 8 / RC. A lane owns units pb + lane + 32 j of its part and keeps the staged activations of one unit in
+// registers across the warp's RW rows. Per stage, each warp reduces its lanes' row sums with shuffles and stores one
+// partial per (row, part) in shared memory; the P partials of a row are summed in a fixed order (deterministic) once
+// every G1_PART_ROWS rows.
 // ------------------------------------------------------------------------------------------------------------
-constexpr int G1_NG = 3;     // consumer groups
-template <int F, int NS, int NG, int TR>
-struct G1Layout {
-    static constexpr int CW = 8 * NG;                  // consumer warps
-    static constexpr int THREADS = (CW + 1) * 32;
-    static constexpr int NSLOT = NS + 2;               // per-tile reduction slots (tiles in flight <= NS + 1)
-    static constexpr int RPL = TR / 2;                 // rows per lane (rows rlo, rlo + 2, ...)
-    static constexpr int RED_PER_SLOT = NG * 8 * RPL;  // one partial per (group, warp, lane row)
-    static constexpr int STAGE = TR * (Geo<F>::chunk_bytes + Geo<F>::scale_bytes);
-    static __host__ __device__ uint32_t bar_bytes() { return uint32_t(round_up(16 * NS, 128)); }
-    static __host__ __device__ uint32_t red_bytes() {
-        return uint32_t(round_up(16 + NSLOT * 4 + NSLOT * RED_PER_SLOT * 4, 128));
-    }
-    static __host__ __device__ uint32_t x_bytes(uint32_t K) { return uint32_t(round_up(int64_t((K + CHW - 1) / CHW) * CHW * 2, 128)); }
-    static __host__ __device__ uint32_t c_bytes(uint32_t K) { return uint32_t(round_up(4 * int64_t(K / 32) * XC<F>::n, 128)); }
-    // + 32: the Q3S unpack reads the word pair holding a unit's scale fields, up to 4 bytes past its row chunk
-    static __host__ __device__ uint32_t total(uint32_t K) {
-        return bar_bytes() + red_bytes() + x_bytes(K) + c_bytes(K) + uint32_t(NS) * STAGE + 32;
-    }
-};
+constexpr int G1_CW = 8;                       // consumer warps
+constexpr int G1_THREADS = (G1_CW + 1) * 32;
+constexpr int G1_MAXNS = 16;                   // stages in the ring at most
+constexpr int G1_PART_ROWS = 256;              // rows per partial-sum round
+constexpr uint32_t G1_HDR = 512;               // mbarriers (2 x 16 x 8 B) + misc words
 
 // Sum R per-lane values over the warp, one value per row: after the call, lanes j * (32 / R) (j < R) hold the warp
 // sum of v[j]. log2(R) transposing exchanges, then a butterfly inside each group of 32 / R lanes.
@@ -379,127 +393,74 @@ __device__ __forceinline__ float warp_rows_sum(float (&v)[R], int lane) {
     return r;
 }
 
-template <int F, int NS, int NG, int TR, bool FULLK>
-__global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_kernel(GemvArgs a) {
-    using G = Geo<F>;
-    using LY = G1Layout<F, NS, NG, TR>;
-    constexpr int NSLOT = LY::NSLOT;
-    constexpr int CW = LY::CW;
-    constexpr int RPL = LY::RPL;
-    constexpr uint32_t STAGE = uint32_t(LY::STAGE);
-    constexpr uint32_t NSG = uint32_t(NS / NG);       // stages per consumer group
-    static_assert(NS % NG == 0, "each consumer group owns NS / NG stages");
-    static_assert(NG * TR <= 32, "producer lanes: TR per group");
-    static_assert(RPL >= 1 && (RPL & (RPL - 1)) == 0 && RPL <= 8, "rows per lane: a power of two");
+struct G1Plan {
+    uint32_t off_part, off_xs, off_cst, off_stages;
+    uint32_t stage_bytes, smem;
+    int ns;
+};
+
+template <int F, int RC, int RW>
+__global__ void __launch_bounds__(G1_THREADS, 2) gemv1_kernel(GemvArgs a, G1Plan pl) {
+    constexpr int P = G1_CW / RC;                // K parts
+    constexpr int SR = RC * RW;                  // rows per stage
+    static_assert(G1_PART_ROWS % SR == 0, "a partial-sum round is a whole number of stages");
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t N = uint32_t(a.N), K = uint32_t(a.K);
-    // this CTA's rows: a contiguous range, the row counts of any two CTAs differ by at most one
+    const uint32_t N = uint32_t(a.N), K = uint32_t(a.K), U = K / 32;
+    const uint32_t RS = uint32_t(a.row_stride);
+    const uint32_t SS = uint32_t(a.scale_stride);
+    // this CTA's rows: a contiguous range; the row counts of any two CTAs differ by at most one
     const uint32_t rq = N / gridDim.x, rm = N % gridDim.x, b = blockIdx.x;
-    const uint32_t rbeg = b * rq + min(b, rm), rend = rbeg + rq + (b < rm ? 1u : 0u);
-    const uint32_t ntl = (rend - rbeg + TR - 1) / TR;  // row tiles of this CTA (the last one may be ragged)
-    const uint32_t nch = (K + CHW - 1) / CHW;
-    const uint32_t U = K / 32;                        // units per row
+    const uint32_t rbeg = b * rq + min(b, rm), nrows = rq + (b < rm ? 1u : 0u);
+    const uint32_t nst = (nrows + SR - 1) / SR;
+    const uint32_t NS = uint32_t(pl.ns);
 
-    uint8_t *p = smem_raw;
-    uint64_t *full = reinterpret_cast<uint64_t *>(p);
-    uint64_t *empty = full + NS;
-    p += LY::bar_bytes();
-    int *misc = reinterpret_cast<int *>(p);           // [0]: max |x| as float bits
-    int *cnt = misc + 4;
-    float *red = reinterpret_cast<float *>(p + 16 + NSLOT * 4);
-    p += LY::red_bytes();
-    uint16_t *xs = reinterpret_cast<uint16_t *>(p);
-    p += LY::x_bytes(K);
-    float *cst = reinterpret_cast<float *>(p);
-    p += LY::c_bytes(K);
-    uint8_t *stages = p;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);
+    uint64_t *empty = full + G1_MAXNS;
+    int *misc = reinterpret_cast<int *>(smem_raw + 2 * G1_MAXNS * 8);   // [4 .. 4 + P): per-part 2^-E
+    float *part = reinterpret_cast<float *>(smem_raw + pl.off_part);
+    uint4 *xs = reinterpret_cast<uint4 *>(smem_raw + pl.off_xs);
+    float *cst = reinterpret_cast<float *>(smem_raw + pl.off_cst);
+    uint8_t *stages = smem_raw + pl.off_stages;
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 8); }
-        for (int s = 0; s < NSLOT; ++s) cnt[s] = 0;
-        misc[0] = 0;
+        for (uint32_t s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], G1_CW); }
         fence_mbar_init();
     }
-    pdl_launch_dependents();     // the next product may begin launching; it still waits for us before reading
+    pdl_launch_dependents();     // the next product may begin launching; it still waits for us before reading x
     __syncthreads();
 
-    if (warp == CW) {
+    if (warp == G1_CW) {
         // ------------------------------------ producer ------------------------------------
-        // Item i of this CTA is (local tile i / nch, chunk i mod nch); group g consumes items g, g + NG, ... from
-        // its private sub-ring of stages [g*NSG, (g+1)*NSG), so every mbarrier is waited on only by the one group
-        // that consumed its previous phase (a parity wait is only meaningful one phase ahead). Producer lanes
-        // g*TR .. g*TR+TR-1 serve group g: lane r copies row r of the tile (bulk copies issued by one thread are
-        // processed one after another, so rows go out from different lanes), or lane 0 copies the whole tile when
-        // its rows are contiguous. The lanes advance in rounds (round k = every group's k-th item), and a round
-        // starts only once every group has released the stage it reuses, so no group runs more than NSG rounds
-        // ahead of another: the per-tile reduction slots, reused every NSLOT = NS + 2 tiles, depend on that bound.
-        constexpr uint32_t PMASK = (NG * TR >= 32) ? 0xffffffffu : ((1u << (NG * TR)) - 1u);
-        const int pg = lane / TR, pr = lane % TR;
-        if (pg < NG) {
+        if (lane == 0) {
             // Packed weights are read before the previous grid has finished only when the caller opted in
             // (QPACK_OPT_WEIGHT_PREFETCH: weights are not written by the kernel just before this one).
             if (!a.weight_prefetch) pdl_wait();
             const uint64_t pol = l2_evict_first_policy();
-            const bool whole_rows = (K == uint32_t(CHW));        // a tile of whole rows is one contiguous range
-            uint32_t k = 0, issued = 0, c = uint32_t(pg), lt = 0;
-            while (c >= nch) { c -= nch; ++lt; }
-            while (true) {
-                const bool have = lt < ntl;
-                if (!__any_sync(PMASK, have)) break;
-                const uint32_t s = uint32_t(pg) * NSG + k % NSG, ph = (k / NSG) & 1u;
-                bool bad = false;
-                if (have && pr == 0 && k >= NSG && !mbar_wait_bounded(&empty[s], ph ^ 1u)) {
-                    // A consumer stopped releasing stages: record it and stop producing; consumers then give up
-                    // on their next bounded wait, so nothing is left waiting.
+            uint32_t k = 0;
+            for (; k < nst; ++k) {
+                const uint32_t s = k % NS;
+                if (k >= NS && !mbar_wait_bounded_hint(&empty[s], ((k / NS) & 1u) ^ 1u)) {
+                    // The consumers stopped releasing stages: record it and stop; they give up on their own
+                    // bounded waits, so nothing is left waiting.
                     atomicOr(&g_fault_gemv, FAULT_WAIT_EMPTY);
-                    bad = true;
+                    break;
                 }
-                if (__any_sync(PMASK, bad)) break;
-                const uint32_t r0 = rbeg + lt * TR;
-                const uint32_t rows = have ? min(uint32_t(TR), rend - r0) : 0u;
-                const uint32_t koff = c * CHW;
-                uint32_t cbytes, sbytes = 0;
-                if constexpr (Fmt<F>::sb) {
-                    const uint32_t off = (koff / 256) * Fmt<F>::bytes;
-                    cbytes = min(uint32_t(G::chunk_bytes), uint32_t(a.row_stride) - off);
-                } else {
-                    cbytes = min(uint32_t(G::chunk_bytes), (K - koff) / 2);
-                    sbytes = min(uint32_t(G::scale_bytes), (uint32_t(a.scale_stride) - koff / 32) * 4);
-                }
-                uint8_t *st = stages + s * STAGE;
-                if (have && pr == 0) mbar_arrive_expect_tx(&full[s], rows * (cbytes + sbytes));
-                __syncwarp(PMASK);                               // expect_tx before any of this item's copies
-                if (have) {
-                    const uint8_t *src0 =
-                        a.packed + int64_t(r0) * a.row_stride + (Fmt<F>::sb ? (koff / 256) * Fmt<F>::bytes : koff / 2);
-                    const uint8_t *ssrc0 =
-                        Fmt<F>::sb ? nullptr : reinterpret_cast<const uint8_t *>(a.gscale + int64_t(r0) * a.scale_stride + koff / 32);
-                    if (whole_rows) {
-                        if (pr == 0) bulk_g2s(st, src0, rows * cbytes, &full[s], pol);
-                        if constexpr (!Fmt<F>::sb) {
-                            if (pr == 1 % TR) bulk_g2s(st + TR * G::chunk_bytes, ssrc0, rows * sbytes, &full[s], pol);
-                        }
-                    } else if (uint32_t(pr) < rows) {
-                        bulk_g2s(st + pr * G::chunk_bytes, src0 + int64_t(pr) * a.row_stride, cbytes, &full[s], pol);
-                        if constexpr (!Fmt<F>::sb)
-                            bulk_g2s(st + TR * G::chunk_bytes + pr * G::scale_bytes,
-                                     ssrc0 + int64_t(pr) * a.scale_stride * 4, sbytes, &full[s], pol);
-                    }
-                    ++issued;
-                }
-                ++k;
-                c += NG;
-                while (c >= nch) { c -= nch; ++lt; }
+                const uint32_t r0 = rbeg + k * SR, rows = min(uint32_t(SR), nrows - k * SR);
+                uint8_t *st = stages + s * pl.stage_bytes;
+                const uint32_t cbytes = rows * RS;
+                const uint32_t sbytes = Fmt<F>::sb ? 0u : rows * SS * 4u;
+                mbar_arrive_expect_tx(&full[s], cbytes + sbytes);
+                bulk_g2s(st, a.packed + int64_t(r0) * RS, cbytes, &full[s], pol);
+                if constexpr (!Fmt<F>::sb)
+                    bulk_g2s(st + SR * RS, a.gscale + int64_t(r0) * SS, sbytes, &full[s], pol);
             }
-            // Drain: wait (bounded) until the last fill of each of the group's stages has landed, so the CTA never
-            // exits with bulk copies still writing its shared memory (consumers that gave up may exit early).
-            if (pr == 0) {
-                for (uint32_t j = (issued > NSG ? issued - NSG : 0u); j < issued; ++j) {
-                    if (!mbar_wait_bounded(&full[uint32_t(pg) * NSG + j % NSG], (j / NSG) & 1u)) {
-                        atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
-                        break;
-                    }
+            // Drain: wait (bounded) until the last fill of every stage has landed, so the CTA never exits with bulk
+            // copies still writing its shared memory (consumers that gave up may have left early).
+            for (uint32_t j = (k > NS ? k - NS : 0u); j < k; ++j) {
+                if (!mbar_wait_bounded_hint(&full[j % NS], (j / NS) & 1u)) {
+                    atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
+                    break;
                 }
             }
         }
@@ -507,13 +468,17 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
     }
 
     // -------------------------------------- consumers --------------------------------------
+    const uint32_t rc = uint32_t(warp) / P, q = uint32_t(warp) % P;
+    const uint32_t pb = q * U / P, pe = (q + 1) * U / P;    // this warp's K part: units [pb, pe)
+    float *uscale = reinterpret_cast<float *>(misc + 4);     // [P]: 2^-E of each part
     pdl_wait();                  // x (and y) may belong to the previous grid
-    int E;                       // scale exponent: activations are staged as x * 2^E, with max |x| * 2^E in [2^14, 2^15)
     {
+        // Per K part, activations are staged as x * 2^E with max |x| * 2^E in [2^14, 2^15) over the part: every
+        // warp of the part finds the max itself (one pass over the part's activations), the RC warps of the part
+        // then stage alternate units and meet at the part's barrier.
         const uint4 *xg = reinterpret_cast<const uint4 *>(a.X);
-        // pass 1: max |x| over the whole vector (fp16 magnitudes order like their bit patterns)
         uint32_t m = 0;
-        for (uint32_t v = tid; v < K / 8; v += CW * 32) {
+        for (uint32_t v = 4 * pb + uint32_t(lane); v < 4 * pe; v += 32) {
             const uint4 raw = __ldg(xg + v);
             const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -521,151 +486,137 @@ __global__ void __launch_bounds__(G1Layout<F, NS, NG, TR>::THREADS, 1) gemv1_ker
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) atomicMax(misc, int(m));
-        named_bar_sync(1, CW * 32);
-        const float xm = h2f_bits(uint16_t(min(uint32_t(misc[0]), 0x7BFFu)));   // inf / nan inputs: clamp the exponent
-        E = (xm > 0.f) ? 14 - (int((__float_as_uint(xm) >> 23) & 255u) - 127) : 0;
-        // pass 2: stage x' = fp16(x * 2^(E - p)) half-unit by half-unit (16 activations, 8 words, 2 vectors)
-        uint4 *xd = reinterpret_cast<uint4 *>(xs);
-        for (uint32_t h = tid; h < K / 16; h += CW * 32) {
-            const uint4 r0 = __ldg(xg + 2 * h), r1 = __ldg(xg + 2 * h + 1);
-            const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-            uint16_t xr[16];
+        const float xm = h2f_bits(uint16_t(min(m, 0x7BFFu)));   // inf / nan inputs: clamp the exponent
+        const int E = (xm > 0.f) ? 14 - (int((__float_as_uint(xm) >> 23) & 255u) - 127) : 0;
+        if (rc == 0 && lane == 0) uscale[q] = exp2i(-E);
+        for (uint32_t t = uint32_t(RC) * uint32_t(lane) + rc; t < pe - pb; t += 32u * RC) {
+            const uint32_t uu = pb + t;
+            uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) { xr[2 * e] = lo16(rw[e]); xr[2 * e + 1] = hi16(rw[e]); }
-            uint32_t w[8];
-            stage_half_unit<F>(xr, E, w);
-            const uint32_t u = h >> 1, hh = h & 1u, cc = u >> 7, uu = u & 127u;
-            xd[(cc * 4 + 2 * hh) * 128 + uu] = make_uint4(w[0], w[1], w[2], w[3]);
-            xd[(cc * 4 + 2 * hh + 1) * 128 + uu] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-        named_bar_sync(1, CW * 32);
-        for (uint32_t u = tid; u < U; u += CW * 32) {
-            uint32_t xv[16];
-            load_xp(xs, u >> 7, u & 127u, xv);
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint4 r0 = __ldg(xg + 4 * uu + 2 * hh), r1 = __ldg(xg + 4 * uu + 2 * hh + 1);
+                const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+                uint16_t xr[16];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { xr[2 * e] = lo16(rw[e]); xr[2 * e + 1] = hi16(rw[e]); }
+                stage_half_unit<F>(xr, E, w + 8 * hh);
+            }
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt)
+                xs[tt * U + uu] = make_uint4(w[4 * tt], w[4 * tt + 1], w[4 * tt + 2], w[4 * tt + 3]);
             float xp[32], xt[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                xp[i] = h2f_bits(xh(xv, i));
+                xp[i] = h2f_bits(xh(w, i));
                 xt[i] = xp[i] * pow2f(xshift<F>(i));
             }
-            unit_consts<F>(xp, xt, cst + u * XC<F>::n);
+            unit_consts<F>(xp, xt, cst + uu * XC<F>::n);
         }
-        named_bar_sync(1, CW * 32);
+        if constexpr (RC > 1) named_bar_sync(2 + int(q), RC * 32);
+        else __syncwarp();
     }
-    const float unscale = exp2i(-E);
-    const uint32_t group = uint32_t(warp) >> 3, wg = uint32_t(warp) & 7u;
-    const uint32_t gl = wg * 32u + uint32_t(lane);
-    const int uc = int(gl & 127u);
-    const uint32_t rlo = gl >> 7;                      // rows rlo, rlo + 2, ..., rlo + TR - 2 of the tile
-    const LaneGeo geo = lane_geo<F>(uc);
-    const uint32_t uoff0 = rlo * uint32_t(G::chunk_bytes) + geo.ubase;
-    const uint32_t soff0 = TR * uint32_t(G::chunk_bytes) + rlo * uint32_t(G::scale_bytes) + 4u * uint32_t(uc);
+    // Lane geometry: the lane owns units u0 + 32 j (j <= jl) of its part; lanes past a short part and positions past
+    // the part's end recompute a valid unit of the same row with the contribution masked off, so the body is
+    // branch-free.
+    const uint32_t u0 = pb + uint32_t(lane);
+    const uint32_t nu = (pe - pb + 31) / 32;          // unit positions of the warp (the last may be partial)
+    const uint32_t u0c = u0 < pe ? u0 : pb;
+    const int jl = u0 < pe ? int((pe - 1 - u0) / 32) : -1;
+    const uint32_t jlc = jl < 0 ? 0u : uint32_t(jl);
+    const LaneGeo geo = lane_geo<F>(int(u0c));
+    constexpr uint32_t JB = step_bytes<F>();
 
-    // own items: the group's k-th item is item group + NG*k, in stage group*NSG + k mod NSG
-    uint32_t sl = 0, ph = 0;
-    uint32_t lt = 0, c = group, ib = 0, slot = 0;      // ib = item index of the tile's first chunk
-    while (c >= nch && lt < ntl) { c -= nch; ++lt; ib += nch; if (++slot == uint32_t(NSLOT)) slot = 0; }
+    uint32_t ph = 0, s = 0;
     bool dead = false;
-    float acc[RPL];
-#pragma unroll
-    for (int j = 0; j < RPL; ++j) acc[j] = 0.f;
-    while (lt < ntl) {
-        const uint32_t r0 = rbeg + lt * TR;
-        const uint32_t s = group * NSG + sl;
+    for (uint32_t k = 0; k < nst; ++k) {
         if (!dead && !mbar_wait_bounded(&full[s], ph)) {
             if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
             dead = true;
         }
-        {
-            const uint8_t *st = stages + s * STAGE;
-            uint32_t ucv = uint32_t(uc);
-            bool use = !dead;
-            if constexpr (!FULLK) {
-                const uint32_t units = min(uint32_t(UPC), (K - c * CHW) / 32);
-                use = use && (uint32_t(uc) < units);
-                ucv = min(ucv, units - 1);                 // stay on this item's data
-            }
-            uint32_t xv[16];
-            load_xp(xs, c, ucv, xv);
-            float cv[XC<F>::n];
-            const float *cp = cst + (c * UPC + ucv) * XC<F>::n;
+        const uint32_t rows = min(uint32_t(SR), nrows - k * SR);
+        float acc[RW];
 #pragma unroll
-            for (int q = 0; q < XC<F>::n; ++q) cv[q] = cp[q];
-            const uint8_t *u0 = st + uoff0;
-            const float *sp0 = reinterpret_cast<const float *>(st + soff0);
+        for (int i = 0; i < RW; ++i) acc[i] = 0.f;
+        if (!dead) {
+            const uint8_t *st = stages + s * pl.stage_bytes;
+            const uint8_t *ub0 = st + geo.ubase;
+            const float *sb0 = reinterpret_cast<const float *>(st + SR * RS) + u0c;
+            for (uint32_t j = 0; j < nu; ++j) {
+                const uint32_t jj = min(j, jlc);
+                const bool uv = int(j) <= jl;
+                const uint32_t u = u0c + 32u * jj;
+                uint32_t xv[16];
+                load_xp(xs, U, u, xv);
+                float cv[XC<F>::n];
 #pragma unroll
-            for (int j = 0; j < RPL; ++j) {
-                const float d = row_dot<F>(u0 + 2 * j * G::chunk_bytes, sp0 + 2 * j * (G::scale_bytes / 4), geo, cv, xv);
-                acc[j] += use ? d : 0.f;
-            }
-        }
-        if (c + NG >= nch) {
-            // this group's last item of the tile: one value per (warp, row) into the tile's slot, then a counter;
-            // the warp completing the count sums the tile's partials in a fixed order and writes y.
-            const float v = warp_rows_sum<RPL>(acc, lane);
-            float *rs = red + slot * LY::RED_PER_SLOT + (group * 8 + wg) * RPL;
-            if ((lane & (32 / RPL - 1)) == 0) rs[lane / (32 / RPL)] = v;
-            __syncwarp();
-            int last = 0;
-            if (lane == 0) {
-                __threadfence_block();
-                const int expected = 8 * int(min(uint32_t(NG), nch));
-                last = (atomicAdd(&cnt[slot], 1) == expected - 1);
-                if (last) __threadfence_block();
-            }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {
-                // lane r < TR: tile row r = 2 j + rl, summed over the four warps holding rows of parity rl in every
-                // contributing group
-                if (lane < TR) {
-                    const int rl = lane & 1, j = lane >> 1;
-                    const float *sb = red + slot * LY::RED_PER_SLOT;
-                    float yv = 0.f;
+                for (int cc = 0; cc < XC<F>::n; ++cc) cv[cc] = cst[u * XC<F>::n + cc];
+                const uint8_t *ub = ub0 + jj * JB;
+                const float *sbp = sb0 + 32u * jj;
 #pragma unroll
-                    for (int gr = 0; gr < NG; ++gr) {
-                        bool contributed = nch >= uint32_t(NG);
-                        if (!contributed) {
-                            for (uint32_t cc = 0; cc < nch; ++cc) contributed |= ((ib + cc) % NG) == uint32_t(gr);
-                        }
-                        if (contributed) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) yv += sb[(gr * 8 + 4 * rl + q) * RPL + j];
-                        }
-                    }
-                    if (r0 + uint32_t(lane) < rend) a.Y[r0 + lane] = yv * unscale;
+                for (int i = 0; i < RW; ++i) {
+                    const uint32_t r = rc + uint32_t(RC * i);
+                    const uint32_t rr = min(r, rows - 1);
+                    row_acc<F>(ub + rr * RS, sbp + rr * SS, geo, cv, xv, uv && r < rows, acc[i]);
                 }
-                __syncwarp();
-                if (lane == 0) cnt[slot] = 0;
             }
-#pragma unroll
-            for (int j = 0; j < RPL; ++j) acc[j] = 0.f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (++sl == NSG) { sl = 0; ph ^= 1u; }
-        c += NG;
-        while (c >= nch) {
-            c -= nch;
-            ++lt;
-            ib += nch;
-            if (++slot == uint32_t(NSLOT)) slot = 0;
+        if (++s == NS) { s = 0; ph ^= 1u; }
+
+        // one partial per (row, part): lanes i * (32 / RW) hold row rc + RC * i after the reduction
+        const float v = warp_rows_sum<RW>(acc, lane);
+        const uint32_t lr = (k * SR) % G1_PART_ROWS;   // stage's first row within the round
+        if ((lane & (32 / RW - 1)) == 0) {
+            const uint32_t r = rc + uint32_t(RC) * uint32_t(lane / (32 / RW));
+            if (r < rows) part[(lr + r) * P + q] = v;
+        }
+        const uint32_t done = k * SR + rows;           // rows of this CTA finished after this stage
+        if (done == nrows || done % G1_PART_ROWS == 0) {
+            named_bar_sync(1, G1_CW * 32);
+            const uint32_t base = (done - 1) / G1_PART_ROWS * G1_PART_ROWS, cnt = done - base;
+            for (uint32_t t = uint32_t(tid); t < cnt; t += G1_CW * 32) {
+                float y = 0.f;
+#pragma unroll
+                for (int pp = 0; pp < P; ++pp) y = fmaf(part[t * P + pp], uscale[pp], y);
+                a.Y[rbeg + base + t] = y;
+            }
+            if (done != nrows) named_bar_sync(1, G1_CW * 32);   // partials of the next round overwrite these
         }
     }
 }
 
-template <int F, int NS, int NG, int TR, bool FULLK>
-static cudaError_t try_launch_gemv1(const GemvArgs &a, cudaStream_t st, bool *launched) {
-    using LY = G1Layout<F, NS, NG, TR>;
-    *launched = false;
-    const uint32_t smem = LY::total(uint32_t(a.K));
-    if (smem > 227u * 1024u) return cudaSuccess;
+// Shared-memory plan of one launch: returns false when even one stage plus the staged activations do not fit.
+template <int F>
+static bool plan_gemv1(const GemvArgs &a, int sr, uint32_t budget, G1Plan *pl) {
+    const uint32_t U = uint32_t(a.K / 32);
+    const uint32_t RS = uint32_t(a.row_stride), SS = uint32_t(a.scale_stride);
+    pl->off_part = G1_HDR;
+    pl->off_xs = pl->off_part + G1_PART_ROWS * (G1_CW / 1) * 4;        // room for P = 8 partials per row
+    pl->off_cst = pl->off_xs + uint32_t(round_up(int64_t(U) * 64, 128));
+    pl->off_stages = pl->off_cst + uint32_t(round_up(int64_t(U) * XC<F>::n * 4, 128));
+    pl->stage_bytes = uint32_t(round_up(int64_t(sr) * RS + (Fmt<F>::sb ? 0 : int64_t(sr) * SS * 4), 128));
+    // + 32: the Q3S unpack reads the word pair holding a unit's scale fields, up to 4 bytes past its row
+    const int64_t room = int64_t(budget) - pl->off_stages - 32;
+    if (room < int64_t(pl->stage_bytes) * 2) return false;
+    pl->ns = int(room / pl->stage_bytes < G1_MAXNS ? room / pl->stage_bytes : G1_MAXNS);
+    pl->smem = pl->off_stages + uint32_t(pl->ns) * pl->stage_bytes + 32;
+    return true;
+}
+
+template <int F, int RC, int RW>
+static cudaError_t launch_gemv1_cfg(const GemvArgs &a, cudaStream_t st) {
+    // Two CTAs per SM when the ring keeps at least 3 stages within half of the SM's shared memory; else one.
+    G1Plan pl;
+    if (!plan_gemv1<F>(a, RC * RW, 110u * 1024u, &pl) || pl.ns < 3) {
+        if (!plan_gemv1<F>(a, RC * RW, 227u * 1024u, &pl)) return cudaErrorInvalidValue;
+    }
     static int opted[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!opted[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemv1_kernel<F, NS, NG, TR, FULLK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(gemv1_kernel<F, RC, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              227 * 1024);
         if (e != cudaSuccess) return e;
         opted[dev] = 1;
@@ -674,49 +625,30 @@ static cudaError_t try_launch_gemv1(const GemvArgs &a, cudaStream_t st, bool *la
     if (a.N < grid) grid = int(a.N);                   // every CTA gets at least one row
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
-    cfg.blockDim = dim3(unsigned(LY::THREADS));
-    cfg.dynamicSmemBytes = smem;
+    cfg.blockDim = dim3(unsigned(G1_THREADS));
+    cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = a.weight_prefetch ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    *launched = true;
-    return cudaLaunchKernelEx(&cfg, gemv1_kernel<F, NS, NG, TR, FULLK>, a);
+    return cudaLaunchKernelEx(&cfg, gemv1_kernel<F, RC, RW>, a, pl);
 }
 
-// Largest ring (a multiple of G1_NG stages, so every group owns the same number) that fits beside the staged
-// activations; about 200 KB of stages keeps far more bytes in flight per SM than the memory latency needs.
-template <int F, int TR, bool FULLK>
-static cudaError_t launch_gemv1_k(const GemvArgs &a, cudaStream_t st) {
-    bool done = false;
-    cudaError_t e;
-    constexpr int SB = G1Layout<F, 3, G1_NG, TR>::STAGE;
-    if constexpr (SB * 15 <= 200 * 1024) {
-        e = try_launch_gemv1<F, 15, G1_NG, TR, FULLK>(a, st, &done);
-        if (e != cudaSuccess || done) return e;
-    }
-    if constexpr (SB * 12 <= 200 * 1024) {
-        e = try_launch_gemv1<F, 12, G1_NG, TR, FULLK>(a, st, &done);
-        if (e != cudaSuccess || done) return e;
-    }
-    e = try_launch_gemv1<F, 9, G1_NG, TR, FULLK>(a, st, &done);
-    if (e != cudaSuccess || done) return e;
-    e = try_launch_gemv1<F, 6, G1_NG, TR, FULLK>(a, st, &done);
-    if (e != cudaSuccess || done) return e;
-    e = try_launch_gemv1<F, 3, G1_NG, TR, FULLK>(a, st, &done);
-    if (e != cudaSuccess || done) return e;
-    return cudaErrorInvalidValue;
-}
-
-#ifndef QPACK_G1_TR
-#define QPACK_G1_TR 8
-#endif
+// Stage shape from the row size: about 8-28 KB per stage (one bulk copy moves it), 2 row classes x 4 K parts while
+// a part of a row still gives every lane a unit (K >= 4096) and rows are short, 1 row class x 8 parts for long rows.
 template <int F>
 static cudaError_t launch_gemv1(const GemvArgs &a, cudaStream_t st) {
-    if (a.K % CHW == 0) return launch_gemv1_k<F, QPACK_G1_TR, true>(a, st);
-    return launch_gemv1_k<F, QPACK_G1_TR, false>(a, st);
+    const int64_t row = a.row_stride + (Fmt<F>::sb ? 0 : a.scale_stride * 4);
+    constexpr int64_t LIM = 28 * 1024;
+    if (a.K <= 16384) {
+        if (8 * row <= LIM) return launch_gemv1_cfg<F, 2, 4>(a, st);
+        if (4 * row <= LIM) return launch_gemv1_cfg<F, 2, 2>(a, st);
+        if (2 * row <= LIM) return launch_gemv1_cfg<F, 2, 1>(a, st);
+    }
+    if (2 * row <= LIM) return launch_gemv1_cfg<F, 1, 2>(a, st);
+    return launch_gemv1_cfg<F, 1, 1>(a, st);
 }
 
 namespace {

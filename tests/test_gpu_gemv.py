@@ -98,6 +98,26 @@ def test_gemv_rows_spread_over_all_sms(qpg, orc, name):
     assert qpg.qpack_fetch_fault_flags() == 0
 
 
+# (N, K): many rows per CTA with ragged stages; more than 256 rows per CTA (several partial-sum rounds); the
+# 7B down-projection width; long rows (one row class, eight K parts); and the largest K the batch-1 path takes.
+STAGE_SHAPES = [(1531, 4096), (45613, 256), (613, 11008), (311, 20480), (160, 32768)]
+
+
+@pytest.mark.parametrize("name", ALL)
+@pytest.mark.parametrize("shape", STAGE_SHAPES, ids=[f"{n}x{k}" for n, k in STAGE_SHAPES])
+def test_gemv_stage_shapes(qpg, orc, name, shape):
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    N, K = shape
+    rp, rgs = case(orc, fmt, N, K, 660 + N % 97)
+    x = synth.normal((K,), 1.0, 661 + K % 89, dtype=torch.float16)
+    y = run_gemv(qpg, fmt, rp, rgs, N, K, x)
+    y_ref = orc.gemv(fmt, N, K, rp, rgs, x.numpy().view(np.uint16), nthreads=8)
+    deq = orc.dequant(fmt, N, K, rp, rgs)
+    gemv_bound_check(y, y_ref, deq, x.numpy().astype(np.float64)[None, :])
+    assert qpg.qpack_fetch_fault_flags() == 0
+
+
 @pytest.mark.parametrize("name", ALL)
 def test_gemv_large_activations_and_zero_rows(qpg, orc, name):
     from bit_weight_quantized_qpack_gb300 import synth
