@@ -147,6 +147,13 @@ __device__ __forceinline__ bool mbar_wait_bounded_hint(uint64_t *bar, uint32_t p
     return false;
 }
 
+// Shared-memory atomic add with acquire-release semantics at CTA scope; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cta(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+    return old;
+}
+
 // 1-D bulk copy global -> shared, completion signalled on `bar` as transaction bytes.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar,

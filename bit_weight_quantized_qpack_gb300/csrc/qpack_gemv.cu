@@ -4,26 +4,26 @@
 // (2/3/5/6-bit article, lpnh.cn/news/2857666, §1.2: time per token = weight bytes / bandwidth; DBHOO-CIM
 // article, pwwt.cn/news/4452170, §3.3: dequantization must stay fused, never materialised).
 //
-// Batch-1 kernel (gemv1_kernel), one persistent CTA per SM:
-//   warp 16      producer: streams (4-row tile x 4096-weight chunk) segments of the packed rows into a ring of
-//                shared-memory stages with 1-D bulk copies (cp.async.bulk, completion on an mbarrier), L2
-//                evict-first because each byte is used once.
-//   warps 0..15  two consumer groups of 8 warps; group g consumes the stages whose item index has parity g. In
-//                a group, lane l of warp w owns the 32-weight unit uc = (32w + l) mod 128 of the rows
-//                (32w + l) div 128 and that + 2, so its activations are loaded once for two rows.
+// Batch-1 kernel (gemv1_kernel), one persistent CTA per SM (two fit, so consecutive products overlap):
+//   warp 8       producer: 2-D TMA tensor copies of (8-row tile x K chunk) boxes of the packed rows into a ring of
+//                shared-memory stages (completion on mbarriers, L2 evict-first because each byte is used once).
+//   warps 0..7   consumers: row class x K part of every stage; lane l owns one 32-weight unit of each chunk.
 // Unpacking (2/3/5/6-bit article §3.3: separate unpack from multiply-add, factor s*(q.x) + m*sum(x)): codes are
 // OR-ed into the mantissa of an fp16 1024.0 with one LOP3 per pair of weights, so a half holds 1024 + u*2^p
 // exactly, p being the code's bit position inside its 16-bit half. The activations are staged in shared memory
 // pre-scaled by 2^-p of the code they meet (x' = fp16(x * 2^-p), exact unless subnormal), so one fp32 FMA with
 // fp16 inputs (exact product) per weight accumulates 1024*x' + u*x for every class into one accumulator. The
 // 1024*sum(x') terms, the symmetric code offsets and the asymmetric minima are removed per sub-block with
-// activation sums that each CTA precomputes once. Per-row results are combined without a block barrier: each
-// warp reduces its two rows, publishes the partials and bumps a per-tile counter; the warp completing the count
-// sums the partials in a fixed order (deterministic) and writes y.
+// activation sums that each CTA precomputes once. Per row, each warp reduces its lanes' sums with shuffles and
+// stores one partial per K part in shared memory; the partials are scaled back by each part's power of two and
+// summed in a fixed order (deterministic) before y is written.
 //
 // Small-batch kernel (stream_kernel, M = 2..16): same producer; each unit is dequantized exactly to fp32
 // registers and multiplied against the M activation rows.
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "qpack_dev.cuh"
 #include "qpack_launch.h"
@@ -346,31 +346,37 @@ __device__ __forceinline__ void load_xp(const uint4 *xs, uint32_t U, uint32_t u,
         xv[4 * t] = v.x; xv[4 * t + 1] = v.y; xv[4 * t + 2] = v.z; xv[4 * t + 3] = v.w;
     }
 }
-// Bytes of one unit position step (32 units) of a row: unit u + 32 lies 4 super-blocks (1024 weights) further on,
-// at the same offsets within its super-block, so a lane's unit geometry is computed once.
+// Scale exponent of a K part from its max |x| (fp16 magnitude bits): x * 2^E has max in [2^14, 2^15); 0 for an all-zero
+// part; inf / nan inputs clamp to the largest finite magnitude.
+__device__ __forceinline__ int part_exponent(uint32_t mbits) {
+    const float xm = h2f_bits(uint16_t(min(mbits, 0x7BFFu)));
+    return (xm > 0.f) ? 14 - (int((__float_as_uint(xm) >> 23) & 255u) - 127) : 0;
+}
+
+// Stage one unit: raw = its 32 fp16 activations (four 16-byte vectors), E = the part's scale exponent. Writes the
+// unit's four staged vectors (x' = fp16(x * 2^(E - p)), see stage_half_unit) and its activation constants.
 template <int F>
-__host__ __device__ constexpr uint32_t step_bytes() { return Fmt<F>::sb ? 4u * Fmt<F>::bytes : 512u; }
-
-}  // namespace
-
-// ------------------------------------------------------------------------------------------------------------
-// Batch-1 fused dequant-GEMV kernel.
-//
-// One CTA per SM, sized so that two fit on an SM (the next product in the stream, launched as a programmatic
-// dependent, starts streaming its weights while this one finishes). Warp 8 is the producer: its lane 0 copies
-// stages of SR = RC * RW consecutive whole rows (codes as one contiguous bulk copy, Q4G32 scales as a second one)
-// into a ring of shared-memory stages. Warps 0..7 consume every stage together: warp w handles row class
-// rc = w / P (rows rc, rc + RC, ... of the stage: RW rows) over K part q = w % P (units [q U / P, (q+1) U / P)),
-// P = 8 / RC. A lane owns units pb + lane + 32 j of its part and keeps the staged activations of one unit in
-// registers across the warp's RW rows. Per stage, each warp reduces its lanes' row sums with shuffles and stores one
-// partial per (row, part) in shared memory; the P partials of a row are summed in a fixed order (deterministic) once
-// every G1_PART_ROWS rows.
-// ------------------------------------------------------------------------------------------------------------
-constexpr int G1_CW = 8;                       // consumer warps
-constexpr int G1_THREADS = (G1_CW + 1) * 32;
-constexpr int G1_MAXNS = 16;                   // stages in the ring at most
-constexpr int G1_PART_ROWS = 256;              // rows per partial-sum round
-constexpr uint32_t G1_HDR = 512;               // mbarriers (2 x 16 x 8 B) + misc words
+__device__ __forceinline__ void stage_unit(const uint4 (&raw)[4], int E, uint4 *xs, float *cst, uint32_t U, uint32_t u) {
+    uint32_t w[16];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t rw[8] = {raw[2 * hh].x, raw[2 * hh].y, raw[2 * hh].z, raw[2 * hh].w,
+                                raw[2 * hh + 1].x, raw[2 * hh + 1].y, raw[2 * hh + 1].z, raw[2 * hh + 1].w};
+        uint16_t xr[16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { xr[2 * e] = lo16(rw[e]); xr[2 * e + 1] = hi16(rw[e]); }
+        stage_half_unit<F>(xr, E, w + 8 * hh);
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) xs[t * U + u] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+    float xp[32], xt[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        xp[i] = h2f_bits(xh(w, i));
+        xt[i] = xp[i] * pow2f(xshift<F>(i));
+    }
+    unit_consts<F>(xp, xt, cst + u * XC<F>::n);
+}
 
 // Sum R per-lane values over the warp, one value per row: after the call, lanes j * (32 / R) (j < R) hold the warp
 // sum of v[j]. log2(R) transposing exchanges, then a butterfly inside each group of 32 / R lanes.
@@ -393,75 +399,119 @@ __device__ __forceinline__ float warp_rows_sum(float (&v)[R], int lane) {
     return r;
 }
 
+// 2-D tensor copy global -> shared (box of the tensor map at coordinates {x, y}), completion on `bar` as bytes.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------------------------------
+// Batch-1 fused dequant-GEMV kernel.
+//
+// The packed matrix is read through a 2-D TMA tensor map over (rows x 8-byte words): one tensor copy moves a tile of
+// TR = 8 rows x one K chunk (CHW weights) into a shared-memory stage, so every stage has the same compile-time layout
+// (row r of the chunk at r * CB bytes) whatever K is; words past the row end and rows past N arrive as zeros and are
+// masked by the consumers. One CTA per SM, sized so that two fit on an SM: the next product in the stream, launched
+// as a programmatic dependent, starts streaming its weights while this one finishes.
+// Warp 8 is the producer (one lane issues the copies into a ring of stages). Warps 0..7 consume every stage together:
+// warp w handles row class rc = w / P (rows rc, rc + RC, ...: RW rows) over K part q = w % P of the chunk (32 units;
+// lane l owns unit 32 q + l of every chunk) and keeps the staged activations of that unit in registers across its
+// rows. Row sums accumulate over the chunks of a tile; then each warp reduces its lanes with shuffles and stores one
+// partial per (row, part), and the P partials of a row are summed in a fixed order (deterministic) every G1_PART_ROWS
+// rows. Activations are staged per part with the part's own power-of-two scale (max |x| * 2^E in [2^14, 2^15)).
+// ------------------------------------------------------------------------------------------------------------
+constexpr int G1_CW = 16;                      // consumer warps
+template <int F> struct T1 {
+    static constexpr int CHW = (F == FMT_Q5S || F == FMT_Q6S) ? 2048 : 4096;      // weights per K chunk
+    static constexpr int UPC = CHW / 32;                                          // units per chunk
+    static constexpr int P = UPC / 32;                                            // K parts of 32 units
+    static constexpr int RC = G1_CW / P;                                          // row classes
+    static constexpr int RW = F == FMT_Q4G32 ? 4 : (P == 4 ? 8 : 4);              // rows per warp and stage
+    static constexpr int TR = RC * RW;                                            // rows per tile
+    static constexpr int CB = Fmt<F>::sb ? (CHW / 256) * Fmt<F>::bytes : CHW / 2; // code bytes per row chunk
+    static constexpr int SB = Fmt<F>::sb ? 0 : (CHW / 32) * 4;                    // Q4G32 scale bytes per row chunk
+    static constexpr int TX = TR * (CB + SB);                                     // bytes a stage receives
+    static constexpr int STAGE = (TX + 127) / 128 * 128;
+    static_assert(CB % 16 == 0 && CB / 8 <= 256 && SB / 8 <= 256, "tensor-map box limits");
+};
+constexpr int G1_THREADS = (G1_CW + 1) * 32;
+constexpr int G1_CORES = G1_CW <= 8 ? 1 : 0;   // two CTAs per SM possible (registers and threads)
+constexpr int G1_MAXNS = 16;                   // stages in the ring at most
+constexpr int G1_PRE = 1;                      // stage fills issued before the activations are staged
+constexpr int G1_PART_ROWS = 256;              // rows per partial-sum round
+constexpr uint32_t G1_HDR = 512;               // mbarriers (2 x 16 x 8 B) + misc words
+
 struct G1Plan {
-    uint32_t off_part, off_xs, off_cst, off_stages;
-    uint32_t stage_bytes, smem;
+    uint32_t off_part, off_xs, off_cst, off_stages, smem;
     int ns;
 };
 
-template <int F, int RC, int RW>
-__global__ void __launch_bounds__(G1_THREADS, 2) gemv1_kernel(GemvArgs a, G1Plan pl) {
-    constexpr int P = G1_CW / RC;                // K parts
-    constexpr int SR = RC * RW;                  // rows per stage
-    static_assert(G1_PART_ROWS % SR == 0, "a partial-sum round is a whole number of stages");
-    extern __shared__ __align__(128) uint8_t smem_raw[];
+template <int F>
+__global__ void __launch_bounds__(G1_THREADS, 1 + G1_CORES)
+    gemv1_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
+                 GemvArgs a, G1Plan pl) {
+    using T = T1<F>;
+    constexpr int P = T::P, RC = T::RC, RW = T::RW, TR = T::TR, CB = T::CB, SB = T::SB, UPC = T::UPC;
+    static_assert(G1_PART_ROWS % TR == 0, "a partial-sum round is a whole number of tiles");
+    extern __shared__ __align__(1024) uint8_t smem_g1[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t N = uint32_t(a.N), K = uint32_t(a.K), U = K / 32;
-    const uint32_t RS = uint32_t(a.row_stride);
-    const uint32_t SS = uint32_t(a.scale_stride);
     // this CTA's rows: a contiguous range; the row counts of any two CTAs differ by at most one
     const uint32_t rq = N / gridDim.x, rm = N % gridDim.x, b = blockIdx.x;
     const uint32_t rbeg = b * rq + min(b, rm), nrows = rq + (b < rm ? 1u : 0u);
-    const uint32_t nst = (nrows + SR - 1) / SR;
+    const uint32_t nch = (U + UPC - 1) / UPC;              // K chunks per row
+    const uint32_t nit = (nrows + TR - 1) / TR * nch;      // stages of this CTA: tiles x chunks
     const uint32_t NS = uint32_t(pl.ns);
 
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);
-    uint64_t *empty = full + G1_MAXNS;
-    int *misc = reinterpret_cast<int *>(smem_raw + 2 * G1_MAXNS * 8);   // [4 .. 4 + P): per-part 2^-E
-    float *part = reinterpret_cast<float *>(smem_raw + pl.off_part);
-    uint4 *xs = reinterpret_cast<uint4 *>(smem_raw + pl.off_xs);
-    float *cst = reinterpret_cast<float *>(smem_raw + pl.off_cst);
-    uint8_t *stages = smem_raw + pl.off_stages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_g1);                  // [NS] stage filled
+    uint32_t *rel = reinterpret_cast<uint32_t *>(smem_g1 + G1_MAXNS * 8);    // [NS] warps done with the stage
+    uint64_t *xready = reinterpret_cast<uint64_t *>(smem_g1 + G1_MAXNS * 12);  // activations staged
+    float *uscale = reinterpret_cast<float *>(smem_g1 + 2 * G1_MAXNS * 8);   // [P]: 2^-E of each part
+    uint32_t *pmax = reinterpret_cast<uint32_t *>(smem_g1 + 2 * G1_MAXNS * 8 + 32);   // [P]: max |x| bits per part
+    float *part = reinterpret_cast<float *>(smem_g1 + pl.off_part);
+    uint4 *xs = reinterpret_cast<uint4 *>(smem_g1 + pl.off_xs);
+    float *cst = reinterpret_cast<float *>(smem_g1 + pl.off_cst);
+    uint8_t *stages = smem_g1 + pl.off_stages;
 
     if (tid == 0) {
-        for (uint32_t s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], G1_CW); }
+        for (uint32_t s = 0; s < NS; ++s) { mbar_init(&full[s], 1); rel[s] = 0; }
+        for (int i = 0; i < P; ++i) pmax[i] = 0;
+        mbar_init(xready, 1);
         fence_mbar_init();
     }
     pdl_launch_dependents();     // the next product may begin launching; it still waits for us before reading x
     __syncthreads();
+    const uint64_t pol = l2_evict_first_policy();
+    // Fill of item j (tile j / nch, chunk j % nch) into stage j % NS.
+    auto fill = [&](uint32_t j) {
+        const uint32_t s = j % NS, tj = j / nch, cj = j - tj * nch;
+        uint8_t *st = stages + s * uint32_t(T::STAGE);
+        mbar_arrive_expect_tx(&full[s], uint32_t(T::TX));
+        tma_load_2d(st, &tm_codes, int(cj * (CB / 8)), int(rbeg + tj * TR), &full[s], pol);
+        if constexpr (SB > 0) tma_load_2d(st + TR * CB, &tm_scales, int(cj * (SB / 8)), int(rbeg + tj * TR), &full[s], pol);
+    };
 
     if (warp == G1_CW) {
         // ------------------------------------ producer ------------------------------------
+        // The first NS fills; every later fill is issued by the consumer warp that releases the stage last, so
+        // nobody polls for free stages.
         if (lane == 0) {
             // Packed weights are read before the previous grid has finished only when the caller opted in
-            // (QPACK_OPT_WEIGHT_PREFETCH: weights are not written by the kernel just before this one).
+            // (QPACK_OPT_WEIGHT_PREFETCH: weights are not written by the kernel just before this one). Only the first
+            // G1_PRE fills go out before the activations are staged: a deeper early prefetch fills the memory queues
+            // and delays the activation loads on the critical path.
             if (!a.weight_prefetch) pdl_wait();
-            const uint64_t pol = l2_evict_first_policy();
-            uint32_t k = 0;
-            for (; k < nst; ++k) {
-                const uint32_t s = k % NS;
-                if (k >= NS && !mbar_wait_bounded_hint(&empty[s], ((k / NS) & 1u) ^ 1u)) {
-                    // The consumers stopped releasing stages: record it and stop; they give up on their own
-                    // bounded waits, so nothing is left waiting.
-                    atomicOr(&g_fault_gemv, FAULT_WAIT_EMPTY);
-                    break;
-                }
-                const uint32_t r0 = rbeg + k * SR, rows = min(uint32_t(SR), nrows - k * SR);
-                uint8_t *st = stages + s * pl.stage_bytes;
-                const uint32_t cbytes = rows * RS;
-                const uint32_t sbytes = Fmt<F>::sb ? 0u : rows * SS * 4u;
-                mbar_arrive_expect_tx(&full[s], cbytes + sbytes);
-                bulk_g2s(st, a.packed + int64_t(r0) * RS, cbytes, &full[s], pol);
-                if constexpr (!Fmt<F>::sb)
-                    bulk_g2s(st + SR * RS, a.gscale + int64_t(r0) * SS, sbytes, &full[s], pol);
-            }
-            // Drain: wait (bounded) until the last fill of every stage has landed, so the CTA never exits with bulk
-            // copies still writing its shared memory (consumers that gave up may have left early).
-            for (uint32_t j = (k > NS ? k - NS : 0u); j < k; ++j) {
-                if (!mbar_wait_bounded_hint(&full[j % NS], (j / NS) & 1u)) {
-                    atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
-                    break;
-                }
+            uint32_t j = 0;
+            for (; j < nit && j < NS && j < uint32_t(G1_PRE); ++j) fill(j);
+            if (j < nit && j < NS) {
+                if (!mbar_wait_bounded_hint(xready, 0u)) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
+                for (; j < nit && j < NS; ++j) fill(j);
             }
         }
         return;
@@ -469,155 +519,197 @@ __global__ void __launch_bounds__(G1_THREADS, 2) gemv1_kernel(GemvArgs a, G1Plan
 
     // -------------------------------------- consumers --------------------------------------
     const uint32_t rc = uint32_t(warp) / P, q = uint32_t(warp) % P;
-    const uint32_t pb = q * U / P, pe = (q + 1) * U / P;    // this warp's K part: units [pb, pe)
-    float *uscale = reinterpret_cast<float *>(misc + 4);     // [P]: 2^-E of each part
+    const uint32_t uc = q * 32u + uint32_t(lane);           // this lane's unit within every chunk
     pdl_wait();                  // x (and y) may belong to the previous grid
     {
-        // Per K part, activations are staged as x * 2^E with max |x| * 2^E in [2^14, 2^15) over the part: every
-        // warp of the part finds the max itself (one pass over the part's activations), the RC warps of the part
-        // then stage alternate units and meet at the part's barrier.
+        // Staging: thread t handles units t, t + NT, ... (K <= 32768). A warp's 32 consecutive units
+        // are one 32-unit run of one chunk, i.e. of one K part, so a part's max |x| is a warp max plus one shared
+        // atomic per warp; after a barrier every thread stages its units from registers.
+        constexpr uint32_t NT = G1_CW * 32;
+        constexpr int HU = int((1024 + NT - 1) / NT);       // units per thread at the largest K (32768)
         const uint4 *xg = reinterpret_cast<const uint4 *>(a.X);
-        uint32_t m = 0;
-        for (uint32_t v = 4 * pb + uint32_t(lane); v < 4 * pe; v += 32) {
-            const uint4 raw = __ldg(xg + v);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint4 raw[HU][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) m = max(m, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
-        }
+        for (int h = 0; h < HU; ++h) {
+            const uint32_t u = uint32_t(tid) + h * NT;
+            uint32_t m = 0;
+            if (u < U) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float xm = h2f_bits(uint16_t(min(m, 0x7BFFu)));   // inf / nan inputs: clamp the exponent
-        const int E = (xm > 0.f) ? 14 - (int((__float_as_uint(xm) >> 23) & 255u) - 127) : 0;
-        if (rc == 0 && lane == 0) uscale[q] = exp2i(-E);
-        for (uint32_t t = uint32_t(RC) * uint32_t(lane) + rc; t < pe - pb; t += 32u * RC) {
-            const uint32_t uu = pb + t;
-            uint32_t w[16];
+                for (int t = 0; t < 4; ++t) raw[h][t] = __ldg(xg + 4 * u + t);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint4 r0 = __ldg(xg + 4 * uu + 2 * hh), r1 = __ldg(xg + 4 * uu + 2 * hh + 1);
-                const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-                uint16_t xr[16];
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t w[4] = {raw[h][t].x, raw[h][t].y, raw[h][t].z, raw[h][t].w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) { xr[2 * e] = lo16(rw[e]); xr[2 * e + 1] = hi16(rw[e]); }
-                stage_half_unit<F>(xr, E, w + 8 * hh);
+                    for (int e = 0; e < 4; ++e) m = max(m, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+                }
             }
+            if (uint32_t(tid - lane) + h * NT < U) {            // the warp's first unit exists
 #pragma unroll
-            for (int tt = 0; tt < 4; ++tt)
-                xs[tt * U + uu] = make_uint4(w[4 * tt], w[4 * tt + 1], w[4 * tt + 2], w[4 * tt + 3]);
-            float xp[32], xt[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                xp[i] = h2f_bits(xh(w, i));
-                xt[i] = xp[i] * pow2f(xshift<F>(i));
+                for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+                if (lane == 0) atomicMax(&pmax[((uint32_t(tid) + h * NT) % UPC) / 32], m);
             }
-            unit_consts<F>(xp, xt, cst + uu * XC<F>::n);
         }
-        if constexpr (RC > 1) named_bar_sync(2 + int(q), RC * 32);
-        else __syncwarp();
+        named_bar_sync(1, G1_CW * 32);
+#pragma unroll
+        for (int h = 0; h < HU; ++h) {
+            const uint32_t u = uint32_t(tid) + h * NT;
+            if (u < U) stage_unit<F>(raw[h], part_exponent(pmax[(u % UPC) / 32]), xs, cst, U, u);
+        }
+        if (tid < P) uscale[tid] = exp2i(-part_exponent(pmax[tid]));
+        named_bar_sync(1, G1_CW * 32);
+        if (tid == 0) mbar_arrive(xready);
     }
-    // Lane geometry: the lane owns units u0 + 32 j (j <= jl) of its part; lanes past a short part and positions past
-    // the part's end recompute a valid unit of the same row with the contribution masked off, so the body is
-    // branch-free.
-    const uint32_t u0 = pb + uint32_t(lane);
-    const uint32_t nu = (pe - pb + 31) / 32;          // unit positions of the warp (the last may be partial)
-    const uint32_t u0c = u0 < pe ? u0 : pb;
-    const int jl = u0 < pe ? int((pe - 1 - u0) / 32) : -1;
-    const uint32_t jlc = jl < 0 ? 0u : uint32_t(jl);
-    const LaneGeo geo = lane_geo<F>(int(u0c));
-    constexpr uint32_t JB = step_bytes<F>();
 
-    uint32_t ph = 0, s = 0;
+    const LaneGeo geo = lane_geo<F>(int(uc));
+    const bool last_full = (U % UPC) == 0;                 // every lane has a unit in the last chunk too
+    uint32_t ph = 0, s = 0, c = 0, t = 0;
     bool dead = false;
-    for (uint32_t k = 0; k < nst; ++k) {
+    float acc[RW];
+#pragma unroll
+    for (int i = 0; i < RW; ++i) acc[i] = 0.f;
+    for (uint32_t k = 0; k < nit; ++k) {
         if (!dead && !mbar_wait_bounded(&full[s], ph)) {
             if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
             dead = true;
         }
-        const uint32_t rows = min(uint32_t(SR), nrows - k * SR);
-        float acc[RW];
-#pragma unroll
-        for (int i = 0; i < RW; ++i) acc[i] = 0.f;
+        const uint32_t rows = min(uint32_t(TR), nrows - t * TR);
         if (!dead) {
-            const uint8_t *st = stages + s * pl.stage_bytes;
-            const uint8_t *ub0 = st + geo.ubase;
-            const float *sb0 = reinterpret_cast<const float *>(st + SR * RS) + u0c;
-            for (uint32_t j = 0; j < nu; ++j) {
-                const uint32_t jj = min(j, jlc);
-                const bool uv = int(j) <= jl;
-                const uint32_t u = u0c + 32u * jj;
-                uint32_t xv[16];
-                load_xp(xs, U, u, xv);
-                float cv[XC<F>::n];
+            const uint8_t *st = stages + s * uint32_t(T::STAGE);
+            const uint8_t *ub = st + rc * CB + geo.ubase;
+            const float *sp = reinterpret_cast<const float *>(st + TR * CB + rc * SB) + uc;
+            const uint32_t u = c * UPC + uc;
+            const bool uv = u < U;
+            uint32_t xv[16];
+            load_xp(xs, U, uv ? u : U - 1, xv);
+            float cv[XC<F>::n];
 #pragma unroll
-                for (int cc = 0; cc < XC<F>::n; ++cc) cv[cc] = cst[u * XC<F>::n + cc];
-                const uint8_t *ub = ub0 + jj * JB;
-                const float *sbp = sb0 + 32u * jj;
+            for (int cc = 0; cc < XC<F>::n; ++cc) cv[cc] = cst[(uv ? u : U - 1) * XC<F>::n + cc];
+            if (rows == uint32_t(TR) && (last_full || c + 1 < nch)) {
 #pragma unroll
-                for (int i = 0; i < RW; ++i) {
-                    const uint32_t r = rc + uint32_t(RC * i);
-                    const uint32_t rr = min(r, rows - 1);
-                    row_acc<F>(ub + rr * RS, sbp + rr * SS, geo, cv, xv, uv && r < rows, acc[i]);
-                }
+                for (int i = 0; i < RW; ++i)
+                    row_acc<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, cv, xv, true, acc[i]);
+            } else {
+                // ragged tile or chunk: rows past the tile's end are skipped (uniform branches), lanes past K masked
+#pragma unroll
+                for (int i = 0; i < RW; ++i)
+                    if (rc + uint32_t(RC * i) < rows)
+                        row_acc<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, cv, xv, uv, acc[i]);
+            }
+            // Release the stage; the warp that releases it last refills it with item k + NS (acq_rel: the other
+            // warps' reads of the stage happen before the copy is issued).
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t n = atom_add_acq_rel_cta(&rel[s], 1u);
+                if (n % G1_CW == G1_CW - 1 && k + NS < nit) fill(k + NS);
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
         if (++s == NS) { s = 0; ph ^= 1u; }
+        if (++c < nch) continue;
 
-        // one partial per (row, part): lanes i * (32 / RW) hold row rc + RC * i after the reduction
+        // tile done: one partial per (row, part); lanes i * (32 / RW) hold row rc + RC * i after the reduction
+        c = 0;
         const float v = warp_rows_sum<RW>(acc, lane);
-        const uint32_t lr = (k * SR) % G1_PART_ROWS;   // stage's first row within the round
+#pragma unroll
+        for (int i = 0; i < RW; ++i) acc[i] = 0.f;
+        const uint32_t lr = (t * TR) % G1_PART_ROWS;        // tile's first row within the round
         if ((lane & (32 / RW - 1)) == 0) {
             const uint32_t r = rc + uint32_t(RC) * uint32_t(lane / (32 / RW));
             if (r < rows) part[(lr + r) * P + q] = v;
         }
-        const uint32_t done = k * SR + rows;           // rows of this CTA finished after this stage
+        const uint32_t done = t * TR + rows;                // rows of this CTA finished after this tile
+        ++t;
         if (done == nrows || done % G1_PART_ROWS == 0) {
             named_bar_sync(1, G1_CW * 32);
             const uint32_t base = (done - 1) / G1_PART_ROWS * G1_PART_ROWS, cnt = done - base;
-            for (uint32_t t = uint32_t(tid); t < cnt; t += G1_CW * 32) {
-                float y = 0.f;
+            for (uint32_t r = uint32_t(tid); r < cnt; r += G1_CW * 32) {
+                float yv = 0.f;
 #pragma unroll
-                for (int pp = 0; pp < P; ++pp) y = fmaf(part[t * P + pp], uscale[pp], y);
-                a.Y[rbeg + base + t] = y;
+                for (int pp = 0; pp < P; ++pp) yv = fmaf(part[r * P + pp], uscale[pp], yv);
+                a.Y[rbeg + base + r] = yv;
             }
             if (done != nrows) named_bar_sync(1, G1_CW * 32);   // partials of the next round overwrite these
         }
     }
+    // Never leave with a copy still writing shared memory: the last fill of every stage has landed (bounded; only a
+    // warp that gave up on a wait can get here before that).
+    if (dead && lane == 0) {
+        for (uint32_t j = (nit > NS ? nit - NS : 0u); j < nit; ++j)
+            if (!mbar_wait_bounded(&full[j % NS], (j / NS) & 1u)) break;
+    }
 }
 
-// Shared-memory plan of one launch: returns false when even one stage plus the staged activations do not fit.
+// Shared-memory plan of one launch: returns false when two stages plus the staged activations do not fit `budget`.
 template <int F>
-static bool plan_gemv1(const GemvArgs &a, int sr, uint32_t budget, G1Plan *pl) {
+static bool plan_gemv1(const GemvArgs &a, uint32_t budget, G1Plan *pl) {
+    using T = T1<F>;
     const uint32_t U = uint32_t(a.K / 32);
-    const uint32_t RS = uint32_t(a.row_stride), SS = uint32_t(a.scale_stride);
     pl->off_part = G1_HDR;
-    pl->off_xs = pl->off_part + G1_PART_ROWS * (G1_CW / 1) * 4;        // room for P = 8 partials per row
+    pl->off_xs = pl->off_part + G1_PART_ROWS * T::P * 4;
     pl->off_cst = pl->off_xs + uint32_t(round_up(int64_t(U) * 64, 128));
-    pl->off_stages = pl->off_cst + uint32_t(round_up(int64_t(U) * XC<F>::n * 4, 128));
-    pl->stage_bytes = uint32_t(round_up(int64_t(sr) * RS + (Fmt<F>::sb ? 0 : int64_t(sr) * SS * 4), 128));
-    // + 32: the Q3S unpack reads the word pair holding a unit's scale fields, up to 4 bytes past its row
+    pl->off_stages = uint32_t(round_up(pl->off_cst + int64_t(U) * XC<F>::n * 4, 1024));
+    // + 32: the Q3S / Q6S unpack reads up to 4 bytes past a row chunk
     const int64_t room = int64_t(budget) - pl->off_stages - 32;
-    if (room < int64_t(pl->stage_bytes) * 2) return false;
-    pl->ns = int(room / pl->stage_bytes < G1_MAXNS ? room / pl->stage_bytes : G1_MAXNS);
-    pl->smem = pl->off_stages + uint32_t(pl->ns) * pl->stage_bytes + 32;
+    if (room < int64_t(T::STAGE) * 2) return false;
+    pl->ns = int(room / T::STAGE < G1_MAXNS ? room / T::STAGE : G1_MAXNS);
+    pl->smem = pl->off_stages + uint32_t(pl->ns) * uint32_t(T::STAGE) + 32;
     return true;
 }
 
-template <int F, int RC, int RW>
-static cudaError_t launch_gemv1_cfg(const GemvArgs &a, cudaStream_t st) {
-    // Two CTAs per SM when the ring keeps at least 3 stages within half of the SM's shared memory; else one.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tensor map over a row-major byte matrix [rows][stride] viewed as 8-byte words: boxes of box_words x box_rows.
+static cudaError_t encode_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t stride_bytes,
+                               uint32_t box_words, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {cuuint64_t(stride_bytes / 8), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(stride_bytes)};
+    const cuuint32_t box[2] = {box_words, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int F>
+static cudaError_t launch_gemv1(const GemvArgs &a, cudaStream_t st) {
+    using T = T1<F>;
+    // Two CTAs per SM (the next product's CTA streams its first weights while this one finishes) when the kernel
+    // fits twice on an SM and the ring keeps at least 3 stages within half of the shared memory; else one.
     G1Plan pl;
-    if (!plan_gemv1<F>(a, RC * RW, 110u * 1024u, &pl) || pl.ns < 3) {
-        if (!plan_gemv1<F>(a, RC * RW, 227u * 1024u, &pl)) return cudaErrorInvalidValue;
+    if (!(G1_CORES && plan_gemv1<F>(a, 110u * 1024u, &pl) && pl.ns >= 3)) {
+        if (!plan_gemv1<F>(a, 227u * 1024u, &pl)) return cudaErrorInvalidValue;
+    }
+    CUtensorMap tmc, tms;
+    cudaError_t e = encode_rows(&tmc, a.packed, a.N, a.row_stride, uint32_t(T::CB / 8), uint32_t(T::TR));
+    if (e != cudaSuccess) return e;
+    if constexpr (T::SB > 0) {
+        e = encode_rows(&tms, a.gscale, a.N, a.scale_stride * 4, uint32_t(T::SB / 8), uint32_t(T::TR));
+        if (e != cudaSuccess) return e;
+    } else {
+        tms = tmc;
     }
     static int opted[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!opted[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemv1_kernel<F, RC, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
+        e = cudaFuncSetAttribute(gemv1_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         opted[dev] = 1;
     }
@@ -633,22 +725,7 @@ static cudaError_t launch_gemv1_cfg(const GemvArgs &a, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = a.weight_prefetch ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv1_kernel<F, RC, RW>, a, pl);
-}
-
-// Stage shape from the row size: about 8-28 KB per stage (one bulk copy moves it), 2 row classes x 4 K parts while
-// a part of a row still gives every lane a unit (K >= 4096) and rows are short, 1 row class x 8 parts for long rows.
-template <int F>
-static cudaError_t launch_gemv1(const GemvArgs &a, cudaStream_t st) {
-    const int64_t row = a.row_stride + (Fmt<F>::sb ? 0 : a.scale_stride * 4);
-    constexpr int64_t LIM = 28 * 1024;
-    if (a.K <= 16384) {
-        if (8 * row <= LIM) return launch_gemv1_cfg<F, 2, 4>(a, st);
-        if (4 * row <= LIM) return launch_gemv1_cfg<F, 2, 2>(a, st);
-        if (2 * row <= LIM) return launch_gemv1_cfg<F, 2, 1>(a, st);
-    }
-    if (2 * row <= LIM) return launch_gemv1_cfg<F, 1, 2>(a, st);
-    return launch_gemv1_cfg<F, 1, 1>(a, st);
+    return cudaLaunchKernelEx(&cfg, gemv1_kernel<F>, tmc, tms, a, pl);
 }
 
 namespace {
