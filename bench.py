@@ -213,6 +213,125 @@ def decode_7b_extra(qp, torch, synth, dev, steps=10):
     return out
 
 
+def _time_graph(torch, fn, dev, reps=5, warm=3):
+    """Capture fn (a sequence of launches on its own stream) in one CUDA graph; seconds per replay."""
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        fn(s)
+        torch.cuda.synchronize(dev)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            fn(s)
+        for _ in range(warm):
+            gr.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(s)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / 1e3 / reps
+
+
+# FP32 FMA peak of the CUDA cores at the maximum SM clock (152 SMs x 128 lanes x 2 flops x 2.07 GHz); the small-batch
+# products are bound by it once M multiply-adds per weight outweigh the packed bytes.
+FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def int4_4096_extra(qp, torch, synth, dev, hbm_peak):
+    """INT4 group-32 GEMV on the 4096x4096 matrix with 0.1% outliers (the INT4 workload), batch 1."""
+    N = K = 4096
+    W = synth.normal_with_outliers((N, K), 0.02, 0.001, 0.1, 0.5, seed=0).to(dev)
+    p0, g0 = qp.qpack_quantize_pack(qp.Q4G32, W)
+    del W
+    wb = qp.layout(qp.Q4G32, N, K)["weight_bytes"]
+    R = max(8, int(-(-8 * (126 << 20) // wb)))
+    P = [p0.clone() for _ in range(R)]
+    G = [g0.clone() for _ in range(R)]
+    X = synth.normal((R, K), 1.0, seed=1, device=dev, dtype=torch.float16)
+    Y = torch.empty((R, N), device=dev)
+
+    def fn(s):
+        for i in range(R):
+            qp.qgemv(qp.Q4G32, P[i], G[i], N, K, X[i], Y[i], stream=s)
+
+    t = _time_graph(torch, fn, dev, reps=20) / R
+    return {"GBps": wb / t / 1e9, "pct_hbm_peak": wb / t / 1e9 / hbm_peak, "us_per_gemv": t * 1e6,
+            "bytes_per_gemv": wb, "copies": R}
+
+
+def small_batch_extra(qp, torch, synth, dev, hbm_peak):
+    """Decode products with M = 1..16 activation rows over 80 layers of 70B-shaped MLP weights (gate/up 28672x8192,
+    down 8192x28672, Laplace(0, 0.01)), streamed in turn: one pass = 240 products."""
+    shapes = [(28672, 8192), (28672, 8192), (8192, 28672)]
+    out = {}
+    for name in ("Q4G32", "Q5S"):
+        fmt = qp.FORMATS[name]
+        mats, total, weights = [], 0, 0
+        for layer in range(80):
+            for mi, (N, K) in enumerate(shapes):
+                W = synth.laplace((N, K), 0.01, seed=synth.seed_for(4, layer, mi), device=dev)
+                p, g = qp.qpack_quantize_pack(fmt, W)
+                del W
+                mats.append((p, g, N, K))
+                total += qp.layout(fmt, N, K)["weight_bytes"]
+                weights += N * K
+        res = {}
+        for M in (1, 2, 4, 8, 16):
+            X = {K: synth.normal((M, K), 1.0, seed=100 + M + K, device=dev, dtype=torch.float16) for K in (8192, 28672)}
+            Y = {N: torch.empty((M, N), device=dev) for N in (8192, 28672)}
+
+            def fn(s):
+                for p, g, N, K in mats:
+                    qp.qgemm_small(fmt, p, g, N, K, X[K], Y[N], stream=s)
+
+            t = _time_graph(torch, fn, dev, reps=3)
+            tf = 2.0 * M * weights / t / 1e12
+            res[f"M{M}"] = {"GBps": total / t / 1e9, "pct_hbm_peak": total / t / 1e9 / hbm_peak,
+                            "TFLOPs": tf, "pct_ffma_peak": tf / FFMA_TFLOPS,
+                            "tok_per_s_equiv": M / t, "ms_per_pass": t * 1e3}
+        out[name] = {"bytes_per_pass": total, "launches_per_pass": len(mats), **res}
+        del mats
+        torch.cuda.empty_cache()
+    return out
+
+
+def prefill_extra(qp, torch, synth, dev, bf16_peak, hbm_peak):
+    """Prefill GEMM (M = 2048 bf16 tokens) on the tensor cores, and the quantize+pack kernels on the same fp16
+    matrices (INT4 14336x4096, 6-bit 4096x14336; Laplace(0, 0.02), seed 7)."""
+    out = {"gemm": {}, "quantize_pack": {}}
+    M = 2048
+    for name, (N, K) in (("Q4G32", (14336, 4096)), ("Q6S", (4096, 14336))):
+        fmt = qp.FORMATS[name]
+        W = synth.laplace((N, K), 0.02, seed=7, device=dev, dtype=torch.float16)
+        p, g = qp.qpack_quantize_pack(fmt, W)
+        X = synth.normal((M, K), 1.0, seed=8, device=dev, dtype=torch.bfloat16)
+        Y = torch.empty((M, N), device=dev, dtype=torch.bfloat16)
+
+        def fn(s):
+            qp.qgemm_prefill(fmt, p, g, N, K, X, Y, stream=s)
+
+        t = _time_graph(torch, fn, dev, reps=10)
+        tf = 2.0 * M * N * K / t / 1e12
+        out["gemm"][f"{name}_{N}x{K}"] = {"TFLOPs": tf, "pct_bf16_peak": tf / bf16_peak, "us": t * 1e6, "M": M}
+        for qn in ("Q4G32", "Q2S", "Q3S", "Q5S", "Q6S"):
+            qf = qp.FORMATS[qn]
+            pk, gk = qp.alloc_packed(qf, N, K, dev)
+            lay = qp.layout(qf, N, K)
+
+            def qfn(s):
+                qp.qpack_quantize_pack(qf, W, pk, gk, stream=s)
+
+            tq = _time_graph(torch, qfn, dev, reps=10)
+            moved = W.numel() * 2 + lay["weight_bytes"]
+            out["quantize_pack"][f"{qn}_{N}x{K}"] = {"GBps": moved / tq / 1e9, "pct_hbm_peak": moved / tq / 1e9 / hbm_peak,
+                                                     "us": tq * 1e6}
+        del W, p, g, X, Y
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
@@ -324,7 +443,10 @@ def run_ours(args, world, rank, local):
         if not args.no_extra:
             del P, X, Y
             torch.cuda.empty_cache()
-            extra = {"decode_7b": decode_7b_extra(qp, torch, synth, dev)}
+            extra = {"decode_7b": decode_7b_extra(qp, torch, synth, dev),
+                     "int4_4096": int4_4096_extra(qp, torch, synth, dev, hbm_peak),
+                     "small_batch_70b_mlp": small_batch_extra(qp, torch, synth, dev, hbm_peak),
+                     "prefill_2048": prefill_extra(qp, torch, synth, dev, bf16_peak, hbm_peak)}
 
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["csrc_digest"] == csrc_digest() else None
     line = {
