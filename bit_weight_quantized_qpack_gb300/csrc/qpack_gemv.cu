@@ -4,10 +4,10 @@
 // (2/3/5/6-bit article, lpnh.cn/news/2857666, §1.2: time per token = weight bytes / bandwidth; DBHOO-CIM
 // article, pwwt.cn/news/4452170, §3.3: dequantization must stay fused, never materialised).
 //
-// Batch-1 kernel (gemv1_kernel), one persistent CTA per SM (two fit, so consecutive products overlap):
-//   warp 8       producer: 2-D TMA tensor copies of (8-row tile x K chunk) boxes of the packed rows into a ring of
+// Batch-1 kernel (gemv1_kernel<F, 1>), one persistent CTA per SM:
+//   warp 16      producer: 2-D TMA tensor copies of (row tile x K chunk) boxes of the packed rows into a ring of
 //                shared-memory stages (completion on mbarriers, L2 evict-first because each byte is used once).
-//   warps 0..7   consumers: row class x K part of every stage; lane l owns one 32-weight unit of each chunk.
+//   warps 0..15  consumers: row class x K part of every stage; lane l owns one 32-weight unit of each chunk.
 // Unpacking (2/3/5/6-bit article §3.3: separate unpack from multiply-add, factor s*(q.x) + m*sum(x)): codes are
 // OR-ed into the mantissa of an fp16 1024.0 with one LOP3 per pair of weights, so a half holds 1024 + u*2^p
 // exactly, p being the code's bit position inside its 16-bit half. The activations are staged in shared memory
@@ -18,8 +18,8 @@
 // stores one partial per K part in shared memory; the partials are scaled back by each part's power of two and
 // summed in a fixed order (deterministic) before y is written.
 //
-// Small-batch kernel (stream_kernel, M = 2..16): same producer; each unit is dequantized exactly to fp32
-// registers and multiplied against the M activation rows.
+// Small batches (M = 2..16) use the same kernel with MT activation rows: each unit-row is unpacked once and
+// multiplied against every staged activation row; rows beyond what shared memory holds go in further launches.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -34,37 +34,13 @@ __device__ int g_fault_gemv = 0;
 
 namespace {
 
-constexpr int TILE_R = 4;                // rows per tile
-constexpr int CHW = 4096;                // weights per chunk (stage width)
-constexpr int UPC = CHW / 32;            // 32-weight units per chunk
 constexpr uint32_t MAGIC2 = 0x64006400u; // fp16 1024.0 in both halves
 constexpr uint32_t MAGICF = 0x4B000000u; // fp32 2^23
-
-template <int F> struct Geo {
-    // bytes of one row's chunk in shared memory (codes; Q4G32 scales are a separate region)
-    static constexpr int chunk_bytes = Fmt<F>::sb ? (CHW / 256) * Fmt<F>::bytes : CHW / 2;
-    static constexpr int scale_bytes = Fmt<F>::sb ? 0 : (CHW / 32) * 4;
-    static constexpr int stage_bytes = TILE_R * (chunk_bytes + scale_bytes);
-};
 
 __device__ __forceinline__ uint16_t lo16(uint32_t v) { return uint16_t(v & 0xFFFFu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t v) { return uint16_t(v >> 16); }
 __device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
-__device__ __forceinline__ float hbits(const uint8_t *p) { return h2f_bits(*reinterpret_cast<const uint16_t *>(p)); }
 __device__ __forceinline__ float small_int_f(uint32_t bits_or_magic) { return __uint_as_float(bits_or_magic) - 8388608.0f; }
-
-// Read `n` consecutive 32-bit words starting at a 2-byte aligned shared-memory address.
-template <int n>
-__device__ __forceinline__ void lds_words_a2(const uint8_t *p, uint32_t *w) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t *base = reinterpret_cast<const uint32_t *>(a & ~uintptr_t(3));
-    const uint32_t sh = uint32_t(a & 3u) * 8u;   // 0 or 16
-    uint32_t r[n + 1];
-#pragma unroll
-    for (int i = 0; i <= n; ++i) r[i] = base[i];
-#pragma unroll
-    for (int i = 0; i < n; ++i) w[i] = __funnelshift_r(r[i], r[i + 1], sh);
-}
 
 // acc += lo(codes) * xa + hi(codes) * xb with exact products (fp16 x fp16 -> fp32 FMA).
 __device__ __forceinline__ float fma2h(uint32_t codes, uint16_t xa, uint16_t xb, float acc) {
@@ -324,6 +300,158 @@ __device__ __forceinline__ void row_acc(const uint8_t *u, const float *sp, const
     }
 }
 
+// ------------------------------------------------------------------------------------------------------------
+// Multi-row form of the same math (small-batch products): a unit-row is unpacked once into 16 words of fp16 code
+// pairs (the LOP3 outputs of row_acc, in the same order) plus its sub-block scale factors, then multiplied against
+// several staged activation rows. hw[j] holds the codes of staging slots hslot<F>(j, 0) (low half) and
+// hslot<F>(j, 1) (high half); words 0..7 belong to sub-block 0 and 8..15 to sub-block 1 (formats with one 32-weight
+// sub-block use the same split for two independent accumulators).
+// ------------------------------------------------------------------------------------------------------------
+template <int F>
+__host__ __device__ constexpr int hslot(int j, int h) {
+    if constexpr (F == FMT_Q3S) return 2 * j + h;
+    else if constexpr (F == FMT_Q2S) return 16 * (j / 8) + 4 * (j % 2) + (j % 8) / 2 + 8 * h;
+    else return 8 * (j / 4) + j % 4 + 4 * h;
+}
+struct URow {
+    uint32_t hw[16];
+    float f0, f1;   // sub-block scale factors (w' = f * code for the symmetric part)
+    float g0, g1;   // minima factors of the asymmetric formats (dmin * M_j), else 0
+};
+__device__ __forceinline__ void unpack_nib(uint32_t c, uint32_t *hw) {
+    const uint32_t c2 = c >> 8;
+    hw[0] = lop3_and_or(c, 0x000F000Fu, MAGIC2);
+    hw[1] = lop3_and_or(c, 0x00F000F0u, MAGIC2);
+    hw[2] = lop3_and_or(c2, 0x000F000Fu, MAGIC2);
+    hw[3] = lop3_and_or(c2, 0x00F000F0u, MAGIC2);
+}
+template <int HB>
+__device__ __forceinline__ void unpack_nib_hi(uint32_t c, uint32_t X, uint32_t *hw) {
+    constexpr uint32_t mlo = (HB == 1) ? 0x00100010u : 0x00300030u;
+    constexpr uint32_t mhi = (HB == 1) ? 0x01000100u : 0x03000300u;
+    constexpr int s0 = 4, s1 = (HB == 1) ? 7 : 6, s2 = (HB == 1) ? 2 : 0, s3 = (HB == 1) ? 5 : 2;
+    const uint32_t c2 = c >> 8;
+    hw[0] = lop3_and_or(X << s0, mlo, lop3_and_or(c, 0x000F000Fu, MAGIC2));
+    hw[1] = lop3_and_or(X << s1, mhi, lop3_and_or(c, 0x00F000F0u, MAGIC2));
+    hw[2] = lop3_and_or(X << s2, mlo, lop3_and_or(c2, 0x000F000Fu, MAGIC2));
+    hw[3] = lop3_and_or(X << s3, mhi, lop3_and_or(c2, 0x00F000F0u, MAGIC2));
+}
+__device__ __forceinline__ void unpack_crumb(uint32_t c, uint32_t *hw) {
+    const uint32_t c2 = c >> 8;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t m = (3u << (2 * k)) * 0x00010001u;
+        hw[2 * k] = lop3_and_or(c, m, MAGIC2);
+        hw[2 * k + 1] = lop3_and_or(c2, m, MAGIC2);
+    }
+}
+__device__ __forceinline__ void unpack_tri(uint32_t W0, uint32_t W1, uint32_t W2, uint32_t *hw) {
+    hw[0] = lop3_and_or(W0, 0x00070007u, MAGIC2);
+    hw[1] = lop3_and_or(W0, 0x00380038u, MAGIC2);
+    hw[2] = lop3_and_or(W0, 0x01C001C0u, MAGIC2);
+    hw[3] = lop3_and_or(W1, 0x000E000Eu, MAGIC2);
+    hw[4] = lop3_and_or(W1, 0x00700070u, MAGIC2);
+    hw[5] = lop3_and_or(W1, 0x03800380u, MAGIC2);
+    hw[6] = lop3_and_or(W2, 0x001C001Cu, MAGIC2);
+    hw[7] = lop3_and_or(W2, 0x00E000E0u, MAGIC2);
+}
+
+// Unpack one unit-row (same operands as row_acc); `on` false zeroes its scale factors.
+template <int F>
+__device__ __forceinline__ void unpack_row(const uint8_t *u, const float *sp, const LaneGeo &g, bool on, URow &r) {
+    r.g0 = r.g1 = 0.f;
+    if constexpr (F == FMT_Q4G32) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(u);
+        r.f0 = r.f1 = on ? sp[0] : 0.f;
+        unpack_nib(w.x, r.hw); unpack_nib(w.y, r.hw + 4); unpack_nib(w.z, r.hw + 8); unpack_nib(w.w, r.hw + 12);
+    } else if constexpr (F == FMT_Q2S) {
+        const uint32_t w0 = lds32(u), w1 = lds32(u + 4);
+        const uint32_t dd = on ? lds32(u + g.o2) : 0u;
+        const uint32_t lm = *reinterpret_cast<const uint16_t *>(u + g.o1);
+        const uint32_t t = __byte_perm(lm, 0u, 0x4140u);
+        const uint32_t hl = hadd2_bits(lop3_and_or(t, 0x000F000Fu, MAGIC2), HNEG1024);
+        const uint32_t hm = hadd2_bits(lop3_and_or(t >> 4, 0x000F000Fu, MAGIC2), HNEG1024);
+        r.f0 = fma_h(lo16(hl), lo16(dd), 0.f);
+        r.f1 = fma_h(hi16(hl), lo16(dd), 0.f);
+        r.g0 = fma_h(lo16(hm), hi16(dd), 0.f);
+        r.g1 = fma_h(hi16(hm), hi16(dd), 0.f);
+        unpack_crumb(w0, r.hw); unpack_crumb(w1, r.hw + 8);
+    } else if constexpr (F == FMT_Q3S) {
+        const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
+        const uint32_t w0 = wp[0], w1 = wp[1];
+        const uint32_t *qp = reinterpret_cast<const uint32_t *>(u + g.o1);
+        const uint32_t w2 = qp[0], w3 = qp[1];
+        const uint32_t *fp = reinterpret_cast<const uint32_t *>(u + g.o2);
+        const uint32_t f = __funnelshift_r(fp[0], fp[1], g.sh1);
+        const uint32_t lh = hadd2_bits(lop3_and_or(lop3_sel(f << 10, f, 0xFFFF0000u), 0x003F003Fu, MAGIC2), HNEG1024);
+        const uint16_t D = on ? *reinterpret_cast<const uint16_t *>(u + g.o3) : uint16_t(0);
+        r.f0 = fma_h(lo16(lh), D, 0.f);
+        r.f1 = fma_h(hi16(lh), D, 0.f);
+        unpack_tri(__byte_perm(w0, w1, g.p0), __byte_perm(w0, w1, g.p1), __byte_perm(w0, w1, g.p2), r.hw);
+        unpack_tri(__byte_perm(w2, w3, g.q0), __byte_perm(w2, w3, g.q1), __byte_perm(w2, w3, g.q2), r.hw + 8);
+    } else if constexpr (F == FMT_Q5S) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(u);
+        const uint32_t H = lds32(u + g.o1);
+        const uint4 fld = *reinterpret_cast<const uint4 *>(u + g.o2);
+        const uint32_t ddw = on ? fld.w : 0u;
+        const float2 Dd = __half22float2(*reinterpret_cast<const __half2 *>(&ddw));
+        const uint64_t lo64 = (uint64_t(fld.y) << 32) | fld.x, hi64 = (uint64_t(fld.z) << 32) | fld.y;
+        const float L = small_int_f(lop3_and_or(uint32_t(lo64 >> g.sh0), 63u, MAGICF));
+        const float Mv = small_int_f(lop3_and_or(uint32_t(hi64 >> (g.sh1 - 32u)), 63u, MAGICF));
+        r.f0 = r.f1 = Dd.x * L;
+        r.g0 = Dd.y * Mv;
+        unpack_nib_hi<1>(w.x, lop3_sel(H, H << 12, 0x0000FFFFu), r.hw);
+        unpack_nib_hi<1>(w.y, lop3_sel(H >> 8, H << 4, 0x0000FFFFu), r.hw + 4);
+        unpack_nib_hi<1>(w.z, lop3_sel(H >> 16, H >> 4, 0x0000FFFFu), r.hw + 8);
+        unpack_nib_hi<1>(w.w, lop3_sel(H >> 24, H >> 12, 0x0000FFFFu), r.hw + 12);
+    } else {
+        const uint32_t sh = g.sh0;
+        const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
+        const uint32_t r0 = wp[0], r1 = wp[1], r2 = wp[2], r3 = wp[3], r4 = wp[4];
+        const uint32_t *hp = reinterpret_cast<const uint32_t *>(u + g.o1);
+        const uint32_t q0 = hp[0], q1 = hp[1], q2 = hp[2];
+        const uint32_t h0 = __funnelshift_r(q0, q1, sh), h1 = __funnelshift_r(q1, q2, sh);
+        const uint32_t lv = *reinterpret_cast<const uint16_t *>(u + g.o2);
+        const uint32_t lh = hadd2_bits(lop3_xor_or(__byte_perm(lv, 0u, 0x4140u), 0x00800080u, MAGIC2), HNEG1152);
+        const uint16_t D = on ? *reinterpret_cast<const uint16_t *>(u + g.o3) : uint16_t(0);
+        r.f0 = fma_h(lo16(lh), D, 0.f);
+        r.f1 = fma_h(hi16(lh), D, 0.f);
+        unpack_nib_hi<2>(__funnelshift_r(r0, r1, sh), __byte_perm(h0, 0u, 0x4140u), r.hw);
+        unpack_nib_hi<2>(__funnelshift_r(r1, r2, sh), __byte_perm(h0, 0u, 0x4342u), r.hw + 4);
+        unpack_nib_hi<2>(__funnelshift_r(r2, r3, sh), __byte_perm(h1, 0u, 0x4140u), r.hw + 8);
+        unpack_nib_hi<2>(__funnelshift_r(r3, r4, sh), __byte_perm(h1, 0u, 0x4342u), r.hw + 12);
+    }
+}
+
+// acc += sum_i w'_i x_i of an unpacked unit-row against one staged activation row (xv, c: that row's unit constants).
+template <int F>
+__device__ __forceinline__ void dot_row(const URow &r, const uint32_t *xv, const float *c, float &acc) {
+    float a0, a1;
+    if constexpr (F == FMT_Q4G32 || F == FMT_Q5S) { a0 = -c[0]; a1 = 0.f; }
+    else if constexpr (F == FMT_Q2S) { a0 = -c[0]; a1 = -c[2]; }
+    else { a0 = -c[0]; a1 = -c[1]; }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        a0 = fma_h(lo16(r.hw[j]), xh(xv, hslot<F>(j, 0)), a0);
+        a0 = fma_h(hi16(r.hw[j]), xh(xv, hslot<F>(j, 1)), a0);
+        a1 = fma_h(lo16(r.hw[8 + j]), xh(xv, hslot<F>(8 + j, 0)), a1);
+        a1 = fma_h(hi16(r.hw[8 + j]), xh(xv, hslot<F>(8 + j, 1)), a1);
+    }
+    if constexpr (F == FMT_Q4G32) {
+        acc = fmaf(r.f0, a0 + a1, acc);
+    } else if constexpr (F == FMT_Q5S) {
+        acc = fmaf(r.f0, a0 + a1, acc);
+        acc = fmaf(-r.g0, c[1], acc);
+    } else {
+        acc = fmaf(r.f0, a0, acc);
+        acc = fmaf(r.f1, a1, acc);
+        if constexpr (F == FMT_Q2S) {
+            acc = fmaf(-r.g0, c[1], acc);
+            acc = fmaf(-r.g1, c[3], acc);
+        }
+    }
+}
+
 // Staged activations: the 16 words of unit u are four 16-byte vectors at vector index t * U + u (t = 0..3, U = K / 32
 // units per row), so consecutive lanes (consecutive units) read consecutive vectors. Half-unit hh (elements
 // 16 hh .. 16 hh + 15) is words 8 hh .. 8 hh + 7, i.e. vectors t = 2 hh and 2 hh + 1.
@@ -412,56 +540,61 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 }  // namespace
 
 // ------------------------------------------------------------------------------------------------------------
-// Batch-1 fused dequant-GEMV kernel.
+// Fused dequant-GEMV kernel for MT activation rows (MT = 1: the batch-1 decode product; MT = 2..16: small batches).
 //
 // The packed matrix is read through a 2-D TMA tensor map over (rows x 8-byte words): one tensor copy moves a tile of
-// TR = 8 rows x one K chunk (CHW weights) into a shared-memory stage, so every stage has the same compile-time layout
+// TR rows x one K chunk (CHW weights) into a shared-memory stage, so every stage has the same compile-time layout
 // (row r of the chunk at r * CB bytes) whatever K is; words past the row end and rows past N arrive as zeros and are
-// masked by the consumers. One CTA per SM, sized so that two fit on an SM: the next product in the stream, launched
-// as a programmatic dependent, starts streaming its weights while this one finishes.
-// Warp 8 is the producer (one lane issues the copies into a ring of stages). Warps 0..7 consume every stage together:
-// warp w handles row class rc = w / P (rows rc, rc + RC, ...: RW rows) over K part q = w % P of the chunk (32 units;
-// lane l owns unit 32 q + l of every chunk) and keeps the staged activations of that unit in registers across its
-// rows. Row sums accumulate over the chunks of a tile; then each warp reduces its lanes with shuffles and stores one
-// partial per (row, part), and the P partials of a row are summed in a fixed order (deterministic) every G1_PART_ROWS
-// rows. Activations are staged per part with the part's own power-of-two scale (max |x| * 2^E in [2^14, 2^15)).
+// masked by the consumers. One CTA per SM; the next product in the stream, launched as a programmatic dependent,
+// starts streaming its weights as soon as this CTA leaves its SM.
+// Warp 16 is the producer (one lane issues the first copies; every later copy is issued by the consumer warp that
+// releases a stage last). Warps 0..15 consume every stage together: warp w handles row class rc = w / P (rows rc,
+// rc + RC, ...: RW rows) over K part q = w % P of the chunk (32 units; lane l owns unit 32 q + l of every chunk).
+// With MT = 1 a lane unpacks and multiplies in one pass (row_acc); with MT > 1 it unpacks each unit-row once
+// (unpack_row) and multiplies it against the MT staged activation rows (dot_row), so every weight is read and
+// unpacked once for the whole batch. Row sums accumulate over the chunks of a tile; then each warp reduces its lanes
+// with shuffles and stores one partial per (row, activation row, part), and the P partials are summed in a fixed
+// order (deterministic). Activations are staged per (row, part) with a power-of-two scale (max |x| * 2^E in
+// [2^14, 2^15)).
 // ------------------------------------------------------------------------------------------------------------
 constexpr int G1_CW = 16;                      // consumer warps
-template <int F> struct T1 {
+template <int F, int MT = 1> struct T1 {
     static constexpr int CHW = (F == FMT_Q5S || F == FMT_Q6S) ? 2048 : 4096;      // weights per K chunk
     static constexpr int UPC = CHW / 32;                                          // units per chunk
     static constexpr int P = UPC / 32;                                            // K parts of 32 units
     static constexpr int RC = G1_CW / P;                                          // row classes
-    static constexpr int RW = F == FMT_Q4G32 ? 4 : (P == 4 ? 8 : 4);              // rows per warp and stage
+    static constexpr int RW = MT > 2 ? 2 : (F == FMT_Q4G32 ? 4 : (P == 4 ? 8 : 4)); // rows per warp and stage
     static constexpr int TR = RC * RW;                                            // rows per tile
+    static constexpr int PR = MT > 1 ? (256 / MT > TR ? 256 / MT : TR) : 256;     // rows per partial-sum round
     static constexpr int CB = Fmt<F>::sb ? (CHW / 256) * Fmt<F>::bytes : CHW / 2; // code bytes per row chunk
     static constexpr int SB = Fmt<F>::sb ? 0 : (CHW / 32) * 4;                    // Q4G32 scale bytes per row chunk
     static constexpr int TX = TR * (CB + SB);                                     // bytes a stage receives
     static constexpr int STAGE = (TX + 127) / 128 * 128;
     static_assert(CB % 16 == 0 && CB / 8 <= 256 && SB / 8 <= 256, "tensor-map box limits");
+    static_assert(PR % TR == 0 && RW * MT <= 32, "tile and reduction shapes");
 };
 constexpr int G1_THREADS = (G1_CW + 1) * 32;
-constexpr int G1_CORES = G1_CW <= 8 ? 1 : 0;   // two CTAs per SM possible (registers and threads)
 constexpr int G1_MAXNS = 16;                   // stages in the ring at most
 constexpr int G1_PRE = 1;                      // stage fills issued before the activations are staged
-constexpr int G1_PART_ROWS = 256;              // rows per partial-sum round
-constexpr uint32_t G1_HDR = 512;               // mbarriers (2 x 16 x 8 B) + misc words
+constexpr uint32_t G1_HDR = 1024;              // mbarriers, release counters, per-(row, part) scales
 
 struct G1Plan {
     uint32_t off_part, off_xs, off_cst, off_stages, smem;
     int ns;
 };
 
-template <int F>
-__global__ void __launch_bounds__(G1_THREADS, 1 + G1_CORES)
+template <int F, int MT>
+__global__ void __launch_bounds__(G1_THREADS, 1)
     gemv1_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                  GemvArgs a, G1Plan pl) {
-    using T = T1<F>;
-    constexpr int P = T::P, RC = T::RC, RW = T::RW, TR = T::TR, CB = T::CB, SB = T::SB, UPC = T::UPC;
-    static_assert(G1_PART_ROWS % TR == 0, "a partial-sum round is a whole number of tiles");
+    using T = T1<F, MT>;
+    constexpr int P = T::P, RC = T::RC, RW = T::RW, TR = T::TR, CB = T::CB, SB = T::SB, UPC = T::UPC, PR = T::PR;
+    constexpr int NX = XC<F>::n;
+    constexpr uint32_t NT = G1_CW * 32;
     extern __shared__ __align__(1024) uint8_t smem_g1[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t N = uint32_t(a.N), K = uint32_t(a.K), U = K / 32;
+    const uint32_t Mg = uint32_t(a.M);                     // activation rows of this launch (<= MT)
     // this CTA's rows: a contiguous range; the row counts of any two CTAs differ by at most one
     const uint32_t rq = N / gridDim.x, rm = N % gridDim.x, b = blockIdx.x;
     const uint32_t rbeg = b * rq + min(b, rm), nrows = rq + (b < rm ? 1u : 0u);
@@ -472,16 +605,16 @@ __global__ void __launch_bounds__(G1_THREADS, 1 + G1_CORES)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem_g1);                  // [NS] stage filled
     uint32_t *rel = reinterpret_cast<uint32_t *>(smem_g1 + G1_MAXNS * 8);    // [NS] warps done with the stage
     uint64_t *xready = reinterpret_cast<uint64_t *>(smem_g1 + G1_MAXNS * 12);  // activations staged
-    float *uscale = reinterpret_cast<float *>(smem_g1 + 2 * G1_MAXNS * 8);   // [P]: 2^-E of each part
-    uint32_t *pmax = reinterpret_cast<uint32_t *>(smem_g1 + 2 * G1_MAXNS * 8 + 32);   // [P]: max |x| bits per part
+    float *uscale = reinterpret_cast<float *>(smem_g1 + 256);                // [MT][P]: 2^-E per (row, part)
+    uint32_t *pmax = reinterpret_cast<uint32_t *>(smem_g1 + 512);            // [MT][P]: max |x| bits
     float *part = reinterpret_cast<float *>(smem_g1 + pl.off_part);
-    uint4 *xs = reinterpret_cast<uint4 *>(smem_g1 + pl.off_xs);
-    float *cst = reinterpret_cast<float *>(smem_g1 + pl.off_cst);
+    uint4 *xs = reinterpret_cast<uint4 *>(smem_g1 + pl.off_xs);              // [MT][4][U]
+    float *cst = reinterpret_cast<float *>(smem_g1 + pl.off_cst);            // [MT][U][NX]
     uint8_t *stages = smem_g1 + pl.off_stages;
 
     if (tid == 0) {
         for (uint32_t s = 0; s < NS; ++s) { mbar_init(&full[s], 1); rel[s] = 0; }
-        for (int i = 0; i < P; ++i) pmax[i] = 0;
+        for (int i = 0; i < MT * P; ++i) pmax[i] = 0;
         mbar_init(xready, 1);
         fence_mbar_init();
     }
@@ -499,8 +632,6 @@ __global__ void __launch_bounds__(G1_THREADS, 1 + G1_CORES)
 
     if (warp == G1_CW) {
         // ------------------------------------ producer ------------------------------------
-        // The first NS fills; every later fill is issued by the consumer warp that releases the stage last, so
-        // nobody polls for free stages.
         if (lane == 0) {
             // Packed weights are read before the previous grid has finished only when the caller opted in
             // (QPACK_OPT_WEIGHT_PREFETCH: weights are not written by the kernel just before this one). Only the first
@@ -522,40 +653,77 @@ __global__ void __launch_bounds__(G1_THREADS, 1 + G1_CORES)
     const uint32_t uc = q * 32u + uint32_t(lane);           // this lane's unit within every chunk
     pdl_wait();                  // x (and y) may belong to the previous grid
     {
-        // Staging: thread t handles units t, t + NT, ... (K <= 32768). A warp's 32 consecutive units
-        // are one 32-unit run of one chunk, i.e. of one K part, so a part's max |x| is a warp max plus one shared
-        // atomic per warp; after a barrier every thread stages its units from registers.
-        constexpr uint32_t NT = G1_CW * 32;
-        constexpr int HU = int((1024 + NT - 1) / NT);       // units per thread at the largest K (32768)
         const uint4 *xg = reinterpret_cast<const uint4 *>(a.X);
-        uint4 raw[HU][4];
+        if constexpr (MT == 1) {
+            // Thread t handles units t, t + NT, ... (K <= 32768). A warp's 32 consecutive units are one 32-unit run of
+            // one chunk, i.e. of one K part, so a part's max |x| is a warp max plus one shared atomic per warp; after
+            // a barrier every thread stages its units from registers.
+            constexpr int HU = int((1024 + NT - 1) / NT);   // units per thread at the largest K
+            uint4 raw[HU][4];
 #pragma unroll
-        for (int h = 0; h < HU; ++h) {
-            const uint32_t u = uint32_t(tid) + h * NT;
-            uint32_t m = 0;
-            if (u < U) {
+            for (int h = 0; h < HU; ++h) {
+                const uint32_t u = uint32_t(tid) + h * NT;
+                uint32_t mx = 0;
+                if (u < U) {
 #pragma unroll
-                for (int t = 0; t < 4; ++t) raw[h][t] = __ldg(xg + 4 * u + t);
+                    for (int t = 0; t < 4; ++t) raw[h][t] = __ldg(xg + 4 * u + t);
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t w[4] = {raw[h][t].x, raw[h][t].y, raw[h][t].z, raw[h][t].w};
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t w[4] = {raw[h][t].x, raw[h][t].y, raw[h][t].z, raw[h][t].w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) m = max(m, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+                        for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+                    }
+                }
+                if (uint32_t(tid - lane) + h * NT < U) {            // the warp's first unit exists
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    if (lane == 0) atomicMax(&pmax[((uint32_t(tid) + h * NT) % UPC) / 32], mx);
                 }
             }
-            if (uint32_t(tid - lane) + h * NT < U) {            // the warp's first unit exists
+            named_bar_sync(1, G1_CW * 32);
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-                if (lane == 0) atomicMax(&pmax[((uint32_t(tid) + h * NT) % UPC) / 32], m);
+            for (int h = 0; h < HU; ++h) {
+                const uint32_t u = uint32_t(tid) + h * NT;
+                if (u < U) stage_unit<F>(raw[h], part_exponent(pmax[(u % UPC) / 32]), xs, cst, U, u);
+            }
+        } else {
+            // MT x U units (activation row m, unit u): item i = m * Upad + u, Upad = U rounded up to 32, so a warp's 32
+            // consecutive items are one 32-unit run of one chunk of one row, i.e. of one (row, K part). Two passes:
+            // the max, then (after a barrier) a reload and the staging. Rows m >= Mg of a short group stage zeros.
+            const uint32_t Upad = (U + 31) / 32 * 32, items = uint32_t(MT) * Upad;
+            for (uint32_t it = uint32_t(tid); it < items; it += NT) {
+                const uint32_t m = it / Upad, u = it - m * Upad;
+                uint32_t mx = 0;
+                if (u < U && m < Mg) {
+                    const uint4 *xr = xg + (int64_t(m) * a.ldx) / 8 + 4 * u;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint4 v = __ldg(xr + t);
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                if (lane == 0) atomicMax(&pmax[m * P + (u % UPC) / 32], mx);
+            }
+            named_bar_sync(1, G1_CW * 32);
+            for (uint32_t it = uint32_t(tid); it < items; it += NT) {
+                const uint32_t m = it / Upad, u = it - m * Upad;
+                if (u < U) {
+                    uint4 raw[4] = {};
+                    if (m < Mg) {
+                        const uint4 *xr = xg + (int64_t(m) * a.ldx) / 8 + 4 * u;
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) raw[t] = __ldg(xr + t);
+                    }
+                    stage_unit<F>(raw, part_exponent(pmax[m * P + (u % UPC) / 32]), xs + m * 4 * U, cst + m * U * NX, U, u);
+                }
             }
         }
-        named_bar_sync(1, G1_CW * 32);
-#pragma unroll
-        for (int h = 0; h < HU; ++h) {
-            const uint32_t u = uint32_t(tid) + h * NT;
-            if (u < U) stage_unit<F>(raw[h], part_exponent(pmax[(u % UPC) / 32]), xs, cst, U, u);
-        }
-        if (tid < P) uscale[tid] = exp2i(-part_exponent(pmax[tid]));
+        if (tid < MT * P) uscale[tid] = exp2i(-part_exponent(pmax[tid]));
+        // every consumer meets here: masked lanes read the last unit's staged activations, whichever part staged it
         named_bar_sync(1, G1_CW * 32);
         if (tid == 0) mbar_arrive(xready);
     }
@@ -564,9 +732,9 @@ __global__ void __launch_bounds__(G1_THREADS, 1 + G1_CORES)
     const bool last_full = (U % UPC) == 0;                 // every lane has a unit in the last chunk too
     uint32_t ph = 0, s = 0, c = 0, t = 0;
     bool dead = false;
-    float acc[RW];
+    float acc[RW * MT];
 #pragma unroll
-    for (int i = 0; i < RW; ++i) acc[i] = 0.f;
+    for (int i = 0; i < RW * MT; ++i) acc[i] = 0.f;
     for (uint32_t k = 0; k < nit; ++k) {
         if (!dead && !mbar_wait_bounded(&full[s], ph)) {
             if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
@@ -579,21 +747,59 @@ __global__ void __launch_bounds__(G1_THREADS, 1 + G1_CORES)
             const float *sp = reinterpret_cast<const float *>(st + TR * CB + rc * SB) + uc;
             const uint32_t u = c * UPC + uc;
             const bool uv = u < U;
-            uint32_t xv[16];
-            load_xp(xs, U, uv ? u : U - 1, xv);
-            float cv[XC<F>::n];
+            const uint32_t uu = uv ? u : U - 1;
+            const bool full_tile = rows == uint32_t(TR) && (last_full || c + 1 < nch);
+            if constexpr (MT == 1) {
+                uint32_t xv[16];
+                load_xp(xs, U, uu, xv);
+                float cv[NX];
 #pragma unroll
-            for (int cc = 0; cc < XC<F>::n; ++cc) cv[cc] = cst[(uv ? u : U - 1) * XC<F>::n + cc];
-            if (rows == uint32_t(TR) && (last_full || c + 1 < nch)) {
+                for (int cc = 0; cc < NX; ++cc) cv[cc] = cst[uu * NX + cc];
+                if (full_tile) {
 #pragma unroll
-                for (int i = 0; i < RW; ++i)
-                    row_acc<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, cv, xv, true, acc[i]);
+                    for (int i = 0; i < RW; ++i)
+                        row_acc<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, cv, xv, true, acc[i]);
+                } else {
+                    // ragged tile or chunk: rows past the tile's end are skipped (uniform branches), lanes past K masked
+#pragma unroll
+                    for (int i = 0; i < RW; ++i)
+                        if (rc + uint32_t(RC * i) < rows)
+                            row_acc<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, cv, xv, uv, acc[i]);
+                }
+            } else if constexpr (MT == 2) {
+                // both activation rows stay in registers; each unit-row is unpacked once and used twice
+                uint32_t xv0[16], xv1[16];
+                load_xp(xs, U, uu, xv0);
+                load_xp(xs + 4 * U, U, uu, xv1);
+                float cv0[NX], cv1[NX];
+#pragma unroll
+                for (int cc = 0; cc < NX; ++cc) { cv0[cc] = cst[uu * NX + cc]; cv1[cc] = cst[(U + uu) * NX + cc]; }
+#pragma unroll
+                for (int i = 0; i < RW; ++i) {
+                    if (full_tile || rc + uint32_t(RC * i) < rows) {
+                        URow ur;
+                        unpack_row<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, full_tile || uv, ur);
+                        dot_row<F>(ur, xv0, cv0, acc[2 * i]);
+                        dot_row<F>(ur, xv1, cv1, acc[2 * i + 1]);
+                    }
+                }
             } else {
-                // ragged tile or chunk: rows past the tile's end are skipped (uniform branches), lanes past K masked
+                // each unit-row unpacked once, then multiplied against every activation row
+                URow ur[RW];
 #pragma unroll
                 for (int i = 0; i < RW; ++i)
-                    if (rc + uint32_t(RC * i) < rows)
-                        row_acc<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, cv, xv, uv, acc[i]);
+                    unpack_row<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo,
+                                  full_tile || (uv && rc + uint32_t(RC * i) < rows), ur[i]);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    uint32_t xv[16];
+                    load_xp(xs + m * 4 * U, U, uu, xv);
+                    float cv[NX];
+#pragma unroll
+                    for (int cc = 0; cc < NX; ++cc) cv[cc] = cst[(m * U + uu) * NX + cc];
+#pragma unroll
+                    for (int i = 0; i < RW; ++i) dot_row<F>(ur[i], xv, cv, acc[i * MT + m]);
+                }
             }
             // Release the stage; the warp that releases it last refills it with item k + NS (acq_rel: the other
             // warps' reads of the stage happen before the copy is issued).
@@ -606,26 +812,30 @@ __global__ void __launch_bounds__(G1_THREADS, 1 + G1_CORES)
         if (++s == NS) { s = 0; ph ^= 1u; }
         if (++c < nch) continue;
 
-        // tile done: one partial per (row, part); lanes i * (32 / RW) hold row rc + RC * i after the reduction
+        // tile done: one partial per (row, activation row, part); after the reduction lanes j * (32 / (RW MT)) hold
+        // value j = i * MT + m, i.e. row rc + RC * i and activation row m
         c = 0;
-        const float v = warp_rows_sum<RW>(acc, lane);
+        constexpr int R = RW * MT;
+        const float v = warp_rows_sum<R>(acc, lane);
 #pragma unroll
-        for (int i = 0; i < RW; ++i) acc[i] = 0.f;
-        const uint32_t lr = (t * TR) % G1_PART_ROWS;        // tile's first row within the round
-        if ((lane & (32 / RW - 1)) == 0) {
-            const uint32_t r = rc + uint32_t(RC) * uint32_t(lane / (32 / RW));
-            if (r < rows) part[(lr + r) * P + q] = v;
+        for (int i = 0; i < R; ++i) acc[i] = 0.f;
+        const uint32_t lr = (t * TR) % PR;                   // tile's first row within the round
+        if ((lane & (32 / R - 1)) == 0) {
+            const uint32_t j = uint32_t(lane) / (32 / R), i = j / MT, m = j % MT;
+            const uint32_t r = rc + uint32_t(RC) * i;
+            if (r < rows) part[((lr + r) * MT + m) * P + q] = v;
         }
         const uint32_t done = t * TR + rows;                // rows of this CTA finished after this tile
         ++t;
-        if (done == nrows || done % G1_PART_ROWS == 0) {
+        if (done == nrows || done % PR == 0) {
             named_bar_sync(1, G1_CW * 32);
-            const uint32_t base = (done - 1) / G1_PART_ROWS * G1_PART_ROWS, cnt = done - base;
-            for (uint32_t r = uint32_t(tid); r < cnt; r += G1_CW * 32) {
+            const uint32_t base = (done - 1) / PR * PR, cnt = done - base;
+            for (uint32_t e = uint32_t(tid); e < cnt * MT; e += G1_CW * 32) {
+                const uint32_t r = e / MT, m = e - r * MT;
                 float yv = 0.f;
 #pragma unroll
-                for (int pp = 0; pp < P; ++pp) yv = fmaf(part[r * P + pp], uscale[pp], yv);
-                a.Y[rbeg + base + r] = yv;
+                for (int pp = 0; pp < P; ++pp) yv = fmaf(part[(r * MT + m) * P + pp], uscale[m * P + pp], yv);
+                if (m < Mg) a.Y[int64_t(m) * a.ldy + rbeg + base + r] = yv;
             }
             if (done != nrows) named_bar_sync(1, G1_CW * 32);   // partials of the next round overwrite these
         }
@@ -639,14 +849,14 @@ __global__ void __launch_bounds__(G1_THREADS, 1 + G1_CORES)
 }
 
 // Shared-memory plan of one launch: returns false when two stages plus the staged activations do not fit `budget`.
-template <int F>
+template <int F, int MT>
 static bool plan_gemv1(const GemvArgs &a, uint32_t budget, G1Plan *pl) {
-    using T = T1<F>;
+    using T = T1<F, MT>;
     const uint32_t U = uint32_t(a.K / 32);
     pl->off_part = G1_HDR;
-    pl->off_xs = pl->off_part + G1_PART_ROWS * T::P * 4;
-    pl->off_cst = pl->off_xs + uint32_t(round_up(int64_t(U) * 64, 128));
-    pl->off_stages = uint32_t(round_up(pl->off_cst + int64_t(U) * XC<F>::n * 4, 1024));
+    pl->off_xs = pl->off_part + uint32_t(T::PR * MT * T::P * 4);
+    pl->off_cst = pl->off_xs + uint32_t(round_up(int64_t(MT) * U * 64, 128));
+    pl->off_stages = uint32_t(round_up(pl->off_cst + int64_t(MT) * U * XC<F>::n * 4, 1024));
     // + 32: the Q3S / Q6S unpack reads up to 4 bytes past a row chunk
     const int64_t room = int64_t(budget) - pl->off_stages - 32;
     if (room < int64_t(T::STAGE) * 2) return false;
@@ -686,15 +896,10 @@ static cudaError_t encode_rows(CUtensorMap *m, const void *base, int64_t rows, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int F>
-static cudaError_t launch_gemv1(const GemvArgs &a, cudaStream_t st) {
-    using T = T1<F>;
-    // Two CTAs per SM (the next product's CTA streams its first weights while this one finishes) when the kernel
-    // fits twice on an SM and the ring keeps at least 3 stages within half of the shared memory; else one.
-    G1Plan pl;
-    if (!(G1_CORES && plan_gemv1<F>(a, 110u * 1024u, &pl) && pl.ns >= 3)) {
-        if (!plan_gemv1<F>(a, 227u * 1024u, &pl)) return cudaErrorInvalidValue;
-    }
+// One launch for activation rows [0, a.M) of `a` (a.M <= MT). The plan must already be known to fit.
+template <int F, int MT>
+static cudaError_t launch_gemv_mt(const GemvArgs &a, const G1Plan &pl, cudaStream_t st) {
+    using T = T1<F, MT>;
     CUtensorMap tmc, tms;
     cudaError_t e = encode_rows(&tmc, a.packed, a.N, a.row_stride, uint32_t(T::CB / 8), uint32_t(T::TR));
     if (e != cudaSuccess) return e;
@@ -709,7 +914,7 @@ static cudaError_t launch_gemv1(const GemvArgs &a, cudaStream_t st) {
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!opted[dev]) {
-        e = cudaFuncSetAttribute(gemv1_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        e = cudaFuncSetAttribute(gemv1_kernel<F, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         opted[dev] = 1;
     }
@@ -725,290 +930,40 @@ static cudaError_t launch_gemv1(const GemvArgs &a, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = a.weight_prefetch ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv1_kernel<F>, tmc, tms, a, pl);
+    return cudaLaunchKernelEx(&cfg, gemv1_kernel<F, MT>, tmc, tms, a, pl);
 }
 
-namespace {
-// ------------------------------------------------------------------------------------------------------------
-// Exact unit decode for the small-batch path: 32 dequantized fp32 weights (same roundings as FORMATS.md).
-// ------------------------------------------------------------------------------------------------------------
-template <int F>
-__device__ __forceinline__ void decode_unit(const uint8_t *row, const float *scl, int uc, float w[32]) {
-    if constexpr (F == FMT_Q4G32) {
-        const uint4 c = *reinterpret_cast<const uint4 *>(row + 16 * uc);
-        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-        const float s = scl[uc];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = __fmul_rn(s, float(int((cw[i >> 3] >> (4 * (i & 7))) & 15u) - 8));
-    } else if constexpr (F == FMT_Q2S) {
-        const int sbk = uc >> 3, su = uc & 7;
-        const uint8_t *blk = row + sbk * 84;
-        const uint32_t cw[2] = {lds32(blk + 8 * su), lds32(blk + 8 * su + 4)};
-        const float D = hbits(blk + 80), Dm = hbits(blk + 82);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t lm = blk[64 + 2 * su + h];
-            const float es = __fmul_rn(D, float(lm & 15u)), em = __fmul_rn(Dm, float(lm >> 4));
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                w[16 * h + i] = __fsub_rn(__fmul_rn(es, float((cw[h] >> (2 * i)) & 3u)), em);
-        }
-    } else if constexpr (F == FMT_Q3S) {
-        const int sbk = uc >> 3, su = uc & 7;
-        const uint8_t *blk = row + sbk * 110;
-        uint32_t s[3];
-        lds_words_a2<3>(blk + 12 * su, s);
-        const uint32_t v[4] = {s[0], __funnelshift_r(s[0], s[1], 24), __funnelshift_r(s[1], s[2], 16), s[2] >> 8};
-        const float D = hbits(blk + 108);
-        const uint8_t *fb = blk + 96 + 3 * (su >> 1);
-        const uint32_t f = uint32_t(fb[0]) | (uint32_t(fb[1]) << 8) | (uint32_t(fb[2]) << 16);
-        const int j0 = (2 * su) & 3;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float es = __fmul_rn(D, float((f >> (6 * (j0 + h))) & 63u));
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int g = 2 * h + (i >> 3), t = i & 7;
-                w[16 * h + i] = __fmul_rn(es, float(int((v[g] >> (3 * t)) & 7u) - 4));
-            }
-        }
-    } else if constexpr (F == FMT_Q5S) {
-        const int sbk = uc >> 3, su = uc & 7;
-        const uint8_t *blk = row + sbk * 176;
-        const uint4 c = *reinterpret_cast<const uint4 *>(blk + 16 * su);
-        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-        const uint32_t H = lds32(blk + 128 + 4 * su);
-        const float D = hbits(blk + 172), Dm = hbits(blk + 174);
-        const uint8_t *fl = blk + 160 + 3 * (su >> 2), *fm = blk + 166 + 3 * (su >> 2);
-        const uint32_t vl = uint32_t(fl[0]) | (uint32_t(fl[1]) << 8) | (uint32_t(fl[2]) << 16);
-        const uint32_t vm = uint32_t(fm[0]) | (uint32_t(fm[1]) << 8) | (uint32_t(fm[2]) << 16);
-        const float es = __fmul_rn(D, float((vl >> (6 * (su & 3))) & 63u));
-        const float em = __fmul_rn(Dm, float((vm >> (6 * (su & 3))) & 63u));
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t u = ((cw[i >> 3] >> (4 * (i & 7))) & 15u) | (((H >> i) & 1u) << 4);
-            w[i] = __fsub_rn(__fmul_rn(es, float(u)), em);
-        }
-    } else {
-        const int sbk = uc >> 3, su = uc & 7;
-        const uint8_t *blk = row + sbk * 210;
-        uint32_t c[4], h[2];
-        lds_words_a2<4>(blk + 16 * su, c);
-        lds_words_a2<2>(blk + 128 + 8 * su, h);
-        const float D = hbits(blk + 208);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const float es = __fmul_rn(D, float(int8_t(blk[192 + 2 * su + hh])));
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int ii = 16 * hh + i;
-                const uint32_t u = ((c[ii >> 3] >> (4 * (ii & 7))) & 15u) | (((h[hh] >> (2 * i)) & 3u) << 4);
-                w[ii] = __fmul_rn(es, float(int(u) - 32));
-            }
-        }
-    }
-}
-
-
-}  // namespace
-
-// ------------------------------------------------------------------------------------------------------------
-// Small-batch kernel (M = 2..16): 8 consumer warps, warp pair p owns row p of the 4-row tile; each lane
-// dequantizes two 32-weight units exactly and multiplies them against the M activation rows (read through L1).
-// ------------------------------------------------------------------------------------------------------------
-constexpr int NCW = 8;
-constexpr int NTHREADS = (NCW + 1) * 32;
-constexpr int SMEM_BUDGET = 220 * 1024;
-
+// Activation rows in groups of MT (their staged activations share one SM's shared memory with the weight ring):
+// every group is one launch over the whole packed matrix.
 template <int F, int MT>
-__global__ void __launch_bounds__(NTHREADS, 1) stream_kernel(GemvArgs a, int NS) {
-    using G = Geo<F>;
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t N = a.N, K = a.K;
-    const int64_t ntiles = (N + TILE_R - 1) / TILE_R;
-    const int nchunks = int((K + CHW - 1) / CHW);
-
-    uint8_t *p = smem_raw;
-    uint64_t *full = reinterpret_cast<uint64_t *>(p);
-    uint64_t *empty = full + NS;
-    p += round_up(16 * NS, 128);
-    float *red = reinterpret_cast<float *>(p);
-    p += round_up(2 * NCW * MT * 4, 128);
-    uint8_t *stages = p;
-
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], NCW); }
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    if (warp == NCW) {
-        const uint64_t pol = l2_evict_first_policy();
-        int it = 0;
-        bool bad = false;
-        for (int64_t tile = blockIdx.x; tile < ntiles && !bad; tile += gridDim.x) {
-            const int64_t r0 = tile * TILE_R;
-            const int rows = int(N - r0 < TILE_R ? N - r0 : TILE_R);
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = it % NS;
-                const uint32_t ph = uint32_t(it / NS) & 1u;
-                if (it >= NS) {
-                    bool ok = true;
-                    if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1u);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) { if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_EMPTY); bad = true; break; }
-                }
-                int64_t cbytes, sbytes = 0;
-                const int64_t koff = int64_t(c) * CHW;
-                if constexpr (Fmt<F>::sb) {
-                    const int64_t off = (koff / 256) * Fmt<F>::bytes;
-                    cbytes = a.row_stride - off < G::chunk_bytes ? a.row_stride - off : G::chunk_bytes;
-                } else {
-                    cbytes = (K - koff) / 2 < G::chunk_bytes ? (K - koff) / 2 : G::chunk_bytes;
-                    const int64_t sb = (a.scale_stride - koff / 32) * 4;
-                    sbytes = sb < G::scale_bytes ? sb : G::scale_bytes;
-                }
-                uint8_t *st = stages + int64_t(s) * G::stage_bytes;
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(rows * (cbytes + sbytes)));
-                __syncwarp();
-                if (lane < rows) {
-                    const int64_t r = r0 + lane;
-                    const uint8_t *src;
-                    if constexpr (Fmt<F>::sb) src = a.packed + r * a.row_stride + (koff / 256) * Fmt<F>::bytes;
-                    else src = a.packed + r * a.row_stride + koff / 2;
-                    bulk_g2s(st + lane * G::chunk_bytes, src, uint32_t(cbytes), &full[s], pol);
-                } else if (!Fmt<F>::sb && lane >= 8 && lane < 8 + rows) {
-                    const int64_t r = r0 + (lane - 8);
-                    const uint8_t *src = reinterpret_cast<const uint8_t *>(a.gscale + r * a.scale_stride + koff / 32);
-                    bulk_g2s(st + TILE_R * G::chunk_bytes + (lane - 8) * G::scale_bytes, src, uint32_t(sbytes),
-                             &full[s], pol);
-                }
-                ++it;
-            }
-        }
-        // Drain: wait (bounded) for the last fill of each stage, so the CTA never exits with bulk copies in flight.
-        if (lane == 0) {
-            for (int j = (it > NS ? it - NS : 0); j < it; ++j) {
-                if (!mbar_wait_bounded(&full[j % NS], uint32_t(j / NS) & 1u)) {
-                    atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
-                    break;
-                }
-            }
-        }
-        return;
-    }
-
-    const int pair = warp >> 1, half = warp & 1;    // warp pair `pair` owns row `pair` of the tile
-    int it = 0, tcount = 0;
-    bool dead = false;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tcount) {
-        const int64_t r0 = tile * TILE_R;
-        const bool row_ok = (r0 + pair) < N;
-        float acc[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = it % NS;
-            const uint32_t ph = uint32_t(it / NS) & 1u;
-            if (!dead) {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait_bounded(&full[s], ph);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) { if (lane == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL); dead = true; }
-            }
-            const int64_t koff = int64_t(c) * CHW;
-            const int units = int((K - koff) / 32 < UPC ? (K - koff) / 32 : UPC);
-            const uint8_t *st = stages + int64_t(s) * G::stage_bytes;
-            const uint8_t *row = st + pair * G::chunk_bytes;
-            const float *scl = reinterpret_cast<const float *>(st + TILE_R * G::chunk_bytes + pair * G::scale_bytes);
-            if (row_ok && !dead) {
-#pragma unroll
-                for (int v = 0; v < 2; ++v) {
-                    const int uc = 64 * half + 32 * v + lane;
-                    if (uc < units) {
-                        float w[32];
-                        decode_unit<F>(row, scl, uc, w);
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            if (m < a.M) {
-                                const uint4 *xp = reinterpret_cast<const uint4 *>(a.X + m * a.ldx + koff + 32 * uc);
-                                float t = 0.f;
-#pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    const uint4 xq = __ldg(xp + q);
-                                    const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w};
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        t = fmaf(w[8 * q + 2 * e], h2f_bits(lo16(xw[e])), t);
-                                        t = fmaf(w[8 * q + 2 * e + 1], h2f_bits(hi16(xw[e])), t);
-                                    }
-                                }
-                                acc[m] += t;
-                            }
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            ++it;
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            float v = acc[m];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            acc[m] = v;
-        }
-        float *rb = red + (tcount & 1) * NCW * MT;
-        if (lane == 0) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m) rb[warp * MT + m] = acc[m];
-        }
-        named_bar_sync(2 + pair, 64);
-        if (half == 0 && row_ok && lane < MT && lane < a.M) {
-            const float v = rb[(2 * pair) * MT + lane] + rb[(2 * pair + 1) * MT + lane];
-            a.Y[int64_t(lane) * a.ldy + r0 + pair] = v;
-        }
-    }
-}
-
-template <int F, int MT>
-static cudaError_t launch_stream(const GemvArgs &a, cudaStream_t s) {
-    using G = Geo<F>;
-    const int64_t extra = round_up(2 * NCW * MT * 4, 128);
-    int NS = 0;
-    int64_t tot = 0;
-    for (int ns = 16; ns >= 2; --ns) {
-        tot = round_up(16 * ns, 128) + extra + int64_t(ns) * G::stage_bytes + 32;
-        if (tot <= SMEM_BUDGET) { NS = ns; break; }
-    }
-    if (NS == 0) return cudaErrorInvalidValue;
-    static int opted[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!opted[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(stream_kernel<F, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BUDGET);
+static cudaError_t launch_groups(const GemvArgs &a, const G1Plan &pl, cudaStream_t st) {
+    for (int m0 = 0; m0 < a.M; m0 += MT) {
+        GemvArgs g = a;
+        g.X = a.X + int64_t(m0) * a.ldx;
+        g.Y = a.Y + int64_t(m0) * a.ldy;
+        g.M = a.M - m0 < MT ? a.M - m0 : MT;
+        const cudaError_t e = launch_gemv_mt<F, MT>(g, pl, st);
         if (e != cudaSuccess) return e;
-        opted[dev] = 1;
     }
-    const int64_t ntiles = (a.N + TILE_R - 1) / TILE_R;
-    int grid = num_sms();
-    if (ntiles < grid) grid = int(ntiles);
-    if (grid < 1) return cudaSuccess;
-    stream_kernel<F, MT><<<grid, NTHREADS, size_t(tot), s>>>(a, NS);
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 template <int F>
 static cudaError_t launch_fmt(const GemvArgs &a, cudaStream_t s) {
-    if (a.M <= 1) return launch_gemv1<F>(a, s);
-    if (a.M <= 2) return launch_stream<F, 2>(a, s);
-    if (a.M <= 4) return launch_stream<F, 4>(a, s);
-    if (a.M <= 8) return launch_stream<F, 8>(a, s);
-    return launch_stream<F, 16>(a, s);
+    G1Plan pl;
+    constexpr uint32_t BUDGET = 227u * 1024u;
+    if (a.M <= 1) {
+        if (!plan_gemv1<F, 1>(a, BUDGET, &pl)) return cudaErrorInvalidValue;
+        return launch_gemv_mt<F, 1>(a, pl, s);
+    }
+    // the widest group that still leaves a ring of at least three stages
+    if (a.M > 8 && plan_gemv1<F, 16>(a, BUDGET, &pl) && pl.ns >= 3) return launch_groups<F, 16>(a, pl, s);
+    if (a.M > 4 && plan_gemv1<F, 8>(a, BUDGET, &pl) && pl.ns >= 3) return launch_groups<F, 8>(a, pl, s);
+    if (a.M > 2 && plan_gemv1<F, 4>(a, BUDGET, &pl) && pl.ns >= 3) return launch_groups<F, 4>(a, pl, s);
+    if (plan_gemv1<F, 2>(a, BUDGET, &pl)) return launch_groups<F, 2>(a, pl, s);
+    // long rows of the widest formats: one row of activations per launch
+    if (!plan_gemv1<F, 1>(a, BUDGET, &pl)) return cudaErrorInvalidValue;
+    return launch_groups<F, 1>(a, pl, s);
 }
 
 cudaError_t launch_gemv(int fmt, const GemvArgs &a, cudaStream_t s) {

@@ -151,6 +151,29 @@ def test_small_batch(qpg, orc, name, M):
     gemv_bound_check(Y.cpu().numpy(), Y_ref, deq, X.numpy().astype(np.float64))
 
 
+# (N, K, M): activation rows split into several launches (the staged rows of a group share one SM's shared memory
+# with the weight ring) with a short last group, at the 70B MLP widths.
+SMALL_BATCH_SHAPES = [(613, 8192, 16), (613, 8192, 5), (211, 28672, 16), (211, 28672, 3)]
+
+
+@pytest.mark.parametrize("name", ["Q4G32", "Q3S", "Q5S"])
+@pytest.mark.parametrize("shape", SMALL_BATCH_SHAPES, ids=[f"{n}x{k}xM{m}" for n, k, m in SMALL_BATCH_SHAPES])
+def test_small_batch_groups(qpg, orc, name, shape):
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    N, K, M = shape
+    rp, rgs = case(orc, fmt, N, K, 720 + M + N % 7)
+    X = synth.normal((M, K), 1.0, 820 + M, dtype=torch.float16)
+    pd = torch.from_numpy(rp).cuda()
+    gd = None if rgs is None else torch.from_numpy(rgs).cuda()
+    Y = qpg.qgemm_small(fmt, pd, gd, N, K, X.cuda())
+    torch.cuda.synchronize()
+    Y_ref = orc.gemm(fmt, N, K, rp, rgs, X.numpy().view(np.uint16), nthreads=8)
+    deq = orc.dequant(fmt, N, K, rp, rgs)
+    gemv_bound_check(Y.cpu().numpy(), Y_ref, deq, X.numpy().astype(np.float64))
+    assert qpg.qpack_fetch_fault_flags() == 0
+
+
 def test_small_batch_strided(qpg, orc):
     from bit_weight_quantized_qpack_gb300 import synth
     fmt = qpg.Q5S
