@@ -5,17 +5,23 @@
 // lpnh.cn/news/2857666, §1.2), so it belongs on the tensor cores; the packed weights are still read in their
 // compact form and dequantized on chip (DBHOO-CIM article, pwwt.cn/news/4452170, §3.3: no fp32 weight array).
 //
-// One CTA computes a 128 x 256 tile of Y:
-//   warps 0..3  producers: per 64-wide K step, stage the 128 x 64 bf16 X tile and dequantize the 256 x 64 weight
-//               tile (exact fp32 dequant of FORMATS.md, then bf16 round-to-nearest-even) into shared memory in
-//               the 128-byte-swizzled K-major layout the MMA reads; afterwards they are the epilogue warps
-//               (tcgen05.ld of their 32 TMEM lanes, bf16 conversion, global stores).
-//   warp 4      allocates 256 TMEM columns (the fp32 128 x 256 accumulator); lane 0 issues the tcgen05.mma
-//               instructions (M=128, N=256, K=16 each, both operands from shared-memory descriptors) and commits
-//               them to mbarriers that free the stage and, at the end, publish the accumulator.
+// One CTA computes a 512 x 128 block of Y (four 128-token sub-tiles x 128 weight rows):
+//   warp 9      TMA producer: per 64-wide K step, four 2-D tensor copies bring the 4 x (128 x 64) bf16 X tiles into
+//               shared memory already in the 128-byte-swizzled K-major layout the MMA reads.
+//   warps 0..7  weight producers: per K step, each thread dequantizes one 32-weight unit of one of the 128 weight
+//               rows (exact fp32 dequant of FORMATS.md from aligned global loads, then bf16 round-to-nearest-even)
+//               into the swizzled 128 x 64 weight tile; afterwards they are the epilogue warps (tcgen05.ld of their
+//               TMEM lane quarter, bf16 conversion, global stores).
+//   warp 8      allocates all 512 TMEM columns (four fp32 128 x 128 accumulators); lane 0 issues the tcgen05.mma
+//               instructions (M=128, N=128, K=16; both operands from shared-memory descriptors) and commits them to
+//               mbarriers that free the stage and, at the end, publish the accumulators.
+// Each weight tile is dequantized once for 512 tokens (the dequantization is the CUDA-core cost of this path).
 // Every wait is bounded; on a timeout the kernel records a fault bit, skips the remaining work, still frees its
 // TMEM and returns.
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "qpack_dev.cuh"
 #include "qpack_launch.h"
@@ -26,14 +32,16 @@ __device__ int g_fault_prefill = 0;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 3;
-constexpr int A_BYTES = BM * BK * 2;               // 16 KB
-constexpr int B_BYTES = BN * BK * 2;               // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 48 KB (multiple of 1024)
-constexpr int NPROD = 128;                         // producer / epilogue threads
-constexpr int THREADS = NPROD + 32;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr int BMS = 128, NSUB = 4, BM = BMS * NSUB;   // tokens per sub-tile, sub-tiles, tokens per CTA
+constexpr int BN = 128, BK = 64;                   // weight rows per CTA, K per stage
+constexpr int STAGES = 2;
+constexpr int A_BYTES = BMS * BK * 2;              // 16 KB per X sub-tile
+constexpr int B_BYTES = BN * BK * 2;               // 16 KB weight tile
+constexpr int STAGE_BYTES = NSUB * A_BYTES + B_BYTES;   // 80 KB (multiple of 1024)
+constexpr int NDQW = 8;                            // dequant / epilogue warps
+constexpr int NPROD = NDQW * 32;
+constexpr int THREADS = NPROD + 64;                // + MMA warp + TMA warp
+constexpr uint32_t TMEM_COLS = 512;
 constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
 
 // ------------------------------------------------------------------------------------------------------------
@@ -97,7 +105,7 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
 }
 // Instruction descriptor, kind::f16: D fp32 (bit 4), A bf16 (bits 7-9 = 1), B bf16 (bits 10-12 = 1), both
 // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BMS >> 4) << 24);
 
 // Byte offset of the 16-byte chunk c (K elements 8c..8c+7) of row r inside a 128B-swizzled K-major tile.
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) {
@@ -110,90 +118,112 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return lo | (hi << 16);
 }
 
-__device__ __forceinline__ uint32_t ldg_u8(const uint8_t *p) { return __ldg(p); }
-__device__ __forceinline__ uint32_t ldg_u16(const uint8_t *p) { return uint32_t(__ldg(p)) | (uint32_t(__ldg(p + 1)) << 8); }
-__device__ __forceinline__ uint32_t ldg_u24(const uint8_t *p) { return ldg_u16(p) | (uint32_t(__ldg(p + 2)) << 16); }
+__device__ __forceinline__ uint32_t ldg32(const uint8_t *p) { return __ldg(reinterpret_cast<const uint32_t *>(p)); }
+__device__ __forceinline__ uint32_t ldg16(const uint8_t *p) { return __ldg(reinterpret_cast<const uint16_t *>(p)); }
+// n consecutive 32-bit words starting at a 2-byte aligned global address (aligned loads plus funnel shifts).
+template <int n>
+__device__ __forceinline__ void ldg_words_a2(const uint8_t *p, uint32_t *w) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t *base = reinterpret_cast<const uint32_t *>(a & ~uintptr_t(3));
+    const uint32_t sh = uint32_t(a & 3u) * 8u;   // 0 or 16
+    uint32_t r[n + 1];
+#pragma unroll
+    for (int i = 0; i <= n; ++i) r[i] = __ldg(base + i);
+#pragma unroll
+    for (int i = 0; i < n; ++i) w[i] = __funnelshift_r(r[i], r[i + 1], sh);
+}
+__device__ __forceinline__ float i2f_small(int v) { return float(v); }
 
-// Dequantize 64 consecutive weights (k0 .. k0+63, k0 a multiple of 64) of one packed row to fp32, exactly as
-// FORMATS.md (the same roundings as the dequant kernel and the CPU reference).
+// Dequantize 32-weight unit u of one packed row to fp32, exactly as FORMATS.md (the roundings of the dequant kernel
+// and the CPU reference: the sub-block scale d * L first, then its product with the code, minus dmin * M).
 template <int F>
-__device__ __forceinline__ void dequant64(const uint8_t *row, const float *gs_row, uint32_t k0, float w[64]) {
+__device__ __forceinline__ void dequant_unit(const uint8_t *row, const float *gs_row, uint32_t u, float w[32]) {
     if constexpr (F == FMT_Q4G32) {
-        const uint4 *cp = reinterpret_cast<const uint4 *>(row + k0 / 2);
-        const float s0 = __ldg(gs_row + k0 / 32), s1 = __ldg(gs_row + k0 / 32 + 1);
+        const uint4 c = __ldg(reinterpret_cast<const uint4 *>(row + 16 * u));
+        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+        const float sc = __ldg(gs_row + u);
 #pragma unroll
-        for (int v = 0; v < 2; ++v) {
-            const uint4 c = __ldg(cp + v);
-            const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-            const float s = v ? s1 : s0;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) w[32 * v + i] = __fmul_rn(s, float(int((cw[i >> 3] >> (4 * (i & 7))) & 15u) - 8));
-        }
+        for (int i = 0; i < 32; ++i) w[i] = __fmul_rn(sc, i2f_small(int((cw[i >> 3] >> (4 * (i & 7))) & 15u) - 8));
     } else {
-        const uint32_t b = k0 / 256, j = (k0 % 256) / 64;      // super-block, quarter within it
+        const uint32_t b = u >> 3, su = u & 7u;
         const uint8_t *blk = row + b * Fmt<F>::bytes;
         if constexpr (F == FMT_Q2S) {
-            const float D = h2f_bits(uint16_t(ldg_u16(blk + 80))), Dm = h2f_bits(uint16_t(ldg_u16(blk + 82)));
-#pragma unroll
-            for (int sbi = 0; sbi < 4; ++sbi) {
-                const uint32_t lm = ldg_u8(blk + 64 + 4 * j + sbi);
-                const float es = __fmul_rn(D, float(lm & 15u)), em = __fmul_rn(Dm, float(lm >> 4));
-                const uint32_t cw = ldg_u8(blk + 16 * j + 4 * sbi) | (ldg_u8(blk + 16 * j + 4 * sbi + 1) << 8) |
-                                    (ldg_u8(blk + 16 * j + 4 * sbi + 2) << 16) | (ldg_u8(blk + 16 * j + 4 * sbi + 3) << 24);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) w[16 * sbi + i] = __fsub_rn(__fmul_rn(es, float((cw >> (2 * i)) & 3u)), em);
-            }
-        } else if constexpr (F == FMT_Q3S) {
-            const float D = h2f_bits(uint16_t(ldg_u16(blk + 108)));
-            const uint32_t f = ldg_u24(blk + 96 + 3 * j);          // L_{4j .. 4j+3}
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const uint32_t v = ldg_u24(blk + 24 * j + 3 * g);
-                const float es = __fmul_rn(D, float((f >> (6 * (g >> 1))) & 63u));
-#pragma unroll
-                for (int t = 0; t < 8; ++t) w[8 * g + t] = __fmul_rn(es, float(int((v >> (3 * t)) & 7u) - 4));
-            }
-        } else if constexpr (F == FMT_Q5S) {
-            const float D = h2f_bits(uint16_t(ldg_u16(blk + 172))), Dm = h2f_bits(uint16_t(ldg_u16(blk + 174)));
+            const uint32_t cw[2] = {ldg32(blk + 8 * su), ldg32(blk + 8 * su + 4)};
+            const uint32_t lm = ldg16(blk + 64 + 2 * su);
+            const uint32_t dd = ldg32(blk + 80);
+            const float D = h2f_bits(uint16_t(dd & 0xFFFFu)), Dm = h2f_bits(uint16_t(dd >> 16));
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const uint32_t sub = 2 * j + h;                    // sub-block of 32
-                const uint32_t fl = ldg_u24(blk + 160 + 3 * (sub >> 2)), fm = ldg_u24(blk + 166 + 3 * (sub >> 2));
-                const float es = __fmul_rn(D, float((fl >> (6 * (sub & 3))) & 63u));
-                const float em = __fmul_rn(Dm, float((fm >> (6 * (sub & 3))) & 63u));
-                const uint32_t H = ldg_u8(blk + 128 + 4 * sub) | (ldg_u8(blk + 129 + 4 * sub) << 8) |
-                                   (ldg_u8(blk + 130 + 4 * sub) << 16) | (ldg_u8(blk + 131 + 4 * sub) << 24);
+                const uint32_t l = (lm >> (8 * h)) & 0xFFu;
+                const float es = __fmul_rn(D, float(l & 15u)), em = __fmul_rn(Dm, float(l >> 4));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const uint32_t lo = (ldg_u8(blk + 16 * sub + (i >> 1)) >> (4 * (i & 1))) & 15u;
-                    const uint32_t u = lo | (((H >> i) & 1u) << 4);
-                    w[32 * h + i] = __fsub_rn(__fmul_rn(es, float(u)), em);
-                }
+                for (int i = 0; i < 16; ++i) w[16 * h + i] = __fsub_rn(__fmul_rn(es, float((cw[h] >> (2 * i)) & 3u)), em);
             }
-        } else {
-            const float D = h2f_bits(uint16_t(ldg_u16(blk + 208)));
+        } else if constexpr (F == FMT_Q3S) {
+            uint32_t c3[3];
+            ldg_words_a2<3>(blk + 12 * su, c3);
+            const uint32_t v[4] = {c3[0], __funnelshift_r(c3[0], c3[1], 24), __funnelshift_r(c3[1], c3[2], 16), c3[2] >> 8};
+            // the 12 bits of L_{2su}, L_{2su+1}: bits 12 (su & 1) .. +11 of the 24-bit field group su >> 1, read as two
+            // bytes that stay inside the super-block
+            const uint32_t fb = 96u + 3u * (su >> 1) + (su & 1u);
+            const uint32_t two = uint32_t(__ldg(blk + fb)) | (uint32_t(__ldg(blk + fb + 1)) << 8);
+            const uint32_t fsh = 4u * (su & 1u);
+            const float D = h2f_bits(uint16_t(ldg16(blk + 108)));
 #pragma unroll
-            for (int sbi = 0; sbi < 4; ++sbi) {
-                const uint32_t sub = 4 * j + sbi;                  // sub-block of 16
-                const float es = __fmul_rn(D, float(int8_t(ldg_u8(blk + 192 + sub))));
-                const uint32_t hw = ldg_u8(blk + 128 + 4 * sub) | (ldg_u8(blk + 129 + 4 * sub) << 8) |
-                                    (ldg_u8(blk + 130 + 4 * sub) << 16) | (ldg_u8(blk + 131 + 4 * sub) << 24);
+            for (int h = 0; h < 2; ++h) {
+                const float es = __fmul_rn(D, float((two >> (fsh + 6 * h)) & 63u));
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const uint32_t ii = 16 * sub + i;
-                    const uint32_t lo = (ldg_u8(blk + (ii >> 1)) >> (4 * (ii & 1))) & 15u;
-                    const uint32_t u = lo | (((hw >> (2 * i)) & 3u) << 4);
-                    w[16 * sbi + i] = __fmul_rn(es, float(int(u) - 32));
+                    const int g = 2 * h + (i >> 3), t = i & 7;
+                    w[16 * h + i] = __fmul_rn(es, float(int((v[g] >> (3 * t)) & 7u) - 4));
+                }
+            }
+        } else if constexpr (F == FMT_Q5S) {
+            const uint4 c = __ldg(reinterpret_cast<const uint4 *>(blk + 16 * su));
+            const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+            const uint32_t H = ldg32(blk + 128 + 4 * su);
+            const uint4 fl = __ldg(reinterpret_cast<const uint4 *>(blk + 160));
+            const uint64_t lo64 = (uint64_t(fl.y) << 32) | fl.x, hi64 = (uint64_t(fl.z) << 32) | fl.y;
+            const float D = h2f_bits(uint16_t(fl.w & 0xFFFFu)), Dm = h2f_bits(uint16_t(fl.w >> 16));
+            const float es = __fmul_rn(D, float(uint32_t(lo64 >> (6 * su)) & 63u));
+            const float em = __fmul_rn(Dm, float(uint32_t(hi64 >> (16 + 6 * su)) & 63u));
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint32_t q = ((cw[i >> 3] >> (4 * (i & 7))) & 15u) | (((H >> i) & 1u) << 4);
+                w[i] = __fsub_rn(__fmul_rn(es, float(q)), em);
+            }
+        } else {
+            uint32_t c4[4], h2[2];
+            ldg_words_a2<4>(blk + 16 * su, c4);
+            ldg_words_a2<2>(blk + 128 + 8 * su, h2);
+            const uint32_t ls = ldg16(blk + 192 + 2 * su);
+            const float D = h2f_bits(uint16_t(ldg16(blk + 208)));
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float es = __fmul_rn(D, float(int(int8_t(uint8_t(ls >> (8 * hh))))));
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int ii = 16 * hh + i;
+                    const uint32_t q = ((c4[ii >> 3] >> (4 * (ii & 7))) & 15u) | (((h2[hh] >> (2 * i)) & 3u) << 4);
+                    w[ii] = __fmul_rn(es, float(int(q) - 32));
                 }
             }
         }
     }
 }
 
+// 2-D tensor copy global -> shared (box at coordinates {x, y}), completion on `bar` as bytes.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 }  // namespace
 
 template <int F>
-__global__ void __launch_bounds__(THREADS, 1) prefill_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tm_x, PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;           // 1024-aligned operand area
@@ -206,13 +236,14 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(PrefillArgs a) {
     const int64_t M = a.M, N = a.N, K = a.K;
     const int64_t n0 = int64_t(blockIdx.x) * BN, m0 = int64_t(blockIdx.y) * BM;
     const int nk = int(K / BK);
+    const int nsub = int((M - m0 + BMS - 1) / BMS < NSUB ? (M - m0 + BMS - 1) / BMS : NSUB);   // sub-tiles with tokens
 
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], NPROD); mbar_init(&empty[s], 1); }
+        for (int st = 0; st < STAGES; ++st) { mbar_init(&full[st], NDQW + 1); mbar_init(&empty[st], 1); }
         mbar_init(accum, 1);
         fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == NDQW) {
         tmem_alloc(tmem_slot, TMEM_COLS);
         tmem_relinquish();
     }
@@ -222,57 +253,37 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(PrefillArgs a) {
     const uint32_t tmem_d = *tmem_slot;
     bool dead = false;
 
-    if (warp < 4) {
-        // ---------------------------------- producers ----------------------------------
-        const int t = tid;                                                  // 0..127
+    if (warp < NDQW) {
+        // ------------------------------ weight producers ------------------------------
+        const int r = tid & (BN - 1), h = tid / BN;                         // weight row, K half of the stage
+        const int64_t n = n0 + r;
+        const uint8_t *row = a.packed + n * a.row_stride;
+        const float *gs_row = a.gscale ? a.gscale + n * a.scale_stride : nullptr;
         for (int kt = 0; kt < nk && !dead; ++kt) {
-            const int s = kt % STAGES;
-            if (kt >= STAGES && !mbar_wait_bounded(&empty[s], uint32_t((kt / STAGES) - 1) & 1u)) {
+            const int st = kt % STAGES;
+            if (kt >= STAGES && !mbar_wait_bounded(&empty[st], uint32_t((kt / STAGES) - 1) & 1u)) {
                 atomicOr(&g_fault_prefill, FAULT_WAIT_EMPTY);
                 dead = true;
                 break;
             }
-            uint8_t *As = sm + s * STAGE_BYTES;
-            uint8_t *Bs = As + A_BYTES;
-            const int64_t k0 = int64_t(kt) * BK;
-            // X tile: row t of the 128 x 64 bf16 tile, eight 16-byte chunks
-            {
-                const int64_t m = m0 + t;
-                uint4 v[8];
-                if (m < M) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(a.X + m * a.ldx + k0);
+            uint8_t *Bs = sm + st * STAGE_BYTES + NSUB * A_BYTES;
+            uint4 v[4];
+            if (n < N) {
+                float w[32];
+                dequant_unit<F>(row, gs_row, uint32_t(2 * kt + h), w);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) v[c] = __ldg(src + c);
-                } else {
+                for (int c = 0; c < 4; ++c)
+                    v[c] = make_uint4(pack_bf16x2(w[8 * c], w[8 * c + 1]), pack_bf16x2(w[8 * c + 2], w[8 * c + 3]),
+                                      pack_bf16x2(w[8 * c + 4], w[8 * c + 5]), pack_bf16x2(w[8 * c + 6], w[8 * c + 7]));
+            } else {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
-                }
-#pragma unroll
-                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(As + sw128_off(uint32_t(t), uint32_t(c))) = v[c];
+                for (int c = 0; c < 4; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
             }
-            // weight tile: rows t and t + 128 of the 256 x 64 bf16 tile
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t r = uint32_t(t + 128 * h);
-                const int64_t n = n0 + r;
-                uint4 v[8];
-                if (n < N) {
-                    float w[64];
-                    dequant64<F>(a.packed + n * a.row_stride, a.gscale ? a.gscale + n * a.scale_stride : nullptr,
-                                 uint32_t(k0), w);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        v[c] = make_uint4(pack_bf16x2(w[8 * c], w[8 * c + 1]), pack_bf16x2(w[8 * c + 2], w[8 * c + 3]),
-                                          pack_bf16x2(w[8 * c + 4], w[8 * c + 5]), pack_bf16x2(w[8 * c + 6], w[8 * c + 7]));
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
-                }
-#pragma unroll
-                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(Bs + sw128_off(r, uint32_t(c))) = v[c];
-            }
+            for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(Bs + sw128_off(uint32_t(r), uint32_t(4 * h + c))) = v[c];
             fence_proxy_async_smem();      // make the generic-proxy stores visible to the tensor core
-            mbar_arrive(&full[s]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[st]);
         }
         // ---------------------------------- epilogue ----------------------------------
         {
@@ -284,58 +295,83 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(PrefillArgs a) {
         }
         tc_fence_after();
         if (!dead) {
-            const int64_t m = m0 + 32 * warp + lane;
-            const uint32_t lane_base = tmem_d + (uint32_t(32 * warp) << 16);
+            // warp w reads TMEM lanes 32 (w % 4) .. +31 (its lane quarter) of sub-tiles 2 (w / 4) and 2 (w / 4) + 1
+            const int qw = warp & 3, half = warp >> 2;
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + uint32_t(32 * cc), r);
-                tmem_ld_wait();
-                const int64_t nc = n0 + 32 * cc;
-                if (m < M && nc < N) {
-                    uint16_t *dst = a.Y + m * a.ldy + nc;
-                    if (nc + 32 <= N && a.vec_y) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * half + jj;
+                if (j >= nsub) break;
+                const int64_t m = m0 + int64_t(BMS) * j + 32 * qw + lane;
+                const uint32_t lane_base = tmem_d + (uint32_t(32 * qw) << 16) + uint32_t(BN * j);
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    uint32_t rr[32];
+                    tmem_ld32(lane_base + uint32_t(32 * cc), rr);
+                    tmem_ld_wait();
+                    const int64_t nc = n0 + 32 * cc;
+                    if (m < M && nc < N) {
+                        uint16_t *dst = a.Y + m * a.ldy + nc;
+                        if (nc + 32 <= N && a.vec_y) {
+                            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            d4[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]), __uint_as_float(r[8 * q + 1])),
-                                               pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
-                                               pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
-                                               pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
-                    } else {
-                        for (int q = 0; q < 32 && nc + q < N; ++q)
-                            dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[q])));
+                            for (int q = 0; q < 4; ++q)
+                                d4[q] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * q]), __uint_as_float(rr[8 * q + 1])),
+                                                   pack_bf16x2(__uint_as_float(rr[8 * q + 2]), __uint_as_float(rr[8 * q + 3])),
+                                                   pack_bf16x2(__uint_as_float(rr[8 * q + 4]), __uint_as_float(rr[8 * q + 5])),
+                                                   pack_bf16x2(__uint_as_float(rr[8 * q + 6]), __uint_as_float(rr[8 * q + 7])));
+                        } else {
+                            for (int q = 0; q < 32 && nc + q < N; ++q)
+                                dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(rr[q])));
+                        }
                     }
                 }
             }
         }
-    } else {
+    } else if (warp == NDQW) {
         // ------------------------------------ MMA issuer ------------------------------------
         if (lane == 0) {
             for (int kt = 0; kt < nk; ++kt) {
-                const int s = kt % STAGES;
-                if (!mbar_wait_bounded(&full[s], uint32_t(kt / STAGES) & 1u)) {
+                const int st = kt % STAGES;
+                if (!mbar_wait_bounded(&full[st], uint32_t(kt / STAGES) & 1u)) {
                     atomicOr(&g_fault_prefill, FAULT_WAIT_FULL);
                     dead = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t As = base + uint32_t(s * STAGE_BYTES), Bs = As + A_BYTES;
+                const uint32_t As = base + uint32_t(st * STAGE_BYTES), Bs = As + uint32_t(NSUB * A_BYTES);
+                for (int j = 0; j < nsub; ++j) {
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    umma_bf16(tmem_d, sw128_kmajor_desc(As + 32u * k), sw128_kmajor_desc(Bs + 32u * k), IDESC,
-                              (kt > 0 || k > 0) ? 1u : 0u);
-                umma_commit(&empty[s]);                 // the stage may be refilled once these MMAs have read it
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_bf16(tmem_d + uint32_t(BN * j), sw128_kmajor_desc(As + uint32_t(j * A_BYTES) + 32u * k),
+                                  sw128_kmajor_desc(Bs + 32u * k), IDESC, (kt > 0 || k > 0) ? 1u : 0u);
+                }
+                umma_commit(&empty[st]);                // the stage may be refilled once these MMAs have read it
             }
-            umma_commit(accum);                         // accumulator complete (also on the failure path)
+            umma_commit(accum);                         // accumulators complete (also on the failure path)
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------ X producer ------------------------------------
+        if (lane == 0) {
+            for (int kt = 0; kt < nk; ++kt) {
+                const int st = kt % STAGES;
+                if (kt >= STAGES && !mbar_wait_bounded(&empty[st], uint32_t((kt / STAGES) - 1) & 1u)) {
+                    atomicOr(&g_fault_prefill, FAULT_WAIT_EMPTY);
+                    break;
+                }
+                uint8_t *As = sm + st * STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[st], uint32_t(nsub * A_BYTES));
+                for (int j = 0; j < nsub; ++j)
+                    tma_load_2d(As + j * A_BYTES, &tm_x, kt * BK, int(m0 + int64_t(BMS) * j), &full[st]);
+            }
         }
         __syncwarp();
     }
 
-    // ---- teardown: every TMEM read is finished; free the accumulator ----
+    // ---- teardown: every TMEM read is finished; free the accumulators ----
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == NDQW) {
         tc_fence_after();
         if (lane == 0 && dead) {
             // On the failure path wait (bounded) for the MMAs already issued before freeing their TMEM.
@@ -344,6 +380,37 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(PrefillArgs a) {
         __syncwarp();
         tmem_dealloc(tmem_d, TMEM_COLS);
     }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tensor map over X [M][ldx] bf16: boxes of 64 K x 128 tokens, 128-byte swizzle (the K-major operand layout of the
+// MMA); tokens past M read as zeros.
+static cudaError_t encode_x(CUtensorMap *m, const PrefillArgs &a) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {cuuint64_t(a.K), cuuint64_t(a.M)};
+    const cuuint64_t strides[1] = {cuuint64_t(a.ldx) * 2};
+    const cuuint32_t box[2] = {uint32_t(BK), uint32_t(BMS)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a.X), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int F>
@@ -357,9 +424,12 @@ static cudaError_t launch_prefill_f(const PrefillArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         opted[dev] = 1;
     }
+    CUtensorMap tmx;
+    const cudaError_t e = encode_x(&tmx, a);
+    if (e != cudaSuccess) return e;
     dim3 grid(unsigned((a.N + BN - 1) / BN), unsigned((a.M + BM - 1) / BM));
     if (grid.y > 65535u) return cudaErrorInvalidValue;
-    prefill_kernel<F><<<grid, THREADS, SMEM_BYTES, s>>>(a);
+    prefill_kernel<F><<<grid, THREADS, SMEM_BYTES, s>>>(tmx, a);
     return cudaGetLastError();
 }
 
