@@ -132,84 +132,109 @@ __device__ __forceinline__ void ldg_words_a2(const uint8_t *p, uint32_t *w) {
 #pragma unroll
     for (int i = 0; i < n; ++i) w[i] = __funnelshift_r(r[i], r[i + 1], sh);
 }
-__device__ __forceinline__ float i2f_small(int v) { return float(v); }
 
-// Dequantize 32-weight unit u of one packed row to fp32, exactly as FORMATS.md (the roundings of the dequant kernel
-// and the CPU reference: the sub-block scale d * L first, then its product with the code, minus dmin * M).
+// Dequantization of one 32-weight unit u of a packed row, in two steps so that the loads of the next K step can be in
+// flight while the current one is converted: load_raw gathers the unit's bytes with aligned global loads,
+// unit_bf16 turns them into 16 bf16x2 words. The values are exactly those of FORMATS.md (the sub-block scale d * L
+// first, then its product with the code, minus dmin * M; every step an fp32 rounding) rounded to bf16.
+struct RawUnit {
+    uint32_t c[5];      // code words (formats differ in how many they use)
+    uint32_t e[4];      // high-bit planes / scale fields / super-block scales
+};
 template <int F>
-__device__ __forceinline__ void dequant_unit(const uint8_t *row, const float *gs_row, uint32_t u, float w[32]) {
+__device__ __forceinline__ void load_raw(const uint8_t *row, const float *gs_row, uint32_t u, RawUnit &r) {
     if constexpr (F == FMT_Q4G32) {
         const uint4 c = __ldg(reinterpret_cast<const uint4 *>(row + 16 * u));
-        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-        const float sc = __ldg(gs_row + u);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = __fmul_rn(sc, i2f_small(int((cw[i >> 3] >> (4 * (i & 7))) & 15u) - 8));
+        r.c[0] = c.x; r.c[1] = c.y; r.c[2] = c.z; r.c[3] = c.w;
+        r.e[0] = __float_as_uint(__ldg(gs_row + u));
     } else {
         const uint32_t b = u >> 3, su = u & 7u;
         const uint8_t *blk = row + b * Fmt<F>::bytes;
         if constexpr (F == FMT_Q2S) {
-            const uint32_t cw[2] = {ldg32(blk + 8 * su), ldg32(blk + 8 * su + 4)};
-            const uint32_t lm = ldg16(blk + 64 + 2 * su);
-            const uint32_t dd = ldg32(blk + 80);
-            const float D = h2f_bits(uint16_t(dd & 0xFFFFu)), Dm = h2f_bits(uint16_t(dd >> 16));
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t l = (lm >> (8 * h)) & 0xFFu;
-                const float es = __fmul_rn(D, float(l & 15u)), em = __fmul_rn(Dm, float(l >> 4));
-#pragma unroll
-                for (int i = 0; i < 16; ++i) w[16 * h + i] = __fsub_rn(__fmul_rn(es, float((cw[h] >> (2 * i)) & 3u)), em);
-            }
+            r.c[0] = ldg32(blk + 8 * su); r.c[1] = ldg32(blk + 8 * su + 4);
+            r.e[0] = ldg16(blk + 64 + 2 * su);
+            r.e[1] = ldg32(blk + 80);
         } else if constexpr (F == FMT_Q3S) {
-            uint32_t c3[3];
-            ldg_words_a2<3>(blk + 12 * su, c3);
-            const uint32_t v[4] = {c3[0], __funnelshift_r(c3[0], c3[1], 24), __funnelshift_r(c3[1], c3[2], 16), c3[2] >> 8};
-            // the 12 bits of L_{2su}, L_{2su+1}: bits 12 (su & 1) .. +11 of the 24-bit field group su >> 1, read as two
-            // bytes that stay inside the super-block
+            ldg_words_a2<3>(blk + 12 * su, r.c);
+            // the 12 bits of L_{2su}, L_{2su+1}: bits 12 (su & 1) .. +11 of the 24-bit field group su >> 1, read as
+            // two bytes that stay inside the super-block
             const uint32_t fb = 96u + 3u * (su >> 1) + (su & 1u);
-            const uint32_t two = uint32_t(__ldg(blk + fb)) | (uint32_t(__ldg(blk + fb + 1)) << 8);
-            const uint32_t fsh = 4u * (su & 1u);
-            const float D = h2f_bits(uint16_t(ldg16(blk + 108)));
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float es = __fmul_rn(D, float((two >> (fsh + 6 * h)) & 63u));
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int g = 2 * h + (i >> 3), t = i & 7;
-                    w[16 * h + i] = __fmul_rn(es, float(int((v[g] >> (3 * t)) & 7u) - 4));
-                }
-            }
+            r.e[0] = uint32_t(__ldg(blk + fb)) | (uint32_t(__ldg(blk + fb + 1)) << 8);
+            r.e[1] = ldg16(blk + 108);
         } else if constexpr (F == FMT_Q5S) {
             const uint4 c = __ldg(reinterpret_cast<const uint4 *>(blk + 16 * su));
-            const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-            const uint32_t H = ldg32(blk + 128 + 4 * su);
+            r.c[0] = c.x; r.c[1] = c.y; r.c[2] = c.z; r.c[3] = c.w;
+            r.c[4] = ldg32(blk + 128 + 4 * su);
             const uint4 fl = __ldg(reinterpret_cast<const uint4 *>(blk + 160));
-            const uint64_t lo64 = (uint64_t(fl.y) << 32) | fl.x, hi64 = (uint64_t(fl.z) << 32) | fl.y;
-            const float D = h2f_bits(uint16_t(fl.w & 0xFFFFu)), Dm = h2f_bits(uint16_t(fl.w >> 16));
-            const float es = __fmul_rn(D, float(uint32_t(lo64 >> (6 * su)) & 63u));
-            const float em = __fmul_rn(Dm, float(uint32_t(hi64 >> (16 + 6 * su)) & 63u));
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const uint32_t q = ((cw[i >> 3] >> (4 * (i & 7))) & 15u) | (((H >> i) & 1u) << 4);
-                w[i] = __fsub_rn(__fmul_rn(es, float(q)), em);
-            }
+            r.e[0] = fl.x; r.e[1] = fl.y; r.e[2] = fl.z; r.e[3] = fl.w;
         } else {
-            uint32_t c4[4], h2[2];
-            ldg_words_a2<4>(blk + 16 * su, c4);
-            ldg_words_a2<2>(blk + 128 + 8 * su, h2);
-            const uint32_t ls = ldg16(blk + 192 + 2 * su);
-            const float D = h2f_bits(uint16_t(ldg16(blk + 208)));
+            ldg_words_a2<4>(blk + 16 * su, r.c);
+            ldg_words_a2<2>(blk + 128 + 8 * su, r.e);
+            r.e[2] = ldg16(blk + 192 + 2 * su);
+            r.e[3] = ldg16(blk + 208);
+        }
+    }
+}
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+template <int F>
+__device__ __forceinline__ void unit_bf16(const RawUnit &r, uint32_t u, uint32_t out[16]) {
+    float w[32];
+    if constexpr (F == FMT_Q4G32) {
+        const float sc = __uint_as_float(r.e[0]);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float es = __fmul_rn(D, float(int(int8_t(uint8_t(ls >> (8 * hh))))));
+        for (int i = 0; i < 32; ++i) w[i] = __fmul_rn(sc, float(int((r.c[i >> 3] >> (4 * (i & 7))) & 15u) - 8));
+    } else if constexpr (F == FMT_Q2S) {
+        const float D = h2f_bits(uint16_t(r.e[1] & 0xFFFFu)), Dm = h2f_bits(uint16_t(r.e[1] >> 16));
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int ii = 16 * hh + i;
-                    const uint32_t q = ((c4[ii >> 3] >> (4 * (ii & 7))) & 15u) | (((h2[hh] >> (2 * i)) & 3u) << 4);
-                    w[ii] = __fmul_rn(es, float(int(q) - 32));
-                }
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t l = (r.e[0] >> (8 * h)) & 0xFFu;
+            const float es = __fmul_rn(D, float(l & 15u)), em = __fmul_rn(Dm, float(l >> 4));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[16 * h + i] = __fsub_rn(__fmul_rn(es, float((r.c[h] >> (2 * i)) & 3u)), em);
+        }
+    } else if constexpr (F == FMT_Q3S) {
+        const uint32_t su = u & 7u;
+        const uint32_t v[4] = {r.c[0], __funnelshift_r(r.c[0], r.c[1], 24), __funnelshift_r(r.c[1], r.c[2], 16), r.c[2] >> 8};
+        const uint32_t fsh = 4u * (su & 1u);
+        const float D = h2f_bits(uint16_t(r.e[1]));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float es = __fmul_rn(D, float((r.e[0] >> (fsh + 6 * h)) & 63u));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int g = 2 * h + (i >> 3), t = i & 7;
+                w[16 * h + i] = __fmul_rn(es, float(int((v[g] >> (3 * t)) & 7u) - 4));
+            }
+        }
+    } else if constexpr (F == FMT_Q5S) {
+        const uint32_t su = u & 7u;
+        const uint64_t lo64 = (uint64_t(r.e[1]) << 32) | r.e[0], hi64 = (uint64_t(r.e[2]) << 32) | r.e[1];
+        const float D = h2f_bits(uint16_t(r.e[3] & 0xFFFFu)), Dm = h2f_bits(uint16_t(r.e[3] >> 16));
+        const float es = __fmul_rn(D, float(uint32_t(lo64 >> (6 * su)) & 63u));
+        const float em = __fmul_rn(Dm, float(uint32_t(hi64 >> (16 + 6 * su)) & 63u));
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t q = ((r.c[i >> 3] >> (4 * (i & 7))) & 15u) | (((r.c[4] >> i) & 1u) << 4);
+            w[i] = __fsub_rn(__fmul_rn(es, float(q)), em);
+        }
+    } else {
+        const float D = h2f_bits(uint16_t(r.e[3]));
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const float es = __fmul_rn(D, float(int(int8_t(uint8_t(r.e[2] >> (8 * hh))))));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int ii = 16 * hh + i;
+                const uint32_t q = ((r.c[ii >> 3] >> (4 * (ii & 7))) & 15u) | (((r.e[hh] >> (2 * i)) & 3u) << 4);
+                w[ii] = __fmul_rn(es, float(int(q) - 32));
             }
         }
     }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) out[i] = bf16x2_rn(w[2 * i], w[2 * i + 1]);
 }
 
 // 2-D tensor copy global -> shared (box at coordinates {x, y}), completion on `bar` as bytes.
@@ -259,8 +284,12 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         const int64_t n = n0 + r;
         const uint8_t *row = a.packed + n * a.row_stride;
         const float *gs_row = a.gscale ? a.gscale + n * a.scale_stride : nullptr;
+        // the raw bytes of step kt + 1 are loaded while step kt is converted and stored
+        RawUnit cur = {}, nxt = {};
+        if (n < N && nk > 0) load_raw<F>(row, gs_row, uint32_t(h), cur);
         for (int kt = 0; kt < nk && !dead; ++kt) {
             const int st = kt % STAGES;
+            if (n < N && kt + 1 < nk) load_raw<F>(row, gs_row, uint32_t(2 * (kt + 1) + h), nxt);
             if (kt >= STAGES && !mbar_wait_bounded(&empty[st], uint32_t((kt / STAGES) - 1) & 1u)) {
                 atomicOr(&g_fault_prefill, FAULT_WAIT_EMPTY);
                 dead = true;
@@ -269,16 +298,15 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
             uint8_t *Bs = sm + st * STAGE_BYTES + NSUB * A_BYTES;
             uint4 v[4];
             if (n < N) {
-                float w[32];
-                dequant_unit<F>(row, gs_row, uint32_t(2 * kt + h), w);
+                uint32_t o[16];
+                unit_bf16<F>(cur, uint32_t(2 * kt + h), o);
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    v[c] = make_uint4(pack_bf16x2(w[8 * c], w[8 * c + 1]), pack_bf16x2(w[8 * c + 2], w[8 * c + 3]),
-                                      pack_bf16x2(w[8 * c + 4], w[8 * c + 5]), pack_bf16x2(w[8 * c + 6], w[8 * c + 7]));
+                for (int c = 0; c < 4; ++c) v[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
             }
+            cur = nxt;
 #pragma unroll
             for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(Bs + sw128_off(uint32_t(r), uint32_t(4 * h + c))) = v[c];
             fence_proxy_async_smem();      // make the generic-proxy stores visible to the tensor core
