@@ -128,3 +128,43 @@ def test_q3s_config_matrix_bit_exact(qpg, orc):
     torch.cuda.synchronize()
     rp, _, _ = orc.quantize_pack(orc.Q3S, W.numpy())
     assert np.array_equal(packed.cpu().numpy(), rp)
+
+
+def test_int4_quotients_at_rounding_boundaries(qpg, orc):
+    """Weights whose quotient w / s sits on or next to a half-integer (ties round to even, P2 §3.1's torch.round): the
+    codes must still equal the oracle's (IEEE division, then round half to even)."""
+    s = np.float32(0.01)
+    rng = np.random.default_rng(5)
+    N, K = 64, 4096
+    W = np.empty((N, K), np.float32)
+    for r in range(N):
+        k = rng.integers(-8, 7, K).astype(np.float32) + np.float32(0.5)
+        w = (k * s).astype(np.float32)
+        step = rng.integers(-2, 3, K)                    # the tie itself and its fp32 neighbours
+        w = np.where(step > 0, np.nextafter(w, np.float32(np.inf)), w)
+        w = np.where(step < 0, np.nextafter(w, np.float32(-np.inf)), w)
+        w = np.where(step == 2, np.nextafter(w, np.float32(np.inf)), w)
+        w = np.where(step == -2, np.nextafter(w, np.float32(-np.inf)), w)
+        W[r] = w
+    W[:, ::32] = np.float32(8) * s                        # every group's max: s = max / 8 exactly
+    Wt = torch.from_numpy(W)
+    packed, gs = qpg.qpack_quantize_pack(qpg.Q4G32, Wt.cuda())
+    torch.cuda.synchronize()
+    rp, rgs, _ = orc.quantize_pack(orc.Q4G32, W)
+    assert np.array_equal(packed.cpu().numpy(), rp)
+    assert np.array_equal(gs.cpu().numpy().view(np.uint32), rgs.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_quantize_pack_large_bit_exact(qpg, orc, name):
+    """16.7 M weights per format (the fast quotient's fallback to the exact division is taken about once per 10^4
+    weights): packed bytes and scales bit-exact."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    W = synth.laplace((4096, 4096), 0.02, 77)
+    packed, gs = qpg.qpack_quantize_pack(fmt, W.cuda())
+    torch.cuda.synchronize()
+    rp, rgs, _ = orc.quantize_pack(fmt, W.numpy())
+    assert np.array_equal(packed.cpu().numpy(), rp)
+    if rgs is not None:
+        assert np.array_equal(gs.cpu().numpy().view(np.uint32), rgs.view(np.uint32))
