@@ -168,47 +168,43 @@ def run_reference(args, world, rank):
 
 
 def decode_7b_extra(qp, torch, synth, dev, steps=10):
-    """7B-Llama-shaped decode step per super-block format: tokens/s-equivalent = 1 / (sum of GEMV times)."""
+    """7B-Llama-shaped decode step per super-block format: tokens/s-equivalent = 1 / (sum of GEMV times). Each layer's
+    q/k/v (which read the same activations) are one row-concatenated packed matrix, and so are gate/up, so a layer is
+    4 products (qkv 12288x4096, o 4096x4096, gate|up 22016x4096, down 4096x11008); quantization is per row group,
+    so the packed bytes equal those of the separate matrices. The 7-launch form is timed as well."""
     shapes = [(4096, 4096)] * 4 + [(11008, 4096)] * 2 + [(4096, 11008)]
+    groups = [[0, 1, 2], [3], [4, 5], [6]]           # q|k|v, o, gate|up, down
     out = {}
     for name in ("Q2S", "Q3S", "Q5S", "Q6S"):
         fmt = qp.FORMATS[name]
-        mats, total = [], 0
+        fused, separate, total = [], [], 0
         for layer in range(32):
+            packed = []
             for mi, (N, K) in enumerate(shapes):
                 W = synth.laplace((N, K), 0.02, seed=synth.seed_for(3, layer, mi), device=dev)
                 p, g = qp.qpack_quantize_pack(fmt, W)
                 del W
-                mats.append((p, N, K))
+                packed.append(p)
+                separate.append((p, N, K))
                 total += qp.layout(fmt, N, K)["weight_bytes"]
+            for gidx in groups:
+                K = shapes[gidx[0]][1]
+                fused.append((torch.cat([packed[i] for i in gidx], 0), sum(shapes[i][0] for i in gidx), K))
         x4 = synth.normal((4096,), 1.0, seed=11, device=dev, dtype=torch.float16)
         x11 = synth.normal((11008,), 1.0, seed=12, device=dev, dtype=torch.float16)
-        ys = {4096: torch.empty(4096, device=dev), 11008: torch.empty(11008, device=dev)}
-        s = torch.cuda.Stream(device=dev)
+        ys = {N: torch.empty(N, device=dev) for N in (4096, 11008, 12288, 22016)}
+        res = {}
+        for kind, mats in (("fused", fused), ("separate", separate)):
 
-        def step():
-            for p, N, K in mats:
-                qp.qgemv(fmt, p, None, N, K, x4 if K == 4096 else x11, ys[N], stream=s)
+            def fn(s, mats=mats):
+                for p, N, K in mats:
+                    qp.qgemv(fmt, p, None, N, K, x4 if K == 4096 else x11, ys[N], stream=s)
 
-        with torch.cuda.stream(s):
-            step()
-            torch.cuda.synchronize(dev)
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=s):
-                step()
-            for _ in range(3):
-                gr.replay()
-            torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(s)
-            for _ in range(steps):
-                gr.replay()
-            e1.record(s)
-        torch.cuda.synchronize(dev)
-        t = e0.elapsed_time(e1) / 1e3 / steps
-        out[name] = {"tok_per_s_equiv": 1.0 / t, "GBps": total / t / 1e9, "bytes_per_step": total,
-                     "ms_per_step": t * 1e3, "launches": len(mats)}
-        del mats, gr
+            t = _time_graph(torch, fn, dev, reps=steps)
+            res[kind] = {"tok_per_s_equiv": 1.0 / t, "GBps": total / t / 1e9, "ms_per_step": t * 1e3,
+                         "launches": len(mats)}
+        out[name] = {"bytes_per_step": total, **res["fused"], "separate_launches": res["separate"]}
+        del fused, separate
         torch.cuda.empty_cache()
     return out
 
