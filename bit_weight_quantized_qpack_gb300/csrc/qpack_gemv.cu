@@ -50,17 +50,32 @@ __device__ __forceinline__ float fma2h(uint32_t codes, uint16_t xa, uint16_t xb,
 // x halves of a unit: xv[t] holds x'[2t], x'[2t+1].
 __device__ __forceinline__ uint16_t xh(const uint32_t *xv, int i) { return (i & 1) ? hi16(xv[i >> 1]) : lo16(xv[i >> 1]); }
 
+// Two-way integer dot products: c + a.h0 * b.byte(k) + a.h1 * b.byte(k + 1), a = two signed 16-bit values, b = four
+// unsigned bytes, k = 0 (lo) or 2 (hi). Exact in int32.
+__device__ __forceinline__ int32_t dp2a_lo(uint32_t a, uint32_t b, int32_t c) {
+    int32_t d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int32_t dp2a_hi(uint32_t a, uint32_t b, int32_t c) {
+    int32_t d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// One Q4G32 code word (weights 8j..8j+7, weight 8j+2b in the low nibble of byte b, 8j+2b+1 in the high nibble) against
+// the unit's 16-bit activations A[0..3] = (x0, x2), (x4, x6), (x1, x3), (x5, x7) of those weights: the low nibbles
+// add u * x to lo, the high nibbles, masked in place, add 16 u * x to hi.
+__device__ __forceinline__ void nib_dp(uint32_t c, const uint32_t *A, int32_t &lo, int32_t &hi) {
+    const uint32_t l = c & 0x0F0F0F0Fu, h = c & 0xF0F0F0F0u;
+    lo = dp2a_lo(A[0], l, lo);
+    lo = dp2a_hi(A[1], l, lo);
+    hi = dp2a_lo(A[2], h, hi);
+    hi = dp2a_hi(A[3], h, hi);
+}
+
 // ------------------------------------------------------------------------------------------------------------
 // Unpack + multiply helpers. Two accumulators (a, b) only for instruction-level parallelism.
 // ------------------------------------------------------------------------------------------------------------
-// 8 nibbles, nibble k at bits 4k (weights i0 + k). Bit classes: even k at p = 0, odd k at p = 4.
-__device__ __forceinline__ void nib_word(uint32_t c, const uint32_t *xv, int i0, float &a, float &b) {
-    const uint32_t c2 = c >> 8;
-    a = fma2h(lop3_and_or(c, 0x000F000Fu, MAGIC2), xh(xv, i0 + 0), xh(xv, i0 + 4), a);
-    b = fma2h(lop3_and_or(c, 0x00F000F0u, MAGIC2), xh(xv, i0 + 1), xh(xv, i0 + 5), b);
-    a = fma2h(lop3_and_or(c2, 0x000F000Fu, MAGIC2), xh(xv, i0 + 2), xh(xv, i0 + 6), a);
-    b = fma2h(lop3_and_or(c2, 0x00F000F0u, MAGIC2), xh(xv, i0 + 3), xh(xv, i0 + 7), b);
-}
 // Nibble word with HB extra high bits merged just above each nibble. X holds the high bits of weights
 // i0..i0+3 at bits HB*k (k = 0..3) and of weights i0+4..i0+7 at bits 16 + HB*k; (X << s_k) & mask lands pair
 // k's high bits right above its nibbles.
@@ -122,7 +137,7 @@ __host__ __device__ constexpr int slot_elem(int k, int h) {
 
 // Activation constants per unit (XC<F>::n floats), from the staged x' (see the file comment).
 template <int F> struct XC;
-template <> struct XC<FMT_Q4G32> { static constexpr int n = 1; };   // C
+template <> struct XC<FMT_Q4G32> { static constexpr int n = 2; };   // C (int bits), 2^-(E+4)
 template <> struct XC<FMT_Q2S> { static constexpr int n = 4; };     // C0, S0, C1, S1 (two sub-blocks)
 template <> struct XC<FMT_Q3S> { static constexpr int n = 2; };     // C0, C1
 template <> struct XC<FMT_Q5S> { static constexpr int n = 2; };     // C, S
@@ -134,9 +149,8 @@ __device__ __forceinline__ void unit_consts(const float xp[32], const float xt[3
     float sp[2] = {0.f, 0.f}, st[2] = {0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 32; ++i) { sp[i >> 4] += xp[i]; st[i >> 4] += xt[i]; }
-    if constexpr (F == FMT_Q4G32) {
-        out[0] = 1024.0f * (sp[0] + sp[1]) + 8.0f * (st[0] + st[1]);
-    } else if constexpr (F == FMT_Q2S) {
+    static_assert(F != FMT_Q4G32, "Q4G32 activations are staged as 16-bit integers (stage_unit_i16)");
+    if constexpr (F == FMT_Q2S) {
         out[0] = 1024.0f * sp[0]; out[1] = st[0];
         out[2] = 1024.0f * sp[1]; out[3] = st[1];
     } else if constexpr (F == FMT_Q3S) {
@@ -227,14 +241,15 @@ template <int F>
 __device__ __forceinline__ void row_acc(const uint8_t *u, const float *sp, const LaneGeo &g, const float *c,
                                         const uint32_t *xv, bool on, float &acc) {
     if constexpr (F == FMT_Q4G32) {
+        // 16 * sum (u - 8) x_i in int32 (exact), then one conversion and the group scale times 2^-(E+4)
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
         const float s = on ? sp[0] : 0.f;
-        float a = -c[0], b = 0.f;
-        nib_word(w.x, xv, 0, a, b);
-        nib_word(w.y, xv, 8, a, b);
-        nib_word(w.z, xv, 16, a, b);
-        nib_word(w.w, xv, 24, a, b);
-        acc = fmaf(s, a + b, acc);
+        int32_t lo = 0, hi = __float_as_int(c[0]);
+        nib_dp(w.x, xv + 0, lo, hi);
+        nib_dp(w.y, xv + 4, lo, hi);
+        nib_dp(w.z, xv + 8, lo, hi);
+        nib_dp(w.w, xv + 12, lo, hi);
+        acc = fmaf(float(16 * lo + hi), s * c[1], acc);
     } else if constexpr (F == FMT_Q2S) {
         const uint32_t w0 = lds32(u), w1 = lds32(u + 4);
         const uint32_t dd = on ? lds32(u + g.o2) : 0u;                   // d (low half), dmin (high half)
@@ -318,13 +333,6 @@ struct URow {
     float f0, f1;   // sub-block scale factors (w' = f * code for the symmetric part)
     float g0, g1;   // minima factors of the asymmetric formats (dmin * M_j), else 0
 };
-__device__ __forceinline__ void unpack_nib(uint32_t c, uint32_t *hw) {
-    const uint32_t c2 = c >> 8;
-    hw[0] = lop3_and_or(c, 0x000F000Fu, MAGIC2);
-    hw[1] = lop3_and_or(c, 0x00F000F0u, MAGIC2);
-    hw[2] = lop3_and_or(c2, 0x000F000Fu, MAGIC2);
-    hw[3] = lop3_and_or(c2, 0x00F000F0u, MAGIC2);
-}
 template <int HB>
 __device__ __forceinline__ void unpack_nib_hi(uint32_t c, uint32_t X, uint32_t *hw) {
     constexpr uint32_t mlo = (HB == 1) ? 0x00100010u : 0x00300030u;
@@ -363,7 +371,10 @@ __device__ __forceinline__ void unpack_row(const uint8_t *u, const float *sp, co
     if constexpr (F == FMT_Q4G32) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
         r.f0 = r.f1 = on ? sp[0] : 0.f;
-        unpack_nib(w.x, r.hw); unpack_nib(w.y, r.hw + 4); unpack_nib(w.z, r.hw + 8); unpack_nib(w.w, r.hw + 12);
+        // the dp2a operands: hw[2j] = low nibbles of word j in place, hw[2j + 1] = its high nibbles in place
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { r.hw[2 * j] = wv[j] & 0x0F0F0F0Fu; r.hw[2 * j + 1] = wv[j] & 0xF0F0F0F0u; }
     } else if constexpr (F == FMT_Q2S) {
         const uint32_t w0 = lds32(u), w1 = lds32(u + 4);
         const uint32_t dd = on ? lds32(u + g.o2) : 0u;
@@ -426,8 +437,20 @@ __device__ __forceinline__ void unpack_row(const uint8_t *u, const float *sp, co
 // acc += sum_i w'_i x_i of an unpacked unit-row against one staged activation row (xv, c: that row's unit constants).
 template <int F>
 __device__ __forceinline__ void dot_row(const URow &r, const uint32_t *xv, const float *c, float &acc) {
+    if constexpr (F == FMT_Q4G32) {
+        int32_t lo = 0, hi = __float_as_int(c[0]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            lo = dp2a_lo(xv[4 * j], r.hw[2 * j], lo);
+            lo = dp2a_hi(xv[4 * j + 1], r.hw[2 * j], lo);
+            hi = dp2a_lo(xv[4 * j + 2], r.hw[2 * j + 1], hi);
+            hi = dp2a_hi(xv[4 * j + 3], r.hw[2 * j + 1], hi);
+        }
+        acc = fmaf(float(16 * lo + hi), r.f0 * c[1], acc);
+        return;
+    }
     float a0, a1;
-    if constexpr (F == FMT_Q4G32 || F == FMT_Q5S) { a0 = -c[0]; a1 = 0.f; }
+    if constexpr (F == FMT_Q5S) { a0 = -c[0]; a1 = 0.f; }
     else if constexpr (F == FMT_Q2S) { a0 = -c[0]; a1 = -c[2]; }
     else { a0 = -c[0]; a1 = -c[1]; }
 #pragma unroll
@@ -437,9 +460,7 @@ __device__ __forceinline__ void dot_row(const URow &r, const uint32_t *xv, const
         a1 = fma_h(lo16(r.hw[8 + j]), xh(xv, hslot<F>(8 + j, 0)), a1);
         a1 = fma_h(hi16(r.hw[8 + j]), xh(xv, hslot<F>(8 + j, 1)), a1);
     }
-    if constexpr (F == FMT_Q4G32) {
-        acc = fmaf(r.f0, a0 + a1, acc);
-    } else if constexpr (F == FMT_Q5S) {
+    if constexpr (F == FMT_Q5S) {
         acc = fmaf(r.f0, a0 + a1, acc);
         acc = fmaf(-r.g0, c[1], acc);
     } else {
@@ -483,27 +504,59 @@ __device__ __forceinline__ int part_exponent(uint32_t mbits) {
 
 // Stage one unit: raw = its 32 fp16 activations (four 16-byte vectors), E = the part's scale exponent. Writes the
 // unit's four staged vectors (x' = fp16(x * 2^(E - p)), see stage_half_unit) and its activation constants.
-template <int F>
-__device__ __forceinline__ void stage_unit(const uint4 (&raw)[4], int E, uint4 *xs, float *cst, uint32_t U, uint32_t u) {
-    uint32_t w[16];
+// Q4G32 staging: the unit's 32 activations as 16-bit integers xi = rint(x * 2^E), E = the unit's own exponent (max
+// |x| * 2^E in [2^14, 2^15), so |xi| <= 32752; an inf clamps to 32767, a nan gives 0), vector j holding the dp2a
+// operands of code word j (see nib_dp). Constants: -128 * sum(xi) as int bits (the code offset 8, times the 16 of
+// the high-nibble accumulator) and 2^-(E+4).
+__device__ __forceinline__ void stage_unit_i16(const uint4 (&raw)[4], uint4 *xs, float *cst, uint32_t U, uint32_t u) {
+    const uint32_t hx[16] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w,
+                             raw[2].x, raw[2].y, raw[2].z, raw[2].w, raw[3].x, raw[3].y, raw[3].z, raw[3].w};
+    uint32_t mx = 0;
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t rw[8] = {raw[2 * hh].x, raw[2 * hh].y, raw[2 * hh].z, raw[2 * hh].w,
-                                raw[2 * hh + 1].x, raw[2 * hh + 1].y, raw[2 * hh + 1].z, raw[2 * hh + 1].w};
-        uint16_t xr[16];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { xr[2 * e] = lo16(rw[e]); xr[2 * e + 1] = hi16(rw[e]); }
-        stage_half_unit<F>(xr, E, w + 8 * hh);
-    }
-#pragma unroll
-    for (int t = 0; t < 4; ++t) xs[t * U + u] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
-    float xp[32], xt[32];
+    for (int e = 0; e < 16; ++e) mx = max(mx, max(hx[e] & 0x7FFFu, (hx[e] >> 16) & 0x7FFFu));
+    const int E = part_exponent(mx);
+    const float sc = exp2i(E);
+    int32_t xi[32], sum = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        xp[i] = h2f_bits(xh(w, i));
-        xt[i] = xp[i] * pow2f(xshift<F>(i));
+        const int32_t v = __float2int_rn(h2f_bits((i & 1) ? hi16(hx[i >> 1]) : lo16(hx[i >> 1])) * sc);
+        xi[i] = min(max(v, -32767), 32767);
+        sum += xi[i];
     }
-    unit_consts<F>(xp, xt, cst + u * XC<F>::n);
+    auto pk = [&](int i0, int i1) { return (uint32_t(xi[i0]) & 0xFFFFu) | (uint32_t(xi[i1]) << 16); };
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        xs[j * U + u] = make_uint4(pk(8 * j, 8 * j + 2), pk(8 * j + 4, 8 * j + 6), pk(8 * j + 1, 8 * j + 3),
+                                   pk(8 * j + 5, 8 * j + 7));
+    cst[2 * u] = __int_as_float(-128 * sum);
+    cst[2 * u + 1] = exp2i(-(E + 4));
+}
+
+template <int F>
+__device__ __forceinline__ void stage_unit(const uint4 (&raw)[4], int E, uint4 *xs, float *cst, uint32_t U, uint32_t u) {
+    if constexpr (F == FMT_Q4G32) {
+        stage_unit_i16(raw, xs, cst, U, u);   // per-unit exponent; E (the part's) is not used
+    } else {
+        uint32_t w[16];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t rw[8] = {raw[2 * hh].x, raw[2 * hh].y, raw[2 * hh].z, raw[2 * hh].w,
+                                    raw[2 * hh + 1].x, raw[2 * hh + 1].y, raw[2 * hh + 1].z, raw[2 * hh + 1].w};
+            uint16_t xr[16];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { xr[2 * e] = lo16(rw[e]); xr[2 * e + 1] = hi16(rw[e]); }
+            stage_half_unit<F>(xr, E, w + 8 * hh);
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) xs[t * U + u] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+        float xp[32], xt[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            xp[i] = h2f_bits(xh(w, i));
+            xt[i] = xp[i] * pow2f(xshift<F>(i));
+        }
+        unit_consts<F>(xp, xt, cst + u * XC<F>::n);
+    }
 }
 
 // Sum R per-lane values over the warp, one value per row: after the call, lanes j * (32 / R) (j < R) hold the warp
@@ -674,13 +727,13 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                         for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
                     }
                 }
-                if (uint32_t(tid - lane) + h * NT < U) {            // the warp's first unit exists
+                if (F != FMT_Q4G32 && uint32_t(tid - lane) + h * NT < U) {   // the warp's first unit exists
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                     if (lane == 0) atomicMax(&pmax[((uint32_t(tid) + h * NT) % UPC) / 32], mx);
                 }
             }
-            named_bar_sync(1, G1_CW * 32);
+            if constexpr (F != FMT_Q4G32) named_bar_sync(1, G1_CW * 32);   // Q4G32: per-unit exponents
 #pragma unroll
             for (int h = 0; h < HU; ++h) {
                 const uint32_t u = uint32_t(tid) + h * NT;
@@ -691,7 +744,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
             // consecutive items are one 32-unit run of one chunk of one row, i.e. of one (row, K part). Two passes:
             // the max, then (after a barrier) a reload and the staging. Rows m >= Mg of a short group stage zeros.
             const uint32_t Upad = (U + 31) / 32 * 32, items = uint32_t(MT) * Upad;
-            for (uint32_t it = uint32_t(tid); it < items; it += NT) {
+            for (uint32_t it = uint32_t(tid); F != FMT_Q4G32 && it < items; it += NT) {   // Q4G32: per-unit exponents
                 const uint32_t m = it / Upad, u = it - m * Upad;
                 uint32_t mx = 0;
                 if (u < U && m < Mg) {
@@ -708,7 +761,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                 if (lane == 0) atomicMax(&pmax[m * P + (u % UPC) / 32], mx);
             }
-            named_bar_sync(1, G1_CW * 32);
+            if constexpr (F != FMT_Q4G32) named_bar_sync(1, G1_CW * 32);
             for (uint32_t it = uint32_t(tid); it < items; it += NT) {
                 const uint32_t m = it / Upad, u = it - m * Upad;
                 if (u < U) {
