@@ -8,15 +8,15 @@
 //   warp 16      producer: 2-D TMA tensor copies of (row tile x K chunk) boxes of the packed rows into a ring of
 //                shared-memory stages (completion on mbarriers, L2 evict-first because each byte is used once).
 //   warps 0..15  consumers: row class x K part of every stage; lane l owns one 32-weight unit of each chunk.
-// Unpacking (2/3/5/6-bit article §3.3: separate unpack from multiply-add, factor s*(q.x) + m*sum(x)): codes are
-// OR-ed into the mantissa of an fp16 1024.0 with one LOP3 per pair of weights, so a half holds 1024 + u*2^p
-// exactly, p being the code's bit position inside its 16-bit half. The activations are staged in shared memory
-// pre-scaled by 2^-p of the code they meet (x' = fp16(x * 2^-p), exact unless subnormal), so one fp32 FMA with
-// fp16 inputs (exact product) per weight accumulates 1024*x' + u*x for every class into one accumulator. The
-// 1024*sum(x') terms, the symmetric code offsets and the asymmetric minima are removed per sub-block with
-// activation sums that each CTA precomputes once. Per row, each warp reduces its lanes' sums with shuffles and
-// stores one partial per K part in shared memory; the partials are scaled back by each part's power of two and
-// summed in a fixed order (deterministic) before y is written.
+// Unpacking (2/3/5/6-bit article §3.3: separate unpack from multiply-add, factor s*(q.x) + m*sum(x)) works on integers:
+// each unit-row is unpacked with masks, byte permutes and shifts into eight words whose bytes each hold one code,
+// possibly shifted left inside its byte by a known "bit class"; the activations are staged once per launch as 16-bit
+// fixed point with a per-unit power-of-two scale, in the order the code bytes meet them. dp2a (two 16 x 8-bit
+// products per instruction) accumulates exact int32 sums per class, the classes are folded with integer
+// multiply-adds, and each sub-block-row needs one conversion and one fp32 FMA with its scale; the symmetric code
+// offsets ride in the accumulators' start values and the asymmetric minima use per-unit activation sums. Per row,
+// each warp reduces its lanes' sums with shuffles and stores one partial per K part in shared memory; the partials
+// are summed in a fixed order (deterministic) before y is written.
 //
 // Small batches (M = 2..16) use the same kernel with MT activation rows: each unit-row is unpacked once and
 // multiplied against every staged activation row; rows beyond what shared memory holds go in further launches.
@@ -34,21 +34,27 @@ __device__ int g_fault_gemv = 0;
 
 namespace {
 
-constexpr uint32_t MAGIC2 = 0x64006400u; // fp16 1024.0 in both halves
-constexpr uint32_t MAGICF = 0x4B000000u; // fp32 2^23
+constexpr uint32_t MAGIC2 = 0x64006400u;   // fp16 1024.0 in both halves
+constexpr uint32_t MAGICF = 0x4B000000u;   // fp32 2^23
+constexpr uint32_t HNEG1024 = 0xE400E400u; // fp16 -1024 in both halves
+constexpr uint32_t HNEG1152 = 0xE480E480u; // fp16 -1152 = -(1024 + 128) in both halves
 
 __device__ __forceinline__ uint16_t lo16(uint32_t v) { return uint16_t(v & 0xFFFFu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t v) { return uint16_t(v >> 16); }
 __device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 __device__ __forceinline__ float small_int_f(uint32_t bits_or_magic) { return __uint_as_float(bits_or_magic) - 8388608.0f; }
 
-// acc += lo(codes) * xa + hi(codes) * xb with exact products (fp16 x fp16 -> fp32 FMA).
-__device__ __forceinline__ float fma2h(uint32_t codes, uint16_t xa, uint16_t xb, float acc) {
-    acc = fma_h(lo16(codes), xa, acc);
-    return fma_h(hi16(codes), xb, acc);
+// fp16 pair arithmetic on raw bits: the two halves of a + b (each rounded; exact for the small integers used here).
+__device__ __forceinline__ uint32_t hadd2_bits(uint32_t a, uint32_t b) {
+    const __half2 r = __hadd2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+    return *reinterpret_cast<const uint32_t *>(&r);
 }
-// x halves of a unit: xv[t] holds x'[2t], x'[2t+1].
-__device__ __forceinline__ uint16_t xh(const uint32_t *xv, int i) { return (i & 1) ? hi16(xv[i >> 1]) : lo16(xv[i >> 1]); }
+__device__ __forceinline__ uint32_t lop3_xor_or(uint32_t a, uint32_t b, uint32_t c) {
+    // (a ^ b) | c in one LOP3 (truth table 0xBE)
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xBE;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 
 // Two-way integer dot products: c + a.h0 * b.byte(k) + a.h1 * b.byte(k + 1), a = two signed 16-bit values, b = four
 // unsigned bytes, k = 0 (lo) or 2 (hi). Exact in int32.
@@ -62,123 +68,64 @@ __device__ __forceinline__ int32_t dp2a_hi(uint32_t a, uint32_t b, int32_t c) {
     asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
-// One Q4G32 code word (weights 8j..8j+7, weight 8j+2b in the low nibble of byte b, 8j+2b+1 in the high nibble) against
-// the unit's 16-bit activations A[0..3] = (x0, x2), (x4, x6), (x1, x3), (x5, x7) of those weights: the low nibbles
-// add u * x to lo, the high nibbles, masked in place, add 16 u * x to hi.
-__device__ __forceinline__ void nib_dp(uint32_t c, const uint32_t *A, int32_t &lo, int32_t &hi) {
-    const uint32_t l = c & 0x0F0F0F0Fu, h = c & 0xF0F0F0F0u;
-    lo = dp2a_lo(A[0], l, lo);
-    lo = dp2a_hi(A[1], l, lo);
-    hi = dp2a_lo(A[2], h, hi);
-    hi = dp2a_hi(A[3], h, hi);
-}
 
 // ------------------------------------------------------------------------------------------------------------
-// Unpack + multiply helpers. Two accumulators (a, b) only for instruction-level parallelism.
+// Integer decode. A unit-row (32 weights of one row) is unpacked into eight 32-bit code words (DRow::v) whose bytes
+// each hold one code, possibly shifted left inside its byte by a "bit class" p (the byte is u * 2^p). Staged word
+// a = 2w + h holds the two 16-bit activations that meet byte pair h (bytes 0-1 or 2-3) of code word w; dp_elem<F>
+// says which of the unit's 32 weights each one belongs to. Both bytes of a pair always share one class, so one dp2a
+// adds 2^p (u0 x0 + u1 x1) to the accumulator of class p; the classes are folded with exact integer multiply-adds
+// (sum_p 2^(P - p) acc_p = 2^P sum u x), converted once per sub-block-row and scaled.
 // ------------------------------------------------------------------------------------------------------------
-// Nibble word with HB extra high bits merged just above each nibble. X holds the high bits of weights
-// i0..i0+3 at bits HB*k (k = 0..3) and of weights i0+4..i0+7 at bits 16 + HB*k; (X << s_k) & mask lands pair
-// k's high bits right above its nibbles.
-template <int HB>
-__device__ __forceinline__ void nib_word_hi(uint32_t c, uint32_t X, const uint32_t *xv, int i0, float &a, float &b) {
-    constexpr uint32_t mlo = (HB == 1) ? 0x00100010u : 0x00300030u;
-    constexpr uint32_t mhi = (HB == 1) ? 0x01000100u : 0x03000300u;
-    constexpr int s0 = 4, s1 = (HB == 1) ? 7 : 6, s2 = (HB == 1) ? 2 : 0, s3 = (HB == 1) ? 5 : 2;
-    const uint32_t c2 = c >> 8;
-    a = fma2h(lop3_and_or(X << s0, mlo, lop3_and_or(c, 0x000F000Fu, MAGIC2)), xh(xv, i0 + 0), xh(xv, i0 + 4), a);
-    b = fma2h(lop3_and_or(X << s1, mhi, lop3_and_or(c, 0x00F000F0u, MAGIC2)), xh(xv, i0 + 1), xh(xv, i0 + 5), b);
-    a = fma2h(lop3_and_or(X << s2, mlo, lop3_and_or(c2, 0x000F000Fu, MAGIC2)), xh(xv, i0 + 2), xh(xv, i0 + 6), a);
-    b = fma2h(lop3_and_or(X << s3, mhi, lop3_and_or(c2, 0x00F000F0u, MAGIC2)), xh(xv, i0 + 3), xh(xv, i0 + 7), b);
-}
-// 16 two-bit codes, weight 4b + k at bits 8b + 2k (weights i0 + ...). Bit class p = 2k.
-__device__ __forceinline__ void crumb_word(uint32_t c, const uint32_t *xv, int i0, float &a, float &b) {
-    const uint32_t c2 = c >> 8;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t m = (3u << (2 * k)) * 0x00010001u;
-        a = fma2h(lop3_and_or(c, m, MAGIC2), xh(xv, i0 + k), xh(xv, i0 + 8 + k), a);
-        b = fma2h(lop3_and_or(c2, m, MAGIC2), xh(xv, i0 + 4 + k), xh(xv, i0 + 12 + k), b);
-    }
-}
-// Two 3-byte code groups (weights 8g..8g+7 and 8g+8..8g+15 of a unit, bytes b0 b1 b2 | b3 b4 b5) spread by three
-// byte permutes: W0 = (b0 b1 | b3 b4), W1 = (b1 b2 | b4 b5), W2 = (b2 b2 | b5 b5). Code t of the first group then
-// sits in the low half and code t of the second group in the high half, both at bit p = 3t mod 8 (t = 0..7 ->
-// p = 0, 3, 6, 1, 4, 7, 2, 5), so one LOP3 per pair yields 1024 + u*2^p in both halves. xv word w0 + t holds the
-// two matching staged activations.
-__device__ __forceinline__ void tri_pair(uint32_t W0, uint32_t W1, uint32_t W2, const uint32_t *xv, int w0, float &acc) {
-    acc = fma2h(lop3_and_or(W0, 0x00070007u, MAGIC2), lo16(xv[w0 + 0]), hi16(xv[w0 + 0]), acc);
-    acc = fma2h(lop3_and_or(W0, 0x00380038u, MAGIC2), lo16(xv[w0 + 1]), hi16(xv[w0 + 1]), acc);
-    acc = fma2h(lop3_and_or(W0, 0x01C001C0u, MAGIC2), lo16(xv[w0 + 2]), hi16(xv[w0 + 2]), acc);
-    acc = fma2h(lop3_and_or(W1, 0x000E000Eu, MAGIC2), lo16(xv[w0 + 3]), hi16(xv[w0 + 3]), acc);
-    acc = fma2h(lop3_and_or(W1, 0x00700070u, MAGIC2), lo16(xv[w0 + 4]), hi16(xv[w0 + 4]), acc);
-    acc = fma2h(lop3_and_or(W1, 0x03800380u, MAGIC2), lo16(xv[w0 + 5]), hi16(xv[w0 + 5]), acc);
-    acc = fma2h(lop3_and_or(W2, 0x001C001Cu, MAGIC2), lo16(xv[w0 + 6]), hi16(xv[w0 + 6]), acc);
-    acc = fma2h(lop3_and_or(W2, 0x00E000E0u, MAGIC2), lo16(xv[w0 + 7]), hi16(xv[w0 + 7]), acc);
-}
-
-// 2^e for a small integer e, exactly (e is a compile-time constant where it is used).
-__host__ __device__ constexpr float pow2f(int e) { return e >= 0 ? float(1u << e) : 1.0f / float(1u << (-e)); }
-
-// Bit-class shift p of staging slot i (0..31) of a unit: the activation in that slot is staged as x * 2^(E - p),
-// E being the vector's scale exponent. Slot i is half (i & 1) of staged word i >> 1. For every format but Q3S slot i
-// holds element i; for Q3S word 8*pi + t holds elements 16*pi + t and 16*pi + 8 + t (see tri_pair).
 template <int F>
-__host__ __device__ constexpr int xshift(int i) {
-    if constexpr (F == FMT_Q2S) return 2 * (i & 3);
-    else if constexpr (F == FMT_Q3S) return (3 * ((i >> 1) & 7)) & 7;
-    else return (i & 1) ? 4 : 0;
-}
-// Element (0..15, within a half-unit) staged in half h of word k (0..7) of that half-unit.
-template <int F>
-__host__ __device__ constexpr int slot_elem(int k, int h) {
-    if constexpr (F == FMT_Q3S) return 8 * h + k;
-    else return 2 * k + h;
-}
-
-// Activation constants per unit (XC<F>::n floats), from the staged x' (see the file comment).
-template <int F> struct XC;
-template <> struct XC<FMT_Q4G32> { static constexpr int n = 2; };   // C (int bits), 2^-(E+4)
-template <> struct XC<FMT_Q2S> { static constexpr int n = 4; };     // C0, S0, C1, S1 (two sub-blocks)
-template <> struct XC<FMT_Q3S> { static constexpr int n = 2; };     // C0, C1
-template <> struct XC<FMT_Q5S> { static constexpr int n = 2; };     // C, S
-template <> struct XC<FMT_Q6S> { static constexpr int n = 2; };     // C0, C1
-
-template <int F>
-__device__ __forceinline__ void unit_consts(const float xp[32], const float xt[32], float *out) {
-    // xp = staged x' (as fp32), xt = 2^p * x' (the activation the integer code effectively multiplies)
-    float sp[2] = {0.f, 0.f}, st[2] = {0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 32; ++i) { sp[i >> 4] += xp[i]; st[i >> 4] += xt[i]; }
-    static_assert(F != FMT_Q4G32, "Q4G32 activations are staged as 16-bit integers (stage_unit_i16)");
-    if constexpr (F == FMT_Q2S) {
-        out[0] = 1024.0f * sp[0]; out[1] = st[0];
-        out[2] = 1024.0f * sp[1]; out[3] = st[1];
+__host__ __device__ constexpr int dp_elem(int a, int e) {
+    const int w = a >> 1, h = a & 1;
+    if constexpr (F == FMT_Q4G32 || F == FMT_Q5S) {
+        // word 2j + p: byte b holds weight 8j + 2b + p (p = 0: the low nibbles of code word j, p = 1: the high ones)
+        return 8 * (w >> 1) + (w & 1) + 4 * h + 2 * e;
     } else if constexpr (F == FMT_Q3S) {
-        out[0] = 1024.0f * sp[0] + 4.0f * st[0];
-        out[1] = 1024.0f * sp[1] + 4.0f * st[1];
-    } else if constexpr (F == FMT_Q5S) {
-        out[0] = 1024.0f * (sp[0] + sp[1]);
-        out[1] = st[0] + st[1];
+        // sub-block s = w / 4 (3-byte groups g = 2s, 2s + 1, codes c_t, c'_t = weights 16s + t, 16s + 8 + t):
+        // word 0 = (c0 c'0 | c6 c'6), 1 = (c1 c'1 | c7 c'7), 2 = (c3 c'3 | c4 c'4), 3 = (c2 c5 | c'2 c'5)
+        const int k = w & 3, t = 4 * k + 2 * h + e;
+        const int tab = (t == 0) ? 0 : (t == 1) ? 8 : (t == 2) ? 6 : (t == 3) ? 14 : (t == 4) ? 1 : (t == 5) ? 9
+                      : (t == 6) ? 7 : (t == 7) ? 15 : (t == 8) ? 3 : (t == 9) ? 11 : (t == 10) ? 4 : (t == 11) ? 12
+                      : (t == 12) ? 2 : (t == 13) ? 5 : (t == 14) ? 10 : 13;
+        return 16 * (w >> 2) + tab;
     } else {
-        out[0] = 1024.0f * sp[0] + 32.0f * st[0];
-        out[1] = 1024.0f * sp[1] + 32.0f * st[1];
+        // Q2S, Q6S: word 4s + k: byte b holds weight 16s + 4b + k
+        return 16 * (w >> 2) + (w & 3) + 8 * h + 4 * e;
     }
 }
 
+// Activation constants per unit (XC<F>::n floats; "int" = int32 bits): E is the unit's exponent, XS = 2^-E,
+// Sx_j = the sum of the staged activations of sub-block j.
+template <int F> struct XC;
+template <> struct XC<FMT_Q4G32> { static constexpr int n = 2; };   // int -128 Sx, XS / 16
+template <> struct XC<FMT_Q2S> { static constexpr int n = 3; };     // Sx_0 XS, Sx_1 XS, XS
+template <> struct XC<FMT_Q3S> { static constexpr int n = 3; };     // int -128 Sx_0, int -128 Sx_1, XS / 32
+template <> struct XC<FMT_Q5S> { static constexpr int n = 2; };     // Sx XS, XS
+template <> struct XC<FMT_Q6S> { static constexpr int n = 3; };     // int -128 Sx_0, int -128 Sx_1, XS / 4
+
+struct DRow {
+    uint32_t v[8];   // code words (see dp_elem)
+    float f0, f1;    // sub-block scale factors D * L_j (Q4G32: the group scale; Q5S: f0 only)
+    float g0, g1;    // minima factors Dm * M_j of the asymmetric formats
+};
+
 // ------------------------------------------------------------------------------------------------------------
-// Per-lane geometry of one unit position (uc) within a 4096-weight chunk: byte offsets relative to the unit's
-// aligned code base, so that both rows of a lane use immediate offsets.
+// Per-lane geometry of one unit position (uc) within a K chunk: byte offsets relative to the unit's aligned code
+// base, so that every row of a lane uses immediate offsets.
 // ------------------------------------------------------------------------------------------------------------
 struct LaneGeo {
     uint32_t ubase;      // aligned byte offset of the unit's codes within a row chunk
     int32_t o1, o2, o3;  // format-specific byte offsets relative to ubase
     uint32_t sh0, sh1;   // format-specific shifts
-    uint32_t p0, p1, p2, q0, q1, q2;   // Q3S byte-permute selectors of the two group pairs
+    uint32_t p[4], q[4]; // Q3S byte-permute selectors of the two sub-blocks (words P, Q, R, S)
 };
 
 template <int F>
 __device__ __forceinline__ LaneGeo lane_geo(int uc) {
-    LaneGeo g = {0u, 0, 0, 0, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    LaneGeo g = {};
     const uint32_t sbk = uint32_t(uc) >> 3, su = uint32_t(uc) & 7u;
     if constexpr (F == FMT_Q4G32) {
         g.ubase = 16u * uc;
@@ -190,17 +137,18 @@ __device__ __forceinline__ LaneGeo lane_geo(int uc) {
         const uint32_t a = 110u * sbk + 12u * su;             // code start, 2-byte aligned
         const uint32_t o = a & 3u;                            // 0 or 2
         g.ubase = a - o;
-        g.o1 = int32_t(4u + 2u * o);                          // word pair holding the second group pair's 6 bytes
+        g.o1 = int32_t(4u + 2u * o);                          // word pair holding the second sub-block's 6 bytes
         const uint32_t fa = 110u * sbk + 96u + 3u * (su >> 1);
         uint32_t fw = fa & ~3u, fs = 8u * (fa & 3u) + 6u * ((2u * su) & 3u);
         if (fs >= 32u) { fw += 4u; fs -= 32u; }
         g.o2 = int32_t(fw) - int32_t(g.ubase);                // word pair holding L_j0, L_j0+1 at bits fs..
         g.sh1 = fs;
         g.o3 = int32_t(110u * sbk + 108u) - int32_t(g.ubase); // d
-        // the first group pair starts at byte o of (w0, w1), the second at byte 2 - o of its word pair
-        const uint32_t s0 = o * 0x1111u, s1 = (2u - o) * 0x1111u;
-        g.p0 = 0x4310u + s0; g.p1 = 0x5421u + s0; g.p2 = 0x5522u + s0;
-        g.q0 = 0x4310u + s1; g.q1 = 0x5421u + s1; g.q2 = 0x5522u + s1;
+        // bytes b0..b5 of a sub-block start at byte o (first) or 2 - o (second) of their word pair:
+        // P = (b0 b3 b2 b5), Q = (b1 b4 b1 b4), R = (b0 b1 b3 b4), S = (b1 b2 b4 b5)
+        const uint32_t base[4] = {0x5230u, 0x4141u, 0x4310u, 0x5421u};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { g.p[i] = base[i] + o * 0x1111u; g.q[i] = base[i] + (2u - o) * 0x1111u; }
     } else if constexpr (F == FMT_Q5S) {
         g.ubase = 176u * sbk + 16u * su;
         g.o1 = int32_t(128u + 4u * su) - int32_t(16u * su);   // high-bit plane word
@@ -218,163 +166,40 @@ __device__ __forceinline__ LaneGeo lane_geo(int uc) {
     return g;
 }
 
-// fp16 pair arithmetic on raw bits: the two halves of a + b (each rounded; exact for the small integers used here).
-__device__ __forceinline__ uint32_t hadd2_bits(uint32_t a, uint32_t b) {
-    const __half2 r = __hadd2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
-    return *reinterpret_cast<const uint32_t *>(&r);
+// Q3S sub-block of two 3-byte groups (b0 b1 b2 | b3 b4 b5, code t of a group at bits 3t of its 24-bit value) from its
+// word pair and the four selectors: P & 0x1C1C0707 = (c0 c'0 at bit 0 | c6 c'6 at bit 2), P & 0xE0E03838 = (c1 c'1 at
+// bit 3 | c7 c'7 at bit 5), Q & 0x70700E0E = (c3 c'3 at bit 1 | c4 c'4 at bit 4); the codes c2 (bits 6..8) and c5
+// (bits 15..17) straddle bytes and are shifted down from the 16-bit windows R = (b1b0 | b4b3), S = (b2b1 | b5b4).
+__device__ __forceinline__ void unpack_tri_dp(uint32_t wa, uint32_t wb, const uint32_t *sel, uint32_t *v) {
+    const uint32_t P = __byte_perm(wa, wb, sel[0]), Q = __byte_perm(wa, wb, sel[1]);
+    const uint32_t R = __byte_perm(wa, wb, sel[2]), S = __byte_perm(wa, wb, sel[3]);
+    v[0] = P & 0x1C1C0707u;
+    v[1] = P & 0xE0E03838u;
+    v[2] = Q & 0x70700E0Eu;
+    v[3] = ((R >> 6) & 0x00070007u) | ((S << 1) & 0x07000700u);
 }
-__device__ __forceinline__ uint32_t lop3_xor_or(uint32_t a, uint32_t b, uint32_t c) {
-    // (a ^ b) | c in one LOP3 (truth table 0xBE)
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xBE;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-constexpr uint32_t HNEG1024 = 0xE400E400u;   // fp16 -1024 in both halves
-constexpr uint32_t HNEG1152 = 0xE480E480u;   // fp16 -1152 = -(1024 + 128) in both halves
-
-// acc += sum_i w'_i x_i over one 32-weight unit of one row when `on`, else acc is left unchanged; `u` = aligned unit
-// base in shared memory, `sp` = this row's group-scale pointer (Q4G32), `c` = the unit's activation constants,
-// `xv` = its staged activations. Each sub-block accumulator starts at -C (the activation constant), so no separate
-// subtraction is needed. Sub-block scale integers are turned into exact fp16 values with the 1024 mantissa trick and
-// multiplied by the raw fp16 super-block scale with exact fp16 x fp16 -> fp32 products; masking zeroes that scale.
-template <int F>
-__device__ __forceinline__ void row_acc(const uint8_t *u, const float *sp, const LaneGeo &g, const float *c,
-                                        const uint32_t *xv, bool on, float &acc) {
-    if constexpr (F == FMT_Q4G32) {
-        // 16 * sum (u - 8) x_i in int32 (exact), then one conversion and the group scale times 2^-(E+4)
-        const uint4 w = *reinterpret_cast<const uint4 *>(u);
-        const float s = on ? sp[0] : 0.f;
-        int32_t lo = 0, hi = __float_as_int(c[0]);
-        nib_dp(w.x, xv + 0, lo, hi);
-        nib_dp(w.y, xv + 4, lo, hi);
-        nib_dp(w.z, xv + 8, lo, hi);
-        nib_dp(w.w, xv + 12, lo, hi);
-        acc = fmaf(float(16 * lo + hi), s * c[1], acc);
-    } else if constexpr (F == FMT_Q2S) {
-        const uint32_t w0 = lds32(u), w1 = lds32(u + 4);
-        const uint32_t dd = on ? lds32(u + g.o2) : 0u;                   // d (low half), dmin (high half)
-        const uint32_t lm = *reinterpret_cast<const uint16_t *>(u + g.o1);
-        const uint32_t t = __byte_perm(lm, 0u, 0x4140u);                 // L0 | M0 << 4 at byte 0, L1 | M1 << 4 at byte 2
-        const uint32_t hl = hadd2_bits(lop3_and_or(t, 0x000F000Fu, MAGIC2), HNEG1024);        // (L0, L1)
-        const uint32_t hm = hadd2_bits(lop3_and_or(t >> 4, 0x000F000Fu, MAGIC2), HNEG1024);   // (M0, M1)
-        float a0 = -c[0], b0 = 0.f, a1 = -c[2], b1 = 0.f;
-        crumb_word(w0, xv, 0, a0, b0);
-        crumb_word(w1, xv, 16, a1, b1);
-        acc = fmaf(fma_h(lo16(hl), lo16(dd), 0.f), a0 + b0, acc);
-        acc = fmaf(fma_h(hi16(hl), lo16(dd), 0.f), a1 + b1, acc);
-        acc = fmaf(-fma_h(lo16(hm), hi16(dd), 0.f), c[1], acc);
-        acc = fmaf(-fma_h(hi16(hm), hi16(dd), 0.f), c[3], acc);
-    } else if constexpr (F == FMT_Q3S) {
-        const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
-        const uint32_t w0 = wp[0], w1 = wp[1];
-        const uint32_t *qp = reinterpret_cast<const uint32_t *>(u + g.o1);
-        const uint32_t w2 = qp[0], w3 = qp[1];
-        const uint32_t *fp = reinterpret_cast<const uint32_t *>(u + g.o2);
-        const uint32_t f = __funnelshift_r(fp[0], fp[1], g.sh1);          // L_j0 at bits 0..5, L_j0+1 at bits 6..11
-        const uint32_t lh = hadd2_bits(lop3_and_or(lop3_sel(f << 10, f, 0xFFFF0000u), 0x003F003Fu, MAGIC2), HNEG1024);
-        const uint16_t D = on ? *reinterpret_cast<const uint16_t *>(u + g.o3) : uint16_t(0);
-        float a0 = -c[0], a1 = -c[1];
-        tri_pair(__byte_perm(w0, w1, g.p0), __byte_perm(w0, w1, g.p1), __byte_perm(w0, w1, g.p2), xv, 0, a0);
-        tri_pair(__byte_perm(w2, w3, g.q0), __byte_perm(w2, w3, g.q1), __byte_perm(w2, w3, g.q2), xv, 8, a1);
-        acc = fmaf(fma_h(lo16(lh), D, 0.f), a0, acc);
-        acc = fmaf(fma_h(hi16(lh), D, 0.f), a1, acc);
-    } else if constexpr (F == FMT_Q5S) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(u);
-        const uint32_t H = lds32(u + g.o1);
-        const uint4 fld = *reinterpret_cast<const uint4 *>(u + g.o2);
-        const uint32_t ddw = on ? fld.w : 0u;
-        const float2 Dd = __half22float2(*reinterpret_cast<const __half2 *>(&ddw));
-        const uint64_t lo64 = (uint64_t(fld.y) << 32) | fld.x, hi64 = (uint64_t(fld.z) << 32) | fld.y;
-        const float L = small_int_f(lop3_and_or(uint32_t(lo64 >> g.sh0), 63u, MAGICF));
-        const float M = small_int_f(lop3_and_or(uint32_t(hi64 >> (g.sh1 - 32u)), 63u, MAGICF));
-        float a = -c[0], b = 0.f;
-        nib_word_hi<1>(w.x, lop3_sel(H, H << 12, 0x0000FFFFu), xv, 0, a, b);
-        nib_word_hi<1>(w.y, lop3_sel(H >> 8, H << 4, 0x0000FFFFu), xv, 8, a, b);
-        nib_word_hi<1>(w.z, lop3_sel(H >> 16, H >> 4, 0x0000FFFFu), xv, 16, a, b);
-        nib_word_hi<1>(w.w, lop3_sel(H >> 24, H >> 12, 0x0000FFFFu), xv, 24, a, b);
-        acc = fmaf(Dd.x * L, a + b, acc);
-        acc = fmaf(-(Dd.y * M), c[1], acc);
-    } else {
-        const uint32_t sh = g.sh0;
-        const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
-        const uint32_t r0 = wp[0], r1 = wp[1], r2 = wp[2], r3 = wp[3], r4 = wp[4];
-        const uint32_t *hp = reinterpret_cast<const uint32_t *>(u + g.o1);
-        const uint32_t q0 = hp[0], q1 = hp[1], q2 = hp[2];
-        const uint32_t h0 = __funnelshift_r(q0, q1, sh), h1 = __funnelshift_r(q1, q2, sh);
-        const uint32_t lv = *reinterpret_cast<const uint16_t *>(u + g.o2);
-        // int8 pair -> exact fp16 pair: (b ^ 0x80) in the mantissa of 1024, minus 1024 + 128
-        const uint32_t lh = hadd2_bits(lop3_xor_or(__byte_perm(lv, 0u, 0x4140u), 0x00800080u, MAGIC2), HNEG1152);
-        const uint16_t D = on ? *reinterpret_cast<const uint16_t *>(u + g.o3) : uint16_t(0);
-        float a0 = -c[0], b0 = 0.f, a1 = -c[1], b1 = 0.f;
-        nib_word_hi<2>(__funnelshift_r(r0, r1, sh), __byte_perm(h0, 0u, 0x4140u), xv, 0, a0, b0);
-        nib_word_hi<2>(__funnelshift_r(r1, r2, sh), __byte_perm(h0, 0u, 0x4342u), xv, 8, a0, b0);
-        nib_word_hi<2>(__funnelshift_r(r2, r3, sh), __byte_perm(h1, 0u, 0x4140u), xv, 16, a1, b1);
-        nib_word_hi<2>(__funnelshift_r(r3, r4, sh), __byte_perm(h1, 0u, 0x4342u), xv, 24, a1, b1);
-        acc = fmaf(fma_h(lo16(lh), D, 0.f), a0 + b0, acc);
-        acc = fmaf(fma_h(hi16(lh), D, 0.f), a1 + b1, acc);
-    }
+// Q6S sub-block: low-4 plane words A (weights 0..7) and B (8..15), high-2 plane word H (weight 4b + k at bits 2k of
+// byte b). Words k = 0..3 hold weight 4b + k in byte b: k even at bit 0 (nibble | high bits << 4), k odd at bit 2.
+__device__ __forceinline__ void unpack_six_dp(uint32_t A, uint32_t B, uint32_t H, uint32_t *v) {
+    const uint32_t P0 = __byte_perm(A, B, 0x6420u), P1 = __byte_perm(A, B, 0x7531u), Hs = H << 4;
+    v[0] = (P0 & 0x0F0F0F0Fu) | (Hs & 0x30303030u);
+    v[1] = ((P0 >> 2) & 0x3C3C3C3Cu) | (Hs & 0xC0C0C0C0u);
+    v[2] = (P1 & 0x0F0F0F0Fu) | (H & 0x30303030u);
+    v[3] = ((P1 >> 2) & 0x3C3C3C3Cu) | (H & 0xC0C0C0C0u);
 }
 
-// ------------------------------------------------------------------------------------------------------------
-// Multi-row form of the same math (small-batch products): a unit-row is unpacked once into 16 words of fp16 code
-// pairs (the LOP3 outputs of row_acc, in the same order) plus its sub-block scale factors, then multiplied against
-// several staged activation rows. hw[j] holds the codes of staging slots hslot<F>(j, 0) (low half) and
-// hslot<F>(j, 1) (high half); words 0..7 belong to sub-block 0 and 8..15 to sub-block 1 (formats with one 32-weight
-// sub-block use the same split for two independent accumulators).
-// ------------------------------------------------------------------------------------------------------------
+// Unpack one unit-row: `u` = aligned unit base in shared memory, `sp` = this row's group-scale pointer (Q4G32);
+// `on` false zeroes its scale factors (a masked lane or row). Sub-block scale integers become exact fp16 values with
+// the 1024 mantissa trick and are multiplied by the raw fp16 super-block scale with exact fp16 x fp16 -> fp32 products.
 template <int F>
-__host__ __device__ constexpr int hslot(int j, int h) {
-    if constexpr (F == FMT_Q3S) return 2 * j + h;
-    else if constexpr (F == FMT_Q2S) return 16 * (j / 8) + 4 * (j % 2) + (j % 8) / 2 + 8 * h;
-    else return 8 * (j / 4) + j % 4 + 4 * h;
-}
-struct URow {
-    uint32_t hw[16];
-    float f0, f1;   // sub-block scale factors (w' = f * code for the symmetric part)
-    float g0, g1;   // minima factors of the asymmetric formats (dmin * M_j), else 0
-};
-template <int HB>
-__device__ __forceinline__ void unpack_nib_hi(uint32_t c, uint32_t X, uint32_t *hw) {
-    constexpr uint32_t mlo = (HB == 1) ? 0x00100010u : 0x00300030u;
-    constexpr uint32_t mhi = (HB == 1) ? 0x01000100u : 0x03000300u;
-    constexpr int s0 = 4, s1 = (HB == 1) ? 7 : 6, s2 = (HB == 1) ? 2 : 0, s3 = (HB == 1) ? 5 : 2;
-    const uint32_t c2 = c >> 8;
-    hw[0] = lop3_and_or(X << s0, mlo, lop3_and_or(c, 0x000F000Fu, MAGIC2));
-    hw[1] = lop3_and_or(X << s1, mhi, lop3_and_or(c, 0x00F000F0u, MAGIC2));
-    hw[2] = lop3_and_or(X << s2, mlo, lop3_and_or(c2, 0x000F000Fu, MAGIC2));
-    hw[3] = lop3_and_or(X << s3, mhi, lop3_and_or(c2, 0x00F000F0u, MAGIC2));
-}
-__device__ __forceinline__ void unpack_crumb(uint32_t c, uint32_t *hw) {
-    const uint32_t c2 = c >> 8;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t m = (3u << (2 * k)) * 0x00010001u;
-        hw[2 * k] = lop3_and_or(c, m, MAGIC2);
-        hw[2 * k + 1] = lop3_and_or(c2, m, MAGIC2);
-    }
-}
-__device__ __forceinline__ void unpack_tri(uint32_t W0, uint32_t W1, uint32_t W2, uint32_t *hw) {
-    hw[0] = lop3_and_or(W0, 0x00070007u, MAGIC2);
-    hw[1] = lop3_and_or(W0, 0x00380038u, MAGIC2);
-    hw[2] = lop3_and_or(W0, 0x01C001C0u, MAGIC2);
-    hw[3] = lop3_and_or(W1, 0x000E000Eu, MAGIC2);
-    hw[4] = lop3_and_or(W1, 0x00700070u, MAGIC2);
-    hw[5] = lop3_and_or(W1, 0x03800380u, MAGIC2);
-    hw[6] = lop3_and_or(W2, 0x001C001Cu, MAGIC2);
-    hw[7] = lop3_and_or(W2, 0x00E000E0u, MAGIC2);
-}
-
-// Unpack one unit-row (same operands as row_acc); `on` false zeroes its scale factors.
-template <int F>
-__device__ __forceinline__ void unpack_row(const uint8_t *u, const float *sp, const LaneGeo &g, bool on, URow &r) {
-    r.g0 = r.g1 = 0.f;
+__device__ __forceinline__ void unpack_dp(const uint8_t *u, const float *sp, const LaneGeo &g, bool on, DRow &r) {
+    r.f1 = r.g0 = r.g1 = 0.f;
     if constexpr (F == FMT_Q4G32) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
-        r.f0 = r.f1 = on ? sp[0] : 0.f;
-        // the dp2a operands: hw[2j] = low nibbles of word j in place, hw[2j + 1] = its high nibbles in place
+        r.f0 = on ? sp[0] : 0.f;
         const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) { r.hw[2 * j] = wv[j] & 0x0F0F0F0Fu; r.hw[2 * j + 1] = wv[j] & 0xF0F0F0F0u; }
+        for (int j = 0; j < 4; ++j) { r.v[2 * j] = wv[j] & 0x0F0F0F0Fu; r.v[2 * j + 1] = wv[j] & 0xF0F0F0F0u; }
     } else if constexpr (F == FMT_Q2S) {
         const uint32_t w0 = lds32(u), w1 = lds32(u + 4);
         const uint32_t dd = on ? lds32(u + g.o2) : 0u;
@@ -386,108 +211,144 @@ __device__ __forceinline__ void unpack_row(const uint8_t *u, const float *sp, co
         r.f1 = fma_h(hi16(hl), lo16(dd), 0.f);
         r.g0 = fma_h(lo16(hm), hi16(dd), 0.f);
         r.g1 = fma_h(hi16(hm), hi16(dd), 0.f);
-        unpack_crumb(w0, r.hw); unpack_crumb(w1, r.hw + 8);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            r.v[k] = (w0 >> (2 * k)) & 0x03030303u;
+            r.v[4 + k] = (w1 >> (2 * k)) & 0x03030303u;
+        }
     } else if constexpr (F == FMT_Q3S) {
         const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
-        const uint32_t w0 = wp[0], w1 = wp[1];
         const uint32_t *qp = reinterpret_cast<const uint32_t *>(u + g.o1);
-        const uint32_t w2 = qp[0], w3 = qp[1];
         const uint32_t *fp = reinterpret_cast<const uint32_t *>(u + g.o2);
-        const uint32_t f = __funnelshift_r(fp[0], fp[1], g.sh1);
+        const uint32_t f = __funnelshift_r(fp[0], fp[1], g.sh1);          // L_j0 at bits 0..5, L_j0+1 at bits 6..11
         const uint32_t lh = hadd2_bits(lop3_and_or(lop3_sel(f << 10, f, 0xFFFF0000u), 0x003F003Fu, MAGIC2), HNEG1024);
         const uint16_t D = on ? *reinterpret_cast<const uint16_t *>(u + g.o3) : uint16_t(0);
         r.f0 = fma_h(lo16(lh), D, 0.f);
         r.f1 = fma_h(hi16(lh), D, 0.f);
-        unpack_tri(__byte_perm(w0, w1, g.p0), __byte_perm(w0, w1, g.p1), __byte_perm(w0, w1, g.p2), r.hw);
-        unpack_tri(__byte_perm(w2, w3, g.q0), __byte_perm(w2, w3, g.q1), __byte_perm(w2, w3, g.q2), r.hw + 8);
+        unpack_tri_dp(wp[0], wp[1], g.p, r.v);
+        unpack_tri_dp(qp[0], qp[1], g.q, r.v + 4);
     } else if constexpr (F == FMT_Q5S) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
-        const uint32_t H = lds32(u + g.o1);
+        const uint32_t H = lds32(u + g.o1);                               // bit i = bit 4 of code i
         const uint4 fld = *reinterpret_cast<const uint4 *>(u + g.o2);
         const uint32_t ddw = on ? fld.w : 0u;
         const float2 Dd = __half22float2(*reinterpret_cast<const __half2 *>(&ddw));
         const uint64_t lo64 = (uint64_t(fld.y) << 32) | fld.x, hi64 = (uint64_t(fld.z) << 32) | fld.y;
         const float L = small_int_f(lop3_and_or(uint32_t(lo64 >> g.sh0), 63u, MAGICF));
         const float Mv = small_int_f(lop3_and_or(uint32_t(hi64 >> (g.sh1 - 32u)), 63u, MAGICF));
-        r.f0 = r.f1 = Dd.x * L;
+        r.f0 = Dd.x * L;
         r.g0 = Dd.y * Mv;
-        unpack_nib_hi<1>(w.x, lop3_sel(H, H << 12, 0x0000FFFFu), r.hw);
-        unpack_nib_hi<1>(w.y, lop3_sel(H >> 8, H << 4, 0x0000FFFFu), r.hw + 4);
-        unpack_nib_hi<1>(w.z, lop3_sel(H >> 16, H >> 4, 0x0000FFFFu), r.hw + 8);
-        unpack_nib_hi<1>(w.w, lop3_sel(H >> 24, H >> 12, 0x0000FFFFu), r.hw + 12);
+        // word 2j (2j + 1): the even (odd) weights' nibbles of code word j, each byte's fifth bit spread from bits
+        // 0, 2, 4, 6 (1, 3, 5, 7) of the high-plane byte j by one multiply: bit 2m (+1) lands on bit 8m + 4, and the
+        // cross terms on bits outside 0x10101010
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t hj = H >> (8 * j);
+            r.v[2 * j] = (wv[j] & 0x0F0F0F0Fu) | (((hj & 0x55u) * 0x00410410u) & 0x10101010u);
+            r.v[2 * j + 1] = ((wv[j] >> 4) & 0x0F0F0F0Fu) | (((hj & 0xAAu) * 0x00208208u) & 0x10101010u);
+        }
     } else {
         const uint32_t sh = g.sh0;
         const uint32_t *wp = reinterpret_cast<const uint32_t *>(u);
         const uint32_t r0 = wp[0], r1 = wp[1], r2 = wp[2], r3 = wp[3], r4 = wp[4];
         const uint32_t *hp = reinterpret_cast<const uint32_t *>(u + g.o1);
         const uint32_t q0 = hp[0], q1 = hp[1], q2 = hp[2];
-        const uint32_t h0 = __funnelshift_r(q0, q1, sh), h1 = __funnelshift_r(q1, q2, sh);
         const uint32_t lv = *reinterpret_cast<const uint16_t *>(u + g.o2);
+        // int8 pair -> exact fp16 pair: (b ^ 0x80) in the mantissa of 1024, minus 1024 + 128
         const uint32_t lh = hadd2_bits(lop3_xor_or(__byte_perm(lv, 0u, 0x4140u), 0x00800080u, MAGIC2), HNEG1152);
         const uint16_t D = on ? *reinterpret_cast<const uint16_t *>(u + g.o3) : uint16_t(0);
         r.f0 = fma_h(lo16(lh), D, 0.f);
         r.f1 = fma_h(hi16(lh), D, 0.f);
-        unpack_nib_hi<2>(__funnelshift_r(r0, r1, sh), __byte_perm(h0, 0u, 0x4140u), r.hw);
-        unpack_nib_hi<2>(__funnelshift_r(r1, r2, sh), __byte_perm(h0, 0u, 0x4342u), r.hw + 4);
-        unpack_nib_hi<2>(__funnelshift_r(r2, r3, sh), __byte_perm(h1, 0u, 0x4140u), r.hw + 8);
-        unpack_nib_hi<2>(__funnelshift_r(r3, r4, sh), __byte_perm(h1, 0u, 0x4342u), r.hw + 12);
+        unpack_six_dp(__funnelshift_r(r0, r1, sh), __funnelshift_r(r1, r2, sh), __funnelshift_r(q0, q1, sh), r.v);
+        unpack_six_dp(__funnelshift_r(r2, r3, sh), __funnelshift_r(r3, r4, sh), __funnelshift_r(q1, q2, sh), r.v + 4);
     }
 }
 
-// acc += sum_i w'_i x_i of an unpacked unit-row against one staged activation row (xv, c: that row's unit constants).
+// acc += sum_i w'_i x_i of an unpacked unit-row against one staged activation row (xv: its 16 staged words, c: its
+// unit constants).
 template <int F>
-__device__ __forceinline__ void dot_row(const URow &r, const uint32_t *xv, const float *c, float &acc) {
+__device__ __forceinline__ void dot_dp(const DRow &r, const uint32_t *xv, const float *c, float &acc) {
     if constexpr (F == FMT_Q4G32) {
+        // lo: even weights at class 0; hi: odd weights at class 4, starting at -128 Sx (the code offset 8) -> 16 sum q x
         int32_t lo = 0, hi = __float_as_int(c[0]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            lo = dp2a_lo(xv[4 * j], r.hw[2 * j], lo);
-            lo = dp2a_hi(xv[4 * j + 1], r.hw[2 * j], lo);
-            hi = dp2a_lo(xv[4 * j + 2], r.hw[2 * j + 1], hi);
-            hi = dp2a_hi(xv[4 * j + 3], r.hw[2 * j + 1], hi);
+            lo = dp2a_lo(xv[4 * j], r.v[2 * j], lo);
+            lo = dp2a_hi(xv[4 * j + 1], r.v[2 * j], lo);
+            hi = dp2a_lo(xv[4 * j + 2], r.v[2 * j + 1], hi);
+            hi = dp2a_hi(xv[4 * j + 3], r.v[2 * j + 1], hi);
         }
         acc = fmaf(float(16 * lo + hi), r.f0 * c[1], acc);
-        return;
-    }
-    float a0, a1;
-    if constexpr (F == FMT_Q5S) { a0 = -c[0]; a1 = 0.f; }
-    else if constexpr (F == FMT_Q2S) { a0 = -c[0]; a1 = -c[2]; }
-    else { a0 = -c[0]; a1 = -c[1]; }
+    } else if constexpr (F == FMT_Q5S) {
+        int32_t a = 0, b = 0;                                   // two chains, every byte at class 0
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        a0 = fma_h(lo16(r.hw[j]), xh(xv, hslot<F>(j, 0)), a0);
-        a0 = fma_h(hi16(r.hw[j]), xh(xv, hslot<F>(j, 1)), a0);
-        a1 = fma_h(lo16(r.hw[8 + j]), xh(xv, hslot<F>(8 + j, 0)), a1);
-        a1 = fma_h(hi16(r.hw[8 + j]), xh(xv, hslot<F>(8 + j, 1)), a1);
-    }
-    if constexpr (F == FMT_Q5S) {
-        acc = fmaf(r.f0, a0 + a1, acc);
-        acc = fmaf(-r.g0, c[1], acc);
+        for (int j = 0; j < 4; ++j) {
+            a = dp2a_lo(xv[4 * j], r.v[2 * j], a);
+            a = dp2a_hi(xv[4 * j + 1], r.v[2 * j], a);
+            b = dp2a_lo(xv[4 * j + 2], r.v[2 * j + 1], b);
+            b = dp2a_hi(xv[4 * j + 3], r.v[2 * j + 1], b);
+        }
+        acc = fmaf(float(a + b), r.f0 * c[1], acc);
+        acc = fmaf(-r.g0, c[0], acc);
+    } else if constexpr (F == FMT_Q2S) {
+        const float fs[2] = {r.f0, r.f1}, gs[2] = {r.g0, r.g1};
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            int32_t t = 0;                                      // every byte at class 0
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                t = dp2a_lo(xv[8 * s + 2 * k], r.v[4 * s + k], t);
+                t = dp2a_hi(xv[8 * s + 2 * k + 1], r.v[4 * s + k], t);
+            }
+            acc = fmaf(float(t), fs[s] * c[2], acc);
+            acc = fmaf(-gs[s], c[s], acc);
+        }
+    } else if constexpr (F == FMT_Q3S) {
+        const float fs[2] = {r.f0, r.f1};
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const uint32_t *v = r.v + 4 * s;
+            const uint32_t *x = xv + 8 * s;
+            // class accumulators a_p (p = bit class); a5 starts at -128 Sx_s (the code offset 4, times 32)
+            int32_t a0 = dp2a_lo(x[0], v[0], 0);
+            const int32_t a2 = dp2a_hi(x[1], v[0], 0);
+            const int32_t a3 = dp2a_lo(x[2], v[1], 0);
+            const int32_t a5 = dp2a_hi(x[3], v[1], __float_as_int(c[s]));
+            const int32_t a1 = dp2a_lo(x[4], v[2], 0);
+            const int32_t a4 = dp2a_hi(x[5], v[2], 0);
+            a0 = dp2a_lo(x[6], v[3], a0);
+            a0 = dp2a_hi(x[7], v[3], a0);
+            const int32_t t = ((((a0 * 2 + a1) * 2 + a2) * 2 + a3) * 2 + a4) * 2 + a5;   // 32 sum (u - 4) x
+            acc = fmaf(float(t), fs[s] * c[2], acc);
+        }
     } else {
-        acc = fmaf(r.f0, a0, acc);
-        acc = fmaf(r.f1, a1, acc);
-        if constexpr (F == FMT_Q2S) {
-            acc = fmaf(-r.g0, c[1], acc);
-            acc = fmaf(-r.g1, c[3], acc);
+        const float fs[2] = {r.f0, r.f1};
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const uint32_t *v = r.v + 4 * s;
+            const uint32_t *x = xv + 8 * s;
+            int32_t a0 = 0, a2 = __float_as_int(c[s]);           // classes 0 and 2; a2 starts at -128 Sx_s
+            a0 = dp2a_lo(x[0], v[0], a0);
+            a0 = dp2a_hi(x[1], v[0], a0);
+            a2 = dp2a_lo(x[2], v[1], a2);
+            a2 = dp2a_hi(x[3], v[1], a2);
+            a0 = dp2a_lo(x[4], v[2], a0);
+            a0 = dp2a_hi(x[5], v[2], a0);
+            a2 = dp2a_lo(x[6], v[3], a2);
+            a2 = dp2a_hi(x[7], v[3], a2);
+            acc = fmaf(float(4 * a0 + a2), fs[s] * c[2], acc);  // 4 sum (u - 32) x
         }
     }
 }
 
-// Staged activations: the 16 words of unit u are four 16-byte vectors at vector index t * U + u (t = 0..3, U = K / 32
-// units per row), so consecutive lanes (consecutive units) read consecutive vectors. Half-unit hh (elements
-// 16 hh .. 16 hh + 15) is words 8 hh .. 8 hh + 7, i.e. vectors t = 2 hh and 2 hh + 1.
+// ------------------------------------------------------------------------------------------------------------
+// Activation staging. A unit's 32 activations become 16-bit integers xi = rint(x * 2^E), E = the unit's own exponent
+// (max |x| * 2^E in [2^14, 2^15), so |xi| <= 32752: fp16 x with exponent within 4 of the unit's maximum converts
+// exactly, smaller ones round to 2^-E; an inf clamps to 32767, a nan gives 0), stored as 16 words (four 16-byte
+// vectors at vector index t * U + u, so consecutive lanes read consecutive vectors) in dp_elem order.
+// ------------------------------------------------------------------------------------------------------------
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }   // -126 <= e <= 127
-
-// Stage one half-unit: xr = its 16 raw fp16 activations in element order, E = the vector's scale exponent.
-template <int F>
-__device__ __forceinline__ void stage_half_unit(const uint16_t *xr, int E, uint32_t w[8]) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float f0 = h2f_bits(xr[slot_elem<F>(k, 0)]) * exp2i(E - xshift<F>(2 * k));
-        const float f1 = h2f_bits(xr[slot_elem<F>(k, 1)]) * exp2i(E - xshift<F>(2 * k + 1));
-        w[k] = uint32_t(f2h_bits(f0)) | (uint32_t(f2h_bits(f1)) << 16);
-    }
-}
 __device__ __forceinline__ void load_xp(const uint4 *xs, uint32_t U, uint32_t u, uint32_t xv[16]) {
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -495,67 +356,55 @@ __device__ __forceinline__ void load_xp(const uint4 *xs, uint32_t U, uint32_t u,
         xv[4 * t] = v.x; xv[4 * t + 1] = v.y; xv[4 * t + 2] = v.z; xv[4 * t + 3] = v.w;
     }
 }
-// Scale exponent of a K part from its max |x| (fp16 magnitude bits): x * 2^E has max in [2^14, 2^15); 0 for an all-zero
-// part; inf / nan inputs clamp to the largest finite magnitude.
-__device__ __forceinline__ int part_exponent(uint32_t mbits) {
+// Exponent of a unit from its max |x| (fp16 magnitude bits): 0 for an all-zero unit; inf / nan clamp to the largest
+// finite magnitude. E lies in [-1, 38].
+__device__ __forceinline__ int unit_exponent(uint32_t mbits) {
     const float xm = h2f_bits(uint16_t(min(mbits, 0x7BFFu)));
     return (xm > 0.f) ? 14 - (int((__float_as_uint(xm) >> 23) & 255u) - 127) : 0;
 }
 
-// Stage one unit: raw = its 32 fp16 activations (four 16-byte vectors), E = the part's scale exponent. Writes the
-// unit's four staged vectors (x' = fp16(x * 2^(E - p)), see stage_half_unit) and its activation constants.
-// Q4G32 staging: the unit's 32 activations as 16-bit integers xi = rint(x * 2^E), E = the unit's own exponent (max
-// |x| * 2^E in [2^14, 2^15), so |xi| <= 32752; an inf clamps to 32767, a nan gives 0), vector j holding the dp2a
-// operands of code word j (see nib_dp). Constants: -128 * sum(xi) as int bits (the code offset 8, times the 16 of
-// the high-nibble accumulator) and 2^-(E+4).
-__device__ __forceinline__ void stage_unit_i16(const uint4 (&raw)[4], uint4 *xs, float *cst, uint32_t U, uint32_t u) {
+template <int F>
+__device__ __forceinline__ void stage_unit(const uint4 (&raw)[4], uint4 *xs, float *cst, uint32_t U, uint32_t u) {
     const uint32_t hx[16] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w,
                              raw[2].x, raw[2].y, raw[2].z, raw[2].w, raw[3].x, raw[3].y, raw[3].z, raw[3].w};
     uint32_t mx = 0;
 #pragma unroll
     for (int e = 0; e < 16; ++e) mx = max(mx, max(hx[e] & 0x7FFFu, (hx[e] >> 16) & 0x7FFFu));
-    const int E = part_exponent(mx);
+    const int E = unit_exponent(mx);
     const float sc = exp2i(E);
-    int32_t xi[32], sum = 0;
+    int32_t xi[32], s0 = 0, s1 = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int32_t v = __float2int_rn(h2f_bits((i & 1) ? hi16(hx[i >> 1]) : lo16(hx[i >> 1])) * sc);
         xi[i] = min(max(v, -32767), 32767);
-        sum += xi[i];
+        if (i < 16) s0 += xi[i]; else s1 += xi[i];
     }
-    auto pk = [&](int i0, int i1) { return (uint32_t(xi[i0]) & 0xFFFFu) | (uint32_t(xi[i1]) << 16); };
+    uint32_t st[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        xs[j * U + u] = make_uint4(pk(8 * j, 8 * j + 2), pk(8 * j + 4, 8 * j + 6), pk(8 * j + 1, 8 * j + 3),
-                                   pk(8 * j + 5, 8 * j + 7));
-    cst[2 * u] = __int_as_float(-128 * sum);
-    cst[2 * u + 1] = exp2i(-(E + 4));
-}
-
-template <int F>
-__device__ __forceinline__ void stage_unit(const uint4 (&raw)[4], int E, uint4 *xs, float *cst, uint32_t U, uint32_t u) {
+    for (int a = 0; a < 16; ++a)
+        st[a] = (uint32_t(xi[dp_elem<F>(a, 0)]) & 0xFFFFu) | (uint32_t(xi[dp_elem<F>(a, 1)]) << 16);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) xs[t * U + u] = make_uint4(st[4 * t], st[4 * t + 1], st[4 * t + 2], st[4 * t + 3]);
+    float *c = cst + u * XC<F>::n;
+    const float XS = exp2i(-E);
     if constexpr (F == FMT_Q4G32) {
-        stage_unit_i16(raw, xs, cst, U, u);   // per-unit exponent; E (the part's) is not used
+        c[0] = __int_as_float(-128 * (s0 + s1));
+        c[1] = exp2i(-E - 4);
+    } else if constexpr (F == FMT_Q2S) {
+        c[0] = float(s0) * XS;
+        c[1] = float(s1) * XS;
+        c[2] = XS;
+    } else if constexpr (F == FMT_Q3S) {
+        c[0] = __int_as_float(-128 * s0);
+        c[1] = __int_as_float(-128 * s1);
+        c[2] = exp2i(-E - 5);
+    } else if constexpr (F == FMT_Q5S) {
+        c[0] = float(s0 + s1) * XS;
+        c[1] = XS;
     } else {
-        uint32_t w[16];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t rw[8] = {raw[2 * hh].x, raw[2 * hh].y, raw[2 * hh].z, raw[2 * hh].w,
-                                    raw[2 * hh + 1].x, raw[2 * hh + 1].y, raw[2 * hh + 1].z, raw[2 * hh + 1].w};
-            uint16_t xr[16];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { xr[2 * e] = lo16(rw[e]); xr[2 * e + 1] = hi16(rw[e]); }
-            stage_half_unit<F>(xr, E, w + 8 * hh);
-        }
-#pragma unroll
-        for (int t = 0; t < 4; ++t) xs[t * U + u] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
-        float xp[32], xt[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            xp[i] = h2f_bits(xh(w, i));
-            xt[i] = xp[i] * pow2f(xshift<F>(i));
-        }
-        unit_consts<F>(xp, xt, cst + u * XC<F>::n);
+        c[0] = __int_as_float(-128 * s0);
+        c[1] = __int_as_float(-128 * s1);
+        c[2] = exp2i(-E - 2);
     }
 }
 
@@ -603,12 +452,10 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 // Warp 16 is the producer (one lane issues the first copies; every later copy is issued by the consumer warp that
 // releases a stage last). Warps 0..15 consume every stage together: warp w handles row class rc = w / P (rows rc,
 // rc + RC, ...: RW rows) over K part q = w % P of the chunk (32 units; lane l owns unit 32 q + l of every chunk).
-// With MT = 1 a lane unpacks and multiplies in one pass (row_acc); with MT > 1 it unpacks each unit-row once
-// (unpack_row) and multiplies it against the MT staged activation rows (dot_row), so every weight is read and
-// unpacked once for the whole batch. Row sums accumulate over the chunks of a tile; then each warp reduces its lanes
-// with shuffles and stores one partial per (row, activation row, part), and the P partials are summed in a fixed
-// order (deterministic). Activations are staged per (row, part) with a power-of-two scale (max |x| * 2^E in
-// [2^14, 2^15)).
+// Every lane unpacks each of its unit-rows once (unpack_dp) and multiplies it against the MT staged activation rows
+// (dot_dp), so every weight is read and unpacked once for the whole batch. Row sums accumulate over the chunks of a
+// tile; then each warp reduces its lanes with shuffles and stores one partial per (row, activation row, part), and
+// the P partials are summed in a fixed order (deterministic).
 // ------------------------------------------------------------------------------------------------------------
 constexpr int G1_CW = 16;                      // consumer warps
 template <int F, int MT = 1> struct T1 {
@@ -629,7 +476,7 @@ template <int F, int MT = 1> struct T1 {
 constexpr int G1_THREADS = (G1_CW + 1) * 32;
 constexpr int G1_MAXNS = 16;                   // stages in the ring at most
 constexpr int G1_PRE = 1;                      // stage fills issued before the activations are staged
-constexpr uint32_t G1_HDR = 1024;              // mbarriers, release counters, per-(row, part) scales
+constexpr uint32_t G1_HDR = 1024;              // mbarriers and release counters
 
 struct G1Plan {
     uint32_t off_part, off_xs, off_cst, off_stages, smem;
@@ -658,8 +505,6 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem_g1);                  // [NS] stage filled
     uint32_t *rel = reinterpret_cast<uint32_t *>(smem_g1 + G1_MAXNS * 8);    // [NS] warps done with the stage
     uint64_t *xready = reinterpret_cast<uint64_t *>(smem_g1 + G1_MAXNS * 12);  // activations staged
-    float *uscale = reinterpret_cast<float *>(smem_g1 + 256);                // [MT][P]: 2^-E per (row, part)
-    uint32_t *pmax = reinterpret_cast<uint32_t *>(smem_g1 + 512);            // [MT][P]: max |x| bits
     float *part = reinterpret_cast<float *>(smem_g1 + pl.off_part);
     uint4 *xs = reinterpret_cast<uint4 *>(smem_g1 + pl.off_xs);              // [MT][4][U]
     float *cst = reinterpret_cast<float *>(smem_g1 + pl.off_cst);            // [MT][U][NX]
@@ -667,7 +512,6 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
 
     if (tid == 0) {
         for (uint32_t s = 0; s < NS; ++s) { mbar_init(&full[s], 1); rel[s] = 0; }
-        for (int i = 0; i < MT * P; ++i) pmax[i] = 0;
         mbar_init(xready, 1);
         fence_mbar_init();
     }
@@ -707,75 +551,29 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
     pdl_wait();                  // x (and y) may belong to the previous grid
     {
         const uint4 *xg = reinterpret_cast<const uint4 *>(a.X);
-        if constexpr (MT == 1) {
-            // Thread t handles units t, t + NT, ... (K <= 32768). A warp's 32 consecutive units are one 32-unit run of
-            // one chunk, i.e. of one K part, so a part's max |x| is a warp max plus one shared atomic per warp; after
-            // a barrier every thread stages its units from registers.
-            constexpr int HU = int((1024 + NT - 1) / NT);   // units per thread at the largest K
-            uint4 raw[HU][4];
+        // Thread t stages items t, t + NT, ... (item i = unit u of activation row m, i = m * U + u), each unit with its
+        // own exponent, so no unit waits for another; the loads of XD items go out before any of them is staged.
+        constexpr int XD = 2;
+        const uint32_t items = uint32_t(MT) * U;
+        for (uint32_t i0 = uint32_t(tid); i0 < items; i0 += XD * NT) {
+            uint4 raw[XD][4];
 #pragma unroll
-            for (int h = 0; h < HU; ++h) {
-                const uint32_t u = uint32_t(tid) + h * NT;
-                uint32_t mx = 0;
-                if (u < U) {
+            for (int d = 0; d < XD; ++d) {
+                const uint32_t it = i0 + d * NT, m = it / U, u = it - m * U;
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) raw[h][t] = __ldg(xg + 4 * u + t);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t w[4] = {raw[h][t].x, raw[h][t].y, raw[h][t].z, raw[h][t].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
-                    }
-                }
-                if (F != FMT_Q4G32 && uint32_t(tid - lane) + h * NT < U) {   // the warp's first unit exists
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                    if (lane == 0) atomicMax(&pmax[((uint32_t(tid) + h * NT) % UPC) / 32], mx);
-                }
-            }
-            if constexpr (F != FMT_Q4G32) named_bar_sync(1, G1_CW * 32);   // Q4G32: per-unit exponents
-#pragma unroll
-            for (int h = 0; h < HU; ++h) {
-                const uint32_t u = uint32_t(tid) + h * NT;
-                if (u < U) stage_unit<F>(raw[h], part_exponent(pmax[(u % UPC) / 32]), xs, cst, U, u);
-            }
-        } else {
-            // MT x U units (activation row m, unit u): item i = m * Upad + u, Upad = U rounded up to 32, so a warp's 32
-            // consecutive items are one 32-unit run of one chunk of one row, i.e. of one (row, K part). Two passes:
-            // the max, then (after a barrier) a reload and the staging. Rows m >= Mg of a short group stage zeros.
-            const uint32_t Upad = (U + 31) / 32 * 32, items = uint32_t(MT) * Upad;
-            for (uint32_t it = uint32_t(tid); F != FMT_Q4G32 && it < items; it += NT) {   // Q4G32: per-unit exponents
-                const uint32_t m = it / Upad, u = it - m * Upad;
-                uint32_t mx = 0;
-                if (u < U && m < Mg) {
+                for (int t = 0; t < 4; ++t) raw[d][t] = make_uint4(0u, 0u, 0u, 0u);
+                if (it < items && m < Mg) {
                     const uint4 *xr = xg + (int64_t(m) * a.ldx) / 8 + 4 * u;
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint4 v = __ldg(xr + t);
-                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
-                    }
+                    for (int t = 0; t < 4; ++t) raw[d][t] = __ldg(xr + t);
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                if (lane == 0) atomicMax(&pmax[m * P + (u % UPC) / 32], mx);
             }
-            if constexpr (F != FMT_Q4G32) named_bar_sync(1, G1_CW * 32);
-            for (uint32_t it = uint32_t(tid); it < items; it += NT) {
-                const uint32_t m = it / Upad, u = it - m * Upad;
-                if (u < U) {
-                    uint4 raw[4] = {};
-                    if (m < Mg) {
-                        const uint4 *xr = xg + (int64_t(m) * a.ldx) / 8 + 4 * u;
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) raw[t] = __ldg(xr + t);
-                    }
-                    stage_unit<F>(raw, part_exponent(pmax[m * P + (u % UPC) / 32]), xs + m * 4 * U, cst + m * U * NX, U, u);
-                }
+            for (int d = 0; d < XD; ++d) {
+                const uint32_t it = i0 + d * NT, m = it / U, u = it - m * U;
+                if (it < items) stage_unit<F>(raw[d], xs + m * 4 * U, cst + m * U * NX, U, u);
             }
         }
-        if (tid < MT * P) uscale[tid] = exp2i(-part_exponent(pmax[tid]));
         // every consumer meets here: masked lanes read the last unit's staged activations, whichever part staged it
         named_bar_sync(1, G1_CW * 32);
         if (tid == 0) mbar_arrive(xready);
@@ -810,14 +608,20 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 for (int cc = 0; cc < NX; ++cc) cv[cc] = cst[uu * NX + cc];
                 if (full_tile) {
 #pragma unroll
-                    for (int i = 0; i < RW; ++i)
-                        row_acc<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, cv, xv, true, acc[i]);
+                    for (int i = 0; i < RW; ++i) {
+                        DRow dr;
+                        unpack_dp<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, true, dr);
+                        dot_dp<F>(dr, xv, cv, acc[i]);
+                    }
                 } else {
                     // ragged tile or chunk: rows past the tile's end are skipped (uniform branches), lanes past K masked
 #pragma unroll
                     for (int i = 0; i < RW; ++i)
-                        if (rc + uint32_t(RC * i) < rows)
-                            row_acc<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, cv, xv, uv, acc[i]);
+                        if (rc + uint32_t(RC * i) < rows) {
+                            DRow dr;
+                            unpack_dp<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, uv, dr);
+                            dot_dp<F>(dr, xv, cv, acc[i]);
+                        }
                 }
             } else if constexpr (MT == 2) {
                 // both activation rows stay in registers; each unit-row is unpacked once and used twice
@@ -830,18 +634,18 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < RW; ++i) {
                     if (full_tile || rc + uint32_t(RC * i) < rows) {
-                        URow ur;
-                        unpack_row<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, full_tile || uv, ur);
-                        dot_row<F>(ur, xv0, cv0, acc[2 * i]);
-                        dot_row<F>(ur, xv1, cv1, acc[2 * i + 1]);
+                        DRow ur;
+                        unpack_dp<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, full_tile || uv, ur);
+                        dot_dp<F>(ur, xv0, cv0, acc[2 * i]);
+                        dot_dp<F>(ur, xv1, cv1, acc[2 * i + 1]);
                     }
                 }
             } else {
                 // each unit-row unpacked once, then multiplied against every activation row
-                URow ur[RW];
+                DRow ur[RW];
 #pragma unroll
                 for (int i = 0; i < RW; ++i)
-                    unpack_row<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo,
+                    unpack_dp<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo,
                                   full_tile || (uv && rc + uint32_t(RC * i) < rows), ur[i]);
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
@@ -851,7 +655,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
 #pragma unroll
                     for (int cc = 0; cc < NX; ++cc) cv[cc] = cst[(m * U + uu) * NX + cc];
 #pragma unroll
-                    for (int i = 0; i < RW; ++i) dot_row<F>(ur[i], xv, cv, acc[i * MT + m]);
+                    for (int i = 0; i < RW; ++i) dot_dp<F>(ur[i], xv, cv, acc[i * MT + m]);
                 }
             }
             // Release the stage; the warp that releases it last refills it with item k + NS (acq_rel: the other
@@ -887,7 +691,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 const uint32_t r = e / MT, m = e - r * MT;
                 float yv = 0.f;
 #pragma unroll
-                for (int pp = 0; pp < P; ++pp) yv = fmaf(part[(r * MT + m) * P + pp], uscale[m * P + pp], yv);
+                for (int pp = 0; pp < P; ++pp) yv += part[(r * MT + m) * P + pp];
                 if (m < Mg) a.Y[int64_t(m) * a.ldy + rbeg + base + r] = yv;
             }
             if (done != nrows) named_bar_sync(1, G1_CW * 32);   // partials of the next round overwrite these

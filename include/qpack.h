@@ -117,7 +117,10 @@ int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const fl
 
 /* Fused dequant-GEMV (decode, batch 1; P1 §1.2 and §3.3, P2 §3.3 "fused dequantization"):
  *   y[r] = sum_k w'[r,k] * x[k],  r < N
- * packed weights are read exactly once and unpacked in registers; fp32 accumulation.
+ * packed weights are read exactly once and unpacked in registers. x is rounded once to 16-bit fixed point per
+ * 32-element unit (step 2^-E, max |x| * 2^E in [2^14, 2^15): an element's rounding error is at most 2^-15 of its
+ * unit's max |x|, and x with an exponent within 4 of that max is exact); code x activation sums are exact int32
+ * within a sub-block, fp32 across sub-blocks.
  *  packed, group_scales  as produced by qpack_pack (group_scales NULL except Q4G32), 16-byte aligned
  *  x                     [K] fp16, 16-byte aligned
  *  y                     [N] fp32, 4-byte aligned
@@ -129,7 +132,7 @@ int qgemv(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, 
 
 /* Small-batch decode GEMM (P2 §5.2 decode vs prefill; batch up to 16):
  *   Y[m, r] = sum_k w'[r,k] * X[m,k],  m < M, r < N,  1 <= M <= 16
- * each packed weight is read once and reused across the M activation rows; fp32 accumulation.
+ * each packed weight is read once and reused across the M activation rows; activations and sums as in qgemv.
  *  X  [M, ldx] fp16, 16-byte aligned, ldx >= K and ldx a multiple of 8
  *  Y  [M, ldy] fp32, ldy >= N
  * Same parity bound as qgemv, per element. */
