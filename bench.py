@@ -230,9 +230,10 @@ def _time_graph(torch, fn, dev, reps=5, warm=3):
     return e0.elapsed_time(e1) / 1e3 / reps
 
 
-# FP32 FMA peak of the CUDA cores at the maximum SM clock (152 SMs x 128 lanes x 2 flops x 2.07 GHz); the small-batch
-# products are bound by it once M multiply-adds per weight outweigh the packed bytes.
-FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# Integer dot-product peak of the CUDA cores at the maximum SM clock: dp2a (two 16 x 8-bit multiply-adds) issues at
+# 60 per clock per SM on this GPU (measured), so 152 SMs x 60 x 2 MACs x 2 ops x 2.07 GHz; the small-batch products
+# are bound by it once M multiply-adds per weight outweigh the packed bytes.
+DP2A_TOPS = 152 * 60 * 2 * 2 * 2.07e9 / 1e12
 
 
 def int4_4096_extra(qp, torch, synth, dev, hbm_peak):
@@ -285,7 +286,7 @@ def small_batch_extra(qp, torch, synth, dev, hbm_peak):
             t = _time_graph(torch, fn, dev, reps=3)
             tf = 2.0 * M * weights / t / 1e12
             res[f"M{M}"] = {"GBps": total / t / 1e9, "pct_hbm_peak": total / t / 1e9 / hbm_peak,
-                            "TFLOPs": tf, "pct_ffma_peak": tf / FFMA_TFLOPS,
+                            "TOPs": tf, "pct_dp2a_peak": tf / DP2A_TOPS,
                             "tok_per_s_equiv": M / t, "ms_per_pass": t * 1e3}
         out[name] = {"bytes_per_pass": total, "launches_per_pass": len(mats), **res}
         del mats
