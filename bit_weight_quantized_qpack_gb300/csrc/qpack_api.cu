@@ -239,7 +239,6 @@ int qgemm_small(int fmt, const uint8_t *packed, const float *group_scales, int64
     if (!X || !Y) return QPACK_ERR_ARG;
     if (ldx < K || ldy < N) return QPACK_ERR_SHAPE;
     if (!aligned(X, 16) || (ldx % 8) || !aligned(Y, 4)) return QPACK_ERR_ALIGN;
-    if (M == 1 && K > 32768) return QPACK_ERR_UNSUPPORTED;   // staged activations + ring fit one SM
     if (N == 0 || M == 0) return QPACK_OK;
     GemvArgs a = {};
     a.packed = packed;

@@ -4,10 +4,10 @@
 // (2/3/5/6-bit article, lpnh.cn/news/2857666, §1.2: time per token = weight bytes / bandwidth; DBHOO-CIM
 // article, pwwt.cn/news/4452170, §3.3: dequantization must stay fused, never materialised).
 //
-// Batch-1 kernel (gemv1_kernel<F, 1>), one persistent CTA per SM:
-//   warp 16      producer: 2-D TMA tensor copies of (row tile x K chunk) boxes of the packed rows into a ring of
-//                shared-memory stages (completion on mbarriers, L2 evict-first because each byte is used once).
-//   warps 0..15  consumers: row class x K part of every stage; lane l owns one 32-weight unit of each chunk.
+// Batch-1 kernel (gemv1_kernel<F, 1>), one persistent CTA of 16 warps per SM: 2-D TMA tensor copies of (row tile x
+// K chunk) boxes of the packed rows stream into a ring of shared-memory stages (completion on mbarriers, L2
+// evict-first because each byte is used once); warp w takes row class x K part of every stage, lane l one 32-weight
+// unit of each chunk. Thread 0 issues the first copies; every later copy is issued by the warp that frees a stage.
 // Unpacking (2/3/5/6-bit article §3.3: separate unpack from multiply-add, factor s*(q.x) + m*sum(x)) works on integers:
 // each unit-row is unpacked with masks, byte permutes and shifts into eight words whose bytes each hold one code,
 // possibly shifted left inside its byte by a known "bit class"; the activations are staged once per launch as 16-bit
@@ -449,9 +449,9 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 // (row r of the chunk at r * CB bytes) whatever K is; words past the row end and rows past N arrive as zeros and are
 // masked by the consumers. One CTA per SM; the next product in the stream, launched as a programmatic dependent,
 // starts streaming its weights as soon as this CTA leaves its SM.
-// Warp 16 is the producer (one lane issues the first copies; every later copy is issued by the consumer warp that
-// releases a stage last). Warps 0..15 consume every stage together: warp w handles row class rc = w / P (rows rc,
-// rc + RC, ...: RW rows) over K part q = w % P of the chunk (32 units; lane l owns unit 32 q + l of every chunk).
+// Thread 0 issues the first copies; every later copy is issued by the warp that releases a stage last. The 16
+// warps consume every stage together: warp w handles row class rc = w / P (rows rc, rc + RC, ...: RW rows) over K
+// part q = w % P of the chunk (32 units; lane l owns unit 32 q + l of every chunk).
 // Every lane unpacks each of its unit-rows once (unpack_dp) and multiplies it against the MT staged activation rows
 // (dot_dp), so every weight is read and unpacked once for the whole batch. Row sums accumulate over the chunks of a
 // tile; then each warp reduces its lanes with shuffles and stores one partial per (row, activation row, part), and
@@ -463,7 +463,7 @@ template <int F, int MT = 1> struct T1 {
     static constexpr int UPC = CHW / 32;                                          // units per chunk
     static constexpr int P = UPC / 32;                                            // K parts of 32 units
     static constexpr int RC = G1_CW / P;                                          // row classes
-    static constexpr int RW = MT > 2 ? 2 : (F == FMT_Q4G32 ? 4 : (P == 4 ? 8 : 4)); // rows per warp and stage
+    static constexpr int RW = MT > 4 ? 2 : MT > 2 ? 4 : (F == FMT_Q4G32 ? 4 : (P == 4 ? 8 : 4)); // rows per warp and stage
     static constexpr int TR = RC * RW;                                            // rows per tile
     static constexpr int PR = MT > 1 ? (256 / MT > TR ? 256 / MT : TR) : 256;     // rows per partial-sum round
     static constexpr int CB = Fmt<F>::sb ? (CHW / 256) * Fmt<F>::bytes : CHW / 2; // code bytes per row chunk
@@ -473,7 +473,7 @@ template <int F, int MT = 1> struct T1 {
     static_assert(CB % 16 == 0 && CB / 8 <= 256 && SB / 8 <= 256, "tensor-map box limits");
     static_assert(PR % TR == 0 && RW * MT <= 32, "tile and reduction shapes");
 };
-constexpr int G1_THREADS = (G1_CW + 1) * 32;
+constexpr int G1_THREADS = G1_CW * 32;          // 16 warps: up to 128 registers a thread
 constexpr int G1_MAXNS = 16;                   // stages in the ring at most
 constexpr int G1_PRE = 1;                      // stage fills issued before the activations are staged
 constexpr uint32_t G1_HDR = 1024;              // mbarriers and release counters
@@ -504,7 +504,6 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem_g1);                  // [NS] stage filled
     uint32_t *rel = reinterpret_cast<uint32_t *>(smem_g1 + G1_MAXNS * 8);    // [NS] warps done with the stage
-    uint64_t *xready = reinterpret_cast<uint64_t *>(smem_g1 + G1_MAXNS * 12);  // activations staged
     float *part = reinterpret_cast<float *>(smem_g1 + pl.off_part);
     uint4 *xs = reinterpret_cast<uint4 *>(smem_g1 + pl.off_xs);              // [MT][4][U]
     float *cst = reinterpret_cast<float *>(smem_g1 + pl.off_cst);            // [MT][U][NX]
@@ -512,7 +511,6 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
 
     if (tid == 0) {
         for (uint32_t s = 0; s < NS; ++s) { mbar_init(&full[s], 1); rel[s] = 0; }
-        mbar_init(xready, 1);
         fence_mbar_init();
     }
     pdl_launch_dependents();     // the next product may begin launching; it still waits for us before reading x
@@ -523,26 +521,19 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
         const uint32_t s = j % NS, tj = j / nch, cj = j - tj * nch;
         uint8_t *st = stages + s * uint32_t(T::STAGE);
         mbar_arrive_expect_tx(&full[s], uint32_t(T::TX));
-        tma_load_2d(st, &tm_codes, int(cj * (CB / 8)), int(rbeg + tj * TR), &full[s], pol);
-        if constexpr (SB > 0) tma_load_2d(st + TR * CB, &tm_scales, int(cj * (SB / 8)), int(rbeg + tj * TR), &full[s], pol);
+        const int ck = int(a.kc0) + int(cj);
+        tma_load_2d(st, &tm_codes, ck * (CB / 8), int(rbeg + tj * TR), &full[s], pol);
+        if constexpr (SB > 0) tma_load_2d(st + TR * CB, &tm_scales, ck * (SB / 8), int(rbeg + tj * TR), &full[s], pol);
     };
 
-    if (warp == G1_CW) {
-        // ------------------------------------ producer ------------------------------------
-        if (lane == 0) {
-            // Packed weights are read before the previous grid has finished only when the caller opted in
-            // (QPACK_OPT_WEIGHT_PREFETCH: weights are not written by the kernel just before this one). Only the first
-            // G1_PRE fills go out before the activations are staged: a deeper early prefetch fills the memory queues
-            // and delays the activation loads on the critical path.
-            if (!a.weight_prefetch) pdl_wait();
-            uint32_t j = 0;
-            for (; j < nit && j < NS && j < uint32_t(G1_PRE); ++j) fill(j);
-            if (j < nit && j < NS) {
-                if (!mbar_wait_bounded_hint(xready, 0u)) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL);
-                for (; j < nit && j < NS; ++j) fill(j);
-            }
-        }
-        return;
+    // Thread 0 issues the first G1_PRE fills now and the rest of the ring once the activations are staged; every
+    // later fill is issued by the warp that releases a stage last. Packed weights are read before the previous grid
+    // has finished only when the caller opted in (QPACK_OPT_WEIGHT_PREFETCH: weights are not written by the kernel
+    // just before this one). Only the first fill goes out before the activations are staged: a deeper early
+    // prefetch fills the memory queues and delays the activation loads on the critical path.
+    if (tid == 0) {
+        if (!a.weight_prefetch) pdl_wait();
+        for (uint32_t j = 0; j < nit && j < NS && j < uint32_t(G1_PRE); ++j) fill(j);
     }
 
     // -------------------------------------- consumers --------------------------------------
@@ -576,7 +567,8 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
         }
         // every consumer meets here: masked lanes read the last unit's staged activations, whichever part staged it
         named_bar_sync(1, G1_CW * 32);
-        if (tid == 0) mbar_arrive(xready);
+        if (tid == 0)
+            for (uint32_t j = uint32_t(G1_PRE); j < nit && j < NS; ++j) fill(j);
     }
 
     const LaneGeo geo = lane_geo<F>(int(uc));
@@ -692,7 +684,10 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 float yv = 0.f;
 #pragma unroll
                 for (int pp = 0; pp < P; ++pp) yv += part[(r * MT + m) * P + pp];
-                if (m < Mg) a.Y[int64_t(m) * a.ldy + rbeg + base + r] = yv;
+                if (m < Mg) {
+                    float *yp = a.Y + int64_t(m) * a.ldy + rbeg + base + r;
+                    *yp = a.accumulate ? *yp + yv : yv;
+                }
             }
             if (done != nrows) named_bar_sync(1, G1_CW * 32);   // partials of the next round overwrite these
         }
@@ -790,37 +785,44 @@ static cudaError_t launch_gemv_mt(const GemvArgs &a, const G1Plan &pl, cudaStrea
     return cudaLaunchKernelEx(&cfg, gemv1_kernel<F, MT>, tmc, tms, a, pl);
 }
 
-// Activation rows in groups of MT (their staged activations share one SM's shared memory with the weight ring):
-// every group is one launch over the whole packed matrix.
+// All M <= MT activation rows in one group, K in splits of whole chunks: the widest split whose staged activations
+// leave room for a ring of at least two stages (MT <= 2) or three (MT >= 4). Every split is one launch over its
+// columns of the packed rows, so the weights are read once however long the rows are; the first split writes Y, the
+// later ones add to it (stream order, so the sum over the splits is taken in a fixed order).
 template <int F, int MT>
-static cudaError_t launch_groups(const GemvArgs &a, const G1Plan &pl, cudaStream_t st) {
-    for (int m0 = 0; m0 < a.M; m0 += MT) {
+static cudaError_t launch_split(const GemvArgs &a, cudaStream_t s) {
+    constexpr uint32_t BUDGET = 227u * 1024u;
+    constexpr int64_t CW = T1<F, MT>::CHW;
+    const int min_ns = MT <= 2 ? 2 : 3;
+    const int64_t nchunks = (a.K + CW - 1) / CW;
+    for (int64_t parts = 1; parts <= nchunks; ++parts) {
+        const int64_t ks = (nchunks + parts - 1) / parts * CW;
         GemvArgs g = a;
-        g.X = a.X + int64_t(m0) * a.ldx;
-        g.Y = a.Y + int64_t(m0) * a.ldy;
-        g.M = a.M - m0 < MT ? a.M - m0 : MT;
-        const cudaError_t e = launch_gemv_mt<F, MT>(g, pl, st);
-        if (e != cudaSuccess) return e;
+        g.K = ks < a.K ? ks : a.K;
+        G1Plan pl;
+        if (!plan_gemv1<F, MT>(g, BUDGET, &pl) || (pl.ns < min_ns && parts < nchunks)) continue;
+        for (int64_t k0 = 0; k0 < a.K; k0 += ks) {
+            GemvArgs h = a;
+            h.K = ks < a.K - k0 ? ks : a.K - k0;
+            h.X = a.X + k0;
+            h.kc0 = k0 / CW;
+            h.accumulate = k0 > 0 ? 1 : 0;
+            if (!plan_gemv1<F, MT>(h, BUDGET, &pl)) return cudaErrorInvalidValue;
+            const cudaError_t e = launch_gemv_mt<F, MT>(h, pl, s);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
     }
-    return cudaSuccess;
+    return cudaErrorInvalidValue;
 }
 
 template <int F>
 static cudaError_t launch_fmt(const GemvArgs &a, cudaStream_t s) {
-    G1Plan pl;
-    constexpr uint32_t BUDGET = 227u * 1024u;
-    if (a.M <= 1) {
-        if (!plan_gemv1<F, 1>(a, BUDGET, &pl)) return cudaErrorInvalidValue;
-        return launch_gemv_mt<F, 1>(a, pl, s);
-    }
-    // the widest group that still leaves a ring of at least three stages
-    if (a.M > 8 && plan_gemv1<F, 16>(a, BUDGET, &pl) && pl.ns >= 3) return launch_groups<F, 16>(a, pl, s);
-    if (a.M > 4 && plan_gemv1<F, 8>(a, BUDGET, &pl) && pl.ns >= 3) return launch_groups<F, 8>(a, pl, s);
-    if (a.M > 2 && plan_gemv1<F, 4>(a, BUDGET, &pl) && pl.ns >= 3) return launch_groups<F, 4>(a, pl, s);
-    if (plan_gemv1<F, 2>(a, BUDGET, &pl)) return launch_groups<F, 2>(a, pl, s);
-    // long rows of the widest formats: one row of activations per launch
-    if (!plan_gemv1<F, 1>(a, BUDGET, &pl)) return cudaErrorInvalidValue;
-    return launch_groups<F, 1>(a, pl, s);
+    if (a.M <= 1) return launch_split<F, 1>(a, s);
+    if (a.M <= 2) return launch_split<F, 2>(a, s);
+    if (a.M <= 4) return launch_split<F, 4>(a, s);
+    if (a.M <= 8) return launch_split<F, 8>(a, s);
+    return launch_split<F, 16>(a, s);
 }
 
 cudaError_t launch_gemv(int fmt, const GemvArgs &a, cudaStream_t s) {

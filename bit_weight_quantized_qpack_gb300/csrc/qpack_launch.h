@@ -45,6 +45,9 @@ struct GemvArgs {
     int M;
     int weight_prefetch;      // 1: launched as a programmatic dependent of the previous kernel and allowed to
                               //    stream packed weights before that kernel has finished (caller's opt-in)
+    int64_t kc0;              // first K chunk of this launch: it covers columns [kc0 * chunk, kc0 * chunk + K) of
+                              //    the packed rows (X already points at column kc0 * chunk)
+    int accumulate;           // 1: add the products to Y (a later K split), 0: overwrite Y
 };
 cudaError_t launch_gemv(int fmt, const GemvArgs &a, cudaStream_t s);
 

@@ -124,8 +124,8 @@ int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const fl
  *  packed, group_scales  as produced by qpack_pack (group_scales NULL except Q4G32), 16-byte aligned
  *  x                     [K] fp16, 16-byte aligned
  *  y                     [N] fp32, 4-byte aligned
- *  K                     at most 32768 (QPACK_ERR_UNSUPPORTED beyond: the staged activations share one SM's
- *                        shared memory with the weight ring)
+ *  K                     any multiple of the format's group (rows longer than one SM's shared memory can stage go
+ *                        in K splits whose products are added to y in split order)
  * Parity bound against an fp64 sum: |y[r] - y_ref[r]| <= 1e-4 * ||w'_r||_2 * ||x||_2. */
 int qgemv(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, const uint16_t *x,
           float *y, qpack_stream_t stream);

@@ -119,6 +119,23 @@ def test_gemv_stage_shapes(qpg, orc, name, shape):
 
 
 @pytest.mark.parametrize("name", ALL)
+@pytest.mark.parametrize("K", [32768 + 256, 65536 + 4096 + 256])
+def test_gemv_long_rows_in_k_splits(qpg, orc, name, K):
+    """Batch-1 rows longer than one SM can stage beside the weight ring: the product is taken in K splits whose partial
+    products are added to y in split order."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    N = 157
+    rp, rgs = case(orc, fmt, N, K, 680 + K % 13)
+    x = synth.normal((K,), 1.0, 681, dtype=torch.float16)
+    y = run_gemv(qpg, fmt, rp, rgs, N, K, x)
+    y_ref = orc.gemv(fmt, N, K, rp, rgs, x.numpy().view(np.uint16), nthreads=8)
+    deq = orc.dequant(fmt, N, K, rp, rgs)
+    gemv_bound_check(y, y_ref, deq, x.numpy().astype(np.float64)[None, :])
+    assert qpg.qpack_fetch_fault_flags() == 0
+
+
+@pytest.mark.parametrize("name", ALL)
 def test_gemv_large_activations_and_zero_rows(qpg, orc, name):
     from bit_weight_quantized_qpack_gb300 import synth
     fmt = qpg.FORMATS[name]
@@ -151,12 +168,13 @@ def test_small_batch(qpg, orc, name, M):
     gemv_bound_check(Y.cpu().numpy(), Y_ref, deq, X.numpy().astype(np.float64))
 
 
-# (N, K, M): activation rows split into several launches (the staged rows of a group share one SM's shared memory
-# with the weight ring) with a short last group, at the 70B MLP widths.
-SMALL_BATCH_SHAPES = [(613, 8192, 16), (613, 8192, 5), (211, 28672, 16), (211, 28672, 3)]
+# (N, K, M): rows whose staged activations do not fit one SM's shared memory beside the weight ring go in K splits
+# (one launch per split, the later ones adding to Y), at the 70B MLP widths, with a ragged last split.
+SMALL_BATCH_SHAPES = [(613, 8192, 16), (613, 8192, 5), (211, 28672, 16), (211, 28672, 3), (97, 28672 + 256, 16),
+                      (97, 28672 + 256, 7)]
 
 
-@pytest.mark.parametrize("name", ["Q4G32", "Q3S", "Q5S"])
+@pytest.mark.parametrize("name", ALL)
 @pytest.mark.parametrize("shape", SMALL_BATCH_SHAPES, ids=[f"{n}x{k}xM{m}" for n, k, m in SMALL_BATCH_SHAPES])
 def test_small_batch_groups(qpg, orc, name, shape):
     from bit_weight_quantized_qpack_gb300 import synth
