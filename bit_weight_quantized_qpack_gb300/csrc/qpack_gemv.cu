@@ -479,8 +479,9 @@ constexpr int G1_PRE = 1;                      // stage fills issued before the 
 constexpr uint32_t G1_HDR = 1024;              // mbarriers and release counters
 
 struct G1Plan {
-    uint32_t off_part, off_xs, off_cst, off_stages, smem;
+    uint32_t off_part, off_xs, off_cst, off_xraw, off_stages, smem;
     int ns;
+    int xt;   // batch 1, long streams: x arrives by one bulk copy queued ahead of the rest of the ring (see launch_split)
 };
 
 template <int F, int MT>
@@ -508,9 +509,13 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
     uint4 *xs = reinterpret_cast<uint4 *>(smem_g1 + pl.off_xs);              // [MT][4][U]
     float *cst = reinterpret_cast<float *>(smem_g1 + pl.off_cst);            // [MT][U][NX]
     uint8_t *stages = smem_g1 + pl.off_stages;
+    const bool xt = MT == 1 && pl.xt != 0;
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(smem_g1 + G1_MAXNS * 12);   // raw x landed (xt)
+    const uint4 *xraw = reinterpret_cast<const uint4 *>(smem_g1 + pl.off_xraw);
 
     if (tid == 0) {
         for (uint32_t s = 0; s < NS; ++s) { mbar_init(&full[s], 1); rel[s] = 0; }
+        if (xt) mbar_init(xbar, 1);
         fence_mbar_init();
     }
     pdl_launch_dependents();     // the next product may begin launching; it still waits for us before reading x
@@ -534,12 +539,23 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
     if (tid == 0) {
         if (!a.weight_prefetch) pdl_wait();
         for (uint32_t j = 0; j < nit && j < NS && j < uint32_t(G1_PRE); ++j) fill(j);
+        if (xt) {
+            // x by one bulk copy as soon as the previous grid is done, ahead of the rest of the ring in the copy queue
+            if (a.weight_prefetch) pdl_wait();
+            mbar_arrive_expect_tx(xbar, K * 2u);
+            bulk_g2s(const_cast<uint4 *>(xraw), a.X, K * 2u, xbar, l2_evict_last_policy());
+            for (uint32_t j = uint32_t(G1_PRE); j < nit && j < NS; ++j) fill(j);
+        }
     }
 
     // -------------------------------------- consumers --------------------------------------
     const uint32_t rc = uint32_t(warp) / P, q = uint32_t(warp) % P;
     const uint32_t uc = q * 32u + uint32_t(lane);           // this lane's unit within every chunk
     pdl_wait();                  // x (and y) may belong to the previous grid
+    bool xlost = false;
+    if (xt) {
+        if (!mbar_wait_bounded(xbar, 0u)) { xlost = true; if (tid == 0) atomicOr(&g_fault_gemv, FAULT_WAIT_FULL); }
+    }
     {
         const uint4 *xg = reinterpret_cast<const uint4 *>(a.X);
         // Thread t stages items t, t + NT, ... (item i = unit u of activation row m, i = m * U + u), each unit with its
@@ -554,9 +570,14 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
 #pragma unroll
                 for (int t = 0; t < 4; ++t) raw[d][t] = make_uint4(0u, 0u, 0u, 0u);
                 if (it < items && m < Mg) {
-                    const uint4 *xr = xg + (int64_t(m) * a.ldx) / 8 + 4 * u;
+                    if (xt) {
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) raw[d][t] = __ldg(xr + t);
+                        for (int t = 0; t < 4; ++t) raw[d][t] = xraw[4 * u + t];
+                    } else {
+                        const uint4 *xr = xg + (int64_t(m) * a.ldx) / 8 + 4 * u;
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) raw[d][t] = __ldg(xr + t);
+                    }
                 }
             }
 #pragma unroll
@@ -567,7 +588,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
         }
         // every consumer meets here: masked lanes read the last unit's staged activations, whichever part staged it
         named_bar_sync(1, G1_CW * 32);
-        if (tid == 0)
+        if (!xt && tid == 0)
             for (uint32_t j = uint32_t(G1_PRE); j < nit && j < NS; ++j) fill(j);
     }
 
@@ -698,17 +719,21 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
         for (uint32_t j = (nit > NS ? nit - NS : 0u); j < nit; ++j)
             if (!mbar_wait_bounded(&full[j % NS], (j / NS) & 1u)) break;
     }
+    if (xlost && tid == 0) mbar_wait_bounded(xbar, 0u);   // the activation copy too (xt)
 }
 
 // Shared-memory plan of one launch: returns false when two stages plus the staged activations do not fit `budget`.
 template <int F, int MT>
-static bool plan_gemv1(const GemvArgs &a, uint32_t budget, G1Plan *pl) {
+static bool plan_gemv1(const GemvArgs &a, uint32_t budget, G1Plan *pl, bool xt = false) {
     using T = T1<F, MT>;
     const uint32_t U = uint32_t(a.K / 32);
     pl->off_part = G1_HDR;
     pl->off_xs = pl->off_part + uint32_t(T::PR * MT * T::P * 4);
     pl->off_cst = pl->off_xs + uint32_t(round_up(int64_t(MT) * U * 64, 128));
-    pl->off_stages = uint32_t(round_up(pl->off_cst + int64_t(MT) * U * XC<F>::n * 4, 1024));
+    pl->off_xraw = uint32_t(round_up(pl->off_cst + int64_t(MT) * U * XC<F>::n * 4, 128));
+    const int64_t xraw_bytes = (xt && MT == 1) ? round_up(int64_t(a.K) * 2, 128) : 0;
+    pl->xt = (xt && MT == 1) ? 1 : 0;
+    pl->off_stages = uint32_t(round_up(pl->off_xraw + xraw_bytes, 1024));
     // + 32: the Q3S / Q6S unpack reads up to 4 bytes past a row chunk
     const int64_t room = int64_t(budget) - pl->off_stages - 32;
     if (room < int64_t(T::STAGE) * 2) return false;
@@ -808,6 +833,18 @@ static cudaError_t launch_split(const GemvArgs &a, cudaStream_t s) {
             h.kc0 = k0 / CW;
             h.accumulate = k0 > 0 ? 1 : 0;
             if (!plan_gemv1<F, MT>(h, BUDGET, &pl)) return cudaErrorInvalidValue;
+            if constexpr (MT == 1) {
+                // Batch 1 with more stages per CTA than the ring holds: x by a bulk copy queued right behind the first
+                // fill and the whole ring filled at once beats staging x first (measured; with a ring that holds all
+                // of a CTA's stages the early fills only delay x, and a raw x buffer that costs the ring stages
+                // below four loses more than it gains).
+                using T = T1<F, MT>;
+                const int64_t grid = num_sms() < h.N ? num_sms() : h.N;
+                const int64_t rows = (h.N + grid - 1) / grid;
+                const int64_t nit = (rows + T::TR - 1) / T::TR * ((h.K + T::CHW - 1) / T::CHW);
+                G1Plan px;
+                if (plan_gemv1<F, MT>(h, BUDGET, &px, true) && nit > px.ns && px.ns >= (pl.ns < 4 ? pl.ns : 4)) pl = px;
+            }
             const cudaError_t e = launch_gemv_mt<F, MT>(h, pl, s);
             if (e != cudaSuccess) return e;
         }
