@@ -9,8 +9,8 @@
 //   warp 9      TMA producer: per 64-wide K step, four 2-D tensor copies bring the 4 x (128 x 64) bf16 X tiles into
 //               shared memory already in the 128-byte-swizzled K-major layout the MMA reads.
 //   warps 0..7  weight producers: per K step, each thread dequantizes one 32-weight unit of one of the 128 weight
-//               rows (exact fp32 dequant of FORMATS.md from aligned global loads, then bf16 round-to-nearest-even)
-//               into the swizzled 128 x 64 weight tile; afterwards they are the epilogue warps (tcgen05.ld of their
+//               rows (exact fp32 dequant of FORMATS.md from aligned global loads issued three K steps ahead, then
+//               bf16 round-to-nearest-even) into the swizzled 128 x 64 weight tile; afterwards they are the epilogue warps (tcgen05.ld of their
 //               TMEM lane quarter, bf16 conversion, global stores).
 //   warp 8      allocates all 512 TMEM columns (four fp32 128 x 128 accumulators); lane 0 issues the tcgen05.mma
 //               instructions (M=128, N=128, K=16; both operands from shared-memory descriptors) and commits them to
@@ -284,34 +284,46 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         const int64_t n = n0 + r;
         const uint8_t *row = a.packed + n * a.row_stride;
         const float *gs_row = a.gscale ? a.gscale + n * a.scale_stride : nullptr;
-        // the raw bytes of step kt + 1 are loaded while step kt is converted and stored
-        RawUnit cur = {}, nxt = {};
-        if (n < N && nk > 0) load_raw<F>(row, gs_row, uint32_t(h), cur);
-        for (int kt = 0; kt < nk && !dead; ++kt) {
+        // The raw bytes of step k + 3 are loaded while step k is converted and stored: four register slots in fixed
+        // roles (the loop is unrolled by four), so no slot is copied while its loads are in flight.
+        RawUnit S0 = {}, S1 = {}, S2 = {}, S3 = {};
+        if (n < N) {
+            if (nk > 0) load_raw<F>(row, gs_row, uint32_t(h), S0);
+            if (nk > 1) load_raw<F>(row, gs_row, uint32_t(2 + h), S1);
+            if (nk > 2) load_raw<F>(row, gs_row, uint32_t(4 + h), S2);
+        }
+        auto step = [&](int kt, const RawUnit &use, RawUnit &into) {
+            if (kt >= nk || dead) return;
             const int st = kt % STAGES;
-            if (n < N && kt + 1 < nk) load_raw<F>(row, gs_row, uint32_t(2 * (kt + 1) + h), nxt);
+            if (n < N && kt + 3 < nk) load_raw<F>(row, gs_row, uint32_t(2 * (kt + 3) + h), into);
             if (kt >= STAGES && !mbar_wait_bounded(&empty[st], uint32_t((kt / STAGES) - 1) & 1u)) {
                 atomicOr(&g_fault_prefill, FAULT_WAIT_EMPTY);
                 dead = true;
-                break;
+                return;
             }
             uint8_t *Bs = sm + st * STAGE_BYTES + NSUB * A_BYTES;
             uint4 v[4];
             if (n < N) {
                 uint32_t o[16];
-                unit_bf16<F>(cur, uint32_t(2 * kt + h), o);
+                unit_bf16<F>(use, uint32_t(2 * kt + h), o);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) v[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
             }
-            cur = nxt;
 #pragma unroll
             for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(Bs + sw128_off(uint32_t(r), uint32_t(4 * h + c))) = v[c];
             fence_proxy_async_smem();      // make the generic-proxy stores visible to the tensor core
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[st]);
+        };
+#pragma unroll 1
+        for (int kt = 0; kt < nk && !dead; kt += 4) {
+            step(kt, S0, S3);
+            step(kt + 1, S1, S0);
+            step(kt + 2, S2, S1);
+            step(kt + 3, S3, S2);
         }
         // ---------------------------------- epilogue ----------------------------------
         {
