@@ -258,6 +258,46 @@ def int4_4096_extra(qp, torch, synth, dev, hbm_peak):
             "bytes_per_gemv": wb, "copies": R}
 
 
+def mixed_7b_extra(qp, torch, synth, dev, steps=10):
+    """7B-Llama-shaped decode step with a per-matrix format mix (2/3/5/6-bit article §2.4: the sensitive attention
+    projections get 5 or 6 bits, the wide feed-forward matrices 2 or 3): q and k Q5S, v and o Q6S, gate, up and down
+    Q3S. Launches per layer: q|k (row-concatenated), v, o, gate|up, down. Same weights and activations as the
+    single-format step."""
+    shapes = [(4096, 4096)] * 4 + [(11008, 4096)] * 2 + [(4096, 11008)]
+    fmts = ["Q5S", "Q5S", "Q6S", "Q6S", "Q3S", "Q3S", "Q3S"]
+    groups = [[0, 1], [2], [3], [4, 5], [6]]
+    launches, total, weights = [], 0, 0
+    for layer in range(32):
+        packed = []
+        for mi, (N, K) in enumerate(shapes):
+            fmt = qp.FORMATS[fmts[mi]]
+            W = synth.laplace((N, K), 0.02, seed=synth.seed_for(3, layer, mi), device=dev)
+            p, _ = qp.qpack_quantize_pack(fmt, W)
+            del W
+            packed.append(p)
+            total += qp.layout(fmt, N, K)["weight_bytes"]
+            weights += N * K
+        for gidx in groups:
+            K = shapes[gidx[0]][1]
+            launches.append((qp.FORMATS[fmts[gidx[0]]], torch.cat([packed[i] for i in gidx], 0),
+                             sum(shapes[i][0] for i in gidx), K))
+    x4 = synth.normal((4096,), 1.0, seed=11, device=dev, dtype=torch.float16)
+    x11 = synth.normal((11008,), 1.0, seed=12, device=dev, dtype=torch.float16)
+    ys = {N: torch.empty(N, device=dev) for N in (4096, 8192, 11008, 22016)}
+
+    def fn(s):
+        for fmt, p, N, K in launches:
+            qp.qgemv(fmt, p, None, N, K, x4 if K == 4096 else x11, ys[N], stream=s)
+
+    t = _time_graph(torch, fn, dev, reps=steps)
+    out = {"formats": "q,k Q5S; v,o Q6S; gate,up,down Q3S", "bpw": 8.0 * total / weights,
+           "bytes_per_step": total, "tok_per_s_equiv": 1.0 / t, "GBps": total / t / 1e9, "ms_per_step": t * 1e3,
+           "launches": len(launches)}
+    del launches
+    torch.cuda.empty_cache()
+    return out
+
+
 def small_batch_extra(qp, torch, synth, dev, hbm_peak):
     """Decode products with M = 1..16 activation rows over 80 layers of 70B-shaped MLP weights (gate/up 28672x8192,
     down 8192x28672, Laplace(0, 0.01)), streamed in turn: one pass = 240 products."""
@@ -441,6 +481,7 @@ def run_ours(args, world, rank, local):
             del P, X, Y
             torch.cuda.empty_cache()
             extra = {"decode_7b": decode_7b_extra(qp, torch, synth, dev),
+                     "decode_7b_mixed": mixed_7b_extra(qp, torch, synth, dev),
                      "int4_4096": int4_4096_extra(qp, torch, synth, dev, hbm_peak),
                      "small_batch_70b_mlp": small_batch_extra(qp, torch, synth, dev, hbm_peak),
                      "prefill_2048": prefill_extra(qp, torch, synth, dev, bf16_peak, hbm_peak)}

@@ -95,3 +95,27 @@ def test_config4_70b_mlp_small_batch(qpg, orc, name):
             del p, g
             torch.cuda.empty_cache()
     assert qpg.qpack_fetch_fault_flags() == 0
+
+
+def test_config3_mixed_format_layer(qpg, orc):
+    """The mixed-format decode step (q and k Q5S, v and o Q6S, feed-forward Q3S; 2/3/5/6-bit article §2.4): every
+    launch of layer 0, with q|k and gate|up row-concatenated."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    shapes = [(4096, 4096)] * 4 + [(11008, 4096)] * 2 + [(4096, 11008)]
+    fmts = ["Q5S", "Q5S", "Q6S", "Q6S", "Q3S", "Q3S", "Q3S"]
+    groups = [[0, 1], [2], [3], [4, 5], [6]]
+    x4 = synth.normal((4096,), 1.0, seed=11, device="cuda", dtype=torch.float16)
+    x11 = synth.normal((11008,), 1.0, seed=12, device="cuda", dtype=torch.float16)
+    Ws = [synth.laplace((N, K), 0.02, seed=synth.seed_for(3, 0, mi), device="cuda") for mi, (N, K) in enumerate(shapes)]
+    for gi, gidx in enumerate(groups):
+        fmt = qpg.FORMATS[fmts[gidx[0]]]
+        K = shapes[gidx[0]][1]
+        N = sum(shapes[i][0] for i in gidx)
+        pc = torch.cat([qpg.qpack_quantize_pack(fmt, Ws[i])[0] for i in gidx], 0)
+        x = x4 if K == 4096 else x11
+        y = qpg.qgemv(fmt, pc, None, N, K, x)
+        torch.cuda.synchronize()
+        rows = sampled_rows(N, 500 + gi)
+        W_rows = torch.cat([Ws[i] for i in gidx], 0)[torch.as_tensor(rows, device="cuda")].cpu().numpy()
+        check_rows(qpg, orc, fmt, W_rows, pc, None, rows, x[None, :], y[None, :])
+    assert qpg.qpack_fetch_fault_flags() == 0
