@@ -1,7 +1,8 @@
 """qpack oracle — TEST INFRASTRUCTURE ONLY.
 
 Python (ctypes + numpy) front of the plain C++ oracle in ``qpack_oracle.cpp``: the five weight formats'
-quantizers, packers, unpackers, dequantization and fp64-accumulated products, written from the source pages
+quantizers, packers, unpackers, dequantization and fp64-accumulated products, and the 8-bit KV-cache quantizer and
+dequantizer (P1 §4.1; the Mix-Quant article, lnrk.cn/news/34246, §2.3), written from the source pages
 (P1 = the 2/3/5/6-bit quantization article, lpnh.cn/news/2857666; P2 = the DBHOO-CIM INT4 CPU inference
 article, pwwt.cn/news/4452170) and FORMATS.md.
 
@@ -70,6 +71,8 @@ def lib():
                 "orc_dequant_rows": [I, I64, I64, P, P, I64, I64, P],
                 "orc_gemm_rows": [I, I64, I64, P, P, I64, P, I64, I64, I64, P, I],
                 "orc_prefill_sample": [I, I64, I64, P, P, P, I64, I64, P, P, I64, I, P],
+                "orc_kv_quantize": [P, I64, P, P],
+                "orc_kv_dequant": [P, P, I64, P],
             }
             for name, args in sigs.items():
                 fn = getattr(L, name)
@@ -268,3 +271,27 @@ def quantize_pack(fmt, W):
     parts = quantize(fmt, W)
     packed, gs = pack(fmt, W.shape[0], W.shape[1], parts)
     return packed, gs, parts["flags"]
+
+
+# ---------------------------------------------------------------------------------------------------------
+# 8-bit KV cache (2/3/5/6-bit article §4.1; Mix-Quant article §2.3)
+# ---------------------------------------------------------------------------------------------------------
+def kv_quantize(v_f16_bits):
+    """fp16 bit patterns (any shape, size a multiple of 32, groups of 32 consecutive elements) ->
+    (int8 codes of the same shape, fp16 scale bit patterns [size / 32])."""
+    v = _c(v_f16_bits, np.uint16)
+    q = np.empty(v.shape, np.int8)
+    s = np.empty(v.size // 32, np.uint16)
+    if lib().orc_kv_quantize(_p(v), v.size, _p(q), _p(s)) != 0:
+        raise ValueError("kv_quantize: size must be a multiple of 32")
+    return q, s
+
+
+def kv_dequant(q, scales):
+    """int8 codes + fp16 scale bit patterns -> fp16 bit patterns of the codes' shape."""
+    q = _c(q, np.int8)
+    s = _c(scales, np.uint16)
+    out = np.empty(q.shape, np.uint16)
+    if lib().orc_kv_dequant(_p(q), _p(s), q.size, _p(out)) != 0:
+        raise ValueError("kv_dequant: size must be a multiple of 32")
+    return out

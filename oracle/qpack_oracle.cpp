@@ -605,4 +605,44 @@ int orc_prefill_sample(int fmt, int64_t N, int64_t K, const uint8_t *packed, con
     return 0;
 }
 
+// ---------------------------------------------------------------------------------------------------------
+// 8-bit KV cache. The 2/3/5/6-bit article (§4.1) quantizes the KV cache to 8 bits with every 32 elements sharing
+// one fp16 scale (about 1.06 bytes per element, half the fp16 size); the Mix-Quant article (§2.3) dequantizes such
+// an int8 cache back to fp16. Reading (plainest, the super-block rules at 8 bits): groups of 32 consecutive
+// elements, d = max|v| / 127 in fp32 rounded to fp16 and used rounded from there on, q = clamp(rint(v / d), -127,
+// 127) (0 when d is 0), dequant v' = fp16(d * q). Inputs are fp16 and finite.
+// ---------------------------------------------------------------------------------------------------------
+int orc_kv_quantize(const uint16_t *v, int64_t n, int8_t *q, uint16_t *scales) {
+    if (n < 0 || n % 32 != 0) return -1;
+    for (int64_t g = 0; g < n / 32; ++g) {
+        float a = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            const float x = std::fabs(f16_to_f32(v[32 * g + i]));
+            if (x > a) a = x;
+        }
+        const uint16_t d16 = f32_to_f16(a / 127.0f);
+        const float d = f16_to_f32(d16);
+        scales[g] = d16;
+        for (int i = 0; i < 32; ++i) {
+            float t = 0.0f;
+            if (d > 0.0f) {
+                t = std::nearbyint(f16_to_f32(v[32 * g + i]) / d);
+                if (t > 127.0f) t = 127.0f;
+                if (t < -127.0f) t = -127.0f;
+            }
+            q[32 * g + i] = int8_t(t);
+        }
+    }
+    return 0;
+}
+
+int orc_kv_dequant(const int8_t *q, const uint16_t *scales, int64_t n, uint16_t *out) {
+    if (n < 0 || n % 32 != 0) return -1;
+    for (int64_t g = 0; g < n / 32; ++g) {
+        const float d = f16_to_f32(scales[g]);
+        for (int i = 0; i < 32; ++i) out[32 * g + i] = f32_to_f16(d * float(q[32 * g + i]));
+    }
+    return 0;
+}
+
 }  // extern "C"
