@@ -298,6 +298,25 @@ def mixed_7b_extra(qp, torch, synth, dev, steps=10):
     return out
 
 
+def kv_cache_extra(qp, torch, synth, dev, hbm_peak):
+    """8-bit KV cache of the 7B grouped-query model at 8192 tokens (2 x 32 layers x 8 KV heads x 8192 x 128 fp16,
+    1.07 GB; 2/3/5/6-bit article §4.1): quantize (fp16 in, int8 + one fp16 scale per 32 out) and dequantize back.
+    Both are HBM streams of 2 + 34/32 bytes per element; the cache is far larger than L2."""
+    v = synth.normal((2, 32, 8, 8192, 128), 1.0, seed=21, device=dev, dtype=torch.float16)
+    n = v.numel()
+    q, s = qp.qpack_kv_quantize(v)
+    out = qp.qpack_kv_dequant(q, s)
+    nbytes = n * 2 + n + (n // 32) * 2
+    res = {"elements": n, "bytes_per_call": nbytes}
+    for name, fn in (("quantize", lambda st: qp.qpack_kv_quantize(v, q, s, stream=st)),
+                     ("dequant", lambda st: qp.qpack_kv_dequant(q, s, out, stream=st))):
+        t = _time_graph(torch, fn, dev, reps=10)
+        res[name] = {"GBps": nbytes / t / 1e9, "pct_hbm_peak": nbytes / t / 1e9 / hbm_peak, "us": t * 1e6}
+    del v, q, s, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def small_batch_extra(qp, torch, synth, dev, hbm_peak):
     """Decode products with M = 1..16 activation rows over 80 layers of 70B-shaped MLP weights (gate/up 28672x8192,
     down 8192x28672, Laplace(0, 0.01)), streamed in turn: one pass = 240 products."""
@@ -484,7 +503,8 @@ def run_ours(args, world, rank, local):
                      "decode_7b_mixed": mixed_7b_extra(qp, torch, synth, dev),
                      "int4_4096": int4_4096_extra(qp, torch, synth, dev, hbm_peak),
                      "small_batch_70b_mlp": small_batch_extra(qp, torch, synth, dev, hbm_peak),
-                     "prefill_2048": prefill_extra(qp, torch, synth, dev, bf16_peak, hbm_peak)}
+                     "prefill_2048": prefill_extra(qp, torch, synth, dev, bf16_peak, hbm_peak),
+                     "kv_cache_8bit": kv_cache_extra(qp, torch, synth, dev, hbm_peak)}
 
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["csrc_digest"] == csrc_digest() else None
     line = {
@@ -526,9 +546,16 @@ def run_ncu_case(args):
     _build.build()
     import bit_weight_quantized_qpack_gb300 as qp
     from bit_weight_quantized_qpack_gb300 import synth
+    dev = torch.device("cuda", 0)
+    if args.ncu_case == "kv":
+        v = synth.normal((args.M, args.N, args.K), 1.0, seed=21, device=dev, dtype=torch.float16)
+        q, s = qp.qpack_kv_quantize(v)
+        out = qp.qpack_kv_dequant(q, s)
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_case": "kv", "elements": v.numel(), "faults": qp.qpack_fetch_fault_flags()}))
+        return 0
     fmt = qp.FORMATS[args.fmt]
     N, K = args.N, args.K
-    dev = torch.device("cuda", 0)
     W = synth.laplace((N, K), 0.02, seed=1, device=dev)
     p0, g0 = qp.qpack_quantize_pack(fmt, W)
     del W
@@ -566,7 +593,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 7B decode-step extra")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true", help="disable QPACK_OPT_WEIGHT_PREFETCH")
-    ap.add_argument("--ncu-case", choices=["gemv", "small", "prefill"], default=None,
+    ap.add_argument("--ncu-case", choices=["gemv", "small", "prefill", "kv"], default=None,
                     help="short run of one product for an ncu capture (see profiles/)")
     ap.add_argument("--fmt", default="Q3S")
     ap.add_argument("--N", type=int, default=N_ROWS)

@@ -57,6 +57,8 @@ def lib():
                 "qgemv": ([I, P, P, I64, I64, P, P, P], I),
                 "qgemm_small": ([I, P, P, I64, I64, I, P, I64, P, I64, P], I),
                 "qgemm_prefill": ([I, P, P, I64, I64, I64, P, I64, P, I64, P], I),
+                "qpack_kv_quantize": ([P, I64, P, P, P], I),
+                "qpack_kv_dequant": ([P, P, I64, P, P], I),
                 "qpack_status_string": ([I], ctypes.c_char_p),
                 "qpack_fetch_fault_flags": ([ctypes.POINTER(ctypes.c_int32)], I),
                 "qpack_version": ([], I),
@@ -192,6 +194,24 @@ def qgemm_prefill(fmt, packed, group_scales, N, K, X, Y=None, stream=None):
                              _ptr(Y), Y.stride(0), _stream(stream))
     _check(rc, "qgemm_prefill")
     return Y
+
+
+def qpack_kv_quantize(v, codes=None, scales=None, stream=None):
+    """fp16 KV tensor (any shape, contiguous, numel a multiple of 32) -> (int8 codes of its shape, fp16 scales
+    [numel / 32]): one fp16 scale per 32 consecutive elements."""
+    n = v.numel()
+    codes = torch.empty(v.shape, dtype=torch.int8, device=v.device) if codes is None else codes
+    scales = torch.empty(n // 32, dtype=torch.float16, device=v.device) if scales is None else scales
+    _check(lib().qpack_kv_quantize(_ptr(v), n, _ptr(codes), _ptr(scales), _stream(stream)), "qpack_kv_quantize")
+    return codes, scales
+
+
+def qpack_kv_dequant(codes, scales, out=None, stream=None):
+    """int8 codes + fp16 scales -> fp16 tensor of the codes' shape."""
+    out = torch.empty(codes.shape, dtype=torch.float16, device=codes.device) if out is None else out
+    _check(lib().qpack_kv_dequant(_ptr(codes), _ptr(scales), codes.numel(), _ptr(out), _stream(stream)),
+           "qpack_kv_dequant")
+    return out
 
 
 def qpack_fetch_fault_flags() -> int:

@@ -291,6 +291,22 @@ int qgemm_prefill(int fmt, const uint8_t *packed, const float *group_scales, int
     return cuda_status(e);
 }
 
+int qpack_kv_quantize(const uint16_t *v, int64_t n, int8_t *codes, uint16_t *scales, qpack_stream_t stream) {
+    if (n < 0 || n % 32 != 0) return QPACK_ERR_SHAPE;
+    if (n == 0) return QPACK_OK;
+    if (!v || !codes || !scales) return QPACK_ERR_ARG;
+    if (!aligned(v, 16) || !aligned(codes, 8) || !aligned(scales, 2)) return QPACK_ERR_ALIGN;
+    return cuda_status(launch_kv_quantize(v, n, codes, scales, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int qpack_kv_dequant(const int8_t *codes, const uint16_t *scales, int64_t n, uint16_t *out, qpack_stream_t stream) {
+    if (n < 0 || n % 32 != 0) return QPACK_ERR_SHAPE;
+    if (n == 0) return QPACK_OK;
+    if (!codes || !scales || !out) return QPACK_ERR_ARG;
+    if (!aligned(codes, 8) || !aligned(scales, 2) || !aligned(out, 16)) return QPACK_ERR_ALIGN;
+    return cuda_status(launch_kv_dequant(codes, scales, n, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char *qpack_status_string(int status) {
     switch (status) {
         case QPACK_OK: return "QPACK_OK";

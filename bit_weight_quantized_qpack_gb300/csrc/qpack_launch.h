@@ -67,6 +67,9 @@ struct PrefillArgs {
 cudaError_t launch_prefill(int fmt, const PrefillArgs &a, cudaStream_t s);
 
 // Per-translation-unit device fault words (bounded waits that gave up). Read and cleared synchronously.
+// 8-bit KV cache (qpack_kv.cu); n a positive multiple of 32, pointers checked by the caller.
+cudaError_t launch_kv_quantize(const uint16_t *v, int64_t n, int8_t *q, uint16_t *scales, cudaStream_t s);
+cudaError_t launch_kv_dequant(const int8_t *q, const uint16_t *scales, int64_t n, uint16_t *out, cudaStream_t s);
 cudaError_t fetch_fault_gemv(int32_t *flags);
 cudaError_t fetch_fault_prefill(int32_t *flags);
 

@@ -150,6 +150,22 @@ int qgemm_small(int fmt, const uint8_t *packed, const float *group_scales, int64
 int qgemm_prefill(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, int64_t M,
                   const uint16_t *X, int64_t ldx, uint16_t *Y, int64_t ldy, qpack_stream_t stream);
 
+/* 8-bit KV cache (2/3/5/6-bit article §4.1: the KV cache in 8 bits with one fp16 scale per 32 elements, about
+ * 1.06 bytes per element instead of 2). Groups are 32 consecutive elements of the flat array.
+ *   d = fp16_rn(max|v| / 127) (fp32 division; the rounded d is the one used), q = clamp(rint(v / d), -127, 127),
+ *   q = 0 when d == 0.
+ *  v       [n] fp16 keys or values, 16-byte aligned; finite (non-finite inputs give unspecified codes, no fault)
+ *  codes   [n] int8 out, 8-byte aligned
+ *  scales  [n / 32] fp16 out, 2-byte aligned
+ *  n       a multiple of 32 (QPACK_ERR_SHAPE otherwise); 0 launches nothing
+ * Codes and scales are bit-identical to the oracle's. The caller owns every buffer. */
+int qpack_kv_quantize(const uint16_t *v, int64_t n, int8_t *codes, uint16_t *scales, qpack_stream_t stream);
+
+/* Inverse of qpack_kv_quantize (the Mix-Quant article §2.3: the int8 cache dequantized to fp16 in bulk):
+ *   out[i] = fp16_rn(d_g * q_i), g = i / 32 (the product is exact in fp32).
+ *  codes 8-byte aligned, scales 2-byte aligned, out [n] fp16 16-byte aligned; n a multiple of 32. */
+int qpack_kv_dequant(const int8_t *codes, const uint16_t *scales, int64_t n, uint16_t *out, qpack_stream_t stream);
+
 /* Human-readable name of a qpack_status value. Never NULL. */
 const char *qpack_status_string(int status);
 

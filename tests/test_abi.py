@@ -76,7 +76,14 @@ def test_argument_validation_rejects_before_launch(qp):
     assert L.qpack_quantize_pack(qp.Q2S, good, 7, 8, 256, good, None, None, None) == ARG
     assert L.qpack_quantize_pack(qp.Q2S, odd, 0, 8, 256, good, None, None, None) == ALIGN
     assert L.qpack_dequant(qp.Q6S, -1, 256, good, None, good, None) == ARG
+    assert L.qpack_kv_quantize(good, 48, good, good, None) == SHAPE
+    assert L.qpack_kv_quantize(good, 64, None, good, None) == ARG
+    assert L.qpack_kv_quantize(odd, 64, good, good, None) == ALIGN
+    assert L.qpack_kv_dequant(good, good, 64, odd, None) == ALIGN
+    assert L.qpack_kv_dequant(good, good, -32, good, None) == SHAPE
     # empty problems are accepted and launch nothing
+    assert L.qpack_kv_quantize(good, 0, good, good, None) == 0
+    assert L.qpack_kv_dequant(good, good, 0, good, None) == 0
     assert L.qgemv(qp.Q3S, good, None, 0, 4096, good, good, None) == 0
     assert L.qgemm_small(qp.Q3S, good, None, 8, 4096, 0, good, 4096, good, 8, None) == 0
 
