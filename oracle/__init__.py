@@ -18,8 +18,8 @@ import threading
 
 import numpy as np
 
-Q4G32, Q2S, Q3S, Q5S, Q6S = 0, 1, 2, 3, 4
-FORMATS = {"Q4G32": Q4G32, "Q2S": Q2S, "Q3S": Q3S, "Q5S": Q5S, "Q6S": Q6S}
+Q4G32, Q2S, Q3S, Q5S, Q6S, Q4G32H = 0, 1, 2, 3, 4, 5
+FORMATS = {"Q4G32": Q4G32, "Q2S": Q2S, "Q3S": Q3S, "Q5S": Q5S, "Q6S": Q6S, "Q4G32H": Q4G32H}
 FLAG_RANGE = 1
 
 # (bits, sub-blocks, weights per sub-block, Lmax, asymmetric, bytes per super-block) — P1 §2.3 byte table,
@@ -151,6 +151,31 @@ def unpack6x4(packed):
 # ---------------------------------------------------------------------------------------------------------
 # formats
 # ---------------------------------------------------------------------------------------------------------
+def _gs(fmt, group_scales):
+    """The INT4 group-scale array in its stored type: fp32 (Q4G32) or fp16 bit patterns (Q4G32H)."""
+    if group_scales is None:
+        return None
+    return _c(group_scales, np.uint16 if fmt == Q4G32H else np.float32)
+
+
+def _parts(fmt, N, K):
+    q = np.zeros((N, K), np.int8)
+    parts = dict(q=q, gscale=None, sub_scale=None, sub_min=None, d=None, dmin=None)
+    if fmt == Q4G32:
+        parts["gscale"] = np.zeros((N, K // 32), np.float32)
+    elif fmt == Q4G32H:
+        parts["d"] = np.zeros((N, K // 32), np.uint16)          # the fp16 group scales
+    else:
+        bits, nsub, sublen, lmax, asym, nbytes = SB[fmt]
+        nb = K // 256
+        parts["sub_scale"] = np.zeros((N, nb * nsub), np.uint8)
+        parts["d"] = np.zeros((N, nb), np.uint16)
+        if asym:
+            parts["sub_min"] = np.zeros((N, nb * nsub), np.uint8)
+            parts["dmin"] = np.zeros((N, nb), np.uint16)
+    return parts
+
+
 def layout(fmt, N, K):
     """dict(row_stride, packed_bytes, scale_stride, scale_bytes, block_bytes); raises ValueError on bad K."""
     out = np.zeros(5, np.int64)
@@ -162,21 +187,12 @@ def layout(fmt, N, K):
 
 
 def quantize(fmt, W):
-    """Quantize fp32 W [N, K] into unpacked parts: dict(q, gscale | sub_scale, sub_min, d, dmin, flags)."""
+    """Quantize fp32 W [N, K] into unpacked parts: dict(q, gscale | sub_scale, sub_min, d, dmin, flags); Q4G32H keeps
+    its fp16 group scales in d [N, K/32]."""
     W = _c(W, np.float32)
     N, K = W.shape
-    q = np.zeros((N, K), np.int8)
-    parts = dict(q=q, gscale=None, sub_scale=None, sub_min=None, d=None, dmin=None)
-    if fmt == Q4G32:
-        parts["gscale"] = np.zeros((N, K // 32), np.float32)
-    else:
-        bits, nsub, sublen, lmax, asym, nbytes = SB[fmt]
-        nb = K // 256
-        parts["sub_scale"] = np.zeros((N, nb * nsub), np.uint8)
-        parts["d"] = np.zeros((N, nb), np.uint16)
-        if asym:
-            parts["sub_min"] = np.zeros((N, nb * nsub), np.uint8)
-            parts["dmin"] = np.zeros((N, nb), np.uint16)
+    parts = _parts(fmt, N, K)
+    q = parts["q"]
     rc = lib().orc_quantize(int(fmt), _p(W), N, K, _p(q), _p(parts["gscale"]), _p(parts["sub_scale"]),
                             _p(parts["sub_min"]), _p(parts["d"]), _p(parts["dmin"]))
     if rc < 0:
@@ -186,10 +202,15 @@ def quantize(fmt, W):
 
 
 def pack(fmt, N, K, parts):
-    """Pack unpacked parts -> (packed uint8 [N, row_stride], group_scales fp32 [N, S] or None)."""
+    """Pack unpacked parts -> (packed uint8 [N, row_stride], group scales [N, S] (fp32 for Q4G32, fp16 bit patterns
+    for Q4G32H) or None)."""
     lay = layout(fmt, N, K)
     packed = np.zeros((N, lay["row_stride"]), np.uint8)
-    gs = np.zeros((N, lay["scale_stride"]), np.float32) if fmt == Q4G32 else None
+    gs = None
+    if fmt == Q4G32:
+        gs = np.zeros((N, lay["scale_stride"]), np.float32)
+    elif fmt == Q4G32H:
+        gs = np.zeros((N, lay["scale_stride"]), np.uint16)
     g = lambda k, dt: None if parts.get(k) is None else _c(parts[k], dt)
     rc = lib().orc_pack(int(fmt), N, K, _p(_c(parts["q"], np.int8)), _p(g("gscale", np.float32)),
                         _p(g("sub_scale", np.uint8)), _p(g("sub_min", np.uint8)), _p(g("d", np.uint16)),
@@ -201,19 +222,9 @@ def pack(fmt, N, K, parts):
 
 def unpack(fmt, N, K, packed, group_scales=None):
     packed = _c(packed, np.uint8)
-    gs = None if group_scales is None else _c(group_scales, np.float32)
-    q = np.zeros((N, K), np.int8)
-    parts = dict(q=q, gscale=None, sub_scale=None, sub_min=None, d=None, dmin=None)
-    if fmt == Q4G32:
-        parts["gscale"] = np.zeros((N, K // 32), np.float32)
-    else:
-        bits, nsub, sublen, lmax, asym, nbytes = SB[fmt]
-        nb = K // 256
-        parts["sub_scale"] = np.zeros((N, nb * nsub), np.uint8)
-        parts["d"] = np.zeros((N, nb), np.uint16)
-        if asym:
-            parts["sub_min"] = np.zeros((N, nb * nsub), np.uint8)
-            parts["dmin"] = np.zeros((N, nb), np.uint16)
+    gs = _gs(fmt, group_scales)
+    parts = _parts(fmt, N, K)
+    q = parts["q"]
     rc = lib().orc_unpack(int(fmt), N, K, _p(packed), _p(gs), _p(q), _p(parts["gscale"]), _p(parts["sub_scale"]),
                           _p(parts["sub_min"]), _p(parts["d"]), _p(parts["dmin"]))
     if rc != 0:
@@ -225,7 +236,7 @@ def dequant(fmt, N, K, packed, group_scales=None, r0=0, nrows=None):
     """fp32 dequantized rows [r0, r0 + nrows) of a packed matrix."""
     nrows = N - r0 if nrows is None else nrows
     out = np.zeros((nrows, K), np.float32)
-    gs = None if group_scales is None else _c(group_scales, np.float32)
+    gs = _gs(fmt, group_scales)
     rc = lib().orc_dequant_rows(int(fmt), N, K, _p(_c(packed, np.uint8)), _p(gs), r0, nrows, _p(out))
     if rc != 0:
         raise ValueError(f"orc_dequant_rows rc={rc}")
@@ -240,7 +251,7 @@ def gemm(fmt, N, K, packed, group_scales, X_f16_bits, r0=0, nrows=None, nthreads
     M = X.shape[0]
     nrows = N - r0 if nrows is None else nrows
     Y = np.zeros((M, nrows), np.float64)
-    gs = None if group_scales is None else _c(group_scales, np.float32)
+    gs = _gs(fmt, group_scales)
     rc = lib().orc_gemm_rows(int(fmt), N, K, _p(_c(packed, np.uint8)), _p(gs), M, _p(X), X.shape[1], r0, nrows,
                              _p(Y), int(nthreads))
     if rc != 0:
@@ -257,7 +268,7 @@ def prefill_sample(fmt, N, K, packed, group_scales, X_bf16_bits, ms, ns, round_w
     X = _c(X_bf16_bits, np.uint16)
     ms = _c(ms, np.int64); ns = _c(ns, np.int64)
     out = np.zeros(ms.size, np.float64)
-    gs = None if group_scales is None else _c(group_scales, np.float32)
+    gs = _gs(fmt, group_scales)
     rc = lib().orc_prefill_sample(int(fmt), N, K, _p(_c(packed, np.uint8)), _p(gs), _p(X), X.shape[1], X.shape[0],
                                   _p(ms), _p(ns), ms.size, int(bool(round_w)), _p(out))
     if rc != 0:

@@ -104,7 +104,7 @@ float bf16_to_f32(uint16_t b) { return bits_f32(uint32_t(b) << 16); }
 // Format descriptions (P1 §2.3 byte table; P2 §3.2 / §4.1 for INT4).
 // ----------------------------------------------------------------------------------------------------------
 
-enum { Q4G32 = 0, Q2S = 1, Q3S = 2, Q5S = 3, Q6S = 4 };
+enum { Q4G32 = 0, Q2S = 1, Q3S = 2, Q5S = 3, Q6S = 4, Q4G32H = 5 };
 
 struct SbFormat {
     int bits;      // code width b
@@ -184,6 +184,29 @@ void quantize_q4g32_row(const float *w, int64_t K, int8_t *q, float *scales) {
         }
         scales[g] = scale;
     }
+}
+
+// INT4 group-32 with an fp16 group scale (P1 §2.1: an fp16 scale per 32 weights costs 0.5 bpw, so 4.5 bpw). Reading
+// (the P2 rule with the scale stored in fp16, used rounded as the super-block formats use d): s = max|w| / 8 in
+// fp32, s16 = fp16(s), D = s16 as fp32; q = D > 0 ? clamp(rint(w / D), -8, 7) : 0 (no 1e-12 floor: a scale that
+// rounds to 0 gives zero codes). Returns the RANGE flag if s16 overflows.
+int quantize_q4g32h_row(const float *w, int64_t K, int8_t *q, uint16_t *scales) {
+    int flags = 0;
+    for (int64_t g = 0; g < K / 32; ++g) {
+        const float *wg = w + 32 * g;
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) amax = std::fmax(amax, std::fabs(wg[i]));
+        const uint16_t s16 = f32_to_f16(amax / 8.0f);
+        const float D = f16_to_f32(s16);
+        if ((s16 & 0x7FFFu) == 0x7C00u) flags |= 1;
+        for (int i = 0; i < 32; ++i) {
+            float t = 0.0f;
+            if (D > 0.0f) t = clampf(std::nearbyint(wg[i] / D), -8.0f, 7.0f);
+            q[32 * g + i] = int8_t(t);
+        }
+        scales[g] = s16;
+    }
+    return flags;
 }
 
 // Two-level round-to-nearest super-block quantizer (P1 §2.1 "fp16 super-block scale -> low-bit sub-block
@@ -378,12 +401,13 @@ void dequant_sb(const SbFormat &F, int fmt, const int8_t *q, const uint8_t *L, c
 // Dequantize row r of a packed matrix into out[K].
 void dequant_row(int fmt, const uint8_t *packed, const float *gs, int64_t K, int64_t r, int64_t row_stride,
                  int64_t scale_stride, float *out) {
-    if (fmt == Q4G32) {
+    if (fmt == Q4G32 || fmt == Q4G32H) {
         const uint8_t *row = packed + r * row_stride;
+        const uint16_t *gs16 = reinterpret_cast<const uint16_t *>(gs);
         for (int64_t k = 0; k < K; ++k) {
             uint8_t byte = row[k >> 1];
             int u = (k & 1) ? (byte >> 4) : (byte & 15);
-            float s = gs[r * scale_stride + k / 32];
+            float s = fmt == Q4G32 ? gs[r * scale_stride + k / 32] : f16_to_f32(gs16[r * scale_stride + k / 32]);
             out[k] = s * float(u - 8);
         }
         return;
@@ -400,7 +424,7 @@ void dequant_row(int fmt, const uint8_t *packed, const float *gs, int64_t K, int
 
 bool shape_ok(int fmt, int64_t N, int64_t K) {
     if (N < 0 || K < 0) return false;
-    if (fmt == Q4G32) return K % 32 == 0;
+    if (fmt == Q4G32 || fmt == Q4G32H) return K % 32 == 0;
     SbFormat F;
     if (!sb_format(fmt, &F)) return false;
     return K % 256 == 0;
@@ -424,8 +448,9 @@ void orc_unpack5(const uint8_t *p, uint8_t *q, int64_t ngroups) { for (int64_t g
 void orc_pack6x4(const uint8_t *f, uint8_t *p, int64_t ngroups) { for (int64_t g = 0; g < ngroups; ++g) pack6x4(f + 4 * g, p + 3 * g); }
 void orc_unpack6x4(const uint8_t *p, uint8_t *f, int64_t ngroups) { for (int64_t g = 0; g < ngroups; ++g) unpack6x4(p + 3 * g, f + 4 * g); }
 
-// Layout: out[0] = packed row stride (bytes), out[1] = packed bytes, out[2] = Q4G32 scale row stride
-// (floats, 0 otherwise), out[3] = Q4G32 scale bytes (0 otherwise), out[4] = super-block bytes (0 for Q4G32).
+// Layout: out[0] = packed row stride (bytes), out[1] = packed bytes, out[2] = INT4 scale row stride (elements:
+// fp32 for Q4G32, fp16 for Q4G32H, rows padded to 16 bytes; 0 otherwise), out[3] = INT4 scale bytes (0
+// otherwise), out[4] = super-block bytes (0 for the INT4 formats).
 // Returns 0, or -2 for a shape the format does not accept.
 int orc_layout(int fmt, int64_t N, int64_t K, int64_t *out) {
     if (!shape_ok(fmt, N, K)) return -2;
@@ -434,6 +459,14 @@ int orc_layout(int fmt, int64_t N, int64_t K, int64_t *out) {
         out[1] = N * (K / 2);
         out[2] = round_up(K / 32, 4);
         out[3] = N * out[2] * 4;
+        out[4] = 0;
+        return 0;
+    }
+    if (fmt == Q4G32H) {
+        out[0] = K / 2;
+        out[1] = N * (K / 2);
+        out[2] = round_up(K / 32, 8);
+        out[3] = N * out[2] * 2;
         out[4] = 0;
         return 0;
     }
@@ -447,7 +480,8 @@ int orc_layout(int fmt, int64_t N, int64_t K, int64_t *out) {
     return 0;
 }
 
-// Quantize W (fp32, [N][K]) into unpacked parts. Q4G32 writes q and gscale [N][K/32]; super-block formats
+// Quantize W (fp32, [N][K]) into unpacked parts. Q4G32 writes q and gscale [N][K/32]; Q4G32H writes q and its
+// fp16 group scales into d [N][K/32]; super-block formats
 // write q, sub_scale [N][nb*nsub], sub_min (asymmetric only), d and dmin [N][nb]. Returns flags (1 = RANGE)
 // or -2 for a bad shape.
 int orc_quantize(int fmt, const float *W, int64_t N, int64_t K, int8_t *q, float *gscale, uint8_t *sub_scale,
@@ -457,6 +491,10 @@ int orc_quantize(int fmt, const float *W, int64_t N, int64_t K, int8_t *q, float
     if (fmt == Q4G32) {
         for (int64_t r = 0; r < N; ++r) quantize_q4g32_row(W + r * K, K, q + r * K, gscale + r * (K / 32));
         return 0;
+    }
+    if (fmt == Q4G32H) {
+        for (int64_t r = 0; r < N; ++r) flags |= quantize_q4g32h_row(W + r * K, K, q + r * K, d + r * (K / 32));
+        return flags;
     }
     SbFormat F;
     sb_format(fmt, &F);
@@ -474,15 +512,18 @@ int orc_pack(int fmt, int64_t N, int64_t K, const int8_t *q, const float *gscale
     int64_t lay[5];
     if (orc_layout(fmt, N, K, lay)) return -2;
     std::memset(packed, 0, size_t(lay[1]));
-    if (fmt == Q4G32) {
+    if (fmt == Q4G32 || fmt == Q4G32H) {
+        uint16_t *gs16 = reinterpret_cast<uint16_t *>(group_scales);
         for (int64_t r = 0; r < N; ++r) {
             uint8_t *row = packed + r * lay[0];
             for (int64_t j = 0; j < K / 2; ++j) {
                 uint8_t u0 = uint8_t(q[r * K + 2 * j] + 8), u1 = uint8_t(q[r * K + 2 * j + 1] + 8);
                 row[j] = uint8_t((u0 & 15u) | ((u1 & 15u) << 4));
             }
-            for (int64_t g = 0; g < lay[2]; ++g)
-                group_scales[r * lay[2] + g] = (g < K / 32) ? gscale[r * (K / 32) + g] : 0.0f;
+            for (int64_t g = 0; g < lay[2]; ++g) {
+                if (fmt == Q4G32) group_scales[r * lay[2] + g] = (g < K / 32) ? gscale[r * (K / 32) + g] : 0.0f;
+                else gs16[r * lay[2] + g] = (g < K / 32) ? d[r * (K / 32) + g] : uint16_t(0);
+            }
         }
         return 0;
     }
@@ -504,7 +545,8 @@ int orc_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float
                float *gscale, uint8_t *sub_scale, uint8_t *sub_min, uint16_t *d, uint16_t *dmin) {
     int64_t lay[5];
     if (orc_layout(fmt, N, K, lay)) return -2;
-    if (fmt == Q4G32) {
+    if (fmt == Q4G32 || fmt == Q4G32H) {
+        const uint16_t *gs16 = reinterpret_cast<const uint16_t *>(group_scales);
         for (int64_t r = 0; r < N; ++r) {
             const uint8_t *row = packed + r * lay[0];
             for (int64_t k = 0; k < K; ++k) {
@@ -512,7 +554,10 @@ int orc_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float
                 uint8_t u = (k & 1) ? uint8_t(byte >> 4) : uint8_t(byte & 15u);
                 q[r * K + k] = int8_t(int(u) - 8);
             }
-            for (int64_t g = 0; g < K / 32; ++g) gscale[r * (K / 32) + g] = group_scales[r * lay[2] + g];
+            for (int64_t g = 0; g < K / 32; ++g) {
+                if (fmt == Q4G32) gscale[r * (K / 32) + g] = group_scales[r * lay[2] + g];
+                else d[r * (K / 32) + g] = gs16[r * lay[2] + g];
+            }
         }
         return 0;
     }
