@@ -236,13 +236,14 @@ def _time_graph(torch, fn, dev, reps=5, warm=3):
 DP2A_TOPS = 152 * 60 * 2 * 2 * 2.07e9 / 1e12
 
 
-def int4_4096_extra(qp, torch, synth, dev, hbm_peak):
-    """INT4 group-32 GEMV on the 4096x4096 matrix with 0.1% outliers (the INT4 workload), batch 1."""
-    N = K = 4096
+def int4_4096_extra(qp, torch, synth, dev, hbm_peak, fmt=None, N=4096, K=4096):
+    """INT4 group-32 GEMV on the 4096x4096 matrix with 0.1% outliers (the INT4 workload), batch 1; also used for the
+    fp16-scale variant and other shapes."""
+    fmt = qp.Q4G32 if fmt is None else fmt
     W = synth.normal_with_outliers((N, K), 0.02, 0.001, 0.1, 0.5, seed=0).to(dev)
-    p0, g0 = qp.qpack_quantize_pack(qp.Q4G32, W)
+    p0, g0 = qp.qpack_quantize_pack(fmt, W)
     del W
-    wb = qp.layout(qp.Q4G32, N, K)["weight_bytes"]
+    wb = qp.layout(fmt, N, K)["weight_bytes"]
     R = max(8, int(-(-8 * (126 << 20) // wb)))
     P = [p0.clone() for _ in range(R)]
     G = [g0.clone() for _ in range(R)]
@@ -251,7 +252,7 @@ def int4_4096_extra(qp, torch, synth, dev, hbm_peak):
 
     def fn(s):
         for i in range(R):
-            qp.qgemv(qp.Q4G32, P[i], G[i], N, K, X[i], Y[i], stream=s)
+            qp.qgemv(fmt, P[i], G[i], N, K, X[i], Y[i], stream=s)
 
     t = _time_graph(torch, fn, dev, reps=20) / R
     return {"GBps": wb / t / 1e9, "pct_hbm_peak": wb / t / 1e9 / hbm_peak, "us_per_gemv": t * 1e6,
@@ -502,6 +503,9 @@ def run_ours(args, world, rank, local):
             extra = {"decode_7b": decode_7b_extra(qp, torch, synth, dev),
                      "decode_7b_mixed": mixed_7b_extra(qp, torch, synth, dev),
                      "int4_4096": int4_4096_extra(qp, torch, synth, dev, hbm_peak),
+                     "int4_fp16_scales": {
+                         "4096x4096": int4_4096_extra(qp, torch, synth, dev, hbm_peak, qp.Q4G32H),
+                         "28672x8192": int4_4096_extra(qp, torch, synth, dev, hbm_peak, qp.Q4G32H, 28672, 8192)},
                      "small_batch_70b_mlp": small_batch_extra(qp, torch, synth, dev, hbm_peak),
                      "prefill_2048": prefill_extra(qp, torch, synth, dev, bf16_peak, hbm_peak),
                      "kv_cache_8bit": kv_cache_extra(qp, torch, synth, dev, hbm_peak)}
@@ -556,6 +560,13 @@ def run_ncu_case(args):
         return 0
     fmt = qp.FORMATS[args.fmt]
     N, K = args.N, args.K
+    if args.ncu_case == "quant":
+        W16 = synth.laplace((N, K), 0.02, seed=7, device=dev).half()
+        for _ in range(3):
+            qp.qpack_quantize_pack(fmt, W16)
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_case": "quant", "fmt": args.fmt, "N": N, "K": K, "faults": qp.qpack_fetch_fault_flags()}))
+        return 0
     W = synth.laplace((N, K), 0.02, seed=1, device=dev)
     p0, g0 = qp.qpack_quantize_pack(fmt, W)
     del W
@@ -593,7 +604,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 7B decode-step extra")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true", help="disable QPACK_OPT_WEIGHT_PREFETCH")
-    ap.add_argument("--ncu-case", choices=["gemv", "small", "prefill", "kv"], default=None,
+    ap.add_argument("--ncu-case", choices=["gemv", "small", "prefill", "kv", "quant"], default=None,
                     help="short run of one product for an ncu capture (see profiles/)")
     ap.add_argument("--fmt", default="Q3S")
     ap.add_argument("--N", type=int, default=N_ROWS)

@@ -49,7 +49,8 @@ namespace {
 
 using namespace qpack;
 
-bool fmt_ok(int fmt) { return fmt >= QPACK_Q4G32 && fmt <= QPACK_Q6S; }
+bool fmt_ok(int fmt) { return fmt >= QPACK_Q4G32 && fmt <= QPACK_Q4G32H; }
+bool is_int4_fmt(int fmt) { return fmt == QPACK_Q4G32 || fmt == QPACK_Q4G32H; }
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct FmtInfo { int bytes, nsub; bool asym; };
@@ -65,12 +66,13 @@ FmtInfo info(int fmt) {
 
 int layout(int fmt, int64_t N, int64_t K, qpack_layout_t *o) {
     if (!fmt_ok(fmt) || N < 0 || K < 0 || !o) return QPACK_ERR_ARG;
-    if (fmt == QPACK_Q4G32) {
+    if (is_int4_fmt(fmt)) {
         if (K == 0 || K % 32) return QPACK_ERR_SHAPE;
+        const int64_t es = fmt == QPACK_Q4G32 ? 4 : 2;    // fp32 or fp16 group scales, rows padded to 16 bytes
         o->row_stride = K / 2;
         o->packed_bytes = N * o->row_stride;
-        o->scale_stride = round_up(K / 32, 4);
-        o->scale_bytes = N * o->scale_stride * 4;
+        o->scale_stride = round_up(K / 32, 16 / es);
+        o->scale_bytes = N * o->scale_stride * es;
         o->block_bytes = 0;
         o->nsub = K / 32;
     } else {
@@ -106,6 +108,9 @@ int check_parts(int fmt, const void *codes, const void *gscale, const void *sub_
     if (fmt == QPACK_Q4G32) {
         if (!gscale) return QPACK_ERR_ARG;
         if (!aligned(gscale, 4)) return QPACK_ERR_ALIGN;
+    } else if (fmt == QPACK_Q4G32H) {                      // the fp16 group scales travel in d
+        if (!d) return QPACK_ERR_ARG;
+        if (!aligned(d, 2)) return QPACK_ERR_ALIGN;
     } else {
         const FmtInfo f = info(fmt);
         if (!sub_scale || !d) return QPACK_ERR_ARG;
@@ -118,7 +123,7 @@ int check_parts(int fmt, const void *codes, const void *gscale, const void *sub_
 int check_packed(int fmt, const void *packed, const void *gs) {
     if (!packed) return QPACK_ERR_ARG;
     if (!aligned(packed, 16)) return QPACK_ERR_ALIGN;
-    if (fmt == QPACK_Q4G32) {
+    if (is_int4_fmt(fmt)) {
         if (!gs) return QPACK_ERR_ARG;
         if (!aligned(gs, 16)) return QPACK_ERR_ALIGN;
     }
@@ -156,7 +161,7 @@ int qpack_quantize(int fmt, const void *W, int wdt, int64_t N, int64_t K, int8_t
 
 int qpack_pack(int fmt, int64_t N, int64_t K, const int8_t *codes, const float *gscale, const uint8_t *sub_scale,
                const uint8_t *sub_min, const uint16_t *d, const uint16_t *dmin, uint8_t *packed,
-               float *group_scales, qpack_stream_t stream) {
+               void *group_scales, qpack_stream_t stream) {
     qpack_layout_t L;
     int rc = layout(fmt, N, K, &L);
     if (rc) return rc;
@@ -171,12 +176,12 @@ int qpack_pack(int fmt, int64_t N, int64_t K, const int8_t *codes, const float *
     a.d = const_cast<uint16_t *>(d);
     a.dmin = const_cast<uint16_t *>(dmin);
     a.packed = packed;
-    a.gs_out = group_scales;
+    a.gs_out = static_cast<float *>(group_scales);
     return cuda_status(launch_block_op(fmt, 2, QPACK_F32, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int qpack_quantize_pack(int fmt, const void *W, int wdt, int64_t N, int64_t K, uint8_t *packed,
-                        float *group_scales, int32_t *status, qpack_stream_t stream) {
+                        void *group_scales, int32_t *status, qpack_stream_t stream) {
     qpack_layout_t L;
     int rc = layout(fmt, N, K, &L);
     if (rc) return rc;
@@ -187,12 +192,12 @@ int qpack_quantize_pack(int fmt, const void *W, int wdt, int64_t N, int64_t K, u
     BlockArgs a = base_args(N, K, L);
     a.W = W;
     a.packed = packed;
-    a.gs_out = group_scales;
+    a.gs_out = static_cast<float *>(group_scales);
     a.status = status;
     return cuda_status(launch_block_op(fmt, 1, wdt, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int qpack_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float *group_scales, int8_t *codes,
+int qpack_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const void *group_scales, int8_t *codes,
                  float *gscale, uint8_t *sub_scale, uint8_t *sub_min, uint16_t *d, uint16_t *dmin,
                  qpack_stream_t stream) {
     qpack_layout_t L;
@@ -203,7 +208,7 @@ int qpack_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const flo
     if (N == 0) return QPACK_OK;
     BlockArgs a = base_args(N, K, L);
     a.packed_in = packed;
-    a.gs_in = group_scales;
+    a.gs_in = static_cast<const float *>(group_scales);
     a.codes = codes;
     a.gscale = gscale;
     a.sub_scale = sub_scale;
@@ -213,7 +218,7 @@ int qpack_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const flo
     return cuda_status(launch_block_op(fmt, 3, QPACK_F32, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float *group_scales, float *out,
+int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const void *group_scales, float *out,
                   qpack_stream_t stream) {
     qpack_layout_t L;
     int rc = layout(fmt, N, K, &L);
@@ -224,12 +229,12 @@ int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const fl
     if (N == 0) return QPACK_OK;
     BlockArgs a = base_args(N, K, L);
     a.packed_in = packed;
-    a.gs_in = group_scales;
+    a.gs_in = static_cast<const float *>(group_scales);
     a.out = out;
     return cuda_status(launch_block_op(fmt, 4, QPACK_F32, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int qgemm_small(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, int M,
+int qgemm_small(int fmt, const uint8_t *packed, const void *group_scales, int64_t N, int64_t K, int M,
                 const uint16_t *X, int64_t ldx, float *Y, int64_t ldy, qpack_stream_t stream) {
     qpack_layout_t L;
     int rc = layout(fmt, N, K, &L);
@@ -242,7 +247,7 @@ int qgemm_small(int fmt, const uint8_t *packed, const float *group_scales, int64
     if (N == 0 || M == 0) return QPACK_OK;
     GemvArgs a = {};
     a.packed = packed;
-    a.gscale = group_scales;
+    a.gscale = static_cast<const float *>(group_scales);
     a.N = N;
     a.K = K;
     a.row_stride = L.row_stride;
@@ -256,26 +261,26 @@ int qgemm_small(int fmt, const uint8_t *packed, const float *group_scales, int64
     return cuda_status(launch_gemv(fmt, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int qgemv(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, const uint16_t *x,
+int qgemv(int fmt, const uint8_t *packed, const void *group_scales, int64_t N, int64_t K, const uint16_t *x,
           float *y, qpack_stream_t stream) {
     return qgemm_small(fmt, packed, group_scales, N, K, 1, x, K, y, N, stream);
 }
 
-int qgemm_prefill(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, int64_t M,
+int qgemm_prefill(int fmt, const uint8_t *packed, const void *group_scales, int64_t N, int64_t K, int64_t M,
                   const uint16_t *X, int64_t ldx, uint16_t *Y, int64_t ldy, qpack_stream_t stream) {
     qpack_layout_t L;
     int rc = layout(fmt, N, K, &L);
     if (rc) return rc;
     if ((rc = check_packed(fmt, packed, group_scales))) return rc;
     if (M < 0) return QPACK_ERR_SHAPE;
-    if (fmt == QPACK_Q4G32 && K % 64) return QPACK_ERR_SHAPE;
+    if (is_int4_fmt(fmt) && K % 64) return QPACK_ERR_SHAPE;
     if (!X || !Y) return QPACK_ERR_ARG;
     if (ldx < K || ldy < N) return QPACK_ERR_SHAPE;
     if (!aligned(X, 16) || (ldx % 8) || !aligned(Y, 2)) return QPACK_ERR_ALIGN;
     if (N == 0 || M == 0) return QPACK_OK;
     PrefillArgs a = {};
     a.packed = packed;
-    a.gscale = group_scales;
+    a.gscale = static_cast<const float *>(group_scales);
     a.N = N;
     a.K = K;
     a.M = M;

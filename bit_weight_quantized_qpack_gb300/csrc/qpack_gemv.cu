@@ -80,7 +80,7 @@ __device__ __forceinline__ int32_t dp2a_hi(uint32_t a, uint32_t b, int32_t c) {
 template <int F>
 __host__ __device__ constexpr int dp_elem(int a, int e) {
     const int w = a >> 1, h = a & 1;
-    if constexpr (F == FMT_Q4G32 || F == FMT_Q5S) {
+    if constexpr (kInt4<F> || F == FMT_Q5S) {
         // word 2j + p: byte b holds weight 8j + 2b + p (p = 0: the low nibbles of code word j, p = 1: the high ones)
         return 8 * (w >> 1) + (w & 1) + 4 * h + 2 * e;
     } else if constexpr (F == FMT_Q3S) {
@@ -101,6 +101,7 @@ __host__ __device__ constexpr int dp_elem(int a, int e) {
 // Sx_j = the sum of the staged activations of sub-block j.
 template <int F> struct XC;
 template <> struct XC<FMT_Q4G32> { static constexpr int n = 2; };   // int -128 Sx, XS / 16
+template <> struct XC<FMT_Q4G32H> { static constexpr int n = 2; };  // as Q4G32
 template <> struct XC<FMT_Q2S> { static constexpr int n = 3; };     // Sx_0 XS, Sx_1 XS, XS
 template <> struct XC<FMT_Q3S> { static constexpr int n = 3; };     // int -128 Sx_0, int -128 Sx_1, XS / 32
 template <> struct XC<FMT_Q5S> { static constexpr int n = 2; };     // Sx XS, XS
@@ -127,7 +128,7 @@ template <int F>
 __device__ __forceinline__ LaneGeo lane_geo(int uc) {
     LaneGeo g = {};
     const uint32_t sbk = uint32_t(uc) >> 3, su = uint32_t(uc) & 7u;
-    if constexpr (F == FMT_Q4G32) {
+    if constexpr (kInt4<F>) {
         g.ubase = 16u * uc;
     } else if constexpr (F == FMT_Q2S) {
         g.ubase = 84u * sbk + 8u * su;
@@ -192,11 +193,13 @@ __device__ __forceinline__ void unpack_six_dp(uint32_t A, uint32_t B, uint32_t H
 // `on` false zeroes its scale factors (a masked lane or row). Sub-block scale integers become exact fp16 values with
 // the 1024 mantissa trick and are multiplied by the raw fp16 super-block scale with exact fp16 x fp16 -> fp32 products.
 template <int F>
-__device__ __forceinline__ void unpack_dp(const uint8_t *u, const float *sp, const LaneGeo &g, bool on, DRow &r) {
+__device__ __forceinline__ void unpack_dp(const uint8_t *u, const uint8_t *sp, const LaneGeo &g, bool on, DRow &r) {
     r.f1 = r.g0 = r.g1 = 0.f;
-    if constexpr (F == FMT_Q4G32) {
+    if constexpr (kInt4<F>) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
-        r.f0 = on ? sp[0] : 0.f;
+        // the unit's group scale: fp32 (Q4G32) or fp16 (Q4G32H) at sp
+        if constexpr (F == FMT_Q4G32) r.f0 = on ? *reinterpret_cast<const float *>(sp) : 0.f;
+        else r.f0 = on ? h2f_bits(*reinterpret_cast<const uint16_t *>(sp)) : 0.f;
         const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) { r.v[2 * j] = wv[j] & 0x0F0F0F0Fu; r.v[2 * j + 1] = wv[j] & 0xF0F0F0F0u; }
@@ -269,7 +272,7 @@ __device__ __forceinline__ void unpack_dp(const uint8_t *u, const float *sp, con
 // unit constants).
 template <int F>
 __device__ __forceinline__ void dot_dp(const DRow &r, const uint32_t *xv, const float *c, float &acc) {
-    if constexpr (F == FMT_Q4G32) {
+    if constexpr (kInt4<F>) {
         // lo: even weights at class 0; hi: odd weights at class 4, starting at -128 Sx (the code offset 8) -> 16 sum q x
         int32_t lo = 0, hi = __float_as_int(c[0]);
 #pragma unroll
@@ -387,7 +390,7 @@ __device__ __forceinline__ void stage_unit(const uint4 (&raw)[4], uint4 *xs, flo
     for (int t = 0; t < 4; ++t) xs[t * U + u] = make_uint4(st[4 * t], st[4 * t + 1], st[4 * t + 2], st[4 * t + 3]);
     float *c = cst + u * XC<F>::n;
     const float XS = exp2i(-E);
-    if constexpr (F == FMT_Q4G32) {
+    if constexpr (kInt4<F>) {
         c[0] = __int_as_float(-128 * (s0 + s1));
         c[1] = exp2i(-E - 4);
     } else if constexpr (F == FMT_Q2S) {
@@ -463,11 +466,12 @@ template <int F, int MT = 1> struct T1 {
     static constexpr int UPC = CHW / 32;                                          // units per chunk
     static constexpr int P = UPC / 32;                                            // K parts of 32 units
     static constexpr int RC = G1_CW / P;                                          // row classes
-    static constexpr int RW = MT > 4 ? 2 : MT > 2 ? 4 : (F == FMT_Q4G32 ? 4 : (P == 4 ? 8 : 4)); // rows per warp and stage
+    static constexpr int RW = MT > 4 ? 2 : MT > 2 ? 4 : (kInt4<F> ? 4 : (P == 4 ? 8 : 4)); // rows per warp and stage
     static constexpr int TR = RC * RW;                                            // rows per tile
     static constexpr int PR = MT > 1 ? (256 / MT > TR ? 256 / MT : TR) : 256;     // rows per partial-sum round
     static constexpr int CB = Fmt<F>::sb ? (CHW / 256) * Fmt<F>::bytes : CHW / 2; // code bytes per row chunk
-    static constexpr int SB = Fmt<F>::sb ? 0 : (CHW / 32) * 4;                    // Q4G32 scale bytes per row chunk
+    static constexpr int SE = F == FMT_Q4G32H ? 2 : 4;                            // INT4 group-scale element bytes
+    static constexpr int SB = Fmt<F>::sb ? 0 : (CHW / 32) * SE;                   // INT4 scale bytes per row chunk
     static constexpr int TX = TR * (CB + SB);                                     // bytes a stage receives
     static constexpr int STAGE = (TX + 127) / 128 * 128;
     static_assert(CB % 16 == 0 && CB / 8 <= 256 && SB / 8 <= 256, "tensor-map box limits");
@@ -608,7 +612,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
         if (!dead) {
             const uint8_t *st = stages + s * uint32_t(T::STAGE);
             const uint8_t *ub = st + rc * CB + geo.ubase;
-            const float *sp = reinterpret_cast<const float *>(st + TR * CB + rc * SB) + uc;
+            const uint8_t *sp = st + TR * CB + rc * SB + uc * T::SE;   // INT4: this lane's group scale of row rc
             const uint32_t u = c * UPC + uc;
             const bool uv = u < U;
             const uint32_t uu = uv ? u : U - 1;
@@ -623,7 +627,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < RW; ++i) {
                         DRow dr;
-                        unpack_dp<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, true, dr);
+                        unpack_dp<F>(ub + i * RC * CB, sp + i * RC * SB, geo, true, dr);
                         dot_dp<F>(dr, xv, cv, acc[i]);
                     }
                 } else {
@@ -632,7 +636,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                     for (int i = 0; i < RW; ++i)
                         if (rc + uint32_t(RC * i) < rows) {
                             DRow dr;
-                            unpack_dp<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, uv, dr);
+                            unpack_dp<F>(ub + i * RC * CB, sp + i * RC * SB, geo, uv, dr);
                             dot_dp<F>(dr, xv, cv, acc[i]);
                         }
                 }
@@ -648,7 +652,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 for (int i = 0; i < RW; ++i) {
                     if (full_tile || rc + uint32_t(RC * i) < rows) {
                         DRow ur;
-                        unpack_dp<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo, full_tile || uv, ur);
+                        unpack_dp<F>(ub + i * RC * CB, sp + i * RC * SB, geo, full_tile || uv, ur);
                         dot_dp<F>(ur, xv0, cv0, acc[2 * i]);
                         dot_dp<F>(ur, xv1, cv1, acc[2 * i + 1]);
                     }
@@ -658,7 +662,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 DRow ur[RW];
 #pragma unroll
                 for (int i = 0; i < RW; ++i)
-                    unpack_dp<F>(ub + i * RC * CB, sp + i * RC * (SB / 4), geo,
+                    unpack_dp<F>(ub + i * RC * CB, sp + i * RC * SB, geo,
                                   full_tile || (uv && rc + uint32_t(RC * i) < rows), ur[i]);
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
@@ -781,7 +785,7 @@ static cudaError_t launch_gemv_mt(const GemvArgs &a, const G1Plan &pl, cudaStrea
     cudaError_t e = encode_rows(&tmc, a.packed, a.N, a.row_stride, uint32_t(T::CB / 8), uint32_t(T::TR));
     if (e != cudaSuccess) return e;
     if constexpr (T::SB > 0) {
-        e = encode_rows(&tms, a.gscale, a.N, a.scale_stride * 4, uint32_t(T::SB / 8), uint32_t(T::TR));
+        e = encode_rows(&tms, a.gscale, a.N, a.scale_stride * T::SE, uint32_t(T::SB / 8), uint32_t(T::TR));
         if (e != cudaSuccess) return e;
     } else {
         tms = tmc;
@@ -865,6 +869,7 @@ static cudaError_t launch_fmt(const GemvArgs &a, cudaStream_t s) {
 cudaError_t launch_gemv(int fmt, const GemvArgs &a, cudaStream_t s) {
     switch (fmt) {
         case FMT_Q4G32: return launch_fmt<FMT_Q4G32>(a, s);
+        case FMT_Q4G32H: return launch_fmt<FMT_Q4G32H>(a, s);
         case FMT_Q2S: return launch_fmt<FMT_Q2S>(a, s);
         case FMT_Q3S: return launch_fmt<FMT_Q3S>(a, s);
         case FMT_Q5S: return launch_fmt<FMT_Q5S>(a, s);

@@ -142,11 +142,13 @@ struct RawUnit {
     uint32_t e[4];      // high-bit planes / scale fields / super-block scales
 };
 template <int F>
-__device__ __forceinline__ void load_raw(const uint8_t *row, const float *gs_row, uint32_t u, RawUnit &r) {
-    if constexpr (F == FMT_Q4G32) {
+__device__ __forceinline__ void load_raw(const uint8_t *row, const uint8_t *gs_row, uint32_t u, RawUnit &r) {
+    if constexpr (kInt4<F>) {
         const uint4 c = __ldg(reinterpret_cast<const uint4 *>(row + 16 * u));
         r.c[0] = c.x; r.c[1] = c.y; r.c[2] = c.z; r.c[3] = c.w;
-        r.e[0] = __float_as_uint(__ldg(gs_row + u));
+        // the group scale as fp32 bits: stored fp32 (Q4G32) or fp16 widened exactly (Q4G32H)
+        if constexpr (F == FMT_Q4G32) r.e[0] = __float_as_uint(__ldg(reinterpret_cast<const float *>(gs_row) + u));
+        else r.e[0] = __float_as_uint(h2f_bits(uint16_t(ldg16(gs_row + 2 * u))));
     } else {
         const uint32_t b = u >> 3, su = u & 7u;
         const uint8_t *blk = row + b * Fmt<F>::bytes;
@@ -182,7 +184,7 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 template <int F>
 __device__ __forceinline__ void unit_bf16(const RawUnit &r, uint32_t u, uint32_t out[16]) {
     float w[32];
-    if constexpr (F == FMT_Q4G32) {
+    if constexpr (kInt4<F>) {
         const float sc = __uint_as_float(r.e[0]);
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = __fmul_rn(sc, float(int((r.c[i >> 3] >> (4 * (i & 7))) & 15u) - 8));
@@ -283,7 +285,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         const int r = tid & (BN - 1), h = tid / BN;                         // weight row, K half of the stage
         const int64_t n = n0 + r;
         const uint8_t *row = a.packed + n * a.row_stride;
-        const float *gs_row = a.gscale ? a.gscale + n * a.scale_stride : nullptr;
+        constexpr int64_t SE = F == FMT_Q4G32H ? 2 : 4;                   // INT4 group-scale element bytes
+        const uint8_t *gs_row = a.gscale ? reinterpret_cast<const uint8_t *>(a.gscale) + n * a.scale_stride * SE : nullptr;
         // The raw bytes of step k + 3 are loaded while step k is converted and stored: four register slots in fixed
         // roles (the loop is unrolled by four), so no slot is copied while its loads are in flight.
         RawUnit S0 = {}, S1 = {}, S2 = {}, S3 = {};
@@ -476,6 +479,7 @@ static cudaError_t launch_prefill_f(const PrefillArgs &a, cudaStream_t s) {
 cudaError_t launch_prefill(int fmt, const PrefillArgs &a, cudaStream_t s) {
     switch (fmt) {
         case FMT_Q4G32: return launch_prefill_f<FMT_Q4G32>(a, s);
+        case FMT_Q4G32H: return launch_prefill_f<FMT_Q4G32H>(a, s);
         case FMT_Q2S: return launch_prefill_f<FMT_Q2S>(a, s);
         case FMT_Q3S: return launch_prefill_f<FMT_Q3S>(a, s);
         case FMT_Q5S: return launch_prefill_f<FMT_Q5S>(a, s);

@@ -66,6 +66,25 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
         B.L = B.M = 0;
         B.d16 = B.dm16 = 0;
         return 0;
+    } else if constexpr (F == FMT_Q4G32H) {
+        // P2's rule with the fp16-rounded scale (FORMATS.md §1b)
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
+        a = sub_reduce_max<F>(a);
+        const uint16_t s16 = f2h_bits(__fdiv_rn(a, 8.0f));
+        const float D = h2f_bits(s16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float t = 0.0f;
+            if (D > 0.0f) t = clampf_ord(rintf(__fdiv_rn(w[i], D)), -8.0f, 7.0f);
+            B.u[i] = uint8_t(int(t) + 8);
+        }
+        B.gscale = D;
+        B.L = B.M = 0;
+        B.d16 = s16;
+        B.dm16 = 0;
+        return ((s16 & 0x7FFFu) == 0x7C00u) ? 1 : 0;
     } else if constexpr (!T::asym) {
         const float half_range = float(1 << (T::bits - 1));
         float a = 0.0f;
@@ -134,7 +153,7 @@ __device__ __forceinline__ void st_u32(uint8_t *p, uint32_t v) { *reinterpret_ca
 
 template <int F>
 __device__ __forceinline__ void pack_lane(const LaneBlock &B, int lane, bool valid, uint8_t *blk) {
-    if constexpr (F == FMT_Q4G32) {
+    if constexpr (kInt4<F>) {
         uint32_t v = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) v |= uint32_t(B.u[i] & 15u) << (4 * i);
@@ -215,7 +234,7 @@ __device__ __forceinline__ uint32_t ld_u24(const uint8_t *p) {
 
 template <int F>
 __device__ __forceinline__ void unpack_lane(const uint8_t *blk, int lane, bool valid, LaneBlock &B) {
-    if constexpr (F == FMT_Q4G32) {
+    if constexpr (kInt4<F>) {
         uint32_t v = valid ? ld_u32(blk + 4 * lane) : 0x88888888u;
 #pragma unroll
         for (int i = 0; i < 8; ++i) B.u[i] = uint8_t((v >> (4 * i)) & 15u);
@@ -257,7 +276,7 @@ __device__ __forceinline__ void unpack_lane(const uint8_t *blk, int lane, bool v
 template <int F>
 __device__ __forceinline__ void dequant_lane(const LaneBlock &B, float out[8]) {
     using T = Fmt<F>;
-    if constexpr (F == FMT_Q4G32) {
+    if constexpr (kInt4<F>) {      // gscale: the fp32 scale, or the fp16 scale widened
 #pragma unroll
         for (int i = 0; i < 8; ++i) out[i] = __fmul_rn(B.gscale, float(int(B.u[i]) - 8));
     } else {
@@ -313,6 +332,10 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
             if constexpr (F == FMT_Q4G32) {
                 B.gscale = valid ? a.gscale[r * (a.K / 32) + 8 * b + j] : 0.0f;
                 B.L = B.M = 0; B.d16 = B.dm16 = 0;
+            } else if constexpr (F == FMT_Q4G32H) {
+                B.d16 = valid ? a.d[r * (a.K / 32) + 8 * b + j] : uint16_t(0);
+                B.gscale = h2f_bits(B.d16);
+                B.L = B.M = 0; B.dm16 = 0;
             } else {
                 const int64_t sb = r * a.nbk + b;
                 B.L = a.sub_scale[sb * T::nsub + j];
@@ -324,6 +347,11 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
             const uint8_t *blk = a.packed_in + r * a.row_stride + b * T::bytes;
             unpack_lane<F>(blk, lane, valid, B);
             if constexpr (F == FMT_Q4G32) B.gscale = valid ? a.gs_in[r * a.scale_stride + 8 * b + j] : 0.0f;
+            if constexpr (F == FMT_Q4G32H) {
+                const uint16_t *g16 = reinterpret_cast<const uint16_t *>(a.gs_in);
+                B.d16 = valid ? g16[r * a.scale_stride + 8 * b + j] : uint16_t(0);
+                B.gscale = h2f_bits(B.d16);
+            }
         }
 
         if constexpr (MODE == MODE_QUANT_PARTS || MODE == MODE_UNPACK) {
@@ -336,6 +364,8 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
             const bool first_of_sub = (lane % (T::sublen / 8)) == 0;
             if constexpr (F == FMT_Q4G32) {
                 if (valid && first_of_sub) a.gscale[r * (a.K / 32) + 8 * b + j] = B.gscale;
+            } else if constexpr (F == FMT_Q4G32H) {
+                if (valid && first_of_sub) a.d[r * (a.K / 32) + 8 * b + j] = B.d16;
             } else {
                 const int64_t sb = r * a.nbk + b;
                 if (first_of_sub) {
@@ -356,6 +386,14 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
                 if (b == a.nbk - 1) {                      // zero the scale-row padding
                     const int64_t g0 = a.K / 32;
                     if (g0 + lane < a.scale_stride) a.gs_out[r * a.scale_stride + g0 + lane] = 0.0f;
+                }
+            } else if constexpr (F == FMT_Q4G32H) {
+                uint16_t *g16 = reinterpret_cast<uint16_t *>(a.gs_out);
+                const bool first_of_group = (lane & 3) == 0;
+                if (valid && first_of_group) g16[r * a.scale_stride + 8 * b + j] = B.d16;
+                if (b == a.nbk - 1) {                      // zero the scale-row padding
+                    const int64_t g0 = a.K / 32;
+                    if (g0 + lane < a.scale_stride) g16[r * a.scale_stride + g0 + lane] = 0;
                 }
             } else {
                 if (b == a.nbk - 1) {                      // zero the row padding (< 16 bytes)
@@ -416,7 +454,8 @@ cudaError_t launch_block_op(int fmt, int mode, int wdt, const BlockArgs &a, cuda
         case FMT_Q2S: return launch_mode<FMT_Q2S>(a, mode, wdt, s);
         case FMT_Q3S: return launch_mode<FMT_Q3S>(a, mode, wdt, s);
         case FMT_Q5S: return launch_mode<FMT_Q5S>(a, mode, wdt, s);
-        default: return launch_mode<FMT_Q6S>(a, mode, wdt, s);
+        case FMT_Q6S: return launch_mode<FMT_Q6S>(a, mode, wdt, s);
+        default: return launch_mode<FMT_Q4G32H>(a, mode, wdt, s);
     }
 }
 

@@ -30,13 +30,15 @@ extern "C" {
 typedef struct CUstream_st *qpack_stream_t; /* identical to cudaStream_t */
 
 /* Weight formats. Q4G32: INT4 symmetric, group 32, fp32 group scales (P2 §3.1–§3.2, §4.1).
- * Q2S/Q3S/Q5S/Q6S: 256-weight super-blocks of 84/110/176/210 bytes (P1 §2.3 byte table). */
+ * Q2S/Q3S/Q5S/Q6S: 256-weight super-blocks of 84/110/176/210 bytes (P1 §2.3 byte table).
+ * Q4G32H: the INT4 codes of Q4G32 with fp16 group scales (4.5 bpw, P1 §2.1; FORMATS.md §1b). */
 typedef enum {
     QPACK_Q4G32 = 0,
     QPACK_Q2S = 1,
     QPACK_Q3S = 2,
     QPACK_Q5S = 3,
-    QPACK_Q6S = 4
+    QPACK_Q6S = 4,
+    QPACK_Q4G32H = 5
 } qpack_format;
 
 typedef enum { QPACK_F32 = 0, QPACK_F16 = 1, QPACK_BF16 = 2 } qpack_dtype;
@@ -51,18 +53,18 @@ typedef enum {
     QPACK_ERR_UNSUPPORTED = -6 /* format / path combination not provided */
 } qpack_status;
 
-/* Bit OR-ed into the device status word when a super-block's fp16 d or dmin overflows to infinity
- * (P1 §2.3 warns about fp16 super-scale overflow). */
+/* Bit OR-ed into the device status word when a super-block's fp16 d or dmin, or a Q4G32H fp16 group scale,
+ * overflows to infinity (P1 §2.3 warns about fp16 super-scale overflow). */
 #define QPACK_FLAG_RANGE 1
 
 /* Sizes of the packed representation (host-only, no GPU work).
  *  row_stride    bytes between consecutive packed rows (super-block formats: rows padded to 16 B, P1 §3.3)
  *  packed_bytes  N * row_stride
- *  scale_stride  Q4G32 only: floats between consecutive rows of the separate fp32 scale array
- *                (K/32 rounded up to a multiple of 4, P2 §4.1); 0 otherwise
- *  scale_bytes   Q4G32 only: N * scale_stride * 4; 0 otherwise
- *  block_bytes   bytes per 256-weight super-block (84/110/176/210, P1 §2.3); 0 for Q4G32
- *  nsub          sub-blocks per super-block (16, or 8 for Q5S); for Q4G32 the groups per row (K/32)
+ *  scale_stride  INT4 formats: elements between consecutive rows of the separate group-scale array (fp32 for
+ *                Q4G32, fp16 for Q4G32H; K/32 rounded up so that rows are 16 bytes, P2 §4.1); 0 otherwise
+ *  scale_bytes   INT4 formats: N * scale_stride * (4 or 2); 0 otherwise
+ *  block_bytes   bytes per 256-weight super-block (84/110/176/210, P1 §2.3); 0 for the INT4 formats
+ *  nsub          sub-blocks per super-block (16, or 8 for Q5S); for the INT4 formats the groups per row (K/32)
  *  weight_bytes  packed_bytes + scale_bytes: the bytes one product call streams from memory
  * Returns QPACK_OK, QPACK_ERR_ARG (bad format, negative size, null out) or QPACK_ERR_SHAPE. */
 typedef struct {
@@ -79,11 +81,12 @@ int qpack_layout(int fmt, int64_t N, int64_t K, qpack_layout_t *out);
 /* Quantize W into unpacked parts (P2 §3.1 for Q4G32; two-level round-to-nearest of FORMATS.md §2a/§2b for
  * the super-block formats, following P1 §2.1's fp16 super-scale -> sub-block scale -> weight structure).
  *  W          [N, K] of dtype wdt (F32, F16 or BF16), 16-byte aligned
- *  codes      [N, K] int8: the signed integer q (Q4G32 -8..7, Q3S -4..3, Q6S -32..31, Q2S 0..3, Q5S 0..31)
+ *  codes      [N, K] int8: the signed integer q (Q4G32/Q4G32H -8..7, Q3S -4..3, Q6S -32..31, Q2S 0..3, Q5S 0..31)
  *  gscale     Q4G32: [N, K/32] fp32 group scales; NULL for other formats
- *  sub_scale  super-block formats: [N, K/256 * nsub] uint8 sub-block scale integers L_j; NULL for Q4G32
+ *  sub_scale  super-block formats: [N, K/256 * nsub] uint8 sub-block scale integers L_j; NULL for the INT4 formats
  *  sub_min    Q2S/Q5S: [N, K/256 * nsub] uint8 sub-block minimum integers M_j; NULL otherwise
- *  d, dmin    super-block formats: [N, K/256] fp16 bits of d; dmin for Q2S/Q5S only (NULL otherwise)
+ *  d, dmin    super-block formats: [N, K/256] fp16 bits of d; dmin for Q2S/Q5S only (NULL otherwise).
+ *             Q4G32H: d holds the [N, K/32] fp16 group scales (2-byte aligned), dmin NULL
  *  status     device int32 (may be NULL): QPACK_FLAG_RANGE is OR-ed in; the caller clears it.
  * The results are bit-identical to FORMATS.md's IEEE fp32 definition. */
 int qpack_quantize(int fmt, const void *W, int wdt, int64_t N, int64_t K, int8_t *codes, float *gscale,
@@ -94,25 +97,27 @@ int qpack_quantize(int fmt, const void *W, int wdt, int64_t N, int64_t K, int8_t
  * packing (low nibble = even index) for Q4G32; P1 §2.2 cross-byte packing and §2.3 bit planes for the
  * super-block formats, bit orders of FORMATS.md §2c.
  *  packed        [N, row_stride] bytes, 16-byte aligned; padding bytes are written as zero
- *  group_scales  Q4G32: [N, scale_stride] fp32, 16-byte aligned, padding written as 0.0f; NULL otherwise */
+ *  group_scales  Q4G32: [N, scale_stride] fp32, Q4G32H: [N, scale_stride] fp16; 16-byte aligned, padding
+ *                written as zero; NULL for the super-block formats */
 int qpack_pack(int fmt, int64_t N, int64_t K, const int8_t *codes, const float *gscale, const uint8_t *sub_scale,
                const uint8_t *sub_min, const uint16_t *d, const uint16_t *dmin, uint8_t *packed,
-               float *group_scales, qpack_stream_t stream);
+               void *group_scales, qpack_stream_t stream);
 
-/* Fused quantize + pack: W straight to packed bytes (and Q4G32 group scales) in one pass over W.
+/* Fused quantize + pack: W straight to packed bytes (and INT4 group scales) in one pass over W.
  * Arguments as qpack_quantize (W, wdt, status) and qpack_pack (packed, group_scales). */
 int qpack_quantize_pack(int fmt, const void *W, int wdt, int64_t N, int64_t K, uint8_t *packed,
-                        float *group_scales, int32_t *status, qpack_stream_t stream);
+                        void *group_scales, int32_t *status, qpack_stream_t stream);
 
 /* Inverse of qpack_pack: packed bytes back to unpacked parts (same pointer conventions). */
-int qpack_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float *group_scales, int8_t *codes,
+int qpack_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const void *group_scales, int8_t *codes,
                  float *gscale, uint8_t *sub_scale, uint8_t *sub_min, uint16_t *d, uint16_t *dmin,
                  qpack_stream_t stream);
 
-/* Dequantize a packed matrix to fp32 out [N, K] (the page's self-check path, P1 §3.4): Q4G32 w' = s*q;
+/* Dequantize a packed matrix to fp32 out [N, K] (the page's self-check path, P1 §3.4): Q4G32 w' = s*q,
+ * Q4G32H w' = fp32(s16)*q;
  * symmetric super-blocks w' = (d*L_j)*q; asymmetric w' = (d*L_j)*q - (dmin*M_j), each step an fp32 rounding,
  * no FMA. Bit-identical to FORMATS.md. out must be 16-byte aligned. */
-int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float *group_scales, float *out,
+int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const void *group_scales, float *out,
                   qpack_stream_t stream);
 
 /* Fused dequant-GEMV (decode, batch 1; P1 §1.2 and §3.3, P2 §3.3 "fused dequantization"):
@@ -121,13 +126,13 @@ int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const fl
  * 32-element unit (step 2^-E, max |x| * 2^E in [2^14, 2^15): an element's rounding error is at most 2^-15 of its
  * unit's max |x|, and x with an exponent within 4 of that max is exact); code x activation sums are exact int32
  * within a sub-block, fp32 across sub-blocks.
- *  packed, group_scales  as produced by qpack_pack (group_scales NULL except Q4G32), 16-byte aligned
+ *  packed, group_scales  as produced by qpack_pack (group_scales NULL except the INT4 formats), 16-byte aligned
  *  x                     [K] fp16, 16-byte aligned
  *  y                     [N] fp32, 4-byte aligned
  *  K                     any multiple of the format's group (rows longer than one SM's shared memory can stage go
  *                        in K splits whose products are added to y in split order)
  * Parity bound against an fp64 sum: |y[r] - y_ref[r]| <= 1e-4 * ||w'_r||_2 * ||x||_2. */
-int qgemv(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, const uint16_t *x,
+int qgemv(int fmt, const uint8_t *packed, const void *group_scales, int64_t N, int64_t K, const uint16_t *x,
           float *y, qpack_stream_t stream);
 
 /* Small-batch decode GEMM (P2 §5.2 decode vs prefill; batch up to 16):
@@ -136,18 +141,18 @@ int qgemv(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, 
  *  X  [M, ldx] fp16, 16-byte aligned, ldx >= K and ldx a multiple of 8
  *  Y  [M, ldy] fp32, ldy >= N
  * Same parity bound as qgemv, per element. */
-int qgemm_small(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, int M,
+int qgemm_small(int fmt, const uint8_t *packed, const void *group_scales, int64_t N, int64_t K, int M,
                 const uint16_t *X, int64_t ldx, float *Y, int64_t ldy, qpack_stream_t stream);
 
 /* Prefill dequant GEMM on the tensor cores (P1 §1.2: prefill is a dense [tokens, hidden] x [hidden, hidden]
  * contraction):
  *   Y[m, n] = sum_k bf16(X[m,k]) * bf16(w'[n,k]),  fp32 accumulation, Y rounded to bf16
  * Weight tiles are dequantized to bf16 in shared memory and fed to tcgen05 MMA with TMEM accumulators.
- *  formats  Q4G32 (K a multiple of 64) and the super-block formats (K a multiple of 256)
+ *  formats  Q4G32 and Q4G32H (K a multiple of 64) and the super-block formats (K a multiple of 256)
  *  X        [M, ldx] bf16, 16-byte aligned, ldx >= K, ldx a multiple of 8
  *  Y        [M, ldy] bf16, 2-byte aligned, ldy >= N (16-byte aligned rows with ldy % 8 == 0 store fastest)
  * Parity bound: ||Y - Y_ref||_2 / ||Y_ref||_2 <= 2e-2 with Y_ref in fp64. */
-int qgemm_prefill(int fmt, const uint8_t *packed, const float *group_scales, int64_t N, int64_t K, int64_t M,
+int qgemm_prefill(int fmt, const uint8_t *packed, const void *group_scales, int64_t N, int64_t K, int64_t M,
                   const uint16_t *X, int64_t ldx, uint16_t *Y, int64_t ldy, qpack_stream_t stream);
 
 /* 8-bit KV cache (2/3/5/6-bit article §4.1: the KV cache in 8 bits with one fp16 scale per 32 elements, about

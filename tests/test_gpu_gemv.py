@@ -8,7 +8,7 @@ from conftest import gemv_bound_check, to_np_fp32
 
 pytestmark = pytest.mark.gpu
 
-ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S"]
+ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H"]
 
 
 def case(orc, fmt, N, K, seed, b=0.02):
@@ -20,7 +20,7 @@ def case(orc, fmt, N, K, seed, b=0.02):
 
 def run_gemv(qpg, fmt, rp, rgs, N, K, x):
     pd = torch.from_numpy(rp).cuda()
-    gd = None if rgs is None else torch.from_numpy(rgs).cuda()
+    gd = None if rgs is None else torch.from_numpy(rgs.view(np.int16) if rgs.dtype == np.uint16 else rgs).cuda()
     y = qpg.qgemv(fmt, pd, gd, N, K, x.cuda())
     torch.cuda.synchronize()
     return y.cpu().numpy()
@@ -28,7 +28,7 @@ def run_gemv(qpg, fmt, rp, rgs, N, K, x):
 
 def shapes(name):
     s = [(1, 256), (3, 512), (4, 4096), (37, 4096 + 768), (130, 8192 + 256), (9, 12288)]
-    if name == "Q4G32":
+    if name in ("Q4G32", "Q4G32H"):
         s += [(5, 96), (7, 4096 + 32)]
     return s
 
@@ -160,7 +160,7 @@ def test_small_batch(qpg, orc, name, M):
     rp, rgs = case(orc, fmt, N, K, 700 + M)
     X = synth.normal((M, K), 1.0, 800 + M, dtype=torch.float16)
     pd = torch.from_numpy(rp).cuda()
-    gd = None if rgs is None else torch.from_numpy(rgs).cuda()
+    gd = None if rgs is None else torch.from_numpy(rgs.view(np.int16) if rgs.dtype == np.uint16 else rgs).cuda()
     Y = qpg.qgemm_small(fmt, pd, gd, N, K, X.cuda())
     torch.cuda.synchronize()
     Y_ref = orc.gemm(fmt, N, K, rp, rgs, X.numpy().view(np.uint16))
@@ -183,7 +183,7 @@ def test_small_batch_groups(qpg, orc, name, shape):
     rp, rgs = case(orc, fmt, N, K, 720 + M + N % 7)
     X = synth.normal((M, K), 1.0, 820 + M, dtype=torch.float16)
     pd = torch.from_numpy(rp).cuda()
-    gd = None if rgs is None else torch.from_numpy(rgs).cuda()
+    gd = None if rgs is None else torch.from_numpy(rgs.view(np.int16) if rgs.dtype == np.uint16 else rgs).cuda()
     Y = qpg.qgemm_small(fmt, pd, gd, N, K, X.cuda())
     torch.cuda.synchronize()
     Y_ref = orc.gemm(fmt, N, K, rp, rgs, X.numpy().view(np.uint16), nthreads=8)

@@ -8,7 +8,7 @@ import torch
 
 pytestmark = pytest.mark.gpu
 
-ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S"]
+ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H"]
 
 
 def run_case(qpg, orc, fmt, M, N, K, seed, full=True, nsample=512):
@@ -17,7 +17,7 @@ def run_case(qpg, orc, fmt, M, N, K, seed, full=True, nsample=512):
     rp, rgs, _ = orc.quantize_pack(fmt, W.numpy())
     X = synth.normal((M, K), 1.0, seed + 1).to(torch.bfloat16)
     pd = torch.from_numpy(rp).cuda()
-    gd = None if rgs is None else torch.from_numpy(rgs).cuda()
+    gd = None if rgs is None else torch.from_numpy(rgs.view(np.int16) if rgs.dtype == np.uint16 else rgs).cuda()
     Y = qpg.qgemm_prefill(fmt, pd, gd, N, K, X.cuda())
     torch.cuda.synchronize()
     Yg = Y.float().cpu().numpy()

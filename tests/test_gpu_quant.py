@@ -9,7 +9,7 @@ from conftest import to_np_fp32
 
 pytestmark = pytest.mark.gpu
 
-ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S"]
+ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H"]
 DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -27,7 +27,7 @@ def weights(N, K, seed, dtype=torch.float32):
 
 def shapes(name):
     out = [(1, 256), (37, 1024), (5, 4096 + 256)]
-    if name == "Q4G32":
+    if name in ("Q4G32", "Q4G32H"):
         out += [(9, 96), (3, 32), (6, 4096 + 160)]       # rows ending inside a 256-weight block
     return out
 
@@ -62,8 +62,8 @@ def test_quantize_parts_and_packed_bit_exact(qpg, orc, name, dt):
         cmp_parts(parts, ref)
         rp, rgs = orc.pack(fmt, N, K, ref)
         assert np.array_equal(packed.cpu().numpy(), rp)
-        if rgs is not None:
-            assert np.array_equal(gs.cpu().numpy().view(np.uint32), rgs.view(np.uint32))
+        if rgs is not None:                                # fp32 (Q4G32) or fp16 (Q4G32H) scales, bit for bit
+            assert np.array_equal(gs.cpu().numpy().view(np.uint8), rgs.view(np.uint8))
         assert int(st.item()) == ref["flags"] == 0
 
 
@@ -82,7 +82,7 @@ def test_pack_unpack_dequant_bit_exact(qpg, orc, name):
         assert np.array_equal(packed.cpu().numpy(), rp)
         # unpack and dequantize the oracle's bytes on the GPU
         pd = torch.from_numpy(rp).cuda()
-        gd = None if rgs is None else torch.from_numpy(rgs).cuda()
+        gd = None if rgs is None else torch.from_numpy(rgs.view(np.int16) if rgs.dtype == np.uint16 else rgs).cuda()
         back = qpg.qpack_unpack(fmt, N, K, pd, gd)
         deq = qpg.qpack_dequant(fmt, N, K, pd, gd)
         torch.cuda.synchronize()
@@ -91,7 +91,7 @@ def test_pack_unpack_dequant_bit_exact(qpg, orc, name):
         assert np.array_equal(deq.cpu().numpy().view(np.uint32), rdeq.view(np.uint32))
 
 
-@pytest.mark.parametrize("name", ["Q2S", "Q3S", "Q5S", "Q6S"])
+@pytest.mark.parametrize("name", ["Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H"])
 def test_range_flag(qpg, orc, name):
     fmt = qpg.FORMATS[name]
     W = torch.zeros(3, 512)
