@@ -104,7 +104,11 @@ float bf16_to_f32(uint16_t b) { return bits_f32(uint32_t(b) << 16); }
 // Format descriptions (P1 §2.3 byte table; P2 §3.2 / §4.1 for INT4).
 // ----------------------------------------------------------------------------------------------------------
 
-enum { Q4G32 = 0, Q2S = 1, Q3S = 2, Q5S = 3, Q6S = 4, Q4G32H = 5 };
+enum { Q4G32 = 0, Q2S = 1, Q3S = 2, Q5S = 3, Q6S = 4, Q4G32H = 5, Q4G16 = 6 };
+
+// Weights per INT4 group: 32, or 16 for Q4G16.
+int int4_group(int fmt) { return fmt == Q4G16 ? 16 : 32; }
+bool is_int4(int fmt) { return fmt == Q4G32 || fmt == Q4G32H || fmt == Q4G16; }
 
 struct SbFormat {
     int bits;      // code width b
@@ -171,16 +175,17 @@ void wr16(uint8_t *p, uint16_t v) { p[0] = uint8_t(v); p[1] = uint8_t(v >> 8); }
 // ----------------------------------------------------------------------------------------------------------
 
 // INT4 symmetric group quantizer, P2 §3.1: scale = max|w| / 8 floored at 1e-12, q = clamp(round(w/scale),-8,7).
-void quantize_q4g32_row(const float *w, int64_t K, int8_t *q, float *scales) {
-    for (int64_t g = 0; g < K / 32; ++g) {
-        const float *wg = w + 32 * g;
+// P2 §3.1 for a group of G weights (G = 32; G = 16 is P2 §5.1's remedy for layers with many outlier weights).
+void quantize_int4_row(const float *w, int64_t K, int G, int8_t *q, float *scales) {
+    for (int64_t g = 0; g < K / G; ++g) {
+        const float *wg = w + G * g;
         float amax = 0.0f;
-        for (int i = 0; i < 32; ++i) amax = std::fmax(amax, std::fabs(wg[i]));
+        for (int i = 0; i < G; ++i) amax = std::fmax(amax, std::fabs(wg[i]));
         float scale = amax / 8.0f;
         if (scale < 1e-12f) scale = 1e-12f;
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < G; ++i) {
             float t = std::nearbyint(wg[i] / scale);
-            q[32 * g + i] = int8_t(clampf(t, -8.0f, 7.0f));
+            q[G * g + i] = int8_t(clampf(t, -8.0f, 7.0f));
         }
         scales[g] = scale;
     }
@@ -401,13 +406,14 @@ void dequant_sb(const SbFormat &F, int fmt, const int8_t *q, const uint8_t *L, c
 // Dequantize row r of a packed matrix into out[K].
 void dequant_row(int fmt, const uint8_t *packed, const float *gs, int64_t K, int64_t r, int64_t row_stride,
                  int64_t scale_stride, float *out) {
-    if (fmt == Q4G32 || fmt == Q4G32H) {
+    if (is_int4(fmt)) {
         const uint8_t *row = packed + r * row_stride;
         const uint16_t *gs16 = reinterpret_cast<const uint16_t *>(gs);
+        const int G = int4_group(fmt);
         for (int64_t k = 0; k < K; ++k) {
             uint8_t byte = row[k >> 1];
             int u = (k & 1) ? (byte >> 4) : (byte & 15);
-            float s = fmt == Q4G32 ? gs[r * scale_stride + k / 32] : f16_to_f32(gs16[r * scale_stride + k / 32]);
+            float s = fmt == Q4G32H ? f16_to_f32(gs16[r * scale_stride + k / G]) : gs[r * scale_stride + k / G];
             out[k] = s * float(u - 8);
         }
         return;
@@ -424,7 +430,7 @@ void dequant_row(int fmt, const uint8_t *packed, const float *gs, int64_t K, int
 
 bool shape_ok(int fmt, int64_t N, int64_t K) {
     if (N < 0 || K < 0) return false;
-    if (fmt == Q4G32 || fmt == Q4G32H) return K % 32 == 0;
+    if (is_int4(fmt)) return K % 32 == 0;   // Q4G16 too: rows of whole 32-weight units
     SbFormat F;
     if (!sb_format(fmt, &F)) return false;
     return K % 256 == 0;
@@ -470,6 +476,14 @@ int orc_layout(int fmt, int64_t N, int64_t K, int64_t *out) {
         out[4] = 0;
         return 0;
     }
+    if (fmt == Q4G16) {
+        out[0] = K / 2;
+        out[1] = N * (K / 2);
+        out[2] = round_up(K / 16, 4);
+        out[3] = N * out[2] * 4;
+        out[4] = 0;
+        return 0;
+    }
     SbFormat F;
     sb_format(fmt, &F);
     out[0] = round_up((K / 256) * F.bytes, 16);
@@ -489,7 +503,11 @@ int orc_quantize(int fmt, const float *W, int64_t N, int64_t K, int8_t *q, float
     if (!shape_ok(fmt, N, K)) return -2;
     int flags = 0;
     if (fmt == Q4G32) {
-        for (int64_t r = 0; r < N; ++r) quantize_q4g32_row(W + r * K, K, q + r * K, gscale + r * (K / 32));
+        for (int64_t r = 0; r < N; ++r) quantize_int4_row(W + r * K, K, 32, q + r * K, gscale + r * (K / 32));
+        return 0;
+    }
+    if (fmt == Q4G16) {
+        for (int64_t r = 0; r < N; ++r) quantize_int4_row(W + r * K, K, 16, q + r * K, gscale + r * (K / 16));
         return 0;
     }
     if (fmt == Q4G32H) {
@@ -512,8 +530,9 @@ int orc_pack(int fmt, int64_t N, int64_t K, const int8_t *q, const float *gscale
     int64_t lay[5];
     if (orc_layout(fmt, N, K, lay)) return -2;
     std::memset(packed, 0, size_t(lay[1]));
-    if (fmt == Q4G32 || fmt == Q4G32H) {
+    if (is_int4(fmt)) {
         uint16_t *gs16 = reinterpret_cast<uint16_t *>(group_scales);
+        const int64_t ng = K / int4_group(fmt);
         for (int64_t r = 0; r < N; ++r) {
             uint8_t *row = packed + r * lay[0];
             for (int64_t j = 0; j < K / 2; ++j) {
@@ -521,8 +540,8 @@ int orc_pack(int fmt, int64_t N, int64_t K, const int8_t *q, const float *gscale
                 row[j] = uint8_t((u0 & 15u) | ((u1 & 15u) << 4));
             }
             for (int64_t g = 0; g < lay[2]; ++g) {
-                if (fmt == Q4G32) group_scales[r * lay[2] + g] = (g < K / 32) ? gscale[r * (K / 32) + g] : 0.0f;
-                else gs16[r * lay[2] + g] = (g < K / 32) ? d[r * (K / 32) + g] : uint16_t(0);
+                if (fmt == Q4G32H) gs16[r * lay[2] + g] = (g < ng) ? d[r * ng + g] : uint16_t(0);
+                else group_scales[r * lay[2] + g] = (g < ng) ? gscale[r * ng + g] : 0.0f;
             }
         }
         return 0;
@@ -545,8 +564,9 @@ int orc_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float
                float *gscale, uint8_t *sub_scale, uint8_t *sub_min, uint16_t *d, uint16_t *dmin) {
     int64_t lay[5];
     if (orc_layout(fmt, N, K, lay)) return -2;
-    if (fmt == Q4G32 || fmt == Q4G32H) {
+    if (is_int4(fmt)) {
         const uint16_t *gs16 = reinterpret_cast<const uint16_t *>(group_scales);
+        const int64_t ng = K / int4_group(fmt);
         for (int64_t r = 0; r < N; ++r) {
             const uint8_t *row = packed + r * lay[0];
             for (int64_t k = 0; k < K; ++k) {
@@ -554,9 +574,9 @@ int orc_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float
                 uint8_t u = (k & 1) ? uint8_t(byte >> 4) : uint8_t(byte & 15u);
                 q[r * K + k] = int8_t(int(u) - 8);
             }
-            for (int64_t g = 0; g < K / 32; ++g) {
-                if (fmt == Q4G32) gscale[r * (K / 32) + g] = group_scales[r * lay[2] + g];
-                else d[r * (K / 32) + g] = gs16[r * lay[2] + g];
+            for (int64_t g = 0; g < ng; ++g) {
+                if (fmt == Q4G32H) d[r * ng + g] = gs16[r * lay[2] + g];
+                else gscale[r * ng + g] = group_scales[r * lay[2] + g];
             }
         }
         return 0;
