@@ -11,7 +11,7 @@
 
 namespace qpack {
 
-enum : int { FMT_Q4G32 = 0, FMT_Q2S = 1, FMT_Q3S = 2, FMT_Q5S = 3, FMT_Q6S = 4, FMT_Q4G32H = 5 };
+enum : int { FMT_Q4G32 = 0, FMT_Q2S = 1, FMT_Q3S = 2, FMT_Q5S = 3, FMT_Q6S = 4, FMT_Q4G32H = 5, FMT_Q4G16 = 6 };
 enum : int { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 
 // Bits OR-ed into a per-translation-unit device fault word when a bounded wait gives up.
@@ -30,8 +30,14 @@ template <> struct Fmt<FMT_Q4G32H> {
     static constexpr bool asym = false, sb = false;
     static constexpr int offset = 8;
 };
-// The two INT4 formats share their code layout; only the group-scale type differs.
-template <int F> constexpr bool kInt4 = (F == FMT_Q4G32 || F == FMT_Q4G32H);
+// INT4 symmetric group 16 (fp32 scales): the same codes, one scale per 16 weights.
+template <> struct Fmt<FMT_Q4G16> {
+    static constexpr int bits = 4, nsub = 16, sublen = 16, lmax = 0, bytes = 128;
+    static constexpr bool asym = false, sb = false;
+    static constexpr int offset = 8;
+};
+// The INT4 formats share their code layout; only the group size and the scale type differ.
+template <int F> constexpr bool kInt4 = (F == FMT_Q4G32 || F == FMT_Q4G32H || F == FMT_Q4G16);
 template <> struct Fmt<FMT_Q2S> {
     static constexpr int bits = 2, nsub = 16, sublen = 16, lmax = 15, bytes = 84;
     static constexpr bool asym = true, sb = true;

@@ -102,6 +102,7 @@ __host__ __device__ constexpr int dp_elem(int a, int e) {
 template <int F> struct XC;
 template <> struct XC<FMT_Q4G32> { static constexpr int n = 2; };   // int -128 Sx, XS / 16
 template <> struct XC<FMT_Q4G32H> { static constexpr int n = 2; };  // as Q4G32
+template <> struct XC<FMT_Q4G16> { static constexpr int n = 3; };   // int -128 Sx_0, int -128 Sx_1, XS / 16
 template <> struct XC<FMT_Q2S> { static constexpr int n = 3; };     // Sx_0 XS, Sx_1 XS, XS
 template <> struct XC<FMT_Q3S> { static constexpr int n = 3; };     // int -128 Sx_0, int -128 Sx_1, XS / 32
 template <> struct XC<FMT_Q5S> { static constexpr int n = 2; };     // Sx XS, XS
@@ -197,9 +198,16 @@ __device__ __forceinline__ void unpack_dp(const uint8_t *u, const uint8_t *sp, c
     r.f1 = r.g0 = r.g1 = 0.f;
     if constexpr (kInt4<F>) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
-        // the unit's group scale: fp32 (Q4G32) or fp16 (Q4G32H) at sp
-        if constexpr (F == FMT_Q4G32) r.f0 = on ? *reinterpret_cast<const float *>(sp) : 0.f;
-        else r.f0 = on ? h2f_bits(*reinterpret_cast<const uint16_t *>(sp)) : 0.f;
+        // the unit's group scale(s) at sp: fp32 (Q4G32), fp16 (Q4G32H), or two fp32 (Q4G16: weights 0-15, 16-31)
+        if constexpr (F == FMT_Q4G32) {
+            r.f0 = on ? *reinterpret_cast<const float *>(sp) : 0.f;
+        } else if constexpr (F == FMT_Q4G32H) {
+            r.f0 = on ? h2f_bits(*reinterpret_cast<const uint16_t *>(sp)) : 0.f;
+        } else {
+            const float2 s2 = *reinterpret_cast<const float2 *>(sp);
+            r.f0 = on ? s2.x : 0.f;
+            r.f1 = on ? s2.y : 0.f;
+        }
         const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) { r.v[2 * j] = wv[j] & 0x0F0F0F0Fu; r.v[2 * j + 1] = wv[j] & 0xF0F0F0F0u; }
@@ -272,7 +280,23 @@ __device__ __forceinline__ void unpack_dp(const uint8_t *u, const uint8_t *sp, c
 // unit constants).
 template <int F>
 __device__ __forceinline__ void dot_dp(const DRow &r, const uint32_t *xv, const float *c, float &acc) {
-    if constexpr (kInt4<F>) {
+    if constexpr (F == FMT_Q4G16) {
+        // as below, per 16-weight group: words 0..3 (weights 0-15) and 4..7 (16-31), each with its own scale
+        const float fs[2] = {r.f0, r.f1};
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            int32_t lo = 0, hi = __float_as_int(c[g]);
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * g + jj;
+                lo = dp2a_lo(xv[4 * j], r.v[2 * j], lo);
+                lo = dp2a_hi(xv[4 * j + 1], r.v[2 * j], lo);
+                hi = dp2a_lo(xv[4 * j + 2], r.v[2 * j + 1], hi);
+                hi = dp2a_hi(xv[4 * j + 3], r.v[2 * j + 1], hi);
+            }
+            acc = fmaf(float(16 * lo + hi), fs[g] * c[2], acc);
+        }
+    } else if constexpr (kInt4<F>) {
         // lo: even weights at class 0; hi: odd weights at class 4, starting at -128 Sx (the code offset 8) -> 16 sum q x
         int32_t lo = 0, hi = __float_as_int(c[0]);
 #pragma unroll
@@ -390,7 +414,11 @@ __device__ __forceinline__ void stage_unit(const uint4 (&raw)[4], uint4 *xs, flo
     for (int t = 0; t < 4; ++t) xs[t * U + u] = make_uint4(st[4 * t], st[4 * t + 1], st[4 * t + 2], st[4 * t + 3]);
     float *c = cst + u * XC<F>::n;
     const float XS = exp2i(-E);
-    if constexpr (kInt4<F>) {
+    if constexpr (F == FMT_Q4G16) {
+        c[0] = __int_as_float(-128 * s0);
+        c[1] = __int_as_float(-128 * s1);
+        c[2] = exp2i(-E - 4);
+    } else if constexpr (kInt4<F>) {
         c[0] = __int_as_float(-128 * (s0 + s1));
         c[1] = exp2i(-E - 4);
     } else if constexpr (F == FMT_Q2S) {
@@ -471,7 +499,8 @@ template <int F, int MT = 1> struct T1 {
     static constexpr int PR = MT > 1 ? (256 / MT > TR ? 256 / MT : TR) : 256;     // rows per partial-sum round
     static constexpr int CB = Fmt<F>::sb ? (CHW / 256) * Fmt<F>::bytes : CHW / 2; // code bytes per row chunk
     static constexpr int SE = F == FMT_Q4G32H ? 2 : 4;                            // INT4 group-scale element bytes
-    static constexpr int SB = Fmt<F>::sb ? 0 : (CHW / 32) * SE;                   // INT4 scale bytes per row chunk
+    static constexpr int SU = F == FMT_Q4G16 ? 2 * SE : SE;                       // INT4 scale bytes per 32-weight unit
+    static constexpr int SB = Fmt<F>::sb ? 0 : (CHW / 32) * SU;                   // INT4 scale bytes per row chunk
     static constexpr int TX = TR * (CB + SB);                                     // bytes a stage receives
     static constexpr int STAGE = (TX + 127) / 128 * 128;
     static_assert(CB % 16 == 0 && CB / 8 <= 256 && SB / 8 <= 256, "tensor-map box limits");
@@ -612,7 +641,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
         if (!dead) {
             const uint8_t *st = stages + s * uint32_t(T::STAGE);
             const uint8_t *ub = st + rc * CB + geo.ubase;
-            const uint8_t *sp = st + TR * CB + rc * SB + uc * T::SE;   // INT4: this lane's group scale of row rc
+            const uint8_t *sp = st + TR * CB + rc * SB + uc * T::SU;   // INT4: this lane's group scale(s) of row rc
             const uint32_t u = c * UPC + uc;
             const bool uv = u < U;
             const uint32_t uu = uv ? u : U - 1;
@@ -870,6 +899,7 @@ cudaError_t launch_gemv(int fmt, const GemvArgs &a, cudaStream_t s) {
     switch (fmt) {
         case FMT_Q4G32: return launch_fmt<FMT_Q4G32>(a, s);
         case FMT_Q4G32H: return launch_fmt<FMT_Q4G32H>(a, s);
+        case FMT_Q4G16: return launch_fmt<FMT_Q4G16>(a, s);
         case FMT_Q2S: return launch_fmt<FMT_Q2S>(a, s);
         case FMT_Q3S: return launch_fmt<FMT_Q3S>(a, s);
         case FMT_Q5S: return launch_fmt<FMT_Q5S>(a, s);

@@ -147,8 +147,15 @@ __device__ __forceinline__ void load_raw(const uint8_t *row, const uint8_t *gs_r
         const uint4 c = __ldg(reinterpret_cast<const uint4 *>(row + 16 * u));
         r.c[0] = c.x; r.c[1] = c.y; r.c[2] = c.z; r.c[3] = c.w;
         // the group scale as fp32 bits: stored fp32 (Q4G32) or fp16 widened exactly (Q4G32H)
-        if constexpr (F == FMT_Q4G32) r.e[0] = __float_as_uint(__ldg(reinterpret_cast<const float *>(gs_row) + u));
-        else r.e[0] = __float_as_uint(h2f_bits(uint16_t(ldg16(gs_row + 2 * u))));
+        if constexpr (F == FMT_Q4G32) {
+            r.e[0] = __float_as_uint(__ldg(reinterpret_cast<const float *>(gs_row) + u));
+        } else if constexpr (F == FMT_Q4G32H) {
+            r.e[0] = __float_as_uint(h2f_bits(uint16_t(ldg16(gs_row + 2 * u))));
+        } else {    // Q4G16: the scales of weights 0-15 and 16-31 of the unit
+            const float2 s2 = __ldg(reinterpret_cast<const float2 *>(gs_row) + u);
+            r.e[0] = __float_as_uint(s2.x);
+            r.e[1] = __float_as_uint(s2.y);
+        }
     } else {
         const uint32_t b = u >> 3, su = u & 7u;
         const uint8_t *blk = row + b * Fmt<F>::bytes;
@@ -185,9 +192,10 @@ template <int F>
 __device__ __forceinline__ void unit_bf16(const RawUnit &r, uint32_t u, uint32_t out[16]) {
     float w[32];
     if constexpr (kInt4<F>) {
-        const float sc = __uint_as_float(r.e[0]);
+        const float sc0 = __uint_as_float(r.e[0]), sc1 = F == FMT_Q4G16 ? __uint_as_float(r.e[1]) : sc0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = __fmul_rn(sc, float(int((r.c[i >> 3] >> (4 * (i & 7))) & 15u) - 8));
+        for (int i = 0; i < 32; ++i)
+            w[i] = __fmul_rn(i < 16 ? sc0 : sc1, float(int((r.c[i >> 3] >> (4 * (i & 7))) & 15u) - 8));
     } else if constexpr (F == FMT_Q2S) {
         const float D = h2f_bits(uint16_t(r.e[1] & 0xFFFFu)), Dm = h2f_bits(uint16_t(r.e[1] >> 16));
 #pragma unroll
@@ -480,6 +488,7 @@ cudaError_t launch_prefill(int fmt, const PrefillArgs &a, cudaStream_t s) {
     switch (fmt) {
         case FMT_Q4G32: return launch_prefill_f<FMT_Q4G32>(a, s);
         case FMT_Q4G32H: return launch_prefill_f<FMT_Q4G32H>(a, s);
+        case FMT_Q4G16: return launch_prefill_f<FMT_Q4G16>(a, s);
         case FMT_Q2S: return launch_prefill_f<FMT_Q2S>(a, s);
         case FMT_Q3S: return launch_prefill_f<FMT_Q3S>(a, s);
         case FMT_Q5S: return launch_prefill_f<FMT_Q5S>(a, s);

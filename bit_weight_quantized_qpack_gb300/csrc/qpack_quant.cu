@@ -50,11 +50,11 @@ __device__ __forceinline__ float warp_max(float v) {
 template <int F>
 __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
     using T = Fmt<F>;
-    if constexpr (F == FMT_Q4G32) {
+    if constexpr (F == FMT_Q4G32 || F == FMT_Q4G16) {
         float a = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
-        a = sub_reduce_max<F>(a);                         // group of 32 = 4 lanes
+        a = sub_reduce_max<F>(a);                         // group of 32 = 4 lanes (16 = 2 lanes)
         float s = __fdiv_rn(a, 8.0f);
         if (s < 1e-12f) s = 1e-12f;
 #pragma unroll
@@ -329,8 +329,8 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) B.u[i] = uint8_t(T::offset);
             }
-            if constexpr (F == FMT_Q4G32) {
-                B.gscale = valid ? a.gscale[r * (a.K / 32) + 8 * b + j] : 0.0f;
+            if constexpr (F == FMT_Q4G32 || F == FMT_Q4G16) {
+                B.gscale = valid ? a.gscale[r * (a.K / T::sublen) + T::nsub * b + j] : 0.0f;
                 B.L = B.M = 0; B.d16 = B.dm16 = 0;
             } else if constexpr (F == FMT_Q4G32H) {
                 B.d16 = valid ? a.d[r * (a.K / 32) + 8 * b + j] : uint16_t(0);
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
         } else {  // UNPACK / DEQUANT read packed bytes
             const uint8_t *blk = a.packed_in + r * a.row_stride + b * T::bytes;
             unpack_lane<F>(blk, lane, valid, B);
-            if constexpr (F == FMT_Q4G32) B.gscale = valid ? a.gs_in[r * a.scale_stride + 8 * b + j] : 0.0f;
+            if constexpr (F == FMT_Q4G32 || F == FMT_Q4G16) B.gscale = valid ? a.gs_in[r * a.scale_stride + T::nsub * b + j] : 0.0f;
             if constexpr (F == FMT_Q4G32H) {
                 const uint16_t *g16 = reinterpret_cast<const uint16_t *>(a.gs_in);
                 B.d16 = valid ? g16[r * a.scale_stride + 8 * b + j] : uint16_t(0);
@@ -362,8 +362,8 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
                 *reinterpret_cast<uint2 *>(a.codes + r * a.K + k0) = make_uint2(cw[0], cw[1]);
             }
             const bool first_of_sub = (lane % (T::sublen / 8)) == 0;
-            if constexpr (F == FMT_Q4G32) {
-                if (valid && first_of_sub) a.gscale[r * (a.K / 32) + 8 * b + j] = B.gscale;
+            if constexpr (F == FMT_Q4G32 || F == FMT_Q4G16) {
+                if (valid && first_of_sub) a.gscale[r * (a.K / T::sublen) + T::nsub * b + j] = B.gscale;
             } else if constexpr (F == FMT_Q4G32H) {
                 if (valid && first_of_sub) a.d[r * (a.K / 32) + 8 * b + j] = B.d16;
             } else {
@@ -380,11 +380,11 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
         } else if constexpr (MODE == MODE_QUANT_PACKED || MODE == MODE_PACK) {
             uint8_t *row = a.packed + r * a.row_stride;
             pack_lane<F>(B, lane, valid, row + b * T::bytes);
-            if constexpr (F == FMT_Q4G32) {
-                const bool first_of_group = (lane & 3) == 0;
-                if (valid && first_of_group) a.gs_out[r * a.scale_stride + 8 * b + j] = B.gscale;
+            if constexpr (F == FMT_Q4G32 || F == FMT_Q4G16) {
+                const bool first_of_group = (lane % (T::sublen / 8)) == 0;
+                if (valid && first_of_group) a.gs_out[r * a.scale_stride + T::nsub * b + j] = B.gscale;
                 if (b == a.nbk - 1) {                      // zero the scale-row padding
-                    const int64_t g0 = a.K / 32;
+                    const int64_t g0 = a.K / T::sublen;
                     if (g0 + lane < a.scale_stride) a.gs_out[r * a.scale_stride + g0 + lane] = 0.0f;
                 }
             } else if constexpr (F == FMT_Q4G32H) {
@@ -455,7 +455,8 @@ cudaError_t launch_block_op(int fmt, int mode, int wdt, const BlockArgs &a, cuda
         case FMT_Q3S: return launch_mode<FMT_Q3S>(a, mode, wdt, s);
         case FMT_Q5S: return launch_mode<FMT_Q5S>(a, mode, wdt, s);
         case FMT_Q6S: return launch_mode<FMT_Q6S>(a, mode, wdt, s);
-        default: return launch_mode<FMT_Q4G32H>(a, mode, wdt, s);
+        case FMT_Q4G32H: return launch_mode<FMT_Q4G32H>(a, mode, wdt, s);
+        default: return launch_mode<FMT_Q4G16>(a, mode, wdt, s);
     }
 }
 

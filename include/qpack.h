@@ -31,14 +31,17 @@ typedef struct CUstream_st *qpack_stream_t; /* identical to cudaStream_t */
 
 /* Weight formats. Q4G32: INT4 symmetric, group 32, fp32 group scales (P2 §3.1–§3.2, §4.1).
  * Q2S/Q3S/Q5S/Q6S: 256-weight super-blocks of 84/110/176/210 bytes (P1 §2.3 byte table).
- * Q4G32H: the INT4 codes of Q4G32 with fp16 group scales (4.5 bpw, P1 §2.1; FORMATS.md §1b). */
+ * Q4G32H: the INT4 codes of Q4G32 with fp16 group scales (4.5 bpw, P1 §2.1; FORMATS.md §1b).
+ * Q4G16: the INT4 rule of Q4G32 with groups of 16 weights, fp32 scales (6 bpw, P2 §5.1; FORMATS.md §1c); K a
+ * multiple of 32. */
 typedef enum {
     QPACK_Q4G32 = 0,
     QPACK_Q2S = 1,
     QPACK_Q3S = 2,
     QPACK_Q5S = 3,
     QPACK_Q6S = 4,
-    QPACK_Q4G32H = 5
+    QPACK_Q4G32H = 5,
+    QPACK_Q4G16 = 6
 } qpack_format;
 
 typedef enum { QPACK_F32 = 0, QPACK_F16 = 1, QPACK_BF16 = 2 } qpack_dtype;
@@ -61,10 +64,11 @@ typedef enum {
  *  row_stride    bytes between consecutive packed rows (super-block formats: rows padded to 16 B, P1 §3.3)
  *  packed_bytes  N * row_stride
  *  scale_stride  INT4 formats: elements between consecutive rows of the separate group-scale array (fp32 for
- *                Q4G32, fp16 for Q4G32H; K/32 rounded up so that rows are 16 bytes, P2 §4.1); 0 otherwise
+ *                Q4G32 / Q4G16, fp16 for Q4G32H; K/32 (K/16 for Q4G16) rounded up so that rows are 16 bytes,
+ *                P2 §4.1); 0 otherwise
  *  scale_bytes   INT4 formats: N * scale_stride * (4 or 2); 0 otherwise
  *  block_bytes   bytes per 256-weight super-block (84/110/176/210, P1 §2.3); 0 for the INT4 formats
- *  nsub          sub-blocks per super-block (16, or 8 for Q5S); for the INT4 formats the groups per row (K/32)
+ *  nsub          sub-blocks per super-block (16, or 8 for Q5S); for the INT4 formats the groups per row
  *  weight_bytes  packed_bytes + scale_bytes: the bytes one product call streams from memory
  * Returns QPACK_OK, QPACK_ERR_ARG (bad format, negative size, null out) or QPACK_ERR_SHAPE. */
 typedef struct {
@@ -82,7 +86,7 @@ int qpack_layout(int fmt, int64_t N, int64_t K, qpack_layout_t *out);
  * the super-block formats, following P1 §2.1's fp16 super-scale -> sub-block scale -> weight structure).
  *  W          [N, K] of dtype wdt (F32, F16 or BF16), 16-byte aligned
  *  codes      [N, K] int8: the signed integer q (Q4G32/Q4G32H -8..7, Q3S -4..3, Q6S -32..31, Q2S 0..3, Q5S 0..31)
- *  gscale     Q4G32: [N, K/32] fp32 group scales; NULL for other formats
+ *  gscale     Q4G32: [N, K/32], Q4G16: [N, K/16] fp32 group scales; NULL for other formats
  *  sub_scale  super-block formats: [N, K/256 * nsub] uint8 sub-block scale integers L_j; NULL for the INT4 formats
  *  sub_min    Q2S/Q5S: [N, K/256 * nsub] uint8 sub-block minimum integers M_j; NULL otherwise
  *  d, dmin    super-block formats: [N, K/256] fp16 bits of d; dmin for Q2S/Q5S only (NULL otherwise).
@@ -97,7 +101,7 @@ int qpack_quantize(int fmt, const void *W, int wdt, int64_t N, int64_t K, int8_t
  * packing (low nibble = even index) for Q4G32; P1 §2.2 cross-byte packing and §2.3 bit planes for the
  * super-block formats, bit orders of FORMATS.md §2c.
  *  packed        [N, row_stride] bytes, 16-byte aligned; padding bytes are written as zero
- *  group_scales  Q4G32: [N, scale_stride] fp32, Q4G32H: [N, scale_stride] fp16; 16-byte aligned, padding
+ *  group_scales  Q4G32, Q4G16: [N, scale_stride] fp32, Q4G32H: [N, scale_stride] fp16; 16-byte aligned, padding
  *                written as zero; NULL for the super-block formats */
 int qpack_pack(int fmt, int64_t N, int64_t K, const int8_t *codes, const float *gscale, const uint8_t *sub_scale,
                const uint8_t *sub_min, const uint16_t *d, const uint16_t *dmin, uint8_t *packed,
@@ -148,7 +152,7 @@ int qgemm_small(int fmt, const uint8_t *packed, const void *group_scales, int64_
  * contraction):
  *   Y[m, n] = sum_k bf16(X[m,k]) * bf16(w'[n,k]),  fp32 accumulation, Y rounded to bf16
  * Weight tiles are dequantized to bf16 in shared memory and fed to tcgen05 MMA with TMEM accumulators.
- *  formats  Q4G32 and Q4G32H (K a multiple of 64) and the super-block formats (K a multiple of 256)
+ *  formats  the INT4 formats (K a multiple of 64) and the super-block formats (K a multiple of 256)
  *  X        [M, ldx] bf16, 16-byte aligned, ldx >= K, ldx a multiple of 8
  *  Y        [M, ldy] bf16, 2-byte aligned, ldy >= N (16-byte aligned rows with ldy % 8 == 0 store fastest)
  * Parity bound: ||Y - Y_ref||_2 / ||Y_ref||_2 <= 2e-2 with Y_ref in fp64. */

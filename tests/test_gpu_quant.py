@@ -9,7 +9,7 @@ from conftest import to_np_fp32
 
 pytestmark = pytest.mark.gpu
 
-ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H"]
+ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H", "Q4G16"]
 DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -27,7 +27,7 @@ def weights(N, K, seed, dtype=torch.float32):
 
 def shapes(name):
     out = [(1, 256), (37, 1024), (5, 4096 + 256)]
-    if name in ("Q4G32", "Q4G32H"):
+    if name in ("Q4G32", "Q4G32H", "Q4G16"):
         out += [(9, 96), (3, 32), (6, 4096 + 160)]       # rows ending inside a 256-weight block
     return out
 
