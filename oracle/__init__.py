@@ -18,8 +18,9 @@ import threading
 
 import numpy as np
 
-Q4G32, Q2S, Q3S, Q5S, Q6S, Q4G32H, Q4G16 = 0, 1, 2, 3, 4, 5, 6
-FORMATS = {"Q4G32": Q4G32, "Q2S": Q2S, "Q3S": Q3S, "Q5S": Q5S, "Q6S": Q6S, "Q4G32H": Q4G32H, "Q4G16": Q4G16}
+Q4G32, Q2S, Q3S, Q5S, Q6S, Q4G32H, Q4G16, Q4G32A = 0, 1, 2, 3, 4, 5, 6, 7
+FORMATS = {"Q4G32": Q4G32, "Q2S": Q2S, "Q3S": Q3S, "Q5S": Q5S, "Q6S": Q6S, "Q4G32H": Q4G32H, "Q4G16": Q4G16,
+           "Q4G32A": Q4G32A}
 FLAG_RANGE = 1
 
 # (bits, sub-blocks, weights per sub-block, Lmax, asymmetric, bytes per super-block) — P1 §2.3 byte table,
@@ -161,8 +162,8 @@ def _gs(fmt, group_scales):
 def _parts(fmt, N, K):
     q = np.zeros((N, K), np.int8)
     parts = dict(q=q, gscale=None, sub_scale=None, sub_min=None, d=None, dmin=None)
-    if fmt in (Q4G32, Q4G16):
-        parts["gscale"] = np.zeros((N, K // (16 if fmt == Q4G16 else 32)), np.float32)
+    if fmt in (Q4G32, Q4G16, Q4G32A):   # Q4G32A: (scale, zero point) pairs, [N, K/16]
+        parts["gscale"] = np.zeros((N, K // (32 if fmt == Q4G32 else 16)), np.float32)
     elif fmt == Q4G32H:
         parts["d"] = np.zeros((N, K // 32), np.uint16)          # the fp16 group scales
     else:
@@ -207,7 +208,7 @@ def pack(fmt, N, K, parts):
     lay = layout(fmt, N, K)
     packed = np.zeros((N, lay["row_stride"]), np.uint8)
     gs = None
-    if fmt in (Q4G32, Q4G16):
+    if fmt in (Q4G32, Q4G16, Q4G32A):
         gs = np.zeros((N, lay["scale_stride"]), np.float32)
     elif fmt == Q4G32H:
         gs = np.zeros((N, lay["scale_stride"]), np.uint16)

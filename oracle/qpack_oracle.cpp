@@ -104,11 +104,11 @@ float bf16_to_f32(uint16_t b) { return bits_f32(uint32_t(b) << 16); }
 // Format descriptions (P1 §2.3 byte table; P2 §3.2 / §4.1 for INT4).
 // ----------------------------------------------------------------------------------------------------------
 
-enum { Q4G32 = 0, Q2S = 1, Q3S = 2, Q5S = 3, Q6S = 4, Q4G32H = 5, Q4G16 = 6 };
+enum { Q4G32 = 0, Q2S = 1, Q3S = 2, Q5S = 3, Q6S = 4, Q4G32H = 5, Q4G16 = 6, Q4G32A = 7 };
 
 // Weights per INT4 group: 32, or 16 for Q4G16.
 int int4_group(int fmt) { return fmt == Q4G16 ? 16 : 32; }
-bool is_int4(int fmt) { return fmt == Q4G32 || fmt == Q4G32H || fmt == Q4G16; }
+bool is_int4(int fmt) { return fmt == Q4G32 || fmt == Q4G32H || fmt == Q4G16 || fmt == Q4G32A; }
 
 struct SbFormat {
     int bits;      // code width b
@@ -212,6 +212,30 @@ int quantize_q4g32h_row(const float *w, int64_t K, int8_t *q, uint16_t *scales) 
         scales[g] = s16;
     }
     return flags;
+}
+
+// Asymmetric INT4, group 32 (P2 §5.1: a layer whose weight maxima stand out gets asymmetric quantization). P1 §2.1
+// defines the asymmetric form: q = rint(w / s) + z, w' = s * (q - z), with an integer zero point z. Reading (the
+// pages give no rule for s and z): the group range widened to contain 0, lo = min(0, min w), hi = max(0, max w);
+// s = max((hi - lo) / 15, 1e-12f) (the floor of P2's symmetric rule); z = clamp(rint(-lo / s), 0, 15);
+// q = clamp(rint(w / s) + z, 0, 15); dequant w' = s * (float)(q - z), so a zero weight comes back exactly as 0.
+// The group's pair goes to sm[2g] = s, sm[2g + 1] = (float)z.
+void quantize_q4g32a_row(const float *w, int64_t K, int8_t *q, float *sm) {
+    for (int64_t g = 0; g < K / 32; ++g) {
+        const float *wg = w + 32 * g;
+        float lo = 0.0f, hi = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            lo = std::fmin(lo, wg[i]);
+            hi = std::fmax(hi, wg[i]);
+        }
+        float s = (hi - lo) / 15.0f;
+        if (s < 1e-12f) s = 1e-12f;
+        const int z = int(clampf(std::nearbyint(-lo / s), 0.0f, 15.0f));
+        for (int i = 0; i < 32; ++i)
+            q[32 * g + i] = int8_t(clampf(std::nearbyint(wg[i] / s) + float(z), 0.0f, 15.0f));
+        sm[2 * g] = s;
+        sm[2 * g + 1] = float(z);
+    }
 }
 
 // Two-level round-to-nearest super-block quantizer (P1 §2.1 "fp16 super-block scale -> low-bit sub-block
@@ -413,6 +437,12 @@ void dequant_row(int fmt, const uint8_t *packed, const float *gs, int64_t K, int
         for (int64_t k = 0; k < K; ++k) {
             uint8_t byte = row[k >> 1];
             int u = (k & 1) ? (byte >> 4) : (byte & 15);
+            if (fmt == Q4G32A) {
+                const float s = gs[r * scale_stride + 2 * (k / 32)];
+                const int z = int(gs[r * scale_stride + 2 * (k / 32) + 1]);
+                out[k] = s * float(u - z);
+                continue;
+            }
             float s = fmt == Q4G32H ? f16_to_f32(gs16[r * scale_stride + k / G]) : gs[r * scale_stride + k / G];
             out[k] = s * float(u - 8);
         }
@@ -476,7 +506,7 @@ int orc_layout(int fmt, int64_t N, int64_t K, int64_t *out) {
         out[4] = 0;
         return 0;
     }
-    if (fmt == Q4G16) {
+    if (fmt == Q4G16 || fmt == Q4G32A) {     // Q4G32A: one (scale, zero point) fp32 pair per 32-group
         out[0] = K / 2;
         out[1] = N * (K / 2);
         out[2] = round_up(K / 16, 4);
@@ -510,6 +540,10 @@ int orc_quantize(int fmt, const float *W, int64_t N, int64_t K, int8_t *q, float
         for (int64_t r = 0; r < N; ++r) quantize_int4_row(W + r * K, K, 16, q + r * K, gscale + r * (K / 16));
         return 0;
     }
+    if (fmt == Q4G32A) {
+        for (int64_t r = 0; r < N; ++r) quantize_q4g32a_row(W + r * K, K, q + r * K, gscale + r * (K / 16));
+        return 0;
+    }
     if (fmt == Q4G32H) {
         for (int64_t r = 0; r < N; ++r) flags |= quantize_q4g32h_row(W + r * K, K, q + r * K, d + r * (K / 32));
         return flags;
@@ -532,11 +566,12 @@ int orc_pack(int fmt, int64_t N, int64_t K, const int8_t *q, const float *gscale
     std::memset(packed, 0, size_t(lay[1]));
     if (is_int4(fmt)) {
         uint16_t *gs16 = reinterpret_cast<uint16_t *>(group_scales);
-        const int64_t ng = K / int4_group(fmt);
+        const int64_t ng = fmt == Q4G32A ? K / 16 : K / int4_group(fmt);   // scale-array entries per row
+        const int off = fmt == Q4G32A ? 0 : 8;                              // stored nibble u = q + off
         for (int64_t r = 0; r < N; ++r) {
             uint8_t *row = packed + r * lay[0];
             for (int64_t j = 0; j < K / 2; ++j) {
-                uint8_t u0 = uint8_t(q[r * K + 2 * j] + 8), u1 = uint8_t(q[r * K + 2 * j + 1] + 8);
+                uint8_t u0 = uint8_t(q[r * K + 2 * j] + off), u1 = uint8_t(q[r * K + 2 * j + 1] + off);
                 row[j] = uint8_t((u0 & 15u) | ((u1 & 15u) << 4));
             }
             for (int64_t g = 0; g < lay[2]; ++g) {
@@ -566,13 +601,14 @@ int orc_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const float
     if (orc_layout(fmt, N, K, lay)) return -2;
     if (is_int4(fmt)) {
         const uint16_t *gs16 = reinterpret_cast<const uint16_t *>(group_scales);
-        const int64_t ng = K / int4_group(fmt);
+        const int64_t ng = fmt == Q4G32A ? K / 16 : K / int4_group(fmt);
+        const int off = fmt == Q4G32A ? 0 : 8;
         for (int64_t r = 0; r < N; ++r) {
             const uint8_t *row = packed + r * lay[0];
             for (int64_t k = 0; k < K; ++k) {
                 uint8_t byte = row[k >> 1];
                 uint8_t u = (k & 1) ? uint8_t(byte >> 4) : uint8_t(byte & 15u);
-                q[r * K + k] = int8_t(int(u) - 8);
+                q[r * K + k] = int8_t(int(u) - off);
             }
             for (int64_t g = 0; g < ng; ++g) {
                 if (fmt == Q4G32H) d[r * ng + g] = gs16[r * lay[2] + g];
