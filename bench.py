@@ -509,6 +509,9 @@ def run_ours(args, world, rank, local):
                      "int4_group16": {
                          "4096x4096": int4_4096_extra(qp, torch, synth, dev, hbm_peak, qp.Q4G16),
                          "28672x8192": int4_4096_extra(qp, torch, synth, dev, hbm_peak, qp.Q4G16, 28672, 8192)},
+                     "int4_asymmetric": {
+                         "4096x4096": int4_4096_extra(qp, torch, synth, dev, hbm_peak, qp.Q4G32A),
+                         "28672x8192": int4_4096_extra(qp, torch, synth, dev, hbm_peak, qp.Q4G32A, 28672, 8192)},
                      "small_batch_70b_mlp": small_batch_extra(qp, torch, synth, dev, hbm_peak),
                      "prefill_2048": prefill_extra(qp, torch, synth, dev, bf16_peak, hbm_peak),
                      "kv_cache_8bit": kv_cache_extra(qp, torch, synth, dev, hbm_peak)}

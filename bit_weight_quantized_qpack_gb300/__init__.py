@@ -14,8 +14,9 @@ import threading
 
 import torch
 
-Q4G32, Q2S, Q3S, Q5S, Q6S, Q4G32H, Q4G16 = 0, 1, 2, 3, 4, 5, 6
-FORMATS = {"Q4G32": Q4G32, "Q2S": Q2S, "Q3S": Q3S, "Q5S": Q5S, "Q6S": Q6S, "Q4G32H": Q4G32H, "Q4G16": Q4G16}
+Q4G32, Q2S, Q3S, Q5S, Q6S, Q4G32H, Q4G16, Q4G32A = 0, 1, 2, 3, 4, 5, 6, 7
+FORMATS = {"Q4G32": Q4G32, "Q2S": Q2S, "Q3S": Q3S, "Q5S": Q5S, "Q6S": Q6S, "Q4G32H": Q4G32H, "Q4G16": Q4G16,
+           "Q4G32A": Q4G32A}
 F32, F16, BF16 = 0, 1, 2
 FLAG_RANGE = 1
 # (sub-blocks per super-block, asymmetric) for the super-block formats
@@ -106,7 +107,7 @@ def alloc_packed(fmt, N, K, device="cuda"):
     L = layout(fmt, N, K)
     packed = torch.empty((N, L["row_stride"]), dtype=torch.uint8, device=device)
     gs = None
-    if fmt in (Q4G32, Q4G32H, Q4G16):   # fp32 or fp16 group scales
+    if fmt in (Q4G32, Q4G32H, Q4G16, Q4G32A):   # fp32 or fp16 group scales (Q4G32A: fp32 (s, z) pairs)
         gs = torch.empty((N, L["scale_stride"]), dtype=torch.float16 if fmt == Q4G32H else torch.float32, device=device)
     return packed, gs
 
@@ -114,8 +115,8 @@ def alloc_packed(fmt, N, K, device="cuda"):
 def alloc_parts(fmt, N, K, device="cuda"):
     parts = dict(q=torch.empty((N, K), dtype=torch.int8, device=device), gscale=None, sub_scale=None,
                  sub_min=None, d=None, dmin=None)
-    if fmt in (Q4G32, Q4G16):
-        parts["gscale"] = torch.empty((N, K // (16 if fmt == Q4G16 else 32)), dtype=torch.float32, device=device)
+    if fmt in (Q4G32, Q4G16, Q4G32A):
+        parts["gscale"] = torch.empty((N, K // (32 if fmt == Q4G32 else 16)), dtype=torch.float32, device=device)
     elif fmt == Q4G32H:
         parts["d"] = torch.empty((N, K // 32), dtype=torch.int16, device=device)   # fp16 group-scale bits
     else:

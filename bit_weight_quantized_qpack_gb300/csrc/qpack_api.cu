@@ -49,8 +49,10 @@ namespace {
 
 using namespace qpack;
 
-bool fmt_ok(int fmt) { return fmt >= QPACK_Q4G32 && fmt <= QPACK_Q4G16; }
-bool is_int4_fmt(int fmt) { return fmt == QPACK_Q4G32 || fmt == QPACK_Q4G32H || fmt == QPACK_Q4G16; }
+bool fmt_ok(int fmt) { return fmt >= QPACK_Q4G32 && fmt <= QPACK_Q4G32A; }
+bool is_int4_fmt(int fmt) {
+    return fmt == QPACK_Q4G32 || fmt == QPACK_Q4G32H || fmt == QPACK_Q4G16 || fmt == QPACK_Q4G32A;
+}
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct FmtInfo { int bytes, nsub; bool asym; };
@@ -70,9 +72,10 @@ int layout(int fmt, int64_t N, int64_t K, qpack_layout_t *o) {
         if (K == 0 || K % 32) return QPACK_ERR_SHAPE;
         const int64_t es = fmt == QPACK_Q4G32H ? 2 : 4;   // fp16 or fp32 group scales, rows padded to 16 bytes
         const int64_t g = fmt == QPACK_Q4G16 ? 16 : 32;    // weights per group
+        const int64_t epg = fmt == QPACK_Q4G32A ? 2 : 1;   // scale-array entries per group: Q4G32A keeps (s, z)
         o->row_stride = K / 2;
         o->packed_bytes = N * o->row_stride;
-        o->scale_stride = round_up(K / g, 16 / es);
+        o->scale_stride = round_up(epg * (K / g), 16 / es);
         o->scale_bytes = N * o->scale_stride * es;
         o->block_bytes = 0;
         o->nsub = K / g;
@@ -106,7 +109,7 @@ BlockArgs base_args(int64_t N, int64_t K, const qpack_layout_t &L) {
 int check_parts(int fmt, const void *codes, const void *gscale, const void *sub_scale, const void *sub_min,
                 const void *d, const void *dmin) {
     if (!codes || !aligned(codes, 16)) return codes ? QPACK_ERR_ALIGN : QPACK_ERR_ARG;
-    if (fmt == QPACK_Q4G32 || fmt == QPACK_Q4G16) {
+    if (fmt == QPACK_Q4G32 || fmt == QPACK_Q4G16 || fmt == QPACK_Q4G32A) {
         if (!gscale) return QPACK_ERR_ARG;
         if (!aligned(gscale, 4)) return QPACK_ERR_ALIGN;
     } else if (fmt == QPACK_Q4G32H) {                      // the fp16 group scales travel in d

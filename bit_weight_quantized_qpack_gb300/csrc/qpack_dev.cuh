@@ -11,7 +11,8 @@
 
 namespace qpack {
 
-enum : int { FMT_Q4G32 = 0, FMT_Q2S = 1, FMT_Q3S = 2, FMT_Q5S = 3, FMT_Q6S = 4, FMT_Q4G32H = 5, FMT_Q4G16 = 6 };
+enum : int { FMT_Q4G32 = 0, FMT_Q2S = 1, FMT_Q3S = 2, FMT_Q5S = 3, FMT_Q6S = 4, FMT_Q4G32H = 5, FMT_Q4G16 = 6,
+             FMT_Q4G32A = 7 };
 enum : int { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 
 // Bits OR-ed into a per-translation-unit device fault word when a bounded wait gives up.
@@ -36,8 +37,14 @@ template <> struct Fmt<FMT_Q4G16> {
     static constexpr bool asym = false, sb = false;
     static constexpr int offset = 8;
 };
-// The INT4 formats share their code layout; only the group size and the scale type differ.
-template <int F> constexpr bool kInt4 = (F == FMT_Q4G32 || F == FMT_Q4G32H || F == FMT_Q4G16);
+// INT4 asymmetric group 32: unsigned codes u = q (no offset), an fp32 (scale, zero point) pair per group.
+template <> struct Fmt<FMT_Q4G32A> {
+    static constexpr int bits = 4, nsub = 8, sublen = 32, lmax = 0, bytes = 128;
+    static constexpr bool asym = true, sb = false;
+    static constexpr int offset = 0;
+};
+// The INT4 formats share their code layout; only the group size, the offset and the scale words differ.
+template <int F> constexpr bool kInt4 = (F == FMT_Q4G32 || F == FMT_Q4G32H || F == FMT_Q4G16 || F == FMT_Q4G32A);
 template <> struct Fmt<FMT_Q2S> {
     static constexpr int bits = 2, nsub = 16, sublen = 16, lmax = 15, bytes = 84;
     static constexpr bool asym = true, sb = true;

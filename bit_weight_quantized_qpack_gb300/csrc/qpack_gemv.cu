@@ -103,6 +103,7 @@ template <int F> struct XC;
 template <> struct XC<FMT_Q4G32> { static constexpr int n = 2; };   // int -128 Sx, XS / 16
 template <> struct XC<FMT_Q4G32H> { static constexpr int n = 2; };  // as Q4G32
 template <> struct XC<FMT_Q4G16> { static constexpr int n = 3; };   // int -128 Sx_0, int -128 Sx_1, XS / 16
+template <> struct XC<FMT_Q4G32A> { static constexpr int n = 3; };  // int -16 Sx, int -(2^23 bits) * (-16 Sx), XS / 16
 template <> struct XC<FMT_Q2S> { static constexpr int n = 3; };     // Sx_0 XS, Sx_1 XS, XS
 template <> struct XC<FMT_Q3S> { static constexpr int n = 3; };     // int -128 Sx_0, int -128 Sx_1, XS / 32
 template <> struct XC<FMT_Q5S> { static constexpr int n = 2; };     // Sx XS, XS
@@ -111,7 +112,7 @@ template <> struct XC<FMT_Q6S> { static constexpr int n = 3; };     // int -128 
 struct DRow {
     uint32_t v[8];   // code words (see dp_elem)
     float f0, f1;    // sub-block scale factors D * L_j (Q4G32: the group scale; Q5S: f0 only)
-    float g0, g1;    // minima factors Dm * M_j of the asymmetric formats
+    float g0, g1;    // minima factors Dm * M_j of the asymmetric formats (Q4G32A g0: bits of z + 2^23)
 };
 
 // ------------------------------------------------------------------------------------------------------------
@@ -198,11 +199,16 @@ __device__ __forceinline__ void unpack_dp(const uint8_t *u, const uint8_t *sp, c
     r.f1 = r.g0 = r.g1 = 0.f;
     if constexpr (kInt4<F>) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
-        // the unit's group scale(s) at sp: fp32 (Q4G32), fp16 (Q4G32H), or two fp32 (Q4G16: weights 0-15, 16-31)
+        // the unit's group scale(s) at sp: fp32 (Q4G32), fp16 (Q4G32H), two fp32 (Q4G16: weights 0-15, 16-31), or
+        // the fp32 pair (s, z) (Q4G32A; z + 2^23 puts the integer z in the low mantissa bits, exactly)
         if constexpr (F == FMT_Q4G32) {
             r.f0 = on ? *reinterpret_cast<const float *>(sp) : 0.f;
         } else if constexpr (F == FMT_Q4G32H) {
             r.f0 = on ? h2f_bits(*reinterpret_cast<const uint16_t *>(sp)) : 0.f;
+        } else if constexpr (F == FMT_Q4G32A) {
+            const float2 s2 = *reinterpret_cast<const float2 *>(sp);
+            r.f0 = on ? s2.x : 0.f;
+            r.g0 = __fadd_rn(s2.y, 8388608.0f);
         } else {
             const float2 s2 = *reinterpret_cast<const float2 *>(sp);
             r.f0 = on ? s2.x : 0.f;
@@ -297,8 +303,10 @@ __device__ __forceinline__ void dot_dp(const DRow &r, const uint32_t *xv, const 
             acc = fmaf(float(16 * lo + hi), fs[g] * c[2], acc);
         }
     } else if constexpr (kInt4<F>) {
-        // lo: even weights at class 0; hi: odd weights at class 4, starting at -128 Sx (the code offset 8) -> 16 sum q x
+        // lo: even weights at class 0; hi: odd weights at class 4, starting at -128 Sx (the code offset 8) -> 16 sum q x;
+        // Q4G32A starts hi at -16 z Sx = (z + 2^23 bits) * (-16 Sx) + c[1] (exact modulo 2^32) -> 16 sum (u - z) x
         int32_t lo = 0, hi = __float_as_int(c[0]);
+        if constexpr (F == FMT_Q4G32A) hi = __float_as_int(r.g0) * hi + __float_as_int(c[1]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             lo = dp2a_lo(xv[4 * j], r.v[2 * j], lo);
@@ -306,7 +314,7 @@ __device__ __forceinline__ void dot_dp(const DRow &r, const uint32_t *xv, const 
             hi = dp2a_lo(xv[4 * j + 2], r.v[2 * j + 1], hi);
             hi = dp2a_hi(xv[4 * j + 3], r.v[2 * j + 1], hi);
         }
-        acc = fmaf(float(16 * lo + hi), r.f0 * c[1], acc);
+        acc = fmaf(float(16 * lo + hi), r.f0 * c[F == FMT_Q4G32A ? 2 : 1], acc);
     } else if constexpr (F == FMT_Q5S) {
         int32_t a = 0, b = 0;                                   // two chains, every byte at class 0
 #pragma unroll
@@ -418,6 +426,11 @@ __device__ __forceinline__ void stage_unit(const uint4 (&raw)[4], uint4 *xs, flo
         c[0] = __int_as_float(-128 * s0);
         c[1] = __int_as_float(-128 * s1);
         c[2] = exp2i(-E - 4);
+    } else if constexpr (F == FMT_Q4G32A) {
+        const int32_t c0 = -16 * (s0 + s1);
+        c[0] = __int_as_float(c0);
+        c[1] = __uint_as_float(0u - 0x4B000000u * uint32_t(c0));
+        c[2] = exp2i(-E - 4);
     } else if constexpr (kInt4<F>) {
         c[0] = __int_as_float(-128 * (s0 + s1));
         c[1] = exp2i(-E - 4);
@@ -499,7 +512,7 @@ template <int F, int MT = 1> struct T1 {
     static constexpr int PR = MT > 1 ? (256 / MT > TR ? 256 / MT : TR) : 256;     // rows per partial-sum round
     static constexpr int CB = Fmt<F>::sb ? (CHW / 256) * Fmt<F>::bytes : CHW / 2; // code bytes per row chunk
     static constexpr int SE = F == FMT_Q4G32H ? 2 : 4;                            // INT4 group-scale element bytes
-    static constexpr int SU = F == FMT_Q4G16 ? 2 * SE : SE;                       // INT4 scale bytes per 32-weight unit
+    static constexpr int SU = (F == FMT_Q4G16 || F == FMT_Q4G32A) ? 2 * SE : SE;  // INT4 scale bytes per 32-weight unit
     static constexpr int SB = Fmt<F>::sb ? 0 : (CHW / 32) * SU;                   // INT4 scale bytes per row chunk
     static constexpr int TX = TR * (CB + SB);                                     // bytes a stage receives
     static constexpr int STAGE = (TX + 127) / 128 * 128;
@@ -900,6 +913,7 @@ cudaError_t launch_gemv(int fmt, const GemvArgs &a, cudaStream_t s) {
         case FMT_Q4G32: return launch_fmt<FMT_Q4G32>(a, s);
         case FMT_Q4G32H: return launch_fmt<FMT_Q4G32H>(a, s);
         case FMT_Q4G16: return launch_fmt<FMT_Q4G16>(a, s);
+        case FMT_Q4G32A: return launch_fmt<FMT_Q4G32A>(a, s);
         case FMT_Q2S: return launch_fmt<FMT_Q2S>(a, s);
         case FMT_Q3S: return launch_fmt<FMT_Q3S>(a, s);
         case FMT_Q5S: return launch_fmt<FMT_Q5S>(a, s);

@@ -151,7 +151,7 @@ __device__ __forceinline__ void load_raw(const uint8_t *row, const uint8_t *gs_r
             r.e[0] = __float_as_uint(__ldg(reinterpret_cast<const float *>(gs_row) + u));
         } else if constexpr (F == FMT_Q4G32H) {
             r.e[0] = __float_as_uint(h2f_bits(uint16_t(ldg16(gs_row + 2 * u))));
-        } else {    // Q4G16: the scales of weights 0-15 and 16-31 of the unit
+        } else {    // Q4G16: the scales of weights 0-15 and 16-31 of the unit; Q4G32A: the pair (s, z)
             const float2 s2 = __ldg(reinterpret_cast<const float2 *>(gs_row) + u);
             r.e[0] = __float_as_uint(s2.x);
             r.e[1] = __float_as_uint(s2.y);
@@ -193,9 +193,10 @@ __device__ __forceinline__ void unit_bf16(const RawUnit &r, uint32_t u, uint32_t
     float w[32];
     if constexpr (kInt4<F>) {
         const float sc0 = __uint_as_float(r.e[0]), sc1 = F == FMT_Q4G16 ? __uint_as_float(r.e[1]) : sc0;
+        const int z = F == FMT_Q4G32A ? int(__uint_as_float(r.e[1])) : 8;     // the code offset, or the zero point
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-            w[i] = __fmul_rn(i < 16 ? sc0 : sc1, float(int((r.c[i >> 3] >> (4 * (i & 7))) & 15u) - 8));
+            w[i] = __fmul_rn(i < 16 ? sc0 : sc1, float(int((r.c[i >> 3] >> (4 * (i & 7))) & 15u) - z));
     } else if constexpr (F == FMT_Q2S) {
         const float D = h2f_bits(uint16_t(r.e[1] & 0xFFFFu)), Dm = h2f_bits(uint16_t(r.e[1] >> 16));
 #pragma unroll
@@ -489,6 +490,7 @@ cudaError_t launch_prefill(int fmt, const PrefillArgs &a, cudaStream_t s) {
         case FMT_Q4G32: return launch_prefill_f<FMT_Q4G32>(a, s);
         case FMT_Q4G32H: return launch_prefill_f<FMT_Q4G32H>(a, s);
         case FMT_Q4G16: return launch_prefill_f<FMT_Q4G16>(a, s);
+        case FMT_Q4G32A: return launch_prefill_f<FMT_Q4G32A>(a, s);
         case FMT_Q2S: return launch_prefill_f<FMT_Q2S>(a, s);
         case FMT_Q3S: return launch_prefill_f<FMT_Q3S>(a, s);
         case FMT_Q5S: return launch_prefill_f<FMT_Q5S>(a, s);

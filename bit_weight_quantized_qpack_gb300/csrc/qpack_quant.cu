@@ -23,7 +23,8 @@ struct LaneBlock {
     uint8_t u[8];     // stored codes (q + offset)
     int L, M;         // this lane's sub-block scale / minimum integers
     uint16_t d16, dm16;
-    float gscale;     // Q4G32: this lane's group scale
+    float gscale;     // INT4: this lane's group scale
+    float gzero;      // Q4G32A: the group's zero point as stored (an integer value); M holds it as an int
 };
 
 template <int F>
@@ -66,8 +67,30 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
         B.L = B.M = 0;
         B.d16 = B.dm16 = 0;
         return 0;
+    } else if constexpr (F == FMT_Q4G32A) {
+        // Asymmetric INT4 (DBHOO-CIM article §5.1) in the zero-point form w' = s (q - z) of the 2/3/5/6-bit
+        // article §2.1: the group range widened to contain 0, spread over 15 steps; z = rint(-lo / s).
+        float lo = 0.0f, hi = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { lo = fminf(lo, w[i]); hi = fmaxf(hi, w[i]); }
+        lo = sub_reduce_min<F>(lo);
+        hi = sub_reduce_max<F>(hi);
+        float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+        if (s < 1e-12f) s = 1e-12f;
+        const int z = int(clampf_ord(rintf(__fdiv_rn(-lo, s)), 0.0f, 15.0f));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float t = clampf_ord(__fadd_rn(rintf(__fdiv_rn(w[i], s)), float(z)), 0.0f, 15.0f);
+            B.u[i] = uint8_t(int(t));
+        }
+        B.gscale = s;
+        B.gzero = float(z);
+        B.M = z;
+        B.L = 0;
+        B.d16 = B.dm16 = 0;
+        return 0;
     } else if constexpr (F == FMT_Q4G32H) {
-        // P2's rule with the fp16-rounded scale (FORMATS.md §1b)
+        // P2's rule with the fp16-rounded scale
         float a = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
@@ -276,9 +299,10 @@ __device__ __forceinline__ void unpack_lane(const uint8_t *blk, int lane, bool v
 template <int F>
 __device__ __forceinline__ void dequant_lane(const LaneBlock &B, float out[8]) {
     using T = Fmt<F>;
-    if constexpr (kInt4<F>) {      // gscale: the fp32 scale, or the fp16 scale widened
+    if constexpr (kInt4<F>) {      // gscale: the fp32 scale, or the fp16 scale widened; q - z for Q4G32A
+        const int z = F == FMT_Q4G32A ? B.M : 8;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) out[i] = __fmul_rn(B.gscale, float(int(B.u[i]) - 8));
+        for (int i = 0; i < 8; ++i) out[i] = __fmul_rn(B.gscale, float(int(B.u[i]) - z));
     } else {
         const float D = h2f_bits(B.d16);
         const float es = __fmul_rn(D, float(B.L));
@@ -308,7 +332,7 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
         const int64_t k0 = 256 * b + 8 * lane;           // first weight of this lane within the row
         const bool valid = k0 < a.K;                      // only INT4 rows can end inside a block
         LaneBlock B;
-        B.gscale = 0.0f;
+        B.gscale = B.gzero = 0.0f;
         const int j = lane / (T::sublen / 8);             // this lane's group / sub-block within the block
         if constexpr (MODE == MODE_QUANT_PARTS || MODE == MODE_QUANT_PACKED) {
             float w[8];
@@ -336,6 +360,11 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
                 B.d16 = valid ? a.d[r * (a.K / 32) + 8 * b + j] : uint16_t(0);
                 B.gscale = h2f_bits(B.d16);
                 B.L = B.M = 0; B.dm16 = 0;
+            } else if constexpr (F == FMT_Q4G32A) {
+                const int64_t e = r * (a.K / 16) + 2 * (8 * b + j);
+                B.gscale = valid ? a.gscale[e] : 0.0f;
+                B.gzero = valid ? a.gscale[e + 1] : 0.0f;
+                B.L = B.M = 0; B.d16 = B.dm16 = 0;
             } else {
                 const int64_t sb = r * a.nbk + b;
                 B.L = a.sub_scale[sb * T::nsub + j];
@@ -352,6 +381,12 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
                 B.d16 = valid ? g16[r * a.scale_stride + 8 * b + j] : uint16_t(0);
                 B.gscale = h2f_bits(B.d16);
             }
+            if constexpr (F == FMT_Q4G32A) {
+                const int64_t e = r * a.scale_stride + 2 * (8 * b + j);
+                B.gscale = valid ? a.gs_in[e] : 0.0f;
+                B.gzero = valid ? a.gs_in[e + 1] : 0.0f;
+                B.M = int(B.gzero);
+            }
         }
 
         if constexpr (MODE == MODE_QUANT_PARTS || MODE == MODE_UNPACK) {
@@ -366,6 +401,12 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
                 if (valid && first_of_sub) a.gscale[r * (a.K / T::sublen) + T::nsub * b + j] = B.gscale;
             } else if constexpr (F == FMT_Q4G32H) {
                 if (valid && first_of_sub) a.d[r * (a.K / 32) + 8 * b + j] = B.d16;
+            } else if constexpr (F == FMT_Q4G32A) {
+                if (valid && first_of_sub) {
+                    const int64_t e = r * (a.K / 16) + 2 * (8 * b + j);
+                    a.gscale[e] = B.gscale;
+                    a.gscale[e + 1] = B.gzero;
+                }
             } else {
                 const int64_t sb = r * a.nbk + b;
                 if (first_of_sub) {
@@ -385,6 +426,16 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
                 if (valid && first_of_group) a.gs_out[r * a.scale_stride + T::nsub * b + j] = B.gscale;
                 if (b == a.nbk - 1) {                      // zero the scale-row padding
                     const int64_t g0 = a.K / T::sublen;
+                    if (g0 + lane < a.scale_stride) a.gs_out[r * a.scale_stride + g0 + lane] = 0.0f;
+                }
+            } else if constexpr (F == FMT_Q4G32A) {
+                if (valid && (lane & 3) == 0) {
+                    const int64_t e = r * a.scale_stride + 2 * (8 * b + j);
+                    a.gs_out[e] = B.gscale;
+                    a.gs_out[e + 1] = B.gzero;
+                }
+                if (b == a.nbk - 1) {                      // zero the scale-row padding
+                    const int64_t g0 = a.K / 16;
                     if (g0 + lane < a.scale_stride) a.gs_out[r * a.scale_stride + g0 + lane] = 0.0f;
                 }
             } else if constexpr (F == FMT_Q4G32H) {
@@ -456,7 +507,8 @@ cudaError_t launch_block_op(int fmt, int mode, int wdt, const BlockArgs &a, cuda
         case FMT_Q5S: return launch_mode<FMT_Q5S>(a, mode, wdt, s);
         case FMT_Q6S: return launch_mode<FMT_Q6S>(a, mode, wdt, s);
         case FMT_Q4G32H: return launch_mode<FMT_Q4G32H>(a, mode, wdt, s);
-        default: return launch_mode<FMT_Q4G16>(a, mode, wdt, s);
+        case FMT_Q4G16: return launch_mode<FMT_Q4G16>(a, mode, wdt, s);
+        default: return launch_mode<FMT_Q4G32A>(a, mode, wdt, s);
     }
 }
 

@@ -33,7 +33,9 @@ typedef struct CUstream_st *qpack_stream_t; /* identical to cudaStream_t */
  * Q2S/Q3S/Q5S/Q6S: 256-weight super-blocks of 84/110/176/210 bytes (P1 §2.3 byte table).
  * Q4G32H: the INT4 codes of Q4G32 with fp16 group scales (4.5 bpw, P1 §2.1; FORMATS.md §1b).
  * Q4G16: the INT4 rule of Q4G32 with groups of 16 weights, fp32 scales (6 bpw, P2 §5.1; FORMATS.md §1c); K a
- * multiple of 32. */
+ * multiple of 32.
+ * Q4G32A: INT4 asymmetric, group 32 (P2 §5.1; P1 §2.1's zero-point form w' = s*(q - z)): unsigned codes 0..15,
+ * one fp32 pair (s, z) per group with z an integer value 0..15 (6 bpw; FORMATS.md §1d). */
 typedef enum {
     QPACK_Q4G32 = 0,
     QPACK_Q2S = 1,
@@ -41,7 +43,8 @@ typedef enum {
     QPACK_Q5S = 3,
     QPACK_Q6S = 4,
     QPACK_Q4G32H = 5,
-    QPACK_Q4G16 = 6
+    QPACK_Q4G16 = 6,
+    QPACK_Q4G32A = 7
 } qpack_format;
 
 typedef enum { QPACK_F32 = 0, QPACK_F16 = 1, QPACK_BF16 = 2 } qpack_dtype;
@@ -64,8 +67,8 @@ typedef enum {
  *  row_stride    bytes between consecutive packed rows (super-block formats: rows padded to 16 B, P1 §3.3)
  *  packed_bytes  N * row_stride
  *  scale_stride  INT4 formats: elements between consecutive rows of the separate group-scale array (fp32 for
- *                Q4G32 / Q4G16, fp16 for Q4G32H; K/32 (K/16 for Q4G16) rounded up so that rows are 16 bytes,
- *                P2 §4.1); 0 otherwise
+ *                Q4G32 / Q4G16 / Q4G32A, fp16 for Q4G32H; K/32 (K/16 for Q4G16 and for Q4G32A's (s, z) pairs)
+ *                rounded up so that rows are 16 bytes, P2 §4.1); 0 otherwise
  *  scale_bytes   INT4 formats: N * scale_stride * (4 or 2); 0 otherwise
  *  block_bytes   bytes per 256-weight super-block (84/110/176/210, P1 §2.3); 0 for the INT4 formats
  *  nsub          sub-blocks per super-block (16, or 8 for Q5S); for the INT4 formats the groups per row
@@ -85,8 +88,10 @@ int qpack_layout(int fmt, int64_t N, int64_t K, qpack_layout_t *out);
 /* Quantize W into unpacked parts (P2 §3.1 for Q4G32; two-level round-to-nearest of FORMATS.md §2a/§2b for
  * the super-block formats, following P1 §2.1's fp16 super-scale -> sub-block scale -> weight structure).
  *  W          [N, K] of dtype wdt (F32, F16 or BF16), 16-byte aligned
- *  codes      [N, K] int8: the signed integer q (Q4G32/Q4G32H -8..7, Q3S -4..3, Q6S -32..31, Q2S 0..3, Q5S 0..31)
- *  gscale     Q4G32: [N, K/32], Q4G16: [N, K/16] fp32 group scales; NULL for other formats
+ *  codes      [N, K] int8: the integer q (Q4G32/Q4G32H/Q4G16 -8..7, Q4G32A 0..15, Q3S -4..3, Q6S -32..31,
+ *             Q2S 0..3, Q5S 0..31)
+ *  gscale     Q4G32: [N, K/32], Q4G16: [N, K/16] fp32 group scales; Q4G32A: [N, K/16] fp32, the pair (s, z) of
+ *             group g at 2g, 2g + 1; NULL for other formats
  *  sub_scale  super-block formats: [N, K/256 * nsub] uint8 sub-block scale integers L_j; NULL for the INT4 formats
  *  sub_min    Q2S/Q5S: [N, K/256 * nsub] uint8 sub-block minimum integers M_j; NULL otherwise
  *  d, dmin    super-block formats: [N, K/256] fp16 bits of d; dmin for Q2S/Q5S only (NULL otherwise).
@@ -101,8 +106,9 @@ int qpack_quantize(int fmt, const void *W, int wdt, int64_t N, int64_t K, int8_t
  * packing (low nibble = even index) for Q4G32; P1 §2.2 cross-byte packing and §2.3 bit planes for the
  * super-block formats, bit orders of FORMATS.md §2c.
  *  packed        [N, row_stride] bytes, 16-byte aligned; padding bytes are written as zero
- *  group_scales  Q4G32, Q4G16: [N, scale_stride] fp32, Q4G32H: [N, scale_stride] fp16; 16-byte aligned, padding
- *                written as zero; NULL for the super-block formats */
+ *  group_scales  Q4G32, Q4G16, Q4G32A: [N, scale_stride] fp32, Q4G32H: [N, scale_stride] fp16; 16-byte aligned,
+ *                padding written as zero; NULL for the super-block formats. Q4G32A pairs are copied bit for bit;
+ *                the products and qpack_dequant read z as an integer 0..15 */
 int qpack_pack(int fmt, int64_t N, int64_t K, const int8_t *codes, const float *gscale, const uint8_t *sub_scale,
                const uint8_t *sub_min, const uint16_t *d, const uint16_t *dmin, uint8_t *packed,
                void *group_scales, qpack_stream_t stream);
@@ -118,7 +124,7 @@ int qpack_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const voi
                  qpack_stream_t stream);
 
 /* Dequantize a packed matrix to fp32 out [N, K] (the page's self-check path, P1 §3.4): Q4G32 w' = s*q,
- * Q4G32H w' = fp32(s16)*q;
+ * Q4G32H w' = fp32(s16)*q; Q4G32A w' = s*(q - z);
  * symmetric super-blocks w' = (d*L_j)*q; asymmetric w' = (d*L_j)*q - (dmin*M_j), each step an fp32 rounding,
  * no FMA. Bit-identical to FORMATS.md. out must be 16-byte aligned. */
 int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const void *group_scales, float *out,

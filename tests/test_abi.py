@@ -67,6 +67,8 @@ def test_argument_validation_rejects_before_launch(qp):
     assert L.qgemv(qp.Q3S, good, None, 8, 4096 + 32, good, good, None) == SHAPE
     assert L.qgemv(qp.Q3S, odd, None, 8, 4096, good, good, None) == ALIGN
     assert L.qgemv(qp.Q4G32, good, None, 8, 4096, good, good, None) == ARG
+    assert L.qgemv(qp.Q4G32A, good, None, 8, 4096, good, good, None) == ARG
+    assert L.qpack_pack(qp.Q4G32A, 8, 4096, good, None, None, None, None, None, good, good, None) == ARG
     assert L.qgemv(9, good, good, 8, 4096, good, good, None) == ARG
     assert L.qgemv(qp.Q3S, good, None, 8, 4096, odd, good, None) == ALIGN
     assert L.qgemm_small(qp.Q5S, good, None, 8, 4096, 17, good, 4096, good, 8, None) == SHAPE

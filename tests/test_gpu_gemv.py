@@ -8,7 +8,7 @@ from conftest import gemv_bound_check, to_np_fp32
 
 pytestmark = pytest.mark.gpu
 
-ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H", "Q4G16"]
+ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H", "Q4G16", "Q4G32A"]
 
 
 def case(orc, fmt, N, K, seed, b=0.02):
@@ -28,7 +28,7 @@ def run_gemv(qpg, fmt, rp, rgs, N, K, x):
 
 def shapes(name):
     s = [(1, 256), (3, 512), (4, 4096), (37, 4096 + 768), (130, 8192 + 256), (9, 12288)]
-    if name in ("Q4G32", "Q4G32H", "Q4G16"):
+    if name in ("Q4G32", "Q4G32H", "Q4G16", "Q4G32A"):
         s += [(5, 96), (7, 4096 + 32)]
     return s
 

@@ -8,7 +8,7 @@ import torch
 
 pytestmark = pytest.mark.gpu
 
-ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H", "Q4G16"]
+ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H", "Q4G16", "Q4G32A"]
 
 
 def run_case(qpg, orc, fmt, M, N, K, seed, full=True, nsample=512):

@@ -9,7 +9,7 @@ from conftest import to_np_fp32
 
 pytestmark = pytest.mark.gpu
 
-ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H", "Q4G16"]
+ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H", "Q4G16", "Q4G32A"]
 DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -27,7 +27,7 @@ def weights(N, K, seed, dtype=torch.float32):
 
 def shapes(name):
     out = [(1, 256), (37, 1024), (5, 4096 + 256)]
-    if name in ("Q4G32", "Q4G32H", "Q4G16"):
+    if name in ("Q4G32", "Q4G32H", "Q4G16", "Q4G32A"):
         out += [(9, 96), (3, 32), (6, 4096 + 160)]       # rows ending inside a 256-weight block
     return out
 
@@ -168,3 +168,44 @@ def test_quantize_pack_large_bit_exact(qpg, orc, name):
     assert np.array_equal(packed.cpu().numpy(), rp)
     if rgs is not None:
         assert np.array_equal(gs.cpu().numpy().view(np.uint32), rgs.view(np.uint32))
+
+
+def test_q4g32a_skewed_and_degenerate_groups_bit_exact(qpg, orc):
+    """Asymmetric INT4 groups of every shape the zero-point rule distinguishes (DBHOO-CIM article §5.1; 2/3/5/6-bit
+    article §2.1): positive-only (z = 0), negative-only (z = 15), constant, all-zero (the 1e-12 floor), exact lattices
+    w = s (u - z) whose quotients land on integers, half-integer quotients (ties to even), subnormal and huge
+    magnitudes (a range near the fp32 limit), and zeros mixed into skewed groups."""
+    rng = np.random.default_rng(77)
+    G = []
+    G.append(np.abs(rng.standard_normal(32)) + 0.1)
+    G.append(-np.abs(rng.standard_normal(32)) - 0.1)
+    G.append(np.full(32, 0.3))
+    G.append(np.full(32, -2.5))
+    G.append(np.zeros(32))
+    for _ in range(8):
+        s, z = 2.0 ** rng.integers(-12, 3), rng.integers(0, 16)
+        u = rng.integers(0, 16, 32)
+        u[:2] = (0, 15)
+        G.append(s * (u - z))
+        G.append(s * (u - z + 0.5 * rng.choice([-1, 1], 32)).clip(-z, 15 - z))
+    G.append(rng.standard_normal(32) * 1e-41)
+    G.append(np.concatenate([[1.5e38, -1.5e38], rng.standard_normal(30) * 1e37]))
+    g = rng.standard_normal(32) + 2.0
+    g[rng.random(32) < 0.3] = 0.0
+    G.append(g)
+    while len(G) % 8:
+        G.append(rng.standard_normal(32))
+    W = np.concatenate(G).astype(np.float32).reshape(-1, 256)
+    N, K = W.shape
+    fmt = qpg.Q4G32A
+    parts = qpg.qpack_quantize(fmt, torch.from_numpy(W).cuda())
+    packed, gs = qpg.qpack_quantize_pack(fmt, torch.from_numpy(W).cuda())
+    deq = qpg.qpack_dequant(fmt, N, K, packed, gs)
+    torch.cuda.synchronize()
+    ref = orc.quantize(fmt, W)
+    cmp_parts(parts, ref)
+    rp, rgs = orc.pack(fmt, N, K, ref)
+    assert np.array_equal(packed.cpu().numpy(), rp)
+    assert np.array_equal(gs.cpu().numpy().view(np.uint32), rgs.view(np.uint32))
+    rdeq = orc.dequant(fmt, N, K, rp, rgs)
+    assert np.array_equal(deq.cpu().numpy().view(np.uint32), rdeq.view(np.uint32))
