@@ -1,8 +1,8 @@
 // qpack_dev.cuh — device-side building blocks shared by the qpack kernels (sm_103a).
 //
 // Format traits follow the byte table of the 2/3/5/6-bit quantization article (lpnh.cn/news/2857666, §2.3)
-// and the INT4 layout of the DBHOO-CIM article (pwwt.cn/news/4452170, §3.2, §4.1), with the bit orders fixed
-// in FORMATS.md. The PTX wrappers cover the mbarrier / bulk-copy pipeline used by the streaming kernels.
+// and the INT4 layout of the DBHOO-CIM article (pwwt.cn/news/4452170, §3.2, §4.1); where the pages leave a bit
+// order open, fields are little-endian with weight i at the lowest free bit. The PTX wrappers cover the mbarrier / bulk-copy pipeline used by the streaming kernels.
 #pragma once
 
 #include <cuda_fp16.h>

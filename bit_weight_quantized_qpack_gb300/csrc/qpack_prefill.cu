@@ -9,8 +9,8 @@
 //   warp 9      TMA producer: per 64-wide K step, four 2-D tensor copies bring the 4 x (128 x 64) bf16 X tiles into
 //               shared memory already in the 128-byte-swizzled K-major layout the MMA reads.
 //   warps 0..7  weight producers: per K step, each thread dequantizes one 32-weight unit of one of the 128 weight
-//               rows (exact fp32 dequant of FORMATS.md from aligned global loads issued three K steps ahead, then
-//               bf16 round-to-nearest-even) into the swizzled 128 x 64 weight tile; afterwards they are the epilogue warps (tcgen05.ld of their
+//               rows (the exact fp32 dequantized value, from aligned global loads issued three K steps ahead,
+//               then bf16 round-to-nearest-even) into the swizzled 128 x 64 weight tile; afterwards they are the epilogue warps (tcgen05.ld of their
 //               TMEM lane quarter, bf16 conversion, global stores).
 //   warp 8      allocates all 512 TMEM columns (four fp32 128 x 128 accumulators); lane 0 issues the tcgen05.mma
 //               instructions (M=128, N=128, K=16; both operands from shared-memory descriptors) and commits them to
@@ -135,8 +135,9 @@ __device__ __forceinline__ void ldg_words_a2(const uint8_t *p, uint32_t *w) {
 
 // Dequantization of one 32-weight unit u of a packed row, in two steps so that the loads of the next K step can be in
 // flight while the current one is converted: load_raw gathers the unit's bytes with aligned global loads,
-// unit_bf16 turns them into 16 bf16x2 words. The values are exactly those of FORMATS.md (the sub-block scale d * L
-// first, then its product with the code, minus dmin * M; every step an fp32 rounding) rounded to bf16.
+// unit_bf16 turns them into 16 bf16x2 words. The values are exactly the dequantized weights of the format (the
+// sub-block scale d * L first, then its product with the code, minus dmin * M; every step an fp32 rounding) rounded
+// to bf16.
 struct RawUnit {
     uint32_t c[5];      // code words (formats differ in how many they use)
     uint32_t e[4];      // high-bit planes / scale fields / super-block scales

@@ -3,11 +3,13 @@
 // One warp owns one 256-weight block of a row (a super-block, or eight INT4 groups); lane l owns weights
 // 8l .. 8l+7 of the block. Loads are 16-byte vectors, the per-group / per-sub-block reductions are warp
 // shuffles, and every floating-point step uses an explicitly rounded intrinsic (no FMA contraction) so that
-// codes, scales and dequantized values are bit-identical to the IEEE definition in FORMATS.md.
+// codes, scales and dequantized values are bit-identical to the formats' IEEE fp32 definition (round to nearest
+// even, true division, no FMA).
 //
 // Quantizers: INT4 group-32 per the DBHOO-CIM article (pwwt.cn/news/4452170) §3.1; two-level round-to-nearest
-// super-blocks per the 2/3/5/6-bit article (lpnh.cn/news/2857666) §2.1 and §2.3 with the reading of
-// FORMATS.md §2a/§2b. Packing: §3.2 of the INT4 article (low nibble first), §2.2 (8 three-bit codes in 3
+// super-blocks per the 2/3/5/6-bit article (lpnh.cn/news/2857666) §2.1 and §2.3 (sub-block scales from each
+// sub-block's own range, an fp16 super-block scale used rounded, integer sub-block scales against it, codes against
+// the rounded sub-block scale). Packing: §3.2 of the INT4 article (low nibble first), §2.2 (8 three-bit codes in 3
 // bytes, four 6-bit fields in 3 bytes) and §2.3 (4-bit plane + high-bit plane) of the 2/3/5/6-bit article.
 #include <cuda_runtime.h>
 
@@ -168,7 +170,7 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
 }
 
 // ------------------------------------------------------------------------------------------------------------
-// Packing of one block (layouts of FORMATS.md §1 and §2c). `blk` points at the block's first packed byte;
+// Packing of one block (byte offsets as written in each branch). `blk` points at the block's first packed byte;
 // `valid` is false for lanes beyond a partial INT4 row tail.
 // ------------------------------------------------------------------------------------------------------------
 __device__ __forceinline__ void st_u16(uint8_t *p, uint32_t v) { *reinterpret_cast<uint16_t *>(p) = uint16_t(v); }
@@ -295,7 +297,7 @@ __device__ __forceinline__ void unpack_lane(const uint8_t *blk, int lane, bool v
     }
 }
 
-// Dequantize a lane's 8 weights (FORMATS.md step 5 of each quantizer; Q4G32 w' = s * q).
+// Dequantize a lane's 8 weights (Q4G32 w' = s * q; super-blocks (d * L) * q, minus dmin * M when asymmetric).
 template <int F>
 __device__ __forceinline__ void dequant_lane(const LaneBlock &B, float out[8]) {
     using T = Fmt<F>;

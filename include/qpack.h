@@ -4,8 +4,8 @@
  * GB300 (sm_103a).
  *
  * Sources. P1 = the 2/3/5/6-bit quantization article (lpnh.cn/news/2857666); P2 = the DBHOO-CIM INT4 CPU
- * inference article (pwwt.cn/news/4452170). FORMATS.md in the source tree fixes every bit order the pages
- * leave open.
+ * inference article (pwwt.cn/news/4452170). Where the pages leave a bit order open, fields are little-endian
+ * with weight i at the lowest free bit.
  *
  * Conventions shared by every entry point:
  *  - W is row-major [N, K]: N output features (rows), K input features. Groups and super-blocks run along K.
@@ -31,11 +31,12 @@ typedef struct CUstream_st *qpack_stream_t; /* identical to cudaStream_t */
 
 /* Weight formats. Q4G32: INT4 symmetric, group 32, fp32 group scales (P2 §3.1–§3.2, §4.1).
  * Q2S/Q3S/Q5S/Q6S: 256-weight super-blocks of 84/110/176/210 bytes (P1 §2.3 byte table).
- * Q4G32H: the INT4 codes of Q4G32 with fp16 group scales (4.5 bpw, P1 §2.1; FORMATS.md §1b).
- * Q4G16: the INT4 rule of Q4G32 with groups of 16 weights, fp32 scales (6 bpw, P2 §5.1; FORMATS.md §1c); K a
+ * Q4G32H: the INT4 codes of Q4G32 with fp16 group scales, used rounded (4.5 bpw, P1 §2.1).
+ * Q4G16: the INT4 rule of Q4G32 with groups of 16 weights, fp32 scales (6 bpw, P2 §5.1); K a
  * multiple of 32.
  * Q4G32A: INT4 asymmetric, group 32 (P2 §5.1; P1 §2.1's zero-point form w' = s*(q - z)): unsigned codes 0..15,
- * one fp32 pair (s, z) per group with z an integer value 0..15 (6 bpw; FORMATS.md §1d). */
+ * one fp32 pair (s, z) per group with z an integer value 0..15 (6 bpw): lo = min(0, min w), hi = max(0, max w),
+ * s = max((hi - lo) / 15, 1e-12), z = clamp(rint(-lo / s), 0, 15), q = clamp(rint(w / s) + z, 0, 15). */
 typedef enum {
     QPACK_Q4G32 = 0,
     QPACK_Q2S = 1,
@@ -85,8 +86,9 @@ typedef struct {
 } qpack_layout_t;
 int qpack_layout(int fmt, int64_t N, int64_t K, qpack_layout_t *out);
 
-/* Quantize W into unpacked parts (P2 §3.1 for Q4G32; two-level round-to-nearest of FORMATS.md §2a/§2b for
- * the super-block formats, following P1 §2.1's fp16 super-scale -> sub-block scale -> weight structure).
+/* Quantize W into unpacked parts (P2 §3.1 for Q4G32; two-level round-to-nearest for the super-block formats,
+ * following P1 §2.1's fp16 super-scale -> sub-block scale -> weight structure: each sub-block's own scale, fp16 d
+ * (and dmin) used rounded, integer sub-block scales against it, codes against the rounded sub-block scale).
  *  W          [N, K] of dtype wdt (F32, F16 or BF16), 16-byte aligned
  *  codes      [N, K] int8: the integer q (Q4G32/Q4G32H/Q4G16 -8..7, Q4G32A 0..15, Q3S -4..3, Q6S -32..31,
  *             Q2S 0..3, Q5S 0..31)
@@ -97,14 +99,14 @@ int qpack_layout(int fmt, int64_t N, int64_t K, qpack_layout_t *out);
  *  d, dmin    super-block formats: [N, K/256] fp16 bits of d; dmin for Q2S/Q5S only (NULL otherwise).
  *             Q4G32H: d holds the [N, K/32] fp16 group scales (2-byte aligned), dmin NULL
  *  status     device int32 (may be NULL): QPACK_FLAG_RANGE is OR-ed in; the caller clears it.
- * The results are bit-identical to FORMATS.md's IEEE fp32 definition. */
+ * The results are bit-identical to the IEEE fp32 definition (round to nearest even, true division, no FMA). */
 int qpack_quantize(int fmt, const void *W, int wdt, int64_t N, int64_t K, int8_t *codes, float *gscale,
                    uint8_t *sub_scale, uint8_t *sub_min, uint16_t *d, uint16_t *dmin, int32_t *status,
                    qpack_stream_t stream);
 
 /* Pack unpacked parts (layouts as produced by qpack_quantize) into the format's bytes: P2 §3.2 nibble
  * packing (low nibble = even index) for Q4G32; P1 §2.2 cross-byte packing and §2.3 bit planes for the
- * super-block formats, bit orders of FORMATS.md §2c.
+ * super-block formats (little-endian fields, weight i at the lowest free bit).
  *  packed        [N, row_stride] bytes, 16-byte aligned; padding bytes are written as zero
  *  group_scales  Q4G32, Q4G16, Q4G32A: [N, scale_stride] fp32, Q4G32H: [N, scale_stride] fp16; 16-byte aligned,
  *                padding written as zero; NULL for the super-block formats. Q4G32A pairs are copied bit for bit;
@@ -126,7 +128,7 @@ int qpack_unpack(int fmt, int64_t N, int64_t K, const uint8_t *packed, const voi
 /* Dequantize a packed matrix to fp32 out [N, K] (the page's self-check path, P1 §3.4): Q4G32 w' = s*q,
  * Q4G32H w' = fp32(s16)*q; Q4G32A w' = s*(q - z);
  * symmetric super-blocks w' = (d*L_j)*q; asymmetric w' = (d*L_j)*q - (dmin*M_j), each step an fp32 rounding,
- * no FMA. Bit-identical to FORMATS.md. out must be 16-byte aligned. */
+ * no FMA. out must be 16-byte aligned. */
 int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const void *group_scales, float *out,
                   qpack_stream_t stream);
 

@@ -4,7 +4,7 @@ Python (ctypes + numpy) front of the plain C++ oracle in ``qpack_oracle.cpp``: t
 quantizers, packers, unpackers, dequantization and fp64-accumulated products, and the 8-bit KV-cache quantizer and
 dequantizer (P1 §4.1; the Mix-Quant article, lnrk.cn/news/34246, §2.3), written from the source pages
 (P1 = the 2/3/5/6-bit quantization article, lpnh.cn/news/2857666; P2 = the DBHOO-CIM INT4 CPU inference
-article, pwwt.cn/news/4452170) and FORMATS.md.
+article, pwwt.cn/news/4452170), with the readings of what they leave open stated in ``qpack_oracle.cpp``.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may import this package.
 It never imports the CUDA package and the CUDA package never imports it.
@@ -23,8 +23,8 @@ FORMATS = {"Q4G32": Q4G32, "Q2S": Q2S, "Q3S": Q3S, "Q5S": Q5S, "Q6S": Q6S, "Q4G3
            "Q4G32A": Q4G32A}
 FLAG_RANGE = 1
 
-# (bits, sub-blocks, weights per sub-block, Lmax, asymmetric, bytes per super-block) — P1 §2.3 byte table,
-# read as in FORMATS.md §2.
+# (bits, sub-blocks, weights per sub-block, Lmax, asymmetric, bytes per super-block) — P1 §2.3 byte table (Q5S:
+# 8 sub-blocks of 32 with 6-bit scale and minimum; Q2S: 4-bit scale and minimum; Q3S / Q6S symmetric).
 SB = {
     Q2S: (2, 16, 16, 15, True, 84),
     Q3S: (3, 16, 16, 63, False, 110),

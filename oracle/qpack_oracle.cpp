@@ -10,8 +10,8 @@
 // std::nearbyint rounds half to even).
 //
 // Sources. P1 = the 2/3/5/6-bit quantization article (lpnh.cn/news/2857666); P2 = the DBHOO-CIM INT4 CPU
-// inference article (pwwt.cn/news/4452170). Where a page leaves a choice open the reading recorded in
-// FORMATS.md is followed and named in the comment of the function that makes it.
+// inference article (pwwt.cn/news/4452170). Where a page leaves a choice open, the comment of the function that
+// makes the choice states the reading it follows.
 //
 // Pins: every function is pinned by tests under tests/ that do not re-derive it from itself (hand-computed
 // fixtures, exact lattices, one-hot products, exhaustive converter checks, round trips).
@@ -238,9 +238,13 @@ void quantize_q4g32a_row(const float *w, int64_t K, int8_t *q, float *sm) {
     }
 }
 
-// Two-level round-to-nearest super-block quantizer (P1 §2.1 "fp16 super-block scale -> low-bit sub-block
-// scale -> weight"; byte budget from P1 §2.3). The pages print no algorithm for it; the reading is the
-// one written in FORMATS.md §2a/§2b. Returns the RANGE flag if fp16(d) or fp16(dmin) overflows.
+// Two-level round-to-nearest super-block quantizer (P1 §2.1: fp16 super-block scale, then low-bit sub-block
+// scales, then the weights; byte budget from P1 §2.3). The pages print no algorithm for it. Reading: each
+// sub-block's own scale s_j (symmetric: max |w| / 2^(b-1); asymmetric: (max w - min(0, min w)) / (2^b - 1), with
+// minimum m_j = 0 - min(0, min w)); d = fp16(max_j s_j / Lmax) (dmin likewise from the m_j), used rounded; the
+// sub-block integers L_j = clamp(rint(s_j / d), 0, Lmax) (M_j likewise); the codes against the rounded sub-block
+// scale e = d * L_j: symmetric clamp(rint(w / e), -2^(b-1), 2^(b-1) - 1), asymmetric clamp(rint((w + dmin * M_j) / e),
+// 0, 2^b - 1); a zero scale gives zero integers. Returns the RANGE flag if fp16(d) or fp16(dmin) overflows.
 int quantize_sb_row(const SbFormat &F, const float *w, int64_t K, int8_t *q, uint8_t *sub_scale,
                     uint8_t *sub_min, uint16_t *d_out, uint16_t *dmin_out) {
     int flags = 0;
@@ -317,7 +321,8 @@ int quantize_sb_row(const SbFormat &F, const float *w, int64_t K, int8_t *q, uin
 }
 
 // ----------------------------------------------------------------------------------------------------------
-// Packing and unpacking of one super-block (layouts of FORMATS.md §2c) and of one INT4 row (P2 §3.2).
+// Packing and unpacking of one super-block (P1 §2.2 / §2.3; bit orders little-endian, weight i at the lowest free
+// bit, as each function states) and of one INT4 row (P2 §3.2).
 // ----------------------------------------------------------------------------------------------------------
 
 void pack_sb(int fmt, const int8_t *q, const uint8_t *L, const uint8_t *M, uint16_t d, uint16_t dmin, uint8_t *p) {
@@ -409,7 +414,8 @@ void unpack_sb(int fmt, const uint8_t *p, int8_t *q, uint8_t *L, uint8_t *M, uin
     }
 }
 
-// Dequantize one super-block from its unpacked parts (FORMATS.md §2a step 5 / §2b step 5).
+// Dequantize one super-block from its unpacked parts: w' = (d * L_j) * q (symmetric) or (d * L_j) * q - dmin * M_j
+// (asymmetric), each product and difference an fp32 rounding, no FMA.
 void dequant_sb(const SbFormat &F, int fmt, const int8_t *q, const uint8_t *L, const uint8_t *M, uint16_t d,
                 uint16_t dmin, float *out) {
     float D = f16_to_f32(d);

@@ -1,5 +1,5 @@
 """GPU parity of quantize / pack / fused quantize+pack / unpack / dequantize: every code, packed byte, scale and
-dequantized value must equal the oracle's bit for bit (FORMATS.md; DBHOO-CIM article §3.1-§3.2 for INT4,
+dequantized value must equal the oracle's bit for bit (DBHOO-CIM article §3.1-§3.2 for INT4,
 2/3/5/6-bit article §2.1-§2.3 for the super-block formats)."""
 import numpy as np
 import pytest

@@ -114,7 +114,7 @@ def test_exact_lattice(orc, name):
 
 def test_q3s_code_layout_closed_form(orc):
     # P1 §2.2 unpack3: 8 codes in 3 bytes, code t at bits 3t -> the 24-bit value is the base-8 number with
-    # digit t = u_t; stored u = q + 4 (FORMATS.md).
+    # digit t = u_t; stored u = q + 4 (offset binary for the symmetric 3-bit codes).
     rng = np.random.default_rng(30)
     u = rng.integers(0, 8, 256)
     parts = dict(q=(u - 4).astype(np.int8)[None, :], sub_scale=np.arange(16, dtype=np.uint8)[None, :] * 4 + 1,
