@@ -60,3 +60,19 @@ def test_kv_7b_cache_shape(qpg, orc):
         assert np.array_equal(sf[st // 32:(st + 4096) // 32].cpu().numpy().view(np.uint16), rs)
         assert np.array_equal(of[st:st + 4096].cpu().numpy().view(np.uint16), orc.kv_dequant(rq, rs))
     assert qpg.qpack_fetch_fault_flags() == 0
+
+
+def test_kv_rounding_boundaries(qpg, orc):
+    """Elements on and next to the half-integer multiples (k + 1/2) d of their group's scale, over scales spanning the
+    fp16 range: the codes must equal rint of the correctly rounded quotient (ties to even), as in the oracle."""
+    rng = np.random.default_rng(9)
+    G = 8192
+    m = np.exp(rng.uniform(np.log(1e-3), np.log(6e4), G)).astype(np.float16)          # each group's max |v|
+    d = (m.astype(np.float32) / np.float32(127)).astype(np.float16).astype(np.float64)
+    k = rng.integers(-127, 127, (G, 31))
+    v = ((k + 0.5) * d[:, None]).astype(np.float16)             # the tie itself where fp16 holds it, else a neighbour
+    bits = v.view(np.uint16).astype(np.int32) + rng.integers(-1, 2, (G, 31))            # and adjacent fp16 values
+    v = (bits & 0xFFFF).astype(np.uint16).view(np.float16)
+    v = np.where(np.isfinite(v.astype(np.float32)), v, np.float16(0))
+    grp = np.concatenate([m[:, None], v], axis=1).reshape(-1)
+    check(qpg, orc, torch.from_numpy(grp.copy()))
