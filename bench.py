@@ -35,9 +35,10 @@ METRIC = "fused dequant-GEMV effective weight GB/s & % of GB300 HBM peak; decode
 N_ROWS, K_COLS = 11008, 4096
 FALLBACK_HBM, FALLBACK_BF16 = 6800.0, 1900.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one headline launch from an ncu capture, valid only for the
-# CUDA sources whose digest is recorded here (profiles/gemv_q3s_11008x4096.md gives the command).
-TRAFFIC = {"csrc_digest": "4a6fac7d84da5b1f", "bytes_per_launch": 19442176}
+# dram__bytes_read.sum + dram__bytes_write.sum of one headline launch from an ncu capture (the third gemv1_kernel
+# launch of `python bench.py --ncu-case gemv --fmt Q3S --N 11008 --K 4096 --copies 12`), valid only for the CUDA
+# sources whose digest is recorded here.
+TRAFFIC = {"csrc_digest": "b01138eebdebde19", "bytes_per_launch": 19442688}
 
 
 def csrc_digest() -> str:
@@ -611,7 +612,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true", help="disable QPACK_OPT_WEIGHT_PREFETCH")
     ap.add_argument("--ncu-case", choices=["gemv", "small", "prefill", "kv", "quant"], default=None,
-                    help="short run of one product for an ncu capture (see profiles/)")
+                    help="short run of one product, sized for an ncu capture")
     ap.add_argument("--fmt", default="Q3S")
     ap.add_argument("--N", type=int, default=N_ROWS)
     ap.add_argument("--K", type=int, default=K_COLS)
