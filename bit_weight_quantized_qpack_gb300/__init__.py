@@ -230,6 +230,7 @@ def qpack_status_string(status: int) -> str:
 
 
 OPT_WEIGHT_PREFETCH = 1
+OPT_PREFILL_TILE_ROWS = 2
 
 
 def qpack_set_option(option: int, value: int) -> None:

@@ -15,6 +15,7 @@
 namespace qpack {
 
 int set_weight_prefetch(int v);
+int set_prefill_tile_rows(int v);
 
 int num_sms() {
     static int cached[64] = {0};
@@ -40,6 +41,21 @@ int set_weight_prefetch(int v) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
     g_weight_prefetch[dev] = v ? 1 : 0;
+    return 0;
+}
+
+static int g_prefill_rows[64] = {0};
+
+int prefill_tile_rows() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    return g_prefill_rows[dev];
+}
+
+int set_prefill_tile_rows(int v) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    g_prefill_rows[dev] = v;
     return 0;
 }
 
@@ -338,8 +354,12 @@ int qpack_fetch_fault_flags(int32_t *flags) {
 }
 
 int qpack_set_option(int option, int value) {
-    if (option != QPACK_OPT_WEIGHT_PREFETCH) return QPACK_ERR_ARG;
-    return set_weight_prefetch(value) == 0 ? QPACK_OK : QPACK_ERR_CUDA;
+    if (option == QPACK_OPT_WEIGHT_PREFETCH) return set_weight_prefetch(value) == 0 ? QPACK_OK : QPACK_ERR_CUDA;
+    if (option == QPACK_OPT_PREFILL_TILE_ROWS) {
+        if (value != 0 && value != 112 && value != 128) return QPACK_ERR_ARG;
+        return set_prefill_tile_rows(value) == 0 ? QPACK_OK : QPACK_ERR_CUDA;
+    }
+    return QPACK_ERR_ARG;
 }
 
 int qpack_version(void) { return 1 * 10000 + 0 * 100 + 0; }

@@ -75,5 +75,6 @@ cudaError_t fetch_fault_prefill(int32_t *flags);
 
 int num_sms();
 int weight_prefetch_enabled();   // per-device option QPACK_OPT_WEIGHT_PREFETCH
+int prefill_tile_rows();         // per-device option QPACK_OPT_PREFILL_TILE_ROWS (0: chosen per launch)
 
 }  // namespace qpack

@@ -33,16 +33,18 @@ __device__ int g_fault_prefill = 0;
 namespace {
 
 constexpr int BMS = 128, NSUB = 4, BM = BMS * NSUB;   // tokens per sub-tile, sub-tiles, tokens per CTA
-constexpr int BN = 128, BK = 64;                   // weight rows per CTA, K per stage
+constexpr int BNMAX = 128, BK = 64;                // weight rows per CTA (at most), K per stage
 constexpr int STAGES = 2;
 constexpr int A_BYTES = BMS * BK * 2;              // 16 KB per X sub-tile
-constexpr int B_BYTES = BN * BK * 2;               // 16 KB weight tile
-constexpr int STAGE_BYTES = NSUB * A_BYTES + B_BYTES;   // 80 KB (multiple of 1024)
+// Per weight-tile height BN (128, or 112 when that fills the GPU's SMs better): the BN x 64 bf16 weight tile and
+// one stage (four X sub-tiles + the weight tile; a multiple of 1024 bytes since BN is a multiple of 8).
+template <int BN> constexpr int kBBytes = BN * BK * 2;
+template <int BN> constexpr int kStageBytes = NSUB * A_BYTES + kBBytes<BN>;
 constexpr int NDQW = 8;                            // dequant / epilogue warps
 constexpr int NPROD = NDQW * 32;
 constexpr int THREADS = NPROD + 64;                // + MMA warp + TMA warp
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+template <int BN> constexpr int kSmemBytes = 1024 /*alignment slack*/ + STAGES * kStageBytes<BN> + 256 /*barriers*/;
 
 // ------------------------------------------------------------------------------------------------------------
 // tcgen05 / TMEM wrappers (PTX ISA, tcgen05 family)
@@ -105,7 +107,8 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
 }
 // Instruction descriptor, kind::f16: D fp32 (bit 4), A bf16 (bits 7-9 = 1), B bf16 (bits 10-12 = 1), both
 // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BMS >> 4) << 24);
+template <int BN>
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BMS >> 4) << 24);
 
 // Byte offset of the 16-byte chunk c (K elements 8c..8c+7) of row r inside a 128B-swizzled K-major tile.
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) {
@@ -259,8 +262,11 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 
 }  // namespace
 
-template <int F>
+template <int F, int BN>
 __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tm_x, PrefillArgs a) {
+    static_assert(BN % 16 == 0 && BN <= BNMAX, "MMA N: a multiple of 16, at most 128 (one TMEM quarter per sub-tile)");
+    constexpr int STAGE_BYTES = kStageBytes<BN>;
+    constexpr uint32_t IDESC = kIdesc<BN>;
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;           // 1024-aligned operand area
@@ -292,7 +298,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 
     if (warp < NDQW) {
         // ------------------------------ weight producers ------------------------------
-        const int r = tid & (BN - 1), h = tid / BN;                         // weight row, K half of the stage
+        const int r = tid & (BNMAX - 1), h = tid / BNMAX;                   // weight row, K half of the stage
+        const bool rin = r < BN;                                            // rows past a short tile stay idle
         const int64_t n = n0 + r;
         const uint8_t *row = a.packed + n * a.row_stride;
         constexpr int64_t SE = F == FMT_Q4G32H ? 2 : 4;                   // INT4 group-scale element bytes
@@ -300,7 +307,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         // The raw bytes of step k + 3 are loaded while step k is converted and stored: four register slots in fixed
         // roles (the loop is unrolled by four), so no slot is copied while its loads are in flight.
         RawUnit S0 = {}, S1 = {}, S2 = {}, S3 = {};
-        if (n < N) {
+        if (rin && n < N) {
             if (nk > 0) load_raw<F>(row, gs_row, uint32_t(h), S0);
             if (nk > 1) load_raw<F>(row, gs_row, uint32_t(2 + h), S1);
             if (nk > 2) load_raw<F>(row, gs_row, uint32_t(4 + h), S2);
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         auto step = [&](int kt, const RawUnit &use, RawUnit &into) {
             if (kt >= nk || dead) return;
             const int st = kt % STAGES;
-            if (n < N && kt + 3 < nk) load_raw<F>(row, gs_row, uint32_t(2 * (kt + 3) + h), into);
+            if (rin && n < N && kt + 3 < nk) load_raw<F>(row, gs_row, uint32_t(2 * (kt + 3) + h), into);
             if (kt >= STAGES && !mbar_wait_bounded(&empty[st], uint32_t((kt / STAGES) - 1) & 1u)) {
                 atomicOr(&g_fault_prefill, FAULT_WAIT_EMPTY);
                 dead = true;
@@ -325,8 +332,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 #pragma unroll
                 for (int c = 0; c < 4; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
             }
+            if (rin) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(Bs + sw128_off(uint32_t(r), uint32_t(4 * h + c))) = v[c];
+                for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(Bs + sw128_off(uint32_t(r), uint32_t(4 * h + c))) = v[c];
+            }
             fence_proxy_async_smem();      // make the generic-proxy stores visible to the tensor core
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[st]);
@@ -355,26 +364,30 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
                 const int j = 2 * half + jj;
                 if (j >= nsub) break;
                 const int64_t m = m0 + int64_t(BMS) * j + 32 * qw + lane;
-                const uint32_t lane_base = tmem_d + (uint32_t(32 * qw) << 16) + uint32_t(BN * j);
+                const uint32_t lane_base = tmem_d + (uint32_t(32 * qw) << 16) + uint32_t(BNMAX * j);
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {
+                for (int cc = 0; cc < (BN + 31) / 32; ++cc) {
                     uint32_t rr[32];
-                    tmem_ld32(lane_base + uint32_t(32 * cc), rr);
+                    tmem_ld32(lane_base + uint32_t(32 * cc), rr);   // columns past BN are read, never stored
                     tmem_ld_wait();
+                    const int w = BN - 32 * cc < 32 ? BN - 32 * cc : 32;   // columns of this chunk (16 or 32)
                     const int64_t nc = n0 + 32 * cc;
                     if (m < M && nc < N) {
                         uint16_t *dst = a.Y + m * a.ldy + nc;
-                        if (nc + 32 <= N && a.vec_y) {
+                        if (nc + w <= N && a.vec_y) {
                             uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
-                                d4[q] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * q]), __uint_as_float(rr[8 * q + 1])),
-                                                   pack_bf16x2(__uint_as_float(rr[8 * q + 2]), __uint_as_float(rr[8 * q + 3])),
-                                                   pack_bf16x2(__uint_as_float(rr[8 * q + 4]), __uint_as_float(rr[8 * q + 5])),
-                                                   pack_bf16x2(__uint_as_float(rr[8 * q + 6]), __uint_as_float(rr[8 * q + 7])));
+                                if (8 * q < w)
+                                    d4[q] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * q]), __uint_as_float(rr[8 * q + 1])),
+                                                       pack_bf16x2(__uint_as_float(rr[8 * q + 2]), __uint_as_float(rr[8 * q + 3])),
+                                                       pack_bf16x2(__uint_as_float(rr[8 * q + 4]), __uint_as_float(rr[8 * q + 5])),
+                                                       pack_bf16x2(__uint_as_float(rr[8 * q + 6]), __uint_as_float(rr[8 * q + 7])));
                         } else {
-                            for (int q = 0; q < 32 && nc + q < N; ++q)
-                                dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(rr[q])));
+#pragma unroll
+                            for (int q = 0; q < 32; ++q)
+                                if (q < w && nc + q < N)
+                                    dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(rr[q])));
                         }
                     }
                 }
@@ -395,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
                 for (int j = 0; j < nsub; ++j) {
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        umma_bf16(tmem_d + uint32_t(BN * j), sw128_kmajor_desc(As + uint32_t(j * A_BYTES) + 32u * k),
+                        umma_bf16(tmem_d + uint32_t(BNMAX * j), sw128_kmajor_desc(As + uint32_t(j * A_BYTES) + 32u * k),
                                   sw128_kmajor_desc(Bs + 32u * k), IDESC, (kt > 0 || k > 0) ? 1u : 0u);
                 }
                 umma_commit(&empty[st]);                // the stage may be refilled once these MMAs have read it
@@ -466,24 +479,40 @@ static cudaError_t encode_x(CUtensorMap *m, const PrefillArgs &a) {
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int F>
-static cudaError_t launch_prefill_f(const PrefillArgs &a, cudaStream_t s) {
+template <int F, int BN>
+static cudaError_t launch_prefill_bn(const PrefillArgs &a, const CUtensorMap &tmx, cudaStream_t s) {
     static int opted[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!opted[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<F, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes<BN>);
         if (e != cudaSuccess) return e;
         opted[dev] = 1;
     }
+    dim3 grid(unsigned((a.N + BN - 1) / BN), unsigned((a.M + BM - 1) / BM));
+    if (grid.y > 65535u) return cudaErrorInvalidValue;
+    prefill_kernel<F, BN><<<grid, THREADS, kSmemBytes<BN>, s>>>(tmx, a);
+    return cudaGetLastError();
+}
+
+// Weight-tile height: 128 rows, or 112 when that takes fewer waves of CTAs per row of weight tiles than 128 does
+// in proportion to the tile (one CTA per SM; time per CTA about proportional to its rows).
+static int prefill_bn(const PrefillArgs &a) {
+    const int64_t sms = num_sms(), mt = (a.M + BM - 1) / BM;
+    auto cost = [&](int64_t bn) { return ((a.N + bn - 1) / bn * mt + sms - 1) / sms * bn; };
+    return cost(112) < cost(128) ? 112 : 128;
+}
+
+template <int F>
+static cudaError_t launch_prefill_f(const PrefillArgs &a, cudaStream_t s) {
     CUtensorMap tmx;
     const cudaError_t e = encode_x(&tmx, a);
     if (e != cudaSuccess) return e;
-    dim3 grid(unsigned((a.N + BN - 1) / BN), unsigned((a.M + BM - 1) / BM));
-    if (grid.y > 65535u) return cudaErrorInvalidValue;
-    prefill_kernel<F><<<grid, THREADS, SMEM_BYTES, s>>>(tmx, a);
-    return cudaGetLastError();
+    const int forced = prefill_tile_rows();
+    const int bn = forced ? forced : prefill_bn(a);
+    return bn == 112 ? launch_prefill_bn<F, 112>(a, tmx, s) : launch_prefill_bn<F, 128>(a, tmx, s);
 }
 
 cudaError_t launch_prefill(int fmt, const PrefillArgs &a, cudaStream_t s) {

@@ -196,9 +196,13 @@ int qpack_fetch_fault_flags(int32_t *flags);
  *  previous kernel in the stream and start streaming their packed weights before that kernel has finished
  *  (activations are still read only after it has finished, and outputs written after). The caller guarantees
  *  that the packed weights and scales of a product are not written by the kernel launched just before it on
- *  that stream (true for a decode loop over resident weights). Returns QPACK_OK, QPACK_ERR_ARG (unknown
- *  option) or QPACK_ERR_CUDA (no current device). Host-only. */
+ *  that stream (true for a decode loop over resident weights).
+ *  QPACK_OPT_PREFILL_TILE_ROWS (default 0): weight rows per qgemm_prefill CTA tile. 0 chooses per launch (128,
+ *  or 112 when that needs fewer SM-waves in proportion to the tile); 112 or 128 forces one. Both meet the
+ *  prefill bound below.
+ * Returns QPACK_OK, QPACK_ERR_ARG (unknown option or value) or QPACK_ERR_CUDA (no current device). Host-only. */
 #define QPACK_OPT_WEIGHT_PREFETCH 1
+#define QPACK_OPT_PREFILL_TILE_ROWS 2
 int qpack_set_option(int option, int value);
 
 /* Library version: major * 10000 + minor * 100 + patch. */

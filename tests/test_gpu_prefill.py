@@ -51,11 +51,26 @@ def test_prefill_single_tile_int4(qpg, orc):
     run_case(qpg, orc, qpg.Q4G32, 128, 256, 64, 10)
 
 
+@pytest.fixture(params=[0, 112, 128], ids=["tile-auto", "tile-112", "tile-128"])
+def tile_rows(request, qpg):
+    """The weight-tile height of the prefill CTAs: chosen per launch (the default), or forced to 112 or 128 rows."""
+    qpg.qpack_set_option(qpg.OPT_PREFILL_TILE_ROWS, request.param)
+    yield request.param
+    qpg.qpack_set_option(qpg.OPT_PREFILL_TILE_ROWS, 0)
+
+
 @pytest.mark.parametrize("name", ALL)
-def test_prefill_ragged(qpg, orc, name):
+def test_prefill_ragged(qpg, orc, name, tile_rows):
     fmt = qpg.FORMATS[name]
     for i, (M, N, K) in enumerate([(128, 256, 256), (1, 300, 512), (130, 512, 256), (257, 260, 768)]):
         run_case(qpg, orc, fmt, M, N, K, 20 + i)
+
+
+def test_prefill_tile_rows_option_values(qpg):
+    L = qpg.lib()
+    assert L.qpack_set_option(qpg.OPT_PREFILL_TILE_ROWS, 96) == -1
+    assert L.qpack_set_option(99, 0) == -1
+    assert L.qpack_set_option(qpg.OPT_PREFILL_TILE_ROWS, 0) == 0
 
 
 def test_prefill_config_int4_14336x4096(qpg, orc):
