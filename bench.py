@@ -38,13 +38,15 @@ FALLBACK_HBM, FALLBACK_BF16 = 6800.0, 1900.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one headline launch from an ncu capture (the third gemv1_kernel
 # launch of `python bench.py --ncu-case gemv --fmt Q3S --N 11008 --K 4096 --copies 12`), valid only for the CUDA
 # sources whose digest is recorded here.
-TRAFFIC = {"csrc_digest": "b01138eebdebde19", "bytes_per_launch": 19442688}
+TRAFFIC = {"csrc_digest": "efd5ace630e67d2e", "bytes_per_launch": 19442688}
 
 
 def csrc_digest() -> str:
+    """Digest of the sources the batch-1 decode kernel's code comes from (its own file and the device helpers): a
+    traffic figure measured on other sources is not reported."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "bit_weight_quantized_qpack_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in ("qpack_gemv.cu", "qpack_dev.cuh"):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
