@@ -35,6 +35,7 @@ namespace {
 constexpr int BMS = 128, NSUB = 4, BM = BMS * NSUB;   // tokens per sub-tile, sub-tiles, tokens per CTA
 constexpr int BNMAX = 128, BK = 64;                // weight rows per CTA (at most), K per stage
 constexpr int STAGES = 2;
+constexpr int PD = 3;                              // K steps the packed-weight loads run ahead of the dequantization
 constexpr int A_BYTES = BMS * BK * 2;              // 16 KB per X sub-tile
 // Per weight-tile height BN (128, or 112 when that fills the GPU's SMs better): the BN x 64 bf16 weight tile and
 // one stage (four X sub-tiles + the weight tile; a multiple of 1024 bytes since BN is a multiple of 8).
@@ -304,18 +305,18 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         const uint8_t *row = a.packed + n * a.row_stride;
         constexpr int64_t SE = F == FMT_Q4G32H ? 2 : 4;                   // INT4 group-scale element bytes
         const uint8_t *gs_row = a.gscale ? reinterpret_cast<const uint8_t *>(a.gscale) + n * a.scale_stride * SE : nullptr;
-        // The raw bytes of step k + 3 are loaded while step k is converted and stored: four register slots in fixed
-        // roles (the loop is unrolled by four), so no slot is copied while its loads are in flight.
-        RawUnit S0 = {}, S1 = {}, S2 = {}, S3 = {};
+        // The raw bytes of step k + PD are loaded while step k is converted and stored: PD + 1 register slots in
+        // fixed roles (the loop is unrolled by PD + 1), so no slot is copied while its loads are in flight.
+        RawUnit S[PD + 1] = {};
         if (rin && n < N) {
-            if (nk > 0) load_raw<F>(row, gs_row, uint32_t(h), S0);
-            if (nk > 1) load_raw<F>(row, gs_row, uint32_t(2 + h), S1);
-            if (nk > 2) load_raw<F>(row, gs_row, uint32_t(4 + h), S2);
+#pragma unroll
+            for (int i = 0; i < PD; ++i)
+                if (i < nk) load_raw<F>(row, gs_row, uint32_t(2 * i + h), S[i]);
         }
         auto step = [&](int kt, const RawUnit &use, RawUnit &into) {
             if (kt >= nk || dead) return;
             const int st = kt % STAGES;
-            if (rin && n < N && kt + 3 < nk) load_raw<F>(row, gs_row, uint32_t(2 * (kt + 3) + h), into);
+            if (rin && n < N && kt + PD < nk) load_raw<F>(row, gs_row, uint32_t(2 * (kt + PD) + h), into);
             if (kt >= STAGES && !mbar_wait_bounded(&empty[st], uint32_t((kt / STAGES) - 1) & 1u)) {
                 atomicOr(&g_fault_prefill, FAULT_WAIT_EMPTY);
                 dead = true;
@@ -341,11 +342,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
             if (lane == 0) mbar_arrive(&full[st]);
         };
 #pragma unroll 1
-        for (int kt = 0; kt < nk && !dead; kt += 4) {
-            step(kt, S0, S3);
-            step(kt + 1, S1, S0);
-            step(kt + 2, S2, S1);
-            step(kt + 3, S3, S2);
+        for (int kt = 0; kt < nk && !dead; kt += PD + 1) {
+#pragma unroll
+            for (int i = 0; i <= PD; ++i) step(kt + i, S[i], S[(i + PD) % (PD + 1)]);
         }
         // ---------------------------------- epilogue ----------------------------------
         {
