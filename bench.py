@@ -33,6 +33,8 @@ if ROOT not in sys.path:
 
 METRIC = "fused dequant-GEMV effective weight GB/s & % of GB300 HBM peak; decode tok/s equiv"
 N_ROWS, K_COLS = 11008, 4096
+WORKLOAD = "3-bit super-block fused dequant-GEMV, W 11008x4096 (Laplace(0,0.015), seed 0), batch-1 fp16 x, fp32 y"
+FORMAT_DESC = "Q3S (110 B / 256 weights)"
 FALLBACK_HBM, FALLBACK_BF16 = 6800.0, 1900.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one headline launch from an ncu capture (the third gemv1_kernel
@@ -161,8 +163,8 @@ def run_reference(args, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "3-bit super-block GEMV 11008x4096, batch 1 (one full GEMV per step)",
-                       "format": "Q3S", "N": N_ROWS, "K": K_COLS, "bytes_per_gemv": int(packed.nbytes)},
+            "config": {"workload": WORKLOAD, "format": FORMAT_DESC, "N": N_ROWS, "K": K_COLS, "batch": 1,
+                       "bytes_per_gemv": int(packed.nbytes)},
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": n, "kind": "oracle",
                              "sample": f"{args.steps} full GEMVs, fp64 oracle, {n} threads"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -524,9 +526,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "3-bit super-block fused dequant-GEMV, W 11008x4096 (Laplace(0,0.015), seed 0), "
-                               "batch-1 fp16 x, fp32 y",
-                   "format": "Q3S (110 B / 256 weights)", "N": N_ROWS, "K": K_COLS, "batch": 1,
+        "config": {"workload": WORKLOAD, "format": FORMAT_DESC, "N": N_ROWS, "K": K_COLS, "batch": 1,
                    "copies_per_step": R, "bytes_per_gemv": wbytes,
                    "l2": f"inputs larger than L2: {R} distinct packed copies ({R * wbytes / 1e9:.2f} GB) per step",
                    "parallelism": "one GPU per rank; row shards need no exchange (weak-scaling replicas)",
