@@ -152,7 +152,7 @@ def test_gemv_large_activations_and_zero_rows(qpg, orc, name):
 
 
 @pytest.mark.parametrize("name", ALL)
-@pytest.mark.parametrize("M", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("M", [2, 3, 4, 6, 8, 11, 16])
 def test_small_batch(qpg, orc, name, M):
     from bit_weight_quantized_qpack_gb300 import synth
     fmt = qpg.FORMATS[name]
