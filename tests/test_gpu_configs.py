@@ -75,12 +75,14 @@ def test_config3_decode_step_layers(qpg, orc, name):
     assert qpg.qpack_fetch_fault_flags() == 0
 
 
-@pytest.mark.parametrize("name", ["Q4G32", "Q5S"])
-def test_config4_70b_mlp_small_batch(qpg, orc, name):
+@pytest.mark.parametrize("name,layers", [("Q4G32", (0, 79)), ("Q5S", (0, 79)), ("Q4G32H", (0,)), ("Q4G16", (0,)),
+                                         ("Q4G32A", (0,))])
+def test_config4_70b_mlp_small_batch(qpg, orc, name, layers):
+    """The INT4 variants (fp16 scales, group 16, asymmetric) run the same launches on layer 0."""
     from bit_weight_quantized_qpack_gb300 import synth
     fmt = qpg.FORMATS[name]
     shapes = [(28672, 8192), (28672, 8192), (8192, 28672)]
-    for layer in (0, 79):
+    for layer in layers:
         for mi, (N, K) in enumerate(shapes):
             W = synth.laplace((N, K), 0.01, seed=synth.seed_for(4, layer, mi), device="cuda")
             p, g = qpg.qpack_quantize_pack(fmt, W)
