@@ -79,6 +79,33 @@ def _check(rc: int, what: str):
         raise QpackError(f"{what}: {msg} (status {rc})")
 
 
+def _need(t, dtype, what, numel=None, rows=None, cols=None):
+    """Argument checks the C ABI cannot make (it sees only pointers): element type, size and, for matrices, a row-major
+    layout with unit column stride. Raises QpackError before anything is launched."""
+    if t.dtype != dtype:
+        raise QpackError(f"{what}: expected {dtype}, got {t.dtype}")
+    if rows is not None:
+        if t.dim() != 2 or t.shape[0] < rows or t.shape[1] < cols or (t.shape[1] > 1 and t.stride(1) != 1):
+            raise QpackError(f"{what}: expected a row-major matrix of at least {rows} x {cols}, got {tuple(t.shape)} "
+                             f"with strides {tuple(t.stride())}")
+    elif numel is not None:
+        if not t.is_contiguous() or t.numel() < numel:
+            raise QpackError(f"{what}: expected a contiguous tensor of at least {numel} elements, got "
+                             f"{tuple(t.shape)}")
+
+
+def _need_packed(fmt, N, K, packed, group_scales):
+    L = layout(fmt, N, K)
+    _need(packed, torch.uint8, "packed", numel=L["packed_bytes"])
+    if L["scale_bytes"]:
+        if group_scales is None:
+            raise QpackError("group_scales: required by this format")
+        gdt = torch.float16 if int(fmt) == Q4G32H else torch.float32
+        if group_scales.dtype == torch.int16 and gdt == torch.float16:
+            gdt = torch.int16                                   # fp16 bit patterns held as int16
+        _need(group_scales, gdt, "group_scales", numel=L["scale_bytes"] // group_scales.element_size())
+
+
 def _ptr(t):
     if t is None:
         return None
@@ -93,7 +120,12 @@ def _stream(stream=None):
 
 
 def _dt(t):
-    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[t.dtype]
+    d = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}.get(t.dtype)
+    if d is None:
+        raise QpackError(f"W: expected float32, float16 or bfloat16, got {t.dtype}")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise QpackError(f"W: expected a contiguous [N, K] matrix, got {tuple(t.shape)}")
+    return d
 
 
 def layout(fmt: int, N: int, K: int) -> dict:
@@ -131,9 +163,10 @@ def alloc_parts(fmt, N, K, device="cuda"):
 
 
 def qpack_quantize(fmt, W, parts=None, status=None, stream=None):
+    wdt = _dt(W)
     N, K = W.shape
     parts = alloc_parts(fmt, N, K, W.device) if parts is None else parts
-    rc = lib().qpack_quantize(int(fmt), _ptr(W), _dt(W), N, K, _ptr(parts["q"]), _ptr(parts["gscale"]),
+    rc = lib().qpack_quantize(int(fmt), _ptr(W), wdt, N, K, _ptr(parts["q"]), _ptr(parts["gscale"]),
                               _ptr(parts["sub_scale"]), _ptr(parts["sub_min"]), _ptr(parts["d"]),
                               _ptr(parts["dmin"]), _ptr(status), _stream(stream))
     _check(rc, "qpack_quantize")
@@ -151,10 +184,11 @@ def qpack_pack(fmt, N, K, parts, packed=None, group_scales=None, stream=None):
 
 
 def qpack_quantize_pack(fmt, W, packed=None, group_scales=None, status=None, stream=None):
+    wdt = _dt(W)
     N, K = W.shape
     if packed is None:
         packed, group_scales = alloc_packed(fmt, N, K, W.device)
-    rc = lib().qpack_quantize_pack(int(fmt), _ptr(W), _dt(W), N, K, _ptr(packed), _ptr(group_scales),
+    rc = lib().qpack_quantize_pack(int(fmt), _ptr(W), wdt, N, K, _ptr(packed), _ptr(group_scales),
                                    _ptr(status), _stream(stream))
     _check(rc, "qpack_quantize_pack")
     return packed, group_scales
@@ -177,15 +211,21 @@ def qpack_dequant(fmt, N, K, packed, group_scales=None, out=None, stream=None):
 
 
 def qgemv(fmt, packed, group_scales, N, K, x, y=None, stream=None):
+    _need_packed(fmt, N, K, packed, group_scales)
+    _need(x, torch.float16, "x", numel=K)
     y = torch.empty(N, dtype=torch.float32, device=x.device) if y is None else y
+    _need(y, torch.float32, "y", numel=N)
     rc = lib().qgemv(int(fmt), _ptr(packed), _ptr(group_scales), N, K, _ptr(x), _ptr(y), _stream(stream))
     _check(rc, "qgemv")
     return y
 
 
 def qgemm_small(fmt, packed, group_scales, N, K, X, Y=None, stream=None):
+    _need_packed(fmt, N, K, packed, group_scales)
     M = X.shape[0]
+    _need(X, torch.float16, "X", rows=M, cols=K)
     Y = torch.empty((M, N), dtype=torch.float32, device=X.device) if Y is None else Y
+    _need(Y, torch.float32, "Y", rows=M, cols=N)
     rc = lib().qgemm_small(int(fmt), _ptr(packed), _ptr(group_scales), N, K, M, _ptr(X), X.stride(0), _ptr(Y),
                            Y.stride(0), _stream(stream))
     _check(rc, "qgemm_small")
@@ -193,8 +233,11 @@ def qgemm_small(fmt, packed, group_scales, N, K, X, Y=None, stream=None):
 
 
 def qgemm_prefill(fmt, packed, group_scales, N, K, X, Y=None, stream=None):
+    _need_packed(fmt, N, K, packed, group_scales)
     M = X.shape[0]
+    _need(X, torch.bfloat16, "X", rows=M, cols=K)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    _need(Y, torch.bfloat16, "Y", rows=M, cols=N)
     rc = lib().qgemm_prefill(int(fmt), _ptr(packed), _ptr(group_scales), N, K, M, _ptr(X), X.stride(0),
                              _ptr(Y), Y.stride(0), _stream(stream))
     _check(rc, "qgemm_prefill")
@@ -205,15 +248,21 @@ def qpack_kv_quantize(v, codes=None, scales=None, stream=None):
     """fp16 KV tensor (any shape, contiguous, numel a multiple of 32) -> (int8 codes of its shape, fp16 scales
     [numel / 32]): one fp16 scale per 32 consecutive elements."""
     n = v.numel()
+    _need(v, torch.float16, "v", numel=n)
     codes = torch.empty(v.shape, dtype=torch.int8, device=v.device) if codes is None else codes
     scales = torch.empty(n // 32, dtype=torch.float16, device=v.device) if scales is None else scales
+    _need(codes, torch.int8, "codes", numel=n)
+    _need(scales, torch.float16, "scales", numel=n // 32)
     _check(lib().qpack_kv_quantize(_ptr(v), n, _ptr(codes), _ptr(scales), _stream(stream)), "qpack_kv_quantize")
     return codes, scales
 
 
 def qpack_kv_dequant(codes, scales, out=None, stream=None):
     """int8 codes + fp16 scales -> fp16 tensor of the codes' shape."""
+    _need(codes, torch.int8, "codes", numel=codes.numel())
+    _need(scales, torch.float16, "scales", numel=codes.numel() // 32)
     out = torch.empty(codes.shape, dtype=torch.float16, device=codes.device) if out is None else out
+    _need(out, torch.float16, "out", numel=codes.numel())
     _check(lib().qpack_kv_dequant(_ptr(codes), _ptr(scales), codes.numel(), _ptr(out), _stream(stream)),
            "qpack_kv_dequant")
     return out

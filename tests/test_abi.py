@@ -94,3 +94,32 @@ def test_status_strings(qp):
     for s in (0, -1, -2, -3, -4, -5, -6, 12345):
         assert qp.qpack_status_string(s)
     assert qp.qpack_version() >= 10000
+
+
+def test_binding_checks_types_and_sizes_before_any_launch(qp):
+    """The Python binding rejects tensors whose element type, size or layout the C ABI cannot see (it takes bare
+    pointers) before anything reaches the device; CPU tensors suffice since the checks come first."""
+    import pytest
+    import torch
+    N, K = 8, 256
+    L = qp.layout(qp.Q3S, N, K)
+    packed = torch.zeros((N, L["row_stride"]), dtype=torch.uint8)
+    x16 = torch.zeros(K, dtype=torch.float16)
+    with pytest.raises(qp.QpackError, match="x: expected torch.float16"):
+        qp.qgemv(qp.Q3S, packed, None, N, K, torch.zeros(K, dtype=torch.float32))
+    with pytest.raises(qp.QpackError, match="packed"):
+        qp.qgemv(qp.Q3S, packed[: N - 1], None, N, K, x16)
+    with pytest.raises(qp.QpackError, match="group_scales: required"):
+        qp.qgemv(qp.Q4G32, torch.zeros((N, K // 2), dtype=torch.uint8), None, N, K, x16)
+    with pytest.raises(qp.QpackError, match="y: expected"):
+        qp.qgemv(qp.Q3S, packed, None, N, K, x16, torch.zeros(N, dtype=torch.float16))
+    with pytest.raises(qp.QpackError, match="X: expected torch.bfloat16"):
+        qp.qgemm_prefill(qp.Q3S, packed, None, N, K, torch.zeros((4, K), dtype=torch.float16))
+    with pytest.raises(qp.QpackError, match="X: expected a row-major matrix"):
+        qp.qgemm_small(qp.Q3S, packed, None, N, K, torch.zeros((K, 4), dtype=torch.float16).t())
+    with pytest.raises(qp.QpackError, match="v: expected torch.float16"):
+        qp.qpack_kv_quantize(torch.zeros(64, dtype=torch.float32))
+    with pytest.raises(qp.QpackError, match="W: expected float32"):
+        qp.qpack_quantize_pack(qp.Q3S, torch.zeros((N, K), dtype=torch.int8))
+    with pytest.raises(qp.QpackError, match="CUDA tensors"):
+        qp.qgemv(qp.Q3S, packed, None, N, K, x16)
