@@ -262,3 +262,35 @@ def test_weight_prefetch_dependent_chain(qpg, orc):
         xb = xin.cpu().numpy().view(np.uint16)
         y_ref = orc.gemv(fmt, N, K, rp, None, xb, nthreads=8)
         gemv_bound_check(y.cpu().numpy(), y_ref, orc.dequant(fmt, N, K, rp, None), xin.cpu().numpy().astype(np.float64)[None, :])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_differential_sweep(qpg, orc, seed):
+    """Differential sweep with fixed seeds: a random format, shape and batch per case (rows 1..3000, K up to ~12K in
+    whole groups or super-blocks, M 1..16, Laplace scale over three decades); the GPU quantizes and packs (bytes
+    compared with the oracle's) and multiplies (products within the bound)."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    rng = np.random.default_rng(9000 + seed)
+    name = ALL[int(rng.integers(len(ALL)))]
+    fmt = qpg.FORMATS[name]
+    blk = 32 if name.startswith("Q4G") else 256
+    N = int(rng.integers(1, 3001))
+    K = blk * int(rng.integers(1, 12288 // blk + 1))
+    if name.startswith("Q4G") and rng.random() < 0.5:
+        K = 64 * max(1, K // 64)
+    M = int(rng.integers(1, 17))
+    b = float(10.0 ** rng.uniform(-3, 0))
+    W = synth.laplace((N, K), b, 9100 + seed)
+    p, g = qpg.qpack_quantize_pack(fmt, W.cuda())
+    rp, rgs, _ = orc.quantize_pack(fmt, W.numpy())
+    torch.cuda.synchronize()
+    assert np.array_equal(p.cpu().numpy(), rp), name
+    if rgs is not None:
+        assert np.array_equal(g.cpu().numpy().view(np.uint8), rgs.view(np.uint8)), name
+    X = synth.normal((M, K), float(10.0 ** rng.uniform(-2, 2)), 9200 + seed, dtype=torch.float16)
+    Y = qpg.qgemm_small(fmt, p, g, N, K, X.cuda()) if M > 1 else qpg.qgemv(fmt, p, g, N, K, X[0].cuda())[None, :]
+    torch.cuda.synchronize()
+    Y_ref = orc.gemm(fmt, N, K, rp, rgs, X.numpy().view(np.uint16), nthreads=8)
+    deq = orc.dequant(fmt, N, K, rp, rgs)
+    gemv_bound_check(Y.cpu().numpy(), Y_ref, deq, X.numpy().astype(np.float64))
+    assert qpg.qpack_fetch_fault_flags() == 0
