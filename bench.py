@@ -40,7 +40,7 @@ FALLBACK_HBM, FALLBACK_BF16 = 6800.0, 1900.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one headline launch from an ncu capture (the third gemv1_kernel
 # launch of `python bench.py --ncu-case gemv --fmt Q3S --N 11008 --K 4096 --copies 12`), valid only for the CUDA
 # sources whose digest is recorded here.
-TRAFFIC = {"csrc_digest": "efd5ace630e67d2e", "bytes_per_launch": 19442688}
+TRAFFIC = {"csrc_digest": "14edc04f57156a17", "bytes_per_launch": 19442688}
 
 
 def csrc_digest() -> str:

@@ -507,7 +507,7 @@ template <int F, int MT = 1> struct T1 {
     static constexpr int UPC = CHW / 32;                                          // units per chunk
     static constexpr int P = UPC / 32;                                            // K parts of 32 units
     static constexpr int RC = G1_CW / P;                                          // row classes
-    static constexpr int RW = MT > 4 ? 2 : MT > 2 ? 4 : (kInt4<F> ? 4 : (P == 4 ? 8 : 4)); // rows per warp and stage
+    static constexpr int RW = MT > 4 ? 2 : MT > 2 ? 4 : MT == 2 ? 8 : (kInt4<F> ? 4 : (P == 4 ? 8 : 4)); // rows per warp and stage
     static constexpr int TR = RC * RW;                                            // rows per tile
     static constexpr int PR = MT > 1 ? (256 / MT > TR ? 256 / MT : TR) : 256;     // rows per partial-sum round
     static constexpr int CB = Fmt<F>::sb ? (CHW / 256) * Fmt<F>::bytes : CHW / 2; // code bytes per row chunk
