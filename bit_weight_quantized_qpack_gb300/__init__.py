@@ -19,6 +19,7 @@ FORMATS = {"Q4G32": Q4G32, "Q2S": Q2S, "Q3S": Q3S, "Q5S": Q5S, "Q6S": Q6S, "Q4G3
            "Q4G32A": Q4G32A}
 F32, F16, BF16 = 0, 1, 2
 FLAG_RANGE = 1
+FAULT_NONFINITE_X = 16
 # (sub-blocks per super-block, asymmetric) for the super-block formats
 _SB = {Q2S: (16, True), Q3S: (16, False), Q5S: (8, True), Q6S: (16, False)}
 

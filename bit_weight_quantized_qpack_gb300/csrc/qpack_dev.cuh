@@ -15,8 +15,9 @@ enum : int { FMT_Q4G32 = 0, FMT_Q2S = 1, FMT_Q3S = 2, FMT_Q5S = 3, FMT_Q6S = 4, 
              FMT_Q4G32A = 7 };
 enum : int { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 
-// Bits OR-ed into a per-translation-unit device fault word when a bounded wait gives up.
-enum : int { FAULT_WAIT_FULL = 1, FAULT_WAIT_EMPTY = 2, FAULT_WAIT_MMA = 4, FAULT_WAIT_TMEM = 8 };
+// Bits OR-ed into a per-translation-unit device fault word when a bounded wait gives up, or when a decode product met
+// an inf or nan activation (its outputs are then nan; the public value is QPACK_FAULT_NONFINITE_X).
+enum : int { FAULT_WAIT_FULL = 1, FAULT_WAIT_EMPTY = 2, FAULT_WAIT_MMA = 4, FAULT_WAIT_TMEM = 8, FAULT_NONFINITE_X = 16 };
 
 template <int F> struct Fmt;
 // INT4 symmetric group 32: 16 code bytes per group, fp32 scale in a separate array.

@@ -134,22 +134,26 @@ int qpack_dequant(int fmt, int64_t N, int64_t K, const uint8_t *packed, const vo
 
 /* Fused dequant-GEMV (decode, batch 1; P1 §1.2 and §3.3, P2 §3.3 "fused dequantization"):
  *   y[r] = sum_k w'[r,k] * x[k],  r < N
- * packed weights are read exactly once and unpacked in registers. x is rounded once to 16-bit fixed point per
- * 32-element unit (step 2^-E, max |x| * 2^E in [2^14, 2^15): an element's rounding error is at most 2^-15 of its
- * unit's max |x|, and x with an exponent within 4 of that max is exact); code x activation sums are exact int32
- * within a sub-block, fp32 across sub-blocks.
+ * packed weights are read exactly once and unpacked in registers. x is rounded once to 16-bit integers per
+ * 16-element half of each 32-element unit: step sigma = m / 32767 (m = the half's largest |x|), so every staged
+ * value is within m / 65000 of x and the half's largest element is exact to 2.4e-7 relative; code x activation sums
+ * are exact int32 within a half, fp32 across halves. Worst case over all finite fp16 x, the staging moves y[r] by at
+ * most sqrt(15) / 65000 * ||w'_r||_2 * ||x||_2 = 6.0e-5 * ||w'_r||_2 * ||x||_2.
  *  packed, group_scales  as produced by qpack_pack (group_scales NULL except the INT4 formats), 16-byte aligned
  *  x                     [K] fp16, 16-byte aligned
  *  y                     [N] fp32, 4-byte aligned
  *  K                     any multiple of the format's group (rows longer than one SM's shared memory can stage go
  *                        in K splits whose products are added to y in split order)
- * Parity bound against an fp64 sum: |y[r] - y_ref[r]| <= 1e-4 * ||w'_r||_2 * ||x||_2. */
+ * Parity bound against an fp64 sum: |y[r] - y_ref[r]| <= 1e-4 * ||w'_r||_2 * ||x||_2 for every finite x.
+ * Non-finite activations: if x holds an inf or a nan, every y[r] is nan and QPACK_FAULT_NONFINITE_X is set in the
+ * fault word (qpack_fetch_fault_flags); the IEEE sum would be nan or +-inf, and the call refuses to pick one. */
 int qgemv(int fmt, const uint8_t *packed, const void *group_scales, int64_t N, int64_t K, const uint16_t *x,
           float *y, qpack_stream_t stream);
 
 /* Small-batch decode GEMM (P2 §5.2 decode vs prefill; batch up to 16):
  *   Y[m, r] = sum_k w'[r,k] * X[m,k],  m < M, r < N,  1 <= M <= 16
- * each packed weight is read once and reused across the M activation rows; activations and sums as in qgemv.
+ * each packed weight is read once and reused across the M activation rows; activations and sums as in qgemv
+ * (a non-finite activation makes every output of its row nan and sets QPACK_FAULT_NONFINITE_X).
  *  X  [M, ldx] fp16, 16-byte aligned, ldx >= K and ldx a multiple of 8
  *  Y  [M, ldy] fp32, ldy >= N
  * Same parity bound as qgemv, per element. */
@@ -187,8 +191,10 @@ int qpack_kv_dequant(const int8_t *codes, const uint16_t *scales, int64_t n, uin
 const char *qpack_status_string(int status);
 
 /* Device-side fault record: bounded waits inside the kernels that give up OR a bit into a per-device word
- * instead of hanging. Copies the current device's word to *flags (synchronous) and clears it.
+ * instead of hanging, and the decode products OR in QPACK_FAULT_NONFINITE_X when an activation was inf or nan.
+ * Copies the current device's word to *flags (synchronous) and clears it.
  * Returns QPACK_OK or QPACK_ERR_CUDA. A non-zero *flags means some kernel result is invalid. */
+#define QPACK_FAULT_NONFINITE_X 16
 int qpack_fetch_fault_flags(int32_t *flags);
 
 /* Per-device options (the device current at the call).

@@ -58,13 +58,16 @@ def test_gemv_one_hot_columns(qpg, orc, name):
         x = torch.zeros(K, dtype=torch.float16)
         x[k] = 1.0
         y = run_gemv(qpg, fmt, rp, rgs, N, K, x)
-        assert np.allclose(y, deq[:, k], rtol=1e-6, atol=1e-9 * np.abs(deq).max())
+        # the staged 1.0 is 32767 steps of fl(1/32767): exact to 2.4e-7, and the asymmetric formats subtract the
+        # minimum term separately, so a small w' can carry the roundings of its two larger terms
+        tol = 1e-6 * np.abs(deq[:, k]) + 1e-6 * np.abs(deq).max(axis=1)
+        assert np.all(np.abs(y - deq[:, k]) <= tol)
 
 
 @pytest.mark.parametrize("name", ALL)
 def test_gemv_tiny_and_mixed_magnitude_activations(qpg, orc, name):
     """The bound scales with ||x||, so it must hold for activations near the fp16 subnormal range and for vectors
-    whose entries span many binades (the staged activations are rescaled by a power of two per vector)."""
+    whose entries span many binades (the staged activations carry one step per 16 activations)."""
     from bit_weight_quantized_qpack_gb300 import synth
     fmt = qpg.FORMATS[name]
     N, K = 19, 4096 + 512
@@ -169,9 +172,10 @@ def test_small_batch(qpg, orc, name, M):
 
 
 # (N, K, M): rows whose staged activations do not fit one SM's shared memory beside the weight ring go in K splits
-# (one launch per split, the later ones adding to Y), at the 70B MLP widths, with a ragged last split.
-SMALL_BATCH_SHAPES = [(613, 8192, 16), (613, 8192, 5), (211, 28672, 16), (211, 28672, 3), (97, 28672 + 256, 16),
-                      (97, 28672 + 256, 7)]
+# (one launch per split, the later ones adding to Y), at the 70B MLP widths, with a ragged last split; at M = 2 the
+# 8-rows-per-warp tiles are full (613 rows over the SMs) and ragged (211 rows), and 28672 takes a 3-way K split.
+SMALL_BATCH_SHAPES = [(613, 8192, 16), (613, 8192, 5), (613, 8192, 2), (211, 28672, 16), (211, 28672, 3),
+                      (211, 28672, 2), (97, 28672 + 256, 16), (97, 28672 + 256, 7)]
 
 
 @pytest.mark.parametrize("name", ALL)
