@@ -62,9 +62,7 @@ def lib():
             sigs = {
                 "orc_f32_to_f16": [P, P, I64], "orc_f16_to_f32": [P, P, I64],
                 "orc_f32_to_bf16": [P, P, I64], "orc_bf16_to_f32": [P, P, I64],
-                "orc_pack3": [P, P, I64], "orc_unpack3": [P, P, I64],
-                "orc_pack5": [P, P, I64], "orc_unpack5": [P, P, I64],
-                "orc_pack6x4": [P, P, I64], "orc_unpack6x4": [P, P, I64],
+                "orc_run_pack": [P, I, I64, P], "orc_run_unpack": [P, I, I64, P],
                 "orc_layout": [I, I64, I64, P],
                 "orc_quantize": [I, P, I64, I64, P, P, P, P, P, P],
                 "orc_pack": [I, I64, I64, P, P, P, P, P, P, P, P],
@@ -79,8 +77,7 @@ def lib():
                 fn = getattr(L, name)
                 fn.argtypes = args
                 fn.restype = I if name not in ("orc_f32_to_f16", "orc_f16_to_f32", "orc_f32_to_bf16",
-                                               "orc_bf16_to_f32", "orc_pack3", "orc_unpack3", "orc_pack5",
-                                               "orc_unpack5", "orc_pack6x4", "orc_unpack6x4") else None
+                                               "orc_bf16_to_f32", "orc_run_pack", "orc_run_unpack") else None
             _lib = L
     return _lib
 
@@ -119,34 +116,16 @@ def bf16_bits_to_f32(h):
 # ---------------------------------------------------------------------------------------------------------
 # generic cross-byte packers (P1 §2.2)
 # ---------------------------------------------------------------------------------------------------------
-def pack3(codes):
-    c = _c(codes, np.uint8); n = c.size // 8; p = np.empty(3 * n, np.uint8)
-    lib().orc_pack3(_p(c), _p(p), n); return p
+def run_pack(fields, width):
+    """n fields of `width` bits laid end to end, least significant bit first (field i at bits width*i..): P1 §2.2's
+    cross-byte packing (width 3: 8 codes in 3 bytes; width 6: 4 fields in 3 bytes; width 5: 8 codes in 5 bytes)."""
+    f = _c(fields, np.uint8); n = f.size; p = np.empty((width * n + 7) // 8, np.uint8)
+    lib().orc_run_pack(_p(f), int(width), n, _p(p)); return p
 
 
-def unpack3(packed):
-    p = _c(packed, np.uint8); n = p.size // 3; q = np.empty(8 * n, np.uint8)
-    lib().orc_unpack3(_p(p), _p(q), n); return q
-
-
-def pack5(codes):
-    c = _c(codes, np.uint8); n = c.size // 8; p = np.empty(5 * n, np.uint8)
-    lib().orc_pack5(_p(c), _p(p), n); return p
-
-
-def unpack5(packed):
-    p = _c(packed, np.uint8); n = p.size // 5; q = np.empty(8 * n, np.uint8)
-    lib().orc_unpack5(_p(p), _p(q), n); return q
-
-
-def pack6x4(fields):
-    f = _c(fields, np.uint8); n = f.size // 4; p = np.empty(3 * n, np.uint8)
-    lib().orc_pack6x4(_p(f), _p(p), n); return p
-
-
-def unpack6x4(packed):
-    p = _c(packed, np.uint8); n = p.size // 3; f = np.empty(4 * n, np.uint8)
-    lib().orc_unpack6x4(_p(p), _p(f), n); return f
+def run_unpack(packed, width, n):
+    p = _c(packed, np.uint8); f = np.empty(n, np.uint8)
+    lib().orc_run_unpack(_p(p), int(width), int(n), _p(f)); return f
 
 
 # ---------------------------------------------------------------------------------------------------------

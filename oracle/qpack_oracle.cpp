@@ -134,37 +134,27 @@ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 float clampf(float v, float lo, float hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
 // ----------------------------------------------------------------------------------------------------------
-// Generic cross-byte packers (P1 §2.2): 8 three-bit codes in 3 bytes, 8 five-bit codes in 5 bytes, and four
-// six-bit fields in 3 bytes, little-endian bit order.
+// Bit runs. Every packed field of the super-block formats (P1 §2.2 cross-byte codes, §2.3 bit planes and sub-block
+// scale fields) is a "run": consecutive fields of one width w laid end to end in a little-endian bit string, field
+// i taking bits w*i .. w*i + w - 1, where bit b of the string is bit (b mod 8) of byte b / 8 (least significant bit
+// first). The two functions below move one field in or out bit by bit through that global bit index; the format
+// layouts further down are nothing but (run start, width, field index) triples.
 // ----------------------------------------------------------------------------------------------------------
 
-void pack3(const uint8_t *q, uint8_t *p) {
+void run_put(uint8_t *run, int w, int64_t i, uint32_t v) {
+    for (int k = 0; k < w; ++k) {
+        const int64_t b = int64_t(w) * i + k;                 // global bit index of bit k of field i
+        const uint8_t bit = uint8_t(1u << (b % 8));
+        if ((v >> k) & 1u) run[b / 8] |= bit; else run[b / 8] &= uint8_t(~bit);
+    }
+}
+uint32_t run_get(const uint8_t *run, int w, int64_t i) {
     uint32_t v = 0;
-    for (int i = 0; i < 8; ++i) v |= uint32_t(q[i] & 7u) << (3 * i);
-    p[0] = uint8_t(v); p[1] = uint8_t(v >> 8); p[2] = uint8_t(v >> 16);
-}
-void unpack3(const uint8_t *p, uint8_t *q) {
-    uint32_t v = uint32_t(p[0]) | (uint32_t(p[1]) << 8) | (uint32_t(p[2]) << 16);
-    for (int i = 0; i < 8; ++i) q[i] = uint8_t((v >> (3 * i)) & 7u);
-}
-void pack5(const uint8_t *q, uint8_t *p) {
-    uint64_t v = 0;
-    for (int i = 0; i < 8; ++i) v |= uint64_t(q[i] & 31u) << (5 * i);
-    for (int b = 0; b < 5; ++b) p[b] = uint8_t(v >> (8 * b));
-}
-void unpack5(const uint8_t *p, uint8_t *q) {
-    uint64_t v = 0;
-    for (int b = 0; b < 5; ++b) v |= uint64_t(p[b]) << (8 * b);
-    for (int i = 0; i < 8; ++i) q[i] = uint8_t((v >> (5 * i)) & 31u);
-}
-void pack6x4(const uint8_t *f, uint8_t *p) {
-    uint32_t v = 0;
-    for (int i = 0; i < 4; ++i) v |= uint32_t(f[i] & 63u) << (6 * i);
-    p[0] = uint8_t(v); p[1] = uint8_t(v >> 8); p[2] = uint8_t(v >> 16);
-}
-void unpack6x4(const uint8_t *p, uint8_t *f) {
-    uint32_t v = uint32_t(p[0]) | (uint32_t(p[1]) << 8) | (uint32_t(p[2]) << 16);
-    for (int i = 0; i < 4; ++i) f[i] = uint8_t((v >> (6 * i)) & 63u);
+    for (int k = 0; k < w; ++k) {
+        const int64_t b = int64_t(w) * i + k;
+        v |= uint32_t((run[b / 8] >> (b % 8)) & 1u) << k;
+    }
+    return v;
 }
 
 uint16_t rd16(const uint8_t *p) { return uint16_t(p[0] | (p[1] << 8)); }
@@ -325,92 +315,70 @@ int quantize_sb_row(const SbFormat &F, const float *w, int64_t K, int8_t *q, uin
 // bit, as each function states) and of one INT4 row (P2 §3.2).
 // ----------------------------------------------------------------------------------------------------------
 
+// Layouts (FORMATS.md §2c): Q2S codes = run of 2-bit fields at byte 0, sub-block nibbles L_j, M_j = fields 2j, 2j + 1
+// of a 4-bit run at byte 64, d at 80, dmin at 82. Q3S codes (offset q + 4) = 3-bit run at 0 (so a 3-byte group holds
+// 8 codes, P1 §2.2), L_j = 6-bit run at 96 (four fields per 3 bytes), d at 108. Q5S low nibbles = 4-bit run at 0,
+// fifth bits = 1-bit run at 128, fields L_0..7, M_0..7 = 6-bit run at 160, d at 172, dmin at 174. Q6S (offset
+// q + 32) low nibbles = 4-bit run at 0, top two bits = 2-bit run at 128, int8 L_j at 192, d at 208. fp16 values are
+// stored little-endian.
 void pack_sb(int fmt, const int8_t *q, const uint8_t *L, const uint8_t *M, uint16_t d, uint16_t dmin, uint8_t *p) {
+    SbFormat F;
+    sb_format(fmt, &F);
+    std::memset(p, 0, size_t(F.bytes));
     switch (fmt) {
-        case Q2S: {
-            std::memset(p, 0, 84);
-            for (int i = 0; i < 256; ++i) p[i >> 2] |= uint8_t((uint8_t(q[i]) & 3u) << (2 * (i & 3)));
-            for (int j = 0; j < 16; ++j) p[64 + j] = uint8_t((L[j] & 15u) | ((M[j] & 15u) << 4));
+        case Q2S:
+            for (int i = 0; i < 256; ++i) run_put(p, 2, i, uint8_t(q[i]));
+            for (int j = 0; j < 16; ++j) { run_put(p + 64, 4, 2 * j, L[j]); run_put(p + 64, 4, 2 * j + 1, M[j]); }
             wr16(p + 80, d); wr16(p + 82, dmin);
             break;
-        }
-        case Q3S: {
-            for (int g = 0; g < 32; ++g) {
-                uint8_t u[8];
-                for (int t = 0; t < 8; ++t) u[t] = uint8_t(q[8 * g + t] + 4);
-                pack3(u, p + 3 * g);
-            }
-            for (int r = 0; r < 4; ++r) pack6x4(L + 4 * r, p + 96 + 3 * r);
+        case Q3S:
+            for (int i = 0; i < 256; ++i) run_put(p, 3, i, uint32_t(q[i] + 4));
+            for (int j = 0; j < 16; ++j) run_put(p + 96, 6, j, L[j]);
             wr16(p + 108, d);
             break;
-        }
-        case Q5S: {
-            std::memset(p, 0, 176);
+        case Q5S:
             for (int i = 0; i < 256; ++i) {
-                uint8_t u = uint8_t(q[i]);
-                p[i >> 1] |= uint8_t((u & 15u) << (4 * (i & 1)));
-                p[128 + (i >> 3)] |= uint8_t(((u >> 4) & 1u) << (i & 7));
+                const uint32_t u = uint8_t(q[i]);
+                run_put(p, 4, i, u % 16);
+                run_put(p + 128, 1, i, u / 16);
             }
-            uint8_t fields[16];
-            for (int j = 0; j < 8; ++j) { fields[j] = L[j]; fields[8 + j] = M[j]; }
-            for (int r = 0; r < 4; ++r) pack6x4(fields + 4 * r, p + 160 + 3 * r);
+            for (int j = 0; j < 8; ++j) { run_put(p + 160, 6, j, L[j]); run_put(p + 160, 6, 8 + j, M[j]); }
             wr16(p + 172, d); wr16(p + 174, dmin);
             break;
-        }
-        case Q6S: {
-            std::memset(p, 0, 210);
+        case Q6S:
             for (int i = 0; i < 256; ++i) {
-                uint8_t u = uint8_t(q[i] + 32);
-                p[i >> 1] |= uint8_t((u & 15u) << (4 * (i & 1)));
-                p[128 + (i >> 2)] |= uint8_t(((u >> 4) & 3u) << (2 * (i & 3)));
+                const uint32_t u = uint32_t(q[i] + 32);
+                run_put(p, 4, i, u % 16);
+                run_put(p + 128, 2, i, u / 16);
             }
             for (int j = 0; j < 16; ++j) p[192 + j] = L[j];
             wr16(p + 208, d);
             break;
-        }
     }
 }
 
 void unpack_sb(int fmt, const uint8_t *p, int8_t *q, uint8_t *L, uint8_t *M, uint16_t *d, uint16_t *dmin) {
     switch (fmt) {
-        case Q2S: {
-            for (int i = 0; i < 256; ++i) q[i] = int8_t((p[i >> 2] >> (2 * (i & 3))) & 3u);
-            for (int j = 0; j < 16; ++j) { L[j] = p[64 + j] & 15u; M[j] = p[64 + j] >> 4; }
+        case Q2S:
+            for (int i = 0; i < 256; ++i) q[i] = int8_t(run_get(p, 2, i));
+            for (int j = 0; j < 16; ++j) { L[j] = uint8_t(run_get(p + 64, 4, 2 * j)); M[j] = uint8_t(run_get(p + 64, 4, 2 * j + 1)); }
             *d = rd16(p + 80); *dmin = rd16(p + 82);
             break;
-        }
-        case Q3S: {
-            for (int g = 0; g < 32; ++g) {
-                uint8_t u[8];
-                unpack3(p + 3 * g, u);
-                for (int t = 0; t < 8; ++t) q[8 * g + t] = int8_t(int(u[t]) - 4);
-            }
-            for (int r = 0; r < 4; ++r) unpack6x4(p + 96 + 3 * r, L + 4 * r);
+        case Q3S:
+            for (int i = 0; i < 256; ++i) q[i] = int8_t(int(run_get(p, 3, i)) - 4);
+            for (int j = 0; j < 16; ++j) L[j] = uint8_t(run_get(p + 96, 6, j));
             *d = rd16(p + 108);
             break;
-        }
-        case Q5S: {
-            for (int i = 0; i < 256; ++i) {
-                uint8_t lo = (p[i >> 1] >> (4 * (i & 1))) & 15u;
-                uint8_t hi = (p[128 + (i >> 3)] >> (i & 7)) & 1u;
-                q[i] = int8_t(lo | (hi << 4));
-            }
-            uint8_t fields[16];
-            for (int r = 0; r < 4; ++r) unpack6x4(p + 160 + 3 * r, fields + 4 * r);
-            for (int j = 0; j < 8; ++j) { L[j] = fields[j]; M[j] = fields[8 + j]; }
+        case Q5S:
+            for (int i = 0; i < 256; ++i) q[i] = int8_t(run_get(p, 4, i) + 16 * run_get(p + 128, 1, i));
+            for (int j = 0; j < 8; ++j) { L[j] = uint8_t(run_get(p + 160, 6, j)); M[j] = uint8_t(run_get(p + 160, 6, 8 + j)); }
             *d = rd16(p + 172); *dmin = rd16(p + 174);
             break;
-        }
-        case Q6S: {
-            for (int i = 0; i < 256; ++i) {
-                uint8_t lo = (p[i >> 1] >> (4 * (i & 1))) & 15u;
-                uint8_t hi = (p[128 + (i >> 2)] >> (2 * (i & 3))) & 3u;
-                q[i] = int8_t(int(lo | (hi << 4)) - 32);
-            }
+        case Q6S:
+            for (int i = 0; i < 256; ++i) q[i] = int8_t(int(run_get(p, 4, i) + 16 * run_get(p + 128, 2, i)) - 32);
             for (int j = 0; j < 16; ++j) L[j] = p[192 + j];
             *d = rd16(p + 208);
             break;
-        }
     }
 }
 
@@ -482,13 +450,14 @@ void orc_f16_to_f32(const uint16_t *x, float *y, int64_t n) { for (int64_t i = 0
 void orc_f32_to_bf16(const float *x, uint16_t *y, int64_t n) { for (int64_t i = 0; i < n; ++i) y[i] = f32_to_bf16(x[i]); }
 void orc_bf16_to_f32(const uint16_t *x, float *y, int64_t n) { for (int64_t i = 0; i < n; ++i) y[i] = bf16_to_f32(x[i]); }
 
-// ---- generic cross-byte packers (P1 §2.2), n groups at a time ----
-void orc_pack3(const uint8_t *q, uint8_t *p, int64_t ngroups) { for (int64_t g = 0; g < ngroups; ++g) pack3(q + 8 * g, p + 3 * g); }
-void orc_unpack3(const uint8_t *p, uint8_t *q, int64_t ngroups) { for (int64_t g = 0; g < ngroups; ++g) unpack3(p + 3 * g, q + 8 * g); }
-void orc_pack5(const uint8_t *q, uint8_t *p, int64_t ngroups) { for (int64_t g = 0; g < ngroups; ++g) pack5(q + 8 * g, p + 5 * g); }
-void orc_unpack5(const uint8_t *p, uint8_t *q, int64_t ngroups) { for (int64_t g = 0; g < ngroups; ++g) unpack5(p + 5 * g, q + 8 * g); }
-void orc_pack6x4(const uint8_t *f, uint8_t *p, int64_t ngroups) { for (int64_t g = 0; g < ngroups; ++g) pack6x4(f + 4 * g, p + 3 * g); }
-void orc_unpack6x4(const uint8_t *p, uint8_t *f, int64_t ngroups) { for (int64_t g = 0; g < ngroups; ++g) unpack6x4(p + 3 * g, f + 4 * g); }
+// ---- bit runs (P1 §2.2), exported for the round-trip pins: n fields of width w ----
+void orc_run_pack(const uint8_t *f, int w, int64_t n, uint8_t *p) {
+    std::memset(p, 0, size_t((int64_t(w) * n + 7) / 8));
+    for (int64_t i = 0; i < n; ++i) run_put(p, w, i, f[i]);
+}
+void orc_run_unpack(const uint8_t *p, int w, int64_t n, uint8_t *f) {
+    for (int64_t i = 0; i < n; ++i) f[i] = uint8_t(run_get(p, w, i));
+}
 
 // Layout: out[0] = packed row stride (bytes), out[1] = packed bytes, out[2] = INT4 scale row stride (elements:
 // fp32 for Q4G32, fp16 for Q4G32H, rows padded to 16 bytes; 0 otherwise), out[3] = INT4 scale bytes (0

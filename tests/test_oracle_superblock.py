@@ -196,24 +196,20 @@ def test_million_value_roundtrip(orc, name):
     assert N * K >= count
 
 
-def test_generic_packers_closed_form_and_roundtrip(orc):
+def test_bit_runs_closed_form_and_roundtrip(orc):
+    """P1 §2.2 cross-byte packing as bit runs: 8 three-bit codes in 3 bytes, 8 five-bit codes in 5 bytes and 4
+    six-bit fields in 3 bytes. A million random fields per width round-trip, and on a prefix each group's
+    little-endian byte value is the base-2^width number whose digit i is field i."""
     rng = np.random.default_rng(50)
-    n = 1_000_000 // 8 + 1
-    for width, pk, up, per in ((3, orc.pack3, orc.unpack3, 3), (5, orc.pack5, orc.unpack5, 5)):
-        c = rng.integers(0, 2 ** width, 8 * n).astype(np.uint8)
-        p = pk(c)
-        assert p.size == per * n
-        assert np.array_equal(up(p), c)
-        # closed form on a prefix: the little-endian value is the base-2^width number with digit i = code i
+    for width, per_group, group_bytes in ((3, 8, 3), (5, 8, 5), (6, 4, 3), (2, 4, 1), (4, 2, 1), (1, 8, 1)):
+        n = (1_000_000 // per_group + 1) * per_group
+        c = rng.integers(0, 2 ** width, n).astype(np.uint8)
+        p = orc.run_pack(c, width)
+        assert p.size == n // per_group * group_bytes
+        assert np.array_equal(orc.run_unpack(p, width, n), c)
         for g in range(200):
-            v = sum(int(p[per * g + b]) << (8 * b) for b in range(per))
-            assert v == sum(int(c[8 * g + i]) * (2 ** width) ** i for i in range(8))
-    f = rng.integers(0, 64, 4 * n).astype(np.uint8)
-    p = orc.pack6x4(f)
-    assert np.array_equal(orc.unpack6x4(p), f)
-    for g in range(200):
-        v = int(p[3 * g]) + 256 * int(p[3 * g + 1]) + 65536 * int(p[3 * g + 2])
-        assert v == sum(int(f[4 * g + i]) * 64 ** i for i in range(4))
+            v = sum(int(p[group_bytes * g + b]) << (8 * b) for b in range(group_bytes))
+            assert v == sum(int(c[per_group * g + i]) * (2 ** width) ** i for i in range(per_group))
 
 
 @pytest.mark.parametrize("name", FMTS)
