@@ -36,6 +36,9 @@ N_ROWS, K_COLS = 11008, 4096
 WORKLOAD = "3-bit super-block fused dequant-GEMV, W 11008x4096 (Laplace(0,0.015), seed 0), batch-1 fp16 x, fp32 y"
 FORMAT_DESC = "Q3S (110 B / 256 weights)"
 FALLBACK_HBM, FALLBACK_BF16 = 6800.0, 1900.0
+# The decode arithmetic: activations rounded to int16 per 16-element half (step max|x| / 32767), times the unsigned
+# integer codes by dp2a into exact int32 sums per half, then fp32 scaling and fp32 accumulation.
+DTYPE = "int16 x uint8 (dp2a) -> int32 per 16 activations, fp32 scale and accumulate"
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one headline launch from an ncu capture (the third gemv1_kernel
 # launch of `python bench.py --ncu-case gemv --fmt Q3S --N 11008 --K 4096 --copies 12`), valid only for the CUDA
@@ -262,6 +265,36 @@ def int4_4096_extra(qp, torch, synth, dev, hbm_peak, fmt=None, N=4096, K=4096):
     t = _time_graph(torch, fn, dev, reps=20) / R
     return {"GBps": wb / t / 1e9, "pct_hbm_peak": wb / t / 1e9 / hbm_peak, "us_per_gemv": t * 1e6,
             "bytes_per_gemv": wb, "copies": R}
+
+
+def batch1_all_formats_extra(qp, torch, synth, dev, hbm_peak, N=28672, K=8192):
+    """Batch-1 fused dequant-GEMV of every format on one 70B-shaped gate/up matrix (28672x8192, Laplace(0, 0.01),
+    seed 4), over distinct packed copies totalling at least 4x L2, back to back in one CUDA graph: the per-format
+    rate once the per-launch chain is small next to the stream."""
+    out = {}
+    W = synth.laplace((N, K), 0.01, seed=4, device=dev)
+    for name, fmt in qp.FORMATS.items():
+        p0, g0 = qp.qpack_quantize_pack(fmt, W)
+        wb = qp.layout(fmt, N, K)["weight_bytes"]
+        R = max(3, int(-(-4 * (126 << 20) // wb)))
+        P = [p0.clone() for _ in range(R)]
+        G = [None if g0 is None else g0.clone() for _ in range(R)]
+        del p0, g0
+        x = synth.normal((K,), 1.0, seed=5, device=dev, dtype=torch.float16)
+        Y = torch.empty((R, N), device=dev)
+
+        def fn(s):
+            for i in range(R):
+                qp.qgemv(fmt, P[i], G[i], N, K, x, Y[i], stream=s)
+
+        t = _time_graph(torch, fn, dev, reps=10) / R
+        out[name] = {"GBps": wb / t / 1e9, "pct_hbm_peak": wb / t / 1e9 / hbm_peak, "us_per_gemv": t * 1e6,
+                     "bytes_per_gemv": wb, "copies": R}
+        del P, G, Y
+        torch.cuda.empty_cache()
+    del W
+    torch.cuda.empty_cache()
+    return out
 
 
 def mixed_7b_extra(qp, torch, synth, dev, steps=10):
@@ -514,7 +547,8 @@ def run_ours(args, world, rank, local):
         if not args.no_extra:
             del P, X, Y
             torch.cuda.empty_cache()
-            extra = {"decode_7b": decode_7b_extra(qp, torch, synth, dev),
+            extra = {"batch1_all_formats_28672x8192": batch1_all_formats_extra(qp, torch, synth, dev, hbm_peak),
+                     "decode_7b": decode_7b_extra(qp, torch, synth, dev),
                      "decode_7b_mixed": mixed_7b_extra(qp, torch, synth, dev),
                      "int4_4096": int4_4096_extra(qp, torch, synth, dev, hbm_peak),
                      "int4_fp16_scales": {
@@ -534,7 +568,7 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
         "config": {"workload": WORKLOAD, "format": FORMAT_DESC, "N": N_ROWS, "K": K_COLS, "batch": 1,
                    "copies_per_step": R, "bytes_per_gemv": wbytes,
                    "l2": f"inputs larger than L2: {R} distinct packed copies ({R * wbytes / 1e9:.2f} GB) per step",

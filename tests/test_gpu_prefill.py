@@ -11,6 +11,17 @@ pytestmark = pytest.mark.gpu
 ALL = ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S", "Q4G32H", "Q4G16", "Q4G32A"]
 
 
+def corner_tiles(M, N, T=128):
+    """Every element of the four T x T output tiles at the corners of Y (clipped to M x N): whole CTA tiles at the
+    first and last token and weight-row positions, where a per-tile descriptor or epilogue fault would show."""
+    ms, ns = [], []
+    for m0 in sorted({0, max(0, M - T)}):
+        for n0 in sorted({0, max(0, N - T)}):
+            mm, nn = np.meshgrid(np.arange(m0, min(M, m0 + T)), np.arange(n0, min(N, n0 + T)), indexing="ij")
+            ms.append(mm.ravel()); ns.append(nn.ravel())
+    return np.concatenate(ms), np.concatenate(ns)
+
+
 def run_case(qpg, orc, fmt, M, N, K, seed, full=True, nsample=512):
     from bit_weight_quantized_qpack_gb300 import synth
     W = synth.laplace((N, K), 0.02, seed)
@@ -27,8 +38,9 @@ def run_case(qpg, orc, fmt, M, N, K, seed, full=True, nsample=512):
         ms, ns = ms.ravel(), ns.ravel()
     else:
         rng = np.random.default_rng(seed)
-        ms = rng.integers(0, M, nsample)
-        ns = rng.integers(0, N, nsample)
+        cm, cn = corner_tiles(M, N)
+        ms = np.concatenate([rng.integers(0, M, nsample), cm])
+        ns = np.concatenate([rng.integers(0, N, nsample), cn])
     order = np.argsort(ns, kind="stable")
     ms, ns = ms[order], ns[order]
     ref = orc.prefill_sample(fmt, N, K, rp, rgs, Xb, ms, ns, round_w=True)
@@ -74,8 +86,11 @@ def test_prefill_tile_rows_option_values(qpg):
 
 
 def test_prefill_config_int4_14336x4096(qpg, orc):
+    """The prefill workload's INT4 matrix at M = 2048: 512 random outputs plus the four corner 128 x 128 tiles."""
     run_case(qpg, orc, qpg.Q4G32, 2048, 14336, 4096, 7, full=False)
 
 
-def test_prefill_config_q6s_4096x14336(qpg, orc):
+def test_prefill_config_q6s_4096x14336(qpg, orc, tile_rows):
+    """The prefill workload's 6-bit matrix at M = 2048, with each weight-tile height: 512 random outputs plus the four
+    corner 128 x 128 tiles (with 112-row tiles the last corner spans two CTAs and a ragged 64-row tile)."""
     run_case(qpg, orc, qpg.Q6S, 2048, 4096, 14336, 7, full=False)

@@ -170,6 +170,25 @@ def test_quantize_pack_large_bit_exact(qpg, orc, name):
         assert np.array_equal(gs.cpu().numpy().view(np.uint32), rgs.view(np.uint32))
 
 
+@pytest.mark.parametrize("name", ["Q4G32", "Q2S", "Q3S", "Q5S", "Q6S"])
+@pytest.mark.parametrize("shape", [(14336, 4096), (4096, 14336)], ids=["14336x4096", "4096x14336"])
+def test_prefill_config_fp16_matrices_bit_exact(qpg, orc, name, shape):
+    """The prefill workload's weights exactly as the benchmark quantizes them: Laplace(0, 0.02), seed 7, held as fp16,
+    14336x4096 and 4096x14336, each of the five base formats, fused quantize+pack from fp16 on the GPU. The oracle
+    quantizes the same values widened to fp32 (exact), so packed bytes and scales must match bit for bit."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    N, K = shape
+    W16 = synth.laplace((N, K), 0.02, seed=7, dtype=torch.float16)
+    packed, gs = qpg.qpack_quantize_pack(fmt, W16.cuda())
+    torch.cuda.synchronize()
+    rp, rgs, flags = orc.quantize_pack(fmt, W16.float().numpy())
+    assert flags == 0
+    assert np.array_equal(packed.cpu().numpy(), rp)
+    if rgs is not None:
+        assert np.array_equal(gs.cpu().numpy().view(np.uint32), rgs.view(np.uint32))
+
+
 def test_q4g32a_skewed_and_degenerate_groups_bit_exact(qpg, orc):
     """Asymmetric INT4 groups of every shape the zero-point rule distinguishes (DBHOO-CIM article §5.1; 2/3/5/6-bit
     article §2.1): positive-only (z = 0), negative-only (z = 15), constant, all-zero (the 1e-12 floor), exact lattices
