@@ -167,7 +167,8 @@ int qgemm_small(int fmt, const uint8_t *packed, const void *group_scales, int64_
  *  formats  the INT4 formats (K a multiple of 64) and the super-block formats (K a multiple of 256)
  *  X        [M, ldx] bf16, 16-byte aligned, ldx >= K, ldx a multiple of 8
  *  Y        [M, ldy] bf16, 2-byte aligned, ldy >= N (16-byte aligned rows with ldy % 8 == 0 store fastest)
- * Parity bound: ||Y - Y_ref||_2 / ||Y_ref||_2 <= 2e-2 with Y_ref in fp64. */
+ * Parity bound: ||Y - Y_ref||_2 / ||Y_ref||_2 <= 2e-2 with Y_ref in fp64.
+ * No workspace argument: accumulators live in TMEM and tiles in shared memory, and Y is written directly. */
 int qgemm_prefill(int fmt, const uint8_t *packed, const void *group_scales, int64_t N, int64_t K, int64_t M,
                   const uint16_t *X, int64_t ldx, uint16_t *Y, int64_t ldy, qpack_stream_t stream);
 
