@@ -220,6 +220,7 @@ def decode_7b_extra(qp, torch, synth, dev, steps=10):
 def _time_graph(torch, fn, dev, reps=5, warm=3):
     """Capture fn (a sequence of launches on its own stream) in one CUDA graph; seconds per replay."""
     s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))     # the inputs were written on the current stream
     with torch.cuda.stream(s):
         fn(s)
         torch.cuda.synchronize(dev)
@@ -460,6 +461,7 @@ def run_ours(args, world, rank, local):
     X = synth.normal((R, K_COLS), 1.0, seed=1, device=dev, dtype=torch.float16)
     Y = torch.empty((R, N_ROWS), dtype=torch.float32, device=dev)
     s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))     # the inputs were written on the current stream
 
     def step():
         for i in range(R):
