@@ -5,7 +5,11 @@
 // lpnh.cn/news/2857666, §1.2), so it belongs on the tensor cores; the packed weights are still read in their
 // compact form and dequantized on chip (DBHOO-CIM article, pwwt.cn/news/4452170, §3.3: no fp32 weight array).
 //
-// One CTA computes a 512 x 128 block of Y (four 128-token sub-tiles x 128 weight rows):
+// Two kernels. The pair kernel (prefill_pair_kernel, further below) spreads each tensor-core instruction over a
+// cluster of two CTAs on two SMs (512 tokens x 256 weight rows per pair) and is the default for the INT4 formats
+// and the 2-bit format. The single-CTA kernel (prefill_kernel) is the default for the 3-, 5- and 6-bit formats.
+//
+// Single-CTA kernel: one CTA computes a 512 x 128 block of Y (four 128-token sub-tiles x 128 weight rows):
 //   warp 9      TMA producer: per 64-wide K step, four 2-D tensor copies bring the 4 x (128 x 64) bf16 X tiles into
 //               shared memory already in the 128-byte-swizzled K-major layout the MMA reads.
 //   warps 0..7  weight producers: per K step, each thread dequantizes one 32-weight unit of one of the 128 weight
@@ -261,6 +265,76 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+
+// ------------------------------------------------------------------------------------------------------------
+// CTA-pair (cluster of two) building blocks for the pair kernel below (PTX ISA: tcgen05 with .cta_group::2,
+// mapa, cluster-scope mbarrier arrive / try_wait, barrier.cluster).
+// ------------------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t cta_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(cta_addr), "r"(rank));
+    return r;
+}
+// Arrive on an mbarrier anywhere in the cluster, releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait on a local mbarrier whose arrivals may come from the peer CTA (false after `limit` polls).
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t parity, uint32_t limit = (1u << 22)) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+    return false;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// TMEM allocation for a CTA pair: one warp of each of the two CTAs executes these together.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D (both CTAs' TMEM) (+)= A (M/2 rows in each CTA's shared memory) x B (N/2 rows in each)^T, issued by one
+// thread of the even CTA.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask` when the pair MMAs issued so far are done.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"(cta_mask)
+        : "memory");
+}
 }  // namespace
 
 template <int F, int BN>
@@ -447,6 +521,237 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     }
 }
 
+
+// ------------------------------------------------------------------------------------------------------------
+// Pair kernel: a cluster of two CTAs on two SMs computes a 512 x 256 block of Y with tcgen05.mma.cta_group::2
+// (M = 256 tokens, N = 256 weight rows per instruction). CTA r of the pair holds, per 64-wide K step,
+//   A: two 128 x 64 bf16 X tiles (tokens m0 + 256 j + 128 r .. +127 of token sub-tile j = 0, 1), by TMA,
+//   B: the 128 x 64 bf16 weight tile of its own weight rows n0 + 128 r .. +127, dequantized by its warps 0..7,
+// and its TMEM receives the 128 x 256 fp32 accumulators of its own tokens for both sub-tiles (all 512 columns).
+// Each SM thus reads 8 KB of operands per 256 x 256 x 16 MMA instead of the 8 KB per 128 x 128 x 16 of the
+// single-CTA kernel, and still dequantizes each weight once per 512 tokens.
+//   warps 0..7    dequant (arriving on the local wfull barrier), then epilogue (tcgen05.ld of their TMEM lane
+//                 quarter, bf16 stores)
+//   warp 8        TMEM allocation (both CTAs, together); lane 0 of the even CTA issues the MMAs
+//   warp 9        lane 0: X tiles by TMA into this CTA's stage (completion on the local xfull barrier)
+//   warps 10..13  lane 0 of warp 10 + st forwards stage st: once this CTA's xfull[st] and wfull[st] phases have
+//                 completed, one cluster-scope release-arrive on the even CTA's full[st]
+// The even CTA's full[st] completes with the two CTAs' forwarding arrivals. A cluster-scope release costs ~0.6 us
+// (measured with globaltimer stamps), so it is made by threads with no loads in flight, one warp per ring stage so
+// that the releases of consecutive stages overlap (one forwarding thread for all stages, or the dequant warps
+// arriving across the cluster themselves, held the kernel below the single-CTA one). The MMA commits arrive on
+// empty[st] and, at the end, on accum in both CTAs (multicast).
+// ------------------------------------------------------------------------------------------------------------
+namespace {
+constexpr int P2_NSUB = 2;                                 // token sub-tiles (pair MMAs of M = 256)
+constexpr int P2_ROWS = 128;                               // weight rows per CTA (pair N = 256)
+constexpr int P2_STAGES = 4;
+constexpr int P2_STAGE = P2_NSUB * A_BYTES + P2_ROWS * BK * 2;     // 48 KB
+constexpr int P2_NFWD = P2_STAGES;                         // forwarding warps: stage st is forwarded by warp NDQW + 2 + st
+constexpr int P2_THREADS = NPROD + 64 + 32 * P2_NFWD;      // + MMA warp, TMA warp, forwarding warps
+constexpr int P2_SMEM = 1024 + P2_STAGES * P2_STAGE + 256;
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, N = 256 (N >> 3 at bits 17-22),
+// M = 256 (M >> 4 at bits 24-28).
+constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(256 >> 3) << 17) | (uint32_t(256 >> 4) << 24);
+}  // namespace
+
+template <int F>
+__global__ void __launch_bounds__(P2_THREADS, 1) prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_x, PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;           // 1024-aligned operand area
+    uint8_t *sm = smem_raw + (base - smem_u32(smem_raw));
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + P2_STAGES * P2_STAGE);   // used in the even CTA
+    uint64_t *empty = full + P2_STAGES;
+    uint64_t *xfull = empty + P2_STAGES;
+    uint64_t *wfull = xfull + P2_STAGES;                                     // this CTA's weight tile stored
+    uint64_t *accum = wfull + P2_STAGES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int64_t M = a.M, N = a.N, K = a.K;
+    const int64_t np = int64_t(blockIdx.x >> 1) * (2 * P2_ROWS);             // the pair's first weight row
+    const int64_t n0 = np + int64_t(rank) * P2_ROWS;                         // this CTA's weight rows
+    const int64_t m0 = int64_t(blockIdx.y) * (2 * P2_NSUB * BMS);            // the pair's first token
+    const int nk = int(K / BK);
+    // sub-tiles with any token in the pair, and this CTA's own 128 tokens of sub-tile j start at m0 + 256 j + 128 r
+    const int nsub = int((M - m0 + 2 * BMS - 1) / (2 * BMS) < P2_NSUB ? (M - m0 + 2 * BMS - 1) / (2 * BMS) : P2_NSUB);
+    auto own_tok0 = [&](int j) { return m0 + int64_t(2 * BMS) * j + int64_t(BMS) * rank; };
+    int nload = 0;                                                           // this CTA's sub-tiles with tokens
+    for (int j = 0; j < nsub; ++j) nload += own_tok0(j) < M ? 1 : 0;
+
+    if (tid == 0) {
+        for (int st = 0; st < P2_STAGES; ++st) {
+            mbar_init(&full[st], 2);                     // the two CTAs' forwarding arrivals
+            mbar_init(&empty[st], 1);
+            mbar_init(&xfull[st], 1);
+            mbar_init(&wfull[st], NDQW);
+        }
+        mbar_init(accum, 1);
+        fence_mbar_init();
+    }
+    if (warp == NDQW) {
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();            // both CTAs: barriers initialised and TMEM allocated before any cross-CTA use
+    tc_fence_after();
+    const uint32_t tmem_d = *tmem_slot;
+    const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), 0);      // the even CTA's full[0], cluster address
+    bool dead = false;
+
+    if (warp < NDQW) {
+        // ------------------------------ weight producers ------------------------------
+        const int r = tid & (BNMAX - 1), h = tid / BNMAX;                   // weight row, K half of the stage
+        const int64_t n = n0 + r;
+        const uint8_t *row = a.packed + n * a.row_stride;
+        constexpr int64_t SE = F == FMT_Q4G32H ? 2 : 4;
+        const uint8_t *gs_row = a.gscale ? reinterpret_cast<const uint8_t *>(a.gscale) + n * a.scale_stride * SE : nullptr;
+        RawUnit S[PD + 1] = {};
+        if (n < N) {
+#pragma unroll
+            for (int i = 0; i < PD; ++i)
+                if (i < nk) load_raw<F>(row, gs_row, uint32_t(2 * i + h), S[i]);
+        }
+        auto step = [&](int kt, const RawUnit &use, RawUnit &into) {
+            if (kt >= nk || dead) return;
+            const int st = kt % P2_STAGES;
+            if (n < N && kt + PD < nk) load_raw<F>(row, gs_row, uint32_t(2 * (kt + PD) + h), into);
+            if (kt >= P2_STAGES && !mbar_wait_cluster_bounded(&empty[st], uint32_t((kt / P2_STAGES) - 1) & 1u)) {
+                atomicOr(&g_fault_prefill, FAULT_WAIT_EMPTY);
+                dead = true;
+                return;
+            }
+            uint8_t *Bs = sm + st * P2_STAGE + P2_NSUB * A_BYTES;
+            uint4 v[4];
+            if (n < N) {
+                uint32_t o[16];
+                unit_bf16<F>(use, uint32_t(2 * kt + h), o);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(Bs + sw128_off(uint32_t(r), uint32_t(4 * h + c))) = v[c];
+            // the generic-proxy stores, visible to the tensor cores; this CTA's forwarding warp passes the stage on
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wfull[st]);
+        };
+#pragma unroll 1
+        for (int kt = 0; kt < nk && !dead; kt += PD + 1) {
+#pragma unroll
+            for (int i = 0; i <= PD; ++i) step(kt + i, S[i], S[(i + PD) % (PD + 1)]);
+        }
+        // ---------------------------------- epilogue ----------------------------------
+        {
+            const bool seen = dead ? false : mbar_wait_cluster_bounded(accum, 0u);
+            const bool ok = __any_sync(0xffffffffu, seen);
+            if (!ok && lane == 0) atomicOr(&g_fault_prefill, FAULT_WAIT_MMA);
+            dead = !ok;
+        }
+        tc_fence_after();
+        // warp w reads TMEM lanes 32 (w % 4) .. +31 (its lane quarter: this CTA's tokens) of sub-tile w / 4
+        const int qw = warp & 3, j = warp >> 2;
+        if (!dead && j < nsub) {
+            const int64_t m = own_tok0(j) + 32 * qw + lane;
+            const uint32_t lane_base = tmem_d + (uint32_t(32 * qw) << 16) + uint32_t(256 * j);
+#pragma unroll 1
+            for (int cc = 0; cc < 256 / 32; ++cc) {
+                uint32_t rr[32];
+                tmem_ld32(lane_base + uint32_t(32 * cc), rr);
+                tmem_ld_wait();
+                const int64_t nc = np + 32 * cc;
+                if (m < M && nc < N) {
+                    uint16_t *dst = a.Y + m * a.ldy + nc;
+                    if (nc + 32 <= N && a.vec_y) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            d4[q] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * q]), __uint_as_float(rr[8 * q + 1])),
+                                               pack_bf16x2(__uint_as_float(rr[8 * q + 2]), __uint_as_float(rr[8 * q + 3])),
+                                               pack_bf16x2(__uint_as_float(rr[8 * q + 4]), __uint_as_float(rr[8 * q + 5])),
+                                               pack_bf16x2(__uint_as_float(rr[8 * q + 6]), __uint_as_float(rr[8 * q + 7])));
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q)
+                            if (nc + q < N) dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(rr[q])));
+                    }
+                }
+            }
+        }
+    } else if (warp == NDQW) {
+        // ------------------------------------ MMA issuer (even CTA) ------------------------------------
+        if (leader && lane == 0) {
+            for (int kt = 0; kt < nk; ++kt) {
+                const int st = kt % P2_STAGES;
+                if (!mbar_wait_cluster_bounded(&full[st], uint32_t(kt / P2_STAGES) & 1u)) {
+                    atomicOr(&g_fault_prefill, FAULT_WAIT_FULL);
+                    dead = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t As = base + uint32_t(st * P2_STAGE), Bs = As + uint32_t(P2_NSUB * A_BYTES);
+                for (int j = 0; j < nsub; ++j) {
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_bf16_pair(tmem_d + uint32_t(256 * j), sw128_kmajor_desc(As + uint32_t(j * A_BYTES) + 32u * k),
+                                       sw128_kmajor_desc(Bs + 32u * k), kIdescPair, (kt > 0 || k > 0) ? 1u : 0u);
+                }
+                umma_commit_pair(&empty[st], uint16_t(0x3));   // both CTAs may refill the stage once these MMAs are done
+            }
+            umma_commit_pair(accum, uint16_t(0x3));             // accumulators complete (also on the failure path)
+        }
+        __syncwarp();
+    } else if (warp == NDQW + 1) {
+        // ------------------------------------ X producer ------------------------------------
+        if (lane == 0) {
+            for (int kt = 0; kt < nk; ++kt) {
+                const int st = kt % P2_STAGES;
+                if (kt >= P2_STAGES && !mbar_wait_cluster_bounded(&empty[st], uint32_t((kt / P2_STAGES) - 1) & 1u)) {
+                    atomicOr(&g_fault_prefill, FAULT_WAIT_EMPTY);
+                    break;
+                }
+                uint8_t *As = sm + st * P2_STAGE;
+                mbar_arrive_expect_tx(&xfull[st], uint32_t(nload * A_BYTES));
+                for (int j = 0; j < nsub; ++j)
+                    if (own_tok0(j) < M) tma_load_2d(As + j * A_BYTES, &tm_x, kt * BK, int(own_tok0(j)), &xfull[st]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // --------------------- forward "X landed" to the even CTA's full barrier ---------------------
+        if (lane == 0) {
+            for (int kt = warp - (NDQW + 2); kt < nk; kt += P2_NFWD) {
+                const int st = kt % P2_STAGES;
+                if (!mbar_wait_bounded(&xfull[st], uint32_t(kt / P2_STAGES) & 1u) ||
+                    !mbar_wait_bounded(&wfull[st], uint32_t(kt / P2_STAGES) & 1u)) {
+                    atomicOr(&g_fault_prefill, FAULT_WAIT_FULL);
+                    break;
+                }
+                mbar_arrive_cluster(full0_leader + uint32_t(st) * 8u);
+            }
+        }
+        __syncwarp();
+    }
+
+    // ---- teardown: both CTAs' TMEM reads and the pair's MMAs are finished before the TMEM is freed ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == NDQW && leader && lane == 0 && dead) (void)mbar_wait_cluster_bounded(accum, 0u, 1u << 16);
+    __syncwarp();
+    cluster_sync_all();
+    if (warp == NDQW) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_d, TMEM_COLS);
+    }
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -496,12 +801,47 @@ static cudaError_t launch_prefill_bn(const PrefillArgs &a, const CUtensorMap &tm
     return cudaGetLastError();
 }
 
-// Weight-tile height: 128 rows, or 112 when that takes fewer waves of CTAs per row of weight tiles than 128 does
-// in proportion to the tile (one CTA per SM; time per CTA about proportional to its rows).
+// Weight-tile height of the single-CTA kernel: 128 rows, or 112 when that takes fewer waves of CTAs per row of
+// weight tiles than 128 does in proportion to the tile (one CTA per SM; time per CTA about proportional to its rows).
 static int prefill_bn(const PrefillArgs &a) {
     const int64_t sms = num_sms(), mt = (a.M + BM - 1) / BM;
     auto cost = [&](int64_t bn) { return ((a.N + bn - 1) / bn * mt + sms - 1) / sms * bn; };
     return cost(112) < cost(128) ? 112 : 128;
+}
+
+// The pair kernel halves the operand reads each SM's shared memory serves to the tensor cores, which pays off where
+// dequantization is cheap: on the prefill workload's matrices (M = 2048, 14336x4096 and 4096x14336) it is 4-17%
+// faster than the single-CTA kernel for the INT4 formats and the 2-bit format, and 5-16% slower for the 3-, 5- and
+// 6-bit formats, whose dequantization bounds both kernels (there two SMs in lock step wait for the slower one).
+template <int F> constexpr bool kPairPrefill = kInt4<F> || F == FMT_Q2S;
+
+// The CTA-pair kernel: clusters of two CTAs, each pair a 512-token x 256-weight-row block of Y.
+template <int F>
+static cudaError_t launch_prefill_pair(const PrefillArgs &a, const CUtensorMap &tmx, cudaStream_t s) {
+    static int opted[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!opted[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, P2_SMEM);
+        if (e != cudaSuccess) return e;
+        opted[dev] = 1;
+    }
+    const int64_t gx = 2 * ((a.N + 2 * P2_ROWS - 1) / (2 * P2_ROWS)), gy = (a.M + 2 * P2_NSUB * BMS - 1) / (2 * P2_NSUB * BMS);
+    if (gx > 0x7FFFFFFF || gy > 65535) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(gx), unsigned(gy));
+    cfg.blockDim = dim3(unsigned(P2_THREADS));
+    cfg.dynamicSmemBytes = P2_SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<F>, tmx, a);
 }
 
 template <int F>
@@ -510,6 +850,7 @@ static cudaError_t launch_prefill_f(const PrefillArgs &a, cudaStream_t s) {
     const cudaError_t e = encode_x(&tmx, a);
     if (e != cudaSuccess) return e;
     const int forced = prefill_tile_rows();
+    if (forced == 256 || (forced == 0 && kPairPrefill<F>)) return launch_prefill_pair<F>(a, tmx, s);
     const int bn = forced ? forced : prefill_bn(a);
     return bn == 112 ? launch_prefill_bn<F, 112>(a, tmx, s) : launch_prefill_bn<F, 128>(a, tmx, s);
 }

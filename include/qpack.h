@@ -163,7 +163,8 @@ int qgemm_small(int fmt, const uint8_t *packed, const void *group_scales, int64_
 /* Prefill dequant GEMM on the tensor cores (P1 §1.2: prefill is a dense [tokens, hidden] x [hidden, hidden]
  * contraction):
  *   Y[m, n] = sum_k bf16(X[m,k]) * bf16(w'[n,k]),  fp32 accumulation, Y rounded to bf16
- * Weight tiles are dequantized to bf16 in shared memory and fed to tcgen05 MMA with TMEM accumulators.
+ * Weight tiles are dequantized to bf16 in shared memory and fed to tcgen05 MMA with TMEM accumulators; by
+ * default two CTAs on two SMs share each MMA (see QPACK_OPT_PREFILL_TILE_ROWS).
  *  formats  the INT4 formats (K a multiple of 64) and the super-block formats (K a multiple of 256)
  *  X        [M, ldx] bf16, 16-byte aligned, ldx >= K, ldx a multiple of 8
  *  Y        [M, ldy] bf16, 2-byte aligned, ldy >= N (16-byte aligned rows with ldy % 8 == 0 store fastest)
@@ -204,9 +205,12 @@ int qpack_fetch_fault_flags(int32_t *flags);
  *  (activations are still read only after it has finished, and outputs written after). The caller guarantees
  *  that the packed weights and scales of a product are not written by the kernel launched just before it on
  *  that stream (true for a decode loop over resident weights).
- *  QPACK_OPT_PREFILL_TILE_ROWS (default 0): weight rows per qgemm_prefill CTA tile. 0 chooses per launch (128,
- *  or 112 when that needs fewer SM-waves in proportion to the tile); 112 or 128 forces one. Both meet the
- *  prefill bound below.
+ *  QPACK_OPT_PREFILL_TILE_ROWS (default 0): the qgemm_prefill tiling. 256: pairs of CTAs on two SMs (a cluster
+ *  of two), each pair a 512-token x 256-weight-row block of Y computed by tcgen05 MMAs of M = 256 tokens and
+ *  N = 256 weight rows spread over the pair. 112 or 128: one CTA per 512-token x 112- or 128-row block (MMAs of
+ *  M = 128, N = 112 or 128). 0 chooses per launch: pairs for the INT4 formats and the 2-bit format, single CTAs
+ *  (128 rows, or 112 when that needs fewer SM-waves in proportion to the tile) for the others. All of them meet
+ *  the prefill bound.
  * Returns QPACK_OK, QPACK_ERR_ARG (unknown option or value) or QPACK_ERR_CUDA (no current device). Host-only. */
 #define QPACK_OPT_WEIGHT_PREFETCH 1
 #define QPACK_OPT_PREFILL_TILE_ROWS 2
