@@ -7,7 +7,7 @@
 //
 // Two kernels. The pair kernel (prefill_pair_kernel, further below) spreads each tensor-core instruction over a
 // cluster of two CTAs on two SMs (512 tokens x 256 weight rows per pair) and is the default for the INT4 formats
-// and the 2-bit format. The single-CTA kernel (prefill_kernel) is the default for the 3-, 5- and 6-bit formats.
+// and the 2- and 5-bit formats. The single-CTA kernel (prefill_kernel) is the default for the 3- and 6-bit formats.
 //
 // Single-CTA kernel: one CTA computes a 512 x 128 block of Y (four 128-token sub-tiles x 128 weight rows):
 //   warp 9      TMA producer: per 64-wide K step, four 2-D tensor copies bring the 4 x (128 x 64) bf16 X tiles into
@@ -197,60 +197,113 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
 }
+// Codes are unpacked four at a time into the bytes of 32-bit words, each byte one code shifted left inside it by a
+// known bit class p (the byte holds q * 2^p). A byte becomes a float with no conversion instruction: placed in the
+// low mantissa bits of 2^23 it reads 2^23 + q * 2^p, and subtracting 2^23 + off * 2^p leaves (q - off) * 2^p
+// exactly. The scale is taken times 2^-p (exact), so every product is the same real number as scale * (q - off),
+// rounded once: the weights are bit for bit those of the formats' dequantization rule.
+__device__ __forceinline__ float byte_f(uint32_t v, int b) {                  // 2^23 + byte b of v
+    return __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7540u | uint32_t(b)));
+}
+constexpr float TWO23 = 8388608.0f;
+
 template <int F>
 __device__ __forceinline__ void unit_bf16(const RawUnit &r, uint32_t u, uint32_t out[16]) {
     float w[32];
     if constexpr (kInt4<F>) {
+        // weight 8j + 2b: low nibble of byte b of code word j (class 0); weight 8j + 2b + 1: its high nibble (class 4)
         const float sc0 = __uint_as_float(r.e[0]), sc1 = F == FMT_Q4G16 ? __uint_as_float(r.e[1]) : sc0;
-        const int z = F == FMT_Q4G32A ? int(__uint_as_float(r.e[1])) : 8;     // the code offset, or the zero point
+        const float z = F == FMT_Q4G32A ? __uint_as_float(r.e[1]) : 8.0f;   // the code offset, or the zero point
+        const float off0 = __fadd_rn(TWO23, z), off4 = __fadd_rn(TWO23, 16.0f * z);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            w[i] = __fmul_rn(i < 16 ? sc0 : sc1, float(int((r.c[i >> 3] >> (4 * (i & 7))) & 15u) - z));
+        for (int j = 0; j < 4; ++j) {
+            const float sc = j < 2 ? sc0 : sc1, sc4 = sc * 0.0625f;
+            const uint32_t lo = r.c[j] & 0x0F0F0F0Fu, hi = r.c[j] & 0xF0F0F0F0u;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                w[8 * j + 2 * b] = __fmul_rn(sc, __fsub_rn(byte_f(lo, b), off0));
+                w[8 * j + 2 * b + 1] = __fmul_rn(sc4, __fsub_rn(byte_f(hi, b), off4));
+            }
+        }
     } else if constexpr (F == FMT_Q2S) {
+        // weight 4b + k of a sub-block: bits 2k of byte b of its code word (class 2k)
         const float D = h2f_bits(uint16_t(r.e[1] & 0xFFFFu)), Dm = h2f_bits(uint16_t(r.e[1] >> 16));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const uint32_t l = (r.e[0] >> (8 * h)) & 0xFFu;
             const float es = __fmul_rn(D, float(l & 15u)), em = __fmul_rn(Dm, float(l >> 4));
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[16 * h + i] = __fsub_rn(__fmul_rn(es, float((r.c[h] >> (2 * i)) & 3u)), em);
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t v = r.c[h] & (0x03030303u << (2 * k));
+                const float sk = es * (k == 0 ? 1.0f : k == 1 ? 0.25f : k == 2 ? 0.0625f : 0.015625f);
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    w[16 * h + 4 * b + k] = __fsub_rn(__fmul_rn(sk, __fsub_rn(byte_f(v, b), TWO23)), em);
+            }
         }
     } else if constexpr (F == FMT_Q3S) {
+        // per sub-block (two 3-byte groups b0 b1 b2 | b3 b4 b5, code t of a group at bits 3t, weights t and 8 + t):
+        // byte permutes P = (b0 b3 b2 b5), Q = (b1 b4 b1 b4), R = (b0 b1 b3 b4), S = (b1 b2 b4 b5), then
+        //   P & 0x1C1C0707: weights 0, 8 (class 0), 6, 14 (class 2);  P & 0xE0E03838: 1, 9 (3), 7, 15 (5)
+        //   Q & 0x70700E0E: 3, 11 (1), 4, 12 (4);  the codes straddling bytes (2, 5, 10, 13) from R and S, class 0
         const uint32_t su = u & 7u;
-        const uint32_t v[4] = {r.c[0], __funnelshift_r(r.c[0], r.c[1], 24), __funnelshift_r(r.c[1], r.c[2], 16), r.c[2] >> 8};
         const uint32_t fsh = 4u * (su & 1u);
         const float D = h2f_bits(uint16_t(r.e[1]));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const float es = __fmul_rn(D, float((r.e[0] >> (fsh + 6 * h)) & 63u));
+            const uint32_t wa = r.c[h], wb = r.c[h + 1], o = h == 0 ? 0u : 0x2222u;   // bytes 6h .. 6h + 5
+            const uint32_t P = __byte_perm(wa, wb, 0x5230u + o), Q = __byte_perm(wa, wb, 0x4141u + o);
+            const uint32_t R = __byte_perm(wa, wb, 0x4310u + o), S = __byte_perm(wa, wb, 0x5421u + o);
+            const uint32_t v[4] = {P & 0x1C1C0707u, P & 0xE0E03838u, Q & 0x70700E0Eu,
+                                   ((R >> 6) & 0x00070007u) | ((S << 1) & 0x07000700u)};
+            constexpr int wi[4][4] = {{0, 8, 6, 14}, {1, 9, 7, 15}, {3, 11, 4, 12}, {2, 5, 10, 13}};
+            constexpr int cl[4][4] = {{0, 0, 2, 2}, {3, 3, 5, 5}, {1, 1, 4, 4}, {0, 0, 0, 0}};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int g = 2 * h + (i >> 3), t = i & 7;
-                w[16 * h + i] = __fmul_rn(es, float(int((v[g] >> (3 * t)) & 7u) - 4));
-            }
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const float p2 = float(1 << cl[k][b]);                      // 2^p, exact
+                    w[16 * h + wi[k][b]] =
+                        __fmul_rn(es * (1.0f / p2), __fsub_rn(byte_f(v[k], b), TWO23 + 4.0f * p2));
+                }
         }
     } else if constexpr (F == FMT_Q5S) {
+        // weight 8j + 2b (+1): the low (high) nibble of byte b of code word j, with its fifth bit spread from bit 2b
+        // (2b + 1) of byte j of the high-bit plane by one multiply (bit 2m lands on bit 8m + 4, cross terms elsewhere)
         const uint32_t su = u & 7u;
         const uint64_t lo64 = (uint64_t(r.e[1]) << 32) | r.e[0], hi64 = (uint64_t(r.e[2]) << 32) | r.e[1];
         const float D = h2f_bits(uint16_t(r.e[3] & 0xFFFFu)), Dm = h2f_bits(uint16_t(r.e[3] >> 16));
         const float es = __fmul_rn(D, float(uint32_t(lo64 >> (6 * su)) & 63u));
         const float em = __fmul_rn(Dm, float(uint32_t(hi64 >> (16 + 6 * su)) & 63u));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t q = ((r.c[i >> 3] >> (4 * (i & 7))) & 15u) | (((r.c[4] >> i) & 1u) << 4);
-            w[i] = __fsub_rn(__fmul_rn(es, float(q)), em);
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t hj = r.c[4] >> (8 * j);
+            const uint32_t ve = (r.c[j] & 0x0F0F0F0Fu) | (((hj & 0x55u) * 0x00410410u) & 0x10101010u);
+            const uint32_t vo = ((r.c[j] >> 4) & 0x0F0F0F0Fu) | (((hj & 0xAAu) * 0x00208208u) & 0x10101010u);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                w[8 * j + 2 * b] = __fsub_rn(__fmul_rn(es, __fsub_rn(byte_f(ve, b), TWO23)), em);
+                w[8 * j + 2 * b + 1] = __fsub_rn(__fmul_rn(es, __fsub_rn(byte_f(vo, b), TWO23)), em);
+            }
         }
     } else {
+        // per sub-block: low-4 plane words A (weights 0-7), B (8-15), high-2 plane H (weight 4b + k at bits 2k of
+        // byte b). Word k holds weight 4b + k in byte b: k even at class 0 (nibble | high bits << 4), k odd at class 2.
         const float D = h2f_bits(uint16_t(r.e[3]));
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const float es = __fmul_rn(D, float(int(int8_t(uint8_t(r.e[2] >> (8 * hh))))));
+            const float es = __fmul_rn(D, float(int(int8_t(uint8_t(r.e[2] >> (8 * hh)))))), es2 = es * 0.25f;
+            const uint32_t A = r.c[2 * hh], B = r.c[2 * hh + 1], H = r.e[hh];
+            const uint32_t P0 = __byte_perm(A, B, 0x6420u), P1 = __byte_perm(A, B, 0x7531u), Hs = H << 4;
+            const uint32_t v[4] = {(P0 & 0x0F0F0F0Fu) | (Hs & 0x30303030u), ((P0 >> 2) & 0x3C3C3C3Cu) | (Hs & 0xC0C0C0C0u),
+                                   (P1 & 0x0F0F0F0Fu) | (H & 0x30303030u), ((P1 >> 2) & 0x3C3C3C3Cu) | (H & 0xC0C0C0C0u)};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int ii = 16 * hh + i;
-                const uint32_t q = ((r.c[ii >> 3] >> (4 * (ii & 7))) & 15u) | (((r.e[hh] >> (2 * i)) & 3u) << 4);
-                w[ii] = __fmul_rn(es, float(int(q) - 32));
-            }
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    w[16 * hh + 4 * b + k] = (k & 1) ? __fmul_rn(es2, __fsub_rn(byte_f(v[k], b), TWO23 + 128.0f))
+                                                     : __fmul_rn(es, __fsub_rn(byte_f(v[k], b), TWO23 + 32.0f));
         }
     }
 #pragma unroll
@@ -810,10 +863,10 @@ static int prefill_bn(const PrefillArgs &a) {
 }
 
 // The pair kernel halves the operand reads each SM's shared memory serves to the tensor cores, which pays off where
-// dequantization is cheap: on the prefill workload's matrices (M = 2048, 14336x4096 and 4096x14336) it is 4-17%
-// faster than the single-CTA kernel for the INT4 formats and the 2-bit format, and 5-16% slower for the 3-, 5- and
+// the dequantization keeps up: on the prefill workload's matrices (M = 2048, 14336x4096 and 4096x14336) it is
+// faster than the single-CTA kernel for the INT4 formats, the 2-bit and the 5-bit format, and slower for the 3- and
 // 6-bit formats, whose dequantization bounds both kernels (there two SMs in lock step wait for the slower one).
-template <int F> constexpr bool kPairPrefill = kInt4<F> || F == FMT_Q2S;
+template <int F> constexpr bool kPairPrefill = kInt4<F> || F == FMT_Q2S || F == FMT_Q5S;
 
 // The CTA-pair kernel: clusters of two CTAs, each pair a 512-token x 256-weight-row block of Y.
 template <int F>
