@@ -245,7 +245,7 @@ __device__ __forceinline__ void unpack_dp(const uint8_t *u, const uint8_t *sp, c
         unpack_tri_dp(qp[0], qp[1], g.q, r.v + 4);
     } else if constexpr (F == FMT_Q5S) {
         const uint4 w = *reinterpret_cast<const uint4 *>(u);
-        const uint32_t H = lds32(u + g.o1);                               // bit i = bit 4 of code i
+        const uint32_t H = lds32(u + g.o1);                               // the unit's high-bit word
         const uint4 fld = *reinterpret_cast<const uint4 *>(u + g.o2);
         const uint32_t ddw = on ? fld.w : 0u;
         const float2 Dd = __half22float2(*reinterpret_cast<const __half2 *>(&ddw));
@@ -254,15 +254,16 @@ __device__ __forceinline__ void unpack_dp(const uint8_t *u, const uint8_t *sp, c
         const float Mv = small_int_f(lop3_and_or(uint32_t(hi64 >> (g.sh1 - 32u)), 63u, MAGICF));
         r.f0 = Dd.x * L;
         r.g0 = Dd.y * Mv;
-        // word 2j (2j + 1): the even (odd) weights' nibbles of code word j, each byte's fifth bit spread from bits
-        // 0, 2, 4, 6 (1, 3, 5, 7) of the high-plane byte j by one multiply: bit 2m (+1) lands on bit 8m + 4, and the
-        // cross terms on bits outside 0x10101010
+        // word 2j (2j + 1): the even (odd) weights' nibbles of code word j with their fifth bits. hj = bit lane j of the
+        // high-bit word: bit 8b + 4 = weight 8j + 2b, bit 8((b + 1) & 3) = weight 8j + 2b + 1. The even codes take
+        // hj's bits 4 beside the low nibbles (one select); the odd codes take hj's bits 0 beside the high nibbles, and
+        // one funnel shift by 4 (hj supplying the top bits) moves them down into whole bytes.
         const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t hj = H >> (8 * j);
-            r.v[2 * j] = (wv[j] & 0x0F0F0F0Fu) | (((hj & 0x55u) * 0x00410410u) & 0x10101010u);
-            r.v[2 * j + 1] = ((wv[j] >> 4) & 0x0F0F0F0Fu) | (((hj & 0xAAu) * 0x00208208u) & 0x10101010u);
+            const uint32_t hj = (H >> j) & 0x11111111u;
+            r.v[2 * j] = lop3_sel(wv[j], hj, 0x0F0F0F0Fu);
+            r.v[2 * j + 1] = __funnelshift_r(lop3_sel(wv[j], hj, 0xF0F0F0F0u), hj, 4);
         }
     } else {
         const uint32_t sh = g.sh0;

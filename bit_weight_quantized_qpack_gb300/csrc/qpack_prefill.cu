@@ -269,8 +269,9 @@ __device__ __forceinline__ void unit_bf16(const RawUnit &r, uint32_t u, uint32_t
                 }
         }
     } else if constexpr (F == FMT_Q5S) {
-        // weight 8j + 2b (+1): the low (high) nibble of byte b of code word j, with its fifth bit spread from bit 2b
-        // (2b + 1) of byte j of the high-bit plane by one multiply (bit 2m lands on bit 8m + 4, cross terms elsewhere)
+        // weight 8j + 2b (+1): the low (high) nibble of byte b of code word j with its fifth bit from bit lane j of the
+        // unit's high-bit word (bit 8b + 4, or bit 8((b + 1) & 3) for the odd weight): one select for the even codes,
+        // a select and a funnel shift by 4 for the odd ones
         const uint32_t su = u & 7u;
         const uint64_t lo64 = (uint64_t(r.e[1]) << 32) | r.e[0], hi64 = (uint64_t(r.e[2]) << 32) | r.e[1];
         const float D = h2f_bits(uint16_t(r.e[3] & 0xFFFFu)), Dm = h2f_bits(uint16_t(r.e[3] >> 16));
@@ -278,9 +279,9 @@ __device__ __forceinline__ void unit_bf16(const RawUnit &r, uint32_t u, uint32_t
         const float em = __fmul_rn(Dm, float(uint32_t(hi64 >> (16 + 6 * su)) & 63u));
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t hj = r.c[4] >> (8 * j);
-            const uint32_t ve = (r.c[j] & 0x0F0F0F0Fu) | (((hj & 0x55u) * 0x00410410u) & 0x10101010u);
-            const uint32_t vo = ((r.c[j] >> 4) & 0x0F0F0F0Fu) | (((hj & 0xAAu) * 0x00208208u) & 0x10101010u);
+            const uint32_t hj = (r.c[4] >> j) & 0x11111111u;
+            const uint32_t ve = lop3_sel(r.c[j], hj, 0x0F0F0F0Fu);
+            const uint32_t vo = __funnelshift_r(lop3_sel(r.c[j], hj, 0xF0F0F0F0u), hj, 4);
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 w[8 * j + 2 * b] = __fsub_rn(__fmul_rn(es, __fsub_rn(byte_f(ve, b), TWO23)), em);

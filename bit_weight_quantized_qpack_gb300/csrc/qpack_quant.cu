@@ -209,14 +209,20 @@ __device__ __forceinline__ void pack_lane(const LaneBlock &B, int lane, bool val
         }
         if (lane == 0) st_u16(blk + 108, B.d16);
     } else if constexpr (F == FMT_Q5S) {
+        // high-bit word of the lane's 32-weight unit (lanes 4c .. 4c + 3; this lane = code word j = lane & 3):
+        // weight 8j + 2b at bit 8b + 4 + j, weight 8j + 2b + 1 at bit 8((b + 1) & 3) + j
+        const uint32_t j = uint32_t(lane) & 3u;
         uint32_t lo = 0, hi = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
+            const uint32_t b = uint32_t(i) >> 1, pos = (i & 1) ? 8u * ((b + 1u) & 3u) + j : 8u * b + 4u + j;
             lo |= uint32_t(B.u[i] & 15u) << (4 * i);
-            hi |= uint32_t((B.u[i] >> 4) & 1u) << i;
+            hi |= uint32_t((B.u[i] >> 4) & 1u) << pos;
         }
+        hi |= __shfl_xor_sync(0xffffffffu, hi, 1);
+        hi |= __shfl_xor_sync(0xffffffffu, hi, 2);
         st_u32(blk + 4 * lane, lo);
-        blk[128 + lane] = uint8_t(hi);
+        if (j == 0) st_u32(blk + 128 + lane, hi);
         // fields 0..7 = L_0..L_7 (sub-block j in lanes 4j..4j+3), fields 8..15 = M_0..M_7; lane r < 4 packs
         // fields 4r..4r+3.
         const int r = lane & 3;
@@ -280,9 +286,13 @@ __device__ __forceinline__ void unpack_lane(const uint8_t *blk, int lane, bool v
         B.L = int((f >> (6 * (j & 3))) & 63u); B.M = 0;
         B.d16 = uint16_t(ld_u16(blk + 108)); B.dm16 = 0;
     } else if constexpr (F == FMT_Q5S) {
-        uint32_t lo = ld_u32(blk + 4 * lane), hi = blk[128 + lane];
+        const uint32_t cw = uint32_t(lane) & 3u;   // the lane's code word within its unit
+        uint32_t lo = ld_u32(blk + 4 * lane), hi = ld_u32(blk + 128 + 4 * (lane >> 2));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) B.u[i] = uint8_t(((lo >> (4 * i)) & 15u) | (((hi >> i) & 1u) << 4));
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t b = uint32_t(i) >> 1, pos = (i & 1) ? 8u * ((b + 1u) & 3u) + cw : 8u * b + 4u + cw;
+            B.u[i] = uint8_t(((lo >> (4 * i)) & 15u) | (((hi >> pos) & 1u) << 4));
+        }
         const int j = lane >> 2;
         uint32_t fl = ld_u24(blk + 160 + 3 * (j >> 2)), fm = ld_u24(blk + 166 + 3 * (j >> 2));
         B.L = int((fl >> (6 * (j & 3))) & 63u);

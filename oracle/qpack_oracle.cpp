@@ -315,12 +315,21 @@ int quantize_sb_row(const SbFormat &F, const float *w, int64_t K, int8_t *q, uin
 // bit, as each function states) and of one INT4 row (P2 §3.2).
 // ----------------------------------------------------------------------------------------------------------
 
-// Layouts (FORMATS.md §2c): Q2S codes = run of 2-bit fields at byte 0, sub-block nibbles L_j, M_j = fields 2j, 2j + 1
-// of a 4-bit run at byte 64, d at 80, dmin at 82. Q3S codes (offset q + 4) = 3-bit run at 0 (so a 3-byte group holds
-// 8 codes, P1 §2.2), L_j = 6-bit run at 96 (four fields per 3 bytes), d at 108. Q5S low nibbles = 4-bit run at 0,
-// fifth bits = 1-bit run at 128, fields L_0..7, M_0..7 = 6-bit run at 160, d at 172, dmin at 174. Q6S (offset
-// q + 32) low nibbles = 4-bit run at 0, top two bits = 2-bit run at 128, int8 L_j at 192, d at 208. fp16 values are
-// stored little-endian.
+// Layouts: Q2S codes = run of 2-bit fields at byte 0, sub-block nibbles L_j, M_j = fields 2j, 2j + 1 of a 4-bit run
+// at byte 64, d at 80, dmin at 82. Q3S codes (offset q + 4) = 3-bit run at 0 (so a 3-byte group holds 8 codes,
+// P1 §2.2), L_j = 6-bit run at 96 (four fields per 3 bytes), d at 108. Q5S low nibbles = 4-bit run at 0, fifth bits
+// = 1-bit run at 128 in the order q5s_hbit gives, fields L_0..7, M_0..7 = 6-bit run at 160, d at 172, dmin at 174.
+// Q6S (offset q + 32) low nibbles = 4-bit run at 0, top two bits = 2-bit run at 128, int8 L_j at 192, d at 208.
+// fp16 values are stored little-endian.
+
+// Position, in the Q5S high-bit run (P1 §2.3 gives it 32 B and no bit order), of the fifth bit of weight i. The run
+// is read as one 32-bit little-endian word per 32 weights; weight 32c + 8j + 2b + e (j, b in 0..3, e in 0..1) takes
+// bit 8b + 4 + j of word c when e = 0 and bit 8((b + 1) mod 4) + j when e = 1. Every bit of the word is used once.
+int64_t q5s_hbit(int64_t i) {
+    const int64_t c = i >> 5;
+    const int t = int(i & 31), j = t >> 3, b = (t >> 1) & 3, e = t & 1;
+    return 32 * c + (e == 0 ? 8 * b + 4 + j : 8 * ((b + 1) & 3) + j);
+}
 void pack_sb(int fmt, const int8_t *q, const uint8_t *L, const uint8_t *M, uint16_t d, uint16_t dmin, uint8_t *p) {
     SbFormat F;
     sb_format(fmt, &F);
@@ -340,7 +349,7 @@ void pack_sb(int fmt, const int8_t *q, const uint8_t *L, const uint8_t *M, uint1
             for (int i = 0; i < 256; ++i) {
                 const uint32_t u = uint8_t(q[i]);
                 run_put(p, 4, i, u % 16);
-                run_put(p + 128, 1, i, u / 16);
+                run_put(p + 128, 1, q5s_hbit(i), u / 16);
             }
             for (int j = 0; j < 8; ++j) { run_put(p + 160, 6, j, L[j]); run_put(p + 160, 6, 8 + j, M[j]); }
             wr16(p + 172, d); wr16(p + 174, dmin);
@@ -370,7 +379,7 @@ void unpack_sb(int fmt, const uint8_t *p, int8_t *q, uint8_t *L, uint8_t *M, uin
             *d = rd16(p + 108);
             break;
         case Q5S:
-            for (int i = 0; i < 256; ++i) q[i] = int8_t(run_get(p, 4, i) + 16 * run_get(p + 128, 1, i));
+            for (int i = 0; i < 256; ++i) q[i] = int8_t(run_get(p, 4, i) + 16 * run_get(p + 128, 1, q5s_hbit(i)));
             for (int j = 0; j < 8; ++j) { L[j] = uint8_t(run_get(p + 160, 6, j)); M[j] = uint8_t(run_get(p + 160, 6, 8 + j)); }
             *d = rd16(p + 172); *dmin = rd16(p + 174);
             break;

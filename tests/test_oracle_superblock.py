@@ -141,14 +141,19 @@ def test_q2s_q5s_q6s_layout_closed_form(orc):
     assert all(p[b] == sum(int(u[4 * b + k]) * 4 ** k for k in range(4)) for b in range(64))
     assert all(p[64 + j] == Ls[j] + 16 * Ms[j] for j in range(16))
     assert p[80] + 256 * p[81] == 0x1234 and p[82] + 256 * p[83] == 0x5678
-    # Q5S: low plane byte = lo(u_2b) + 16 lo(u_2b+1); high plane byte = sum_t hi(u_8c+t) 2^t; 16 six-bit fields
+    # Q5S: low plane byte = lo(u_2b) + 16 lo(u_2b+1); high plane byte m of the 4-byte word of weights 32c .. 32c + 31:
+    # bit 4 + j = hi(u_{32c+8j+2m}), bit j = hi(u_{32c+8j+2((m+3) mod 4)+1}); 16 six-bit fields
     u = rng.integers(0, 32, 256)
     Ls, Ms = rng.integers(0, 64, 8), rng.integers(0, 64, 8)
     parts = dict(q=u.astype(np.int8)[None], sub_scale=Ls.astype(np.uint8)[None], sub_min=Ms.astype(np.uint8)[None],
                  d=np.array([[0x0101]], np.uint16), dmin=np.array([[0x0202]], np.uint16))
     p = orc.pack(orc.Q5S, 1, 256, parts)[0][0].astype(np.int64)
     assert all(p[b] == u[2 * b] % 16 + 16 * (u[2 * b + 1] % 16) for b in range(128))
-    assert all(p[128 + c] == sum(int(u[8 * c + t] // 16) * 2 ** t for t in range(8)) for c in range(32))
+    for c in range(8):
+        for m in range(4):
+            even = sum(int(u[32 * c + 8 * j + 2 * m] // 16) * 2 ** (4 + j) for j in range(4))
+            odd = sum(int(u[32 * c + 8 * j + 2 * ((m + 3) % 4) + 1] // 16) * 2 ** j for j in range(4))
+            assert p[128 + 4 * c + m] == even + odd, (c, m)
     fields = list(Ls) + list(Ms)
     for r in range(4):
         v = p[160 + 3 * r] + 256 * p[161 + 3 * r] + 65536 * p[162 + 3 * r]
