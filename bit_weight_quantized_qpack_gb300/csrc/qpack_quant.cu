@@ -4,7 +4,9 @@
 // 8l .. 8l+7 of the block. Loads are 16-byte vectors, the per-group / per-sub-block reductions are warp
 // shuffles, and every floating-point step uses an explicitly rounded intrinsic (no FMA contraction) so that
 // codes, scales and dequantized values are bit-identical to the formats' IEEE fp32 definition (round to nearest
-// even, true division, no FMA).
+// even, true division, no FMA). The per-weight quotients are taken from one correctly rounded reciprocal per group
+// (rint_quot), which provably rounds to the same integer as the true quotient except within a stated distance of
+// a half-integer, where the true quotient is computed instead.
 //
 // Quantizers: INT4 group-32 per the DBHOO-CIM article (pwwt.cn/news/4452170) §3.1; two-level round-to-nearest
 // super-blocks per the 2/3/5/6-bit article (lpnh.cn/news/2857666) §2.1 and §2.3 (sub-block scales from each
@@ -19,6 +21,17 @@
 namespace qpack {
 
 enum : int { MODE_QUANT_PARTS = 0, MODE_QUANT_PACKED = 1, MODE_PACK = 2, MODE_UNPACK = 3, MODE_DEQUANT = 4 };
+
+
+// rint(fl(w / s)) from rs = the correctly rounded 1/s: t = rs * w (one rounded product) is within 2^-22 |t| of the
+// correctly rounded quotient, so where t lies farther than 2^-21 |t| from a half-integer both round to the same
+// integer; nearer (and for NaN) the quotient itself decides.
+__device__ __forceinline__ float rint_quot(float w, float s, float rs) {
+    const float t = __fmul_rn(w, rs);
+    const float q = rintf(t);
+    if (!(fabsf(__fsub_rn(t, q)) <= __fmaf_rn(fabsf(t), -0x1p-21f, 0.5f))) return rintf(__fdiv_rn(w, s));
+    return q;
+}
 
 // Per-lane state of one 256-weight block.
 struct LaneBlock {
@@ -60,9 +73,10 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
         a = sub_reduce_max<F>(a);                         // group of 32 = 4 lanes (16 = 2 lanes)
         float s = __fdiv_rn(a, 8.0f);
         if (s < 1e-12f) s = 1e-12f;
+        const float rs = __frcp_rn(s);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float t = clampf_ord(rintf(__fdiv_rn(w[i], s)), -8.0f, 7.0f);
+            float t = clampf_ord(rint_quot(w[i], s, rs), -8.0f, 7.0f);
             B.u[i] = uint8_t(int(t) + 8);
         }
         B.gscale = s;
@@ -80,9 +94,10 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
         float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
         if (s < 1e-12f) s = 1e-12f;
         const int z = int(clampf_ord(rintf(__fdiv_rn(-lo, s)), 0.0f, 15.0f));
+        const float rs = __frcp_rn(s);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float t = clampf_ord(__fadd_rn(rintf(__fdiv_rn(w[i], s)), float(z)), 0.0f, 15.0f);
+            const float t = clampf_ord(__fadd_rn(rint_quot(w[i], s, rs), float(z)), 0.0f, 15.0f);
             B.u[i] = uint8_t(int(t));
         }
         B.gscale = s;
@@ -99,10 +114,11 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
         a = sub_reduce_max<F>(a);
         const uint16_t s16 = f2h_bits(__fdiv_rn(a, 8.0f));
         const float D = h2f_bits(s16);
+        const float rs = __frcp_rn(D);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float t = 0.0f;
-            if (D > 0.0f) t = clampf_ord(rintf(__fdiv_rn(w[i], D)), -8.0f, 7.0f);
+            if (D > 0.0f) t = clampf_ord(rint_quot(w[i], D, rs), -8.0f, 7.0f);
             B.u[i] = uint8_t(int(t) + 8);
         }
         B.gscale = D;
@@ -124,10 +140,11 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
         float L = 0.0f;
         if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
         const float e = __fmul_rn(D, L);
+        const float re = __frcp_rn(e);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float t = 0.0f;
-            if (e > 0.0f) t = clampf_ord(rintf(__fdiv_rn(w[i], e)), -half_range, half_range - 1.0f);
+            if (e > 0.0f) t = clampf_ord(rint_quot(w[i], e, re), -half_range, half_range - 1.0f);
             B.u[i] = uint8_t(int(t) + T::offset);
         }
         B.L = int(L);
@@ -154,10 +171,11 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
         if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
         if (Dm > 0.0f) M = clampf_ord(rintf(__fdiv_rn(m, Dm)), 0.0f, float(T::lmax));
         const float es = __fmul_rn(D, L), em = __fmul_rn(Dm, M);
+        const float re = __frcp_rn(es);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float t = 0.0f;
-            if (es > 0.0f) t = clampf_ord(rintf(__fdiv_rn(__fadd_rn(w[i], em), es)), 0.0f, levels);
+            if (es > 0.0f) t = clampf_ord(rint_quot(__fadd_rn(w[i], em), es, re), 0.0f, levels);
             B.u[i] = uint8_t(int(t));
         }
         B.L = int(L);
@@ -339,8 +357,11 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const int64_t total = a.N * a.nbk;
     int flags = 0;
-    for (int64_t wb = warp0; wb < total; wb += nwarps) {
-        const int64_t r = wb / a.nbk, b = wb - r * a.nbk;
+    // (row, block) of this warp's first block and of the grid stride: one division each, then additions
+    int64_t r = warp0 / a.nbk, b = warp0 - r * a.nbk;
+    const int64_t sr = nwarps / a.nbk, sb = nwarps - sr * a.nbk;
+    for (int64_t wb = warp0; wb < total; wb += nwarps, r += sr, b += sb) {
+        if (b >= a.nbk) { b -= a.nbk; ++r; }
         const int64_t k0 = 256 * b + 8 * lane;           // first weight of this lane within the row
         const bool valid = k0 < a.K;                      // only INT4 rows can end inside a block
         LaneBlock B;
