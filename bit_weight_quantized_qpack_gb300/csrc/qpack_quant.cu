@@ -23,14 +23,23 @@ namespace qpack {
 enum : int { MODE_QUANT_PARTS = 0, MODE_QUANT_PACKED = 1, MODE_PACK = 2, MODE_UNPACK = 3, MODE_DEQUANT = 4 };
 
 
-// rint(fl(w / s)) from rs = the correctly rounded 1/s: t = rs * w (one rounded product) is within 2^-22 |t| of the
+// rint(fl(v / s)) from rs = the correctly rounded 1/s: t = rs * w (one rounded product) is within 2^-22 |t| of the
 // correctly rounded quotient, so where t lies farther than 2^-21 |t| from a half-integer both round to the same
 // integer; nearer (and for NaN) the quotient itself decides.
-__device__ __forceinline__ float rint_quot(float w, float s, float rs) {
-    const float t = __fmul_rn(w, rs);
-    const float q = rintf(t);
-    if (!(fabsf(__fsub_rn(t, q)) <= __fmaf_rn(fabsf(t), -0x1p-21f, 0.5f))) return rintf(__fdiv_rn(w, s));
-    return q;
+// The lane's eight quotients at once: one branch for the rare lane with any value near a half-integer, which then
+// takes all eight true quotients.
+__device__ __forceinline__ void rint_quot8(const float v[8], float s, float rs, float q[8]) {
+    bool near = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float t = __fmul_rn(v[i], rs);
+        q[i] = rintf(t);
+        near |= !(fabsf(__fsub_rn(t, q[i])) <= __fmaf_rn(fabsf(t), -0x1p-21f, 0.5f));
+    }
+    if (near) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = rintf(__fdiv_rn(v[i], s));
+    }
 }
 
 // Per-lane state of one 256-weight block.
@@ -71,12 +80,13 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
         a = sub_reduce_max<F>(a);                         // group of 32 = 4 lanes (16 = 2 lanes)
-        float s = __fdiv_rn(a, 8.0f);
+        float s = __fmul_rn(a, 0.125f);                   // a / 8: the same real number, rounded the same way
         if (s < 1e-12f) s = 1e-12f;
-        const float rs = __frcp_rn(s);
+        float q[8];
+        rint_quot8(w, s, __frcp_rn(s), q);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float t = clampf_ord(rint_quot(w[i], s, rs), -8.0f, 7.0f);
+            float t = clampf_ord(q[i], -8.0f, 7.0f);
             B.u[i] = uint8_t(int(t) + 8);
         }
         B.gscale = s;
@@ -94,10 +104,11 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
         float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
         if (s < 1e-12f) s = 1e-12f;
         const int z = int(clampf_ord(rintf(__fdiv_rn(-lo, s)), 0.0f, 15.0f));
-        const float rs = __frcp_rn(s);
+        float q[8];
+        rint_quot8(w, s, __frcp_rn(s), q);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float t = clampf_ord(__fadd_rn(rint_quot(w[i], s, rs), float(z)), 0.0f, 15.0f);
+            const float t = clampf_ord(__fadd_rn(q[i], float(z)), 0.0f, 15.0f);
             B.u[i] = uint8_t(int(t));
         }
         B.gscale = s;
@@ -112,13 +123,13 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
         a = sub_reduce_max<F>(a);
-        const uint16_t s16 = f2h_bits(__fdiv_rn(a, 8.0f));
+        const uint16_t s16 = f2h_bits(__fmul_rn(a, 0.125f));   // a / 8, as above
         const float D = h2f_bits(s16);
-        const float rs = __frcp_rn(D);
+        float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (D > 0.0f) rint_quot8(w, D, __frcp_rn(D), q);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float t = 0.0f;
-            if (D > 0.0f) t = clampf_ord(rint_quot(w[i], D, rs), -8.0f, 7.0f);
+            const float t = clampf_ord(q[i], -8.0f, 7.0f);
             B.u[i] = uint8_t(int(t) + 8);
         }
         B.gscale = D;
@@ -132,7 +143,7 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
         a = sub_reduce_max<F>(a);
-        const float s = __fdiv_rn(a, half_range);
+        const float s = __fmul_rn(a, 1.0f / half_range);   // a / 2^(b-1): the same real number, rounded the same way
         const float smax = warp_max(s);
         const float d = __fdiv_rn(smax, float(T::lmax));
         const uint16_t d16 = f2h_bits(d);
@@ -140,13 +151,14 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
         float L = 0.0f;
         if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
         const float e = __fmul_rn(D, L);
-        const float re = __frcp_rn(e);
+        float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (e > 0.0f) {
+            rint_quot8(w, e, __frcp_rn(e), q);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float t = 0.0f;
-            if (e > 0.0f) t = clampf_ord(rint_quot(w[i], e, re), -half_range, half_range - 1.0f);
-            B.u[i] = uint8_t(int(t) + T::offset);
+            for (int i = 0; i < 8; ++i) q[i] = clampf_ord(q[i], -half_range, half_range - 1.0f);
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) B.u[i] = uint8_t(int(q[i]) + T::offset);
         B.L = int(L);
         B.M = 0;
         B.d16 = d16;
@@ -171,13 +183,17 @@ __device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
         if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
         if (Dm > 0.0f) M = clampf_ord(rintf(__fdiv_rn(m, Dm)), 0.0f, float(T::lmax));
         const float es = __fmul_rn(D, L), em = __fmul_rn(Dm, M);
-        const float re = __frcp_rn(es);
+        float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (es > 0.0f) {
+            float v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float t = 0.0f;
-            if (es > 0.0f) t = clampf_ord(rint_quot(__fadd_rn(w[i], em), es, re), 0.0f, levels);
-            B.u[i] = uint8_t(int(t));
+            for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(w[i], em);
+            rint_quot8(v, es, __frcp_rn(es), q);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = clampf_ord(q[i], 0.0f, levels);
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) B.u[i] = uint8_t(int(q[i]));
         B.L = int(L);
         B.M = int(M);
         B.d16 = d16;
