@@ -362,6 +362,45 @@ __device__ __forceinline__ void dequant_lane(const LaneBlock &B, float out[8]) {
     }
 }
 
+// A lane's 8 input weights as loaded (two 16-byte vectors for fp32, one for fp16 / bf16): the quantizers load the
+// next block's while they work on the current one.
+struct Raw8 {
+    uint4 v0, v1;
+};
+template <int WDT>
+__device__ __forceinline__ Raw8 ld_raw8(const void *W, int64_t idx) {
+    Raw8 r;
+    if constexpr (WDT == DT_F32) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const float *>(W) + idx);
+        r.v0 = __ldg(p);
+        r.v1 = __ldg(p + 1);
+    } else {
+        r.v0 = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(W) + idx));
+        r.v1 = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return r;
+}
+template <int WDT>
+__device__ __forceinline__ void cvt_raw8(const Raw8 &r, float *w) {
+    if constexpr (WDT == DT_F32) {
+        const uint32_t u[8] = {r.v0.x, r.v0.y, r.v0.z, r.v0.w, r.v1.x, r.v1.y, r.v1.z, r.v1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = __uint_as_float(u[i]);
+    } else {
+        const uint32_t u[4] = {r.v0.x, r.v0.y, r.v0.z, r.v0.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (WDT == DT_F16) {
+                w[2 * i] = h2f_bits(uint16_t(u[i] & 0xFFFFu));
+                w[2 * i + 1] = h2f_bits(uint16_t(u[i] >> 16));
+            } else {
+                w[2 * i] = __uint_as_float(u[i] << 16);
+                w[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------------------------------------
 // The block kernel: one template per (format, mode, input dtype).
 // ------------------------------------------------------------------------------------------------------------
@@ -376,17 +415,29 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
     // (row, block) of this warp's first block and of the grid stride: one division each, then additions
     int64_t r = warp0 / a.nbk, b = warp0 - r * a.nbk;
     const int64_t sr = nwarps / a.nbk, sb = nwarps - sr * a.nbk;
+    constexpr bool QUANT = MODE == MODE_QUANT_PARTS || MODE == MODE_QUANT_PACKED;
+    // quantizers: the input of this warp's next block is in flight while the current block is worked on
+    Raw8 nxt = {};
+    if constexpr (QUANT) {
+        if (warp0 < total && 256 * b + 8 * lane < a.K) nxt = ld_raw8<WDT>(a.W, r * a.K + 256 * b + 8 * lane);
+    }
     for (int64_t wb = warp0; wb < total; wb += nwarps, r += sr, b += sb) {
         if (b >= a.nbk) { b -= a.nbk; ++r; }
         const int64_t k0 = 256 * b + 8 * lane;           // first weight of this lane within the row
         const bool valid = k0 < a.K;                      // only INT4 rows can end inside a block
+        Raw8 cur = nxt;
+        if constexpr (QUANT) {
+            int64_t r2 = r + sr, b2 = b + sb;
+            if (b2 >= a.nbk) { b2 -= a.nbk; ++r2; }
+            if (wb + nwarps < total && 256 * b2 + 8 * lane < a.K) nxt = ld_raw8<WDT>(a.W, r2 * a.K + 256 * b2 + 8 * lane);
+        }
         LaneBlock B;
         B.gscale = B.gzero = 0.0f;
         const int j = lane / (T::sublen / 8);             // this lane's group / sub-block within the block
         if constexpr (MODE == MODE_QUANT_PARTS || MODE == MODE_QUANT_PACKED) {
             float w[8];
             if (valid) {
-                load8<WDT>(a.W, r * a.K + k0, w);
+                cvt_raw8<WDT>(cur, w);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) w[i] = 0.0f;
@@ -521,7 +572,7 @@ template <int F, int MODE, int WDT>
 static cudaError_t launch_block(const BlockArgs &a, cudaStream_t s) {
     const int64_t warps = a.N * a.nbk;
     int64_t blocks = (warps + 7) / 8;
-    const int64_t cap = 152 * 16;
+    const int64_t cap = int64_t(num_sms()) * 16;          // ~4 waves of resident CTAs (measured: faster than 1)
     if (blocks > cap) blocks = cap;
     if (blocks < 1) return cudaSuccess;
     block_kernel<F, MODE, WDT><<<unsigned(blocks), 256, 0, s>>>(a);
