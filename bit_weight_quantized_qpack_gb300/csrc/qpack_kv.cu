@@ -13,6 +13,7 @@
 
 #include "qpack_dev.cuh"
 #include "qpack_launch.h"
+#include "qpack_quot.cuh"
 
 namespace qpack {
 namespace {
@@ -46,11 +47,12 @@ __global__ void __launch_bounds__(KV_THREADS) kv_quantize_kernel(const uint4 *__
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
             const uint16_t d16 = f2h(__fdiv_rn(a, 127.0f));
             const float d = h2f(d16);
+            float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (d > 0.0f) rint_quot8(x, d, __frcp_rn(d), r);    // rint(v / d), the true quotient's rounding
             uint32_t packed[2] = {0u, 0u};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                float t = 0.0f;
-                if (d > 0.0f) t = fminf(127.0f, fmaxf(-127.0f, rintf(__fdiv_rn(x[e], d))));
+                const float t = fminf(127.0f, fmaxf(-127.0f, r[e]));
                 packed[e >> 2] |= (uint32_t(int32_t(t)) & 0xFFu) << (8 * (e & 3));
             }
             if (live) {

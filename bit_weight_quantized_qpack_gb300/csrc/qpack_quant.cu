@@ -17,30 +17,12 @@
 
 #include "qpack_dev.cuh"
 #include "qpack_launch.h"
+#include "qpack_quot.cuh"
 
 namespace qpack {
 
 enum : int { MODE_QUANT_PARTS = 0, MODE_QUANT_PACKED = 1, MODE_PACK = 2, MODE_UNPACK = 3, MODE_DEQUANT = 4 };
 
-
-// rint(fl(v / s)) from rs = the correctly rounded 1/s: t = rs * w (one rounded product) is within 2^-22 |t| of the
-// correctly rounded quotient, so where t lies farther than 2^-21 |t| from a half-integer both round to the same
-// integer; nearer (and for NaN) the quotient itself decides.
-// The lane's eight quotients at once: one branch for the rare lane with any value near a half-integer, which then
-// takes all eight true quotients.
-__device__ __forceinline__ void rint_quot8(const float v[8], float s, float rs, float q[8]) {
-    bool near = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float t = __fmul_rn(v[i], rs);
-        q[i] = rintf(t);
-        near |= !(fabsf(__fsub_rn(t, q[i])) <= __fmaf_rn(fabsf(t), -0x1p-21f, 0.5f));
-    }
-    if (near) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = rintf(__fdiv_rn(v[i], s));
-    }
-}
 
 // Per-lane state of one 256-weight block.
 struct LaneBlock {
