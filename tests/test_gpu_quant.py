@@ -155,10 +155,85 @@ def test_int4_quotients_at_rounding_boundaries(qpg, orc):
     assert np.array_equal(gs.cpu().numpy().view(np.uint32), rgs.view(np.uint32))
 
 
+@pytest.mark.parametrize("name,G", [("Q4G16", 16), ("Q4G32H", 32)])
+def test_int4_variants_quotients_at_rounding_boundaries(qpg, orc, name, G):
+    """As above for group 16 and for the fp16 group scale, with s = 2^-7 (exact in fp16, so the fp16-rounded scale is s
+    itself): quotients on and next to half-integers, every group's maximum 8 s."""
+    s = np.float32(2.0 ** -7)
+    rng = np.random.default_rng(6)
+    N, K = 64, 4096
+    k = rng.integers(-8, 7, (N, K)).astype(np.float32) + np.float32(0.5)
+    W = (k * s).astype(np.float32)
+    step = rng.integers(-1, 2, (N, K))
+    W = np.where(step > 0, np.nextafter(W, np.float32(np.inf)), W)
+    W = np.where(step < 0, np.nextafter(W, np.float32(-np.inf)), W).astype(np.float32)
+    W[:, ::G] = np.float32(8) * s
+    fmt = qpg.FORMATS[name]
+    packed, gs = qpg.qpack_quantize_pack(fmt, torch.from_numpy(W).cuda())
+    torch.cuda.synchronize()
+    rp, rgs, _ = orc.quantize_pack(fmt, W)
+    assert np.array_equal(packed.cpu().numpy(), rp)
+    g = gs.cpu().numpy()
+    assert np.array_equal(g.view(np.uint16 if g.dtype == np.int16 or g.dtype == np.float16 else np.uint32),
+                          rgs.view(np.uint16 if rgs.dtype in (np.uint16, np.float16) else np.uint32))
+
+
+@pytest.mark.parametrize("name", ["Q2S", "Q3S", "Q5S", "Q6S"])
+def test_superblock_quotients_at_rounding_boundaries(qpg, orc, name):
+    """Weights on and next to the half-integer quotients of their sub-block's rounded scale: w = (k + 1/2) e, or
+    (k + 1/2) e_s - e_m for the asymmetric formats (the quotient is (w + e_m) / e_s), with e the oracle's own
+    d16 * L_j. Each sub-block keeps its smallest and largest weight and the others stay between them, so every
+    scale is unchanged; the codes, where the quantizer's quotient from a reciprocal defers to the true division, must
+    equal the oracle's (2/3/5/6-bit article §2.1, rounding half to even)."""
+    from bit_weight_quantized_qpack_gb300 import synth
+    fmt = qpg.FORMATS[name]
+    bits, nsub, sublen, lmax, asym, _ = orc.SB[fmt]
+    N, K = 32, 1024
+    W = synth.laplace((N, K), 0.02, seed=61).numpy().astype(np.float32)
+    P = orc.quantize(fmt, W)
+    D = orc.f16_bits_to_f32(P["d"])
+    Dm = orc.f16_bits_to_f32(P["dmin"]) if asym else None
+    rng = np.random.default_rng(62)
+    placed = 0
+    for r in range(N):
+        for j in range((K // 256) * nsub):
+            seg = slice(j * sublen, (j + 1) * sublen)
+            w = W[r, seg].copy()
+            lo_i, hi_i = int(np.argmin(w)), int(np.argmax(w))
+            Lj = np.float32(np.int8(P["sub_scale"][r, j]) if name == "Q6S" else P["sub_scale"][r, j])
+            e = np.float32(np.float32(D[r, j // nsub]) * Lj)
+            if not e > 0:
+                continue
+            if asym:
+                em = np.float32(np.float32(Dm[r, j // nsub]) * np.float32(P["sub_min"][r, j]))
+                k = rng.integers(0, 2 ** bits - 1, sublen).astype(np.float32) + np.float32(0.5)
+                v = (k * e - em).astype(np.float32)
+            else:
+                k = rng.integers(-(2 ** (bits - 1)), 2 ** (bits - 1) - 1, sublen).astype(np.float32) + np.float32(0.5)
+                v = (k * e).astype(np.float32)
+            step = rng.integers(-1, 2, sublen)
+            v = np.where(step > 0, np.nextafter(v, np.float32(np.inf)), v)
+            v = np.where(step < 0, np.nextafter(v, np.float32(-np.inf)), v).astype(np.float32)
+            v = np.clip(v, w[lo_i], w[hi_i]).astype(np.float32)
+            v[lo_i], v[hi_i] = w[lo_i], w[hi_i]
+            W[r, seg] = v
+            placed += sublen - 2
+    assert placed > N * K // 2
+    P2 = orc.quantize(fmt, W)
+    for key in ("sub_scale", "sub_min", "d", "dmin"):          # the construction kept every scale
+        if P[key] is not None:
+            assert np.array_equal(P[key], P2[key]), key
+    packed, _ = qpg.qpack_quantize_pack(fmt, torch.from_numpy(W).cuda())
+    torch.cuda.synchronize()
+    rp, _, _ = orc.quantize_pack(fmt, W)
+    assert np.array_equal(packed.cpu().numpy(), rp)
+
+
 @pytest.mark.parametrize("name", ALL)
 def test_quantize_pack_large_bit_exact(qpg, orc, name):
-    """16.7 M weights per format (the fast quotient's fallback to the exact division is taken about once per 10^4
-    weights): packed bytes and scales bit-exact."""
+    """16.7 M weights per format (random weights rarely come near a rounding boundary, where the quantizer's quotient
+    from a reciprocal defers to the true division; the boundary tests take that path on purpose): packed bytes and
+    scales bit-exact."""
     from bit_weight_quantized_qpack_gb300 import synth
     fmt = qpg.FORMATS[name]
     W = synth.laplace((4096, 4096), 0.02, 77)
