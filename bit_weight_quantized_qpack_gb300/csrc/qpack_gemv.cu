@@ -291,6 +291,7 @@ __device__ __forceinline__ void dot_dp(const DRow &r, const uint32_t *xv, const 
         // per half g (code words 2g, 2g + 1): lo = even weights at class 0, hi = odd weights at class 4, hi starting
         // at -128 Sx_g (the code offset 8) -> 16 lo + hi = 16 sum q x; Q4G32A starts hi at z (-16 Sx_g) -> 16 sum (u - z) x.
         // Q4G16 has one scale per half, the other INT4 formats one per unit.
+        float tg[2];
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
             int32_t lo = 0, hi = __float_as_int(c[g]);
@@ -303,21 +304,26 @@ __device__ __forceinline__ void dot_dp(const DRow &r, const uint32_t *xv, const 
                 hi = dp2a_lo(xv[4 * j + 2], r.v[2 * j + 1], hi);
                 hi = dp2a_hi(xv[4 * j + 3], r.v[2 * j + 1], hi);
             }
-            const float sg = F == FMT_Q4G16 ? (g ? r.f1 : r.f0) : r.f0;
-            acc = fmaf(float(16 * lo + hi), sg * c[2 + g], acc);
+            tg[g] = float(16 * lo + hi);
+        }
+        if constexpr (F == FMT_Q4G16) {
+            acc = fmaf(tg[0], r.f0 * c[2], acc);
+            acc = fmaf(tg[1], r.f1 * c[3], acc);
+        } else {
+            // one scale for the unit: sigma-weighted halves first, then the scale
+            acc = fmaf(fmaf(tg[1], c[3], tg[0] * c[2]), r.f0, acc);
         }
     } else if constexpr (F == FMT_Q5S) {
-        // four chains, every byte at class 0: (a_g, b_g) = even / odd weights of half g
-        int32_t a[2] = {0, 0}, b[2] = {0, 0};
+        // one chain per half, every byte at class 0; the sigma-weighted halves first, then the sub-block scale
+        int32_t a[2] = {0, 0};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             a[j >> 1] = dp2a_lo(xv[4 * j], r.v[2 * j], a[j >> 1]);
             a[j >> 1] = dp2a_hi(xv[4 * j + 1], r.v[2 * j], a[j >> 1]);
-            b[j >> 1] = dp2a_lo(xv[4 * j + 2], r.v[2 * j + 1], b[j >> 1]);
-            b[j >> 1] = dp2a_hi(xv[4 * j + 3], r.v[2 * j + 1], b[j >> 1]);
+            a[j >> 1] = dp2a_lo(xv[4 * j + 2], r.v[2 * j + 1], a[j >> 1]);
+            a[j >> 1] = dp2a_hi(xv[4 * j + 3], r.v[2 * j + 1], a[j >> 1]);
         }
-        acc = fmaf(float(a[0] + b[0]), r.f0 * c[1], acc);
-        acc = fmaf(float(a[1] + b[1]), r.f0 * c[2], acc);
+        acc = fmaf(fmaf(float(a[1]), c[2], float(a[0]) * c[1]), r.f0, acc);
         acc = fmaf(-r.g0, c[0], acc);
     } else if constexpr (F == FMT_Q2S) {
         const float fs[2] = {r.f0, r.f1}, gs[2] = {r.g0, r.g1};
