@@ -1,8 +1,9 @@
 // qpack_quant.cu — quantize, pack, fused quantize+pack, unpack and dequantize kernels (sm_103a).
 //
-// One warp owns one 256-weight block of a row (a super-block, or eight INT4 groups); lane l owns weights
-// 8l .. 8l+7 of the block. Loads are 16-byte vectors, the per-group / per-sub-block reductions are warp
-// shuffles, and every floating-point step uses an explicitly rounded intrinsic (no FMA contraction) so that
+// The quantizers (quant16_kernel) give each half-warp one 256-weight block of a row (a super-block, or eight INT4
+// groups), lane ll owning weights 16 ll .. 16 ll + 15; pack, unpack and dequantize (block_kernel) give each warp one
+// block, lane l owning weights 8 l .. 8 l + 7. Loads are 16-byte vectors, the per-group / per-sub-block reductions
+// are shuffles, and every floating-point step uses an explicitly rounded intrinsic (no FMA contraction) so that
 // codes, scales and dequantized values are bit-identical to the formats' IEEE fp32 definition (round to nearest
 // even, true division, no FMA). The per-weight quotients are taken from one correctly rounded reciprocal per group
 // (rint_quot), which provably rounds to the same integer as the true quotient except within a stated distance of
@@ -32,158 +33,6 @@ struct LaneBlock {
     float gscale;     // INT4: this lane's group scale
     float gzero;      // Q4G32A: the group's zero point as stored (an integer value); M holds it as an int
 };
-
-template <int F>
-__device__ __forceinline__ float sub_reduce_max(float v) {
-    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-    if (Fmt<F>::sublen == 32) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-    return v;
-}
-template <int F>
-__device__ __forceinline__ float sub_reduce_min(float v) {
-    v = fminf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-    if (Fmt<F>::sublen == 32) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-    return v;
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-// ------------------------------------------------------------------------------------------------------------
-// Quantization of one block held by the warp. Returns the RANGE flag (fp16 d / dmin overflow).
-// ------------------------------------------------------------------------------------------------------------
-template <int F>
-__device__ __forceinline__ int quantize_lane(const float w[8], LaneBlock &B) {
-    using T = Fmt<F>;
-    if constexpr (F == FMT_Q4G32 || F == FMT_Q4G16) {
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
-        a = sub_reduce_max<F>(a);                         // group of 32 = 4 lanes (16 = 2 lanes)
-        float s = __fmul_rn(a, 0.125f);                   // a / 8: the same real number, rounded the same way
-        if (s < 1e-12f) s = 1e-12f;
-        float q[8];
-        rint_quot8(w, s, __frcp_rn(s), q);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float t = clampf_ord(q[i], -8.0f, 7.0f);
-            B.u[i] = uint8_t(int(t) + 8);
-        }
-        B.gscale = s;
-        B.L = B.M = 0;
-        B.d16 = B.dm16 = 0;
-        return 0;
-    } else if constexpr (F == FMT_Q4G32A) {
-        // Asymmetric INT4 (DBHOO-CIM article §5.1) in the zero-point form w' = s (q - z) of the 2/3/5/6-bit
-        // article §2.1: the group range widened to contain 0, spread over 15 steps; z = rint(-lo / s).
-        float lo = 0.0f, hi = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { lo = fminf(lo, w[i]); hi = fmaxf(hi, w[i]); }
-        lo = sub_reduce_min<F>(lo);
-        hi = sub_reduce_max<F>(hi);
-        float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
-        if (s < 1e-12f) s = 1e-12f;
-        const int z = int(clampf_ord(rintf(__fdiv_rn(-lo, s)), 0.0f, 15.0f));
-        float q[8];
-        rint_quot8(w, s, __frcp_rn(s), q);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float t = clampf_ord(__fadd_rn(q[i], float(z)), 0.0f, 15.0f);
-            B.u[i] = uint8_t(int(t));
-        }
-        B.gscale = s;
-        B.gzero = float(z);
-        B.M = z;
-        B.L = 0;
-        B.d16 = B.dm16 = 0;
-        return 0;
-    } else if constexpr (F == FMT_Q4G32H) {
-        // P2's rule with the fp16-rounded scale
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
-        a = sub_reduce_max<F>(a);
-        const uint16_t s16 = f2h_bits(__fmul_rn(a, 0.125f));   // a / 8, as above
-        const float D = h2f_bits(s16);
-        float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (D > 0.0f) rint_quot8(w, D, __frcp_rn(D), q);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float t = clampf_ord(q[i], -8.0f, 7.0f);
-            B.u[i] = uint8_t(int(t) + 8);
-        }
-        B.gscale = D;
-        B.L = B.M = 0;
-        B.d16 = s16;
-        B.dm16 = 0;
-        return ((s16 & 0x7FFFu) == 0x7C00u) ? 1 : 0;
-    } else if constexpr (!T::asym) {
-        const float half_range = float(1 << (T::bits - 1));
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(w[i]));
-        a = sub_reduce_max<F>(a);
-        const float s = __fmul_rn(a, 1.0f / half_range);   // a / 2^(b-1): the same real number, rounded the same way
-        const float smax = warp_max(s);
-        const float d = __fdiv_rn(smax, float(T::lmax));
-        const uint16_t d16 = f2h_bits(d);
-        const float D = h2f_bits(d16);
-        float L = 0.0f;
-        if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
-        const float e = __fmul_rn(D, L);
-        float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (e > 0.0f) {
-            rint_quot8(w, e, __frcp_rn(e), q);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = clampf_ord(q[i], -half_range, half_range - 1.0f);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) B.u[i] = uint8_t(int(q[i]) + T::offset);
-        B.L = int(L);
-        B.M = 0;
-        B.d16 = d16;
-        B.dm16 = 0;
-        B.gscale = 0.0f;
-        return ((d16 & 0x7FFFu) == 0x7C00u) ? 1 : 0;
-    } else {
-        const float levels = float((1 << T::bits) - 1);
-        float lo = 0.0f, hi = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { lo = fminf(lo, w[i]); hi = fmaxf(hi, w[i]); }
-        lo = sub_reduce_min<F>(lo);
-        hi = sub_reduce_max<F>(hi);
-        const float s = __fdiv_rn(__fsub_rn(hi, lo), levels);
-        const float m = __fsub_rn(0.0f, lo);
-        const float smax = fmaxf(0.0f, warp_max(s));
-        const float mmax = fmaxf(0.0f, warp_max(m));
-        const uint16_t d16 = f2h_bits(__fdiv_rn(smax, float(T::lmax)));
-        const uint16_t dm16 = f2h_bits(__fdiv_rn(mmax, float(T::lmax)));
-        const float D = h2f_bits(d16), Dm = h2f_bits(dm16);
-        float L = 0.0f, M = 0.0f;
-        if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
-        if (Dm > 0.0f) M = clampf_ord(rintf(__fdiv_rn(m, Dm)), 0.0f, float(T::lmax));
-        const float es = __fmul_rn(D, L), em = __fmul_rn(Dm, M);
-        float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (es > 0.0f) {
-            float v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(w[i], em);
-            rint_quot8(v, es, __frcp_rn(es), q);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = clampf_ord(q[i], 0.0f, levels);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) B.u[i] = uint8_t(int(q[i]));
-        B.L = int(L);
-        B.M = int(M);
-        B.d16 = d16;
-        B.dm16 = dm16;
-        B.gscale = 0.0f;
-        return (((d16 & 0x7FFFu) == 0x7C00u) || ((dm16 & 0x7FFFu) == 0x7C00u)) ? 1 : 0;
-    }
-}
 
 // ------------------------------------------------------------------------------------------------------------
 // Packing of one block (byte offsets as written in each branch). `blk` points at the block's first packed byte;
@@ -384,7 +233,7 @@ __device__ __forceinline__ void cvt_raw8(const Raw8 &r, float *w) {
 }
 
 // ------------------------------------------------------------------------------------------------------------
-// The block kernel: one template per (format, mode, input dtype).
+// The block kernel (pack, unpack, dequantize): one warp per 256-weight block, 8 weights a lane.
 // ------------------------------------------------------------------------------------------------------------
 template <int F, int MODE, int WDT>
 __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
@@ -393,39 +242,18 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
     const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const int64_t total = a.N * a.nbk;
-    int flags = 0;
+    static_assert(MODE == MODE_PACK || MODE == MODE_UNPACK || MODE == MODE_DEQUANT, "quantizers: quant16_kernel");
     // (row, block) of this warp's first block and of the grid stride: one division each, then additions
     int64_t r = warp0 / a.nbk, b = warp0 - r * a.nbk;
     const int64_t sr = nwarps / a.nbk, sb = nwarps - sr * a.nbk;
-    constexpr bool QUANT = MODE == MODE_QUANT_PARTS || MODE == MODE_QUANT_PACKED;
-    // quantizers: the input of this warp's next block is in flight while the current block is worked on
-    Raw8 nxt = {};
-    if constexpr (QUANT) {
-        if (warp0 < total && 256 * b + 8 * lane < a.K) nxt = ld_raw8<WDT>(a.W, r * a.K + 256 * b + 8 * lane);
-    }
     for (int64_t wb = warp0; wb < total; wb += nwarps, r += sr, b += sb) {
         if (b >= a.nbk) { b -= a.nbk; ++r; }
         const int64_t k0 = 256 * b + 8 * lane;           // first weight of this lane within the row
         const bool valid = k0 < a.K;                      // only INT4 rows can end inside a block
-        Raw8 cur = nxt;
-        if constexpr (QUANT) {
-            int64_t r2 = r + sr, b2 = b + sb;
-            if (b2 >= a.nbk) { b2 -= a.nbk; ++r2; }
-            if (wb + nwarps < total && 256 * b2 + 8 * lane < a.K) nxt = ld_raw8<WDT>(a.W, r2 * a.K + 256 * b2 + 8 * lane);
-        }
         LaneBlock B;
         B.gscale = B.gzero = 0.0f;
         const int j = lane / (T::sublen / 8);             // this lane's group / sub-block within the block
-        if constexpr (MODE == MODE_QUANT_PARTS || MODE == MODE_QUANT_PACKED) {
-            float w[8];
-            if (valid) {
-                cvt_raw8<WDT>(cur, w);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = 0.0f;
-            }
-            flags |= quantize_lane<F>(w, B);
-        } else if constexpr (MODE == MODE_PACK) {
+        if constexpr (MODE == MODE_PACK) {
             if (valid) {
                 uint2 c = *reinterpret_cast<const uint2 *>(a.codes + r * a.K + k0);
                 uint32_t cw[2] = {c.x, c.y};
@@ -471,7 +299,7 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
             }
         }
 
-        if constexpr (MODE == MODE_QUANT_PARTS || MODE == MODE_UNPACK) {
+        if constexpr (MODE == MODE_UNPACK) {
             if (valid) {
                 uint32_t cw[2] = {0u, 0u};
 #pragma unroll
@@ -500,7 +328,7 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
                     if (T::asym) a.dmin[sb] = B.dm16;
                 }
             }
-        } else if constexpr (MODE == MODE_QUANT_PACKED || MODE == MODE_PACK) {
+        } else if constexpr (MODE == MODE_PACK) {
             uint8_t *row = a.packed + r * a.row_stride;
             pack_lane<F>(B, lane, valid, row + b * T::bytes);
             if constexpr (F == FMT_Q4G32 || F == FMT_Q4G16) {
@@ -544,10 +372,384 @@ __global__ void __launch_bounds__(256) block_kernel(BlockArgs a) {
             }
         }
     }
-    if constexpr (MODE == MODE_QUANT_PARTS || MODE == MODE_QUANT_PACKED) {
-        flags = __any_sync(0xffffffffu, flags != 0) ? 1 : 0;
-        if (flags && lane == 0 && a.status) atomicOr(a.status, 1);
+}
+
+// ------------------------------------------------------------------------------------------------------------
+// Quantizers with 16 weights a lane. Each half-warp owns one 256-weight block: lane ll = lane & 15 holds weights
+// 16 ll .. 16 ll + 15, so a warp quantizes two blocks per pass and every per-block step (the reductions, the
+// super-block scale, the sub-block integers, the index and address arithmetic) serves twice the weights it does
+// with 8 weights a lane. Every shuffle stays inside the half-warp (xor offsets below 16); groups and sub-blocks of
+// 16 weights are one lane, those of 32 two neighbouring lanes.
+// ------------------------------------------------------------------------------------------------------------
+struct LaneQ {
+    uint8_t u[16];    // stored codes (q + offset)
+    int L, M;         // the lane's sub-block scale / minimum integers (INT4 asymmetric: M = z)
+    uint16_t d16, dm16;
+    float gscale;     // INT4: the lane's group scale
+    float gzero;      // Q4G32A: the group's zero point as stored
+};
+
+template <int F>
+__device__ __forceinline__ float grp_max16(float v) {           // over the lanes of a group / sub-block
+    if constexpr (Fmt<F>::sublen == 32) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    return v;
+}
+template <int F>
+__device__ __forceinline__ float grp_min16(float v) {
+    if constexpr (Fmt<F>::sublen == 32) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    return v;
+}
+__device__ __forceinline__ float block_max16(float v) {          // over the 16 lanes of a block
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Quantization of the lane's 16 weights: INT4 s = max|w| / 8 (floor 1e-12), q = clamp(rint(w / s), -8, 7) (fp16
+// scale: the fp16-rounded s; asymmetric: s = (hi - lo) / 15, z = rint(-lo / s)); super-blocks: the sub-block scale
+// (and minimum) from its own range, d (and dmin) = fp16(max over the block / Lmax), integer L_j (M_j) against the
+// rounded d, codes against d * L_j. Returns the RANGE flag (an fp16 scale that overflowed).
+template <int F>
+__device__ __forceinline__ int quantize16(const float w[16], LaneQ &B) {
+    using T = Fmt<F>;
+    B.gscale = B.gzero = 0.0f;
+    B.L = B.M = 0;
+    B.d16 = B.dm16 = 0;
+    if constexpr (F == FMT_Q4G32 || F == FMT_Q4G16) {
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(w[i]));
+        a = grp_max16<F>(a);
+        float s = __fmul_rn(a, 0.125f);                   // a / 8: the same real number, rounded the same way
+        if (s < 1e-12f) s = 1e-12f;
+        float q[16];
+        rint_quot<16>(w, s, __frcp_rn(s), q);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(clampf_ord(q[i], -8.0f, 7.0f)) + 8);
+        B.gscale = s;
+        return 0;
+    } else if constexpr (F == FMT_Q4G32A) {
+        float lo = 0.0f, hi = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) { lo = fminf(lo, w[i]); hi = fmaxf(hi, w[i]); }
+        lo = grp_min16<F>(lo);
+        hi = grp_max16<F>(hi);
+        float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+        if (s < 1e-12f) s = 1e-12f;
+        const int z = int(clampf_ord(rintf(__fdiv_rn(-lo, s)), 0.0f, 15.0f));
+        float q[16];
+        rint_quot<16>(w, s, __frcp_rn(s), q);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(clampf_ord(__fadd_rn(q[i], float(z)), 0.0f, 15.0f)));
+        B.gscale = s;
+        B.gzero = float(z);
+        B.M = z;
+        return 0;
+    } else if constexpr (F == FMT_Q4G32H) {
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(w[i]));
+        a = grp_max16<F>(a);
+        const uint16_t s16 = f2h_bits(__fmul_rn(a, 0.125f));
+        const float D = h2f_bits(s16);
+        float q[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q[i] = 0.0f;
+        if (D > 0.0f) rint_quot<16>(w, D, __frcp_rn(D), q);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(clampf_ord(q[i], -8.0f, 7.0f)) + 8);
+        B.gscale = D;
+        B.d16 = s16;
+        return ((s16 & 0x7FFFu) == 0x7C00u) ? 1 : 0;
+    } else if constexpr (!T::asym) {
+        const float half_range = float(1 << (T::bits - 1));
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(w[i]));
+        a = grp_max16<F>(a);
+        const float s = __fmul_rn(a, 1.0f / half_range);
+        const float smax = block_max16(s);
+        const uint16_t d16 = f2h_bits(__fdiv_rn(smax, float(T::lmax)));
+        const float D = h2f_bits(d16);
+        float L = 0.0f;
+        if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
+        const float e = __fmul_rn(D, L);
+        float q[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q[i] = 0.0f;
+        if (e > 0.0f) {
+            rint_quot<16>(w, e, __frcp_rn(e), q);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) q[i] = clampf_ord(q[i], -half_range, half_range - 1.0f);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(q[i]) + T::offset);
+        B.L = int(L);
+        B.d16 = d16;
+        return ((d16 & 0x7FFFu) == 0x7C00u) ? 1 : 0;
+    } else {
+        const float levels = float((1 << T::bits) - 1);
+        float lo = 0.0f, hi = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) { lo = fminf(lo, w[i]); hi = fmaxf(hi, w[i]); }
+        lo = grp_min16<F>(lo);
+        hi = grp_max16<F>(hi);
+        const float s = __fdiv_rn(__fsub_rn(hi, lo), levels);
+        const float m = __fsub_rn(0.0f, lo);
+        const float smax = fmaxf(0.0f, block_max16(s));
+        const float mmax = fmaxf(0.0f, block_max16(m));
+        const uint16_t d16 = f2h_bits(__fdiv_rn(smax, float(T::lmax)));
+        const uint16_t dm16 = f2h_bits(__fdiv_rn(mmax, float(T::lmax)));
+        const float D = h2f_bits(d16), Dm = h2f_bits(dm16);
+        float L = 0.0f, M = 0.0f;
+        if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
+        if (Dm > 0.0f) M = clampf_ord(rintf(__fdiv_rn(m, Dm)), 0.0f, float(T::lmax));
+        const float es = __fmul_rn(D, L), em = __fmul_rn(Dm, M);
+        float q[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q[i] = 0.0f;
+        if (es > 0.0f) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(w[i], em);
+            rint_quot<16>(v, es, __frcp_rn(es), q);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) q[i] = clampf_ord(q[i], 0.0f, levels);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(q[i]));
+        B.L = int(L);
+        B.M = int(M);
+        B.d16 = d16;
+        B.dm16 = dm16;
+        return (((d16 & 0x7FFFu) == 0x7C00u) || ((dm16 & 0x7FFFu) == 0x7C00u)) ? 1 : 0;
     }
+}
+
+// Packed bytes of one block from its 16 lanes (the byte layouts of pack_lane; `blk` = the block's first byte, `on`
+// false for a half-warp without a block or an INT4 lane past the row's end). Every lane runs the shuffles.
+template <int F>
+__device__ __forceinline__ void pack16(const LaneQ &B, int lane, bool on, uint8_t *blk) {
+    const int ll = lane & 15, hb = lane & 16;
+    if constexpr (kInt4<F>) {
+        uint32_t v0 = 0, v1 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v0 |= uint32_t(B.u[i] & 15u) << (4 * i);
+            v1 |= uint32_t(B.u[8 + i] & 15u) << (4 * i);
+        }
+        if (on) *reinterpret_cast<uint2 *>(blk + 8 * ll) = make_uint2(v0, v1);
+    } else if constexpr (F == FMT_Q2S) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v |= uint32_t(B.u[i] & 3u) << (2 * i);
+        if (on) {
+            st_u32(blk + 4 * ll, v);
+            blk[64 + ll] = uint8_t((B.L & 15) | ((B.M & 15) << 4));
+            if (ll == 0) { st_u16(blk + 80, B.d16); st_u16(blk + 82, B.dm16); }
+        }
+    } else if constexpr (F == FMT_Q3S) {
+        uint64_t v = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v |= uint64_t(B.u[i] & 7u) << (3 * i);
+        // 16 six-bit sub-scales, 4 per 3 bytes: lane r < 4 packs L_{4r..4r+3}; L_j lives in lane j
+        uint32_t f = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int Lk = __shfl_sync(0xffffffffu, B.L, hb | (4 * (ll & 3) + k));
+            f |= uint32_t(Lk & 63) << (6 * k);
+        }
+        if (on) {
+            uint8_t *p = blk + 6 * ll;                     // 2-byte aligned
+            st_u16(p, uint32_t(v));
+            st_u16(p + 2, uint32_t(v >> 16));
+            st_u16(p + 4, uint32_t(v >> 32));
+            if (ll < 4) {
+                uint8_t *q = blk + 96 + 3 * ll;
+                q[0] = uint8_t(f); q[1] = uint8_t(f >> 8); q[2] = uint8_t(f >> 16);
+            }
+            if (ll == 0) st_u16(blk + 108, B.d16);
+        }
+    } else if constexpr (F == FMT_Q5S) {
+        // high-bit word of the lane's 32-weight unit c = ll >> 1 (this lane: code words j = 2 (ll & 1), + 1):
+        // weight 8j + 2b at bit 8b + 4 + j, weight 8j + 2b + 1 at bit 8((b + 1) & 3) + j
+        uint32_t lo0 = 0, lo1 = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t t = uint32_t(16 * (ll & 1) + i), j = t >> 3, b = (t >> 1) & 3u;
+            const uint32_t pos = (t & 1u) ? 8u * ((b + 1u) & 3u) + j : 8u * b + 4u + j;
+            if (i < 8) lo0 |= uint32_t(B.u[i] & 15u) << (4 * i);
+            else lo1 |= uint32_t(B.u[i] & 15u) << (4 * (i - 8));
+            hi |= uint32_t((B.u[i] >> 4) & 1u) << pos;
+        }
+        hi |= __shfl_xor_sync(0xffffffffu, hi, 1);
+        // fields 0..7 = L_0..L_7 (sub-block j in lanes 2j, 2j + 1), 8..15 = M_0..M_7; lane r < 4 packs 4r..4r+3
+        const int r = ll & 3;
+        uint32_t f = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int src = hb | (8 * (r & 1) + 2 * k);
+            const int Lk = __shfl_sync(0xffffffffu, B.L, src);
+            const int Mk = __shfl_sync(0xffffffffu, B.M, src);
+            f |= uint32_t((r >= 2 ? Mk : Lk) & 63) << (6 * k);
+        }
+        if (on) {
+            *reinterpret_cast<uint2 *>(blk + 8 * ll) = make_uint2(lo0, lo1);
+            if ((ll & 1) == 0) st_u32(blk + 128 + 2 * ll, hi);
+            if (ll < 4) {
+                uint8_t *q = blk + 160 + 3 * ll;
+                q[0] = uint8_t(f); q[1] = uint8_t(f >> 8); q[2] = uint8_t(f >> 16);
+            }
+            if (ll == 0) st_u32(blk + 172, uint32_t(B.d16) | (uint32_t(B.dm16) << 16));
+        }
+    } else {  // Q6S
+        uint32_t lo0 = 0, lo1 = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            lo0 |= uint32_t(B.u[i] & 15u) << (4 * i);
+            lo1 |= uint32_t(B.u[8 + i] & 15u) << (4 * i);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hi |= uint32_t((B.u[i] >> 4) & 3u) << (2 * i);
+        if (on) {
+            uint8_t *p = blk + 8 * ll;                     // the block start is only 2-byte aligned
+            st_u16(p, lo0 & 0xFFFFu); st_u16(p + 2, lo0 >> 16);
+            st_u16(p + 4, lo1 & 0xFFFFu); st_u16(p + 6, lo1 >> 16);
+            st_u16(blk + 128 + 4 * ll, hi & 0xFFFFu);
+            st_u16(blk + 128 + 4 * ll + 2, hi >> 16);
+            blk[192 + ll] = uint8_t(B.L);
+            if (ll == 0) st_u16(blk + 208, B.d16);
+        }
+    }
+}
+
+// A lane's 16 input weights as loaded (four 16-byte vectors for fp32, two for fp16 / bf16).
+struct Raw16 {
+    Raw8 p0, p1;
+};
+template <int WDT>
+__device__ __forceinline__ Raw16 ld_raw16(const void *W, int64_t idx) {
+    return Raw16{ld_raw8<WDT>(W, idx), ld_raw8<WDT>(W, idx + 8)};
+}
+
+template <int F, int MODE, int WDT>
+__global__ void __launch_bounds__(256) quant16_kernel(BlockArgs a) {
+    using T = Fmt<F>;
+    const int lane = threadIdx.x & 31, hw = lane >> 4, ll = lane & 15;
+    const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int64_t total = a.N * a.nbk;                    // 256-weight blocks
+    const int64_t npairs = (total + 1) / 2;               // a warp takes blocks 2 p and 2 p + 1 of pair p
+    const int64_t step = 2 * nwarps;                      // blocks between a half-warp's passes
+    int64_t blk = 2 * warp0 + hw;
+    int64_t r = blk / a.nbk, b = blk - r * a.nbk;
+    const int64_t sr = step / a.nbk, sb = step - sr * a.nbk;
+    int flags = 0;
+    Raw16 nxt = {};
+    if (blk < total && 256 * b + 16 * ll < a.K) nxt = ld_raw16<WDT>(a.W, r * a.K + 256 * b + 16 * ll);
+    for (int64_t pv = warp0; pv < npairs; pv += nwarps, blk += step, r += sr, b += sb) {
+        if (b >= a.nbk) { b -= a.nbk; ++r; }
+        const bool live = blk < total;                    // the grid's last pair may hold a single block
+        const int64_t k0 = 256 * b + 16 * ll;             // first weight of this lane within the row
+        const bool valid = live && k0 < a.K;              // only INT4 rows can end inside a block
+        const Raw16 cur = nxt;
+        {
+            int64_t r2 = r + sr, b2 = b + sb;
+            if (b2 >= a.nbk) { b2 -= a.nbk; ++r2; }
+            if (blk + step < total && 256 * b2 + 16 * ll < a.K)
+                nxt = ld_raw16<WDT>(a.W, r2 * a.K + 256 * b2 + 16 * ll);
+        }
+        float w[16];
+        if (valid) {
+            cvt_raw8<WDT>(cur.p0, w);
+            cvt_raw8<WDT>(cur.p1, w + 8);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = 0.0f;
+        }
+        LaneQ B;
+        flags |= quantize16<F>(w, B);
+        const int j = ll / (T::sublen / 16);              // this lane's group / sub-block within the block
+        const bool first_of_sub = (ll % (T::sublen / 16)) == 0;
+        if constexpr (MODE == MODE_QUANT_PARTS) {
+            if (valid) {
+                uint32_t cw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int i = 0; i < 16; ++i) cw[i >> 2] |= uint32_t(uint8_t(int(B.u[i]) - T::offset)) << (8 * (i & 3));
+                uint2 *dst = reinterpret_cast<uint2 *>(a.codes + r * a.K + k0);
+                dst[0] = make_uint2(cw[0], cw[1]);
+                dst[1] = make_uint2(cw[2], cw[3]);
+            }
+            if constexpr (F == FMT_Q4G32 || F == FMT_Q4G16) {
+                if (valid && first_of_sub) a.gscale[r * (a.K / T::sublen) + T::nsub * b + j] = B.gscale;
+            } else if constexpr (F == FMT_Q4G32H) {
+                if (valid && first_of_sub) a.d[r * (a.K / 32) + 8 * b + j] = B.d16;
+            } else if constexpr (F == FMT_Q4G32A) {
+                if (valid && first_of_sub) {
+                    const int64_t e = r * (a.K / 16) + 2 * (8 * b + j);
+                    a.gscale[e] = B.gscale;
+                    a.gscale[e + 1] = B.gzero;
+                }
+            } else if (live) {
+                const int64_t sbk = r * a.nbk + b;
+                if (first_of_sub) {
+                    a.sub_scale[sbk * T::nsub + j] = uint8_t(B.L);
+                    if (T::asym) a.sub_min[sbk * T::nsub + j] = uint8_t(B.M);
+                }
+                if (ll == 0) {
+                    a.d[sbk] = B.d16;
+                    if (T::asym) a.dmin[sbk] = B.dm16;
+                }
+            }
+        } else {
+            uint8_t *row = a.packed + (live ? r : 0) * a.row_stride;
+            pack16<F>(B, lane, kInt4<F> ? valid : live, row + b * T::bytes);
+            if (live) {
+                if constexpr (F == FMT_Q4G32 || F == FMT_Q4G16) {
+                    if (valid && first_of_sub) a.gs_out[r * a.scale_stride + T::nsub * b + j] = B.gscale;
+                    if (b == a.nbk - 1) {                  // zero the scale-row padding
+                        const int64_t g0 = a.K / T::sublen;
+                        if (g0 + ll < a.scale_stride) a.gs_out[r * a.scale_stride + g0 + ll] = 0.0f;
+                    }
+                } else if constexpr (F == FMT_Q4G32A) {
+                    if (valid && first_of_sub) {
+                        const int64_t e = r * a.scale_stride + 2 * (8 * b + j);
+                        a.gs_out[e] = B.gscale;
+                        a.gs_out[e + 1] = B.gzero;
+                    }
+                    if (b == a.nbk - 1) {
+                        const int64_t g0 = a.K / 16;
+                        if (g0 + ll < a.scale_stride) a.gs_out[r * a.scale_stride + g0 + ll] = 0.0f;
+                    }
+                } else if constexpr (F == FMT_Q4G32H) {
+                    uint16_t *g16 = reinterpret_cast<uint16_t *>(a.gs_out);
+                    if (valid && first_of_sub) g16[r * a.scale_stride + 8 * b + j] = B.d16;
+                    if (b == a.nbk - 1) {
+                        const int64_t g0 = a.K / 32;
+                        if (g0 + ll < a.scale_stride) g16[r * a.scale_stride + g0 + ll] = 0;
+                    }
+                } else {
+                    if (b == a.nbk - 1) {                  // zero the row padding (< 16 bytes)
+                        const int64_t used = a.nbk * T::bytes;
+                        if (used + ll < a.row_stride) row[used + ll] = 0;
+                    }
+                }
+            }
+        }
+    }
+    flags = __any_sync(0xffffffffu, flags != 0) ? 1 : 0;
+    if (flags && lane == 0 && a.status) atomicOr(a.status, 1);
+}
+
+template <int F, int MODE, int WDT>
+static cudaError_t launch_quant16(const BlockArgs &a, cudaStream_t s) {
+    const int64_t pairs = (a.N * a.nbk + 1) / 2;
+    int64_t blocks = (pairs + 7) / 8;
+    const int64_t cap = int64_t(num_sms()) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) return cudaSuccess;
+    quant16_kernel<F, MODE, WDT><<<unsigned(blocks), 256, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 template <int F, int MODE, int WDT>
@@ -564,9 +766,9 @@ static cudaError_t launch_block(const BlockArgs &a, cudaStream_t s) {
 template <int F, int MODE>
 static cudaError_t launch_wdt(const BlockArgs &a, int wdt, cudaStream_t s) {
     switch (wdt) {
-        case DT_F32: return launch_block<F, MODE, DT_F32>(a, s);
-        case DT_F16: return launch_block<F, MODE, DT_F16>(a, s);
-        default: return launch_block<F, MODE, DT_BF16>(a, s);
+        case DT_F32: return launch_quant16<F, MODE, DT_F32>(a, s);
+        case DT_F16: return launch_quant16<F, MODE, DT_F16>(a, s);
+        default: return launch_quant16<F, MODE, DT_BF16>(a, s);
     }
 }
 
