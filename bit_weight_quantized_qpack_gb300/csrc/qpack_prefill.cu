@@ -6,16 +6,17 @@
 // compact form and dequantized on chip (DBHOO-CIM article, pwwt.cn/news/4452170, §3.3: no fp32 weight array).
 //
 // Two kernels. The pair kernel (prefill_pair_kernel, further below) spreads each tensor-core instruction over a
-// cluster of two CTAs on two SMs (512 tokens x 256 weight rows per pair) and is the default for the INT4 formats
-// and the 2- and 5-bit formats. The single-CTA kernel (prefill_kernel) is the default for the 3- and 6-bit formats.
+// cluster of two CTAs on two SMs (512 tokens x 256 weight rows per pair) and is the default for every format. The
+// single-CTA kernel (prefill_kernel) serves the tile heights 112 and 128 when they are asked for.
 //
 // Single-CTA kernel: one CTA computes a 512 x 128 block of Y (four 128-token sub-tiles x 128 weight rows):
 //   warp 9      TMA producer: per 64-wide K step, four 2-D tensor copies bring the 4 x (128 x 64) bf16 X tiles into
 //               shared memory already in the 128-byte-swizzled K-major layout the MMA reads.
 //   warps 0..7  weight producers: per K step, each thread dequantizes one 32-weight unit of one of the 128 weight
 //               rows (the exact fp32 dequantized value, from aligned global loads issued three K steps ahead,
-//               then bf16 round-to-nearest-even) into the swizzled 128 x 64 weight tile; afterwards they are the epilogue warps (tcgen05.ld of their
-//               TMEM lane quarter, bf16 conversion, global stores).
+//               then bf16 round-to-nearest-even) into the swizzled 128 x 64 weight tile, the two threads of a row
+//               side by side in a warp; afterwards they are the epilogue warps (tcgen05.ld of their TMEM lane
+//               quarter, bf16 conversion, global stores).
 //   warp 8      allocates all 512 TMEM columns (four fp32 128 x 128 accumulators); lane 0 issues the tcgen05.mma
 //               instructions (M=128, N=128, K=16; both operands from shared-memory descriptors) and commits them to
 //               mbarriers that free the stage and, at the end, publish the accumulators.
@@ -427,7 +428,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 
     if (warp < NDQW) {
         // ------------------------------ weight producers ------------------------------
-        const int r = tid & (BNMAX - 1), h = tid / BNMAX;                   // weight row, K half of the stage
+        // weight row and K half of the stage: the two lanes of a row pair up in the warp, so that each warp-wide
+        // load of packed bytes touches 16 rows (the two units of a row are adjacent) instead of 32
+        const int r = 16 * warp + (lane >> 1), h = lane & 1;
         const bool rin = r < BN;                                            // rows past a short tile stay idle
         const int64_t n = n0 + r;
         const uint8_t *row = a.packed + n * a.row_stride;
@@ -659,7 +662,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1) prefill_pair_kernel(const __gri
 
     if (warp < NDQW) {
         // ------------------------------ weight producers ------------------------------
-        const int r = tid & (BNMAX - 1), h = tid / BNMAX;                   // weight row, K half of the stage
+        // weight row and K half of the stage, the two lanes of a row side by side (see prefill_kernel)
+        const int r = 16 * warp + (lane >> 1), h = lane & 1;
         const int64_t n = n0 + r;
         const uint8_t *row = a.packed + n * a.row_stride;
         constexpr int64_t SE = F == FMT_Q4G32H ? 2 : 4;
@@ -863,11 +867,10 @@ static int prefill_bn(const PrefillArgs &a) {
     return cost(112) < cost(128) ? 112 : 128;
 }
 
-// The pair kernel halves the operand reads each SM's shared memory serves to the tensor cores, which pays off where
-// the dequantization keeps up: on the prefill workload's matrices (M = 2048, 14336x4096 and 4096x14336) it is
-// faster than the single-CTA kernel for the INT4 formats, the 2-bit and the 5-bit format, and slower for the 3- and
-// 6-bit formats, whose dequantization bounds both kernels (there two SMs in lock step wait for the slower one).
-template <int F> constexpr bool kPairPrefill = kInt4<F> || F == FMT_Q2S || F == FMT_Q5S;
+// The pair kernel halves the operand reads each SM's shared memory serves to the tensor cores; on the prefill
+// workload's matrices (M = 2048, 14336x4096 and 4096x14336) it is faster than the single-CTA kernel for every format
+// (measured once the two lanes of a weight row share a warp's packed-weight loads).
+template <int F> constexpr bool kPairPrefill = true;
 
 // The CTA-pair kernel: clusters of two CTAs, each pair a 512-token x 256-weight-row block of Y.
 template <int F>

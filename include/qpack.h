@@ -208,9 +208,8 @@ int qpack_fetch_fault_flags(int32_t *flags);
  *  QPACK_OPT_PREFILL_TILE_ROWS (default 0): the qgemm_prefill tiling. 256: pairs of CTAs on two SMs (a cluster
  *  of two), each pair a 512-token x 256-weight-row block of Y computed by tcgen05 MMAs of M = 256 tokens and
  *  N = 256 weight rows spread over the pair. 112 or 128: one CTA per 512-token x 112- or 128-row block (MMAs of
- *  M = 128, N = 112 or 128). 0 chooses per launch: pairs for the INT4 formats and the 2- and 5-bit formats,
- *  single CTAs (128 rows, or 112 when that needs fewer SM-waves in proportion to the tile) for the 3- and 6-bit
- *  formats. All of them meet the prefill bound.
+ *  M = 128, N = 112 or 128). 0 (the default) takes the pairs for every format. All of them meet the prefill
+ *  bound.
  * Returns QPACK_OK, QPACK_ERR_ARG (unknown option or value) or QPACK_ERR_CUDA (no current device). Host-only. */
 #define QPACK_OPT_WEIGHT_PREFETCH 1
 #define QPACK_OPT_PREFILL_TILE_ROWS 2
