@@ -356,7 +356,7 @@ int qpack_fetch_fault_flags(int32_t *flags) {
 int qpack_set_option(int option, int value) {
     if (option == QPACK_OPT_WEIGHT_PREFETCH) return set_weight_prefetch(value) == 0 ? QPACK_OK : QPACK_ERR_CUDA;
     if (option == QPACK_OPT_PREFILL_TILE_ROWS) {
-        if (value != 0 && value != 112 && value != 128 && value != 256) return QPACK_ERR_ARG;
+        if (value != 0 && value != 112 && value != 128 && value != 224 && value != 256) return QPACK_ERR_ARG;
         return set_prefill_tile_rows(value) == 0 ? QPACK_OK : QPACK_ERR_CUDA;
     }
     return QPACK_ERR_ARG;

@@ -580,11 +580,12 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 
 
 // ------------------------------------------------------------------------------------------------------------
-// Pair kernel: a cluster of two CTAs on two SMs computes a 512 x 256 block of Y with tcgen05.mma.cta_group::2
-// (M = 256 tokens, N = 256 weight rows per instruction). CTA r of the pair holds, per 64-wide K step,
+// Pair kernel: a cluster of two CTAs on two SMs computes a 512 x 2 PR block of Y with tcgen05.mma.cta_group::2
+// (M = 256 tokens, N = 2 PR weight rows per instruction; PR = 128, or 112 to spread a 4096-row matrix over more
+// SMs). CTA r of the pair holds, per 64-wide K step,
 //   A: two 128 x 64 bf16 X tiles (tokens m0 + 256 j + 128 r .. +127 of token sub-tile j = 0, 1), by TMA,
-//   B: the 128 x 64 bf16 weight tile of its own weight rows n0 + 128 r .. +127, dequantized by its warps 0..7,
-// and its TMEM receives the 128 x 256 fp32 accumulators of its own tokens for both sub-tiles (all 512 columns).
+//   B: the PR x 64 bf16 weight tile of its own weight rows np + PR r .. +PR-1, dequantized by its warps 0..7,
+// and its TMEM receives the 128 x 2 PR fp32 accumulators of its own tokens for both sub-tiles (256 columns each).
 // Each SM thus reads 8 KB of operands per 256 x 256 x 16 MMA instead of the 8 KB per 128 x 128 x 16 of the
 // single-CTA kernel, and still dequantizes each weight once per 512 tokens.
 //   warps 0..7    dequant (arriving on the local wfull barrier), then epilogue (tcgen05.ld of their TMEM lane
@@ -601,19 +602,22 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 // ------------------------------------------------------------------------------------------------------------
 namespace {
 constexpr int P2_NSUB = 2;                                 // token sub-tiles (pair MMAs of M = 256)
-constexpr int P2_ROWS = 128;                               // weight rows per CTA (pair N = 256)
+constexpr int P2_ROWS = 128;                               // weight rows per CTA at most (shared-memory tile height)
 constexpr int P2_STAGES = 4;
 constexpr int P2_STAGE = P2_NSUB * A_BYTES + P2_ROWS * BK * 2;     // 48 KB
 constexpr int P2_NFWD = P2_STAGES;                         // forwarding warps: stage st is forwarded by warp NDQW + 2 + st
 constexpr int P2_THREADS = NPROD + 64 + 32 * P2_NFWD;      // + MMA warp, TMA warp, forwarding warps
 constexpr int P2_SMEM = 1024 + P2_STAGES * P2_STAGE + 256;
-// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, N = 256 (N >> 3 at bits 17-22),
-// M = 256 (M >> 4 at bits 24-28).
-constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(256 >> 3) << 17) | (uint32_t(256 >> 4) << 24);
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, N = 2 PR weight rows over the pair (N >> 3 at
+// bits 17-22), M = 256 (M >> 4 at bits 24-28).
+template <int PR>
+constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(2 * PR >> 3) << 17) | (uint32_t(256 >> 4) << 24);
 }  // namespace
 
-template <int F>
+// PR = weight rows per CTA: 128, or 112 (pair N = 224), which covers more of the SMs on 4096-row matrices.
+template <int F, int PR>
 __global__ void __launch_bounds__(P2_THREADS, 1) prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_x, PrefillArgs a) {
+    static_assert(PR == 112 || PR == 128, "pair tiles of 112 or 128 weight rows per CTA");
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;           // 1024-aligned operand area
@@ -628,8 +632,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1) prefill_pair_kernel(const __gri
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int64_t M = a.M, N = a.N, K = a.K;
-    const int64_t np = int64_t(blockIdx.x >> 1) * (2 * P2_ROWS);             // the pair's first weight row
-    const int64_t n0 = np + int64_t(rank) * P2_ROWS;                         // this CTA's weight rows
+    const int64_t np = int64_t(blockIdx.x >> 1) * (2 * PR);                  // the pair's first weight row
+    const int64_t n0 = np + int64_t(rank) * PR;                              // this CTA's weight rows
     const int64_t m0 = int64_t(blockIdx.y) * (2 * P2_NSUB * BMS);            // the pair's first token
     const int nk = int(K / BK);
     // sub-tiles with any token in the pair, and this CTA's own 128 tokens of sub-tile j start at m0 + 256 j + 128 r
@@ -662,9 +666,11 @@ __global__ void __launch_bounds__(P2_THREADS, 1) prefill_pair_kernel(const __gri
 
     if (warp < NDQW) {
         // ------------------------------ weight producers ------------------------------
-        // weight row and K half of the stage, the two lanes of a row side by side (see prefill_kernel)
-        const int r = 16 * warp + (lane >> 1), h = lane & 1;
-        const int64_t n = n0 + r;
+        // weight row and K half of the stage, the two lanes of a row side by side (see prefill_kernel); PR / 8 rows
+        // per warp (with 112 rows lanes 28..31 are idle)
+        const int r = (PR / 8) * warp + (lane >> 1), h = lane & 1;
+        const bool live = (lane >> 1) < PR / 8;
+        const int64_t n = live ? n0 + r : N;
         const uint8_t *row = a.packed + n * a.row_stride;
         constexpr int64_t SE = F == FMT_Q4G32H ? 2 : 4;
         const uint8_t *gs_row = a.gscale ? reinterpret_cast<const uint8_t *>(a.gscale) + n * a.scale_stride * SE : nullptr;
@@ -694,8 +700,10 @@ __global__ void __launch_bounds__(P2_THREADS, 1) prefill_pair_kernel(const __gri
 #pragma unroll
                 for (int c = 0; c < 4; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
             }
+            if (live) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(Bs + sw128_off(uint32_t(r), uint32_t(4 * h + c))) = v[c];
+                for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(Bs + sw128_off(uint32_t(r), uint32_t(4 * h + c))) = v[c];
+            }
             // the generic-proxy stores, visible to the tensor cores; this CTA's forwarding warp passes the stage on
             fence_proxy_async_smem();
             __syncwarp();
@@ -720,7 +728,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1) prefill_pair_kernel(const __gri
             const int64_t m = own_tok0(j) + 32 * qw + lane;
             const uint32_t lane_base = tmem_d + (uint32_t(32 * qw) << 16) + uint32_t(256 * j);
 #pragma unroll 1
-            for (int cc = 0; cc < 256 / 32; ++cc) {
+            for (int cc = 0; cc < 2 * PR / 32; ++cc) {
                 uint32_t rr[32];
                 tmem_ld32(lane_base + uint32_t(32 * cc), rr);
                 tmem_ld_wait();
@@ -759,7 +767,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1) prefill_pair_kernel(const __gri
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         umma_bf16_pair(tmem_d + uint32_t(256 * j), sw128_kmajor_desc(As + uint32_t(j * A_BYTES) + 32u * k),
-                                       sw128_kmajor_desc(Bs + 32u * k), kIdescPair, (kt > 0 || k > 0) ? 1u : 0u);
+                                       sw128_kmajor_desc(Bs + 32u * k), kIdescPair<PR>, (kt > 0 || k > 0) ? 1u : 0u);
                 }
                 umma_commit_pair(&empty[st], uint16_t(0x3));   // both CTAs may refill the stage once these MMAs are done
             }
@@ -872,33 +880,74 @@ static int prefill_bn(const PrefillArgs &a) {
 // (measured once the two lanes of a weight row share a warp's packed-weight loads).
 template <int F> constexpr bool kPairPrefill = true;
 
-// The CTA-pair kernel: clusters of two CTAs, each pair a 512-token x 256-weight-row block of Y.
-template <int F>
-static cudaError_t launch_prefill_pair(const PrefillArgs &a, const CUtensorMap &tmx, cudaStream_t s) {
-    static int opted[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!opted[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, P2_SMEM);
-        if (e != cudaSuccess) return e;
-        opted[dev] = 1;
-    }
-    const int64_t gx = 2 * ((a.N + 2 * P2_ROWS - 1) / (2 * P2_ROWS)), gy = (a.M + 2 * P2_NSUB * BMS - 1) / (2 * P2_NSUB * BMS);
-    if (gx > 0x7FFFFFFF || gy > 65535) return cudaErrorInvalidValue;
+// The CTA-pair kernel: clusters of two CTAs, each pair a 512-token x 2 PR-weight-row block of Y.
+template <int F, int PR>
+static cudaLaunchConfig_t pair_config(const PrefillArgs &a, cudaStream_t s, cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(gx), unsigned(gy));
+    const int64_t gx = 2 * ((a.N + 2 * PR - 1) / (2 * PR)), gy = (a.M + 2 * P2_NSUB * BMS - 1) / (2 * P2_NSUB * BMS);
+    cfg.gridDim = dim3(unsigned(gx > 0x7FFFFFFF ? 0 : gx), unsigned(gy > 65535 ? 0 : gy));
     cfg.blockDim = dim3(unsigned(P2_THREADS));
     cfg.dynamicSmemBytes = P2_SMEM;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<F>, tmx, a);
+    return cfg;
+}
+
+template <int F, int PR>
+static cudaError_t pair_opt_in() {
+    static int opted[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!opted[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<F, PR>, cudaFuncAttributeMaxDynamicSharedMemorySize, P2_SMEM);
+        if (e != cudaSuccess) return e;
+        opted[dev] = 1;
+    }
+    return cudaSuccess;
+}
+
+template <int F, int PR>
+static cudaError_t launch_prefill_pair(const PrefillArgs &a, const CUtensorMap &tmx, cudaStream_t s) {
+    const cudaError_t e = pair_opt_in<F, PR>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config<F, PR>(a, s, attr);
+    if (cfg.gridDim.x == 0 || cfg.gridDim.y == 0) return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<F, PR>, tmx, a);
+}
+
+// Weight rows per CTA of the pair kernel: 128, or 112 when that takes fewer waves of clusters than 128 does in
+// proportion to the tile. The clusters that fit at once come from the occupancy query, as a pair of CTAs must sit
+// on two SMs of one GPC. A cluster's time is set by its K steps more than by its rows (each step waits on the same
+// round trip), so on a 4096-row matrix at M = 2048 the 112-row pairs (76 clusters instead of 64) gain only 0.5-2%,
+// and lose ~1% for Q3S, which keeps 128.
+template <int F>
+static int prefill_pair_rows(const PrefillArgs &a, cudaStream_t s) {
+    if (F == FMT_Q3S) return 128;
+    static int fit[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 128;
+    if (!fit[dev]) {
+        int n = 0;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = pair_config<F, 112>(a, s, attr);
+        cfg.gridDim = dim3(2u, 1u);                       // one cluster: the query does not depend on the grid
+        if (pair_opt_in<F, 112>() != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, prefill_pair_kernel<F, 112>, &cfg) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            n = num_sms() / 2;
+        }
+        fit[dev] = n;
+    }
+    const int64_t mt = (a.M + 2 * P2_NSUB * BMS - 1) / (2 * P2_NSUB * BMS), c = fit[dev];
+    auto cost = [&](int64_t pr) { return ((a.N + 2 * pr - 1) / (2 * pr) * mt + c - 1) / c * pr; };
+    return cost(112) < cost(128) ? 112 : 128;
 }
 
 template <int F>
@@ -907,7 +956,10 @@ static cudaError_t launch_prefill_f(const PrefillArgs &a, cudaStream_t s) {
     const cudaError_t e = encode_x(&tmx, a);
     if (e != cudaSuccess) return e;
     const int forced = prefill_tile_rows();
-    if (forced == 256 || (forced == 0 && kPairPrefill<F>)) return launch_prefill_pair<F>(a, tmx, s);
+    if (forced == 256) return launch_prefill_pair<F, 128>(a, tmx, s);
+    if (forced == 224) return launch_prefill_pair<F, 112>(a, tmx, s);
+    if (forced == 0 && kPairPrefill<F>)
+        return prefill_pair_rows<F>(a, s) == 112 ? launch_prefill_pair<F, 112>(a, tmx, s) : launch_prefill_pair<F, 128>(a, tmx, s);
     const int bn = forced ? forced : prefill_bn(a);
     return bn == 112 ? launch_prefill_bn<F, 112>(a, tmx, s) : launch_prefill_bn<F, 128>(a, tmx, s);
 }

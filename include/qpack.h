@@ -205,11 +205,11 @@ int qpack_fetch_fault_flags(int32_t *flags);
  *  (activations are still read only after it has finished, and outputs written after). The caller guarantees
  *  that the packed weights and scales of a product are not written by the kernel launched just before it on
  *  that stream (true for a decode loop over resident weights).
- *  QPACK_OPT_PREFILL_TILE_ROWS (default 0): the qgemm_prefill tiling. 256: pairs of CTAs on two SMs (a cluster
- *  of two), each pair a 512-token x 256-weight-row block of Y computed by tcgen05 MMAs of M = 256 tokens and
- *  N = 256 weight rows spread over the pair. 112 or 128: one CTA per 512-token x 112- or 128-row block (MMAs of
- *  M = 128, N = 112 or 128). 0 (the default) takes the pairs for every format. All of them meet the prefill
- *  bound.
+ *  QPACK_OPT_PREFILL_TILE_ROWS (default 0): the qgemm_prefill tiling. 256 or 224: pairs of CTAs on two SMs (a
+ *  cluster of two), each pair a 512-token x 256- or 224-weight-row block of Y computed by tcgen05 MMAs of M = 256
+ *  tokens and N = 256 or 224 weight rows spread over the pair. 112 or 128: one CTA per 512-token x 112- or
+ *  128-row block (MMAs of M = 128, N = 112 or 128). 0 (the default) takes the pairs for every format, of 224 rows
+ *  where they fill more of the SMs at once (not for Q3S), else of 256. All of them meet the prefill bound.
  * Returns QPACK_OK, QPACK_ERR_ARG (unknown option or value) or QPACK_ERR_CUDA (no current device). Host-only. */
 #define QPACK_OPT_WEIGHT_PREFETCH 1
 #define QPACK_OPT_PREFILL_TILE_ROWS 2

@@ -63,10 +63,10 @@ def test_prefill_single_tile_int4(qpg, orc):
     run_case(qpg, orc, qpg.Q4G32, 128, 256, 64, 10)
 
 
-@pytest.fixture(params=[0, 256, 112, 128], ids=["tile-auto", "tile-pair", "tile-112", "tile-128"])
+@pytest.fixture(params=[0, 256, 224, 112, 128], ids=["tile-auto", "tile-pair", "tile-pair-224", "tile-112", "tile-128"])
 def tile_rows(request, qpg):
-    """The prefill tiling: chosen per launch (the default), forced to CTA pairs of 256 weight rows (one cluster of
-    two CTAs sharing each tensor-core instruction), or forced to single CTAs of 112 or 128 weight rows."""
+    """The prefill tiling: chosen per launch (the default), forced to CTA pairs of 256 or 224 weight rows (one
+    cluster of two CTAs sharing each tensor-core instruction), or forced to single CTAs of 112 or 128 weight rows."""
     qpg.qpack_set_option(qpg.OPT_PREFILL_TILE_ROWS, request.param)
     yield request.param
     qpg.qpack_set_option(qpg.OPT_PREFILL_TILE_ROWS, 0)
@@ -83,7 +83,7 @@ def test_prefill_tile_rows_option_values(qpg):
     L = qpg.lib()
     assert L.qpack_set_option(qpg.OPT_PREFILL_TILE_ROWS, 96) == -1
     assert L.qpack_set_option(99, 0) == -1
-    for v in (256, 112, 128, 0):
+    for v in (256, 224, 112, 128, 0):
         assert L.qpack_set_option(qpg.OPT_PREFILL_TILE_ROWS, v) == 0
 
 
@@ -95,5 +95,6 @@ def test_prefill_config_int4_14336x4096(qpg, orc, tile_rows):
 
 def test_prefill_config_q6s_4096x14336(qpg, orc, tile_rows):
     """The prefill workload's 6-bit matrix at M = 2048, with each tiling: 512 random outputs plus the four corner
-    128 x 128 tiles (with 112-row tiles the last corner spans two CTAs and a ragged 64-row tile)."""
+    128 x 128 tiles (with 112-row tiles, single or in pairs, the last corner spans two CTAs and a ragged 64-row
+    tile)."""
     run_case(qpg, orc, qpg.Q6S, 2048, 4096, 14336, 7, full=False)
