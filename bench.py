@@ -664,6 +664,7 @@ def run_ncu_case(args):
     else:
         X = synth.normal((args.M, K), 1.0, seed=2, device=dev, dtype=torch.bfloat16)
         Y = torch.empty((args.M, N), device=dev, dtype=torch.bfloat16)
+        qp.qpack_set_option(qp.OPT_PREFILL_TILE_ROWS, args.prefill_tile_rows)
         for i in range(copies):
             qp.qgemm_prefill(fmt, ps[i], gs[i], N, K, X, Y)
     torch.cuda.synchronize()
@@ -688,6 +689,8 @@ def main():
     ap.add_argument("--N", type=int, default=N_ROWS)
     ap.add_argument("--K", type=int, default=K_COLS)
     ap.add_argument("--M", type=int, default=8)
+    ap.add_argument("--prefill-tile-rows", type=int, default=0, choices=[0, 112, 128, 224, 256],
+                    help="--ncu-case prefill: the tiling (0: chosen per launch; 256/224: CTA pairs; 128/112: single CTAs)")
     args = ap.parse_args()
     if args.ncu_case:
         return run_ncu_case(args)
