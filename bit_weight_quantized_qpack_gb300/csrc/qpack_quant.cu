@@ -7,7 +7,9 @@
 // codes, scales and dequantized values are bit-identical to the formats' IEEE fp32 definition (round to nearest
 // even, true division, no FMA). The per-weight quotients are taken from one correctly rounded reciprocal per group
 // (rint_quot), which provably rounds to the same integer as the true quotient except within a stated distance of
-// a half-integer, where the true quotient is computed instead.
+// a half-integer, where the true quotient is computed instead; the quantizers (but Q6S's) read the rounded code from
+// the bits of the quotient plus 1.5 * 2^23 and clamp it as an integer (rint_codes), keeping the quarter-rate rounding
+// and conversion instructions off the path (Q5S 80 -> 72 us, Q2S 66 -> 61 us on a 14336x4096 matrix).
 //
 // Quantizers: INT4 group-32 per the DBHOO-CIM article (pwwt.cn/news/4452170) §3.1; two-level round-to-nearest
 // super-blocks per the 2/3/5/6-bit article (lpnh.cn/news/2857666) §2.1 and §2.3 (sub-block scales from each
@@ -422,10 +424,7 @@ __device__ __forceinline__ int quantize16(const float w[16], LaneQ &B) {
         a = grp_max16<F>(a);
         float s = __fmul_rn(a, 0.125f);                   // a / 8: the same real number, rounded the same way
         if (s < 1e-12f) s = 1e-12f;
-        float q[16];
-        rint_quot<16>(w, s, __frcp_rn(s), q);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(clampf_ord(q[i], -8.0f, 7.0f)) + 8);
+        rint_codes<16>(w, s, __frcp_rn(s), 0, -8, 7, 8, B.u);
         B.gscale = s;
         return 0;
     } else if constexpr (F == FMT_Q4G32A) {
@@ -437,10 +436,7 @@ __device__ __forceinline__ int quantize16(const float w[16], LaneQ &B) {
         float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
         if (s < 1e-12f) s = 1e-12f;
         const int z = int(clampf_ord(rintf(__fdiv_rn(-lo, s)), 0.0f, 15.0f));
-        float q[16];
-        rint_quot<16>(w, s, __frcp_rn(s), q);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(clampf_ord(__fadd_rn(q[i], float(z)), 0.0f, 15.0f)));
+        rint_codes<16>(w, s, __frcp_rn(s), z, 0, 15, 0, B.u);
         B.gscale = s;
         B.gzero = float(z);
         B.M = z;
@@ -452,12 +448,12 @@ __device__ __forceinline__ int quantize16(const float w[16], LaneQ &B) {
         a = grp_max16<F>(a);
         const uint16_t s16 = f2h_bits(__fmul_rn(a, 0.125f));
         const float D = h2f_bits(s16);
-        float q[16];
+        if (D > 0.0f) {
+            rint_codes<16>(w, D, __frcp_rn(D), 0, -8, 7, 8, B.u);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = 0.0f;
-        if (D > 0.0f) rint_quot<16>(w, D, __frcp_rn(D), q);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(clampf_ord(q[i], -8.0f, 7.0f)) + 8);
+            for (int i = 0; i < 16; ++i) B.u[i] = 8;
+        }
         B.gscale = D;
         B.d16 = s16;
         return ((s16 & 0x7FFFu) == 0x7C00u) ? 1 : 0;
@@ -474,16 +470,21 @@ __device__ __forceinline__ int quantize16(const float w[16], LaneQ &B) {
         float L = 0.0f;
         if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
         const float e = __fmul_rn(D, L);
-        float q[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = 0.0f;
         if (e > 0.0f) {
-            rint_quot<16>(w, e, __frcp_rn(e), q);
+            if constexpr (F == FMT_Q6S) {
+                // the rounding and conversion instructions measured 2% faster here than rint_codes (Q3S: 3% slower)
+                float q[16];
+                rint_quot<16>(w, e, __frcp_rn(e), q);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) q[i] = clampf_ord(q[i], -half_range, half_range - 1.0f);
+                for (int i = 0; i < 16; ++i)
+                    B.u[i] = uint8_t(int(clampf_ord(q[i], -half_range, half_range - 1.0f)) + T::offset);
+            } else {
+                rint_codes<16>(w, e, __frcp_rn(e), 0, -(1 << (T::bits - 1)), (1 << (T::bits - 1)) - 1, T::offset, B.u);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(T::offset);
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(q[i]) + T::offset);
         B.L = int(L);
         B.d16 = d16;
         return ((d16 & 0x7FFFu) == 0x7C00u) ? 1 : 0;
@@ -505,19 +506,15 @@ __device__ __forceinline__ int quantize16(const float w[16], LaneQ &B) {
         if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
         if (Dm > 0.0f) M = clampf_ord(rintf(__fdiv_rn(m, Dm)), 0.0f, float(T::lmax));
         const float es = __fmul_rn(D, L), em = __fmul_rn(Dm, M);
-        float q[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = 0.0f;
         if (es > 0.0f) {
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(w[i], em);
-            rint_quot<16>(v, es, __frcp_rn(es), q);
+            rint_codes<16>(v, es, __frcp_rn(es), 0, 0, (1 << T::bits) - 1, 0, B.u);
+        } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) q[i] = clampf_ord(q[i], 0.0f, levels);
+            for (int i = 0; i < 16; ++i) B.u[i] = 0;
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(q[i]));
         B.L = int(L);
         B.M = int(M);
         B.d16 = d16;
@@ -573,15 +570,17 @@ __device__ __forceinline__ void pack16(const LaneQ &B, int lane, bool on, uint8_
     } else if constexpr (F == FMT_Q5S) {
         // high-bit word of the lane's 32-weight unit c = ll >> 1 (this lane: code words j = 2 (ll & 1), + 1):
         // weight 8j + 2b at bit 8b + 4 + j, weight 8j + 2b + 1 at bit 8((b + 1) & 3) + j
+        // (positions for code words 0, 1, then shifted by 2 for the odd lane's words 2, 3)
         uint32_t lo0 = 0, lo1 = 0, hi = 0;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const uint32_t t = uint32_t(16 * (ll & 1) + i), j = t >> 3, b = (t >> 1) & 3u;
-            const uint32_t pos = (t & 1u) ? 8u * ((b + 1u) & 3u) + j : 8u * b + 4u + j;
+            const uint32_t j = uint32_t(i) >> 3, b = (uint32_t(i) >> 1) & 3u;
+            const uint32_t pos = (i & 1) ? 8u * ((b + 1u) & 3u) + j : 8u * b + 4u + j;
             if (i < 8) lo0 |= uint32_t(B.u[i] & 15u) << (4 * i);
             else lo1 |= uint32_t(B.u[i] & 15u) << (4 * (i - 8));
             hi |= uint32_t((B.u[i] >> 4) & 1u) << pos;
         }
+        hi <<= 2 * (ll & 1);
         hi |= __shfl_xor_sync(0xffffffffu, hi, 1);
         // fields 0..7 = L_0..L_7 (sub-block j in lanes 2j, 2j + 1), 8..15 = M_0..M_7; lane r < 4 packs 4r..4r+3
         const int r = ll & 3;
