@@ -470,17 +470,20 @@ __device__ __forceinline__ int quantize16(const float w[16], LaneQ &B) {
         float L = 0.0f;
         if (D > 0.0f) L = clampf_ord(rintf(__fdiv_rn(s, D)), 0.0f, float(T::lmax));
         const float e = __fmul_rn(D, L);
-        if (e > 0.0f) {
-            if constexpr (F == FMT_Q6S) {
-                // the rounding and conversion instructions measured 2% faster here than rint_codes (Q3S: 3% slower)
-                float q[16];
+        if constexpr (F == FMT_Q6S) {
+            // the rounding and conversion instructions measured 2% faster here than rint_codes (Q3S: 3% slower)
+            float q[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) q[i] = 0.0f;
+            if (e > 0.0f) {
                 rint_quot<16>(w, e, __frcp_rn(e), q);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    B.u[i] = uint8_t(int(clampf_ord(q[i], -half_range, half_range - 1.0f)) + T::offset);
-            } else {
-                rint_codes<16>(w, e, __frcp_rn(e), 0, -(1 << (T::bits - 1)), (1 << (T::bits - 1)) - 1, T::offset, B.u);
+                for (int i = 0; i < 16; ++i) q[i] = clampf_ord(q[i], -half_range, half_range - 1.0f);
             }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(int(q[i]) + T::offset);
+        } else if (e > 0.0f) {
+            rint_codes<16>(w, e, __frcp_rn(e), 0, -(1 << (T::bits - 1)), (1 << (T::bits - 1)) - 1, T::offset, B.u);
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) B.u[i] = uint8_t(T::offset);
