@@ -6,8 +6,8 @@
 // compact form and dequantized on chip (DBHOO-CIM article, pwwt.cn/news/4452170, §3.3: no fp32 weight array).
 //
 // Two kernels. The pair kernel (prefill_pair_kernel, further below) spreads each tensor-core instruction over a
-// cluster of two CTAs on two SMs (512 tokens x 256 weight rows per pair) and is the default for every format. The
-// single-CTA kernel (prefill_kernel) serves the tile heights 112 and 128 when they are asked for.
+// cluster of two CTAs on two SMs (512 tokens x 256 or 224 weight rows per pair) and is the default for every format.
+// The single-CTA kernel (prefill_kernel) serves the tile heights 112 and 128 when they are asked for.
 //
 // Single-CTA kernel: one CTA computes a 512 x 128 block of Y (four 128-token sub-tiles x 128 weight rows):
 //   warp 9      TMA producer: per 64-wide K step, four 2-D tensor copies bring the 4 x (128 x 64) bf16 X tiles into
