@@ -47,14 +47,12 @@ __global__ void __launch_bounds__(KV_THREADS) kv_quantize_kernel(const uint4 *__
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
             const uint16_t d16 = f2h(__fdiv_rn(a, 127.0f));
             const float d = h2f(d16);
-            float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (d > 0.0f) rint_quot8(x, d, __frcp_rn(d), r);    // rint(v / d), the true quotient's rounding
+            // clamp(rint(v / d), -127, 127) as two's-complement bytes, rounded as the true quotient is
+            uint8_t cb[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (d > 0.0f) rint_codes<8>(x, d, __frcp_rn(d), 0, -127, 127, 0, cb);
             uint32_t packed[2] = {0u, 0u};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float t = fminf(127.0f, fmaxf(-127.0f, r[e]));
-                packed[e >> 2] |= (uint32_t(int32_t(t)) & 0xFFu) << (8 * (e & 3));
-            }
+            for (int e = 0; e < 8; ++e) packed[e >> 2] |= uint32_t(cb[e]) << (8 * (e & 3));
             if (live) {
                 q[piece] = make_uint2(packed[0], packed[1]);
                 if ((lane & 3) == 0) sc[piece / 4] = d16;

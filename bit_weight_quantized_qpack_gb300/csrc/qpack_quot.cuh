@@ -24,7 +24,6 @@ __device__ __forceinline__ void rint_quot(const float *v, float s, float rs, flo
         for (int i = 0; i < n; ++i) q[i] = rintf(__fdiv_rn(v[i], s));
     }
 }
-__device__ __forceinline__ void rint_quot8(const float v[8], float s, float rs, float q[8]) { rint_quot<8>(v, s, rs, q); }
 
 // Codes c_i = int(clamp(rint(fl(v_i / s)) + add, lo, hi)) + off for a lane's n values (add a small integer, so the
 // sum is exact; the clamp in the order v < lo ? lo : (v > hi ? hi : v)), with rint_quot's test of the product
