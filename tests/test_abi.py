@@ -88,6 +88,13 @@ def test_argument_validation_rejects_before_launch(qp):
     assert L.qpack_kv_dequant(good, good, 0, good, None) == 0
     assert L.qgemv(qp.Q3S, good, None, 0, 4096, good, good, None) == 0
     assert L.qgemm_small(qp.Q3S, good, None, 8, 4096, 0, good, 4096, good, 8, None) == 0
+    # options: an unknown option or tiling is refused before any device query; the five tilings are accepted (on a
+    # host without a GPU the device query behind them then fails with ERR_CUDA)
+    assert L.qpack_set_option(99, 0) == ARG
+    for v in (96, 64, 240, -1):
+        assert L.qpack_set_option(qp.OPT_PREFILL_TILE_ROWS, v) == ARG
+    for v in (112, 128, 224, 256, 0):          # ends on the default, so later calls on a GPU host are unaffected
+        assert L.qpack_set_option(qp.OPT_PREFILL_TILE_ROWS, v) in (0, -5)
 
 
 def test_status_strings(qp):
